@@ -1,0 +1,442 @@
+"""Benchmark of the MoE layer forward + backward on GB300.
+
+One step = moe_layer_fwd + moe_layer_bwd (router GEMM, top-k, routing maps, permute, grouped
+SwiGLU fc1/fc2, shared expert, combine, and every backward stage) on one batch of seeded
+synthetic tokens resident in HBM.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload deepseek]
+  python bench.py --impl reference ...   # the fp64 CPU oracle timed on the host cores
+
+Default workload: the DeepSeek-style layer (T=16384 tokens, d_model 2688, 128 experts, top-6
+sigmoid routing normalised over the selected experts, expert ffn 1856, one shared expert of
+ffn 1856, Zipf(1.2) router bias), forward + backward.  Its inputs (3.8 GB of expert weights,
+0.5 GB+ per activation array) are far larger than the 129 MB L2, so no L2 flush is needed
+between steps.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_inputs  # noqa: E402
+
+METRIC = "MoE layer fwd+bwd tokens/s; grouped-GEMM TFLOPS and % of bf16 peak, 1 GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ----------------------------------------------------------------------------- work per kernel
+
+def kernel_work(lc):
+    """Algorithmic work of one launch of each kernel kind: ('tensor', FLOPs) or ('hbm', bytes).
+    FLOPs count 2 per multiply-add of the products the method needs (no padding, no dense
+    all-expert work); bytes count each operand the kernel must read or write once."""
+    T, d, E, k, f, fs = lc.T, lc.d, lc.E, lc.k, lc.f, lc.f_shared
+    N = T * k
+    b = 2 if lc.dtype == "bf16" else 4
+    g = 1 if lc.shared_gate else 0
+    w = {
+        "gemm_router": ("tensor", 2.0 * T * d * E),
+        "gemm_fc1_swiglu": ("tensor", 4.0 * N * d * f),
+        "gemm_fc2": ("tensor", 2.0 * N * d * f),
+        "gemm_fc2_dgrad": ("tensor", 2.0 * N * d * f),
+        "gemm_fc2_wgrad": ("tensor", 2.0 * N * d * f),
+        "gemm_fc1_dgrad": ("tensor", 4.0 * N * d * f),
+        "gemm_fc1_wgrad": ("tensor", 4.0 * N * d * f),
+        "gemm_router_dgrad": ("tensor", 2.0 * T * d * E),
+        "gemm_router_wgrad": ("tensor", 2.0 * T * d * (E + g)),
+        "route_topk": ("hbm", T * E * 4 + N * 8),
+        "route_scan": ("hbm", 0.0),
+        "route_slots": ("hbm", N * 4 + N * 8),
+        "permute": ("hbm", T * d * b * (1 + k) + N * 4),
+        "combine": ("hbm", T * d * b * (k + 1) + N * 8 + (T * d * b if fs else 0)),
+        "combine_bwd": ("hbm", T * d * b * (1 + 2 * k) + N * 12 + (2 * T * d * b if fs else 0)),
+        "permute_bwd": ("hbm", T * d * b * (k + 1) + N * 4 + T * d * b * (2 if fs else 1)),
+        "router_bwd": ("hbm", T * E * 4 + N * 12 + T * (E + g) * b),
+        "split_reduce": ("hbm", 0.0),
+        "shared_gate": ("hbm", T * d * b),
+    }
+    if fs:
+        w.update({
+            "gemm_shared_fc1_swiglu": ("tensor", 4.0 * T * d * fs),
+            "gemm_shared_fc2": ("tensor", 2.0 * T * d * fs),
+            "gemm_shared_fc2_dgrad": ("tensor", 2.0 * T * d * fs),
+            "gemm_shared_fc2_wgrad": ("tensor", 2.0 * T * d * fs),
+            "gemm_shared_fc1_dgrad": ("tensor", 4.0 * T * d * fs),
+            "gemm_shared_fc1_wgrad": ("tensor", 4.0 * T * d * fs),
+        })
+    return w
+
+
+def layer_flops(lc, backward=True):
+    fl = 2.0 * lc.T * lc.d * lc.E + 6.0 * lc.T * lc.k * lc.d * lc.f
+    if lc.f_shared:
+        fl += 6.0 * lc.T * lc.d * lc.f_shared + (2.0 * lc.T * lc.d if lc.shared_gate else 0.0)
+    return fl * (3.0 if backward else 1.0)
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_clocks_{os.getpid()}.csv")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample_inputs(lc, inp, n_tok, seed=1234):
+    """A seeded subset of n_tok tokens with every expert's weights, as numpy (fp32 values of the
+    bf16 inputs; the oracle reads them as fp64)."""
+    import numpy as np
+    import torch
+    gen = torch.Generator().manual_seed(seed)
+    sel = torch.randperm(lc.T, generator=gen)[:n_tok].sort().values
+    host = {}
+    for name, t in inp.items():
+        if t is None:
+            host[name] = None
+        elif name in ("x", "dy"):
+            host[name] = t[sel.to(t.device)].float().cpu().numpy()
+        else:
+            host[name] = t.float().cpu().numpy()
+    return host, lc.replace(T=n_tok)
+
+
+def time_oracle(lc_s, host, reps=1):
+    import oracle.moe_oracle as O
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        fwd = O.layer_forward(lc_s, host)
+        O.layer_backward(lc_s, host, fwd, host["dy"])
+    return (time.perf_counter() - t0) / reps
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------- main arm
+
+def run_gpu(args, lc):
+    import torch
+    import torch.distributed as dist
+
+    import moe_expert_layer_gemm_gb300 as moe
+    from moe_expert_layer_gemm_gb300 import build as _build
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    if not os.path.exists(moe._lib.LIB_PATH):
+        if rank == 0:
+            _build.build()
+        if world > 1:
+            dist.barrier()
+    moe.lib()
+    dev = torch.device("cuda", local)
+    # each rank is an independent replica on its own tokens (weak scaling; no exchange)
+    inp = moe_inputs.make_layer_inputs(lc, seed=args.seed + rank, device=dev)
+    cfg = moe.cfg_from(lc)
+    saved = moe.alloc_saved(cfg, dev)
+    f32 = torch.float32
+    y = torch.empty_like(inp["x"])
+    grads = dict(
+        dx=torch.empty_like(inp["x"]),
+        dW_r=torch.empty(lc.E, lc.d, dtype=f32, device=dev),
+        dW1=torch.empty(lc.E, 2 * lc.f, lc.d, dtype=f32, device=dev),
+        dW2=torch.empty(lc.E, lc.d, lc.f, dtype=f32, device=dev),
+        dWs1=torch.empty(2 * lc.f_shared, lc.d, dtype=f32, device=dev) if lc.f_shared else None,
+        dWs2=torch.empty(lc.d, lc.f_shared, dtype=f32, device=dev) if lc.f_shared else None,
+        dw_sg=torch.empty(lc.d, dtype=f32, device=dev) if lc.shared_gate else None,
+    )
+    ws_f = moe.workspace(cfg, moe.WS_LAYER_FWD, dev)
+    ws_b = moe.workspace(cfg, moe.WS_LAYER_BWD, dev)
+    stream = torch.cuda.current_stream()
+
+    def step(x, dy, yout, dxout):
+        moe.moe_layer_fwd(cfg, x, inp["W_r"], inp["b_r"], inp["W1"], inp["W2"], inp["Ws1"],
+                          inp["Ws2"], inp["w_sg"], yout, saved, ws_f)
+        if lc.backward:
+            moe.moe_layer_bwd(cfg, dy, x, inp["W_r"], inp["W1"], inp["W2"], inp["Ws1"], inp["Ws2"],
+                              inp["w_sg"], saved, dxout, grads["dW_r"], grads["dW1"], grads["dW2"],
+                              grads["dWs1"], grads["dWs2"], grads["dw_sg"], ws_b)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step(inp["x"], inp["dy"], y, grads["dx"])
+    torch.cuda.synchronize()
+    moe.check_device_error()
+
+    # ---- device-timed region: inputs resident in HBM
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        try:
+            gpu_index = int(vis.split(",")[local])
+        except (ValueError, IndexError):
+            pass
+    clocks = ClockSampler(gpu_index)
+    moe.trace_read()   # drop anything recorded before
+    moe.trace_enable(True)
+    launches0 = moe.launch_count()
+    barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(inp["x"], inp["dy"], y, grads["dx"])
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    launches = moe.launch_count() - launches0
+    moe.trace_enable(False)
+    trace = moe.trace_read()
+    clk = clocks.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    moe.check_device_error()
+    ms_max = ms_total
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    ms_step = ms_max / args.steps
+    tokens = lc.T * args.steps * world
+    value = tokens / (ms_max / 1e3)
+
+    # ---- end-to-end: pinned host inputs copied in, results copied out, every step
+    x_h = inp["x"].cpu().pin_memory()
+    dy_h = inp["dy"].cpu().pin_memory()
+    y_h = torch.empty_like(x_h).pin_memory()
+    dx_h = torch.empty_like(x_h).pin_memory()
+    x_d = torch.empty_like(inp["x"])
+    dy_d = torch.empty_like(inp["dy"])
+    e2e_steps = max(1, min(args.steps, 10))
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        x_d.copy_(x_h, non_blocking=True)
+        dy_d.copy_(dy_h, non_blocking=True)
+        step(x_d, dy_d, y, grads["dx"])
+        y_h.copy_(y, non_blocking=True)
+        dx_h.copy_(grads["dx"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = lc.T * e2e_steps * world / (e2e_ms / 1e3)
+    esz = inp["x"].element_size()
+    h2d = 2 * lc.T * lc.d * esz
+    d2h = 2 * lc.T * lc.d * esz if lc.backward else lc.T * lc.d * esz
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+
+    # ---- roofline of the dominant kernel (largest share of device time in the timed region)
+    peaks, peak_src = load_peaks()
+    work = kernel_work(lc)
+    kern = {}
+    for name, (n_launch, ms) in trace.items():
+        kind, amount = work.get(name, ("hbm", 0.0))
+        avg_ms = ms / max(1, n_launch)
+        if kind == "tensor":
+            ach = amount / (avg_ms / 1e3) / 1e12
+            unit, peak = "TFLOP/s", peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+        else:
+            ach = amount / (avg_ms / 1e3) / 1e9
+            unit, peak = "GB/s", peaks["hbm_gbs"]
+        kern[name] = {"launches": n_launch, "ms_per_launch": round(avg_ms, 4),
+                      "share": None, "achieved": round(ach, 1), "unit": unit,
+                      "frac": round(ach / peak, 4) if amount else None}
+    tot = sum(ms for _, ms in trace.values()) or 1.0
+    for name, (n_launch, ms) in trace.items():
+        kern[name]["share"] = round(ms / tot, 4)
+    dom = max(trace.items(), key=lambda kv: kv[1][1])[0] if trace else None
+    roof = None
+    if dom:
+        kd = kern[dom]
+        kind = work.get(dom, ("hbm", 0))[0]
+        traffic = None
+        tpath = os.path.join(ROOT, "profiles", "traffic.json")
+        if os.path.exists(tpath):
+            tr = json.load(open(tpath)).get(lc.name, {}).get(dom)
+            if tr is not None:
+                traffic = tr
+        roof = {"bound": kind, "kernel": dom, "achieved": kd["achieved"],
+                "peak": peaks.get("bf16_tflops_sustained") if kind == "tensor" else peaks["hbm_gbs"],
+                "unit": kd["unit"], "frac": kd["frac"], "traffic": traffic,
+                "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if kind == 'tensor' else 'hbm_gbs'})"}
+    gemm_ms = sum(ms for n, (_, ms) in trace.items() if n.startswith("gemm_"))
+    gemm_flops = sum(work[n][1] * trace[n][0] for n in trace if n.startswith("gemm_") and n in work)
+    gemm_tflops = gemm_flops / (gemm_ms / 1e3) / 1e12 if gemm_ms else None
+
+    # ---- CPU oracle on a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        n_tok = args.cpu_tokens
+        host, lc_s = oracle_sample_inputs(lc, inp, n_tok)
+        dt = time_oracle(lc_s, host)
+        cpu = {"value": round(n_tok / dt, 2), "unit": "tokens/s", "cores": cpu_cores(),
+               "kind": "oracle",
+               "sample": f"{n_tok} seeded tokens of the workload, all {lc.E} experts, fwd+bwd in "
+                         f"fp64 numpy ({dt:.1f} s)"}
+
+    flops_step = layer_flops(lc, lc.backward)
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": lc.dtype,
+        "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights, random init)",
+        "config": {"workload": lc.name, "T": lc.T, "d_model": lc.d, "experts": lc.E, "top_k": lc.k,
+                   "ffn": lc.f, "shared_ffn": lc.f_shared,
+                   "score_fn": "sigmoid" if lc.score_fn else "softmax", "renorm": bool(lc.renorm),
+                   "shared_gate": bool(lc.shared_gate), "router_bias": lc.router_bias,
+                   "pass": "fwd+bwd" if lc.backward else "fwd",
+                   "global_batch": lc.T * world, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (expert weights alone exceed 129 MB), no flush"},
+        "tflops": round(flops_step / (ms_step / 1e3) / 1e12, 1),
+        "pct_bf16_peak": round(flops_step / (ms_step / 1e3) / 1e12 / peaks["bf16_tflops_sustained"], 4),
+        "grouped_gemm_tflops": round(gemm_tflops, 1) if gemm_tflops else None,
+        "roofline": roof,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "cpu_baseline": cpu,
+        "kernels": kern,
+    }
+    if world > 1:
+        dist.destroy_process_group()
+    return out
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args, lc):
+    """The fp64 CPU oracle as the reference arm: each step is the oracle's forward + backward on
+    a bounded, seeded sample of the same workload's tokens (all experts)."""
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = moe_inputs.make_layer_inputs(lc, seed=args.seed, device=dev)
+    host, lc_s = oracle_sample_inputs(lc, inp, args.ref_tokens)
+    del inp
+    for _ in range(args.warmup):
+        time_oracle(lc_s, host)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        time_oracle(lc_s, host)
+    dt = time.perf_counter() - t0
+    value = args.ref_tokens * args.steps / dt
+    sample = (f"{args.ref_tokens} seeded tokens of the workload per step, all {lc.E} experts, "
+              f"fp64 numpy forward+backward")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": lc.name, "T": lc.T, "pass": "fwd+bwd"},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="deepseek", choices=list(moe_inputs.CONFIGS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-tokens", type=int, default=256)
+    ap.add_argument("--ref-tokens", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "native" else args.warmup
+    lc = moe_inputs.CONFIGS[args.workload]
+    out = run_reference(args, lc) if args.impl == "reference" else run_gpu(args, lc)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

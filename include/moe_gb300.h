@@ -1,0 +1,221 @@
+/*
+ * moe_gb300.h -- C ABI of a single-GPU (GB300, sm_103a) mixture-of-experts layer:
+ * router GEMM -> top-k -> per-expert histogram / prefix sum / token<->slot permutation ->
+ * permute -> grouped SwiGLU expert GEMMs -> weighted combine (+ optional shared expert),
+ * and the backward pass of all of it.
+ *
+ * What the layer is.  "Megatron-Bridge 深度剖析：MoE 大模型训练加速的工程之道":
+ *   §Motivation -- a DeepSeek-style layer: 128 SwiGLU experts (gate_proj, up_proj,
+ *     down_proj), top-6 sigmoid routing;
+ *   §Expert Parallel 基础, workflow figure -- Step 1 the router picks top-k experts per token;
+ *     Step 2 tokens are regrouped by expert (an all-to-all across GPUs; on one GPU a local
+ *     permutation); Step 3 the experts run and the results go back to token order;
+ *   §计算融合 / Grouped GEMM -- all experts' GEMMs in one launch over ragged token counts,
+ *     expert weights stored contiguously (weight0, weight1, ...);
+ *   §Permute Fusion -- the permutation is a memory copy that groups each expert's tokens;
+ *   §Shared Expert Overlap -- a shared expert every token goes through, added to the routed
+ *     output;
+ *   §权重映射策略 (GatedMLPMapping) -- fc1 = [gate_proj; up_proj], shape (2*ffn, hidden).
+ * "Add Megatron-Core MTP training for Qwen3.5 MoE" (What's in it) -- the shared-expert gate.
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers owned by the caller, unless a parameter says otherwise.
+ *     The library allocates no device memory in any call below; scratch space comes from the
+ *     caller's workspace, sized by moe_workspace_bytes().
+ *   - Every pointer must be 16-byte aligned (MOE_ERR_ALIGNMENT otherwise).
+ *   - All work is enqueued on `stream` (a cudaStream_t passed as void*, NULL = legacy default
+ *     stream) and is asynchronous with respect to the host.  Calls keep no state between
+ *     them; two calls may run concurrently on different streams if their buffers and
+ *     workspaces are distinct.
+ *   - Row-major dense layouts; T tokens, d = d_model, E experts, k experts per token,
+ *     f = expert ffn width, f_s = shared expert ffn width, N = T*k routed rows.
+ *   - Activations and weights are in cfg->dtype (bf16 or fp32).  Router logits, gates and
+ *     all weight gradients are fp32.  Weight gradients are overwritten, not accumulated.
+ *   - Return value: MOE_OK (0) or a negative moe_status.  Argument errors are detected on the
+ *     host before anything is enqueued.  MOE_ERR_CUDA means a launch failed; the message is
+ *     in moe_last_error().  A kernel that detects an inconsistency at run time (a bounded wait
+ *     that ran out, an index out of range) records it in a device error word that
+ *     moe_check_device_error() reads.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,   /* null where a buffer is required, negative size, k > E ... */
+  MOE_ERR_UNSUPPORTED = -2,   /* E > 256, k > 8, d or f not a multiple of 8, ...           */
+  MOE_ERR_WORKSPACE = -3,     /* workspace null or smaller than moe_workspace_bytes()      */
+  MOE_ERR_ALIGNMENT = -4,     /* a pointer is not 16-byte aligned                          */
+  MOE_ERR_CUDA = -5,          /* a CUDA call or launch failed (see moe_last_error())       */
+  MOE_ERR_DEVICE_CHECK = -6   /* a kernel reported a run-time inconsistency                */
+} moe_status;
+
+enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
+enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 };
+
+/* Limits checked by every entry point. */
+enum { MOE_MAX_EXPERTS = 256, MOE_MAX_TOPK = 8 };
+
+/* Layer configuration, passed by pointer to every call.
+ *   score_fn   MOE_SCORE_SOFTMAX or MOE_SCORE_SIGMOID ("moe_router_score_function").
+ *   renorm     1: the k selected gates are divided by their sum (softmax+renorm equals the
+ *              softmax over the k selected logits); 0: raw softmax-over-E / sigmoid scores.
+ *   f_shared   0: no shared expert.
+ *   shared_gate 1: the shared expert's output is scaled by sigmoid(w_sg . x_t).
+ *   dtype      MOE_DTYPE_BF16 (tensor-core path, fp32 accumulation) or MOE_DTYPE_F32
+ *              (fp32 CUDA-core path, for exact-tolerance checks). */
+typedef struct moe_cfg {
+  int32_t T, d, E, k, f, f_shared;
+  int32_t score_fn;
+  int32_t renorm;
+  int32_t shared_gate;
+  int32_t dtype;
+} moe_cfg;
+
+/* Which call a workspace is sized for. */
+enum {
+  MOE_WS_ROUTE = 0,       /* moe_route_topk                           */
+  MOE_WS_FFN_FWD = 1,     /* moe_grouped_swiglu_fwd                   */
+  MOE_WS_FFN_BWD = 2,     /* moe_grouped_swiglu_bwd                   */
+  MOE_WS_LAYER_FWD = 3,   /* moe_layer_fwd                            */
+  MOE_WS_LAYER_BWD = 4    /* moe_layer_bwd                            */
+};
+
+/* Bytes of caller workspace the call `which` needs for cfg (0 if cfg is invalid). */
+size_t moe_workspace_bytes(const moe_cfg* cfg, int which);
+
+/* Router + top-k + routing maps (one GPU's stand-in for the expert-parallel dispatch plan).
+ * "Megatron-Bridge 深度剖析", §Expert Parallel 基础 (Step 1, Router(x) -> TopK scores) and
+ * §核心模块架构 (moe_router_topk, moe_router_score_function).
+ *   x [T,d], W_r [E,d] (dtype); b_r [E] fp32 or NULL (added to the logits).
+ *   logits_in [T,E] fp32 or NULL: if set, the router GEMM is skipped and these logits are
+ *     routed (b_r is then ignored).
+ *   logits_out [T,E] fp32 or NULL: receives the router logits (x.W_r^T + b_r, fp32).
+ *   Outputs: idx [T,k] int32 -- selected experts, by descending logit, equal logits -> lower
+ *     expert index first; gate [T,k] fp32 -- combine weights (softmax / sigmoid, renorm per
+ *     cfg); counts [E], offsets [E+1] int32 (offsets[0]=0, offsets[E]=N); slot_of_pair [T,k],
+ *     token_of_slot [N] int32: pair (t,j) sits in row slot_of_pair[t,j] of the expert-sorted
+ *     layout; inside one expert's rows the tokens ascend.
+ *   Selection is made on fp32 logits and is bit-for-bit deterministic for given logits. */
+int moe_route_topk(const moe_cfg* cfg, const void* x, const void* W_r, const float* b_r,
+                   const float* logits_in, float* logits_out, int32_t* idx, float* gate,
+                   int32_t* counts, int32_t* offsets, int32_t* slot_of_pair,
+                   int32_t* token_of_slot, void* ws, size_t ws_bytes, void* stream);
+
+/* Permute: x_perm[s] = x[token_of_slot[s]] for s < N.  "Megatron-Bridge 深度剖析",
+ * §Permute Fusion (tokens regrouped by expert: one memory copy).
+ *   x [T,d], x_perm [N,d] (dtype); slot_of_pair [T,k] from moe_route_topk. */
+int moe_permute(const moe_cfg* cfg, const void* x, const int32_t* slot_of_pair, void* x_perm,
+                void* stream);
+
+/* Grouped SwiGLU experts, forward.  "Megatron-Bridge 深度剖析", §计算融合 / Grouped GEMM and
+ * §权重映射策略 (GatedMLPMapping: fc1 = [gate; up]).  For every expert e and every row s in
+ * [offsets[e], offsets[e+1]):
+ *   [a | u] = x_perm[s] . W1[e]^T,  h[s] = SiLU(a) * u,  y_perm[s] = h[s] . W2[e]^T.
+ *   x_perm [N,d]; W1 [E,2f,d] (rows 0..f-1 gate, f..2f-1 up); W2 [E,d,f]; offsets [E+1].
+ *   Outputs (dtype): h [N,f]; act [N,2f] = [a | u] (pre-activations, kept for the backward;
+ *   may be NULL if no backward follows); y_perm [N,d].
+ *   The number of rows N is cfg->T*cfg->k (offsets[E] must equal it). */
+int moe_grouped_swiglu_fwd(const moe_cfg* cfg, const void* x_perm, const int32_t* offsets,
+                           const void* W1, const void* W2, void* h, void* act, void* y_perm,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* Grouped SwiGLU experts, backward (chain rule of moe_grouped_swiglu_fwd).
+ *   Inputs: x_perm, offsets, W1, W2, act, h as in the forward; dy_perm [N,d] (dtype).
+ *   Outputs: dx_perm [N,d] (dtype); dW1 [E,2f,d], dW2 [E,d,f] fp32 (experts with no rows
+ *   get zeros).  The gradient of [a | u] is formed in the workspace. */
+int moe_grouped_swiglu_bwd(const moe_cfg* cfg, const void* x_perm, const int32_t* offsets,
+                           const void* W1, const void* W2, const void* act, const void* h,
+                           const void* dy_perm, void* dx_perm, float* dW1, float* dW2,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* Unpermute + weighted combine: "Megatron-Bridge 深度剖析", §Expert Parallel 基础 (Step 3,
+ * results sent back to token order) and §Shared Expert Overlap (shared output added).
+ *   y[t] = sum_{j<k} gate[t,j] * y_perm[slot_of_pair[t,j]]  (+ c_t * shared_out[t])
+ *   accumulated in fp32 in ascending j, the shared term last, rounded once to dtype.
+ *   shared_out [T,d] (dtype) or NULL; shared_coef [T] fp32 or NULL (c_t = 1). */
+int moe_unpermute_combine(const moe_cfg* cfg, const void* y_perm, const float* gate,
+                          const int32_t* slot_of_pair, const void* shared_out,
+                          const float* shared_coef, void* y, void* stream);
+
+/* Backward of moe_unpermute_combine.
+ *   dy_perm[slot(t,j)] = gate[t,j] * dy[t];  dgate[t,j] = <dy[t], y_perm[slot(t,j)]> (fp32);
+ *   with shared_out: dshared[t] = c_t * dy[t] (dtype) and, if shared_coef is set,
+ *   dcoef[t] = <dy[t], shared_out[t]> (fp32).  dshared / dcoef may be NULL when unused. */
+int moe_unpermute_combine_bwd(const moe_cfg* cfg, const void* dy, const void* y_perm,
+                              const float* gate, const int32_t* slot_of_pair,
+                              const void* shared_out, const float* shared_coef, void* dy_perm,
+                              float* dgate, void* dshared, float* dcoef, void* stream);
+
+/* Buffers a forward pass leaves for the backward.  All are caller-owned device buffers with
+ * the shapes given; dtype means cfg->dtype.  The s_* members are used only with a shared
+ * expert (f_s > 0) and s_coef only with the shared gate. */
+typedef struct moe_saved {
+  float* logits;          /* [T,E]  fp32                                       */
+  int32_t* idx;           /* [T,k]                                             */
+  float* gate;            /* [T,k]  fp32                                       */
+  int32_t* counts;        /* [E]                                               */
+  int32_t* offsets;       /* [E+1]                                             */
+  int32_t* slot_of_pair;  /* [T,k]                                             */
+  int32_t* token_of_slot; /* [N]                                               */
+  void* x_perm;           /* [N,d]   dtype                                     */
+  void* act;              /* [N,2f]  dtype  ([a | u] pre-activations)          */
+  void* h;                /* [N,f]   dtype                                     */
+  void* y_perm;           /* [N,d]   dtype                                     */
+  void* s_act;            /* [T,2f_s] dtype                                    */
+  void* s_h;              /* [T,f_s]  dtype                                    */
+  void* s_out;            /* [T,d]    dtype                                    */
+  float* s_coef;          /* [T]  fp32, c_t = sigmoid(w_sg . x_t)              */
+} moe_saved;
+
+/* Whole layer forward: route, permute, grouped SwiGLU, shared expert, combine.
+ *   x [T,d]; W_r [E,d]; b_r [E] fp32 or NULL; W1 [E,2f,d]; W2 [E,d,f];
+ *   Ws1 [2f_s,d], Ws2 [d,f_s] (NULL without shared expert); w_sg [d] (NULL without gate).
+ *   y [T,d].  `saved` receives everything the backward needs. */
+int moe_layer_fwd(const moe_cfg* cfg, const void* x, const void* W_r, const float* b_r,
+                  const void* W1, const void* W2, const void* Ws1, const void* Ws2,
+                  const void* w_sg, void* y, const moe_saved* saved, void* ws, size_t ws_bytes,
+                  void* stream);
+
+/* Whole layer backward, for the upstream gradient dy [T,d].  No gradient flows through the
+ * expert selection (it is piecewise constant in the logits); b_r gets none (an input).
+ *   Outputs: dx [T,d] (dtype); dW_r [E,d], dW1 [E,2f,d], dW2 [E,d,f], dWs1 [2f_s,d],
+ *   dWs2 [d,f_s], dw_sg [d] -- all fp32 (the shared ones NULL when absent). */
+int moe_layer_bwd(const moe_cfg* cfg, const void* dy, const void* x, const void* W_r,
+                  const void* W1, const void* W2, const void* Ws1, const void* Ws2,
+                  const void* w_sg, const moe_saved* saved, void* dx, float* dW_r, float* dW1,
+                  float* dW2, float* dWs1, float* dWs2, float* dw_sg, void* ws, size_t ws_bytes,
+                  void* stream);
+
+/* Message of the last error on this host thread ("" if none). */
+const char* moe_last_error(void);
+
+/* Synchronises `stream`, reads and clears the device error word of the current device.
+ * Returns MOE_OK, MOE_ERR_DEVICE_CHECK (with the kernel's code in *code if code != NULL),
+ * or MOE_ERR_CUDA. */
+int moe_check_device_error(void* stream, int32_t* code);
+
+/* Launch accounting and per-kernel timing (tracing).  moe_trace_enable(1) makes every
+ * launch of this library record CUDA events around itself on its stream; moe_trace_read()
+ * synchronises the device and returns, per kernel kind, launches and total milliseconds.
+ * moe_launch_count() is the number of kernels this library launched in this process. */
+uint64_t moe_launch_count(void);
+int moe_trace_enable(int on);
+/* Fills up to `cap` entries; returns the number of kernel kinds seen (or < 0 on error). */
+int moe_trace_read(char* names, int name_stride, int* launches, double* total_ms, int cap);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,246 @@
+"""ctypes binding of libmoe_gb300.so (declared in include/moe_gb300.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA kernels.  The
+functions take torch CUDA tensors (PyTorch provides device memory and streams) and raise
+RuntimeError with the library's message when a call fails.  There is no fallback: without the
+built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+LIB_PATH = os.path.join(PKG, "_build", "libmoe_gb300.so")
+HEADER = os.path.join(ROOT, "include", "moe_gb300.h")
+
+MOE_OK = 0
+STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_WORKSPACE",
+          -4: "MOE_ERR_ALIGNMENT", -5: "MOE_ERR_CUDA", -6: "MOE_ERR_DEVICE_CHECK"}
+SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
+DTYPE_BF16, DTYPE_F32 = 0, 1
+WS_ROUTE, WS_FFN_FWD, WS_FFN_BWD, WS_LAYER_FWD, WS_LAYER_BWD = range(5)
+
+
+class MoeCfg(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("T", "d", "E", "k", "f", "f_shared", "score_fn", "renorm", "shared_gate", "dtype")]
+
+
+class MoeSaved(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("logits", "idx", "gate", "counts", "offsets", "slot_of_pair", "token_of_slot",
+                 "x_perm", "act", "h", "y_perm", "s_act", "s_h", "s_out", "s_coef")]
+
+
+_VP = ctypes.c_void_p
+_SZ = ctypes.c_size_t
+_CFG = ctypes.POINTER(MoeCfg)
+_SIGS = {
+    "moe_workspace_bytes": (_SZ, [_CFG, ctypes.c_int]),
+    "moe_route_topk": (ctypes.c_int, [_CFG] + [_VP] * 12 + [_SZ, _VP]),
+    "moe_permute": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP]),
+    "moe_grouped_swiglu_fwd": (ctypes.c_int, [_CFG] + [_VP] * 8 + [_SZ, _VP]),
+    "moe_grouped_swiglu_bwd": (ctypes.c_int, [_CFG] + [_VP] * 11 + [_SZ, _VP]),
+    "moe_unpermute_combine": (ctypes.c_int, [_CFG] + [_VP] * 7),
+    "moe_unpermute_combine_bwd": (ctypes.c_int, [_CFG] + [_VP] * 11),
+    "moe_layer_fwd": (ctypes.c_int, [_CFG] + [_VP] * 9 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP]),
+    "moe_layer_bwd": (ctypes.c_int, [_CFG] + [_VP] * 8 + [ctypes.POINTER(MoeSaved)] + [_VP] * 8
+                      + [_SZ, _VP]),
+    "moe_last_error": (ctypes.c_char_p, []),
+    "moe_check_device_error": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_int32)]),
+    "moe_launch_count": (ctypes.c_uint64, []),
+    "moe_trace_enable": (ctypes.c_int, [ctypes.c_int]),
+    "moe_trace_read": (ctypes.c_int, [ctypes.c_char_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                      ctypes.POINTER(ctypes.c_double), ctypes.c_int]),
+    "moe_version": (ctypes.c_int, []),
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"MoE CUDA library not built ({LIB_PATH} missing): run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def header_functions():
+    """Names of the functions include/moe_gb300.h declares."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(moe_[a-z_0-9]+)\s*\(",
+                                 text, re.M)))
+
+
+def _check(rc, what):
+    if rc != MOE_OK:
+        msg = lib().moe_last_error().decode(errors="replace")
+        raise RuntimeError(f"{what}: {STATUS.get(rc, rc)}: {msg}")
+
+
+def make_cfg(T, d, E, k, f, f_shared=0, score_fn=0, renorm=1, shared_gate=0, dtype=DTYPE_BF16):
+    return MoeCfg(T, d, E, k, f, f_shared, score_fn, renorm, shared_gate, dtype)
+
+
+def cfg_from(lc, T=None):
+    """MoeCfg from a moe_inputs.LayerConfig-like object."""
+    return make_cfg(lc.T if T is None else T, lc.d, lc.E, lc.k, lc.f, lc.f_shared, lc.score_fn,
+                    lc.renorm, lc.shared_gate, DTYPE_BF16 if lc.dtype == "bf16" else DTYPE_F32)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def workspace_bytes(cfg, which):
+    return int(lib().moe_workspace_bytes(ctypes.byref(cfg), which))
+
+
+def workspace(cfg, which, device="cuda"):
+    import torch
+    n = workspace_bytes(cfg, which)
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=device)
+
+
+# ----------------------------------------------------------------------------- stage calls
+
+def moe_route_topk(cfg, x, W_r, b_r, logits_in, logits_out, idx, gate, counts, offsets,
+                   slot_of_pair, token_of_slot, ws, stream=None):
+    _check(lib().moe_route_topk(ctypes.byref(cfg), _p(x), _p(W_r), _p(b_r), _p(logits_in),
+                                _p(logits_out), _p(idx), _p(gate), _p(counts), _p(offsets),
+                                _p(slot_of_pair), _p(token_of_slot), _p(ws),
+                                0 if ws is None else ws.numel(), _stream(stream)),
+           "moe_route_topk")
+
+
+def moe_permute(cfg, x, slot_of_pair, x_perm, stream=None):
+    _check(lib().moe_permute(ctypes.byref(cfg), _p(x), _p(slot_of_pair), _p(x_perm),
+                             _stream(stream)), "moe_permute")
+
+
+def moe_grouped_swiglu_fwd(cfg, x_perm, offsets, W1, W2, h, act, y_perm, ws=None, stream=None):
+    _check(lib().moe_grouped_swiglu_fwd(ctypes.byref(cfg), _p(x_perm), _p(offsets), _p(W1), _p(W2),
+                                        _p(h), _p(act), _p(y_perm), _p(ws),
+                                        0 if ws is None else ws.numel(), _stream(stream)),
+           "moe_grouped_swiglu_fwd")
+
+
+def moe_grouped_swiglu_bwd(cfg, x_perm, offsets, W1, W2, act, h, dy_perm, dx_perm, dW1, dW2, ws,
+                           stream=None):
+    _check(lib().moe_grouped_swiglu_bwd(ctypes.byref(cfg), _p(x_perm), _p(offsets), _p(W1), _p(W2),
+                                        _p(act), _p(h), _p(dy_perm), _p(dx_perm), _p(dW1), _p(dW2),
+                                        _p(ws), 0 if ws is None else ws.numel(), _stream(stream)),
+           "moe_grouped_swiglu_bwd")
+
+
+def moe_unpermute_combine(cfg, y_perm, gate, slot_of_pair, shared_out, shared_coef, y, stream=None):
+    _check(lib().moe_unpermute_combine(ctypes.byref(cfg), _p(y_perm), _p(gate), _p(slot_of_pair),
+                                       _p(shared_out), _p(shared_coef), _p(y), _stream(stream)),
+           "moe_unpermute_combine")
+
+
+def moe_unpermute_combine_bwd(cfg, dy, y_perm, gate, slot_of_pair, shared_out, shared_coef,
+                              dy_perm, dgate, dshared, dcoef, stream=None):
+    _check(lib().moe_unpermute_combine_bwd(ctypes.byref(cfg), _p(dy), _p(y_perm), _p(gate),
+                                           _p(slot_of_pair), _p(shared_out), _p(shared_coef),
+                                           _p(dy_perm), _p(dgate), _p(dshared), _p(dcoef),
+                                           _stream(stream)), "moe_unpermute_combine_bwd")
+
+
+# ----------------------------------------------------------------------------- whole layer
+
+SAVED_FIELDS = [f for f, _ in MoeSaved._fields_]
+
+
+def alloc_saved(cfg, device="cuda"):
+    """Caller-owned buffers a forward pass leaves for the backward (torch tensors)."""
+    import torch
+    dt = torch.bfloat16 if cfg.dtype == DTYPE_BF16 else torch.float32
+    T, d, E, k, f, fs = max(cfg.T, 1), cfg.d, cfg.E, cfg.k, cfg.f, cfg.f_shared
+    N = T * k
+    i32, f32 = torch.int32, torch.float32
+    s = dict(
+        logits=torch.empty(T, E, dtype=f32, device=device),
+        idx=torch.empty(T, k, dtype=i32, device=device),
+        gate=torch.empty(T, k, dtype=f32, device=device),
+        counts=torch.empty(E, dtype=i32, device=device),
+        offsets=torch.empty(E + 1, dtype=i32, device=device),
+        slot_of_pair=torch.empty(T, k, dtype=i32, device=device),
+        token_of_slot=torch.empty(max(N, 1), dtype=i32, device=device),
+        x_perm=torch.empty(max(N, 1), d, dtype=dt, device=device),
+        act=torch.empty(max(N, 1), 2 * f, dtype=dt, device=device),
+        h=torch.empty(max(N, 1), f, dtype=dt, device=device),
+        y_perm=torch.empty(max(N, 1), d, dtype=dt, device=device),
+        s_act=torch.empty(T, 2 * fs, dtype=dt, device=device) if fs else None,
+        s_h=torch.empty(T, fs, dtype=dt, device=device) if fs else None,
+        s_out=torch.empty(T, d, dtype=dt, device=device) if fs else None,
+        s_coef=torch.empty(T, dtype=f32, device=device) if cfg.shared_gate else None,
+    )
+    return s
+
+
+def saved_struct(saved):
+    return MoeSaved(*[None if saved[n] is None else saved[n].data_ptr() for n in SAVED_FIELDS])
+
+
+def moe_layer_fwd(cfg, x, W_r, b_r, W1, W2, Ws1, Ws2, w_sg, y, saved, ws, stream=None):
+    st = saved_struct(saved)
+    _check(lib().moe_layer_fwd(ctypes.byref(cfg), _p(x), _p(W_r), _p(b_r), _p(W1), _p(W2), _p(Ws1),
+                               _p(Ws2), _p(w_sg), _p(y), ctypes.byref(st), _p(ws), ws.numel(),
+                               _stream(stream)), "moe_layer_fwd")
+
+
+def moe_layer_bwd(cfg, dy, x, W_r, W1, W2, Ws1, Ws2, w_sg, saved, dx, dW_r, dW1, dW2, dWs1, dWs2,
+                  dw_sg, ws, stream=None):
+    st = saved_struct(saved)
+    _check(lib().moe_layer_bwd(ctypes.byref(cfg), _p(dy), _p(x), _p(W_r), _p(W1), _p(W2), _p(Ws1),
+                               _p(Ws2), _p(w_sg), ctypes.byref(st), _p(dx), _p(dW_r), _p(dW1),
+                               _p(dW2), _p(dWs1), _p(dWs2), _p(dw_sg), _p(ws), ws.numel(),
+                               _stream(stream)), "moe_layer_bwd")
+
+
+def check_device_error(stream=None):
+    code = ctypes.c_int32(0)
+    _check(lib().moe_check_device_error(_stream(stream), ctypes.byref(code)), "device check")
+
+
+def launch_count():
+    return int(lib().moe_launch_count())
+
+
+def trace_enable(on=True):
+    lib().moe_trace_enable(1 if on else 0)
+
+
+def trace_read(cap=64):
+    """{kernel kind: (launches, total ms)} since the last read (synchronises the device)."""
+    stride = 64
+    names = ctypes.create_string_buffer(cap * stride)
+    launches = (ctypes.c_int * cap)()
+    ms = (ctypes.c_double * cap)()
+    n = lib().moe_trace_read(names, stride, launches, ms, cap)
+    if n < 0:
+        _check(n, "moe_trace_read")
+    out = {}
+    for i in range(min(n, cap)):
+        nm = names.raw[i * stride:(i + 1) * stride].split(b"\0", 1)[0].decode()
+        out[nm] = (launches[i], ms[i])
+    return out

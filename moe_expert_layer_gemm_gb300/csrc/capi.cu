@@ -1,0 +1,767 @@
+// C ABI of the MoE layer library: argument checks, workspace carving, the order of the
+// stages, launch accounting, tracing and the device error word.  The arithmetic of every stage
+// runs in the kernels of route.cu, rowops.cu, gemm_tc.cu (bf16) and gemm_simt.cu (fp32).
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+#include "moe_gb300.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ error text
+static thread_local char g_errbuf[512];
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_errbuf, sizeof(g_errbuf), fmt, ap);
+  va_end(ap);
+}
+
+static int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_errbuf, sizeof(g_errbuf), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+// ------------------------------------------------------------------ device error word
+__device__ int g_device_error;
+
+static std::mutex g_dev_mu;
+static int* g_err_ptr[64];
+static int g_sms[64];
+
+static int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  return dev;
+}
+
+int* device_error_word() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+int num_sms() {
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_sms[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_sms[dev] = n > 0 ? n : 1;
+  }
+  return g_sms[dev];
+}
+
+// ------------------------------------------------------------------ launch accounting, tracing
+static std::atomic<uint64_t> g_launches{0};
+static std::atomic<int> g_trace_on{0};
+
+struct TraceRec {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+static std::mutex g_trace_mu;
+static std::vector<TraceRec> g_trace;
+static std::vector<cudaEvent_t> g_event_pool;
+static thread_local cudaEvent_t t_pending_start = nullptr;
+
+static cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+void trace_before(const char*, cudaStream_t s) {
+  if (!g_trace_on.load(std::memory_order_relaxed)) return;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  t_pending_start = take_event();
+  if (t_pending_start) cudaEventRecord(t_pending_start, s);
+}
+
+void trace_after(const char* name, cudaStream_t s) {
+  if (!g_trace_on.load(std::memory_order_relaxed) || !t_pending_start) return;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  cudaEvent_t stop = take_event();
+  if (stop) {
+    cudaEventRecord(stop, s);
+    g_trace.push_back({name, t_pending_start, stop});
+  }
+  t_pending_start = nullptr;
+}
+
+// ------------------------------------------------------------------ workspace carving
+struct Carve {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carve(void* b) : base(static_cast<uint8_t*>(b)) {}
+  void* take(size_t bytes) {
+    off = (off + 255) & ~static_cast<size_t>(255);
+    void* p = base ? base + off : nullptr;
+    off += bytes;
+    return p;
+  }
+};
+
+static size_t esize(const moe_cfg* c) { return c->dtype == MOE_DTYPE_BF16 ? 2 : 4; }
+static int64_t Nrows(const moe_cfg* c) { return static_cast<int64_t>(c->T) * c->k; }
+static int ext_cols(const moe_cfg* c) { return ((c->E + (c->shared_gate ? 1 : 0)) + 63) / 64 * 64; }
+
+static int router_splits(const moe_cfg* c) {
+  const int mr = c->E + (c->shared_gate ? 1 : 0);
+  const int tiles = ((mr + 127) / 128) * ((c->d + 255) / 256);
+  int s = (num_sms() + tiles - 1) / tiles;
+  const int cap_t = c->T / 256 > 1 ? c->T / 256 : 1;
+  if (s > cap_t) s = cap_t;
+  if (s > 64) s = 64;
+  if (s < 1) s = 1;
+  return s;
+}
+
+struct RouteWs {
+  int32_t* hist;
+  int32_t* base;
+  float* logits;
+};
+static RouteWs carve_route(Carve& cv, const moe_cfg* c) {
+  RouteWs w;
+  const size_t nb = static_cast<size_t>(route_blocks(c->T)) * c->E;
+  w.hist = static_cast<int32_t*>(cv.take(nb * 4));
+  w.base = static_cast<int32_t*>(cv.take(nb * 4));
+  w.logits = static_cast<float*>(cv.take(static_cast<size_t>(c->T) * c->E * 4));
+  return w;
+}
+
+struct BwdWs {
+  void* dy_perm;
+  float* dgate;
+  void* dH1;
+  void* dshared;
+  float* dcoef;
+  void* dx_shared;
+  void* dl_ext;
+  float* dz;
+  void* dx_router;
+  float* part;
+};
+static BwdWs carve_bwd(Carve& cv, const moe_cfg* c) {
+  BwdWs w;
+  const size_t es = esize(c);
+  const size_t N = static_cast<size_t>(Nrows(c));
+  const size_t T = static_cast<size_t>(c->T);
+  const bool sh = c->f_shared > 0, gt = c->shared_gate != 0;
+  w.dy_perm = cv.take(N * c->d * es);
+  w.dgate = static_cast<float*>(cv.take(N * 4));
+  size_t h1 = N * 2 * c->f;
+  if (sh && T * 2 * c->f_shared > h1) h1 = T * 2 * c->f_shared;
+  w.dH1 = cv.take(h1 * es);
+  w.dshared = sh ? cv.take(T * c->d * es) : nullptr;
+  w.dcoef = gt ? static_cast<float*>(cv.take(T * 4)) : nullptr;
+  w.dx_shared = sh ? cv.take(T * c->d * es) : nullptr;
+  w.dl_ext = cv.take(T * ext_cols(c) * es);
+  w.dz = static_cast<float*>(cv.take(T * 4));
+  w.dx_router = cv.take(T * c->d * es);
+  const size_t mr = c->E + (gt ? 1 : 0);
+  w.part = static_cast<float*>(cv.take(static_cast<size_t>(router_splits(c)) * mr * c->d * 4));
+  return w;
+}
+
+// ------------------------------------------------------------------ checks
+static int check_cfg(const moe_cfg* c) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cfg is NULL");
+  if (c->T < 0 || c->d <= 0 || c->E <= 0 || c->k <= 0 || c->f <= 0 || c->f_shared < 0)
+    return fail(MOE_ERR_INVALID_ARG, "sizes must be positive (T >= 0): T=%d d=%d E=%d k=%d f=%d f_shared=%d",
+                c->T, c->d, c->E, c->k, c->f, c->f_shared);
+  if (c->E > MOE_MAX_EXPERTS) return fail(MOE_ERR_UNSUPPORTED, "E=%d exceeds %d", c->E, MOE_MAX_EXPERTS);
+  if (c->k > MOE_MAX_TOPK) return fail(MOE_ERR_UNSUPPORTED, "k=%d exceeds %d", c->k, MOE_MAX_TOPK);
+  if (c->k > c->E) return fail(MOE_ERR_INVALID_ARG, "k=%d exceeds E=%d", c->k, c->E);
+  if (c->score_fn != MOE_SCORE_SOFTMAX && c->score_fn != MOE_SCORE_SIGMOID)
+    return fail(MOE_ERR_INVALID_ARG, "score_fn=%d", c->score_fn);
+  if ((c->renorm != 0 && c->renorm != 1) || (c->shared_gate != 0 && c->shared_gate != 1))
+    return fail(MOE_ERR_INVALID_ARG, "renorm and shared_gate must be 0 or 1");
+  if (c->shared_gate && c->f_shared == 0)
+    return fail(MOE_ERR_INVALID_ARG, "shared_gate needs a shared expert (f_shared > 0)");
+  if (c->dtype != MOE_DTYPE_BF16 && c->dtype != MOE_DTYPE_F32)
+    return fail(MOE_ERR_INVALID_ARG, "dtype=%d", c->dtype);
+  const int mult = c->dtype == MOE_DTYPE_BF16 ? 8 : 4;
+  if (c->d % mult || c->f % mult || c->f_shared % mult)
+    return fail(MOE_ERR_UNSUPPORTED, "d, f and f_shared must be multiples of %d (16-byte rows)", mult);
+  if (Nrows(c) > 0x7fffffffLL) return fail(MOE_ERR_UNSUPPORTED, "T*k exceeds 2^31-1");
+  return MOE_OK;
+}
+
+static int check_ptr(const void* p, const char* name, bool required) {
+  if (!p) return required ? fail(MOE_ERR_INVALID_ARG, "%s is NULL", name) : MOE_OK;
+  if (reinterpret_cast<uintptr_t>(p) & 15u)
+    return fail(MOE_ERR_ALIGNMENT, "%s is not 16-byte aligned", name);
+  return MOE_OK;
+}
+
+static int check_ws(const moe_cfg* c, int which, void* ws, size_t ws_bytes) {
+  const size_t need = moe_workspace_bytes(c, which);
+  if (need == 0) return MOE_OK;
+  if (!ws || ws_bytes < need)
+    return fail(MOE_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                ws ? ws_bytes : static_cast<size_t>(0));
+  return check_ptr(ws, "ws", true);
+}
+
+static cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
+
+// ------------------------------------------------------------------ stages
+static int gemm(const moe_cfg* c, const GemmDesc& g, cudaStream_t st) {
+  return c->dtype == MOE_DTYPE_BF16 ? gemm_tc(g, st) : gemm_simt(g, st);
+}
+
+static GemmDesc desc0() {
+  GemmDesc g;
+  memset(&g, 0, sizeof(g));
+  return g;
+}
+
+static Operand opnd(const void* base, int64_t rows, int64_t cols, bool mn) {
+  Operand o;
+  o.base = base;
+  o.rows = rows;
+  o.cols = cols;
+  o.ld = cols;
+  o.mn_major = mn;
+  return o;
+}
+
+static int route_impl(const moe_cfg* c, const void* x, const void* W_r, const float* b_r,
+                      const float* logits_in, float* logits_out, int32_t* idx, float* gate,
+                      int32_t* counts, int32_t* offsets, int32_t* sop, int32_t* tos,
+                      const RouteWs& w, cudaStream_t st) {
+  const float* logits = logits_in;
+  if (!logits) {
+    float* dst = logits_out ? logits_out : w.logits;
+    GemmDesc g = desc0();
+    g.name = "gemm_router";
+    g.sched = RAGGED_M;
+    g.epi = EPI_F32;
+    g.G = 1;
+    g.M = c->T;
+    g.N = c->E;
+    g.K = c->d;
+    g.A = opnd(x, c->T, c->d, false);
+    g.B = opnd(W_r, c->E, c->d, false);
+    g.out = dst;
+    g.ldo = c->E;
+    g.bias = b_r;
+    MOE_TRY(gemm(c, g, st));
+    logits = dst;
+  }
+  MOE_TRY(launch_topk(logits, c->T, c->E, c->k, c->score_fn, c->renorm, idx, gate, w.hist, st));
+  MOE_TRY(launch_scan(w.hist, c->E, route_blocks(c->T), w.base, counts, offsets, st));
+  MOE_TRY(launch_slots(idx, c->T, c->k, c->E, w.base, sop, tos, st));
+  return MOE_OK;
+}
+
+// fc1 + SwiGLU and fc2 for G groups whose rows are given by offsets (null: one group of `rows`).
+static int ffn_fwd_impl(const moe_cfg* c, int G, const int32_t* offsets, int64_t rows, int f,
+                        const void* x_perm, const void* W1, const void* W2, void* h, void* act,
+                        void* y_perm, cudaStream_t st) {
+  const int d = c->d;
+  const bool shared = offsets == nullptr;
+  GemmDesc g1 = desc0();
+  g1.name = shared ? "gemm_shared_fc1_swiglu" : "gemm_fc1_swiglu";
+  g1.sched = RAGGED_M;
+  g1.epi = EPI_SWIGLU_FWD;
+  g1.G = G;
+  g1.offsets = offsets;
+  g1.M = static_cast<int>(rows);
+  g1.N = 2 * f;
+  g1.K = d;
+  g1.A = opnd(x_perm, rows, d, false);
+  g1.B = opnd(W1, static_cast<int64_t>(G) * 2 * f, d, false);
+  g1.b_group_rows = 2 * f;
+  g1.b_up_rows = f;
+  g1.f = f;
+  g1.out = h;
+  g1.ldo = f;
+  g1.out2 = act;
+  g1.ldo2 = 2 * f;
+  MOE_TRY(gemm(c, g1, st));
+  GemmDesc g2 = desc0();
+  g2.name = shared ? "gemm_shared_fc2" : "gemm_fc2";
+  g2.sched = RAGGED_M;
+  g2.epi = EPI_STORE;
+  g2.G = G;
+  g2.offsets = offsets;
+  g2.M = static_cast<int>(rows);
+  g2.N = d;
+  g2.K = f;
+  g2.A = opnd(h, rows, f, false);
+  g2.B = opnd(W2, static_cast<int64_t>(G) * d, f, false);
+  g2.b_group_rows = d;
+  g2.out = y_perm;
+  g2.ldo = d;
+  return gemm(c, g2, st);
+}
+
+// Backward of ffn_fwd_impl.  Order matters when dx_perm aliases dy_perm: dy_perm is last read
+// by the fc2 weight gradient, which runs before the fc1 data gradient writes dx_perm.
+static int ffn_bwd_impl(const moe_cfg* c, int G, const int32_t* offsets, int64_t rows, int f,
+                        const void* x_perm, const void* W1, const void* W2, const void* act,
+                        const void* h, const void* dy_perm, void* dH1, void* dx_perm, float* dW1,
+                        float* dW2, cudaStream_t st) {
+  const int d = c->d;
+  const bool shared = offsets == nullptr;
+  // dh = dy_perm . W2_g  (+ SwiGLU backward -> dH1 = [da | du])
+  GemmDesc a = desc0();
+  a.name = shared ? "gemm_shared_fc2_dgrad" : "gemm_fc2_dgrad";
+  a.sched = RAGGED_M;
+  a.epi = EPI_SWIGLU_BWD;
+  a.G = G;
+  a.offsets = offsets;
+  a.M = static_cast<int>(rows);
+  a.N = f;
+  a.K = d;
+  a.A = opnd(dy_perm, rows, d, false);
+  a.B = opnd(W2, static_cast<int64_t>(G) * d, f, true);
+  a.b_group_rows = d;
+  a.f = f;
+  a.out = dH1;
+  a.ldo = 2 * f;
+  a.aux = act;
+  a.ld_aux = 2 * f;
+  MOE_TRY(gemm(c, a, st));
+  // dW2_g = dy_perm_g^T . h_g
+  GemmDesc b = desc0();
+  b.name = shared ? "gemm_shared_fc2_wgrad" : "gemm_fc2_wgrad";
+  b.sched = RAGGED_K;
+  b.epi = EPI_F32;
+  b.G = G;
+  b.offsets = offsets;
+  b.M = d;
+  b.N = f;
+  b.K = static_cast<int>(rows);
+  b.A = opnd(dy_perm, rows, d, true);
+  b.B = opnd(h, rows, f, true);
+  b.out = dW2;
+  b.ldo = f;
+  b.out_group_stride = static_cast<int64_t>(d) * f;
+  MOE_TRY(gemm(c, b, st));
+  // dx_perm = dH1 . W1_g
+  GemmDesc e = desc0();
+  e.name = shared ? "gemm_shared_fc1_dgrad" : "gemm_fc1_dgrad";
+  e.sched = RAGGED_M;
+  e.epi = EPI_STORE;
+  e.G = G;
+  e.offsets = offsets;
+  e.M = static_cast<int>(rows);
+  e.N = d;
+  e.K = 2 * f;
+  e.A = opnd(dH1, rows, 2 * f, false);
+  e.B = opnd(W1, static_cast<int64_t>(G) * 2 * f, d, true);
+  e.b_group_rows = 2 * f;
+  e.out = dx_perm;
+  e.ldo = d;
+  MOE_TRY(gemm(c, e, st));
+  // dW1_g = dH1_g^T . x_perm_g
+  GemmDesc w = desc0();
+  w.name = shared ? "gemm_shared_fc1_wgrad" : "gemm_fc1_wgrad";
+  w.sched = RAGGED_K;
+  w.epi = EPI_F32;
+  w.G = G;
+  w.offsets = offsets;
+  w.M = 2 * f;
+  w.N = d;
+  w.K = static_cast<int>(rows);
+  w.A = opnd(dH1, rows, 2 * f, true);
+  w.B = opnd(x_perm, rows, d, true);
+  w.out = dW1;
+  w.ldo = d;
+  w.out_group_stride = static_cast<int64_t>(2) * f * d;
+  return gemm(c, w, st);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+// ====================================================================== C ABI
+extern "C" {
+
+int moe_version(void) { return 100; }
+
+const char* moe_last_error(void) { return g_errbuf; }
+
+uint64_t moe_launch_count(void) { return g_launches.load(); }
+
+int moe_trace_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_on.store(on ? 1 : 0);
+  return MOE_OK;
+}
+
+int moe_trace_read(char* names, int name_stride, int* launches, double* total_ms, int cap) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  std::vector<std::string> kinds;
+  std::vector<int> cnt;
+  std::vector<double> ms;
+  for (auto& r : g_trace) {
+    if (cudaEventSynchronize(r.stop) != cudaSuccess)
+      return fail(MOE_ERR_CUDA, "cudaEventSynchronize failed in trace read");
+    float t = 0.f;
+    cudaEventElapsedTime(&t, r.start, r.stop);
+    size_t i = 0;
+    for (; i < kinds.size(); ++i)
+      if (kinds[i] == r.name) break;
+    if (i == kinds.size()) {
+      kinds.emplace_back(r.name);
+      cnt.push_back(0);
+      ms.push_back(0.0);
+    }
+    cnt[i] += 1;
+    ms[i] += t;
+    g_event_pool.push_back(r.start);
+    g_event_pool.push_back(r.stop);
+  }
+  g_trace.clear();
+  const int n = static_cast<int>(kinds.size());
+  for (int i = 0; i < n && i < cap; ++i) {
+    if (names && name_stride > 0) {
+      strncpy(names + static_cast<size_t>(i) * name_stride, kinds[i].c_str(), name_stride - 1);
+      names[static_cast<size_t>(i) * name_stride + name_stride - 1] = 0;
+    }
+    if (launches) launches[i] = cnt[i];
+    if (total_ms) total_ms[i] = ms[i];
+  }
+  return n;
+}
+
+int moe_check_device_error(void* stream, int32_t* code) {
+  if (cudaStreamSynchronize(S(stream)) != cudaSuccess)
+    return fail(MOE_ERR_CUDA, "stream synchronisation failed: %s", cudaGetErrorString(cudaGetLastError()));
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess)
+    return fail(MOE_ERR_CUDA, "reading the device error word failed");
+  if (code) *code = v;
+  if (v) {
+    const int zero = 0;
+    cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+    return fail(MOE_ERR_DEVICE_CHECK, "a kernel reported device error code %d", v);
+  }
+  return MOE_OK;
+}
+
+size_t moe_workspace_bytes(const moe_cfg* c, int which) {
+  if (check_cfg(c) != MOE_OK) return 0;
+  Carve cv(nullptr);
+  switch (which) {
+    case MOE_WS_ROUTE:
+    case MOE_WS_LAYER_FWD:
+      carve_route(cv, c);
+      break;
+    case MOE_WS_FFN_FWD:
+      return 0;
+    case MOE_WS_FFN_BWD:
+      cv.take(static_cast<size_t>(Nrows(c)) * 2 * c->f * esize(c));
+      break;
+    case MOE_WS_LAYER_BWD:
+      carve_bwd(cv, c);
+      break;
+    default:
+      return 0;
+  }
+  return cv.off + 256;
+}
+
+int moe_route_topk(const moe_cfg* c, const void* x, const void* W_r, const float* b_r,
+                   const float* logits_in, float* logits_out, int32_t* idx, float* gate,
+                   int32_t* counts, int32_t* offsets, int32_t* slot_of_pair,
+                   int32_t* token_of_slot, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(c));
+  MOE_TRY(check_ptr(x, "x", !logits_in));
+  MOE_TRY(check_ptr(W_r, "W_r", !logits_in));
+  MOE_TRY(check_ptr(b_r, "b_r", false));
+  MOE_TRY(check_ptr(logits_in, "logits_in", false));
+  MOE_TRY(check_ptr(logits_out, "logits_out", false));
+  MOE_TRY(check_ptr(idx, "idx", true));
+  MOE_TRY(check_ptr(gate, "gate", true));
+  MOE_TRY(check_ptr(counts, "counts", true));
+  MOE_TRY(check_ptr(offsets, "offsets", true));
+  MOE_TRY(check_ptr(slot_of_pair, "slot_of_pair", true));
+  MOE_TRY(check_ptr(token_of_slot, "token_of_slot", true));
+  MOE_TRY(check_ws(c, MOE_WS_ROUTE, ws, ws_bytes));
+  cudaStream_t st = S(stream);
+  if (c->T == 0) {
+    if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * c->E, st) != cudaSuccess ||
+        cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (c->E + 1), st) != cudaSuccess)
+      return fail(MOE_ERR_CUDA, "cudaMemsetAsync failed");
+    return MOE_OK;
+  }
+  Carve cv(ws);
+  RouteWs w = carve_route(cv, c);
+  return route_impl(c, x, W_r, b_r, logits_in, logits_out, idx, gate, counts, offsets,
+                    slot_of_pair, token_of_slot, w, st);
+}
+
+int moe_permute(const moe_cfg* c, const void* x, const int32_t* slot_of_pair, void* x_perm,
+                void* stream) {
+  MOE_TRY(check_cfg(c));
+  MOE_TRY(check_ptr(x, "x", true));
+  MOE_TRY(check_ptr(slot_of_pair, "slot_of_pair", true));
+  MOE_TRY(check_ptr(x_perm, "x_perm", true));
+  return launch_permute(c->dtype, x, slot_of_pair, x_perm, c->T, c->d, c->k, S(stream));
+}
+
+int moe_grouped_swiglu_fwd(const moe_cfg* c, const void* x_perm, const int32_t* offsets,
+                           const void* W1, const void* W2, void* h, void* act, void* y_perm,
+                           void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(c));
+  MOE_TRY(check_ptr(x_perm, "x_perm", true));
+  MOE_TRY(check_ptr(offsets, "offsets", true));
+  MOE_TRY(check_ptr(W1, "W1", true));
+  MOE_TRY(check_ptr(W2, "W2", true));
+  MOE_TRY(check_ptr(h, "h", true));
+  MOE_TRY(check_ptr(act, "act", false));
+  MOE_TRY(check_ptr(y_perm, "y_perm", true));
+  MOE_TRY(check_ws(c, MOE_WS_FFN_FWD, ws, ws_bytes));
+  if (Nrows(c) == 0) return MOE_OK;
+  return ffn_fwd_impl(c, c->E, offsets, Nrows(c), c->f, x_perm, W1, W2, h, act, y_perm, S(stream));
+}
+
+int moe_grouped_swiglu_bwd(const moe_cfg* c, const void* x_perm, const int32_t* offsets,
+                           const void* W1, const void* W2, const void* act, const void* h,
+                           const void* dy_perm, void* dx_perm, float* dW1, float* dW2, void* ws,
+                           size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(c));
+  MOE_TRY(check_ptr(x_perm, "x_perm", true));
+  MOE_TRY(check_ptr(offsets, "offsets", true));
+  MOE_TRY(check_ptr(W1, "W1", true));
+  MOE_TRY(check_ptr(W2, "W2", true));
+  MOE_TRY(check_ptr(act, "act", true));
+  MOE_TRY(check_ptr(h, "h", true));
+  MOE_TRY(check_ptr(dy_perm, "dy_perm", true));
+  MOE_TRY(check_ptr(dx_perm, "dx_perm", true));
+  MOE_TRY(check_ptr(dW1, "dW1", true));
+  MOE_TRY(check_ptr(dW2, "dW2", true));
+  MOE_TRY(check_ws(c, MOE_WS_FFN_BWD, ws, ws_bytes));
+  cudaStream_t st = S(stream);
+  if (Nrows(c) == 0) {
+    if (cudaMemsetAsync(dW1, 0, sizeof(float) * c->E * 2 * c->f * c->d, st) != cudaSuccess ||
+        cudaMemsetAsync(dW2, 0, sizeof(float) * c->E * c->d * c->f, st) != cudaSuccess)
+      return fail(MOE_ERR_CUDA, "cudaMemsetAsync failed");
+    return MOE_OK;
+  }
+  Carve cv(ws);
+  void* dH1 = cv.take(static_cast<size_t>(Nrows(c)) * 2 * c->f * esize(c));
+  return ffn_bwd_impl(c, c->E, offsets, Nrows(c), c->f, x_perm, W1, W2, act, h, dy_perm, dH1,
+                      dx_perm, dW1, dW2, st);
+}
+
+int moe_unpermute_combine(const moe_cfg* c, const void* y_perm, const float* gate,
+                          const int32_t* slot_of_pair, const void* shared_out,
+                          const float* shared_coef, void* y, void* stream) {
+  MOE_TRY(check_cfg(c));
+  MOE_TRY(check_ptr(y_perm, "y_perm", true));
+  MOE_TRY(check_ptr(gate, "gate", true));
+  MOE_TRY(check_ptr(slot_of_pair, "slot_of_pair", true));
+  MOE_TRY(check_ptr(shared_out, "shared_out", false));
+  MOE_TRY(check_ptr(shared_coef, "shared_coef", false));
+  MOE_TRY(check_ptr(y, "y", true));
+  return launch_combine(c->dtype, y_perm, gate, slot_of_pair, shared_out, shared_coef, y, c->T,
+                        c->d, c->k, S(stream));
+}
+
+int moe_unpermute_combine_bwd(const moe_cfg* c, const void* dy, const void* y_perm,
+                              const float* gate, const int32_t* slot_of_pair,
+                              const void* shared_out, const float* shared_coef, void* dy_perm,
+                              float* dgate, void* dshared, float* dcoef, void* stream) {
+  MOE_TRY(check_cfg(c));
+  MOE_TRY(check_ptr(dy, "dy", true));
+  MOE_TRY(check_ptr(y_perm, "y_perm", true));
+  MOE_TRY(check_ptr(gate, "gate", true));
+  MOE_TRY(check_ptr(slot_of_pair, "slot_of_pair", true));
+  MOE_TRY(check_ptr(shared_out, "shared_out", false));
+  MOE_TRY(check_ptr(shared_coef, "shared_coef", false));
+  MOE_TRY(check_ptr(dy_perm, "dy_perm", true));
+  MOE_TRY(check_ptr(dgate, "dgate", true));
+  MOE_TRY(check_ptr(dshared, "dshared", false));
+  MOE_TRY(check_ptr(dcoef, "dcoef", false));
+  return launch_combine_bwd(c->dtype, dy, y_perm, gate, slot_of_pair, shared_out, shared_coef,
+                            dy_perm, dgate, dshared, shared_coef ? dcoef : nullptr, c->T, c->d,
+                            c->k, S(stream));
+}
+
+static int check_saved(const moe_cfg* c, const moe_saved* s) {
+  if (!s) return fail(MOE_ERR_INVALID_ARG, "saved is NULL");
+  MOE_TRY(check_ptr(s->logits, "saved.logits", true));
+  MOE_TRY(check_ptr(s->idx, "saved.idx", true));
+  MOE_TRY(check_ptr(s->gate, "saved.gate", true));
+  MOE_TRY(check_ptr(s->counts, "saved.counts", true));
+  MOE_TRY(check_ptr(s->offsets, "saved.offsets", true));
+  MOE_TRY(check_ptr(s->slot_of_pair, "saved.slot_of_pair", true));
+  MOE_TRY(check_ptr(s->token_of_slot, "saved.token_of_slot", true));
+  MOE_TRY(check_ptr(s->x_perm, "saved.x_perm", true));
+  MOE_TRY(check_ptr(s->act, "saved.act", true));
+  MOE_TRY(check_ptr(s->h, "saved.h", true));
+  MOE_TRY(check_ptr(s->y_perm, "saved.y_perm", true));
+  const bool sh = c->f_shared > 0;
+  MOE_TRY(check_ptr(s->s_act, "saved.s_act", sh));
+  MOE_TRY(check_ptr(s->s_h, "saved.s_h", sh));
+  MOE_TRY(check_ptr(s->s_out, "saved.s_out", sh));
+  MOE_TRY(check_ptr(s->s_coef, "saved.s_coef", c->shared_gate != 0));
+  return MOE_OK;
+}
+
+int moe_layer_fwd(const moe_cfg* c, const void* x, const void* W_r, const float* b_r,
+                  const void* W1, const void* W2, const void* Ws1, const void* Ws2,
+                  const void* w_sg, void* y, const moe_saved* s, void* ws, size_t ws_bytes,
+                  void* stream) {
+  MOE_TRY(check_cfg(c));
+  MOE_TRY(check_ptr(x, "x", true));
+  MOE_TRY(check_ptr(W_r, "W_r", true));
+  MOE_TRY(check_ptr(b_r, "b_r", false));
+  MOE_TRY(check_ptr(W1, "W1", true));
+  MOE_TRY(check_ptr(W2, "W2", true));
+  const bool sh = c->f_shared > 0, gt = c->shared_gate != 0;
+  MOE_TRY(check_ptr(Ws1, "Ws1", sh));
+  MOE_TRY(check_ptr(Ws2, "Ws2", sh));
+  MOE_TRY(check_ptr(w_sg, "w_sg", gt));
+  MOE_TRY(check_ptr(y, "y", true));
+  MOE_TRY(check_saved(c, s));
+  MOE_TRY(check_ws(c, MOE_WS_LAYER_FWD, ws, ws_bytes));
+  cudaStream_t st = S(stream);
+  if (c->T == 0) {
+    if (cudaMemsetAsync(s->counts, 0, sizeof(int32_t) * c->E, st) != cudaSuccess ||
+        cudaMemsetAsync(s->offsets, 0, sizeof(int32_t) * (c->E + 1), st) != cudaSuccess)
+      return fail(MOE_ERR_CUDA, "cudaMemsetAsync failed");
+    return MOE_OK;
+  }
+  Carve cv(ws);
+  RouteWs w = carve_route(cv, c);
+  MOE_TRY(route_impl(c, x, W_r, b_r, nullptr, s->logits, s->idx, s->gate, s->counts, s->offsets,
+                     s->slot_of_pair, s->token_of_slot, w, st));
+  MOE_TRY(launch_permute(c->dtype, x, s->slot_of_pair, s->x_perm, c->T, c->d, c->k, st));
+  MOE_TRY(ffn_fwd_impl(c, c->E, s->offsets, Nrows(c), c->f, s->x_perm, W1, W2, s->h, s->act,
+                       s->y_perm, st));
+  if (sh) {
+    if (gt) MOE_TRY(launch_shared_gate(c->dtype, x, w_sg, s->s_coef, c->T, c->d, st));
+    MOE_TRY(ffn_fwd_impl(c, 1, nullptr, c->T, c->f_shared, x, Ws1, Ws2, s->s_h, s->s_act,
+                         s->s_out, st));
+  }
+  return launch_combine(c->dtype, s->y_perm, s->gate, s->slot_of_pair, sh ? s->s_out : nullptr,
+                        gt ? s->s_coef : nullptr, y, c->T, c->d, c->k, st);
+}
+
+int moe_layer_bwd(const moe_cfg* c, const void* dy, const void* x, const void* W_r,
+                  const void* W1, const void* W2, const void* Ws1, const void* Ws2,
+                  const void* w_sg, const moe_saved* s, void* dx, float* dW_r, float* dW1,
+                  float* dW2, float* dWs1, float* dWs2, float* dw_sg, void* ws, size_t ws_bytes,
+                  void* stream) {
+  MOE_TRY(check_cfg(c));
+  const bool sh = c->f_shared > 0, gt = c->shared_gate != 0;
+  MOE_TRY(check_ptr(dy, "dy", true));
+  MOE_TRY(check_ptr(x, "x", true));
+  MOE_TRY(check_ptr(W_r, "W_r", true));
+  MOE_TRY(check_ptr(W1, "W1", true));
+  MOE_TRY(check_ptr(W2, "W2", true));
+  MOE_TRY(check_ptr(Ws1, "Ws1", sh));
+  MOE_TRY(check_ptr(Ws2, "Ws2", sh));
+  MOE_TRY(check_ptr(w_sg, "w_sg", gt));
+  MOE_TRY(check_saved(c, s));
+  MOE_TRY(check_ptr(dx, "dx", true));
+  MOE_TRY(check_ptr(dW_r, "dW_r", true));
+  MOE_TRY(check_ptr(dW1, "dW1", true));
+  MOE_TRY(check_ptr(dW2, "dW2", true));
+  MOE_TRY(check_ptr(dWs1, "dWs1", sh));
+  MOE_TRY(check_ptr(dWs2, "dWs2", sh));
+  MOE_TRY(check_ptr(dw_sg, "dw_sg", gt));
+  MOE_TRY(check_ws(c, MOE_WS_LAYER_BWD, ws, ws_bytes));
+  cudaStream_t st = S(stream);
+  const int T = c->T, d = c->d, E = c->E, k = c->k;
+  if (T == 0) {
+    bool ok = cudaMemsetAsync(dW_r, 0, sizeof(float) * E * d, st) == cudaSuccess &&
+              cudaMemsetAsync(dW1, 0, sizeof(float) * E * 2 * c->f * d, st) == cudaSuccess &&
+              cudaMemsetAsync(dW2, 0, sizeof(float) * E * d * c->f, st) == cudaSuccess;
+    if (sh)
+      ok = ok && cudaMemsetAsync(dWs1, 0, sizeof(float) * 2 * c->f_shared * d, st) == cudaSuccess &&
+           cudaMemsetAsync(dWs2, 0, sizeof(float) * d * c->f_shared, st) == cudaSuccess;
+    if (gt) ok = ok && cudaMemsetAsync(dw_sg, 0, sizeof(float) * d, st) == cudaSuccess;
+    return ok ? MOE_OK : fail(MOE_ERR_CUDA, "cudaMemsetAsync failed");
+  }
+  Carve cv(ws);
+  BwdWs w = carve_bwd(cv, c);
+  // 1. combine backward
+  MOE_TRY(launch_combine_bwd(c->dtype, dy, s->y_perm, s->gate, s->slot_of_pair,
+                             sh ? s->s_out : nullptr, gt ? s->s_coef : nullptr, w.dy_perm, w.dgate,
+                             w.dshared, w.dcoef, T, d, k, st));
+  // 2. routed experts (dx_perm overwrites dy_perm once it is no longer read)
+  MOE_TRY(ffn_bwd_impl(c, E, s->offsets, Nrows(c), c->f, s->x_perm, W1, W2, s->act, s->h,
+                       w.dy_perm, w.dH1, w.dy_perm, dW1, dW2, st));
+  // 3. shared expert (one group of all T tokens)
+  if (sh)
+    MOE_TRY(ffn_bwd_impl(c, 1, nullptr, T, c->f_shared, x, Ws1, Ws2, s->s_act, s->s_h, w.dshared,
+                         w.dH1, w.dx_shared, dWs1, dWs2, st));
+  // 4. router: dlogits (+ shared gate dz in column E)
+  const int ldx = ext_cols(c);
+  MOE_TRY(launch_router_bwd(c->dtype, s->logits, s->idx, s->gate, w.dgate, gt ? w.dcoef : nullptr,
+                            gt ? s->s_coef : nullptr, w.dl_ext, w.dz, T, E, k, ldx, c->score_fn,
+                            c->renorm, st));
+  // 5. dx_router = dlogits . W_r
+  GemmDesc rd = desc0();
+  rd.name = "gemm_router_dgrad";
+  rd.sched = RAGGED_M;
+  rd.epi = EPI_STORE;
+  rd.G = 1;
+  rd.M = T;
+  rd.N = d;
+  rd.K = E;
+  rd.A = opnd(w.dl_ext, T, ldx, false);
+  rd.B = opnd(W_r, E, d, true);
+  rd.out = w.dx_router;
+  rd.ldo = d;
+  MOE_TRY(gemm(c, rd, st));
+  // 6. [dW_r; dw_sg] = [dlogits | dz]^T . x, split over tokens, then a fixed-order sum
+  const int mr = E + (gt ? 1 : 0);
+  const int S_ = router_splits(c);
+  GemmDesc rw = desc0();
+  rw.name = "gemm_router_wgrad";
+  rw.sched = RAGGED_K;
+  rw.epi = EPI_F32;
+  rw.G = S_;
+  rw.M = mr;
+  rw.N = d;
+  rw.K = T;
+  rw.A = opnd(w.dl_ext, T, ldx, true);
+  rw.B = opnd(x, T, d, true);
+  rw.out = w.part;
+  rw.ldo = d;
+  rw.out_group_stride = static_cast<int64_t>(mr) * d;
+  MOE_TRY(gemm(c, rw, st));
+  MOE_TRY(launch_split_reduce(w.part, S_, mr, d, dW_r, E, gt ? dw_sg : nullptr, st));
+  // 7. dx = sum_j dx_perm[slot(t,j)] + dx_shared + dx_router + dz * w_sg
+  return launch_gather_sum(c->dtype, w.dy_perm, s->slot_of_pair, sh ? w.dx_shared : nullptr,
+                           w.dx_router, gt ? w.dz : nullptr, gt ? w_sg : nullptr, dx, T, d, k, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,569 @@
+// Grouped GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), bf16 in, fp32
+// accumulate.  One kernel template serves every matrix product of the layer:
+//   fc1 + SwiGLU, fc2 (ragged rows per expert), their data gradients (ragged rows, weights read
+//   MN-major), their weight gradients (ragged reduction per expert), the router and the
+//   shared expert (one group).
+// "Megatron-Bridge 深度剖析", §计算融合 / Grouped GEMM: every expert's GEMM in one launch over
+// ragged per-expert token counts.  Here the ragged extents are read on the device from the
+// routing offsets, so the host never synchronises on them.
+//
+// CTA organisation (persistent, one CTA per SM, 6 warps):
+//   warp 0     TMA producer: loads A/B k-blocks into a STAGES-deep shared-memory ring
+//   warp 1     MMA issuer: owns TMEM (2 accumulators of BN fp32 columns), issues
+//              tcgen05.mma (M=128, N=BN, K=16) per k-step, commits to the ring's empty barriers
+//   warps 2-5  epilogue: TMEM -> registers (tcgen05.ld) -> fused epilogue -> global stores,
+//              overlapped with the next tile's MMAs through the second accumulator
+// Tiles are BM=128 rows x BN columns x BK=64; a CTA walks tiles blockIdx.x, +gridDim.x, ...
+#include <cuda.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int MAXG = 256;             // groups per launch (experts, or K splits)
+constexpr int NUM_THREADS = 192;
+constexpr int A_STAGE = BM * BK * 2;  // 16 KB
+
+template <int BN> struct TileCfg {
+  static constexpr int B_STAGE = BN * BK * 2;
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int RING = STAGES * (A_STAGE + B_STAGE);
+  static constexpr int AUX = 4096;   // barriers, TMEM address, abort flag, group tables
+  static constexpr int SMEM = RING + AUX + 1024;
+  static constexpr int TMEM_COLS = 2 * BN;
+};
+
+struct KArgs {
+  int G;
+  const int32_t* offsets;
+  int M, N, K;
+  int64_t b_group_rows, b_up_rows;
+  int f;
+  void* out;
+  int64_t ldo, out_group_stride;
+  void* out2;
+  int64_t ldo2;
+  const void* aux;
+  int64_t ld_aux;
+  const float* bias;
+  int* err;
+};
+
+struct TileInfo {
+  int g, m0, m_end, n0, k0, k_end, kblocks;
+};
+
+__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + __expf(-a)); }
+
+template <int BN, int SCHED, int EPI>
+struct Sched {
+  // Number of output column tiles.
+  __device__ static int n_tiles(const KArgs& p) {
+    if (EPI == EPI_SWIGLU_FWD) return (p.f + BN / 2 - 1) / (BN / 2);
+    return (p.N + BN - 1) / BN;
+  }
+  __device__ static int total(const KArgs& p, const int* s_pre) {
+    if (SCHED == RAGGED_M) return s_pre[p.G] * n_tiles(p);
+    return p.G * ((p.M + BM - 1) / BM) * n_tiles(p);
+  }
+  __device__ static TileInfo decode(const KArgs& p, const int* s_off, const int* s_pre, int tile) {
+    TileInfo ti;
+    const int nt_count = n_tiles(p);
+    if (SCHED == RAGGED_M) {
+      const int mt = tile / nt_count, nt = tile - mt * nt_count;
+      int lo = 0, hi = p.G;   // largest g with s_pre[g] <= mt
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_pre[mid] <= mt) lo = mid; else hi = mid;
+      }
+      ti.g = lo;
+      ti.m0 = s_off[lo] + (mt - s_pre[lo]) * BM;
+      ti.m_end = s_off[lo + 1];
+      ti.n0 = nt * (EPI == EPI_SWIGLU_FWD ? BN / 2 : BN);
+      ti.k0 = 0;
+      ti.k_end = p.K;
+    } else {
+      const int mtc = (p.M + BM - 1) / BM;
+      const int per = mtc * nt_count;
+      ti.g = tile / per;
+      const int r = tile - ti.g * per;
+      const int mt = r / nt_count, nt = r - mt * nt_count;
+      ti.m0 = mt * BM;
+      ti.m_end = p.M;
+      ti.n0 = nt * BN;
+      ti.k0 = s_off[ti.g];
+      ti.k_end = s_off[ti.g + 1];
+    }
+    ti.kblocks = (ti.k_end - ti.k0 + BK - 1) / BK;
+    return ti;
+  }
+};
+
+template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const KArgs p) {
+  using C = TileCfg<BN>;
+  using S = Sched<BN, SCHED, EPI>;
+  constexpr int STAGES = C::STAGES;
+  constexpr uint32_t STAGE_TX = A_STAGE + C::B_STAGE;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* s_off = reinterpret_cast<int*>(tmem_holder + 4);
+  int* s_pre = s_off + (MAXG + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&tfull[i], 1);
+      ptx::mbar_init(&tempty[i], 4);
+    }
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  // Group table: row (RAGGED_M) or reduction (RAGGED_K) offsets, and for RAGGED_M the prefix
+  // of per-group row-tile counts.
+  for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
+    int v;
+    if (p.offsets) v = p.offsets[i];
+    else v = static_cast<int>((static_cast<int64_t>(SCHED == RAGGED_M ? p.M : p.K) * i) / p.G);
+    s_off[i] = v;
+  }
+  __syncthreads();
+  // The offsets must be non-decreasing and stay inside the operands (rows of A for RAGGED_M,
+  // the reduction length for RAGGED_K); otherwise nothing is computed and the error recorded.
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) {
+    const int cap = SCHED == RAGGED_M ? p.M : p.K;
+    int bad = (s_off[0] < 0 || s_off[p.G] > cap) ? 1 : 0;
+    for (int i = 0; i < p.G && !bad; ++i) bad = s_off[i + 1] < s_off[i];
+    s_bad = bad;
+    if (bad) record_error(p.err, DEVERR_BAD_OFFSETS);
+  }
+  __syncthreads();
+  if (s_bad) return;
+  if (SCHED == RAGGED_M && warp == 0) {
+    // s_pre[g] = sum_{g' < g} ceil(rows_g' / BM): lane L scans groups [L*per, (L+1)*per)
+    const int per = (p.G + 31) / 32;
+    const int lo = min(p.G, lane * per), hi = min(p.G, lo + per);
+    int local = 0;
+    for (int g = lo; g < hi; ++g) local += (s_off[g + 1] - s_off[g] + BM - 1) / BM;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int g = lo; g < hi; ++g) {
+      s_pre[g] = run;
+      run += (s_off[g + 1] - s_off[g] + BM - 1) / BM;
+    }
+    if (lane == 31) s_pre[p.G] = incl;
+  }
+  __syncthreads();
+
+  const int total = S::total(p, s_pre);
+  if (static_cast<int>(blockIdx.x) >= total) return;   // nothing for this CTA (uniform)
+
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_holder, C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int armed[STAGES];
+      for (int i = 0; i < STAGES; ++i) armed[i] = -1;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const TileInfo ti = S::decode(p, s_off, s_pre, tile);
+        for (int kb = 0; kb < ti.kblocks; ++kb) {
+          if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(&full[stage], STAGE_TX);
+          armed[stage] = static_cast<int>(phase);
+          uint8_t* a_dst = sA + stage * A_STAGE;
+          uint8_t* b_dst = sB + stage * C::B_STAGE;
+          const int kk = ti.k0 + kb * BK;
+          if (!A_MN) {
+            ptx::tma_load_2d(a_dst, &tmA, &full[stage], kk, ti.m0);
+          } else {
+#pragma unroll
+            for (int c = 0; c < BM / 64; ++c)
+              ptx::tma_load_2d(a_dst + c * (BK * 128), &tmA, &full[stage], ti.m0 + 64 * c, kk);
+          }
+          if (!B_MN) {
+            const int brow = static_cast<int>(ti.g * p.b_group_rows) + ti.n0;
+            if (EPI == EPI_SWIGLU_FWD) {
+              ptx::tma_load_2d(b_dst, &tmB, &full[stage], kk, brow);
+              ptx::tma_load_2d(b_dst + (BN / 2) * 128, &tmB, &full[stage], kk,
+                               brow + static_cast<int>(p.b_up_rows));
+            } else {
+              ptx::tma_load_2d(b_dst, &tmB, &full[stage], kk, brow);
+            }
+          } else {
+            const int krow = (SCHED == RAGGED_M) ? static_cast<int>(ti.g * p.b_group_rows) + kk : kk;
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)
+              ptx::tma_load_2d(b_dst + c * (BK * 128), &tmB, &full[stage], ti.n0 + 64 * c, krow);
+          }
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // Unwinding: let every copy this thread issued land before the CTA exits.
+        for (int i = 0; i < STAGES; ++i) {
+          if (armed[i] < 0) continue;
+          const uint64_t t0 = ptx::globaltimer();
+          while (!ptx::mbar_try_wait(&full[i], static_cast<uint32_t>(armed[i])) &&
+                 ptx::globaltimer() - t0 < 100000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const TileInfo ti = S::decode(p, s_off, s_pre, tile);
+      if (ti.kblocks == 0) continue;
+      if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      for (int kb = 0; kb < ti.kblocks; ++kb) {
+        if (!ptx::mbar_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
+        uint8_t* a_src = sA + stage * A_STAGE;
+        uint8_t* b_src = sB + stage * C::B_STAGE;
+        if (SCHED == RAGGED_K && kb == ti.kblocks - 1) {
+          // Rows of this k-block past the group's end belong to the next group: zero them in
+          // the A tile (MN-major: row r of chunk c is 128 contiguous bytes).
+          const int valid = ti.k_end - (ti.k0 + kb * BK);
+          if (valid < BK) {
+            const int nbytes = (BK - valid) * 128;
+            for (int c = 0; c < BM / 64; ++c) {
+              uint8_t* base = a_src + c * (BK * 128) + valid * 128;
+              for (int o = lane * 16; o < nbytes; o += 32 * 16)
+                *reinterpret_cast<uint4*>(base + o) = make_uint4(0, 0, 0, 0);
+            }
+            ptx::fence_proxy_async_smem();
+          }
+          __syncwarp();
+        }
+        ptx::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a_addr = ptx::smem_u32(a_src), b_addr = ptx::smem_u32(b_src);
+#pragma unroll
+          for (int k16 = 0; k16 < BK / 16; ++k16) {
+            const uint64_t ad = A_MN ? ptx::smem_desc_sw128(a_addr + k16 * 2048, BK * 128, 1024)
+                                     : ptx::smem_desc_sw128(a_addr + k16 * 32, 16, 1024);
+            const uint64_t bd = B_MN ? ptx::smem_desc_sw128(b_addr + k16 * 2048, BK * 128, 1024)
+                                     : ptx::smem_desc_sw128(b_addr + k16 * 32, 16, 1024);
+            ptx::umma_bf16(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
+          }
+          ptx::umma_commit(&empty[stage]);   // frees the smem stage when these MMAs finish
+        }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      if (lane == 0) ptx::umma_commit(&tfull[acc]);   // accumulator ready for the epilogue
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;          // TMEM lane quadrant this warp may access
+    const int r = q * 32 + lane;     // row inside the tile
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const TileInfo ti = S::decode(p, s_off, s_pre, tile);
+      const int row = ti.m0 + r;
+      const bool valid = row < ti.m_end;
+      if (ti.kblocks == 0) {
+        // Empty reduction (an expert with no rows): its weight-gradient block is zero.
+        if (EPI == EPI_F32 && valid) {
+          float* o = static_cast<float*>(p.out) + ti.g * p.out_group_stride + row * p.ldo;
+          for (int c = ti.n0; c < min(p.N, ti.n0 + BN); c += 4)
+            *reinterpret_cast<float4*>(o + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        continue;
+      }
+      if (!ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err)) break;
+      ptx::tc_fence_after();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * BN);
+
+      if (EPI == EPI_SWIGLU_FWD) {
+        bf16* hrow = static_cast<bf16*>(p.out) + row * p.ldo;
+        bf16* arow = static_cast<bf16*>(p.out2) + row * p.ldo2;
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          const int col = ti.n0 + c;
+          if (col >= p.f) break;
+          uint32_t ga[32], up[32];
+          ptx::tmem_ld32(t_row + c, ga);
+          ptx::tmem_ld32(t_row + BN / 2 + c, up);
+          ptx::tmem_ld_wait();
+          if (valid) {
+            const int ncol = min(32, p.f - col);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              if (v * 8 >= ncol) break;
+              float hv[8], av[8], uv[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                av[i] = __uint_as_float(ga[v * 8 + i]);
+                uv[i] = __uint_as_float(up[v * 8 + i]);
+                hv[i] = silu_f(av[i]) * uv[i];
+              }
+              st16(hrow + col + v * 8, pack16(hv, static_cast<const bf16*>(nullptr)));
+              if (p.out2) {
+                st16(arow + col + v * 8, pack16(av, static_cast<const bf16*>(nullptr)));
+                st16(arow + p.f + col + v * 8, pack16(uv, static_cast<const bf16*>(nullptr)));
+              }
+            }
+          }
+        }
+      } else if (EPI == EPI_SWIGLU_BWD) {
+        const bf16* act = static_cast<const bf16*>(p.aux) + row * p.ld_aux;
+        bf16* drow = static_cast<bf16*>(p.out) + row * p.ldo;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          const int col = ti.n0 + c;
+          if (col >= p.f) break;
+          uint32_t dh[32];
+          ptx::tmem_ld32(t_row + c, dh);
+          ptx::tmem_ld_wait();
+          if (valid) {
+            const int ncol = min(32, p.f - col);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              if (v * 8 >= ncol) break;
+              float av[8], uv[8], da[8], du[8];
+              unpack16(ld16(act + col + v * 8), av, static_cast<const bf16*>(nullptr));
+              unpack16(ld16(act + p.f + col + v * 8), uv, static_cast<const bf16*>(nullptr));
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float g = __uint_as_float(dh[v * 8 + i]);
+                const float s = 1.0f / (1.0f + __expf(-av[i]));
+                const float silu = av[i] * s;
+                da[i] = g * uv[i] * (s + av[i] * s * (1.0f - s));
+                du[i] = g * silu;
+              }
+              st16(drow + col + v * 8, pack16(da, static_cast<const bf16*>(nullptr)));
+              st16(drow + p.f + col + v * 8, pack16(du, static_cast<const bf16*>(nullptr)));
+            }
+          }
+        }
+      } else {
+        // EPI_STORE (bf16) or EPI_F32 (+bias)
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          const int col = ti.n0 + c;
+          if (col >= p.N) break;
+          uint32_t v32[32];
+          ptx::tmem_ld32(t_row + c, v32);
+          ptx::tmem_ld_wait();
+          if (valid) {
+            const int ncol = min(32, p.N - col);
+            if (EPI == EPI_STORE) {
+              bf16* o = static_cast<bf16*>(p.out) + row * p.ldo + col;
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                if (v * 8 >= ncol) break;
+                float fv[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) fv[i] = __uint_as_float(v32[v * 8 + i]);
+                st16(o + v * 8, pack16(fv, static_cast<const bf16*>(nullptr)));
+              }
+            } else {
+              float* o = static_cast<float*>(p.out) + ti.g * p.out_group_stride + row * p.ldo + col;
+              if ((p.ldo & 3) != 0 || (ncol & 3) != 0) {
+                // unaligned rows (e.g. router logits with E % 4 != 0): scalar stores
+                for (int i = 0; i < ncol; ++i)
+                  o[i] = __uint_as_float(v32[i]) + (p.bias ? p.bias[col + i] : 0.f);
+                continue;
+              }
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                if (v * 4 >= ncol) break;
+                float4 fv = make_float4(__uint_as_float(v32[v * 4]), __uint_as_float(v32[v * 4 + 1]),
+                                        __uint_as_float(v32[v * 4 + 2]),
+                                        __uint_as_float(v32[v * 4 + 3]));
+                if (p.bias) {
+                  fv.x += p.bias[col + v * 4];
+                  fv.y += p.bias[col + v * 4 + 1];
+                  fv.z += p.bias[col + v * 4 + 2];
+                  fv.w += p.bias[col + v * 4 + 3];
+                }
+                *reinterpret_cast<float4*>(o + v * 4) = fv;
+              }
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// A 2-D bf16 tensor map over op (rows x cols, row pitch ld), box = 64 columns x box_rows,
+// 128-byte swizzle; out-of-bounds elements read as zero.
+int make_map(CUtensorMap* m, const Operand& op, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return MOE_ERR_CUDA;
+  }
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(op.cols), static_cast<cuuint64_t>(op.rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(op.ld) * 2};
+  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(op.base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (%d): rows=%lld cols=%lld ld=%lld box_rows=%d", (int)r,
+              (long long)op.rows, (long long)op.cols, (long long)op.ld, box_rows);
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI>
+int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
+  const char* name = g.name ? g.name : kind;
+  using C = TileCfg<BN>;
+  auto kern = tc_gemm_kernel<BN, A_MN, B_MN, SCHED, EPI>;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  });
+  if (attr_err != cudaSuccess) {
+    set_error("cudaFuncSetAttribute(%s): %s", name, cudaGetErrorString(attr_err));
+    return MOE_ERR_CUDA;
+  }
+  CUtensorMap ma, mb;
+  MOE_TRY(make_map(&ma, g.A, A_MN ? BK : BM));
+  MOE_TRY(make_map(&mb, g.B, B_MN ? BK : (EPI == EPI_SWIGLU_FWD ? BN / 2 : BN)));
+  KArgs a;
+  a.G = g.G;
+  a.offsets = g.offsets;
+  a.M = g.M;
+  a.N = g.N;
+  a.K = g.K;
+  a.b_group_rows = g.b_group_rows;
+  a.b_up_rows = g.b_up_rows;
+  a.f = g.f;
+  a.out = g.out;
+  a.ldo = g.ldo;
+  a.out_group_stride = g.out_group_stride;
+  a.out2 = g.out2;
+  a.ldo2 = g.ldo2;
+  a.aux = g.aux;
+  a.ld_aux = g.ld_aux;
+  a.bias = g.bias;
+  a.err = device_error_word();
+  return launch(name, kern, dim3(num_sms()), dim3(NUM_THREADS), C::SMEM, st, ma, mb, a);
+}
+
+}  // namespace
+
+int gemm_tc(const GemmDesc& g, cudaStream_t st) {
+  if (g.G < 1 || g.G > MAXG) {
+    set_error("gemm_tc: group count %d outside [1, %d]", g.G, MAXG);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (g.sched == RAGGED_M && !g.A.mn_major) {
+    if (g.epi == EPI_SWIGLU_FWD && !g.B.mn_major)
+      return run<256, false, false, RAGGED_M, EPI_SWIGLU_FWD>(g, "gemm_fc1_swiglu", st);
+    if (g.epi == EPI_SWIGLU_BWD && g.B.mn_major)
+      return run<256, false, true, RAGGED_M, EPI_SWIGLU_BWD>(g, "gemm_fc2_dgrad_swiglu_bwd", st);
+    if (g.epi == EPI_STORE && !g.B.mn_major)
+      return run<256, false, false, RAGGED_M, EPI_STORE>(g, "gemm_fc2", st);
+    if (g.epi == EPI_STORE && g.B.mn_major)
+      return run<256, false, true, RAGGED_M, EPI_STORE>(g, "gemm_dgrad", st);
+    if (g.epi == EPI_F32 && !g.B.mn_major) {
+      if (g.N <= 128) return run<128, false, false, RAGGED_M, EPI_F32>(g, "gemm_router", st);
+      return run<256, false, false, RAGGED_M, EPI_F32>(g, "gemm_router", st);
+    }
+  }
+  if (g.sched == RAGGED_K && g.A.mn_major && g.B.mn_major && g.epi == EPI_F32)
+    return run<256, true, true, RAGGED_K, EPI_F32>(g, "gemm_wgrad", st);
+  set_error("gemm_tc: unsupported combination sched=%d epi=%d a_mn=%d b_mn=%d", g.sched, g.epi,
+            (int)g.A.mn_major, (int)g.B.mn_major);
+  return MOE_ERR_UNSUPPORTED;
+}
+
+}  // namespace moe

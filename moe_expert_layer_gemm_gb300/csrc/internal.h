@@ -1,0 +1,127 @@
+// Host-side interfaces between the translation units of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <utility>
+
+#include "moe_gb300.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ launch bookkeeping
+// Every kernel of the library is launched through launch(): it counts the launch and,
+// when tracing is on, brackets it with CUDA events on its stream.
+void trace_before(const char* name, cudaStream_t s);
+void trace_after(const char* name, cudaStream_t s);
+void count_launch();
+void set_error(const char* fmt, ...);
+int* device_error_word();   // per-device error word (nullptr if CUDA is unusable)
+int num_sms();
+
+template <typename... KArgs, typename... Args>
+int launch(const char* name, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+           cudaStream_t st, Args&&... args) {
+  if (grid.x == 0 || grid.y == 0 || grid.z == 0) return MOE_OK;
+  trace_before(name, st);
+  kern<<<grid, block, smem, st>>>(std::forward<Args>(args)...);
+  cudaError_t e = cudaGetLastError();
+  trace_after(name, st);
+  count_launch();
+  if (e != cudaSuccess) {
+    set_error("launch of %s failed: %s", name, cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+#define MOE_TRY(x)                 \
+  do {                             \
+    int _st = (x);                 \
+    if (_st != MOE_OK) return _st; \
+  } while (0)
+
+// ------------------------------------------------------------------ routing (route.cu)
+constexpr int ROUTE_TOK_PER_BLOCK = 256;
+inline int route_blocks(int T) { return (T + ROUTE_TOK_PER_BLOCK - 1) / ROUTE_TOK_PER_BLOCK; }
+
+int launch_topk(const float* logits, int T, int E, int k, int score_fn, int renorm, int32_t* idx,
+                float* gate, int32_t* hist, cudaStream_t st);
+int launch_scan(const int32_t* hist, int E, int nblk, int32_t* base, int32_t* counts,
+                int32_t* offsets, cudaStream_t st);
+int launch_slots(const int32_t* idx, int T, int k, int E, const int32_t* base,
+                 int32_t* slot_of_pair, int32_t* token_of_slot, cudaStream_t st);
+
+// ------------------------------------------------------------------ row kernels (rowops.cu)
+int launch_permute(int dtype, const void* x, const int32_t* slot_of_pair, void* x_perm, int T,
+                   int d, int k, cudaStream_t st);
+int launch_combine(int dtype, const void* y_perm, const float* gate, const int32_t* slot_of_pair,
+                   const void* shared_out, const float* shared_coef, void* y, int T, int d, int k,
+                   cudaStream_t st);
+int launch_combine_bwd(int dtype, const void* dy, const void* y_perm, const float* gate,
+                       const int32_t* slot_of_pair, const void* shared_out,
+                       const float* shared_coef, void* dy_perm, float* dgate, void* dshared,
+                       float* dcoef, int T, int d, int k, cudaStream_t st);
+int launch_gather_sum(int dtype, const void* dx_perm, const int32_t* slot_of_pair,
+                      const void* dx_shared, const void* dx_router, const float* dz,
+                      const void* w_sg, void* dx, int T, int d, int k, cudaStream_t st);
+int launch_shared_gate(int dtype, const void* x, const void* w_sg, float* coef, int T, int d,
+                       cudaStream_t st);
+int launch_router_bwd(int dtype, const float* logits, const int32_t* idx, const float* gate,
+                      const float* dgate, const float* dcoef, const float* coef, void* dl_ext,
+                      float* dz, int T, int E, int k, int ld_ext, int score_fn, int renorm,
+                      cudaStream_t st);
+int launch_split_reduce(const float* part, int S, int rows, int cols, float* out_main,
+                        int main_rows, float* out_extra, cudaStream_t st);
+
+// ------------------------------------------------------------------ grouped GEMMs
+// Scheduling of a grouped GEMM C_g = A_g . B_g^T over groups g < G.
+//   RAGGED_M: rows of group g are [off[g], off[g+1]) of A and of C (offsets on the device; a
+//             null offsets pointer means one group of rows [0, M)).  B_g is the g-th block of
+//             b_group_rows rows of B.  K fixed.
+//   RAGGED_K: C_g is a fixed M x N block (stored at out + g*out_group_stride); the reduction
+//             runs over rows [off[g], off[g+1]) of A and B (null offsets: K split evenly
+//             into G chunks).
+enum Sched { RAGGED_M = 0, RAGGED_K = 1 };
+// Epilogues.
+enum Epi {
+  EPI_STORE = 0,        // C in the activation dtype (bf16 / fp32)
+  EPI_F32 = 1,          // C in fp32 (+ bias[n] if bias != null)
+  EPI_SWIGLU_FWD = 2,   // acc = [gate | up] columns: h = SiLU(a)*u -> out, [a | u] -> out2
+  EPI_SWIGLU_BWD = 3,   // acc = dh: reads [a | u] from aux, writes [da | du] -> out
+};
+
+// One operand: element (row, col) at base[row*ld + col]; `rows`/`cols` are the extents of
+// the whole array as seen by this GEMM.  A K-major operand has the reduction index as col;
+// an MN-major one has it as row.
+struct Operand {
+  const void* base;
+  int64_t rows, cols, ld;
+  bool mn_major;
+};
+
+struct GemmDesc {
+  const char* name;        // trace name (kernel kind) of this product
+  int sched;
+  int epi;
+  int G;
+  const int32_t* offsets;
+  int M, N, K;             // see Sched
+  Operand A, B;
+  int64_t b_group_rows;    // RAGGED_M: row offset of group g inside B
+  int64_t b_up_rows;       // EPI_SWIGLU_FWD: row offset of the up half inside a group
+  int f;                   // SwiGLU width (EPI_SWIGLU_*)
+  void* out;
+  int64_t ldo, out_group_stride;
+  void* out2;
+  int64_t ldo2;
+  const void* aux;
+  int64_t ld_aux;
+  const float* bias;
+};
+
+int gemm_tc(const GemmDesc& g, cudaStream_t st);     // bf16 tcgen05 path (gemm_tc.cu)
+int gemm_simt(const GemmDesc& g, cudaStream_t st);   // fp32 CUDA-core path (gemm_simt.cu)
+
+}  // namespace moe

@@ -1,0 +1,79 @@
+"""The C-ABI library without a GPU: it loads, exports every function include/moe_gb300.h
+declares, and rejects bad arguments on the host with the documented status codes before any
+CUDA work is enqueued."""
+import ctypes
+import os
+
+import pytest
+
+import moe_expert_layer_gemm_gb300 as moe
+
+L = None
+
+
+def setup_module():
+    global L
+    if not os.path.exists(moe._lib.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    L = moe.lib()
+
+
+def test_exports_every_declared_function():
+    names = moe.header_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(L, n), n
+    assert L.moe_version() >= 100
+
+
+def cfg(**kw):
+    base = dict(T=256, d=128, E=8, k=2, f=256, f_shared=0, score_fn=0, renorm=1, shared_gate=0,
+                dtype=0)
+    base.update(kw)
+    return moe.MoeCfg(*[base[n] for n, _ in moe.MoeCfg._fields_])
+
+
+P = ctypes.c_void_p(1 << 20)     # a fake, aligned, never-dereferenced address
+MIS = ctypes.c_void_p((1 << 20) + 8)
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(k=9), -2),                               # k above the maximum
+    (dict(k=3, E=2), -1),                          # k > E
+    (dict(E=300), -2),                             # too many experts
+    (dict(d=100), -2),                             # d not a multiple of 8 (bf16 rows)
+    (dict(T=-1), -1),
+    (dict(score_fn=3), -1),
+    (dict(shared_gate=1), -1),                     # gate without a shared expert
+    (dict(dtype=7), -1),
+])
+def test_bad_config_is_rejected(bad, code):
+    c = cfg(**bad)
+    assert L.moe_permute(ctypes.byref(c), P, P, P, None) == code
+    assert L.moe_workspace_bytes(ctypes.byref(c), 4) == 0
+    assert L.moe_last_error()
+
+
+def test_null_and_misaligned_pointers():
+    c = cfg()
+    assert L.moe_permute(ctypes.byref(c), None, P, P, None) == -1
+    assert b"x" in L.moe_last_error()
+    assert L.moe_permute(ctypes.byref(c), MIS, P, P, None) == -4
+    assert L.moe_unpermute_combine(ctypes.byref(c), P, P, P, None, None, None, None) == -1
+
+
+def test_workspace_too_small():
+    c = cfg()
+    need = L.moe_workspace_bytes(ctypes.byref(c), moe.WS_ROUTE)
+    assert need > 0
+    rc = L.moe_route_topk(ctypes.byref(c), P, P, None, None, None, P, P, P, P, P, P, P, need - 256,
+                          None)
+    assert rc == -3
+
+
+def test_workspace_sizes_grow_with_the_layer():
+    small = cfg(T=256)
+    big = cfg(T=4096)
+    for w in (moe.WS_ROUTE, moe.WS_LAYER_BWD, moe.WS_FFN_BWD):
+        assert L.moe_workspace_bytes(ctypes.byref(big), w) > L.moe_workspace_bytes(ctypes.byref(small), w)

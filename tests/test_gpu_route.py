@@ -1,0 +1,76 @@
+"""Routing stage (moe_route_topk with given fp32 logits) against the oracle: expert indices,
+counts, offsets and both permutation maps bit-for-bit; gates within fp32 rounding.
+
+Includes the routing/permute stress workload at full size (T=65536, E=128, top-8 sigmoid) with
+its degenerate cases: every token on the same 8 experts, 32 experts that receive nothing, and
+integer logits with massive exact ties.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_expert_layer_gemm_gb300 as moe
+import moe_inputs
+import oracle.moe_oracle as O
+
+from .helpers import np64
+
+pytestmark = pytest.mark.gpu
+
+
+def route_gpu(T, E, k, score_fn, renorm, logits):
+    cfg = moe.make_cfg(T, 8, E, k, 8, score_fn=score_fn, renorm=renorm)
+    dev = "cuda"
+    i32 = torch.int32
+    out = dict(idx=torch.full((T, k), -7, dtype=i32, device=dev),
+               gate=torch.full((T, k), float("nan"), device=dev),
+               counts=torch.full((E,), -7, dtype=i32, device=dev),
+               offsets=torch.full((E + 1,), -7, dtype=i32, device=dev),
+               slot_of_pair=torch.full((T, k), -7, dtype=i32, device=dev),
+               token_of_slot=torch.full((max(T * k, 1),), -7, dtype=i32, device=dev))
+    ws = moe.workspace(cfg, moe.WS_ROUTE, dev)
+    moe.moe_route_topk(cfg, None, None, None, logits, None, out["idx"], out["gate"], out["counts"],
+                       out["offsets"], out["slot_of_pair"], out["token_of_slot"], ws)
+    torch.cuda.synchronize()
+    moe.check_device_error()
+    return {n: t.cpu().numpy() for n, t in out.items()}
+
+
+def check_route(T, E, k, score_fn, renorm, logits):
+    g = route_gpu(T, E, k, score_fn, renorm, logits.cuda())
+    lg = logits.cpu().numpy()
+    r = O.route(lg, k, E, score_fn, renorm)
+    assert (g["idx"] == r["idx"]).all(), "idx"
+    assert (g["counts"] == r["counts"]).all(), "counts"
+    assert (g["offsets"] == r["offsets"]).all(), "offsets"
+    assert (g["slot_of_pair"] == r["slot_of_pair"]).all(), "slot_of_pair"
+    assert (g["token_of_slot"][: T * k] == r["token_of_slot"]).all(), "token_of_slot"
+    err = np.abs(g["gate"] - r["gate"]).max() / np.abs(r["gate"]).max()
+    assert err < 2e-6, f"gate error {err}"
+    return g
+
+
+@pytest.mark.parametrize("E,k", [(8, 2), (5, 3), (1, 1), (32, 6), (128, 8), (256, 8), (256, 1),
+                                 (64, 8)])
+@pytest.mark.parametrize("score_fn,renorm", [(0, 1), (0, 0), (1, 1), (1, 0)])
+def test_route_random_logits(E, k, score_fn, renorm):
+    T = 777
+    lg = torch.randn(T, E, generator=torch.Generator().manual_seed(E * 31 + k)) * 2.0
+    check_route(T, E, k, score_fn, renorm, lg)
+
+
+@pytest.mark.parametrize("case", moe_inputs.STRESS_CASES)
+def test_route_stress_full_size(case):
+    lc = moe_inputs.ROUTE_STRESS
+    lg = moe_inputs.make_stress_logits(case, lc.T, lc.E, seed=0)
+    g = check_route(lc.T, lc.E, lc.k, lc.score_fn, lc.renorm, lg)
+    if case == "all_to_8":
+        assert (g["counts"][:8] == lc.T).all() and (g["counts"][8:] == 0).all()
+    if case == "32_empty":
+        assert (g["counts"][lc.E - 32:] == 0).all()
+
+
+@pytest.mark.parametrize("T", [1, 7, 255, 256, 257, 4097])
+def test_route_token_counts_around_block_edges(T):
+    lg = torch.randint(0, 3, (T, 16), generator=torch.Generator().manual_seed(T)).float()
+    check_route(T, 16, 4, 1, 1, lg)

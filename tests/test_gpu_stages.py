@@ -1,0 +1,112 @@
+"""Stage entry points (moe_permute, moe_grouped_swiglu_fwd/bwd, moe_unpermute_combine(_bwd))
+against the oracle's definitions on the same inputs."""
+import numpy as np
+import pytest
+import torch
+
+import moe_expert_layer_gemm_gb300 as moe
+import oracle.moe_oracle as O
+
+from .helpers import assert_close, np64
+
+pytestmark = pytest.mark.gpu
+
+
+def routed(T, E, k, seed=0):
+    g = torch.Generator().manual_seed(seed)
+    lg = torch.randn(T, E, generator=g)
+    r = O.route(lg.numpy(), k, E, O.SOFTMAX, 1)
+    return r
+
+
+@pytest.mark.parametrize("dtype", [moe.DTYPE_BF16, moe.DTYPE_F32])
+def test_permute_is_exact_copy(dtype):
+    T, d, E, k = 1000, 264, 16, 4
+    r = routed(T, E, k)
+    cfg = moe.make_cfg(T, d, E, k, 64, dtype=dtype)
+    tdt = torch.bfloat16 if dtype == moe.DTYPE_BF16 else torch.float32
+    x = torch.randn(T, d).to(tdt).cuda()
+    xp = torch.full((T * k, d), float("nan"), dtype=tdt, device="cuda")
+    moe.moe_permute(cfg, x, torch.from_numpy(r["slot_of_pair"]).cuda(), xp)
+    torch.cuda.synchronize()
+    ref = x.cpu()[torch.from_numpy(r["token_of_slot"]).long()]
+    assert torch.equal(xp.cpu(), ref)
+
+
+def test_grouped_swiglu_fwd_bwd_stage():
+    T, d, E, k, f = 600, 256, 8, 2, 136
+    r = routed(T, E, k, 3)
+    N = T * k
+    cfg = moe.make_cfg(T, d, E, k, f)
+    g = torch.Generator().manual_seed(5)
+    xp = torch.randn(N, d, generator=g).bfloat16()
+    W1 = (torch.randn(E, 2 * f, d, generator=g) * 0.05).bfloat16()
+    W2 = (torch.randn(E, d, f, generator=g) * 0.05).bfloat16()
+    dyp = torch.randn(N, d, generator=g).bfloat16()
+    off = torch.from_numpy(r["offsets"])
+    c = {n: t.cuda() for n, t in dict(xp=xp, W1=W1, W2=W2, dyp=dyp, off=off).items()}
+    h = torch.empty(N, f, dtype=torch.bfloat16, device="cuda")
+    act = torch.empty(N, 2 * f, dtype=torch.bfloat16, device="cuda")
+    yp = torch.empty(N, d, dtype=torch.bfloat16, device="cuda")
+    moe.moe_grouped_swiglu_fwd(cfg, c["xp"], c["off"], c["W1"], c["W2"], h, act, yp)
+    dxp = torch.empty(N, d, dtype=torch.bfloat16, device="cuda")
+    dW1 = torch.empty(E, 2 * f, d, device="cuda")
+    dW2 = torch.empty(E, d, f, device="cuda")
+    ws = moe.workspace(cfg, moe.WS_FFN_BWD)
+    moe.moe_grouped_swiglu_bwd(cfg, c["xp"], c["off"], c["W1"], c["W2"], act, h, c["dyp"], dxp, dW1,
+                               dW2, ws)
+    torch.cuda.synchronize()
+    moe.check_device_error()
+    X, dY = np64(xp), np64(dyp)
+    ref_y = np.zeros((N, d))
+    ref_dx = np.zeros((N, d))
+    o = r["offsets"]
+    for e in range(E):
+        sl = slice(o[e], o[e + 1])
+        y_e, a, u, hh = O.swiglu_ffn(np64(W1[e]), np64(W2[e]), X[sl])
+        ref_y[sl] = y_e
+        dX, dW1e, dW2e = O.swiglu_ffn_backward(np64(W1[e]), np64(W2[e]), X[sl], a, u, hh, dY[sl])
+        ref_dx[sl] = dX
+        assert_close(f"dW1[{e}]", np64(dW1[e]), dW1e, 2e-2)
+        assert_close(f"dW2[{e}]", np64(dW2[e]), dW2e, 2e-2)
+    assert_close("y_perm", np64(yp), ref_y, 2e-2)
+    assert_close("dx_perm", np64(dxp), ref_dx, 2e-2)
+
+
+@pytest.mark.parametrize("shared", [0, 1, 2])
+def test_combine_and_backward(shared):
+    T, d, E, k = 500, 136, 12, 3
+    r = routed(T, E, k, 7)
+    N = T * k
+    cfg = moe.make_cfg(T, d, E, k, 64)
+    g = torch.Generator().manual_seed(9)
+    yp = torch.randn(N, d, generator=g).bfloat16()
+    gate = torch.from_numpy(r["gate"]).float()
+    so = torch.randn(T, d, generator=g).bfloat16() if shared else None
+    coef = torch.rand(T, generator=g) if shared == 2 else None
+    dy = torch.randn(T, d, generator=g).bfloat16()
+    sop = torch.from_numpy(r["slot_of_pair"])
+    cu = lambda t: None if t is None else t.cuda()
+    y = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    moe.moe_unpermute_combine(cfg, cu(yp), cu(gate), cu(sop), cu(so), cu(coef), y)
+    dyp = torch.empty(N, d, dtype=torch.bfloat16, device="cuda")
+    dg = torch.empty(T, k, device="cuda")
+    dso = torch.empty(T, d, dtype=torch.bfloat16, device="cuda") if shared else None
+    dc = torch.empty(T, device="cuda") if shared == 2 else None
+    moe.moe_unpermute_combine_bwd(cfg, cu(dy), cu(yp), cu(gate), cu(sop), cu(so), cu(coef), dyp, dg,
+                                  dso, dc)
+    torch.cuda.synchronize()
+    Y, G, SOP, DY = np64(yp), r["gate"], r["slot_of_pair"], np64(dy)
+    c = np64(coef) if shared == 2 else np.ones(T)
+    ref = np.einsum("tj,tjd->td", G, Y[SOP])
+    if shared:
+        ref = ref + c[:, None] * np64(so)
+    assert_close("y", np64(y), ref, 1e-2)
+    ref_dyp = np.zeros((N, d))
+    ref_dyp[SOP] = G[:, :, None] * DY[:, None, :]
+    assert_close("dy_perm", np64(dyp), ref_dyp, 1e-2)
+    assert_close("dgate", np64(dg), np.einsum("td,tjd->tj", DY, Y[SOP]), 1e-3)
+    if shared:
+        assert_close("dshared", np64(dso), c[:, None] * DY, 1e-2)
+    if shared == 2:
+        assert_close("dcoef", np64(dc), (DY * np64(so)).sum(1), 1e-3)
