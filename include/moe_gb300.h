@@ -109,6 +109,26 @@ int moe_route_topk(const moe_cfg* cfg, const void* x, const void* W_r, const flo
                    int32_t* counts, int32_t* offsets, int32_t* slot_of_pair,
                    int32_t* token_of_slot, void* ws, size_t ws_bytes, void* stream);
 
+/* Routing without a workspace.  The pages have no counterpart: this entry point serves callers
+ * that cannot allocate device memory and cannot lend the library a workspace (for example a
+ * runtime that owns all device memory through its own arena, or a plugin interface that passes
+ * only input and output tensors).  Arguments, outputs and errors are those of moe_route_topk,
+ * without ws / ws_bytes, and with one more requirement: logits_in or logits_out must be set
+ * (the router logits need a caller buffer; MOE_ERR_INVALID_ARG otherwise).
+ *   Scratch: a fixed 512 KB array inside the library, held on every GPU that loads it until the
+ *   process exits.  E * ceil(T/256) must not exceed 65536 (e.g. T = 65536 tokens with E = 256,
+ *   or T = 131072 with E = 128); larger calls return MOE_ERR_UNSUPPORTED.
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress):
+ *   make that first call before any stream capture.
+ *   All calls share the one array and every call overwrites what it reads, so nothing needs
+ *   clearing; but calls whose GPU work overlaps (different streams or host threads without
+ *   ordering between them) race on it and give wrong results: order them.
+ *   Allocates nothing: no cudaMalloc, cudaFree or allocating library routine. */
+int moe_route_topk_noalloc(const moe_cfg* cfg, const void* x, const void* W_r, const float* b_r,
+                           const float* logits_in, float* logits_out, int32_t* idx, float* gate,
+                           int32_t* counts, int32_t* offsets, int32_t* slot_of_pair,
+                           int32_t* token_of_slot, void* stream);
+
 /* Permute: x_perm[s] = x[token_of_slot[s]] for s < N.  "Megatron-Bridge 深度剖析",
  * §Permute Fusion (tokens regrouped by expert: one memory copy).
  *   x [T,d], x_perm [N,d] (dtype); slot_of_pair [T,k] from moe_route_topk. */

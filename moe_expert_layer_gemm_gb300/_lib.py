@@ -41,6 +41,7 @@ _CFG = ctypes.POINTER(MoeCfg)
 _SIGS = {
     "moe_workspace_bytes": (_SZ, [_CFG, ctypes.c_int]),
     "moe_route_topk": (ctypes.c_int, [_CFG] + [_VP] * 12 + [_SZ, _VP]),
+    "moe_route_topk_noalloc": (ctypes.c_int, [_CFG] + [_VP] * 12),
     "moe_permute": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP]),
     "moe_grouped_swiglu_fwd": (ctypes.c_int, [_CFG] + [_VP] * 8 + [_SZ, _VP]),
     "moe_grouped_swiglu_bwd": (ctypes.c_int, [_CFG] + [_VP] * 11 + [_SZ, _VP]),
@@ -129,6 +130,15 @@ def moe_route_topk(cfg, x, W_r, b_r, logits_in, logits_out, idx, gate, counts, o
                                 _p(slot_of_pair), _p(token_of_slot), _p(ws),
                                 0 if ws is None else ws.numel(), _stream(stream)),
            "moe_route_topk")
+
+
+def moe_route_topk_noalloc(cfg, x, W_r, b_r, logits_in, logits_out, idx, gate, counts, offsets,
+                           slot_of_pair, token_of_slot, stream=None):
+    """moe_route_topk without a workspace (scratch inside the library; see the header)."""
+    _check(lib().moe_route_topk_noalloc(ctypes.byref(cfg), _p(x), _p(W_r), _p(b_r), _p(logits_in),
+                                        _p(logits_out), _p(idx), _p(gate), _p(counts), _p(offsets),
+                                        _p(slot_of_pair), _p(token_of_slot), _stream(stream)),
+           "moe_route_topk_noalloc")
 
 
 def moe_permute(cfg, x, slot_of_pair, x_perm, stream=None):

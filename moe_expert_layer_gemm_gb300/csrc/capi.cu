@@ -765,3 +765,26 @@ int moe_layer_bwd(const moe_cfg* c, const void* dy, const void* x, const void* W
 }
 
 }  // extern "C"
+
+namespace moe {
+
+// Entry points into the checks and the routing stages for other translation units.
+int validate_cfg(const moe_cfg* c) { return check_cfg(c); }
+
+int validate_ptr(const void* p, const char* name, bool required) {
+  return check_ptr(p, name, required);
+}
+
+int route_stages(const moe_cfg* c, const void* x, const void* W_r, const float* b_r,
+                 const float* logits_in, float* logits_out, int32_t* idx, float* gate,
+                 int32_t* counts, int32_t* offsets, int32_t* slot_of_pair, int32_t* token_of_slot,
+                 int32_t* hist, int32_t* base, cudaStream_t st) {
+  RouteWs w;
+  w.hist = hist;
+  w.base = base;
+  w.logits = nullptr;
+  return route_impl(c, x, W_r, b_r, logits_in, logits_out, idx, gate, counts, offsets,
+                    slot_of_pair, token_of_slot, w, st);
+}
+
+}  // namespace moe

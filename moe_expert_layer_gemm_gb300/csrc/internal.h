@@ -121,6 +121,14 @@ struct GemmDesc {
   const float* bias;
 };
 
+// Argument checks and the routing stages (capi.cu), for entry points defined elsewhere.
+int validate_cfg(const moe_cfg* c);
+int validate_ptr(const void* p, const char* name, bool required);
+int route_stages(const moe_cfg* c, const void* x, const void* W_r, const float* b_r,
+                 const float* logits_in, float* logits_out, int32_t* idx, float* gate,
+                 int32_t* counts, int32_t* offsets, int32_t* slot_of_pair, int32_t* token_of_slot,
+                 int32_t* hist, int32_t* base, cudaStream_t st);
+
 int gemm_tc(const GemmDesc& g, cudaStream_t st);     // bf16 tcgen05 path (gemm_tc.cu)
 int gemm_simt(const GemmDesc& g, cudaStream_t st);   // fp32 CUDA-core path (gemm_simt.cu)
 

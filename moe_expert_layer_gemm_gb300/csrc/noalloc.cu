@@ -1,0 +1,100 @@
+// Routing for callers that cannot allocate device memory.
+//
+// Some callers of this library cannot call cudaMalloc and have no spare buffer to lend as a
+// workspace: a host runtime that owns every byte of device memory through its own arena and
+// forbids third-party code from allocating (so that its accounting stays exact and no
+// allocation stalls the device in the middle of a step), or a plugin interface that hands the
+// library only its input and output tensors.  moe_route_topk_noalloc serves them: its scratch
+// space (the per-block expert histograms and their prefix sums) is a fixed array inside the
+// library, so a call needs nothing beyond its inputs and outputs.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "moe_gb300.h"
+
+namespace moe {
+
+// Two int32 tables of E * ceil(T / 256) entries each (512 KB in all).  Every GPU that loads the
+// library holds this array until the process exits.
+constexpr int NOALLOC_ROUTE_MAX_ENTRIES = 65536;
+static __device__ __align__(256) int32_t g_route_scratch[2 * NOALLOC_ROUTE_MAX_ENTRIES];
+
+static std::mutex g_scratch_mu;
+static int32_t* g_scratch_ptr[64];
+
+// Device address of the array on the current device, looked up once per device.
+static int route_scratch(int32_t** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    set_error("moe_route_topk_noalloc: no usable current device (%s)", cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_route_scratch);
+    if (e != cudaSuccess || !p) {
+      set_error("moe_route_topk_noalloc: cudaGetSymbolAddress failed on device %d: %s", dev,
+                cudaGetErrorString(e));
+      return MOE_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_scratch_ptr[dev];
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_route_topk_noalloc(const moe_cfg* c, const void* x, const void* W_r,
+                                      const float* b_r, const float* logits_in, float* logits_out,
+                                      int32_t* idx, float* gate, int32_t* counts, int32_t* offsets,
+                                      int32_t* slot_of_pair, int32_t* token_of_slot,
+                                      void* stream) {
+  MOE_TRY(validate_cfg(c));
+  if (!logits_in && !logits_out) {
+    set_error("moe_route_topk_noalloc: logits_in or logits_out must be given (the router "
+              "logits need a caller buffer)");
+    return MOE_ERR_INVALID_ARG;
+  }
+  const int64_t entries = static_cast<int64_t>(c->E) * route_blocks(c->T);
+  if (entries > NOALLOC_ROUTE_MAX_ENTRIES) {
+    set_error("moe_route_topk_noalloc: E * ceil(T/256) = %lld exceeds the built-in scratch of "
+              "%d entries (e.g. T=65536 with E=256); use moe_route_topk with a workspace",
+              static_cast<long long>(entries), NOALLOC_ROUTE_MAX_ENTRIES);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  MOE_TRY(validate_ptr(x, "x", !logits_in));
+  MOE_TRY(validate_ptr(W_r, "W_r", !logits_in));
+  MOE_TRY(validate_ptr(b_r, "b_r", false));
+  MOE_TRY(validate_ptr(logits_in, "logits_in", false));
+  MOE_TRY(validate_ptr(logits_out, "logits_out", false));
+  MOE_TRY(validate_ptr(idx, "idx", true));
+  MOE_TRY(validate_ptr(gate, "gate", true));
+  MOE_TRY(validate_ptr(counts, "counts", true));
+  MOE_TRY(validate_ptr(offsets, "offsets", true));
+  MOE_TRY(validate_ptr(slot_of_pair, "slot_of_pair", true));
+  MOE_TRY(validate_ptr(token_of_slot, "token_of_slot", true));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (c->T == 0) {
+    if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * c->E, st) != cudaSuccess ||
+        cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (c->E + 1), st) != cudaSuccess) {
+      set_error("moe_route_topk_noalloc: cudaMemsetAsync failed");
+      return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+  }
+  int32_t* scratch = nullptr;
+  MOE_TRY(route_scratch(&scratch));
+  // hist and base are written in full by the histogram and scan kernels before they are read,
+  // so the array needs no clearing between calls.
+  int32_t* hist = scratch;
+  int32_t* base = scratch + NOALLOC_ROUTE_MAX_ENTRIES;
+  return route_stages(c, x, W_r, b_r, logits_in, logits_out, idx, gate, counts, offsets,
+                      slot_of_pair, token_of_slot, hist, base, st);
+}
