@@ -68,12 +68,20 @@ MTP_256E = LayerConfig(
 ROUTE_STRESS = LayerConfig("routing-stress T65536 d4096 E128 top8 sigmoid", 65536, 4096, 128, 8,
                            512, score_fn=SIGMOID, renorm=0, backward=False)
 
+# A 32-expert slice of the DeepSeek-style layer: same d_model, ffn, top-k and about the same
+# rows per expert (T*k/E = 768), a quarter of the tokens -- small enough (about 4 GB on the
+# device) for multi-pass profiler captures of the per-expert kernels.
+DEEPSEEK_E32 = DEEPSEEK_128E.replace(
+    name="deepseek-style slice T4096 d2688 E32 top6 sigmoid-renorm f1856 shared1856 zipf1.2",
+    T=4096, E=32)
+
 CONFIGS = {
     "tiny": TINY_F32,
     "qwen3": QWEN3_30B_A3B,
     "deepseek": DEEPSEEK_128E,
     "mtp256": MTP_256E,
     "stress": ROUTE_STRESS,
+    "deepseek_e32": DEEPSEEK_E32,
 }
 
 
