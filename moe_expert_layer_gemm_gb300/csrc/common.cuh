@@ -18,6 +18,7 @@ enum : int {
   DEVERR_BAD_EXPERT = 2,      // an expert index outside [0, E)
   DEVERR_BAD_SLOT = 3,        // a slot outside [0, N)
   DEVERR_BAD_OFFSETS = 4,     // offsets not monotone or not ending at N
+  DEVERR_SMEM_ALIGN = 5,      // dynamic shared memory not 1024-byte aligned
 };
 
 __device__ __forceinline__ void record_error(int* err, int code) {

@@ -11,10 +11,12 @@
 //   warp 0     TMA producer: loads A/B k-blocks into a STAGES-deep shared-memory ring
 //   warp 1     MMA issuer: owns TMEM (2 accumulators of BN fp32 columns), issues
 //              tcgen05.mma (M=128, N=BN, K=16) per k-step, commits to the ring's empty barriers
-//   warps 2-5  epilogue: TMEM -> registers (tcgen05.ld) -> fused epilogue -> global stores,
+//   warps 2-5  epilogue: TMEM -> registers (tcgen05.ld) -> fused epilogue -> a swizzled
+//              shared-memory slab per warp (32 rows x 128 bytes) -> TMA bulk-tensor store,
 //              overlapped with the next tile's MMAs through the second accumulator
 // Tiles are BM=128 rows x BN columns x BK=64; a CTA walks tiles blockIdx.x, +gridDim.x, ...
 #include <cuda.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -31,13 +33,21 @@ constexpr int BK = 64;
 constexpr int MAXG = 256;             // groups per launch (experts, or K splits)
 constexpr int NUM_THREADS = 192;
 constexpr int A_STAGE = BM * BK * 2;  // 16 KB
+constexpr int SLAB = 32 * 128;        // one warp's staging buffer: 32 rows x 128 bytes
 
-template <int BN> struct TileCfg {
+// Router logits (fp32 rows of E columns, E not necessarily a multiple of 4) are written with
+// direct stores; every other product goes out through the staged TMA path.
+template <int SCHED, int EPI> struct OutPath {
+  static constexpr bool tma = !(SCHED == RAGGED_M && EPI == EPI_F32);
+};
+
+template <int BN, bool TMA_OUT> struct TileCfg {
   static constexpr int B_STAGE = BN * BK * 2;
   static constexpr int STAGES = (BN == 256) ? 4 : 6;
   static constexpr int RING = STAGES * (A_STAGE + B_STAGE);
-  static constexpr int AUX = 4096;   // barriers, TMEM address, abort flag, group tables
-  static constexpr int SMEM = RING + AUX + 1024;
+  static constexpr int STAGING = TMA_OUT ? 4 * 2 * SLAB : 0;   // 4 epilogue warps x 2 slabs
+  static constexpr int AUX = 3072;   // barriers, TMEM address, flags, group tables
+  static constexpr int SMEM = RING + STAGING + AUX;
   static constexpr int TMEM_COLS = 2 * BN;
 };
 
@@ -107,31 +117,68 @@ struct Sched {
   }
 };
 
+// ---------------------------------------------------------------- staging slab helpers
+// A slab is 32 rows x 128 bytes laid out as the 128-byte-swizzled box of a TMA map: the 16-byte
+// chunk j of row r sits at r*128 + ((j ^ (r & 7)) * 16).  Lane r owns row r.
+__device__ __forceinline__ void slab_put(uint8_t* slab, int lane, int j, const uint4& v) {
+  *reinterpret_cast<uint4*>(slab + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
+}
+__device__ __forceinline__ uint4 slab_get(const uint8_t* slab, int lane, int j) {
+  return *reinterpret_cast<const uint4*>(slab + lane * 128 + ((j ^ (lane & 7)) << 4));
+}
+// Make the warp's slab writes visible to the TMA engine, then store the slab (lane 0).
+__device__ __forceinline__ void slab_store_2d(const CUtensorMap* m, const uint8_t* slab, int lane,
+                                              int c0, int c1) {
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    ptx::tma_store_2d(m, slab, c0, c1);
+    ptx::bulk_commit();
+  }
+}
+__device__ __forceinline__ void slab_store_3d(const CUtensorMap* m, const uint8_t* slab, int lane,
+                                              int c0, int c1, int c2) {
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    ptx::tma_store_3d(m, slab, c0, c1, c2);
+    ptx::bulk_commit();
+  }
+}
+
 template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const KArgs p) {
-  using C = TileCfg<BN>;
+                   const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
+                   const __grid_constant__ CUtensorMap tmO2, const KArgs p) {
+  constexpr bool TMA_OUT = OutPath<SCHED, EPI>::tma;
+  using C = TileCfg<BN, TMA_OUT>;
   using S = Sched<BN, SCHED, EPI>;
   constexpr int STAGES = C::STAGES;
   constexpr uint32_t STAGE_TX = A_STAGE + C::B_STAGE;
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING);
+  uint8_t* staging = smem + C::RING;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING + C::STAGING);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* epi_bar = tempty + 2;    // one per epilogue warp (TMA loads of saved activations)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(epi_bar + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* s_bad = reinterpret_cast<int*>(tmem_holder + 2);
   int* s_off = reinterpret_cast<int*>(tmem_holder + 4);
   int* s_pre = s_off + (MAXG + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // 128-byte swizzled tiles need 1024-byte aligned shared memory.
+  if ((ptx::smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) record_error(p.err, DEVERR_SMEM_ALIGN);
+    return;
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       ptx::mbar_init(&full[i], 1);
@@ -141,6 +188,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_init(&tfull[i], 1);
       ptx::mbar_init(&tempty[i], 4);
     }
+    for (int i = 0; i < 4; ++i) ptx::mbar_init(&epi_bar[i], 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::tma_prefetch_desc(&tmA);
@@ -157,16 +205,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   // The offsets must be non-decreasing and stay inside the operands (rows of A for RAGGED_M,
   // the reduction length for RAGGED_K); otherwise nothing is computed and the error recorded.
-  __shared__ int s_bad;
   if (threadIdx.x == 0) {
     const int cap = SCHED == RAGGED_M ? p.M : p.K;
     int bad = (s_off[0] < 0 || s_off[p.G] > cap) ? 1 : 0;
     for (int i = 0; i < p.G && !bad; ++i) bad = s_off[i + 1] < s_off[i];
-    s_bad = bad;
+    *s_bad = bad;
     if (bad) record_error(p.err, DEVERR_BAD_OFFSETS);
   }
   __syncthreads();
-  if (s_bad) return;
+  if (*s_bad) return;
   if (SCHED == RAGGED_M && warp == 0) {
     // s_pre[g] = sum_{g' < g} ceil(rows_g' / BM): lane L scans groups [L*per, (L+1)*per)
     const int per = (p.G + 31) / 32;
@@ -312,10 +359,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ epilogue (warps 2..5)
     const int q = warp & 3;          // TMEM lane quadrant this warp may access
     const int r = q * 32 + lane;     // row inside the tile
+    uint8_t* slabs = staging + q * (2 * SLAB);
+    int slab_sel = 0;
+    uint32_t ld_phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
+    // Next free staging slab of this warp: at most one earlier store may still be reading.
+    auto next_slab = [&]() -> uint8_t* {
+      if (lane == 0) ptx::bulk_wait_read<1>();
+      __syncwarp();
+      uint8_t* s = slabs + slab_sel * SLAB;
+      slab_sel ^= 1;
+      return s;
+    };
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const TileInfo ti = S::decode(p, s_off, s_pre, tile);
+      const int row0 = ti.m0 + q * 32;              // first row of this warp's slab
+      const int rows_here = min(32, ti.m_end - row0);
       const int row = ti.m0 + r;
       const bool valid = row < ti.m_end;
       if (ti.kblocks == 0) {
@@ -331,8 +391,139 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
+      // Full slabs go out through TMA (the maps clip at the tensors' edges).  For ragged rows a
+      // slab that crosses the end of its expert's rows would overwrite the next expert's: it is
+      // written with masked stores instead.
+      const bool tma_slab = TMA_OUT && (SCHED == RAGGED_K ? rows_here > 0 : rows_here == 32);
+      bool aborted = false;
 
-      if (EPI == EPI_SWIGLU_FWD) {
+      if (rows_here <= 0) {
+        // no row of this slab exists
+      } else if (tma_slab && EPI == EPI_STORE) {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 64) {
+          const int col = ti.n0 + c;
+          if (col >= p.N) break;
+          uint32_t v0[32], v1[32];
+          ptx::tmem_ld32(t_row + c, v0);
+          ptx::tmem_ld32(t_row + c + 32, v1);
+          ptx::tmem_ld_wait();
+          uint8_t* slab = next_slab();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float a[8], b[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              a[i] = __uint_as_float(v0[8 * j + i]);
+              b[i] = __uint_as_float(v1[8 * j + i]);
+            }
+            slab_put(slab, lane, j, pack16(a, static_cast<const bf16*>(nullptr)));
+            slab_put(slab, lane, 4 + j, pack16(b, static_cast<const bf16*>(nullptr)));
+          }
+          slab_store_2d(&tmO0, slab, lane, col, row0);
+        }
+      } else if (tma_slab && EPI == EPI_F32) {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          const int col = ti.n0 + c;
+          if (col >= p.N) break;
+          uint32_t v[32];
+          ptx::tmem_ld32(t_row + c, v);
+          ptx::tmem_ld_wait();
+          uint8_t* slab = next_slab();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            slab_put(slab, lane, j, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+          slab_store_3d(&tmO0, slab, lane, col, row0, ti.g);
+        }
+      } else if (tma_slab && EPI == EPI_SWIGLU_FWD) {
+        // acc columns [0, BN/2) are gate, [BN/2, BN) up, for h columns n0 .. n0+BN/2
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 64) {
+          const int col = ti.n0 + c;
+          if (col >= p.f) break;
+          uint8_t* slab = next_slab();
+#pragma unroll 1
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t ga[32], up[32];
+            ptx::tmem_ld32(t_row + c + 32 * hf, ga);
+            ptx::tmem_ld32(t_row + BN / 2 + c + 32 * hf, up);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              float hv[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                hv[i] = silu_f(__uint_as_float(ga[8 * j + i])) * __uint_as_float(up[8 * j + i]);
+              slab_put(slab, lane, 4 * hf + j, pack16(hv, static_cast<const bf16*>(nullptr)));
+            }
+          }
+          slab_store_2d(&tmO0, slab, lane, col, row0);
+          if (p.out2) {
+#pragma unroll 1
+            for (int part = 0; part < 2; ++part) {   // 0: gate pre-activation a, 1: up u
+              uint8_t* s2 = next_slab();
+#pragma unroll 1
+              for (int hf = 0; hf < 2; ++hf) {
+                uint32_t v[32];
+                ptx::tmem_ld32(t_row + part * (BN / 2) + c + 32 * hf, v);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  float fv[8];
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) fv[i] = __uint_as_float(v[8 * j + i]);
+                  slab_put(s2, lane, 4 * hf + j, pack16(fv, static_cast<const bf16*>(nullptr)));
+                }
+              }
+              slab_store_2d(part == 0 ? &tmO1 : &tmO2, s2, lane, col, row0);
+            }
+          }
+        }
+      } else if (tma_slab && EPI == EPI_SWIGLU_BWD) {
+        // acc = dh for f columns n0 .. n0+BN.  The saved [a | u] of the slab are brought in by
+        // TMA (map tmO2 over act), combined with dh, and [da | du] written back by TMA.
+        uint8_t* sa = slabs;
+        uint8_t* su = slabs + SLAB;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 64) {
+          const int col = ti.n0 + c;
+          if (col >= p.f) break;
+          if (lane == 0) {
+            ptx::bulk_wait_read<0>();   // both slabs free
+            ptx::mbar_arrive_expect_tx(&epi_bar[q], 2 * SLAB);
+            ptx::tma_load_2d(sa, &tmO2, &epi_bar[q], col, row0);
+            ptx::tma_load_2d(su, &tmO2, &epi_bar[q], p.f + col, row0);
+          }
+          __syncwarp();
+          if (!ptx::mbar_wait(&epi_bar[q], ld_phase, abort_flag, p.err)) { aborted = true; break; }
+          ld_phase ^= 1u;
+#pragma unroll 1
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t dh[32];
+            ptx::tmem_ld32(t_row + c + 32 * hf, dh);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              float av[8], uv[8], da[8], du[8];
+              unpack16(slab_get(sa, lane, 4 * hf + j), av, static_cast<const bf16*>(nullptr));
+              unpack16(slab_get(su, lane, 4 * hf + j), uv, static_cast<const bf16*>(nullptr));
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float g = __uint_as_float(dh[8 * j + i]);
+                const float s = 1.0f / (1.0f + __expf(-av[i]));
+                da[i] = g * uv[i] * (s + av[i] * s * (1.0f - s));
+                du[i] = g * av[i] * s;
+              }
+              slab_put(sa, lane, 4 * hf + j, pack16(da, static_cast<const bf16*>(nullptr)));
+              slab_put(su, lane, 4 * hf + j, pack16(du, static_cast<const bf16*>(nullptr)));
+            }
+          }
+          slab_store_2d(&tmO0, sa, lane, col, row0);
+          slab_store_2d(&tmO1, su, lane, col, row0);
+        }
+      } else if (EPI == EPI_SWIGLU_FWD) {
+        // masked stores (a slab at the end of an expert's rows)
         bf16* hrow = static_cast<bf16*>(p.out) + row * p.ldo;
         bf16* arow = static_cast<bf16*>(p.out2) + row * p.ldo2;
 #pragma unroll 1
@@ -385,9 +576,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               for (int i = 0; i < 8; ++i) {
                 const float g = __uint_as_float(dh[v * 8 + i]);
                 const float s = 1.0f / (1.0f + __expf(-av[i]));
-                const float silu = av[i] * s;
                 da[i] = g * uv[i] * (s + av[i] * s * (1.0f - s));
-                du[i] = g * silu;
+                du[i] = g * av[i] * s;
               }
               st16(drow + col + v * 8, pack16(da, static_cast<const bf16*>(nullptr)));
               st16(drow + p.f + col + v * 8, pack16(du, static_cast<const bf16*>(nullptr)));
@@ -395,7 +585,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       } else {
-        // EPI_STORE (bf16) or EPI_F32 (+bias)
+        // EPI_STORE (bf16) or EPI_F32 (+bias), masked direct stores
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           const int col = ti.n0 + c;
@@ -444,9 +634,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
+      if (aborted) break;
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (lane == 0) ptx::bulk_wait_all();   // every store of this warp has landed
+    __syncwarp();
   }
 
   ptx::tc_fence_before();
@@ -477,33 +670,53 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// A 2-D bf16 tensor map over op (rows x cols, row pitch ld), box = 64 columns x box_rows,
-// 128-byte swizzle; out-of-bounds elements read as zero.
-int make_map(CUtensorMap* m, const Operand& op, int box_rows) {
+// A tensor map with 128-byte swizzle; out-of-bounds elements read as zero and are not written.
+int encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
+           const cuuint64_t* strides_bytes, const cuuint32_t* box) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     set_error("cuTensorMapEncodeTiled is not available from the driver");
     return MOE_ERR_CUDA;
   }
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(op.cols), static_cast<cuuint64_t>(op.rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(op.ld) * 2};
-  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(op.base), dims, strides,
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides_bytes,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
-    set_error("cuTensorMapEncodeTiled failed (%d): rows=%lld cols=%lld ld=%lld box_rows=%d", (int)r,
-              (long long)op.rows, (long long)op.cols, (long long)op.ld, box_rows);
+    set_error("cuTensorMapEncodeTiled failed (%d): rank=%d dims=%llu,%llu box=%u,%u", (int)r, rank,
+              (unsigned long long)dims[0], (unsigned long long)dims[1], box[0], box[1]);
     return MOE_ERR_CUDA;
   }
   return MOE_OK;
 }
 
+// bf16 rows x cols with row pitch ld (elements); box = 64 columns x box_rows.
+int map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box);
+}
+
+// fp32 [G][rows][cols] (group stride gs, row pitch ld, elements); box = 32 x 32 x 1.
+int map_f32_3d(CUtensorMap* m, const void* base, int64_t G, int64_t rows, int64_t cols, int64_t ld,
+               int64_t gs) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(G)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4, static_cast<cuuint64_t>(gs) * 4};
+  cuuint32_t box[3] = {32u, 32u, 1u};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box);
+}
+
+int map_operand(CUtensorMap* m, const Operand& op, int box_rows) {
+  return map_bf16(m, op.base, op.rows, op.cols, op.ld, box_rows);
+}
+
 template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI>
 int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   const char* name = g.name ? g.name : kind;
-  using C = TileCfg<BN>;
+  constexpr bool TMA_OUT = OutPath<SCHED, EPI>::tma;
+  using C = TileCfg<BN, TMA_OUT>;
   auto kern = tc_gemm_kernel<BN, A_MN, B_MN, SCHED, EPI>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -511,12 +724,29 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   });
   if (attr_err != cudaSuccess) {
-    set_error("cudaFuncSetAttribute(%s): %s", name, cudaGetErrorString(attr_err));
+    set_error("cudaFuncSetAttribute(%s, %d bytes): %s", name, C::SMEM, cudaGetErrorString(attr_err));
     return MOE_ERR_CUDA;
   }
-  CUtensorMap ma, mb;
-  MOE_TRY(make_map(&ma, g.A, A_MN ? BK : BM));
-  MOE_TRY(make_map(&mb, g.B, B_MN ? BK : (EPI == EPI_SWIGLU_FWD ? BN / 2 : BN)));
+  CUtensorMap ma, mb, mo[3];
+  memset(mo, 0, sizeof(mo));
+  MOE_TRY(map_operand(&ma, g.A, A_MN ? BK : BM));
+  MOE_TRY(map_operand(&mb, g.B, B_MN ? BK : (EPI == EPI_SWIGLU_FWD ? BN / 2 : BN)));
+  const int64_t rows = g.M;   // RAGGED_M: rows of the output (capacity)
+  if (EPI == EPI_STORE) {
+    MOE_TRY(map_bf16(&mo[0], g.out, rows, g.N, g.ldo, 32));
+  } else if (EPI == EPI_F32 && SCHED == RAGGED_K) {
+    MOE_TRY(map_f32_3d(&mo[0], g.out, g.G, g.M, g.N, g.ldo, g.out_group_stride));
+  } else if (EPI == EPI_SWIGLU_FWD) {
+    MOE_TRY(map_bf16(&mo[0], g.out, rows, g.f, g.ldo, 32));
+    if (g.out2) {
+      MOE_TRY(map_bf16(&mo[1], g.out2, rows, g.f, g.ldo2, 32));
+      MOE_TRY(map_bf16(&mo[2], static_cast<const bf16*>(g.out2) + g.f, rows, g.f, g.ldo2, 32));
+    }
+  } else if (EPI == EPI_SWIGLU_BWD) {
+    MOE_TRY(map_bf16(&mo[0], g.out, rows, g.f, g.ldo, 32));
+    MOE_TRY(map_bf16(&mo[1], static_cast<const bf16*>(g.out) + g.f, rows, g.f, g.ldo, 32));
+    MOE_TRY(map_bf16(&mo[2], g.aux, rows, 2 * static_cast<int64_t>(g.f), g.ld_aux, 32));
+  }
   KArgs a;
   a.G = g.G;
   a.offsets = g.offsets;
@@ -535,7 +765,8 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   a.ld_aux = g.ld_aux;
   a.bias = g.bias;
   a.err = device_error_word();
-  return launch(name, kern, dim3(num_sms()), dim3(NUM_THREADS), C::SMEM, st, ma, mb, a);
+  return launch(name, kern, dim3(num_sms()), dim3(NUM_THREADS), C::SMEM, st, ma, mb, mo[0], mo[1],
+                mo[2], a);
 }
 
 }  // namespace
