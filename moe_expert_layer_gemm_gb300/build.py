@@ -20,6 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + INCLUDE, "-I" + CSRC]
+# Extra nvcc flags (e.g. -D tuning switches); a non-empty value forces a full rebuild.
+EXTRA = os.environ.get("MOE_NVCC_EXTRA", "").split()
 
 
 def nvcc() -> str:
@@ -50,8 +52,8 @@ def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False) 
     for src in sources():
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
-        if force or _stale(obj, [src] + headers):
-            cmd = [cc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        if force or EXTRA or _stale(obj, [src] + headers):
+            cmd = [cc, *ARCH, *FLAGS, *EXTRA, "-c", src, "-o", obj]
             if ptxas_info:
                 cmd.insert(1, "-Xptxas=-v")
             jobs.append(cmd)
@@ -67,7 +69,7 @@ def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False) 
                     sys.stderr.write(" ".join(cmd) + "\n" + p.stdout + p.stderr)
                 if p.returncode != 0:
                     raise RuntimeError(f"nvcc failed on {cmd[-3]}")
-    if force or jobs or _stale(LIB, objs):
+    if force or EXTRA or jobs or _stale(LIB, objs):
         cmd = [cc, *ARCH, "-shared", "-o", LIB, *objs]
         p = subprocess.run(cmd, capture_output=True, text=True)
         if p.returncode != 0:

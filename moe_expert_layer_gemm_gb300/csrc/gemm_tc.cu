@@ -7,13 +7,13 @@
 // ragged per-expert token counts.  Here the ragged extents are read on the device from the
 // routing offsets, so the host never synchronises on them.
 //
-// CTA organisation (persistent, one CTA per SM, 6 warps):
+// CTA organisation (persistent, one CTA per SM):
 //   warp 0     TMA producer: loads A/B k-blocks into a STAGES-deep shared-memory ring
 //   warp 1     MMA issuer: owns TMEM (2 accumulators of BN fp32 columns), issues
 //              tcgen05.mma (M=128, N=BN, K=16) per k-step, commits to the ring's empty barriers
-//   warps 2-5  epilogue: TMEM -> registers (tcgen05.ld) -> fused epilogue -> a swizzled
-//              shared-memory slab per warp (32 rows x 128 bytes) -> TMA bulk-tensor store,
-//              overlapped with the next tile's MMAs through the second accumulator
+//   warps 2..  epilogue (4 or 8 warps): TMEM -> registers (tcgen05.ld) -> fused epilogue ->
+//              a swizzled shared-memory slab per warp (32 rows x 128 bytes) -> TMA bulk-tensor
+//              store, overlapped with the next tile's MMAs through the second accumulator
 // Tiles are BM=128 rows x BN columns x BK=64; a CTA walks tiles blockIdx.x, +gridDim.x, ...
 #include <cuda.h>
 #include <string.h>
@@ -31,7 +31,6 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int MAXG = 256;             // groups per launch (experts, or K splits)
-constexpr int NUM_THREADS = 192;
 constexpr int A_STAGE = BM * BK * 2;  // 16 KB
 constexpr int SLAB = 32 * 128;        // one warp's staging buffer: 32 rows x 128 bytes
 
@@ -41,14 +40,36 @@ template <int SCHED, int EPI> struct OutPath {
   static constexpr bool tma = !(SCHED == RAGGED_M && EPI == EPI_F32);
 };
 
-template <int BN, bool TMA_OUT> struct TileCfg {
+#ifndef MOE_EPI8_WGRAD
+#define MOE_EPI8_WGRAD 0
+#endif
+#ifndef MOE_EPI8_SWIGLU_BWD
+#define MOE_EPI8_SWIGLU_BWD 1
+#endif
+#ifndef MOE_EPI8_OTHER
+#define MOE_EPI8_OTHER 0
+#endif
+
+// Epilogue width: 4 warps (one per TMEM lane quadrant) or 8 (two per quadrant, each on half
+// of the tile's columns) for products whose epilogue is long relative to their MMAs (weight
+// gradients, SwiGLU backward); 8 epilogue warps trade one pipeline stage for staging slabs.
+template <int SCHED, int EPI> struct EpiWidth {
+  static constexpr int warps =
+      !OutPath<SCHED, EPI>::tma ? 4
+      : (SCHED == RAGGED_K ? (MOE_EPI8_WGRAD ? 8 : 4)
+                           : (EPI == EPI_SWIGLU_BWD ? (MOE_EPI8_SWIGLU_BWD ? 8 : 4)
+                                                    : (MOE_EPI8_OTHER ? 8 : 4)));
+};
+
+template <int BN, bool TMA_OUT, int EPI_WARPS> struct TileCfg {
   static constexpr int B_STAGE = BN * BK * 2;
-  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int STAGES = (BN == 256) ? (EPI_WARPS == 8 ? 3 : 4) : 6;
   static constexpr int RING = STAGES * (A_STAGE + B_STAGE);
-  static constexpr int STAGING = TMA_OUT ? 4 * 2 * SLAB : 0;   // 4 epilogue warps x 2 slabs
+  static constexpr int STAGING = TMA_OUT ? EPI_WARPS * 2 * SLAB : 0;   // 2 slabs per warp
   static constexpr int AUX = 3072;   // barriers, TMEM address, flags, group tables
   static constexpr int SMEM = RING + STAGING + AUX;
   static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
 };
 
 struct KArgs {
@@ -147,12 +168,13 @@ __device__ __forceinline__ void slab_store_3d(const CUtensorMap* m, const uint8_
 }
 
 template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
                    const __grid_constant__ CUtensorMap tmO2, const KArgs p) {
   constexpr bool TMA_OUT = OutPath<SCHED, EPI>::tma;
-  using C = TileCfg<BN, TMA_OUT>;
+  constexpr int EPI_WARPS = EpiWidth<SCHED, EPI>::warps;
+  using C = TileCfg<BN, TMA_OUT, EPI_WARPS>;
   using S = Sched<BN, SCHED, EPI>;
   constexpr int STAGES = C::STAGES;
   constexpr uint32_t STAGE_TX = A_STAGE + C::B_STAGE;
@@ -166,7 +188,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* epi_bar = tempty + 2;    // one per epilogue warp (TMA loads of saved activations)
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(epi_bar + 4);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(epi_bar + EPI_WARPS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* s_bad = reinterpret_cast<int*>(tmem_holder + 2);
   int* s_off = reinterpret_cast<int*>(tmem_holder + 4);
@@ -186,9 +208,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&tfull[i], 1);
-      ptx::mbar_init(&tempty[i], 4);
+      ptx::mbar_init(&tempty[i], EPI_WARPS);
     }
-    for (int i = 0; i < 4; ++i) ptx::mbar_init(&epi_bar[i], 1);
+    for (int i = 0; i < EPI_WARPS; ++i) ptx::mbar_init(&epi_bar[i], 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::tma_prefetch_desc(&tmA);
@@ -356,10 +378,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (acc == 0) acc_phase ^= 1u;
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
+    // ------------------------------------------------------------ epilogue (warps 2..)
+    const int e = warp - 2;          // epilogue warp index
     const int q = warp & 3;          // TMEM lane quadrant this warp may access
     const int r = q * 32 + lane;     // row inside the tile
-    uint8_t* slabs = staging + q * (2 * SLAB);
+    // Accumulator columns of this warp: all of them (4 epilogue warps) or one half (8 warps).
+    // For the SwiGLU forward the half is taken in h columns (gate and up halves together).
+    constexpr int NPART = EPI_WARPS / 4;
+    const int part = e / 4;
+    const int span = (EPI == EPI_SWIGLU_FWD ? BN / 2 : BN) / NPART;
+    const int c_lo = part * span, c_hi = c_lo + span;
+    uint8_t* slabs = staging + e * (2 * SLAB);
+    uint64_t* my_bar = &epi_bar[e];
     int slab_sel = 0;
     uint32_t ld_phase = 0;
     int acc = 0;
@@ -382,7 +412,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // Empty reduction (an expert with no rows): its weight-gradient block is zero.
         if (EPI == EPI_F32 && valid) {
           float* o = static_cast<float*>(p.out) + ti.g * p.out_group_stride + row * p.ldo;
-          for (int c = ti.n0; c < min(p.N, ti.n0 + BN); c += 4)
+          for (int c = ti.n0 + c_lo; c < min(p.N, ti.n0 + c_hi); c += 4)
             *reinterpret_cast<float4*>(o + c) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         continue;
@@ -401,7 +431,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // no row of this slab exists
       } else if (tma_slab && EPI == EPI_STORE) {
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 64) {
+        for (int c = c_lo; c < c_hi; c += 64) {
           const int col = ti.n0 + c;
           if (col >= p.N) break;
           uint32_t v0[32], v1[32];
@@ -424,7 +454,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       } else if (tma_slab && EPI == EPI_F32) {
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = c_lo; c < c_hi; c += 32) {
           const int col = ti.n0 + c;
           if (col >= p.N) break;
           uint32_t v[32];
@@ -439,7 +469,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       } else if (tma_slab && EPI == EPI_SWIGLU_FWD) {
         // acc columns [0, BN/2) are gate, [BN/2, BN) up, for h columns n0 .. n0+BN/2
 #pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 64) {
+        for (int c = c_lo; c < c_hi; c += 64) {
           const int col = ti.n0 + c;
           if (col >= p.f) break;
           uint8_t* slab = next_slab();
@@ -486,17 +516,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint8_t* sa = slabs;
         uint8_t* su = slabs + SLAB;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 64) {
+        for (int c = c_lo; c < c_hi; c += 64) {
           const int col = ti.n0 + c;
           if (col >= p.f) break;
           if (lane == 0) {
             ptx::bulk_wait_read<0>();   // both slabs free
-            ptx::mbar_arrive_expect_tx(&epi_bar[q], 2 * SLAB);
-            ptx::tma_load_2d(sa, &tmO2, &epi_bar[q], col, row0);
-            ptx::tma_load_2d(su, &tmO2, &epi_bar[q], p.f + col, row0);
+            ptx::mbar_arrive_expect_tx(my_bar, 2 * SLAB);
+            ptx::tma_load_2d(sa, &tmO2, my_bar, col, row0);
+            ptx::tma_load_2d(su, &tmO2, my_bar, p.f + col, row0);
           }
           __syncwarp();
-          if (!ptx::mbar_wait(&epi_bar[q], ld_phase, abort_flag, p.err)) { aborted = true; break; }
+          if (!ptx::mbar_wait(my_bar, ld_phase, abort_flag, p.err)) { aborted = true; break; }
           ld_phase ^= 1u;
 #pragma unroll 1
           for (int hf = 0; hf < 2; ++hf) {
@@ -527,7 +557,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bf16* hrow = static_cast<bf16*>(p.out) + row * p.ldo;
         bf16* arow = static_cast<bf16*>(p.out2) + row * p.ldo2;
 #pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 32) {
+        for (int c = c_lo; c < c_hi; c += 32) {
           const int col = ti.n0 + c;
           if (col >= p.f) break;
           uint32_t ga[32], up[32];
@@ -558,7 +588,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bf16* act = static_cast<const bf16*>(p.aux) + row * p.ld_aux;
         bf16* drow = static_cast<bf16*>(p.out) + row * p.ldo;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = c_lo; c < c_hi; c += 32) {
           const int col = ti.n0 + c;
           if (col >= p.f) break;
           uint32_t dh[32];
@@ -587,7 +617,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       } else {
         // EPI_STORE (bf16) or EPI_F32 (+bias), masked direct stores
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = c_lo; c < c_hi; c += 32) {
           const int col = ti.n0 + c;
           if (col >= p.N) break;
           uint32_t v32[32];
@@ -716,7 +746,7 @@ template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI>
 int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   const char* name = g.name ? g.name : kind;
   constexpr bool TMA_OUT = OutPath<SCHED, EPI>::tma;
-  using C = TileCfg<BN, TMA_OUT>;
+  using C = TileCfg<BN, TMA_OUT, EpiWidth<SCHED, EPI>::warps>;
   auto kern = tc_gemm_kernel<BN, A_MN, B_MN, SCHED, EPI>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -765,7 +795,7 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   a.ld_aux = g.ld_aux;
   a.bias = g.bias;
   a.err = device_error_word();
-  return launch(name, kern, dim3(num_sms()), dim3(NUM_THREADS), C::SMEM, st, ma, mb, mo[0], mo[1],
+  return launch(name, kern, dim3(num_sms()), dim3(C::THREADS), C::SMEM, st, ma, mb, mo[0], mo[1],
                 mo[2], a);
 }
 
