@@ -63,6 +63,7 @@ def kernel_work(lc):
         "gemm_router_wgrad": ("tensor", 2.0 * T * d * (E + g)),
         "route_topk": ("hbm", T * E * 4 + N * 8),
         "route_scan": ("hbm", 0.0),
+        "route_hist": ("hbm", N * 4),
         "route_slots": ("hbm", N * 4 + N * 8),
         "permute": ("hbm", T * d * b * (1 + k) + N * 4),
         "combine": ("hbm", T * d * b * (k + 1) + N * 8 + (T * d * b if fs else 0)),

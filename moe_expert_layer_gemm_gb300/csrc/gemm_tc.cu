@@ -14,7 +14,8 @@
 //   warps 2..  epilogue (4 or 8 warps): TMEM -> registers (tcgen05.ld) -> fused epilogue ->
 //              a swizzled shared-memory slab per warp (32 rows x 128 bytes) -> TMA bulk-tensor
 //              store, overlapped with the next tile's MMAs through the second accumulator
-// Tiles are BM=128 rows x BN columns x BK=64; a CTA walks tiles blockIdx.x, +gridDim.x, ...
+// Tiles are BM=128 rows x BN columns x BK=64; a CTA (or a 2-CTA cluster, for the weight
+// gradients) walks tiles unit, unit + units, ...
 #include <cuda.h>
 #include <string.h>
 
@@ -50,6 +51,24 @@ template <int SCHED, int EPI> struct OutPath {
 #define MOE_EPI8_OTHER 0
 #endif
 
+#ifndef MOE_MC_WGRAD
+#define MOE_MC_WGRAD 1
+#endif
+
+// Weight gradients run in clusters of two CTAs on vertically adjacent 128-row tiles of the
+// same output block: both need the same B k-block, so each loads half of it and multicasts it
+// into both CTAs' shared memory (this GPU's own memory), cutting operand traffic from L2 by a
+// third.  Each CTA keeps its own MMAs, TMEM and epilogue.
+template <int SCHED, int EPI> struct McMode {
+  static constexpr bool on = SCHED == RAGGED_K && EPI == EPI_F32 && MOE_MC_WGRAD != 0;
+};
+
+// Staging slabs per epilogue warp: the SwiGLU backward needs two (saved a and u); with 8
+// epilogue warps the others make do with one so that the ring keeps four stages.
+template <int EPI, int EPI_WARPS> struct SlabsPerWarp {
+  static constexpr int n = (EPI == EPI_SWIGLU_BWD || EPI_WARPS == 4) ? 2 : 1;
+};
+
 // Epilogue width: 4 warps (one per TMEM lane quadrant) or 8 (two per quadrant, each on half
 // of the tile's columns) for products whose epilogue is long relative to their MMAs (weight
 // gradients, SwiGLU backward); 8 epilogue warps trade one pipeline stage for staging slabs.
@@ -59,14 +78,17 @@ template <int SCHED, int EPI> struct EpiWidth {
       : (SCHED == RAGGED_K ? (MOE_EPI8_WGRAD ? 8 : 4)
                            : (EPI == EPI_SWIGLU_BWD ? (MOE_EPI8_SWIGLU_BWD ? 8 : 4)
                                                     : (MOE_EPI8_OTHER ? 8 : 4)));
+  static constexpr int slabs = SlabsPerWarp<EPI, warps>::n;
 };
 
-template <int BN, bool TMA_OUT, int EPI_WARPS> struct TileCfg {
+template <int BN, bool TMA_OUT, int EPI_WARPS, int SLABS> struct TileCfg {
   static constexpr int B_STAGE = BN * BK * 2;
-  static constexpr int STAGES = (BN == 256) ? (EPI_WARPS == 8 ? 3 : 4) : 6;
-  static constexpr int RING = STAGES * (A_STAGE + B_STAGE);
-  static constexpr int STAGING = TMA_OUT ? EPI_WARPS * 2 * SLAB : 0;   // 2 slabs per warp
+  static constexpr int STAGING = TMA_OUT ? EPI_WARPS * SLABS * SLAB : 0;
   static constexpr int AUX = 3072;   // barriers, TMEM address, flags, group tables
+  static constexpr int MAX_SMEM = 232448;   // opt-in dynamic shared memory per block
+  static constexpr int FIT = (MAX_SMEM - STAGING - AUX) / (A_STAGE + B_STAGE);
+  static constexpr int STAGES = FIT < 6 ? FIT : 6;
+  static constexpr int RING = STAGES * (A_STAGE + B_STAGE);
   static constexpr int SMEM = RING + STAGING + AUX;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
@@ -94,7 +116,7 @@ struct TileInfo {
 
 __device__ __forceinline__ float silu_f(float a) { return a / (1.0f + __expf(-a)); }
 
-template <int BN, int SCHED, int EPI>
+template <int BN, int SCHED, int EPI, int TBM = BM>
 struct Sched {
   // Number of output column tiles.
   __device__ static int n_tiles(const KArgs& p) {
@@ -103,7 +125,7 @@ struct Sched {
   }
   __device__ static int total(const KArgs& p, const int* s_pre) {
     if (SCHED == RAGGED_M) return s_pre[p.G] * n_tiles(p);
-    return p.G * ((p.M + BM - 1) / BM) * n_tiles(p);
+    return p.G * ((p.M + TBM - 1) / TBM) * n_tiles(p);
   }
   __device__ static TileInfo decode(const KArgs& p, const int* s_off, const int* s_pre, int tile) {
     TileInfo ti;
@@ -122,12 +144,12 @@ struct Sched {
       ti.k0 = 0;
       ti.k_end = p.K;
     } else {
-      const int mtc = (p.M + BM - 1) / BM;
+      const int mtc = (p.M + TBM - 1) / TBM;
       const int per = mtc * nt_count;
       ti.g = tile / per;
       const int r = tile - ti.g * per;
       const int mt = r / nt_count, nt = r - mt * nt_count;
-      ti.m0 = mt * BM;
+      ti.m0 = mt * TBM;
       ti.m_end = p.M;
       ti.n0 = nt * BN;
       ti.k0 = s_off[ti.g];
@@ -174,8 +196,10 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
                    const __grid_constant__ CUtensorMap tmO2, const KArgs p) {
   constexpr bool TMA_OUT = OutPath<SCHED, EPI>::tma;
   constexpr int EPI_WARPS = EpiWidth<SCHED, EPI>::warps;
-  using C = TileCfg<BN, TMA_OUT, EPI_WARPS>;
-  using S = Sched<BN, SCHED, EPI>;
+  constexpr int SLABS = EpiWidth<SCHED, EPI>::slabs;
+  using C = TileCfg<BN, TMA_OUT, EPI_WARPS, SLABS>;
+  constexpr bool MC = McMode<SCHED, EPI>::on;
+  using S = Sched<BN, SCHED, EPI, MC ? 2 * BM : BM>;
   constexpr int STAGES = C::STAGES;
   constexpr uint32_t STAGE_TX = A_STAGE + C::B_STAGE;
 
@@ -195,6 +219,11 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
   int* s_pre = s_off + (MAXG + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Tile walker: one per CTA, or one per CTA pair of a cluster (rank 0 takes the upper 128 rows
+  // of the pair's 256-row tile, rank 1 the lower).
+  const uint32_t rank = MC ? ptx::cluster_ctarank() : 0u;
+  const int unit = MC ? static_cast<int>(ptx::cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int units = MC ? static_cast<int>(ptx::cluster_count_x()) : static_cast<int>(gridDim.x);
 
   // 128-byte swizzled tiles need 1024-byte aligned shared memory.
   if ((ptx::smem_u32(smem) & 1023u) != 0) {
@@ -204,7 +233,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       ptx::mbar_init(&full[i], 1);
-      ptx::mbar_init(&empty[i], 1);
+      ptx::mbar_init(&empty[i], MC ? 2 : 1);   // clusters: both CTAs' MMAs release a stage
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&tfull[i], 1);
@@ -258,7 +287,9 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
   __syncthreads();
 
   const int total = S::total(p, s_pre);
-  if (static_cast<int>(blockIdx.x) >= total) return;   // nothing for this CTA (uniform)
+  if (unit >= total) return;   // nothing for this CTA (the same decision in both CTAs of a pair)
+  // Clusters: every barrier of both CTAs is initialised before either writes into the other.
+  if (MC) ptx::cluster_sync();
 
   if (warp == 1) {
     ptx::tmem_alloc(tmem_holder, C::TMEM_COLS);
@@ -277,37 +308,53 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
       int armed[STAGES];
       for (int i = 0; i < STAGES; ++i) armed[i] = -1;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      // Loads of k-block kb of tile ti into `stage` (B halves multicast within a cluster).
+      auto issue = [&](const TileInfo& ti, int kb, int stg) {
+        uint8_t* a_dst = sA + stg * A_STAGE;
+        uint8_t* b_dst = sB + stg * C::B_STAGE;
+        const int kk = ti.k0 + kb * BK;
+        const int m_cta = ti.m0 + static_cast<int>(rank) * BM;
+        auto box = [&](void* dst, const CUtensorMap* m, int c0, int c1) {
+          ptx::tma_load_2d(dst, m, &full[stg], c0, c1);
+        };
+        if (!A_MN) {
+          box(a_dst, &tmA, kk, m_cta);
+        } else {
+#pragma unroll
+          for (int c = 0; c < BM / 64; ++c) box(a_dst + c * (BK * 128), &tmA, m_cta + 64 * c, kk);
+        }
+        if (!B_MN) {
+          const int brow = static_cast<int>(ti.g * p.b_group_rows) + ti.n0;
+          if (EPI == EPI_SWIGLU_FWD) {
+            box(b_dst, &tmB, kk, brow);
+            box(b_dst + (BN / 2) * 128, &tmB, kk, brow + static_cast<int>(p.b_up_rows));
+          } else {
+            box(b_dst, &tmB, kk, brow);
+          }
+        } else {
+          const int krow = (SCHED == RAGGED_M) ? static_cast<int>(ti.g * p.b_group_rows) + kk : kk;
+          if (MC) {
+            // this CTA's half of the B boxes, delivered to both CTAs of the pair
+            constexpr int HALF = BN / 128;
+#pragma unroll
+            for (int i = 0; i < HALF; ++i) {
+              const int c = static_cast<int>(rank) * HALF + i;
+              ptx::tma_load_2d_multicast(b_dst + c * (BK * 128), &tmB, &full[stg], ti.n0 + 64 * c,
+                                         krow, 0x3);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c) box(b_dst + c * (BK * 128), &tmB, ti.n0 + 64 * c, krow);
+          }
+        }
+      };
+      for (int tile = unit; tile < total && ok; tile += units) {
         const TileInfo ti = S::decode(p, s_off, s_pre, tile);
         for (int kb = 0; kb < ti.kblocks; ++kb) {
           if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
           ptx::mbar_arrive_expect_tx(&full[stage], STAGE_TX);
           armed[stage] = static_cast<int>(phase);
-          uint8_t* a_dst = sA + stage * A_STAGE;
-          uint8_t* b_dst = sB + stage * C::B_STAGE;
-          const int kk = ti.k0 + kb * BK;
-          if (!A_MN) {
-            ptx::tma_load_2d(a_dst, &tmA, &full[stage], kk, ti.m0);
-          } else {
-#pragma unroll
-            for (int c = 0; c < BM / 64; ++c)
-              ptx::tma_load_2d(a_dst + c * (BK * 128), &tmA, &full[stage], ti.m0 + 64 * c, kk);
-          }
-          if (!B_MN) {
-            const int brow = static_cast<int>(ti.g * p.b_group_rows) + ti.n0;
-            if (EPI == EPI_SWIGLU_FWD) {
-              ptx::tma_load_2d(b_dst, &tmB, &full[stage], kk, brow);
-              ptx::tma_load_2d(b_dst + (BN / 2) * 128, &tmB, &full[stage], kk,
-                               brow + static_cast<int>(p.b_up_rows));
-            } else {
-              ptx::tma_load_2d(b_dst, &tmB, &full[stage], kk, brow);
-            }
-          } else {
-            const int krow = (SCHED == RAGGED_M) ? static_cast<int>(ti.g * p.b_group_rows) + kk : kk;
-#pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-              ptx::tma_load_2d(b_dst + c * (BK * 128), &tmB, &full[stage], ti.n0 + 64 * c, krow);
-          }
+          issue(ti, kb, stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
@@ -330,7 +377,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+    for (int tile = unit; tile < total && ok; tile += units) {
       const TileInfo ti = S::decode(p, s_off, s_pre, tile);
       if (ti.kblocks == 0) continue;
       if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
@@ -366,7 +413,9 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
                                      : ptx::smem_desc_sw128(b_addr + k16 * 32, 16, 1024);
             ptx::umma_bf16(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
           }
-          ptx::umma_commit(&empty[stage]);   // frees the smem stage when these MMAs finish
+          // frees the smem stage (in both CTAs of a cluster) when these MMAs finish
+          if (MC) ptx::umma_commit_multicast(&empty[stage], 0x3);
+          else ptx::umma_commit(&empty[stage]);
         }
         __syncwarp();
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -388,7 +437,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
     const int part = e / 4;
     const int span = (EPI == EPI_SWIGLU_FWD ? BN / 2 : BN) / NPART;
     const int c_lo = part * span, c_hi = c_lo + span;
-    uint8_t* slabs = staging + e * (2 * SLAB);
+    uint8_t* slabs = staging + e * (SLABS * SLAB);
     uint64_t* my_bar = &epi_bar[e];
     int slab_sel = 0;
     uint32_t ld_phase = 0;
@@ -396,17 +445,21 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
     uint32_t acc_phase = 0;
     // Next free staging slab of this warp: at most one earlier store may still be reading.
     auto next_slab = [&]() -> uint8_t* {
-      if (lane == 0) ptx::bulk_wait_read<1>();
+      if (lane == 0) {
+        if (SLABS == 2) ptx::bulk_wait_read<1>();
+        else ptx::bulk_wait_read<0>();
+      }
       __syncwarp();
       uint8_t* s = slabs + slab_sel * SLAB;
-      slab_sel ^= 1;
+      if (SLABS == 2) slab_sel ^= 1;
       return s;
     };
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int tile = unit; tile < total; tile += units) {
       const TileInfo ti = S::decode(p, s_off, s_pre, tile);
-      const int row0 = ti.m0 + q * 32;              // first row of this warp's slab
+      const int m_cta = ti.m0 + static_cast<int>(rank) * BM;   // this CTA's rows of the tile
+      const int row0 = m_cta + q * 32;              // first row of this warp's slab
       const int rows_here = min(32, ti.m_end - row0);
-      const int row = ti.m0 + r;
+      const int row = m_cta + r;
       const bool valid = row < ti.m_end;
       if (ti.kblocks == 0) {
         // Empty reduction (an expert with no rows): its weight-gradient block is zero.
@@ -674,6 +727,9 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
+  // Clusters: neither CTA leaves while the other may still write into its shared memory or
+  // arrive on its barriers.
+  if (MC) ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
@@ -746,7 +802,7 @@ template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI>
 int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   const char* name = g.name ? g.name : kind;
   constexpr bool TMA_OUT = OutPath<SCHED, EPI>::tma;
-  using C = TileCfg<BN, TMA_OUT, EpiWidth<SCHED, EPI>::warps>;
+  using C = TileCfg<BN, TMA_OUT, EpiWidth<SCHED, EPI>::warps, EpiWidth<SCHED, EPI>::slabs>;
   auto kern = tc_gemm_kernel<BN, A_MN, B_MN, SCHED, EPI>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -795,6 +851,9 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   a.ld_aux = g.ld_aux;
   a.bias = g.bias;
   a.err = device_error_word();
+  if (McMode<SCHED, EPI>::on)
+    return launch_clusters(name, kern, dim3(num_sms() & ~1), dim3(C::THREADS), C::SMEM, 2, st, ma,
+                           mb, mo[0], mo[1], mo[2], a);
   return launch(name, kern, dim3(num_sms()), dim3(C::THREADS), C::SMEM, st, ma, mb, mo[0], mo[1],
                 mo[2], a);
 }

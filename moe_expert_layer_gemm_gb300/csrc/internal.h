@@ -36,6 +36,35 @@ int launch(const char* name, void (*kern)(KArgs...), dim3 grid, dim3 block, size
   return MOE_OK;
 }
 
+// The same, for a kernel launched in clusters of `cluster_x` CTAs along x.
+template <typename... KArgs, typename... Args>
+int launch_clusters(const char* name, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                    unsigned cluster_x, cudaStream_t st, Args&&... args) {
+  if (grid.x == 0 || grid.y == 0 || grid.z == 0) return MOE_OK;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster_x;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  trace_before(name, st);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  trace_after(name, st);
+  count_launch();
+  if (e != cudaSuccess) {
+    set_error("launch of %s (clusters of %u) failed: %s", name, cluster_x, cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
 #define MOE_TRY(x)                 \
   do {                             \
     int _st = (x);                 \

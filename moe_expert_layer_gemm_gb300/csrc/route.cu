@@ -6,15 +6,14 @@
 //   counts[e], offsets[e] = sum_{e'<e} counts[e'],
 //   slot(t, j) = offsets[e] + #{t' < t : t' picked e},  e = idx[t, j].
 //
-// Three launches:
-//   topk  -- one warp per token: k rounds of a warp-wide argmax over fp32 logits (ties ->
-//            lower expert index), gates in fp32; each block of 256 tokens also leaves a
-//            per-expert bitmask of its tokens in shared memory and writes the per-block
-//            counts hist[e][block] (popcounts of the masks).
+// Four launches:
+//   topk  -- one warp per token (grid-stride over all tokens): k rounds of a warp-wide argmax
+//            over fp32 logits (ties -> lower expert index), gates in fp32.
+//   hist  -- one block per 256 tokens: per-expert counts of the block, hist[e][block].
 //   scan  -- one block: exclusive prefix over hist in expert-major order gives, for every
 //            (expert, block), the first slot of that block's tokens of that expert.
-//   slots -- per block: rebuild the bitmasks from idx; the rank of token t among the block's
-//            tokens of expert e is the popcount of the mask bits below t.
+//   slots -- per block: per-expert bitmasks of the block's tokens; the rank of token t among
+//            the block's tokens of expert e is the popcount of the mask bits below t.
 // All integer, so the result is exact and independent of scheduling.
 #include <limits.h>
 
@@ -23,7 +22,7 @@
 
 namespace moe {
 
-constexpr int TPB = ROUTE_TOK_PER_BLOCK;   // tokens per block (8 warps x 32 tokens)
+constexpr int TPB = ROUTE_TOK_PER_BLOCK;   // tokens per histogram / slot block
 constexpr int MASK_WORDS = TPB / 32;        // 8 words of 32 token bits per expert
 constexpr int MAXK = MOE_MAX_TOPK;
 #define NEG_INF __int_as_float(0xff800000u)
@@ -42,21 +41,15 @@ template <int EPL>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E,
                                                    int k, int score_fn, int renorm,
                                                    int32_t* __restrict__ idx,
-                                                   float* __restrict__ gate,
-                                                   int32_t* __restrict__ hist, int nblk) {
-  __shared__ uint32_t mask[MOE_MAX_EXPERTS * MASK_WORDS];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int i = tid; i < E * MASK_WORDS; i += blockDim.x) mask[i] = 0u;
-  __syncthreads();
-
-  const int t_base = blockIdx.x * TPB + warp * 32;
+                                                   float* __restrict__ gate) {
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
   float cur[EPL], nxt[EPL];
-  load_logit_row<EPL>(logits, t_base, T, E, lane, cur);
+  load_logit_row<EPL>(logits, gw, T, E, lane, cur);
 
-  for (int i = 0; i < 32; ++i) {
-    const int t = t_base + i;
-    if (t >= T) break;
-    if (i + 1 < 32) load_logit_row<EPL>(logits, t + 1, T, E, lane, nxt);
+  for (int t = gw; t < T; t += nw) {
+    load_logit_row<EPL>(logits, t + nw, T, E, lane, nxt);   // next token's row in flight
 
     // ---- selection: k rounds of warp argmax, key (logit desc, expert asc)
     uint32_t taken = 0u;
@@ -125,25 +118,37 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
       }
     }
 
-    // ---- outputs: lane j writes pair j; it also marks the token in its expert's mask
+    // ---- outputs: lane j writes pair j
 #pragma unroll
     for (int j = 0; j < MAXK; ++j) {
       if (j < k && lane == j) {
         idx[static_cast<int64_t>(t) * k + j] = sel_e[j];
         gate[static_cast<int64_t>(t) * k + j] = g[j];
-        atomicOr(&mask[sel_e[j] * MASK_WORDS + warp], 1u << i);
       }
     }
 #pragma unroll
     for (int q = 0; q < EPL; ++q) cur[q] = nxt[q];
   }
+}
+
+// Per-block expert counts: hist[e][b] = number of tokens of block b (256 tokens) that picked e.
+__global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ idx, int T, int k,
+                                                   int E, int32_t* __restrict__ hist, int nblk,
+                                                   int* err) {
+  __shared__ int cnt[MOE_MAX_EXPERTS];
+  const int tid = threadIdx.x;
+  for (int i = tid; i < E; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) {
-    int c = 0;
-#pragma unroll
-    for (int w = 0; w < MASK_WORDS; ++w) c += __popc(mask[e * MASK_WORDS + w]);
-    hist[static_cast<int64_t>(e) * nblk + blockIdx.x] = c;
+  const int t = blockIdx.x * TPB + tid;
+  if (t < T) {
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[static_cast<int64_t>(t) * k + j];
+      if (e < 0 || e >= E) record_error(err, DEVERR_BAD_EXPERT);
+      else atomicAdd(&cnt[e], 1);
+    }
   }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) hist[static_cast<int64_t>(e) * nblk + blockIdx.x] = cnt[e];
 }
 
 // Exclusive prefix sum over hist[E][nblk] (expert-major) by one block of 1024 threads.
@@ -243,18 +248,25 @@ __global__ void __launch_bounds__(256) slots_kernel(const int32_t* __restrict__ 
 int launch_topk(const float* logits, int T, int E, int k, int score_fn, int renorm, int32_t* idx,
                 float* gate, int32_t* hist, cudaStream_t st) {
   const int nblk = route_blocks(T);
-  const dim3 grid(nblk), block(256);
+  int blocks = (T + 7) / 8;   // 8 warps per block, one token per warp at a time
+  if (blocks > num_sms() * 8) blocks = num_sms() * 8;
+  const dim3 grid(blocks), block(256);
+  int rc;
   if (E <= 32)
-    return launch("route_topk", topk_kernel<1>, grid, block, 0, st, logits, T, E, k, score_fn,
-                  renorm, idx, gate, hist, nblk);
-  if (E <= 64)
-    return launch("route_topk", topk_kernel<2>, grid, block, 0, st, logits, T, E, k, score_fn,
-                  renorm, idx, gate, hist, nblk);
-  if (E <= 128)
-    return launch("route_topk", topk_kernel<4>, grid, block, 0, st, logits, T, E, k, score_fn,
-                  renorm, idx, gate, hist, nblk);
-  return launch("route_topk", topk_kernel<8>, grid, block, 0, st, logits, T, E, k, score_fn,
-                renorm, idx, gate, hist, nblk);
+    rc = launch("route_topk", topk_kernel<1>, grid, block, 0, st, logits, T, E, k, score_fn, renorm,
+                idx, gate);
+  else if (E <= 64)
+    rc = launch("route_topk", topk_kernel<2>, grid, block, 0, st, logits, T, E, k, score_fn, renorm,
+                idx, gate);
+  else if (E <= 128)
+    rc = launch("route_topk", topk_kernel<4>, grid, block, 0, st, logits, T, E, k, score_fn, renorm,
+                idx, gate);
+  else
+    rc = launch("route_topk", topk_kernel<8>, grid, block, 0, st, logits, T, E, k, score_fn, renorm,
+                idx, gate);
+  MOE_TRY(rc);
+  return launch("route_hist", hist_kernel, dim3(nblk), dim3(TPB), 0, st, idx, T, k, E, hist, nblk,
+                device_error_word());
 }
 
 int launch_scan(const int32_t* hist, int E, int nblk, int32_t* base, int32_t* counts,
