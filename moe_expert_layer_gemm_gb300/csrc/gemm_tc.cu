@@ -462,11 +462,22 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
       const int row = m_cta + r;
       const bool valid = row < ti.m_end;
       if (ti.kblocks == 0) {
-        // Empty reduction (an expert with no rows): its weight-gradient block is zero.
-        if (EPI == EPI_F32 && valid) {
-          float* o = static_cast<float*>(p.out) + ti.g * p.out_group_stride + row * p.ldo;
-          for (int c = ti.n0 + c_lo; c < min(p.N, ti.n0 + c_hi); c += 4)
-            *reinterpret_cast<float4*>(o + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        // Empty reduction (an expert with no rows): its weight-gradient block is zero.  One
+        // zeroed slab is stored to every 32-column chunk of this warp's rows.
+        if (EPI == EPI_F32 && SCHED == RAGGED_K && TMA_OUT && rows_here > 0) {
+          uint8_t* z = next_slab();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) slab_put(z, lane, j, make_uint4(0, 0, 0, 0));
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            for (int c = c_lo; c < c_hi; c += 32) {
+              if (ti.n0 + c >= p.N) break;
+              ptx::tma_store_3d(&tmO0, z, ti.n0 + c, row0, ti.g);
+              ptx::bulk_commit();
+            }
+          }
+          __syncwarp();
         }
         continue;
       }
