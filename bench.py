@@ -271,25 +271,49 @@ def run_gpu(args, lc):
     tokens = lc.T * args.steps * world
     value = tokens / (ms_max / 1e3)
 
-    # ---- end-to-end: pinned host inputs copied in, results copied out, every step
-    x_h = inp["x"].cpu().pin_memory()
-    dy_h = inp["dy"].cpu().pin_memory()
-    y_h = torch.empty_like(x_h).pin_memory()
-    dx_h = torch.empty_like(x_h).pin_memory()
-    x_d = torch.empty_like(inp["x"])
-    dy_d = torch.empty_like(inp["dy"])
+    # ---- end-to-end: every step copies its inputs (x, dy) in from pinned host memory and its
+    # results (y, dx) out to pinned host memory.  Copies run on a second stream, double-
+    # buffered, so that step i+1's upload and step i's download overlap step i's compute.
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    x_h = [inp["x"].cpu().pin_memory() for _ in range(2)]
+    dy_h = [inp["dy"].cpu().pin_memory() for _ in range(2)]
+    y_h = [torch.empty_like(x_h[0]).pin_memory() for _ in range(2)]
+    dx_h = [torch.empty_like(x_h[0]).pin_memory() for _ in range(2)]
+    x_d = [torch.empty_like(inp["x"]) for _ in range(2)]
+    dy_d = [torch.empty_like(inp["dy"]) for _ in range(2)]
+    y_d = [torch.empty_like(inp["x"]) for _ in range(2)]
+    dx_d = [torch.empty_like(inp["x"]) for _ in range(2)]
+    copy = torch.cuda.Stream(device=dev)
+    uploaded = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    downloaded = [torch.cuda.Event() for _ in range(2)]
     barrier()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        x_d.copy_(x_h, non_blocking=True)
-        dy_d.copy_(dy_h, non_blocking=True)
-        step(x_d, dy_d, y, grads["dx"])
-        y_h.copy_(y, non_blocking=True)
-        dx_h.copy_(grads["dx"], non_blocking=True)
+    with torch.cuda.stream(copy):
+        x_d[0].copy_(x_h[0], non_blocking=True)
+        dy_d[0].copy_(dy_h[0], non_blocking=True)
+        uploaded[0].record(copy)
+    for i in range(e2e_steps):
+        b = i & 1
+        stream.wait_event(uploaded[b])
+        step(x_d[b], dy_d[b], y_d[b], dx_d[b])
+        computed[b].record(stream)
+        with torch.cuda.stream(copy):
+            if i + 1 < e2e_steps:
+                nb = b ^ 1
+                if i >= 1:
+                    copy.wait_event(downloaded[nb])   # buffers of step i-1 are out
+                x_d[nb].copy_(x_h[nb], non_blocking=True)
+                dy_d[nb].copy_(dy_h[nb], non_blocking=True)
+                uploaded[nb].record(copy)
+            copy.wait_event(computed[b])
+            y_h[b].copy_(y_d[b], non_blocking=True)
+            dx_h[b].copy_(dx_d[b], non_blocking=True)
+            downloaded[b].record(copy)
+    stream.wait_stream(copy)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
@@ -301,6 +325,7 @@ def run_gpu(args, lc):
     esz = inp["x"].element_size()
     h2d = 2 * lc.T * lc.d * esz
     d2h = 2 * lc.T * lc.d * esz if lc.backward else lc.T * lc.d * esz
+    assert torch.equal(y_h[(e2e_steps - 1) & 1].to(dev), y), "e2e output differs from the device run"
 
     if rank != 0:
         if world > 1:
@@ -431,7 +456,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=512)
     ap.add_argument("--ref-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "native" else args.warmup
     lc = moe_inputs.CONFIGS[args.workload]

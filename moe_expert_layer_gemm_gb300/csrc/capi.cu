@@ -157,6 +157,10 @@ static RouteWs carve_route(Carve& cv, const moe_cfg* c) {
   return w;
 }
 
+// Counters of the weight-gradient GEMMs' run-time tile scheduling, one 16-byte slot per launch
+// (routed fc2, routed fc1, shared fc2, shared fc1, router).
+constexpr int SCHED_SLOTS = 5;
+
 struct BwdWs {
   void* dy_perm;
   float* dgate;
@@ -168,6 +172,7 @@ struct BwdWs {
   float* dz;
   void* dx_router;
   float* part;
+  int* sched;   // tile counters of the weight-gradient GEMMs (SCHED_SLOTS slots of 4 ints)
 };
 static BwdWs carve_bwd(Carve& cv, const moe_cfg* c) {
   BwdWs w;
@@ -188,6 +193,7 @@ static BwdWs carve_bwd(Carve& cv, const moe_cfg* c) {
   w.dx_router = cv.take(T * c->d * es);
   const size_t mr = c->E + (gt ? 1 : 0);
   w.part = static_cast<float*>(cv.take(static_cast<size_t>(router_splits(c)) * mr * c->d * 4));
+  w.sched = static_cast<int*>(cv.take(SCHED_SLOTS * 4 * sizeof(int)));
   return w;
 }
 
@@ -330,7 +336,7 @@ static int ffn_fwd_impl(const moe_cfg* c, int G, const int32_t* offsets, int64_t
 static int ffn_bwd_impl(const moe_cfg* c, int G, const int32_t* offsets, int64_t rows, int f,
                         const void* x_perm, const void* W1, const void* W2, const void* act,
                         const void* h, const void* dy_perm, void* dH1, void* dx_perm, float* dW1,
-                        float* dW2, cudaStream_t st) {
+                        float* dW2, int* sched, cudaStream_t st) {
   const int d = c->d;
   const bool shared = offsets == nullptr;
   // dh = dy_perm . W2_g  (+ SwiGLU backward -> dH1 = [da | du])
@@ -367,6 +373,7 @@ static int ffn_bwd_impl(const moe_cfg* c, int G, const int32_t* offsets, int64_t
   b.out = dW2;
   b.ldo = f;
   b.out_group_stride = static_cast<int64_t>(d) * f;
+  b.tile_ctr = sched;
   MOE_TRY(gemm(c, b, st));
   // dx_perm = dH1 . W1_g
   GemmDesc e = desc0();
@@ -399,6 +406,7 @@ static int ffn_bwd_impl(const moe_cfg* c, int G, const int32_t* offsets, int64_t
   w.out = dW1;
   w.ldo = d;
   w.out_group_stride = static_cast<int64_t>(2) * f * d;
+  w.tile_ctr = sched + 4;
   return gemm(c, w, st);
 }
 
@@ -484,6 +492,7 @@ size_t moe_workspace_bytes(const moe_cfg* c, int which) {
       return 0;
     case MOE_WS_FFN_BWD:
       cv.take(static_cast<size_t>(Nrows(c)) * 2 * c->f * esize(c));
+      cv.take(2 * 4 * sizeof(int));
       break;
     case MOE_WS_LAYER_BWD:
       carve_bwd(cv, c);
@@ -574,8 +583,9 @@ int moe_grouped_swiglu_bwd(const moe_cfg* c, const void* x_perm, const int32_t* 
   }
   Carve cv(ws);
   void* dH1 = cv.take(static_cast<size_t>(Nrows(c)) * 2 * c->f * esize(c));
+  int* sched = static_cast<int*>(cv.take(2 * 4 * sizeof(int)));
   return ffn_bwd_impl(c, c->E, offsets, Nrows(c), c->f, x_perm, W1, W2, act, h, dy_perm, dH1,
-                      dx_perm, dW1, dW2, st);
+                      dx_perm, dW1, dW2, sched, st);
 }
 
 int moe_unpermute_combine(const moe_cfg* c, const void* y_perm, const float* gate,
@@ -717,11 +727,11 @@ int moe_layer_bwd(const moe_cfg* c, const void* dy, const void* x, const void* W
                              w.dshared, w.dcoef, T, d, k, st));
   // 2. routed experts (dx_perm overwrites dy_perm once it is no longer read)
   MOE_TRY(ffn_bwd_impl(c, E, s->offsets, Nrows(c), c->f, s->x_perm, W1, W2, s->act, s->h,
-                       w.dy_perm, w.dH1, w.dy_perm, dW1, dW2, st));
+                       w.dy_perm, w.dH1, w.dy_perm, dW1, dW2, w.sched, st));
   // 3. shared expert (one group of all T tokens)
   if (sh)
     MOE_TRY(ffn_bwd_impl(c, 1, nullptr, T, c->f_shared, x, Ws1, Ws2, s->s_act, s->s_h, w.dshared,
-                         w.dH1, w.dx_shared, dWs1, dWs2, st));
+                         w.dH1, w.dx_shared, dWs1, dWs2, w.sched + 8, st));
   // 4. router: dlogits (+ shared gate dz in column E)
   const int ldx = ext_cols(c);
   MOE_TRY(launch_router_bwd(c->dtype, s->logits, s->idx, s->gate, w.dgate, gt ? w.dcoef : nullptr,
@@ -757,6 +767,7 @@ int moe_layer_bwd(const moe_cfg* c, const void* dy, const void* x, const void* W
   rw.out = w.part;
   rw.ldo = d;
   rw.out_group_stride = static_cast<int64_t>(mr) * d;
+  rw.tile_ctr = w.sched + 16;
   MOE_TRY(gemm(c, rw, st));
   MOE_TRY(launch_split_reduce(w.part, S_, mr, d, dW_r, E, gt ? dw_sg : nullptr, st));
   // 7. dx = sum_j dx_perm[slot(t,j)] + dx_shared + dx_router + dz * w_sg

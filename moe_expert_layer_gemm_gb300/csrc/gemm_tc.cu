@@ -54,14 +54,40 @@ template <int SCHED, int EPI> struct OutPath {
 #ifndef MOE_MC_WGRAD
 #define MOE_MC_WGRAD 1
 #endif
+#ifndef MOE_DYN_WGRAD
+#define MOE_DYN_WGRAD 1
+#endif
 
-// Weight gradients run in clusters of two CTAs on vertically adjacent 128-row tiles of the
-// same output block: both need the same B k-block, so each loads half of it and multicasts it
-// into both CTAs' shared memory (this GPU's own memory), cutting operand traffic from L2 by a
-// third.  Each CTA keeps its own MMAs, TMEM and epilogue.
-template <int SCHED, int EPI> struct McMode {
-  static constexpr bool on = SCHED == RAGGED_K && EPI == EPI_F32 && MOE_MC_WGRAD != 0;
+// Weight gradients with tiles handed out at run time.  Every tile writes a full fp32 block, but
+// its reduction length is its expert's row count, and routing is skewed (a few experts hold most
+// rows).  A static walk gives some CTAs far more reduction work than others and leaves the GPU
+// draining a long tail.  Instead the experts are ordered by row count (most first) and each CTA
+// claims the next tile of that list from a global counter when it is ready for one: the longest
+// tiles start first and the short ones fill in behind them (longest-processing-time-first).
+template <int SCHED, int EPI> struct DynMode {
+  static constexpr bool on = SCHED == RAGGED_K && EPI == EPI_F32 && MOE_DYN_WGRAD != 0;
 };
+
+// Alternatively (static walk), weight gradients run in clusters of two CTAs on vertically
+// adjacent 128-row tiles of the same output block: both need the same B k-block, so each loads
+// half of it and multicasts it into both CTAs' shared memory (this GPU's own memory), cutting
+// operand traffic from L2 by a third.  Each CTA keeps its own MMAs, TMEM and epilogue.
+template <int SCHED, int EPI> struct McMode {
+  static constexpr bool on =
+      SCHED == RAGGED_K && EPI == EPI_F32 && MOE_MC_WGRAD != 0 && !DynMode<SCHED, EPI>::on;
+};
+
+// L2 priorities of the weight gradients: their fp32 blocks are written once and never read
+// back here, so they go out evict-first and do not push the operands (re-read by every tile of
+// an expert) out of L2; the operands may be marked evict-last.
+#ifndef MOE_WGRAD_STORE_HINT
+#define MOE_WGRAD_STORE_HINT 1
+#endif
+#ifndef MOE_WGRAD_LOAD_HINT
+#define MOE_WGRAD_LOAD_HINT 0
+#endif
+
+constexpr int FEED = 8;   // depth of the ring that passes run-time tile indices to the consumers
 
 // Staging slabs per epilogue warp: the SwiGLU backward needs two (saved a and u); with 8
 // epilogue warps the others make do with one so that the ring keeps four stages.
@@ -107,6 +133,7 @@ struct KArgs {
   const void* aux;
   int64_t ld_aux;
   const float* bias;
+  int* tile_ctr;    // run-time scheduling: the next unclaimed tile (zeroed before the launch)
   int* err;
 };
 
@@ -127,7 +154,9 @@ struct Sched {
     if (SCHED == RAGGED_M) return s_pre[p.G] * n_tiles(p);
     return p.G * ((p.M + TBM - 1) / TBM) * n_tiles(p);
   }
-  __device__ static TileInfo decode(const KArgs& p, const int* s_off, const int* s_pre, int tile) {
+  // s_ord (RAGGED_K, run-time scheduling): the groups in tile-list order; null: g ascending.
+  __device__ static TileInfo decode(const KArgs& p, const int* s_off, const int* s_pre,
+                                    const int* s_ord, int tile) {
     TileInfo ti;
     const int nt_count = n_tiles(p);
     if (SCHED == RAGGED_M) {
@@ -146,8 +175,9 @@ struct Sched {
     } else {
       const int mtc = (p.M + TBM - 1) / TBM;
       const int per = mtc * nt_count;
-      ti.g = tile / per;
-      const int r = tile - ti.g * per;
+      const int pos = tile / per;
+      const int r = tile - pos * per;
+      ti.g = s_ord ? s_ord[pos] : pos;
       const int mt = r / nt_count, nt = r - mt * nt_count;
       ti.m0 = mt * TBM;
       ti.m_end = p.M;
@@ -199,6 +229,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
   constexpr int SLABS = EpiWidth<SCHED, EPI>::slabs;
   using C = TileCfg<BN, TMA_OUT, EPI_WARPS, SLABS>;
   constexpr bool MC = McMode<SCHED, EPI>::on;
+  constexpr bool DYN = DynMode<SCHED, EPI>::on;
   using S = Sched<BN, SCHED, EPI, MC ? 2 * BM : BM>;
   constexpr int STAGES = C::STAGES;
   constexpr uint32_t STAGE_TX = A_STAGE + C::B_STAGE;
@@ -212,11 +243,15 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* epi_bar = tempty + 2;    // one per epilogue warp (TMA loads of saved activations)
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(epi_bar + EPI_WARPS);
+  uint64_t* feed_full = epi_bar + EPI_WARPS;   // run-time tile ring (DYN)
+  uint64_t* feed_empty = feed_full + FEED;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(feed_empty + FEED);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* s_bad = reinterpret_cast<int*>(tmem_holder + 2);
   int* s_off = reinterpret_cast<int*>(tmem_holder + 4);
-  int* s_pre = s_off + (MAXG + 1);
+  int* s_pre = s_off + (MAXG + 1);   // RAGGED_M: tile prefix; DYN: groups by row count
+  volatile int* s_feed = s_pre + (MAXG + 1);
+  const int* s_ord = DYN ? s_pre : nullptr;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Tile walker: one per CTA, or one per CTA pair of a cluster (rank 0 takes the upper 128 rows
@@ -240,6 +275,12 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
       ptx::mbar_init(&tempty[i], EPI_WARPS);
     }
     for (int i = 0; i < EPI_WARPS; ++i) ptx::mbar_init(&epi_bar[i], 1);
+    if (DYN) {
+      for (int i = 0; i < FEED; ++i) {
+        ptx::mbar_init(&feed_full[i], 1);
+        ptx::mbar_init(&feed_empty[i], 1 + EPI_WARPS);   // the MMA warp and every epilogue warp
+      }
+    }
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::tma_prefetch_desc(&tmA);
@@ -284,10 +325,23 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
     }
     if (lane == 31) s_pre[p.G] = incl;
   }
+  if (DYN) {
+    // groups by row count, most first (ties: lower index first)
+    for (int g = threadIdx.x; g < p.G; g += blockDim.x) {
+      const int n = s_off[g + 1] - s_off[g];
+      int rank = 0;
+      for (int h = 0; h < p.G; ++h) {
+        const int m = s_off[h + 1] - s_off[h];
+        rank += (m > n || (m == n && h < g)) ? 1 : 0;
+      }
+      s_pre[rank] = g;
+    }
+  }
   __syncthreads();
 
   const int total = S::total(p, s_pre);
-  if (unit >= total) return;   // nothing for this CTA (the same decision in both CTAs of a pair)
+  // nothing for this CTA (the same decision in both CTAs of a pair)
+  if (DYN ? total == 0 : unit >= total) return;
   // Clusters: every barrier of both CTAs is initialised before either writes into the other.
   if (MC) ptx::cluster_sync();
 
@@ -315,7 +369,10 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
         const int kk = ti.k0 + kb * BK;
         const int m_cta = ti.m0 + static_cast<int>(rank) * BM;
         auto box = [&](void* dst, const CUtensorMap* m, int c0, int c1) {
-          ptx::tma_load_2d(dst, m, &full[stg], c0, c1);
+          if (SCHED == RAGGED_K && MOE_WGRAD_LOAD_HINT)
+            ptx::tma_load_2d_hint(dst, m, &full[stg], c0, c1, ptx::policy_evict_last());
+          else
+            ptx::tma_load_2d(dst, m, &full[stg], c0, c1);
         };
         if (!A_MN) {
           box(a_dst, &tmA, kk, m_cta);
@@ -348,8 +405,30 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
           }
         }
       };
-      for (int tile = unit; tile < total && ok; tile += units) {
-        const TileInfo ti = S::decode(p, s_off, s_pre, tile);
+      // Run-time tiles: the next tile is claimed before the current one's loads are issued,
+      // hiding the atomic's latency; -1 once the list is exhausted.
+      auto claim = [&]() -> int {
+        const int t = atomicAdd(p.tile_ctr, 1);
+        return t < total ? t : -1;
+      };
+      int fslot = 0;
+      uint32_t fphase = 0;
+      int next = DYN ? claim() : unit;
+      for (int it = 0; ok; ++it) {
+        int tile;
+        if (DYN) {
+          tile = next;
+          if (!ptx::mbar_wait(&feed_empty[fslot], fphase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+          s_feed[fslot] = tile;
+          ptx::mbar_arrive(&feed_full[fslot]);
+          if (++fslot == FEED) { fslot = 0; fphase ^= 1u; }
+          if (tile < 0) break;
+          next = claim();
+        } else {
+          tile = unit + it * units;
+          if (tile >= total) break;
+        }
+        const TileInfo ti = S::decode(p, s_off, s_pre, s_ord, tile);
         for (int kb = 0; kb < ti.kblocks; ++kb) {
           if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
           ptx::mbar_arrive_expect_tx(&full[stage], STAGE_TX);
@@ -377,8 +456,22 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int tile = unit; tile < total && ok; tile += units) {
-      const TileInfo ti = S::decode(p, s_off, s_pre, tile);
+    int fslot = 0;
+    uint32_t fphase = 0;
+    for (int it = 0; ok; ++it) {
+      int tile;
+      if (DYN) {
+        if (!ptx::mbar_wait(&feed_full[fslot], fphase, abort_flag, p.err)) { ok = false; break; }
+        tile = s_feed[fslot];
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&feed_empty[fslot]);
+        if (++fslot == FEED) { fslot = 0; fphase ^= 1u; }
+        if (tile < 0) break;
+      } else {
+        tile = unit + it * units;
+        if (tile >= total) break;
+      }
+      const TileInfo ti = S::decode(p, s_off, s_pre, s_ord, tile);
       if (ti.kblocks == 0) continue;
       if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
       ptx::tc_fence_after();
@@ -444,6 +537,13 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     // Next free staging slab of this warp: at most one earlier store may still be reading.
+    // fp32 slab -> [g][row][col] (weight gradients: evict-first in L2)
+    auto store_f32 = [&](const uint8_t* src, int col, int row, int g) {
+      if (SCHED == RAGGED_K && MOE_WGRAD_STORE_HINT)
+        ptx::tma_store_3d_hint(&tmO0, src, col, row, g, ptx::policy_evict_first());
+      else
+        ptx::tma_store_3d(&tmO0, src, col, row, g);
+    };
     auto next_slab = [&]() -> uint8_t* {
       if (lane == 0) {
         if (SLABS == 2) ptx::bulk_wait_read<1>();
@@ -454,8 +554,22 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
       if (SLABS == 2) slab_sel ^= 1;
       return s;
     };
-    for (int tile = unit; tile < total; tile += units) {
-      const TileInfo ti = S::decode(p, s_off, s_pre, tile);
+    int fslot = 0;
+    uint32_t fphase = 0;
+    for (int it = 0;; ++it) {
+      int tile;
+      if (DYN) {
+        if (!ptx::mbar_wait(&feed_full[fslot], fphase, abort_flag, p.err)) break;
+        tile = s_feed[fslot];
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&feed_empty[fslot]);
+        if (++fslot == FEED) { fslot = 0; fphase ^= 1u; }
+        if (tile < 0) break;
+      } else {
+        tile = unit + it * units;
+        if (tile >= total) break;
+      }
+      const TileInfo ti = S::decode(p, s_off, s_pre, s_ord, tile);
       const int m_cta = ti.m0 + static_cast<int>(rank) * BM;   // this CTA's rows of the tile
       const int row0 = m_cta + q * 32;              // first row of this warp's slab
       const int rows_here = min(32, ti.m_end - row0);
@@ -473,7 +587,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
           if (lane == 0) {
             for (int c = c_lo; c < c_hi; c += 32) {
               if (ti.n0 + c >= p.N) break;
-              ptx::tma_store_3d(&tmO0, z, ti.n0 + c, row0, ti.g);
+              store_f32(z, ti.n0 + c, row0, ti.g);
               ptx::bulk_commit();
             }
           }
@@ -517,18 +631,41 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
           slab_store_2d(&tmO0, slab, lane, col, row0);
         }
       } else if (tma_slab && EPI == EPI_F32) {
-#pragma unroll 1
-        for (int c = c_lo; c < c_hi; c += 32) {
-          const int col = ti.n0 + c;
-          if (col >= p.N) break;
-          uint32_t v[32];
-          ptx::tmem_ld32(t_row + c, v);
-          ptx::tmem_ld_wait();
+        // 32-column chunks; the TMEM load of chunk i+1 is in flight while chunk i is staged
+        // and stored (two register sets, alternating).
+        auto put = [&](const uint32_t (&v)[32], int col) {
           uint8_t* slab = next_slab();
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             slab_put(slab, lane, j, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
-          slab_store_3d(&tmO0, slab, lane, col, row0, ti.g);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            store_f32(slab, col, row0, ti.g);
+            ptx::bulk_commit();
+          }
+        };
+        auto has = [&](int c) { return c < c_hi && ti.n0 + c < p.N; };
+        uint32_t va[32], vb[32];
+        int c = c_lo;
+        if (has(c)) {
+          ptx::tmem_ld32(t_row + c, va);
+          ptx::tmem_ld_wait(va);
+        }
+#pragma unroll 1
+        while (has(c)) {
+          const bool nb = has(c + 32);
+          if (nb) ptx::tmem_ld32(t_row + c + 32, vb);
+          put(va, ti.n0 + c);
+          if (!nb) break;
+          ptx::tmem_ld_wait(vb);
+          c += 32;
+          const bool na = has(c + 32);
+          if (na) ptx::tmem_ld32(t_row + c + 32, va);
+          put(vb, ti.n0 + c);
+          if (!na) break;
+          ptx::tmem_ld_wait(va);
+          c += 32;
         }
       } else if (tma_slab && EPI == EPI_SWIGLU_FWD) {
         // acc columns [0, BN/2) are gate, [BN/2, BN) up, for h columns n0 .. n0+BN/2
@@ -861,7 +998,18 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   a.aux = g.aux;
   a.ld_aux = g.ld_aux;
   a.bias = g.bias;
+  a.tile_ctr = g.tile_ctr;
   a.err = device_error_word();
+  if (DynMode<SCHED, EPI>::on) {
+    if (!g.tile_ctr) {
+      set_error("%s: run-time tile scheduling needs its counter (GemmDesc.tile_ctr)", name);
+      return MOE_ERR_INVALID_ARG;
+    }
+    if (cudaMemsetAsync(g.tile_ctr, 0, sizeof(int), st) != cudaSuccess) {
+      set_error("%s: clearing the tile counter failed", name);
+      return MOE_ERR_CUDA;
+    }
+  }
   if (McMode<SCHED, EPI>::on)
     return launch_clusters(name, kern, dim3(num_sms() & ~1), dim3(C::THREADS), C::SMEM, 2, st, ma,
                            mb, mo[0], mo[1], mo[2], a);

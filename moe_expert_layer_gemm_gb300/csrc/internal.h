@@ -148,6 +148,7 @@ struct GemmDesc {
   const void* aux;
   int64_t ld_aux;
   const float* bias;
+  int* tile_ctr;           // RAGGED_K (bf16): device counter for run-time tile scheduling
 };
 
 // Argument checks and the routing stages (capi.cu), for entry points defined elsewhere.
