@@ -85,6 +85,32 @@ def kernel_work(lc):
     return w
 
 
+def kernel_source_hash():
+    """sha256 over the library's kernel sources and public header (names and bytes)."""
+    import glob
+    import hashlib
+    files = sorted(glob.glob(os.path.join(ROOT, "moe_expert_layer_gemm_gb300", "csrc", "*")))
+    files.append(os.path.join(ROOT, "include", "moe_gb300.h"))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
+
+
+def captured_traffic(workload, kernel):
+    """DRAM bytes (read + write) of one launch of `kernel`, from the ncu capture summarised in
+    profiles/traffic.json; None when there is none or the kernel sources changed since."""
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(tpath):
+        return None
+    d = json.load(open(tpath))
+    if d.get("source_sha256") != kernel_source_hash():
+        return None
+    rec = d.get("workloads", {}).get(workload, {}).get(kernel)
+    return None if rec is None else rec["total"]
+
+
 def layer_flops(lc, backward=True):
     fl = 2.0 * lc.T * lc.d * lc.E + 6.0 * lc.T * lc.k * lc.d * lc.f
     if lc.f_shared:
@@ -356,12 +382,7 @@ def run_gpu(args, lc):
     if dom:
         kd = kern[dom]
         kind = work.get(dom, ("hbm", 0))[0]
-        traffic = None
-        tpath = os.path.join(ROOT, "profiles", "traffic.json")
-        if os.path.exists(tpath):
-            tr = json.load(open(tpath)).get(lc.name, {}).get(dom)
-            if tr is not None:
-                traffic = tr
+        traffic = captured_traffic(lc.name, dom)
         roof = {"bound": kind, "kernel": dom, "achieved": kd["achieved"],
                 "peak": peaks.get("bf16_tflops_sustained") if kind == "tensor" else peaks["hbm_gbs"],
                 "unit": kd["unit"], "frac": kd["frac"], "traffic": traffic,
