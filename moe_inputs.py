@@ -37,8 +37,10 @@ class LayerConfig:
     shared_gate: int = 0
     dtype: str = "bf16"        # "bf16" or "f32"
     router_init: str = "normal"  # "normal" (N(0, 0.02)) or "uniform" (U(+-1/sqrt(d)))
-    router_bias: str = "none"    # "none" or "zipf1.2"
+    router_bias: str = "none"    # "none", "zipf1.2" or "normal0.05"
     backward: bool = True
+    bias_mode: int = 0           # 0: b_r added to the logits; 1: to the scores, selection only
+    aux_coeff: float = 0.0       # load-balancing loss coefficient (0: no auxiliary loss)
 
     @property
     def N(self) -> int:
@@ -100,6 +102,13 @@ def zipf_router_bias(E: int, s: float = 1.2, seed: int = 0, device="cpu") -> tor
     return (-s * torch.log(r)).to(torch.float32).to(device)
 
 
+def normal_router_bias(E: int, std: float = 0.05, seed: int = 0, device="cpu") -> torch.Tensor:
+    """Per-expert bias ~ N(0, std^2) from its own seeded generator (an expert-bias state of the
+    size a balancing correction reaches next to sigmoid scores in (0, 1))."""
+    g = _gen(seed + 11, "cpu")
+    return (torch.randn(E, generator=g, dtype=torch.float32) * std).to(device)
+
+
 def make_layer_inputs(cfg: LayerConfig, seed: int = 0, device="cpu", T: int | None = None):
     """All tensors of one layer call, drawn from one seeded generator.
 
@@ -121,7 +130,12 @@ def make_layer_inputs(cfg: LayerConfig, seed: int = 0, device="cpu", T: int | No
         out["W_r"] = ((torch.rand(cfg.E, cfg.d, generator=g, device=device) * 2 - 1) * a).to(dt)
     else:
         out["W_r"] = randn(cfg.E, cfg.d, std=0.02)
-    out["b_r"] = zipf_router_bias(cfg.E, 1.2, seed, device) if cfg.router_bias == "zipf1.2" else None
+    if cfg.router_bias == "zipf1.2":
+        out["b_r"] = zipf_router_bias(cfg.E, 1.2, seed, device)
+    elif cfg.router_bias == "normal0.05":
+        out["b_r"] = normal_router_bias(cfg.E, 0.05, seed, device)
+    else:
+        out["b_r"] = None
     out["W1"] = randn(cfg.E, 2 * cfg.f, cfg.d, std=0.02)
     out["W2"] = randn(cfg.E, cfg.d, cfg.f, std=0.02)
     if cfg.f_shared > 0:

@@ -28,7 +28,11 @@ Readings where the pages are silent (each also listed in the design notes):
   * the gate multiplies the expert output in the combine; no biases in the experts;
   * shared gate c_t = sigmoid(w_sg . x_t), a scalar per token;
   * inside one expert's contiguous segment the tokens are in ascending token order;
-  * the router bias b_r is an input (used to make hot experts), not a trained parameter.
+  * the router bias b_r is an input, not a trained parameter: added to the logits (to make
+    hot experts) or, with the expert-bias correction, to the scores for the selection only;
+  * the load-balancing loss is coeff * E * sum_e f_e P_e (share of routed pairs times mean
+    probability), its gradient reaches the logits with the counts held fixed; the expert-bias
+    update is b_e += rate * sign(mean load - load_e).
 
 Evaluation order.  Each (token, expert) pair's FFN is independent of every other pair.  The
 oracle evaluates all pairs that picked the same expert as one matrix product whose rows are
@@ -155,6 +159,83 @@ def route(logits, k, E, score_fn, renorm):
                 token_of_slot=tos)
 
 
+# ----------------------------------------------------------------------------- router variants
+# "Megatron-Bridge 深度剖析", §Nemotron-3-Nano 配置 and its comparison with DeepSeek V3: the
+# sigmoid routing runs with an expert-bias correction (moe_router_enable_expert_bias) and a
+# load-balancing loss of coefficient 1e-4 (moe_aux_loss_coeff) that pushes the tokens to spread
+# evenly over the experts and keeps them from collapsing onto a few.  The pages name both and
+# give no formula; the readings below are the published forms they refer to.
+
+BIAS_LOGIT = 0    # b_r is added to the logits: it moves selection and gates alike
+BIAS_SELECT = 1   # b_r is added to the scores for the selection only; gates never see it
+
+
+def score_probs(logits, score_fn):
+    """Per-token distribution over all E experts read by the balancing loss:
+    softmax(l_t) for softmax routing, s_t / sum(s_t) with s = sigmoid(l_t) for sigmoid."""
+    l = f64(logits)
+    if score_fn == SOFTMAX:
+        z = np.exp(l - l.max(axis=1, keepdims=True))
+        return z / z.sum(axis=1, keepdims=True)
+    s = sigmoid(l)
+    return s / s.sum(axis=1, keepdims=True)
+
+
+def selection_keys(logits32, score_fn, e_bias):
+    """Selection keys under a selection-only expert bias: score + bias in fp32, the score being
+    the softmax over all E (softmax routing) or the sigmoid (sigmoid routing) of the fp32
+    logits.  The keys are formed in fp32 because that is the precision the choice is made in."""
+    l = np.asarray(logits32, dtype=np.float32)
+    b = np.asarray(e_bias, dtype=np.float32)[None, :]
+    if score_fn == SOFTMAX:
+        z = np.exp(l - l.max(axis=1, keepdims=True), dtype=np.float32)
+        sc = z / z.sum(axis=1, keepdims=True, dtype=np.float32)
+    else:
+        sc = np.float32(1.0) / (np.float32(1.0) + np.exp(-l, dtype=np.float32))
+    return (sc.astype(np.float32) + b).astype(np.float32)
+
+
+def aux_loss(logits, counts, k, coeff, score_fn):
+    """Load-balancing loss L = coeff * E * sum_e f_e * P_e over one batch of T tokens, where
+    f_e = counts_e / (T*k) is expert e's share of the routed (token, expert) pairs and
+    P_e = (1/T) sum_t p[t, e] its mean probability (p from score_probs).  With uniform p it is
+    exactly coeff, whatever the counts; it grows as tokens and probability pile on few experts."""
+    p = score_probs(logits, score_fn)
+    T, E = p.shape
+    f = f64(counts) / (T * k)
+    P = p.mean(axis=0)
+    return float(coeff * E * np.dot(f, P))
+
+
+def aux_loss_grad(logits, counts, k, coeff, score_fn):
+    """dL_aux/dlogits [T, E], the counts held fixed (they are piecewise constant).
+    w_e = dL/dp[t, e] = coeff * E * counts_e / (k * T^2);  G_t = sum_e p[t, e] w_e;
+      softmax: dl[t, e] = p[t, e] (w_e - G_t)
+      sigmoid: p = s / S_t, dl[t, e] = s (1 - s) (w_e - G_t) / S_t."""
+    l = f64(logits)
+    T, E = l.shape
+    w = coeff * E * f64(counts) / (k * T * T)
+    if score_fn == SOFTMAX:
+        p = score_probs(l, SOFTMAX)
+        G = p @ w
+        return p * (w[None, :] - G[:, None])
+    s = sigmoid(l)
+    S = s.sum(axis=1, keepdims=True)
+    G = (s / S) @ w
+    return s * (1.0 - s) * (w[None, :] - G[:, None]) / S
+
+
+def expert_bias_update(e_bias, counts, T, k, rate):
+    """Expert-bias correction after a step (the auxiliary-loss-free balancing of DeepSeek V3):
+    b_e <- b_e + rate * sign(T*k/E - counts_e): experts above the mean load lose selection
+    priority, those below gain it, those exactly at it keep their bias.  fp32, as stored."""
+    b = np.asarray(e_bias, dtype=np.float32)
+    E = b.shape[0]
+    mean = np.float32(T * k) / np.float32(E)
+    sgn = np.sign(mean - np.asarray(counts, dtype=np.float32)).astype(np.float32)
+    return (b + np.float32(rate) * sgn).astype(np.float32)
+
+
 def permute(x, token_of_slot):
     """x_perm[s] = x[token_of_slot[s]]: tokens regrouped into expert-contiguous rows."""
     return f64(x)[np.asarray(token_of_slot, dtype=np.int64)]
@@ -203,10 +284,12 @@ def layer_forward(cfg, inp, selection_logits32=None):
     x = f64(inp["x"])
     T = x.shape[0]
     E, k = cfg.E, cfg.k
-    l = router_logits(x, inp["W_r"], inp.get("b_r"))
+    select_bias = getattr(cfg, "bias_mode", BIAS_LOGIT) == BIAS_SELECT and inp.get("b_r") is not None
+    l = router_logits(x, inp["W_r"], None if select_bias else inp.get("b_r"))
     l32 = l.astype(np.float32) if selection_logits32 is None else np.asarray(
         selection_logits32, dtype=np.float32)
-    idx = select_topk(l32, k)
+    keys = selection_keys(l32, cfg.score_fn, inp["b_r"]) if select_bias else l32
+    idx = select_topk(keys, k)
     g = gate_weights(l, idx, cfg.score_fn, cfg.renorm)
     y = np.zeros_like(x)
     pair_out = np.zeros((T, k, x.shape[1]))
@@ -222,6 +305,11 @@ def layer_forward(cfg, inp, selection_logits32=None):
     for j in range(k):
         y += g[:, j:j + 1] * pair_out[:, j]
     out = dict(logits=l, idx=idx, gate=g, pair_out=pair_out, expert_cache=cache)
+    coeff = getattr(cfg, "aux_coeff", 0.0)
+    if coeff:
+        counts = np.bincount(idx.ravel(), minlength=E)
+        out["counts"] = counts
+        out["aux_loss"] = aux_loss(l, counts, k, coeff, cfg.score_fn)
     if cfg.f_shared > 0:
         s_out, s_a, s_u, s_h = swiglu_ffn(inp["Ws1"], inp["Ws2"], x)
         if cfg.shared_gate:
@@ -271,7 +359,8 @@ def gate_backward(logits, idx, g, dg, score_fn, renorm):
 
 
 def layer_backward(cfg, inp, fwd, dy):
-    """Gradients of L = sum(y * dy) with respect to x and every weight (fp64).
+    """Gradients of L = sum(y * dy) (+ L_aux when the configuration has a balancing-loss
+    coefficient) with respect to x and every weight (fp64).
 
     Returns dict: dx, dW_r, dW1, dW2 (+ dWs1, dWs2, dw_sg with the shared expert), and the
     intermediates dg [T, k], dlogits [T, E].
@@ -294,6 +383,9 @@ def layer_backward(cfg, inp, fwd, dy):
         dW2[e] = dW2e
         np.add.at(dx, t_list, dX)
     dl = gate_backward(fwd["logits"], idx, g, dg, cfg.score_fn, cfg.renorm)
+    coeff = getattr(cfg, "aux_coeff", 0.0)
+    if coeff:
+        dl = dl + aux_loss_grad(fwd["logits"], fwd["counts"], k, coeff, cfg.score_fn)
     dW_r = dl.T @ x
     dx += dl @ f64(inp["W_r"])
     out = dict(dx=dx, dW_r=dW_r, dW1=dW1, dW2=dW2, dg=dg, dlogits=dl)
