@@ -59,6 +59,12 @@ typedef enum moe_status {
 
 enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
 enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 };
+/* What the router bias b_r [E] does (cfg->bias_mode). */
+enum {
+  MOE_BIAS_LOGIT = 0,   /* added to the logits: moves the selection and the gates alike       */
+  MOE_BIAS_SELECT = 1   /* expert-bias correction: added to the scores (softmax over E, or
+                           sigmoid) for the selection only; the gates never see it            */
+};
 
 /* Limits checked by every entry point. */
 enum { MOE_MAX_EXPERTS = 256, MOE_MAX_TOPK = 8 };
@@ -70,13 +76,19 @@ enum { MOE_MAX_EXPERTS = 256, MOE_MAX_TOPK = 8 };
  *   f_shared   0: no shared expert.
  *   shared_gate 1: the shared expert's output is scaled by sigmoid(w_sg . x_t).
  *   dtype      MOE_DTYPE_BF16 (tensor-core path, fp32 accumulation) or MOE_DTYPE_F32
- *              (fp32 CUDA-core path, for exact-tolerance checks). */
+ *              (fp32 CUDA-core path, for exact-tolerance checks).
+ *   bias_mode  MOE_BIAS_LOGIT or MOE_BIAS_SELECT (the expert-bias correction of sigmoid
+ *              routing, "moe_router_enable_expert_bias"); see moe_route_topk.
+ *   aux_coeff  coefficient of the load-balancing loss ("moe_aux_loss_coeff", 1e-4 on the
+ *              pages); 0 disables it.  Must be finite and >= 0.  See moe_router_aux_loss. */
 typedef struct moe_cfg {
   int32_t T, d, E, k, f, f_shared;
   int32_t score_fn;
   int32_t renorm;
   int32_t shared_gate;
   int32_t dtype;
+  int32_t bias_mode;
+  float aux_coeff;
 } moe_cfg;
 
 /* Which call a workspace is sized for. */
@@ -94,16 +106,21 @@ size_t moe_workspace_bytes(const moe_cfg* cfg, int which);
 /* Router + top-k + routing maps (one GPU's stand-in for the expert-parallel dispatch plan).
  * "Megatron-Bridge 深度剖析", §Expert Parallel 基础 (Step 1, Router(x) -> TopK scores) and
  * §核心模块架构 (moe_router_topk, moe_router_score_function).
- *   x [T,d], W_r [E,d] (dtype); b_r [E] fp32 or NULL (added to the logits).
+ *   x [T,d], W_r [E,d] (dtype); b_r [E] fp32 or NULL: with MOE_BIAS_LOGIT added to the
+ *     logits; with MOE_BIAS_SELECT the expert bias of the selection (below).
  *   logits_in [T,E] fp32 or NULL: if set, the router GEMM is skipped and these logits are
- *     routed (b_r is then ignored).
- *   logits_out [T,E] fp32 or NULL: receives the router logits (x.W_r^T + b_r, fp32).
- *   Outputs: idx [T,k] int32 -- selected experts, by descending logit, equal logits -> lower
- *     expert index first; gate [T,k] fp32 -- combine weights (softmax / sigmoid, renorm per
+ *     routed (a MOE_BIAS_LOGIT b_r is then ignored; a MOE_BIAS_SELECT b_r still applies).
+ *   logits_out [T,E] fp32 or NULL: receives the router logits (x.W_r^T, + b_r with
+ *     MOE_BIAS_LOGIT, fp32).
+ *   Outputs: idx [T,k] int32 -- selected experts, by descending key, equal keys -> lower
+ *     expert index first; the key is the fp32 logit, or with MOE_BIAS_SELECT the fp32 score
+ *     plus b_r[e] (score = softmax over all E, or sigmoid, of the fp32 logits: "Megatron-
+ *     Bridge 深度剖析", §Nemotron-3-Nano 配置, sigmoid routing with expert-bias correction as
+ *     in DeepSeek V3); gate [T,k] fp32 -- combine weights (softmax / sigmoid, renorm per
  *     cfg); counts [E], offsets [E+1] int32 (offsets[0]=0, offsets[E]=N); slot_of_pair [T,k],
  *     token_of_slot [N] int32: pair (t,j) sits in row slot_of_pair[t,j] of the expert-sorted
  *     layout; inside one expert's rows the tokens ascend.
- *   Selection is made on fp32 logits and is bit-for-bit deterministic for given logits. */
+ *   Selection is made on fp32 keys and is bit-for-bit deterministic for given logits. */
 int moe_route_topk(const moe_cfg* cfg, const void* x, const void* W_r, const float* b_r,
                    const float* logits_in, float* logits_out, int32_t* idx, float* gate,
                    int32_t* counts, int32_t* offsets, int32_t* slot_of_pair,
@@ -193,12 +210,36 @@ typedef struct moe_saved {
   void* s_h;              /* [T,f_s]  dtype                                    */
   void* s_out;            /* [T,d]    dtype                                    */
   float* s_coef;          /* [T]  fp32, c_t = sigmoid(w_sg . x_t)              */
+  float* aux_loss;        /* [1]  fp32 load-balancing loss (cfg->aux_coeff > 0) */
 } moe_saved;
 
+/* Load-balancing loss of one batch: "Megatron-Bridge 深度剖析", §Nemotron-3-Nano 配置
+ * (moe_aux_loss_coeff: a loss that pushes tokens to spread evenly over the experts and keeps
+ * them from collapsing onto a few).  The pages give no formula; this is the switch-style loss
+ *   L = aux_coeff * E * sum_e f_e * P_e,  f_e = counts[e] / (T*k),  P_e = (1/T) sum_t p[t,e],
+ * with p[t,:] the softmax of the logits (softmax routing) or s/sum(s), s = sigmoid(logits)
+ * (sigmoid routing).  It equals aux_coeff when p is uniform.
+ *   logits [T,E] fp32 (as routed: with a MOE_BIAS_LOGIT bias already in them); counts [E]
+ *   from moe_route_topk; aux_loss [1] fp32 output.  Fixed-order sums: deterministic.
+ *   Workspace: MOE_WS_ROUTE.  MOE_ERR_INVALID_ARG if cfg->aux_coeff is 0. */
+int moe_router_aux_loss(const moe_cfg* cfg, const float* logits, const int32_t* counts,
+                        float* aux_loss, void* ws, size_t ws_bytes, void* stream);
+
+/* Expert-bias correction after a step (the auxiliary-loss-free balancing of DeepSeek V3 that
+ * "Megatron-Bridge 深度剖析", §Nemotron-3-Nano 配置 turns on with moe_router_enable_expert_bias):
+ *   e_bias[e] += rate * sign(T*k/E - counts[e])   (fp32; sign(0) = 0),
+ * so an expert above the mean load loses selection priority and one below gains it.
+ *   counts [E] int32 (one batch, from moe_route_topk or moe_layer_fwd's saved counts);
+ *   e_bias [E] fp32, updated in place; the b_r of a MOE_BIAS_SELECT layer.  rate finite. */
+int moe_expert_bias_update(const moe_cfg* cfg, const int32_t* counts, float* e_bias, float rate,
+                           void* stream);
+
 /* Whole layer forward: route, permute, grouped SwiGLU, shared expert, combine.
- *   x [T,d]; W_r [E,d]; b_r [E] fp32 or NULL; W1 [E,2f,d]; W2 [E,d,f];
+ *   x [T,d]; W_r [E,d]; b_r [E] fp32 or NULL (cfg->bias_mode says how it acts);
+ *   W1 [E,2f,d]; W2 [E,d,f];
  *   Ws1 [2f_s,d], Ws2 [d,f_s] (NULL without shared expert); w_sg [d] (NULL without gate).
- *   y [T,d].  `saved` receives everything the backward needs. */
+ *   y [T,d].  `saved` receives everything the backward needs, and with cfg->aux_coeff > 0
+ *   the load-balancing loss in saved->aux_loss (moe_router_aux_loss). */
 int moe_layer_fwd(const moe_cfg* cfg, const void* x, const void* W_r, const float* b_r,
                   const void* W1, const void* W2, const void* Ws1, const void* Ws2,
                   const void* w_sg, void* y, const moe_saved* saved, void* ws, size_t ws_bytes,
@@ -206,6 +247,10 @@ int moe_layer_fwd(const moe_cfg* cfg, const void* x, const void* W_r, const floa
 
 /* Whole layer backward, for the upstream gradient dy [T,d].  No gradient flows through the
  * expert selection (it is piecewise constant in the logits); b_r gets none (an input).
+ * With cfg->aux_coeff > 0 the gradient of the load-balancing loss (weight 1, counts held
+ * fixed) is added to the router's logit gradient:
+ *   w_e = aux_coeff*E*counts[e]/(k*T^2),  G_t = sum_e p[t,e] w_e,
+ *   softmax: dl[t,e] += p[t,e] (w_e - G_t);  sigmoid: dl[t,e] += s(1-s)(w_e - G_t)/sum_e s.
  *   Outputs: dx [T,d] (dtype); dW_r [E,d], dW1 [E,2f,d], dW2 [E,d,f], dWs1 [2f_s,d],
  *   dWs2 [d,f_s], dw_sg [d] -- all fp32 (the shared ones NULL when absent). */
 int moe_layer_bwd(const moe_cfg* cfg, const void* dy, const void* x, const void* W_r,

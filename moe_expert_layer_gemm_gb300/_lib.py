@@ -21,18 +21,20 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3:
           -4: "MOE_ERR_ALIGNMENT", -5: "MOE_ERR_CUDA", -6: "MOE_ERR_DEVICE_CHECK"}
 SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 DTYPE_BF16, DTYPE_F32 = 0, 1
+BIAS_LOGIT, BIAS_SELECT = 0, 1
 WS_ROUTE, WS_FFN_FWD, WS_FFN_BWD, WS_LAYER_FWD, WS_LAYER_BWD = range(5)
 
 
 class MoeCfg(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("T", "d", "E", "k", "f", "f_shared", "score_fn", "renorm", "shared_gate", "dtype")]
+                ("T", "d", "E", "k", "f", "f_shared", "score_fn", "renorm", "shared_gate", "dtype",
+                 "bias_mode")] + [("aux_coeff", ctypes.c_float)]
 
 
 class MoeSaved(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("logits", "idx", "gate", "counts", "offsets", "slot_of_pair", "token_of_slot",
-                 "x_perm", "act", "h", "y_perm", "s_act", "s_h", "s_out", "s_coef")]
+                 "x_perm", "act", "h", "y_perm", "s_act", "s_h", "s_out", "s_coef", "aux_loss")]
 
 
 _VP = ctypes.c_void_p
@@ -50,6 +52,8 @@ _SIGS = {
     "moe_layer_fwd": (ctypes.c_int, [_CFG] + [_VP] * 9 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP]),
     "moe_layer_bwd": (ctypes.c_int, [_CFG] + [_VP] * 8 + [ctypes.POINTER(MoeSaved)] + [_VP] * 8
                       + [_SZ, _VP]),
+    "moe_router_aux_loss": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "moe_expert_bias_update": (ctypes.c_int, [_CFG, _VP, _VP, ctypes.c_float, _VP]),
     "moe_last_error": (ctypes.c_char_p, []),
     "moe_check_device_error": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_int32)]),
     "moe_launch_count": (ctypes.c_uint64, []),
@@ -91,14 +95,17 @@ def _check(rc, what):
         raise RuntimeError(f"{what}: {STATUS.get(rc, rc)}: {msg}")
 
 
-def make_cfg(T, d, E, k, f, f_shared=0, score_fn=0, renorm=1, shared_gate=0, dtype=DTYPE_BF16):
-    return MoeCfg(T, d, E, k, f, f_shared, score_fn, renorm, shared_gate, dtype)
+def make_cfg(T, d, E, k, f, f_shared=0, score_fn=0, renorm=1, shared_gate=0, dtype=DTYPE_BF16,
+             bias_mode=BIAS_LOGIT, aux_coeff=0.0):
+    return MoeCfg(T, d, E, k, f, f_shared, score_fn, renorm, shared_gate, dtype, bias_mode,
+                  aux_coeff)
 
 
 def cfg_from(lc, T=None):
     """MoeCfg from a moe_inputs.LayerConfig-like object."""
     return make_cfg(lc.T if T is None else T, lc.d, lc.E, lc.k, lc.f, lc.f_shared, lc.score_fn,
-                    lc.renorm, lc.shared_gate, DTYPE_BF16 if lc.dtype == "bf16" else DTYPE_F32)
+                    lc.renorm, lc.shared_gate, DTYPE_BF16 if lc.dtype == "bf16" else DTYPE_F32,
+                    getattr(lc, "bias_mode", BIAS_LOGIT), getattr(lc, "aux_coeff", 0.0))
 
 
 def _p(t):
@@ -175,6 +182,17 @@ def moe_unpermute_combine_bwd(cfg, dy, y_perm, gate, slot_of_pair, shared_out, s
                                            _stream(stream)), "moe_unpermute_combine_bwd")
 
 
+def moe_router_aux_loss(cfg, logits, counts, aux_loss, ws, stream=None):
+    _check(lib().moe_router_aux_loss(ctypes.byref(cfg), _p(logits), _p(counts), _p(aux_loss),
+                                     _p(ws), 0 if ws is None else ws.numel(), _stream(stream)),
+           "moe_router_aux_loss")
+
+
+def moe_expert_bias_update(cfg, counts, e_bias, rate, stream=None):
+    _check(lib().moe_expert_bias_update(ctypes.byref(cfg), _p(counts), _p(e_bias), float(rate),
+                                        _stream(stream)), "moe_expert_bias_update")
+
+
 # ----------------------------------------------------------------------------- whole layer
 
 SAVED_FIELDS = [f for f, _ in MoeSaved._fields_]
@@ -203,6 +221,7 @@ def alloc_saved(cfg, device="cuda"):
         s_h=torch.empty(T, fs, dtype=dt, device=device) if fs else None,
         s_out=torch.empty(T, d, dtype=dt, device=device) if fs else None,
         s_coef=torch.empty(T, dtype=f32, device=device) if cfg.shared_gate else None,
+        aux_loss=torch.empty(4, dtype=f32, device=device) if cfg.aux_coeff > 0 else None,
     )
     return s
 

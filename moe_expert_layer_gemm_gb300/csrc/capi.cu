@@ -147,6 +147,7 @@ struct RouteWs {
   int32_t* hist;
   int32_t* base;
   float* logits;
+  float* aux;   // balancing-loss partial sums [route_blocks(T)][E]
 };
 static RouteWs carve_route(Carve& cv, const moe_cfg* c) {
   RouteWs w;
@@ -154,6 +155,7 @@ static RouteWs carve_route(Carve& cv, const moe_cfg* c) {
   w.hist = static_cast<int32_t*>(cv.take(nb * 4));
   w.base = static_cast<int32_t*>(cv.take(nb * 4));
   w.logits = static_cast<float*>(cv.take(static_cast<size_t>(c->T) * c->E * 4));
+  w.aux = static_cast<float*>(cv.take(nb * 4));
   return w;
 }
 
@@ -214,6 +216,10 @@ static int check_cfg(const moe_cfg* c) {
     return fail(MOE_ERR_INVALID_ARG, "shared_gate needs a shared expert (f_shared > 0)");
   if (c->dtype != MOE_DTYPE_BF16 && c->dtype != MOE_DTYPE_F32)
     return fail(MOE_ERR_INVALID_ARG, "dtype=%d", c->dtype);
+  if (c->bias_mode != MOE_BIAS_LOGIT && c->bias_mode != MOE_BIAS_SELECT)
+    return fail(MOE_ERR_INVALID_ARG, "bias_mode=%d", c->bias_mode);
+  if (!(c->aux_coeff >= 0.0f) || c->aux_coeff > 3.0e38f)
+    return fail(MOE_ERR_INVALID_ARG, "aux_coeff must be finite and >= 0");
   const int mult = c->dtype == MOE_DTYPE_BF16 ? 8 : 4;
   if (c->d % mult || c->f % mult || c->f_shared % mult)
     return fail(MOE_ERR_UNSUPPORTED, "d, f and f_shared must be multiples of %d (16-byte rows)", mult);
@@ -264,6 +270,9 @@ static int route_impl(const moe_cfg* c, const void* x, const void* W_r, const fl
                       const float* logits_in, float* logits_out, int32_t* idx, float* gate,
                       int32_t* counts, int32_t* offsets, int32_t* sop, int32_t* tos,
                       const RouteWs& w, cudaStream_t st) {
+  // MOE_BIAS_LOGIT: b_r enters the logits (router GEMM epilogue); MOE_BIAS_SELECT: it is the
+  // selection-only expert bias of the top-k.
+  const bool select_bias = c->bias_mode == MOE_BIAS_SELECT;
   const float* logits = logits_in;
   if (!logits) {
     float* dst = logits_out ? logits_out : w.logits;
@@ -279,11 +288,12 @@ static int route_impl(const moe_cfg* c, const void* x, const void* W_r, const fl
     g.B = opnd(W_r, c->E, c->d, false);
     g.out = dst;
     g.ldo = c->E;
-    g.bias = b_r;
+    g.bias = select_bias ? nullptr : b_r;
     MOE_TRY(gemm(c, g, st));
     logits = dst;
   }
-  MOE_TRY(launch_topk(logits, c->T, c->E, c->k, c->score_fn, c->renorm, idx, gate, w.hist, st));
+  MOE_TRY(launch_topk(logits, c->T, c->E, c->k, c->score_fn, c->renorm,
+                      select_bias ? b_r : nullptr, idx, gate, w.hist, st));
   MOE_TRY(launch_scan(w.hist, c->E, route_blocks(c->T), w.base, counts, offsets, st));
   MOE_TRY(launch_slots(idx, c->T, c->k, c->E, w.base, sop, tos, st));
   return MOE_OK;
@@ -417,7 +427,7 @@ using namespace moe;
 // ====================================================================== C ABI
 extern "C" {
 
-int moe_version(void) { return 100; }
+int moe_version(void) { return 101; }
 
 const char* moe_last_error(void) { return g_errbuf; }
 
@@ -622,6 +632,35 @@ int moe_unpermute_combine_bwd(const moe_cfg* c, const void* dy, const void* y_pe
                             c->k, S(stream));
 }
 
+int moe_router_aux_loss(const moe_cfg* c, const float* logits, const int32_t* counts,
+                        float* aux_loss, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(c));
+  if (!(c->aux_coeff > 0.0f)) return fail(MOE_ERR_INVALID_ARG, "aux_coeff is 0: no loss to compute");
+  MOE_TRY(check_ptr(logits, "logits", true));
+  MOE_TRY(check_ptr(counts, "counts", true));
+  MOE_TRY(check_ptr(aux_loss, "aux_loss", true));
+  MOE_TRY(check_ws(c, MOE_WS_ROUTE, ws, ws_bytes));
+  cudaStream_t st = S(stream);
+  if (c->T == 0)
+    return cudaMemsetAsync(aux_loss, 0, sizeof(float), st) == cudaSuccess
+               ? MOE_OK : fail(MOE_ERR_CUDA, "cudaMemsetAsync failed");
+  Carve cv(ws);
+  RouteWs w = carve_route(cv, c);
+  return launch_aux_loss(logits, counts, c->T, c->E, c->k, c->score_fn, c->aux_coeff, w.aux,
+                         aux_loss, st);
+}
+
+int moe_expert_bias_update(const moe_cfg* c, const int32_t* counts, float* e_bias, float rate,
+                           void* stream) {
+  MOE_TRY(check_cfg(c));
+  MOE_TRY(check_ptr(counts, "counts", true));
+  MOE_TRY(check_ptr(e_bias, "e_bias", true));
+  if (!(rate == rate) || rate > 3.0e38f || rate < -3.0e38f)
+    return fail(MOE_ERR_INVALID_ARG, "rate must be finite");
+  if (c->T == 0) return MOE_OK;   // no batch: no load to correct
+  return launch_bias_update(counts, e_bias, c->T, c->k, c->E, rate, S(stream));
+}
+
 static int check_saved(const moe_cfg* c, const moe_saved* s) {
   if (!s) return fail(MOE_ERR_INVALID_ARG, "saved is NULL");
   MOE_TRY(check_ptr(s->logits, "saved.logits", true));
@@ -640,6 +679,7 @@ static int check_saved(const moe_cfg* c, const moe_saved* s) {
   MOE_TRY(check_ptr(s->s_h, "saved.s_h", sh));
   MOE_TRY(check_ptr(s->s_out, "saved.s_out", sh));
   MOE_TRY(check_ptr(s->s_coef, "saved.s_coef", c->shared_gate != 0));
+  MOE_TRY(check_ptr(s->aux_loss, "saved.aux_loss", c->aux_coeff > 0.0f));
   return MOE_OK;
 }
 
@@ -663,7 +703,8 @@ int moe_layer_fwd(const moe_cfg* c, const void* x, const void* W_r, const float*
   cudaStream_t st = S(stream);
   if (c->T == 0) {
     if (cudaMemsetAsync(s->counts, 0, sizeof(int32_t) * c->E, st) != cudaSuccess ||
-        cudaMemsetAsync(s->offsets, 0, sizeof(int32_t) * (c->E + 1), st) != cudaSuccess)
+        cudaMemsetAsync(s->offsets, 0, sizeof(int32_t) * (c->E + 1), st) != cudaSuccess ||
+        (c->aux_coeff > 0.0f && cudaMemsetAsync(s->aux_loss, 0, sizeof(float), st) != cudaSuccess))
       return fail(MOE_ERR_CUDA, "cudaMemsetAsync failed");
     return MOE_OK;
   }
@@ -671,6 +712,9 @@ int moe_layer_fwd(const moe_cfg* c, const void* x, const void* W_r, const float*
   RouteWs w = carve_route(cv, c);
   MOE_TRY(route_impl(c, x, W_r, b_r, nullptr, s->logits, s->idx, s->gate, s->counts, s->offsets,
                      s->slot_of_pair, s->token_of_slot, w, st));
+  if (c->aux_coeff > 0.0f)
+    MOE_TRY(launch_aux_loss(s->logits, s->counts, c->T, c->E, c->k, c->score_fn, c->aux_coeff,
+                            w.aux, s->aux_loss, st));
   MOE_TRY(launch_permute(c->dtype, x, s->slot_of_pair, s->x_perm, c->T, c->d, c->k, st));
   MOE_TRY(ffn_fwd_impl(c, c->E, s->offsets, Nrows(c), c->f, s->x_perm, W1, W2, s->h, s->act,
                        s->y_perm, st));
@@ -734,9 +778,13 @@ int moe_layer_bwd(const moe_cfg* c, const void* dy, const void* x, const void* W
                          w.dH1, w.dx_shared, dWs1, dWs2, w.sched + 8, st));
   // 4. router: dlogits (+ shared gate dz in column E)
   const int ldx = ext_cols(c);
+  const bool aux = c->aux_coeff > 0.0f;
+  const float aux_w = aux ? static_cast<float>(static_cast<double>(c->aux_coeff) * E /
+                                               (static_cast<double>(k) * T * T))
+                          : 0.0f;
   MOE_TRY(launch_router_bwd(c->dtype, s->logits, s->idx, s->gate, w.dgate, gt ? w.dcoef : nullptr,
                             gt ? s->s_coef : nullptr, w.dl_ext, w.dz, T, E, k, ldx, c->score_fn,
-                            c->renorm, st));
+                            c->renorm, aux ? s->counts : nullptr, aux_w, st));
   // 5. dx_router = dlogits . W_r
   GemmDesc rd = desc0();
   rd.name = "gemm_router_dgrad";
@@ -794,6 +842,7 @@ int route_stages(const moe_cfg* c, const void* x, const void* W_r, const float* 
   w.hist = hist;
   w.base = base;
   w.logits = nullptr;
+  w.aux = nullptr;
   return route_impl(c, x, W_r, b_r, logits_in, logits_out, idx, gate, counts, offsets,
                     slot_of_pair, token_of_slot, w, st);
 }

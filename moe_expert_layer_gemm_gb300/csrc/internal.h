@@ -75,8 +75,14 @@ int launch_clusters(const char* name, void (*kern)(KArgs...), dim3 grid, dim3 bl
 constexpr int ROUTE_TOK_PER_BLOCK = 256;
 inline int route_blocks(int T) { return (T + ROUTE_TOK_PER_BLOCK - 1) / ROUTE_TOK_PER_BLOCK; }
 
-int launch_topk(const float* logits, int T, int E, int k, int score_fn, int renorm, int32_t* idx,
-                float* gate, int32_t* hist, cudaStream_t st);
+// sel_bias: selection-only expert bias [E] (keys = score + bias) or null (keys = logits).
+int launch_topk(const float* logits, int T, int E, int k, int score_fn, int renorm,
+                const float* sel_bias, int32_t* idx, float* gate, int32_t* hist, cudaStream_t st);
+// Load-balancing loss; partial: route_blocks(T) * E floats of scratch.
+int launch_aux_loss(const float* logits, const int32_t* counts, int T, int E, int k, int score_fn,
+                    float coeff, float* partial, float* out, cudaStream_t st);
+int launch_bias_update(const int32_t* counts, float* bias, int T, int k, int E, float rate,
+                       cudaStream_t st);
 int launch_scan(const int32_t* hist, int E, int nblk, int32_t* base, int32_t* counts,
                 int32_t* offsets, cudaStream_t st);
 int launch_slots(const int32_t* idx, int T, int k, int E, const int32_t* base,
@@ -100,7 +106,7 @@ int launch_shared_gate(int dtype, const void* x, const void* w_sg, float* coef, 
 int launch_router_bwd(int dtype, const float* logits, const int32_t* idx, const float* gate,
                       const float* dgate, const float* dcoef, const float* coef, void* dl_ext,
                       float* dz, int T, int E, int k, int ld_ext, int score_fn, int renorm,
-                      cudaStream_t st);
+                      const int32_t* aux_counts, float aux_w, cudaStream_t st);
 int launch_split_reduce(const float* part, int S, int rows, int cols, float* out_main,
                         int main_rows, float* out_extra, cudaStream_t st);
 

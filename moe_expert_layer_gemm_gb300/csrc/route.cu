@@ -8,7 +8,10 @@
 //
 // Four launches:
 //   topk  -- one warp per token (grid-stride over all tokens): k rounds of a warp-wide argmax
-//            over fp32 logits (ties -> lower expert index), gates in fp32.
+//            over fp32 keys (ties -> lower expert index), gates in fp32.  The key is the logit,
+//            or, with a selection-only expert bias ("Megatron-Bridge 深度剖析",
+//            §Nemotron-3-Nano 配置: sigmoid routing with expert-bias correction as in DeepSeek
+//            V3), the fp32 score (softmax over E, or sigmoid) plus the expert's bias.
 //   hist  -- one block per 256 tokens: per-expert counts of the block, hist[e][block].
 //   scan  -- one block: exclusive prefix over hist in expert-major order gives, for every
 //            (expert, block), the first slot of that block's tokens of that expert.
@@ -40,18 +43,53 @@ __device__ __forceinline__ void load_logit_row(const float* __restrict__ logits,
 template <int EPL>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E,
                                                    int k, int score_fn, int renorm,
+                                                   const float* __restrict__ sel_bias,
                                                    int32_t* __restrict__ idx,
                                                    float* __restrict__ gate) {
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
-  float cur[EPL], nxt[EPL];
+  float cur[EPL], nxt[EPL], bias[EPL];
   load_logit_row<EPL>(logits, gw, T, E, lane, cur);
+#pragma unroll
+  for (int q = 0; q < EPL; ++q) {
+    const int e = q * 32 + lane;
+    bias[q] = (sel_bias && e < E) ? __ldg(sel_bias + e) : 0.f;
+  }
 
   for (int t = gw; t < T; t += nw) {
     load_logit_row<EPL>(logits, t + nw, T, E, lane, nxt);   // next token's row in flight
 
-    // ---- selection: k rounds of warp argmax, key (logit desc, expert asc)
+    // ---- selection keys: the logits, or score + expert bias (row max kept for the gates)
+    float key[EPL];
+    float rmax = NEG_INF;
+    if (sel_bias) {
+      if (score_fn == MOE_SCORE_SOFTMAX) {
+#pragma unroll
+        for (int q = 0; q < EPL; ++q) rmax = fmaxf(rmax, cur[q]);
+        rmax = warp_max(rmax);
+        float ex[EPL], part = 0.f;
+#pragma unroll
+        for (int q = 0; q < EPL; ++q) {
+          ex[q] = (q * 32 + lane < E) ? expf(cur[q] - rmax) : 0.f;
+          part += ex[q];
+        }
+        const float z = warp_sum(part);
+#pragma unroll
+        for (int q = 0; q < EPL; ++q)
+          key[q] = (q * 32 + lane < E) ? ex[q] / z + bias[q] : NEG_INF;
+      } else {
+#pragma unroll
+        for (int q = 0; q < EPL; ++q)
+          key[q] = (q * 32 + lane < E) ? sigmoid_f(cur[q]) + bias[q] : NEG_INF;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < EPL; ++q) key[q] = cur[q];
+    }
+
+    // ---- selection: k rounds of warp argmax, order (key desc, expert asc); the selected
+    // experts' logits travel with them for the gates
     uint32_t taken = 0u;
     float sel_v[MAXK];
     int sel_e[MAXK];
@@ -60,26 +98,29 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
       sel_v[j] = NEG_INF;
       sel_e[j] = 0;
       if (j < k) {
-        float bv = NEG_INF;
+        float bv = NEG_INF, bl = NEG_INF;
         int be = INT_MAX;
 #pragma unroll
         for (int q = 0; q < EPL; ++q) {
           const int e = q * 32 + lane;
-          if (!((taken >> q) & 1u) && e < E && (cur[q] > bv || (cur[q] == bv && e < be))) {
-            bv = cur[q];
+          if (!((taken >> q) & 1u) && e < E && (key[q] > bv || (key[q] == bv && e < be))) {
+            bv = key[q];
             be = e;
+            bl = cur[q];
           }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
           const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
           const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+          const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
           if (ov > bv || (ov == bv && oe < be)) {
             bv = ov;
             be = oe;
+            bl = ol;
           }
         }
-        sel_v[j] = bv;
+        sel_v[j] = bl;
         sel_e[j] = be;
         if ((be & 31) == lane) taken |= 1u << (be >> 5);
       }
@@ -88,7 +129,18 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     // ---- gates (fp32)
     float g[MAXK];
     if (score_fn == MOE_SCORE_SOFTMAX) {
-      const float m = sel_v[0];   // the top-1 logit is the row maximum
+      // shift: the row maximum (over all E without renorm, over the selected with it); without
+      // a selection bias the top-1 logit is both
+      float m = sel_v[0];
+      if (sel_bias) {
+        if (renorm) {
+#pragma unroll
+          for (int j = 1; j < MAXK; ++j)
+            if (j < k) m = fmaxf(m, sel_v[j]);
+        } else {
+          m = rmax;
+        }
+      }
       float denom = 0.f;
       if (renorm) {
 #pragma unroll
@@ -245,8 +297,120 @@ __global__ void __launch_bounds__(256) slots_kernel(const int32_t* __restrict__ 
   }
 }
 
-int launch_topk(const float* logits, int T, int E, int k, int score_fn, int renorm, int32_t* idx,
-                float* gate, int32_t* hist, cudaStream_t st) {
+// ----------------------------------------------------------------------------- balancing loss
+// "Megatron-Bridge 深度剖析", §Nemotron-3-Nano 配置 (moe_aux_loss_coeff): the load-balancing loss
+//   L = coeff * E / (k * T^2) * sum_e counts[e] * sum_t p[t, e],
+// p[t,:] = softmax(l_t) (softmax routing) or s / sum(s), s = sigmoid(l_t) (sigmoid routing).
+// Two launches: per-256-token-block column sums of p (each warp sums its tokens in order, the
+// block adds its 8 warps in order), then one block adds the blocks in order and takes the dot
+// with the counts in fp64.  Fixed order throughout: bit-identical reruns.
+template <int EPL>
+__global__ void __launch_bounds__(256) aux_partial_kernel(const float* __restrict__ logits, int T,
+                                                          int E, int score_fn,
+                                                          float* __restrict__ partial) {
+  __shared__ float wsum[8][MOE_MAX_EXPERTS];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float acc[EPL];
+#pragma unroll
+  for (int q = 0; q < EPL; ++q) acc[q] = 0.f;
+  const int t0 = blockIdx.x * TPB;
+  for (int i = warp; i < TPB && t0 + i < T; i += 8) {
+    float v[EPL];
+    load_logit_row<EPL>(logits, t0 + i, T, E, lane, v);
+    float p[EPL], part = 0.f;
+    if (score_fn == MOE_SCORE_SOFTMAX) {
+      float m = NEG_INF;
+#pragma unroll
+      for (int q = 0; q < EPL; ++q) m = fmaxf(m, v[q]);
+      m = warp_max(m);
+#pragma unroll
+      for (int q = 0; q < EPL; ++q) {
+        p[q] = (q * 32 + lane < E) ? expf(v[q] - m) : 0.f;
+        part += p[q];
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < EPL; ++q) {
+        p[q] = (q * 32 + lane < E) ? sigmoid_f(v[q]) : 0.f;
+        part += p[q];
+      }
+    }
+    const float z = warp_sum(part);
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) acc[q] += p[q] / z;
+  }
+#pragma unroll
+  for (int q = 0; q < EPL; ++q)
+    if (q * 32 + lane < E) wsum[warp][q * 32 + lane] = acc[q];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sum += wsum[w][e];
+    partial[static_cast<int64_t>(blockIdx.x) * E + e] = sum;
+  }
+}
+
+__global__ void __launch_bounds__(256) aux_finish_kernel(const float* __restrict__ partial, int nblk,
+                                                         int E, const int32_t* __restrict__ counts,
+                                                         double scale, float* __restrict__ out) {
+  __shared__ double red[256];
+  const int tid = threadIdx.x;
+  double v = 0.0;
+  for (int e = tid; e < E; e += blockDim.x) {
+    double col = 0.0;
+    for (int b = 0; b < nblk; ++b) col += partial[static_cast<int64_t>(b) * E + e];
+    v += col * static_cast<double>(counts[e]);
+  }
+  red[tid] = v;
+  __syncthreads();
+  for (int h = blockDim.x / 2; h > 0; h >>= 1) {
+    if (tid < h) red[tid] += red[tid + h];
+    __syncthreads();
+  }
+  if (tid == 0) out[0] = static_cast<float>(scale * red[0]);
+}
+
+int launch_aux_loss(const float* logits, const int32_t* counts, int T, int E, int k, int score_fn,
+                    float coeff, float* partial, float* out, cudaStream_t st) {
+  const int nblk = route_blocks(T);
+  const dim3 grid(nblk), block(256);
+  int rc;
+  if (E <= 32)
+    rc = launch("aux_partial", aux_partial_kernel<1>, grid, block, 0, st, logits, T, E, score_fn, partial);
+  else if (E <= 64)
+    rc = launch("aux_partial", aux_partial_kernel<2>, grid, block, 0, st, logits, T, E, score_fn, partial);
+  else if (E <= 128)
+    rc = launch("aux_partial", aux_partial_kernel<4>, grid, block, 0, st, logits, T, E, score_fn, partial);
+  else
+    rc = launch("aux_partial", aux_partial_kernel<8>, grid, block, 0, st, logits, T, E, score_fn, partial);
+  MOE_TRY(rc);
+  const double scale = static_cast<double>(coeff) * E / (static_cast<double>(k) * T * T);
+  return launch("aux_finish", aux_finish_kernel, dim3(1), dim3(256), 0, st, partial, nblk, E,
+                counts, scale, out);
+}
+
+// ----------------------------------------------------------------------------- expert bias
+// The expert-bias correction after a step (DeepSeek V3's auxiliary-loss-free balancing):
+//   b[e] += rate * sign(mean - counts[e]),  mean = T*k / E (fp32).
+__global__ void bias_update_kernel(const int32_t* __restrict__ counts, float* __restrict__ bias,
+                                   int E, float mean, float rate) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  const float dlt = mean - static_cast<float>(counts[e]);
+  const float sg = dlt > 0.f ? 1.f : (dlt < 0.f ? -1.f : 0.f);
+  bias[e] = bias[e] + rate * sg;
+}
+
+int launch_bias_update(const int32_t* counts, float* bias, int T, int k, int E, float rate,
+                       cudaStream_t st) {
+  const float mean = static_cast<float>(static_cast<int64_t>(T) * k) / static_cast<float>(E);
+  return launch("expert_bias_update", bias_update_kernel, dim3((E + 255) / 256), dim3(256), 0, st,
+                counts, bias, E, mean, rate);
+}
+
+int launch_topk(const float* logits, int T, int E, int k, int score_fn, int renorm,
+                const float* sel_bias, int32_t* idx, float* gate, int32_t* hist, cudaStream_t st) {
   const int nblk = route_blocks(T);
   int blocks = (T + 7) / 8;   // 8 warps per block, one token per warp at a time
   if (blocks > num_sms() * 8) blocks = num_sms() * 8;
@@ -254,16 +418,16 @@ int launch_topk(const float* logits, int T, int E, int k, int score_fn, int reno
   int rc;
   if (E <= 32)
     rc = launch("route_topk", topk_kernel<1>, grid, block, 0, st, logits, T, E, k, score_fn, renorm,
-                idx, gate);
+                sel_bias, idx, gate);
   else if (E <= 64)
     rc = launch("route_topk", topk_kernel<2>, grid, block, 0, st, logits, T, E, k, score_fn, renorm,
-                idx, gate);
+                sel_bias, idx, gate);
   else if (E <= 128)
     rc = launch("route_topk", topk_kernel<4>, grid, block, 0, st, logits, T, E, k, score_fn, renorm,
-                idx, gate);
+                sel_bias, idx, gate);
   else
     rc = launch("route_topk", topk_kernel<8>, grid, block, 0, st, logits, T, E, k, score_fn, renorm,
-                idx, gate);
+                sel_bias, idx, gate);
   MOE_TRY(rc);
   return launch("route_hist", hist_kernel, dim3(nblk), dim3(TPB), 0, st, idx, T, k, E, hist, nblk,
                 device_error_word());

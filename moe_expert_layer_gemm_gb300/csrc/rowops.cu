@@ -341,7 +341,8 @@ __global__ void __launch_bounds__(ROW_THREADS) router_bwd_kernel(
     const float* __restrict__ logits, const int32_t* __restrict__ idx,
     const float* __restrict__ gate, const float* __restrict__ dgate,
     const float* __restrict__ dcoef, const float* __restrict__ coef, T* __restrict__ dl_ext,
-    float* __restrict__ dz, int Tn, int E, int k, int ld_ext, int score_fn, int renorm, int* err) {
+    float* __restrict__ dz, int Tn, int E, int k, int ld_ext, int score_fn, int renorm,
+    const int32_t* __restrict__ aux_counts, float aux_w, int* err) {
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
@@ -377,12 +378,36 @@ __global__ void __launch_bounds__(ROW_THREADS) router_bwd_kernel(
         ssum += sel_s[j];
       }
     }
+    // softmax over all E (no renorm, or the balancing loss): row maximum and normaliser
     float m = 0.f, denom = 1.f;
-    if (score_fn == MOE_SCORE_SOFTMAX && !renorm) {
-      m = lrow[sel_e[0]];   // top-1 logit = row maximum
+    const bool full_softmax = score_fn == MOE_SCORE_SOFTMAX && (!renorm || aux_counts);
+    if (full_softmax) {
+      float mx = __int_as_float(0xff800000u);
+      for (int e = lane; e < E; e += 32) mx = fmaxf(mx, lrow[e]);
+      m = warp_max(mx);
       float part = 0.f;
       for (int e = lane; e < E; e += 32) part += expf(lrow[e] - m);
       denom = warp_sum(part);
+    }
+    // Balancing loss (counts held fixed): w_e = aux_w * counts[e] = dL/dp[t,e],
+    // G = sum_e p[t,e] w_e;  softmax: dl_e += p_e (w_e - G);
+    // sigmoid (p = s / S): dl_e += s_e (1 - s_e) (w_e - G) / S.
+    float aux_G = 0.f, aux_S = 1.f;
+    if (aux_counts) {
+      float pw = 0.f, ps = 0.f;
+      for (int e = lane; e < E; e += 32) {
+        const float w = aux_w * static_cast<float>(aux_counts[e]);
+        const float v = score_fn == MOE_SCORE_SOFTMAX ? expf(lrow[e] - m) : sigmoid_f(lrow[e]);
+        pw = fmaf(v, w, pw);
+        ps += v;
+      }
+      pw = warp_sum(pw);
+      if (score_fn == MOE_SCORE_SOFTMAX) {
+        aux_G = pw / denom;
+      } else {
+        aux_S = warp_sum(ps);
+        aux_G = pw / aux_S;
+      }
     }
     float dzt = 0.f;
     if (dcoef) {
@@ -415,6 +440,15 @@ __global__ void __launch_bounds__(ROW_THREADS) router_bwd_kernel(
           }
         } else if (jsel >= 0) {
           val = renorm ? (dgj - inner) * sj * (1.0f - sj) / ssum : dgj * sj * (1.0f - sj);
+        }
+        if (aux_counts) {
+          const float w = aux_w * static_cast<float>(aux_counts[col]);
+          if (score_fn == MOE_SCORE_SOFTMAX) {
+            val += expf(lrow[col] - m) / denom * (w - aux_G);
+          } else {
+            const float sc = sigmoid_f(lrow[col]);
+            val += sc * (1.0f - sc) * (w - aux_G) / aux_S;
+          }
         }
       } else if (col == E && dcoef) {
         val = dzt;
@@ -503,14 +537,14 @@ int launch_shared_gate(int dtype, const void* x, const void* w_sg, float* coef, 
 int launch_router_bwd(int dtype, const float* logits, const int32_t* idx, const float* gate,
                       const float* dgate, const float* dcoef, const float* coef, void* dl_ext,
                       float* dz, int T, int E, int k, int ld_ext, int score_fn, int renorm,
-                      cudaStream_t st) {
+                      const int32_t* aux_counts, float aux_w, cudaStream_t st) {
   if (dtype == MOE_DTYPE_BF16)
     return launch("router_bwd", router_bwd_kernel<bf16>, row_grid(T), dim3(ROW_THREADS), 0, st,
                   logits, idx, gate, dgate, dcoef, coef, (bf16*)dl_ext, dz, T, E, k, ld_ext,
-                  score_fn, renorm, device_error_word());
+                  score_fn, renorm, aux_counts, aux_w, device_error_word());
   return launch("router_bwd", router_bwd_kernel<float>, row_grid(T), dim3(ROW_THREADS), 0, st,
                 logits, idx, gate, dgate, dcoef, coef, (float*)dl_ext, dz, T, E, k, ld_ext,
-                score_fn, renorm, device_error_word());
+                score_fn, renorm, aux_counts, aux_w, device_error_word());
 }
 
 int launch_split_reduce(const float* part, int S, int rows, int cols, float* out_main,

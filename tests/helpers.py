@@ -124,12 +124,13 @@ def oracle_layer(lc, inp, backward=True):
 GRAD_NAMES = ["dx", "dW_r", "dW1", "dW2", "dWs1", "dWs2", "dw_sg"]
 
 
-def compare_layer(lc, gpu, ref, tol, backward=True):
+def compare_layer(lc, gpu, ref, tol, backward=True, order_keys=None):
     """Routing exact, float outputs within tol.  Returns the per-tensor errors.
 
     The selected SET of every row must equal the oracle's (inputs come from clean_inputs); the
-    order inside the set must match wherever the oracle's top-(k+1) logits are farther apart
-    than the router GEMM's rounding can move them."""
+    order inside the set must match wherever the oracle's top-(k+1) selection keys (the logits,
+    or `order_keys` when the selection runs on other keys) are farther apart than the router
+    GEMM's rounding can move them."""
     fwd = ref["fwd"]
     s = gpu["saved"]
     errs = {}
@@ -139,7 +140,8 @@ def compare_layer(lc, gpu, ref, tol, backward=True):
     idx = np64(s["idx"]).astype(np.int64)
     oidx = fwd["idx"].astype(np.int64)
     assert (np.sort(idx, 1) == np.sort(oidx, 1)).all(), "selected experts differ from the oracle"
-    clear = order_gap(lg, lc.k) > MARGIN * scale
+    keys = lg if order_keys is None else np.asarray(order_keys, np.float64)
+    clear = order_gap(keys, lc.k) > MARGIN * scale
     assert (idx[clear] == oidx[clear]).all(), "selection order differs on rows with clear margins"
     counts, offsets, sop, tos = O.routing_maps(oidx, lc.E)
     assert (np64(s["counts"]) == counts).all()
@@ -153,6 +155,9 @@ def compare_layer(lc, gpu, ref, tol, backward=True):
     og = np.take_along_axis(fwd["gate"], np.argsort(oidx, 1), 1)
     errs["gate"] = assert_close("gate", gg, og, 1e-4 if tol > 1e-4 else 1e-5)
     errs["y"] = assert_close("y", np64(gpu["y"]), fwd["y"], tol)
+    if "aux_loss" in fwd:
+        errs["aux_loss"] = assert_close("aux_loss", np64(s["aux_loss"])[:1],
+                                        np.array([fwd["aux_loss"]]), 1e-4 if tol > 1e-4 else 1e-5)
     if backward:
         b = ref["bwd"]
         for n in GRAD_NAMES:

@@ -29,7 +29,7 @@ def test_exports_every_declared_function():
 
 def cfg(**kw):
     base = dict(T=256, d=128, E=8, k=2, f=256, f_shared=0, score_fn=0, renorm=1, shared_gate=0,
-                dtype=0)
+                dtype=0, bias_mode=0, aux_coeff=0.0)
     base.update(kw)
     return moe.MoeCfg(*[base[n] for n, _ in moe.MoeCfg._fields_])
 
@@ -47,6 +47,10 @@ MIS = ctypes.c_void_p((1 << 20) + 8)
     (dict(score_fn=3), -1),
     (dict(shared_gate=1), -1),                     # gate without a shared expert
     (dict(dtype=7), -1),
+    (dict(bias_mode=2), -1),
+    (dict(aux_coeff=-1e-4), -1),
+    (dict(aux_coeff=float("nan")), -1),
+    (dict(aux_coeff=float("inf")), -1),
 ])
 def test_bad_config_is_rejected(bad, code):
     c = cfg(**bad)
@@ -77,3 +81,20 @@ def test_workspace_sizes_grow_with_the_layer():
     big = cfg(T=4096)
     for w in (moe.WS_ROUTE, moe.WS_LAYER_BWD, moe.WS_FFN_BWD):
         assert L.moe_workspace_bytes(ctypes.byref(big), w) > L.moe_workspace_bytes(ctypes.byref(small), w)
+
+
+def test_router_variant_entry_points_check_arguments():
+    c = cfg(aux_coeff=1e-4)
+    ws_n = L.moe_workspace_bytes(ctypes.byref(c), 0)
+    assert ws_n > 0
+    # balancing loss: needs a coefficient, logits, counts, an output and the routing workspace
+    c0 = cfg()
+    assert L.moe_router_aux_loss(ctypes.byref(c0), P, P, P, P, ws_n, None) == -1
+    assert L.moe_router_aux_loss(ctypes.byref(c), None, P, P, P, ws_n, None) == -1
+    assert L.moe_router_aux_loss(ctypes.byref(c), P, P, MIS, P, ws_n, None) == -4
+    assert L.moe_router_aux_loss(ctypes.byref(c), P, P, P, P, ws_n - 1, None) == -3
+    # bias update: counts and bias required, finite rate
+    assert L.moe_expert_bias_update(ctypes.byref(c), None, P, ctypes.c_float(1e-3), None) == -1
+    assert L.moe_expert_bias_update(ctypes.byref(c), P, None, ctypes.c_float(1e-3), None) == -1
+    assert L.moe_expert_bias_update(ctypes.byref(c), P, P, ctypes.c_float(float("nan")), None) == -1
+    assert L.moe_last_error()
