@@ -68,13 +68,22 @@ template <int SCHED, int EPI> struct DynMode {
   static constexpr bool on = SCHED == RAGGED_K && EPI == EPI_F32 && MOE_DYN_WGRAD != 0;
 };
 
-// Alternatively (static walk), weight gradients run in clusters of two CTAs on vertically
-// adjacent 128-row tiles of the same output block: both need the same B k-block, so each loads
-// half of it and multicasts it into both CTAs' shared memory (this GPU's own memory), cutting
-// operand traffic from L2 by a third.  Each CTA keeps its own MMAs, TMEM and epilogue.
+// Clusters of two CTAs on vertically adjacent 128-row tiles of the same output block: both
+// need the same B k-block, so each loads half of it and multicasts it into both CTAs' shared
+// memory (this GPU's own memory), cutting each CTA's operand reads from L2 by a third.  Each
+// CTA keeps its own MMAs, TMEM and epilogue.  Row-ragged products walk 256-row tiles inside one
+// expert; the lower CTA of an expert's last tile may have no rows: it still delivers its half
+// of B but skips its A loads and MMAs.  Weight gradients use it only with the static walk.
+// Row-ragged products keep it as a build option: measured slower on GB300 (fc1 + SwiGLU
+// 1.49 -> 1.57 ms, fc2 dgrad 0.98 -> 1.07 ms on the 128-expert layer): the pairs run in
+// lockstep and the extra 256-row tails cost more than the L2 reads saved.
+#ifndef MOE_MC_ROWS
+#define MOE_MC_ROWS 0
+#endif
 template <int SCHED, int EPI> struct McMode {
   static constexpr bool on =
-      SCHED == RAGGED_K && EPI == EPI_F32 && MOE_MC_WGRAD != 0 && !DynMode<SCHED, EPI>::on;
+      (SCHED == RAGGED_K && EPI == EPI_F32 && MOE_MC_WGRAD != 0 && !DynMode<SCHED, EPI>::on) ||
+      (SCHED == RAGGED_M && EPI != EPI_F32 && MOE_MC_ROWS != 0);
 };
 
 // L2 priorities of the weight gradients: their fp32 blocks are written once and never read
@@ -87,24 +96,38 @@ template <int SCHED, int EPI> struct McMode {
 #define MOE_WGRAD_LOAD_HINT 0
 #endif
 
+// 192-column output tiles where they pad the product's width less than 256 (build option:
+// measured slower on GB300 -- fc1 dgrad 1.38 -> 1.55 ms, fc2 dgrad 0.97 -> 1.15 ms at d = 2688,
+// f = 1856 -- the per-FLOP operand traffic and per-tile costs outweigh the saved padding).
+#ifndef MOE_TILE192
+#define MOE_TILE192 0
+#endif
+
 constexpr int FEED = 8;   // depth of the ring that passes run-time tile indices to the consumers
 
-// Staging slabs per epilogue warp: the SwiGLU backward needs two (saved a and u); with 8
-// epilogue warps the others make do with one so that the ring keeps four stages.
-template <int EPI, int EPI_WARPS> struct SlabsPerWarp {
-  static constexpr int n = (EPI == EPI_SWIGLU_BWD || EPI_WARPS == 4) ? 2 : 1;
+// Staging slabs per epilogue warp: the SwiGLU backward needs two (saved a and u); weight
+// gradients take MOE_WGRAD_SLABS (stores in flight per warp); with 8 epilogue warps the others
+// make do with one so that the ring keeps four stages.
+#ifndef MOE_WGRAD_SLABS
+#define MOE_WGRAD_SLABS 2
+#endif
+template <int SCHED, int EPI, int EPI_WARPS> struct SlabsPerWarp {
+  static constexpr int n = EPI == EPI_SWIGLU_BWD ? 2
+                         : SCHED == RAGGED_K ? MOE_WGRAD_SLABS
+                         : EPI_WARPS == 4 ? 2 : 1;
 };
 
 // Epilogue width: 4 warps (one per TMEM lane quadrant) or 8 (two per quadrant, each on half
 // of the tile's columns) for products whose epilogue is long relative to their MMAs (weight
 // gradients, SwiGLU backward); 8 epilogue warps trade one pipeline stage for staging slabs.
-template <int SCHED, int EPI> struct EpiWidth {
+// (8 warps split a tile's columns in two halves of 64-column steps: BN a multiple of 128.)
+template <int BN, int SCHED, int EPI> struct EpiWidth {
   static constexpr int warps =
-      !OutPath<SCHED, EPI>::tma ? 4
+      (!OutPath<SCHED, EPI>::tma || BN % 128 != 0) ? 4
       : (SCHED == RAGGED_K ? (MOE_EPI8_WGRAD ? 8 : 4)
                            : (EPI == EPI_SWIGLU_BWD ? (MOE_EPI8_SWIGLU_BWD ? 8 : 4)
                                                     : (MOE_EPI8_OTHER ? 8 : 4)));
-  static constexpr int slabs = SlabsPerWarp<EPI, warps>::n;
+  static constexpr int slabs = SlabsPerWarp<SCHED, EPI, warps>::n;
 };
 
 template <int BN, bool TMA_OUT, int EPI_WARPS, int SLABS> struct TileCfg {
@@ -116,7 +139,10 @@ template <int BN, bool TMA_OUT, int EPI_WARPS, int SLABS> struct TileCfg {
   static constexpr int STAGES = FIT < 6 ? FIT : 6;
   static constexpr int RING = STAGES * (A_STAGE + B_STAGE);
   static constexpr int SMEM = RING + STAGING + AUX;
-  static constexpr int TMEM_COLS = 2 * BN;
+  // two accumulators of BN columns; allocations are powers of two of at least 32 columns
+  static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
+                                 : 2 * BN <= 256 ? 256 : 512;
+  static constexpr int ACC_STRIDE = TMEM_COLS / 2;   // column of accumulator 1 (aligned)
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
 };
 
@@ -167,7 +193,7 @@ struct Sched {
         if (s_pre[mid] <= mt) lo = mid; else hi = mid;
       }
       ti.g = lo;
-      ti.m0 = s_off[lo] + (mt - s_pre[lo]) * BM;
+      ti.m0 = s_off[lo] + (mt - s_pre[lo]) * TBM;
       ti.m_end = s_off[lo + 1];
       ti.n0 = nt * (EPI == EPI_SWIGLU_FWD ? BN / 2 : BN);
       ti.k0 = 0;
@@ -220,17 +246,19 @@ __device__ __forceinline__ void slab_store_3d(const CUtensorMap* m, const uint8_
 }
 
 template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI>
-__global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
+__global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
                    const __grid_constant__ CUtensorMap tmO2, const KArgs p) {
   constexpr bool TMA_OUT = OutPath<SCHED, EPI>::tma;
-  constexpr int EPI_WARPS = EpiWidth<SCHED, EPI>::warps;
-  constexpr int SLABS = EpiWidth<SCHED, EPI>::slabs;
+  constexpr int EPI_WARPS = EpiWidth<BN, SCHED, EPI>::warps;
+  constexpr int SLABS = EpiWidth<BN, SCHED, EPI>::slabs;
   using C = TileCfg<BN, TMA_OUT, EPI_WARPS, SLABS>;
   constexpr bool MC = McMode<SCHED, EPI>::on;
   constexpr bool DYN = DynMode<SCHED, EPI>::on;
-  using S = Sched<BN, SCHED, EPI, MC ? 2 * BM : BM>;
+  static_assert(!MC || BN % 128 == 0, "cluster pairs split B in 128-row halves");
+  constexpr int TM = MC ? 2 * BM : BM;   // rows of one walker tile (a CTA, or a cluster pair)
+  using S = Sched<BN, SCHED, EPI, TM>;
   constexpr int STAGES = C::STAGES;
   constexpr uint32_t STAGE_TX = A_STAGE + C::B_STAGE;
 
@@ -307,11 +335,11 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
   __syncthreads();
   if (*s_bad) return;
   if (SCHED == RAGGED_M && warp == 0) {
-    // s_pre[g] = sum_{g' < g} ceil(rows_g' / BM): lane L scans groups [L*per, (L+1)*per)
+    // s_pre[g] = sum_{g' < g} ceil(rows_g' / TM): lane L scans groups [L*per, (L+1)*per)
     const int per = (p.G + 31) / 32;
     const int lo = min(p.G, lane * per), hi = min(p.G, lo + per);
     int local = 0;
-    for (int g = lo; g < hi; ++g) local += (s_off[g + 1] - s_off[g] + BM - 1) / BM;
+    for (int g = lo; g < hi; ++g) local += (s_off[g + 1] - s_off[g] + TM - 1) / TM;
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -321,7 +349,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
     int run = incl - local;
     for (int g = lo; g < hi; ++g) {
       s_pre[g] = run;
-      run += (s_off[g + 1] - s_off[g] + BM - 1) / BM;
+      run += (s_off[g + 1] - s_off[g] + TM - 1) / TM;
     }
     if (lane == 31) s_pre[p.G] = incl;
   }
@@ -368,6 +396,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
         uint8_t* b_dst = sB + stg * C::B_STAGE;
         const int kk = ti.k0 + kb * BK;
         const int m_cta = ti.m0 + static_cast<int>(rank) * BM;
+        const bool live = !(MC && SCHED == RAGGED_M) || m_cta < ti.m_end;
         auto box = [&](void* dst, const CUtensorMap* m, int c0, int c1) {
           if (SCHED == RAGGED_K && MOE_WGRAD_LOAD_HINT)
             ptx::tma_load_2d_hint(dst, m, &full[stg], c0, c1, ptx::policy_evict_last());
@@ -375,14 +404,22 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
             ptx::tma_load_2d(dst, m, &full[stg], c0, c1);
         };
         if (!A_MN) {
-          box(a_dst, &tmA, kk, m_cta);
+          if (live) box(a_dst, &tmA, kk, m_cta);
         } else {
 #pragma unroll
           for (int c = 0; c < BM / 64; ++c) box(a_dst + c * (BK * 128), &tmA, m_cta + 64 * c, kk);
         }
         if (!B_MN) {
           const int brow = static_cast<int>(ti.g * p.b_group_rows) + ti.n0;
-          if (EPI == EPI_SWIGLU_FWD) {
+          if (MC) {
+            // this CTA's 128 B rows (SwiGLU: rank 0 the gate block, rank 1 the up block),
+            // delivered to both CTAs of the pair
+            const int row = EPI == EPI_SWIGLU_FWD
+                                ? brow + (rank ? static_cast<int>(p.b_up_rows) : 0)
+                                : brow + static_cast<int>(rank) * (BN / 2);
+            ptx::tma_load_2d_multicast(b_dst + rank * (BN / 2) * 128, &tmB, &full[stg], kk, row,
+                                       0x3);
+          } else if (EPI == EPI_SWIGLU_FWD) {
             box(b_dst, &tmB, kk, brow);
             box(b_dst + (BN / 2) * 128, &tmB, kk, brow + static_cast<int>(p.b_up_rows));
           } else {
@@ -429,9 +466,13 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
           if (tile >= total) break;
         }
         const TileInfo ti = S::decode(p, s_off, s_pre, s_ord, tile);
+        // bytes landing in this CTA per stage: its A block (unless it has no rows) and all of B
+        const bool a_live = !(MC && SCHED == RAGGED_M) ||
+                            ti.m0 + static_cast<int>(rank) * BM < ti.m_end;
+        const uint32_t tx = a_live ? STAGE_TX : STAGE_TX - A_STAGE;
         for (int kb = 0; kb < ti.kblocks; ++kb) {
           if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(&full[stage], STAGE_TX);
+          ptx::mbar_arrive_expect_tx(&full[stage], tx);
           armed[stage] = static_cast<int>(phase);
           issue(ti, kb, stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -475,7 +516,10 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
       if (ti.kblocks == 0) continue;
       if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
       ptx::tc_fence_after();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::ACC_STRIDE);
+      // a cluster CTA without rows in this tile consumes the stages but issues no MMAs
+      const bool a_live = !(MC && SCHED == RAGGED_M) ||
+                          ti.m0 + static_cast<int>(rank) * BM < ti.m_end;
       for (int kb = 0; kb < ti.kblocks; ++kb) {
         if (!ptx::mbar_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
         uint8_t* a_src = sA + stage * A_STAGE;
@@ -500,6 +544,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
           const uint32_t a_addr = ptx::smem_u32(a_src), b_addr = ptx::smem_u32(b_src);
 #pragma unroll
           for (int k16 = 0; k16 < BK / 16; ++k16) {
+            if (!a_live) break;
             const uint64_t ad = A_MN ? ptx::smem_desc_sw128(a_addr + k16 * 2048, BK * 128, 1024)
                                      : ptx::smem_desc_sw128(a_addr + k16 * 32, 16, 1024);
             const uint64_t bd = B_MN ? ptx::smem_desc_sw128(b_addr + k16 * 2048, BK * 128, 1024)
@@ -536,7 +581,6 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
     uint32_t ld_phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    // Next free staging slab of this warp: at most one earlier store may still be reading.
     // fp32 slab -> [g][row][col] (weight gradients: evict-first in L2)
     auto store_f32 = [&](const uint8_t* src, int col, int row, int g) {
       if (SCHED == RAGGED_K && MOE_WGRAD_STORE_HINT)
@@ -544,14 +588,14 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
       else
         ptx::tma_store_3d(&tmO0, src, col, row, g);
     };
+    // Next free staging slab of this warp: at most SLABS-1 earlier stores may still read theirs.
     auto next_slab = [&]() -> uint8_t* {
       if (lane == 0) {
-        if (SLABS == 2) ptx::bulk_wait_read<1>();
-        else ptx::bulk_wait_read<0>();
+        ptx::bulk_wait_read<SLABS - 1>();
       }
       __syncwarp();
       uint8_t* s = slabs + slab_sel * SLAB;
-      if (SLABS == 2) slab_sel ^= 1;
+      if (++slab_sel == SLABS) slab_sel = 0;
       return s;
     };
     int fslot = 0;
@@ -598,7 +642,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<SCHED, EPI>::warps, 1)
       if (!ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err)) break;
       ptx::tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                             static_cast<uint32_t>(acc * BN);
+                             static_cast<uint32_t>(acc * C::ACC_STRIDE);
       // Full slabs go out through TMA (the maps clip at the tensors' edges).  For ragged rows a
       // slab that crosses the end of its expert's rows would overwrite the next expert's: it is
       // written with masked stores instead.
@@ -950,7 +994,7 @@ template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI>
 int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   const char* name = g.name ? g.name : kind;
   constexpr bool TMA_OUT = OutPath<SCHED, EPI>::tma;
-  using C = TileCfg<BN, TMA_OUT, EpiWidth<SCHED, EPI>::warps, EpiWidth<SCHED, EPI>::slabs>;
+  using C = TileCfg<BN, TMA_OUT, EpiWidth<BN, SCHED, EPI>::warps, EpiWidth<BN, SCHED, EPI>::slabs>;
   auto kern = tc_gemm_kernel<BN, A_MN, B_MN, SCHED, EPI>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -964,7 +1008,8 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   CUtensorMap ma, mb, mo[3];
   memset(mo, 0, sizeof(mo));
   MOE_TRY(map_operand(&ma, g.A, A_MN ? BK : BM));
-  MOE_TRY(map_operand(&mb, g.B, B_MN ? BK : (EPI == EPI_SWIGLU_FWD ? BN / 2 : BN)));
+  MOE_TRY(map_operand(&mb, g.B,
+                      B_MN ? BK : ((EPI == EPI_SWIGLU_FWD || McMode<SCHED, EPI>::on) ? BN / 2 : BN)));
   const int64_t rows = g.M;   // RAGGED_M: rows of the output (capacity)
   if (EPI == EPI_STORE) {
     MOE_TRY(map_bf16(&mo[0], g.out, rows, g.N, g.ldo, 32));
@@ -1027,12 +1072,19 @@ int gemm_tc(const GemmDesc& g, cudaStream_t st) {
   if (g.sched == RAGGED_M && !g.A.mn_major) {
     if (g.epi == EPI_SWIGLU_FWD && !g.B.mn_major)
       return run<256, false, false, RAGGED_M, EPI_SWIGLU_FWD>(g, "gemm_fc1_swiglu", st);
+    // Output tiles of 192 or 256 columns, whichever pads the product's width less (e.g.
+    // d = 2688 is 14 x 192, f = 1856 is 10 x 192 - 64 but 8 x 256 - 192); ties take 256.
+    const int ncols = g.epi == EPI_SWIGLU_BWD ? g.f : g.N;
+    const bool n192 = MOE_TILE192 && (ncols + 191) / 192 * 192 < (ncols + 255) / 256 * 256;
     if (g.epi == EPI_SWIGLU_BWD && g.B.mn_major)
-      return run<256, false, true, RAGGED_M, EPI_SWIGLU_BWD>(g, "gemm_fc2_dgrad_swiglu_bwd", st);
+      return n192 ? run<192, false, true, RAGGED_M, EPI_SWIGLU_BWD>(g, "gemm_fc2_dgrad_swiglu_bwd", st)
+                  : run<256, false, true, RAGGED_M, EPI_SWIGLU_BWD>(g, "gemm_fc2_dgrad_swiglu_bwd", st);
     if (g.epi == EPI_STORE && !g.B.mn_major)
-      return run<256, false, false, RAGGED_M, EPI_STORE>(g, "gemm_fc2", st);
+      return n192 ? run<192, false, false, RAGGED_M, EPI_STORE>(g, "gemm_fc2", st)
+                  : run<256, false, false, RAGGED_M, EPI_STORE>(g, "gemm_fc2", st);
     if (g.epi == EPI_STORE && g.B.mn_major)
-      return run<256, false, true, RAGGED_M, EPI_STORE>(g, "gemm_dgrad", st);
+      return n192 ? run<192, false, true, RAGGED_M, EPI_STORE>(g, "gemm_dgrad", st)
+                  : run<256, false, true, RAGGED_M, EPI_STORE>(g, "gemm_dgrad", st);
     if (g.epi == EPI_F32 && !g.B.mn_major) {
       if (g.N <= 128) return run<128, false, false, RAGGED_M, EPI_F32>(g, "gemm_router", st);
       return run<256, false, false, RAGGED_M, EPI_F32>(g, "gemm_router", st);
