@@ -71,6 +71,45 @@ int num_sms() {
   return g_sms[dev];
 }
 
+// ------------------------------------------------------------------ side stream
+// "Megatron-Bridge 深度剖析", §Shared Expert Overlap: the shared expert's computation overlaps
+// the routed path instead of following it.  One library-owned non-blocking stream and a
+// fork/join event pair per device, created on the first layer call (make that call before any
+// stream capture).  A call's forked section is enqueued under g_side_mu so that calls from
+// several host threads do not interleave their records of the shared events.
+#ifndef MOE_SHARED_OVERLAP
+#define MOE_SHARED_OVERLAP 1
+#endif
+#ifndef MOE_SHARED_OVERLAP_FWD
+#define MOE_SHARED_OVERLAP_FWD MOE_SHARED_OVERLAP
+#endif
+#ifndef MOE_SHARED_OVERLAP_BWD
+#define MOE_SHARED_OVERLAP_BWD MOE_SHARED_OVERLAP
+#endif
+
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool ok = false;
+};
+static SideStream g_side[64];
+static std::mutex g_side_mu;
+
+// The device's side stream, or nullptr (then the caller runs everything on its own stream).
+static SideStream* side_stream() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  SideStream& ss = g_side[dev];
+  if (!ss.ok && !ss.s) {
+    ss.ok = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) == cudaSuccess;
+    if (!ss.s) ss.s = reinterpret_cast<cudaStream_t>(-1);   // creation failed: do not retry
+  }
+  return ss.ok ? &ss : nullptr;
+}
+
 // ------------------------------------------------------------------ launch accounting, tracing
 static std::atomic<uint64_t> g_launches{0};
 static std::atomic<int> g_trace_on{0};
@@ -167,6 +206,7 @@ struct BwdWs {
   void* dy_perm;
   float* dgate;
   void* dH1;
+  void* s_dH1;   // the shared expert's [da | du] (its own buffer: it may run concurrently)
   void* dshared;
   float* dcoef;
   void* dx_shared;
@@ -184,9 +224,8 @@ static BwdWs carve_bwd(Carve& cv, const moe_cfg* c) {
   const bool sh = c->f_shared > 0, gt = c->shared_gate != 0;
   w.dy_perm = cv.take(N * c->d * es);
   w.dgate = static_cast<float*>(cv.take(N * 4));
-  size_t h1 = N * 2 * c->f;
-  if (sh && T * 2 * c->f_shared > h1) h1 = T * 2 * c->f_shared;
-  w.dH1 = cv.take(h1 * es);
+  w.dH1 = cv.take(N * 2 * c->f * es);
+  w.s_dH1 = sh ? cv.take(T * 2 * c->f_shared * es) : nullptr;
   w.dshared = sh ? cv.take(T * c->d * es) : nullptr;
   w.dcoef = gt ? static_cast<float*>(cv.take(T * 4)) : nullptr;
   w.dx_shared = sh ? cv.take(T * c->d * es) : nullptr;
@@ -710,18 +749,38 @@ int moe_layer_fwd(const moe_cfg* c, const void* x, const void* W_r, const float*
   }
   Carve cv(ws);
   RouteWs w = carve_route(cv, c);
+  // The shared expert (and its gate) needs only x: it runs on the side stream while the routed
+  // path (routing, permute, grouped SwiGLU) runs on `st`; the combine waits for both.
+  SideStream* side = (sh && MOE_SHARED_OVERLAP_FWD) ? side_stream() : nullptr;
+  std::unique_lock<std::mutex> side_lk(g_side_mu, std::defer_lock);
+  auto shared_fwd = [&](cudaStream_t ss) -> int {
+    if (gt) MOE_TRY(launch_shared_gate(c->dtype, x, w_sg, s->s_coef, c->T, c->d, ss));
+    return ffn_fwd_impl(c, 1, nullptr, c->T, c->f_shared, x, Ws1, Ws2, s->s_h, s->s_act,
+                        s->s_out, ss);
+  };
   MOE_TRY(route_impl(c, x, W_r, b_r, nullptr, s->logits, s->idx, s->gate, s->counts, s->offsets,
                      s->slot_of_pair, s->token_of_slot, w, st));
+  if (side) {
+    side_lk.lock();
+    if (cudaEventRecord(side->fork, st) != cudaSuccess ||
+        cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess)
+      return fail(MOE_ERR_CUDA, "forking the shared expert onto the side stream failed");
+    MOE_TRY(shared_fwd(side->s));
+    if (cudaEventRecord(side->join, side->s) != cudaSuccess)
+      return fail(MOE_ERR_CUDA, "recording the shared expert's completion failed");
+  }
   if (c->aux_coeff > 0.0f)
     MOE_TRY(launch_aux_loss(s->logits, s->counts, c->T, c->E, c->k, c->score_fn, c->aux_coeff,
                             w.aux, s->aux_loss, st));
   MOE_TRY(launch_permute(c->dtype, x, s->slot_of_pair, s->x_perm, c->T, c->d, c->k, st));
   MOE_TRY(ffn_fwd_impl(c, c->E, s->offsets, Nrows(c), c->f, s->x_perm, W1, W2, s->h, s->act,
                        s->y_perm, st));
-  if (sh) {
-    if (gt) MOE_TRY(launch_shared_gate(c->dtype, x, w_sg, s->s_coef, c->T, c->d, st));
-    MOE_TRY(ffn_fwd_impl(c, 1, nullptr, c->T, c->f_shared, x, Ws1, Ws2, s->s_h, s->s_act,
-                         s->s_out, st));
+  if (side) {
+    if (cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess)
+      return fail(MOE_ERR_CUDA, "joining the side stream failed");
+    side_lk.unlock();
+  } else if (sh) {
+    MOE_TRY(shared_fwd(st));
   }
   return launch_combine(c->dtype, s->y_perm, s->gate, s->slot_of_pair, sh ? s->s_out : nullptr,
                         gt ? s->s_coef : nullptr, y, c->T, c->d, c->k, st);
@@ -769,55 +828,78 @@ int moe_layer_bwd(const moe_cfg* c, const void* dy, const void* x, const void* W
   MOE_TRY(launch_combine_bwd(c->dtype, dy, s->y_perm, s->gate, s->slot_of_pair,
                              sh ? s->s_out : nullptr, gt ? s->s_coef : nullptr, w.dy_perm, w.dgate,
                              w.dshared, w.dcoef, T, d, k, st));
-  // 2. routed experts (dx_perm overwrites dy_perm once it is no longer read)
+  // 2.-6. The routed experts run on `st`; the shared expert and the router's backward (which
+  // need only combine-backward outputs) run on the side stream concurrently; dx waits for both.
+  SideStream* side = MOE_SHARED_OVERLAP_BWD ? side_stream() : nullptr;
+  std::unique_lock<std::mutex> side_lk(g_side_mu, std::defer_lock);
+  auto side_work = [&](cudaStream_t ss) -> int {
+    // shared expert (one group of all T tokens)
+    if (sh)
+      MOE_TRY(ffn_bwd_impl(c, 1, nullptr, T, c->f_shared, x, Ws1, Ws2, s->s_act, s->s_h,
+                           w.dshared, w.s_dH1, w.dx_shared, dWs1, dWs2, w.sched + 8, ss));
+    // router: dlogits (+ shared gate dz in column E), with the balancing loss's gradient
+    const int ldx = ext_cols(c);
+    const bool aux = c->aux_coeff > 0.0f;
+    const float aux_w = aux ? static_cast<float>(static_cast<double>(c->aux_coeff) * E /
+                                                 (static_cast<double>(k) * T * T))
+                            : 0.0f;
+    MOE_TRY(launch_router_bwd(c->dtype, s->logits, s->idx, s->gate, w.dgate,
+                              gt ? w.dcoef : nullptr, gt ? s->s_coef : nullptr, w.dl_ext, w.dz, T,
+                              E, k, ldx, c->score_fn, c->renorm, aux ? s->counts : nullptr, aux_w,
+                              ss));
+    // dx_router = dlogits . W_r
+    GemmDesc rd = desc0();
+    rd.name = "gemm_router_dgrad";
+    rd.sched = RAGGED_M;
+    rd.epi = EPI_STORE;
+    rd.G = 1;
+    rd.M = T;
+    rd.N = d;
+    rd.K = E;
+    rd.A = opnd(w.dl_ext, T, ldx, false);
+    rd.B = opnd(W_r, E, d, true);
+    rd.out = w.dx_router;
+    rd.ldo = d;
+    MOE_TRY(gemm(c, rd, ss));
+    // [dW_r; dw_sg] = [dlogits | dz]^T . x, split over tokens, then a fixed-order sum
+    const int mr = E + (gt ? 1 : 0);
+    const int S_ = router_splits(c);
+    GemmDesc rw = desc0();
+    rw.name = "gemm_router_wgrad";
+    rw.sched = RAGGED_K;
+    rw.epi = EPI_F32;
+    rw.G = S_;
+    rw.M = mr;
+    rw.N = d;
+    rw.K = T;
+    rw.A = opnd(w.dl_ext, T, ldx, true);
+    rw.B = opnd(x, T, d, true);
+    rw.out = w.part;
+    rw.ldo = d;
+    rw.out_group_stride = static_cast<int64_t>(mr) * d;
+    rw.tile_ctr = w.sched + 16;
+    MOE_TRY(gemm(c, rw, ss));
+    return launch_split_reduce(w.part, S_, mr, d, dW_r, E, gt ? dw_sg : nullptr, ss);
+  };
+  if (side) {
+    side_lk.lock();
+    if (cudaEventRecord(side->fork, st) != cudaSuccess ||
+        cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess)
+      return fail(MOE_ERR_CUDA, "forking onto the side stream failed");
+    MOE_TRY(side_work(side->s));
+    if (cudaEventRecord(side->join, side->s) != cudaSuccess)
+      return fail(MOE_ERR_CUDA, "recording the side stream's completion failed");
+  }
+  // routed experts (dx_perm overwrites dy_perm once it is no longer read)
   MOE_TRY(ffn_bwd_impl(c, E, s->offsets, Nrows(c), c->f, s->x_perm, W1, W2, s->act, s->h,
                        w.dy_perm, w.dH1, w.dy_perm, dW1, dW2, w.sched, st));
-  // 3. shared expert (one group of all T tokens)
-  if (sh)
-    MOE_TRY(ffn_bwd_impl(c, 1, nullptr, T, c->f_shared, x, Ws1, Ws2, s->s_act, s->s_h, w.dshared,
-                         w.dH1, w.dx_shared, dWs1, dWs2, w.sched + 8, st));
-  // 4. router: dlogits (+ shared gate dz in column E)
-  const int ldx = ext_cols(c);
-  const bool aux = c->aux_coeff > 0.0f;
-  const float aux_w = aux ? static_cast<float>(static_cast<double>(c->aux_coeff) * E /
-                                               (static_cast<double>(k) * T * T))
-                          : 0.0f;
-  MOE_TRY(launch_router_bwd(c->dtype, s->logits, s->idx, s->gate, w.dgate, gt ? w.dcoef : nullptr,
-                            gt ? s->s_coef : nullptr, w.dl_ext, w.dz, T, E, k, ldx, c->score_fn,
-                            c->renorm, aux ? s->counts : nullptr, aux_w, st));
-  // 5. dx_router = dlogits . W_r
-  GemmDesc rd = desc0();
-  rd.name = "gemm_router_dgrad";
-  rd.sched = RAGGED_M;
-  rd.epi = EPI_STORE;
-  rd.G = 1;
-  rd.M = T;
-  rd.N = d;
-  rd.K = E;
-  rd.A = opnd(w.dl_ext, T, ldx, false);
-  rd.B = opnd(W_r, E, d, true);
-  rd.out = w.dx_router;
-  rd.ldo = d;
-  MOE_TRY(gemm(c, rd, st));
-  // 6. [dW_r; dw_sg] = [dlogits | dz]^T . x, split over tokens, then a fixed-order sum
-  const int mr = E + (gt ? 1 : 0);
-  const int S_ = router_splits(c);
-  GemmDesc rw = desc0();
-  rw.name = "gemm_router_wgrad";
-  rw.sched = RAGGED_K;
-  rw.epi = EPI_F32;
-  rw.G = S_;
-  rw.M = mr;
-  rw.N = d;
-  rw.K = T;
-  rw.A = opnd(w.dl_ext, T, ldx, true);
-  rw.B = opnd(x, T, d, true);
-  rw.out = w.part;
-  rw.ldo = d;
-  rw.out_group_stride = static_cast<int64_t>(mr) * d;
-  rw.tile_ctr = w.sched + 16;
-  MOE_TRY(gemm(c, rw, st));
-  MOE_TRY(launch_split_reduce(w.part, S_, mr, d, dW_r, E, gt ? dw_sg : nullptr, st));
+  if (side) {
+    if (cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess)
+      return fail(MOE_ERR_CUDA, "joining the side stream failed");
+    side_lk.unlock();
+  } else {
+    MOE_TRY(side_work(st));
+  }
   // 7. dx = sum_j dx_perm[slot(t,j)] + dx_shared + dx_router + dz * w_sg
   return launch_gather_sum(c->dtype, w.dy_perm, s->slot_of_pair, sh ? w.dx_shared : nullptr,
                            w.dx_router, gt ? w.dz : nullptr, gt ? w_sg : nullptr, dx, T, d, k, st);
