@@ -173,6 +173,25 @@ int moe_grouped_swiglu_bwd(const moe_cfg* cfg, const void* x_perm, const int32_t
                            const void* dy_perm, void* dx_perm, float* dW1, float* dW2,
                            void* ws, size_t ws_bytes, void* stream);
 
+/* The same two calls with the permutation folded into the operand loads ("Megatron-Bridge
+ * 深度剖析", §Permute Fusion): instead of x_perm they take x [T,d] and token_of_slot [N] (from
+ * moe_route_topk) and gather row token_of_slot[s] of x wherever x_perm[s] would be read (fc1's
+ * A operand and fc1's weight-gradient operand), with TMA tile::gather4 copies.  Results are
+ * bit-identical to moe_permute followed by the x_perm calls.  bf16 only (MOE_ERR_UNSUPPORTED
+ * for fp32); a token index outside [0, T) is recorded in the device error word and row 0 is
+ * read instead.  Slower than the explicit permute on GB300 (the gathered copies move 512 bytes
+ * each): kept for callers that cannot hold x_perm's N*d elements. */
+int moe_grouped_swiglu_fwd_gathered(const moe_cfg* cfg, const void* x,
+                                    const int32_t* token_of_slot, const int32_t* offsets,
+                                    const void* W1, const void* W2, void* h, void* act,
+                                    void* y_perm, void* ws, size_t ws_bytes, void* stream);
+int moe_grouped_swiglu_bwd_gathered(const moe_cfg* cfg, const void* x,
+                                    const int32_t* token_of_slot, const int32_t* offsets,
+                                    const void* W1, const void* W2, const void* act,
+                                    const void* h, const void* dy_perm, void* dx_perm,
+                                    float* dW1, float* dW2, void* ws, size_t ws_bytes,
+                                    void* stream);
+
 /* Unpermute + weighted combine: "Megatron-Bridge 深度剖析", §Expert Parallel 基础 (Step 3,
  * results sent back to token order) and §Shared Expert Overlap (shared output added).
  *   y[t] = sum_{j<k} gate[t,j] * y_perm[slot_of_pair[t,j]]  (+ c_t * shared_out[t])
@@ -202,7 +221,8 @@ typedef struct moe_saved {
   int32_t* offsets;       /* [E+1]                                             */
   int32_t* slot_of_pair;  /* [T,k]                                             */
   int32_t* token_of_slot; /* [N]                                               */
-  void* x_perm;           /* [N,d]   dtype                                     */
+  void* x_perm;           /* [N,d]   dtype (unused, may be NULL, by a bf16 library built with
+                             the permutation folded into its GEMMs: MOE_FUSE_PERMUTE=1) */
   void* act;              /* [N,2f]  dtype  ([a | u] pre-activations)          */
   void* h;                /* [N,f]   dtype                                     */
   void* y_perm;           /* [N,d]   dtype                                     */

@@ -47,6 +47,8 @@ _SIGS = {
     "moe_permute": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP]),
     "moe_grouped_swiglu_fwd": (ctypes.c_int, [_CFG] + [_VP] * 8 + [_SZ, _VP]),
     "moe_grouped_swiglu_bwd": (ctypes.c_int, [_CFG] + [_VP] * 11 + [_SZ, _VP]),
+    "moe_grouped_swiglu_fwd_gathered": (ctypes.c_int, [_CFG] + [_VP] * 8 + [_SZ, _VP]),
+    "moe_grouped_swiglu_bwd_gathered": (ctypes.c_int, [_CFG] + [_VP] * 11 + [_SZ, _VP]),
     "moe_unpermute_combine": (ctypes.c_int, [_CFG] + [_VP] * 7),
     "moe_unpermute_combine_bwd": (ctypes.c_int, [_CFG] + [_VP] * 11),
     "moe_layer_fwd": (ctypes.c_int, [_CFG] + [_VP] * 9 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP]),
@@ -166,6 +168,22 @@ def moe_grouped_swiglu_bwd(cfg, x_perm, offsets, W1, W2, act, h, dy_perm, dx_per
                                         _p(act), _p(h), _p(dy_perm), _p(dx_perm), _p(dW1), _p(dW2),
                                         _p(ws), 0 if ws is None else ws.numel(), _stream(stream)),
            "moe_grouped_swiglu_bwd")
+
+
+def moe_grouped_swiglu_fwd_gathered(cfg, x, token_of_slot, offsets, W1, W2, h, act, y_perm,
+                                    ws=None, stream=None):
+    _check(lib().moe_grouped_swiglu_fwd_gathered(
+        ctypes.byref(cfg), _p(x), _p(token_of_slot), _p(offsets), _p(W1), _p(W2), _p(h), _p(act),
+        _p(y_perm), _p(ws), 0 if ws is None else ws.numel(), _stream(stream)),
+        "moe_grouped_swiglu_fwd_gathered")
+
+
+def moe_grouped_swiglu_bwd_gathered(cfg, x, token_of_slot, offsets, W1, W2, act, h, dy_perm,
+                                    dx_perm, dW1, dW2, ws, stream=None):
+    _check(lib().moe_grouped_swiglu_bwd_gathered(
+        ctypes.byref(cfg), _p(x), _p(token_of_slot), _p(offsets), _p(W1), _p(W2), _p(act), _p(h),
+        _p(dy_perm), _p(dx_perm), _p(dW1), _p(dW2), _p(ws), 0 if ws is None else ws.numel(),
+        _stream(stream)), "moe_grouped_swiglu_bwd_gathered")
 
 
 def moe_unpermute_combine(cfg, y_perm, gate, slot_of_pair, shared_out, shared_coef, y, stream=None):

@@ -284,6 +284,20 @@ static int check_ws(const moe_cfg* c, int which, void* ws, size_t ws_bytes) {
 
 static cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
 
+// Build option: the bf16 layer folds the permutation into its GEMMs' operand loads (fc1 and
+// its weight gradient gather x rows by token_of_slot with tile::gather4; no x_perm).  Parity-
+// tested, but slower on GB300: one gather4 copy moves 512 bytes, and the TMA unit's copy rate
+// (about 6 bytes per clock per SM) is well short of the 27 bytes per clock the MMAs consume
+// (fc1 + SwiGLU 1.47 -> 4.5 ms, fc1 weight gradient 1.85 -> 9.8 ms on the 128-expert layer),
+// while the explicit permute kernel moves its bytes at ~90% of HBM bandwidth.  Off by default;
+// the fp32 CUDA-core path always permutes explicitly.
+#ifndef MOE_FUSE_PERMUTE
+#define MOE_FUSE_PERMUTE 0
+#endif
+static bool permute_fused(const moe_cfg* c) {
+  return MOE_FUSE_PERMUTE && c->dtype == MOE_DTYPE_BF16;
+}
+
 // ------------------------------------------------------------------ stages
 static int gemm(const moe_cfg* c, const GemmDesc& g, cudaStream_t st) {
   return c->dtype == MOE_DTYPE_BF16 ? gemm_tc(g, st) : gemm_simt(g, st);
@@ -339,9 +353,12 @@ static int route_impl(const moe_cfg* c, const void* x, const void* W_r, const fl
 }
 
 // fc1 + SwiGLU and fc2 for G groups whose rows are given by offsets (null: one group of `rows`).
+// gather (bf16): fc1 reads row s of its A operand from row gather[s] of x_perm, which is then
+// the unpermuted x with src_rows rows (the permutation folded into the operand load).
 static int ffn_fwd_impl(const moe_cfg* c, int G, const int32_t* offsets, int64_t rows, int f,
                         const void* x_perm, const void* W1, const void* W2, void* h, void* act,
-                        void* y_perm, cudaStream_t st) {
+                        void* y_perm, cudaStream_t st, const int32_t* gather = nullptr,
+                        int64_t src_rows = 0) {
   const int d = c->d;
   const bool shared = offsets == nullptr;
   GemmDesc g1 = desc0();
@@ -353,7 +370,8 @@ static int ffn_fwd_impl(const moe_cfg* c, int G, const int32_t* offsets, int64_t
   g1.M = static_cast<int>(rows);
   g1.N = 2 * f;
   g1.K = d;
-  g1.A = opnd(x_perm, rows, d, false);
+  g1.A = opnd(x_perm, gather ? src_rows : rows, d, false);
+  g1.gather = gather;
   g1.B = opnd(W1, static_cast<int64_t>(G) * 2 * f, d, false);
   g1.b_group_rows = 2 * f;
   g1.b_up_rows = f;
@@ -385,7 +403,8 @@ static int ffn_fwd_impl(const moe_cfg* c, int G, const int32_t* offsets, int64_t
 static int ffn_bwd_impl(const moe_cfg* c, int G, const int32_t* offsets, int64_t rows, int f,
                         const void* x_perm, const void* W1, const void* W2, const void* act,
                         const void* h, const void* dy_perm, void* dH1, void* dx_perm, float* dW1,
-                        float* dW2, int* sched, cudaStream_t st) {
+                        float* dW2, int* sched, cudaStream_t st, const int32_t* gather = nullptr,
+                        int64_t src_rows = 0) {
   const int d = c->d;
   const bool shared = offsets == nullptr;
   // dh = dy_perm . W2_g  (+ SwiGLU backward -> dH1 = [da | du])
@@ -451,7 +470,8 @@ static int ffn_bwd_impl(const moe_cfg* c, int G, const int32_t* offsets, int64_t
   w.N = d;
   w.K = static_cast<int>(rows);
   w.A = opnd(dH1, rows, 2 * f, true);
-  w.B = opnd(x_perm, rows, d, true);
+  w.B = opnd(x_perm, gather ? src_rows : rows, d, true);
+  w.gather = gather;
   w.out = dW1;
   w.ldo = d;
   w.out_group_stride = static_cast<int64_t>(2) * f * d;
@@ -637,6 +657,62 @@ int moe_grouped_swiglu_bwd(const moe_cfg* c, const void* x_perm, const int32_t* 
                       dx_perm, dW1, dW2, sched, st);
 }
 
+int moe_grouped_swiglu_fwd_gathered(const moe_cfg* c, const void* x,
+                                    const int32_t* token_of_slot, const int32_t* offsets,
+                                    const void* W1, const void* W2, void* h, void* act,
+                                    void* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(c));
+  if (c->dtype != MOE_DTYPE_BF16)
+    return fail(MOE_ERR_UNSUPPORTED, "gathered operands need the bf16 tensor-core path");
+  MOE_TRY(check_ptr(x, "x", true));
+  MOE_TRY(check_ptr(token_of_slot, "token_of_slot", true));
+  MOE_TRY(check_ptr(offsets, "offsets", true));
+  MOE_TRY(check_ptr(W1, "W1", true));
+  MOE_TRY(check_ptr(W2, "W2", true));
+  MOE_TRY(check_ptr(h, "h", true));
+  MOE_TRY(check_ptr(act, "act", false));
+  MOE_TRY(check_ptr(y_perm, "y_perm", true));
+  MOE_TRY(check_ws(c, MOE_WS_FFN_FWD, ws, ws_bytes));
+  if (Nrows(c) == 0) return MOE_OK;
+  return ffn_fwd_impl(c, c->E, offsets, Nrows(c), c->f, x, W1, W2, h, act, y_perm, S(stream),
+                      token_of_slot, c->T);
+}
+
+int moe_grouped_swiglu_bwd_gathered(const moe_cfg* c, const void* x,
+                                    const int32_t* token_of_slot, const int32_t* offsets,
+                                    const void* W1, const void* W2, const void* act,
+                                    const void* h, const void* dy_perm, void* dx_perm,
+                                    float* dW1, float* dW2, void* ws, size_t ws_bytes,
+                                    void* stream) {
+  MOE_TRY(check_cfg(c));
+  if (c->dtype != MOE_DTYPE_BF16)
+    return fail(MOE_ERR_UNSUPPORTED, "gathered operands need the bf16 tensor-core path");
+  MOE_TRY(check_ptr(x, "x", true));
+  MOE_TRY(check_ptr(token_of_slot, "token_of_slot", true));
+  MOE_TRY(check_ptr(offsets, "offsets", true));
+  MOE_TRY(check_ptr(W1, "W1", true));
+  MOE_TRY(check_ptr(W2, "W2", true));
+  MOE_TRY(check_ptr(act, "act", true));
+  MOE_TRY(check_ptr(h, "h", true));
+  MOE_TRY(check_ptr(dy_perm, "dy_perm", true));
+  MOE_TRY(check_ptr(dx_perm, "dx_perm", true));
+  MOE_TRY(check_ptr(dW1, "dW1", true));
+  MOE_TRY(check_ptr(dW2, "dW2", true));
+  MOE_TRY(check_ws(c, MOE_WS_FFN_BWD, ws, ws_bytes));
+  cudaStream_t st = S(stream);
+  if (Nrows(c) == 0) {
+    if (cudaMemsetAsync(dW1, 0, sizeof(float) * c->E * 2 * c->f * c->d, st) != cudaSuccess ||
+        cudaMemsetAsync(dW2, 0, sizeof(float) * c->E * c->d * c->f, st) != cudaSuccess)
+      return fail(MOE_ERR_CUDA, "cudaMemsetAsync failed");
+    return MOE_OK;
+  }
+  Carve cv(ws);
+  void* dH1 = cv.take(static_cast<size_t>(Nrows(c)) * 2 * c->f * esize(c));
+  int* sched = static_cast<int*>(cv.take(2 * 4 * sizeof(int)));
+  return ffn_bwd_impl(c, c->E, offsets, Nrows(c), c->f, x, W1, W2, act, h, dy_perm, dH1, dx_perm,
+                      dW1, dW2, sched, st, token_of_slot, c->T);
+}
+
 int moe_unpermute_combine(const moe_cfg* c, const void* y_perm, const float* gate,
                           const int32_t* slot_of_pair, const void* shared_out,
                           const float* shared_coef, void* y, void* stream) {
@@ -709,7 +785,7 @@ static int check_saved(const moe_cfg* c, const moe_saved* s) {
   MOE_TRY(check_ptr(s->offsets, "saved.offsets", true));
   MOE_TRY(check_ptr(s->slot_of_pair, "saved.slot_of_pair", true));
   MOE_TRY(check_ptr(s->token_of_slot, "saved.token_of_slot", true));
-  MOE_TRY(check_ptr(s->x_perm, "saved.x_perm", true));
+  MOE_TRY(check_ptr(s->x_perm, "saved.x_perm", !permute_fused(c)));
   MOE_TRY(check_ptr(s->act, "saved.act", true));
   MOE_TRY(check_ptr(s->h, "saved.h", true));
   MOE_TRY(check_ptr(s->y_perm, "saved.y_perm", true));
@@ -772,9 +848,15 @@ int moe_layer_fwd(const moe_cfg* c, const void* x, const void* W_r, const float*
   if (c->aux_coeff > 0.0f)
     MOE_TRY(launch_aux_loss(s->logits, s->counts, c->T, c->E, c->k, c->score_fn, c->aux_coeff,
                             w.aux, s->aux_loss, st));
-  MOE_TRY(launch_permute(c->dtype, x, s->slot_of_pair, s->x_perm, c->T, c->d, c->k, st));
-  MOE_TRY(ffn_fwd_impl(c, c->E, s->offsets, Nrows(c), c->f, s->x_perm, W1, W2, s->h, s->act,
-                       s->y_perm, st));
+  if (permute_fused(c)) {
+    // "Megatron-Bridge 深度剖析", §Permute Fusion: fc1 gathers its rows from x by token_of_slot
+    MOE_TRY(ffn_fwd_impl(c, c->E, s->offsets, Nrows(c), c->f, x, W1, W2, s->h, s->act,
+                         s->y_perm, st, s->token_of_slot, c->T));
+  } else {
+    MOE_TRY(launch_permute(c->dtype, x, s->slot_of_pair, s->x_perm, c->T, c->d, c->k, st));
+    MOE_TRY(ffn_fwd_impl(c, c->E, s->offsets, Nrows(c), c->f, s->x_perm, W1, W2, s->h, s->act,
+                         s->y_perm, st));
+  }
   if (side) {
     if (cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess)
       return fail(MOE_ERR_CUDA, "joining the side stream failed");
@@ -891,8 +973,12 @@ int moe_layer_bwd(const moe_cfg* c, const void* dy, const void* x, const void* W
       return fail(MOE_ERR_CUDA, "recording the side stream's completion failed");
   }
   // routed experts (dx_perm overwrites dy_perm once it is no longer read)
-  MOE_TRY(ffn_bwd_impl(c, E, s->offsets, Nrows(c), c->f, s->x_perm, W1, W2, s->act, s->h,
-                       w.dy_perm, w.dH1, w.dy_perm, dW1, dW2, w.sched, st));
+  if (permute_fused(c))
+    MOE_TRY(ffn_bwd_impl(c, E, s->offsets, Nrows(c), c->f, x, W1, W2, s->act, s->h, w.dy_perm,
+                         w.dH1, w.dy_perm, dW1, dW2, w.sched, st, s->token_of_slot, T));
+  else
+    MOE_TRY(ffn_bwd_impl(c, E, s->offsets, Nrows(c), c->f, s->x_perm, W1, W2, s->act, s->h,
+                         w.dy_perm, w.dH1, w.dy_perm, dW1, dW2, w.sched, st));
   if (side) {
     if (cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess)
       return fail(MOE_ERR_CUDA, "joining the side stream failed");

@@ -19,6 +19,7 @@ enum : int {
   DEVERR_BAD_SLOT = 3,        // a slot outside [0, N)
   DEVERR_BAD_OFFSETS = 4,     // offsets not monotone or not ending at N
   DEVERR_SMEM_ALIGN = 5,      // dynamic shared memory not 1024-byte aligned
+  DEVERR_BAD_TOKEN = 6,       // a gathered row (token index) outside [0, T)
 };
 
 __device__ __forceinline__ void record_error(int* err, int code) {

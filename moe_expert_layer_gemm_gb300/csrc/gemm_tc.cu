@@ -160,6 +160,8 @@ struct KArgs {
   int64_t ld_aux;
   const float* bias;
   int* tile_ctr;    // run-time scheduling: the next unclaimed tile (zeroed before the launch)
+  const int32_t* gather;   // gathered operand: source row of each operand row
+  int gather_rows;         // rows of the gathered source tensor
   int* err;
 };
 
@@ -245,7 +247,7 @@ __device__ __forceinline__ void slab_store_3d(const CUtensorMap* m, const uint8_
   }
 }
 
-template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI>
+template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, bool GATHER = false>
 __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
@@ -257,6 +259,9 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
   constexpr bool MC = McMode<SCHED, EPI>::on;
   constexpr bool DYN = DynMode<SCHED, EPI>::on;
   static_assert(!MC || BN % 128 == 0, "cluster pairs split B in 128-row halves");
+  // gathered operands: A of a row-ragged product (K-major) or B of a weight gradient (MN-major)
+  static_assert(!GATHER || (!MC && ((SCHED == RAGGED_M && !A_MN) || (SCHED == RAGGED_K && B_MN))),
+                "unsupported gathered operand");
   constexpr int TM = MC ? 2 * BM : BM;   // rows of one walker tile (a CTA, or a cluster pair)
   using S = Sched<BN, SCHED, EPI, TM>;
   constexpr int STAGES = C::STAGES;
@@ -382,7 +387,123 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  if (warp == 0) {
+  if (warp == 0 && GATHER) {
+    // ------------------------------------------------------------ TMA producer, gathered rows
+    // "Megatron-Bridge 深度剖析", §Permute Fusion: the permutation is folded into the operand
+    // load.  The whole warp issues: lane 0 waits on the ring, arms each stage and loads the
+    // plain operand; every lane gathers four of the gathered operand's rows per copy
+    // (tile::gather4).  Rows past the operand's end read row 0 (their products are masked or
+    // multiplied by zeroed rows).
+    int stage = 0;
+    uint32_t phase = 0;
+    int armed[STAGES];
+    for (int i = 0; i < STAGES; ++i) armed[i] = -1;
+    bool ok = true;
+    const int lim = SCHED == RAGGED_M ? p.M : p.K;   // operand rows
+    auto src_row = [&](int s) -> int {
+      if (s < 0 || s >= lim) return 0;
+      const int r = __ldg(p.gather + s);
+      if (r < 0 || r >= p.gather_rows) {
+        record_error(p.err, DEVERR_BAD_TOKEN);
+        return 0;
+      }
+      return r;
+    };
+    auto claim = [&]() -> int {
+      const int t = atomicAdd(p.tile_ctr, 1);
+      return t < total ? t : -1;
+    };
+    int fslot = 0;
+    uint32_t fphase = 0;
+    int next = (DYN && lane == 0) ? claim() : unit;
+    for (int it = 0; ok; ++it) {
+      int tile;
+      if (DYN) {
+        bool w = true;
+        if (lane == 0) {
+          w = ptx::mbar_wait(&feed_empty[fslot], fphase ^ 1u, abort_flag, p.err);
+          if (w) {
+            s_feed[fslot] = next;
+            ptx::mbar_arrive(&feed_full[fslot]);
+          }
+        }
+        w = __shfl_sync(0xffffffffu, w, 0);
+        tile = __shfl_sync(0xffffffffu, next, 0);
+        if (!w) { ok = false; break; }
+        if (++fslot == FEED) { fslot = 0; fphase ^= 1u; }
+        if (tile < 0) break;
+        if (lane == 0) next = claim();
+      } else {
+        tile = unit + it * units;
+        if (tile >= total) break;
+      }
+      const TileInfo ti = S::decode(p, s_off, s_pre, s_ord, tile);
+      // row-ragged: lane j owns rows 4j..4j+3 of the 128-row A tile for the whole tile
+      int ar[4] = {0, 0, 0, 0};
+      if (SCHED == RAGGED_M) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ar[i] = src_row(ti.m0 + 4 * lane + i);
+      }
+      for (int kb = 0; kb < ti.kblocks; ++kb) {
+        const int kk = ti.k0 + kb * BK;
+        // weight gradient: lane j owns k-rows 4q..4q+3 (q = j mod 16) of this k-block, in the
+        // 64-column chunks j/16, j/16 + 2, ...
+        int br[4] = {0, 0, 0, 0};
+        if (SCHED == RAGGED_K) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) br[i] = src_row(kk + 4 * (lane & 15) + i);
+        }
+        bool w = true;
+        if (lane == 0) {
+          w = ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err);
+          if (w) {
+            ptx::mbar_arrive_expect_tx(&full[stage], STAGE_TX);
+            armed[stage] = static_cast<int>(phase);
+          }
+        }
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (!w) { ok = false; break; }
+        uint8_t* a_dst = sA + stage * A_STAGE;
+        uint8_t* b_dst = sB + stage * C::B_STAGE;
+        if (SCHED == RAGGED_M) {
+          ptx::tma_gather4_2d(a_dst + lane * 512, &tmA, &full[stage], kk, ar[0], ar[1], ar[2], ar[3]);
+          if (lane == 0) {
+            const int brow = static_cast<int>(ti.g * p.b_group_rows) + ti.n0;
+            if (EPI == EPI_SWIGLU_FWD) {
+              ptx::tma_load_2d(b_dst, &tmB, &full[stage], kk, brow);
+              ptx::tma_load_2d(b_dst + (BN / 2) * 128, &tmB, &full[stage], kk,
+                               brow + static_cast<int>(p.b_up_rows));
+            } else {
+              ptx::tma_load_2d(b_dst, &tmB, &full[stage], kk, brow);
+            }
+          }
+        } else {
+          if (lane == 0) {
+#pragma unroll
+            for (int c = 0; c < BM / 64; ++c)
+              ptx::tma_load_2d(a_dst + c * (BK * 128), &tmA, &full[stage], ti.m0 + 64 * c, kk);
+          }
+          const int q = lane & 15;
+#pragma unroll
+          for (int c = lane >> 4; c < BN / 64; c += 2)
+            ptx::tma_gather4_2d(b_dst + c * (BK * 128) + q * 512, &tmB, &full[stage],
+                                ti.n0 + 64 * c, br[0], br[1], br[2], br[3]);
+        }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok && lane == 0) {
+      // Unwinding: let every copy of an armed stage land before the CTA exits.
+      for (int i = 0; i < STAGES; ++i) {
+        if (armed[i] < 0) continue;
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(&full[i], static_cast<uint32_t>(armed[i])) &&
+               ptx::globaltimer() - t0 < 100000000ull) {
+        }
+      }
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int stage = 0;
@@ -990,12 +1111,12 @@ int map_operand(CUtensorMap* m, const Operand& op, int box_rows) {
   return map_bf16(m, op.base, op.rows, op.cols, op.ld, box_rows);
 }
 
-template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI>
+template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, bool GATHER = false>
 int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   const char* name = g.name ? g.name : kind;
   constexpr bool TMA_OUT = OutPath<SCHED, EPI>::tma;
   using C = TileCfg<BN, TMA_OUT, EpiWidth<BN, SCHED, EPI>::warps, EpiWidth<BN, SCHED, EPI>::slabs>;
-  auto kern = tc_gemm_kernel<BN, A_MN, B_MN, SCHED, EPI>;
+  auto kern = tc_gemm_kernel<BN, A_MN, B_MN, SCHED, EPI, GATHER>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [&] {
@@ -1007,9 +1128,12 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   }
   CUtensorMap ma, mb, mo[3];
   memset(mo, 0, sizeof(mo));
-  MOE_TRY(map_operand(&ma, g.A, A_MN ? BK : BM));
+  // gathered operands are read one row per box (four rows per tile::gather4 copy)
+  MOE_TRY(map_operand(&ma, g.A, (GATHER && SCHED == RAGGED_M) ? 1 : (A_MN ? BK : BM)));
   MOE_TRY(map_operand(&mb, g.B,
-                      B_MN ? BK : ((EPI == EPI_SWIGLU_FWD || McMode<SCHED, EPI>::on) ? BN / 2 : BN)));
+                      (GATHER && SCHED == RAGGED_K) ? 1
+                      : B_MN ? BK
+                             : ((EPI == EPI_SWIGLU_FWD || McMode<SCHED, EPI>::on) ? BN / 2 : BN)));
   const int64_t rows = g.M;   // RAGGED_M: rows of the output (capacity)
   if (EPI == EPI_STORE) {
     MOE_TRY(map_bf16(&mo[0], g.out, rows, g.N, g.ldo, 32));
@@ -1044,7 +1168,13 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   a.ld_aux = g.ld_aux;
   a.bias = g.bias;
   a.tile_ctr = g.tile_ctr;
+  a.gather = g.gather;
+  a.gather_rows = static_cast<int>(SCHED == RAGGED_M ? g.A.rows : g.B.rows);
   a.err = device_error_word();
+  if (GATHER != (g.gather != nullptr)) {
+    set_error("%s: gathered-operand instantiation does not match the descriptor", name);
+    return MOE_ERR_INVALID_ARG;
+  }
   if (DynMode<SCHED, EPI>::on) {
     if (!g.tile_ctr) {
       set_error("%s: run-time tile scheduling needs its counter (GemmDesc.tile_ctr)", name);
@@ -1071,7 +1201,12 @@ int gemm_tc(const GemmDesc& g, cudaStream_t st) {
   }
   if (g.sched == RAGGED_M && !g.A.mn_major) {
     if (g.epi == EPI_SWIGLU_FWD && !g.B.mn_major)
-      return run<256, false, false, RAGGED_M, EPI_SWIGLU_FWD>(g, "gemm_fc1_swiglu", st);
+      return g.gather ? run<256, false, false, RAGGED_M, EPI_SWIGLU_FWD, true>(g, "gemm_fc1_swiglu", st)
+                      : run<256, false, false, RAGGED_M, EPI_SWIGLU_FWD>(g, "gemm_fc1_swiglu", st);
+    if (g.gather) {
+      set_error("gemm_tc: a gathered A operand is supported for fc1 + SwiGLU only");
+      return MOE_ERR_UNSUPPORTED;
+    }
     // Output tiles of 192 or 256 columns, whichever pads the product's width less (e.g.
     // d = 2688 is 14 x 192, f = 1856 is 10 x 192 - 64 but 8 x 256 - 192); ties take 256.
     const int ncols = g.epi == EPI_SWIGLU_BWD ? g.f : g.N;
@@ -1091,7 +1226,8 @@ int gemm_tc(const GemmDesc& g, cudaStream_t st) {
     }
   }
   if (g.sched == RAGGED_K && g.A.mn_major && g.B.mn_major && g.epi == EPI_F32)
-    return run<256, true, true, RAGGED_K, EPI_F32>(g, "gemm_wgrad", st);
+    return g.gather ? run<256, true, true, RAGGED_K, EPI_F32, true>(g, "gemm_wgrad", st)
+                    : run<256, true, true, RAGGED_K, EPI_F32>(g, "gemm_wgrad", st);
   set_error("gemm_tc: unsupported combination sched=%d epi=%d a_mn=%d b_mn=%d", g.sched, g.epi,
             (int)g.A.mn_major, (int)g.B.mn_major);
   return MOE_ERR_UNSUPPORTED;

@@ -109,6 +109,20 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* desc, ui
       : "memory");
 }
 
+// Four rows of a 2-D tensor, gathered: rows r0..r3 (any order, any rows) at columns
+// [c0, c0 + box width) land as four consecutive box rows at smem_dst, swizzled by their shared
+// memory address like any tiled load.  The tensor map's box is one row high.
+__device__ __forceinline__ void tma_gather4_2d(void* smem_dst, const void* desc, uint64_t* bar,
+                                               int32_t c0, int32_t r0, int32_t r1, int32_t r2,
+                                               int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(desc)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1),
+      "r"(r2), "r"(r3)
+      : "memory");
+}
+
 // Tiled stores from shared memory (bulk-async group); clipped at the tensor bounds.
 __device__ __forceinline__ void tma_store_2d(const void* desc, const void* smem_src, int32_t c0,
                                              int32_t c1) {

@@ -52,7 +52,8 @@ def test_layer_is_deterministic():
     for n in ["y", "dx", "dW_r", "dW1", "dW2", "dWs1", "dWs2"]:
         assert torch.equal(a[n], b[n]), n
     for n in ["idx", "gate", "offsets", "slot_of_pair", "x_perm", "act", "h", "y_perm"]:
-        assert torch.equal(a["saved"][n], b["saved"][n]), n
+        if a["saved"][n] is not None:
+            assert torch.equal(a["saved"][n], b["saved"][n]), n
 
 
 def test_empty_experts_get_zero_weight_gradients():

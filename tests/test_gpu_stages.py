@@ -110,3 +110,55 @@ def test_combine_and_backward(shared):
         assert_close("dshared", np64(dso), c[:, None] * DY, 1e-2)
     if shared == 2:
         assert_close("dcoef", np64(dc), (DY * np64(so)).sum(1), 1e-3)
+
+
+@pytest.mark.parametrize("T,d,E,k,f", [(600, 256, 8, 2, 136), (1000, 384, 32, 6, 200),
+                                       (77, 128, 4, 3, 64)])
+def test_gathered_stages_equal_permute_then_stage(T, d, E, k, f):
+    """The permutation folded into the operand loads (rows of x gathered by token_of_slot):
+    bit-identical to moe_permute followed by the x_perm stage calls, and within the bf16
+    tolerance of the oracle."""
+    r = routed(T, E, k, 11)
+    N = T * k
+    cfg = moe.make_cfg(T, d, E, k, f)
+    g = torch.Generator().manual_seed(13)
+    x = torch.randn(T, d, generator=g).bfloat16().cuda()
+    W1 = (torch.randn(E, 2 * f, d, generator=g) * 0.05).bfloat16().cuda()
+    W2 = (torch.randn(E, d, f, generator=g) * 0.05).bfloat16().cuda()
+    dyp = torch.randn(N, d, generator=g).bfloat16().cuda()
+    off = torch.from_numpy(r["offsets"]).cuda()
+    sop = torch.from_numpy(r["slot_of_pair"]).cuda()
+    tos = torch.from_numpy(r["token_of_slot"]).cuda()
+    bf = torch.bfloat16
+
+    def run(gathered):
+        h = torch.empty(N, f, dtype=bf, device="cuda")
+        act = torch.empty(N, 2 * f, dtype=bf, device="cuda")
+        yp = torch.empty(N, d, dtype=bf, device="cuda")
+        dxp = torch.empty(N, d, dtype=bf, device="cuda")
+        dW1 = torch.empty(E, 2 * f, d, device="cuda")
+        dW2 = torch.empty(E, d, f, device="cuda")
+        ws = moe.workspace(cfg, moe.WS_FFN_BWD)
+        if gathered:
+            moe.moe_grouped_swiglu_fwd_gathered(cfg, x, tos, off, W1, W2, h, act, yp)
+            moe.moe_grouped_swiglu_bwd_gathered(cfg, x, tos, off, W1, W2, act, h, dyp, dxp, dW1,
+                                                dW2, ws)
+        else:
+            xp = torch.empty(N, d, dtype=bf, device="cuda")
+            moe.moe_permute(cfg, x, sop, xp)
+            moe.moe_grouped_swiglu_fwd(cfg, xp, off, W1, W2, h, act, yp)
+            moe.moe_grouped_swiglu_bwd(cfg, xp, off, W1, W2, act, h, dyp, dxp, dW1, dW2, ws)
+        torch.cuda.synchronize()
+        moe.check_device_error()
+        return dict(h=h, act=act, yp=yp, dxp=dxp, dW1=dW1, dW2=dW2)
+
+    a, b = run(True), run(False)
+    for n in a:
+        assert torch.equal(a[n], b[n]), n
+    X = np64(x)[r["token_of_slot"]]
+    o = r["offsets"]
+    ref_y = np.zeros((N, d))
+    for e in range(E):
+        sl = slice(o[e], o[e + 1])
+        ref_y[sl] = O.swiglu_ffn(np64(W1[e]), np64(W2[e]), X[sl])[0]
+    assert_close("y_perm", np64(a["yp"]), ref_y, 2e-2)
