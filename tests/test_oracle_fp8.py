@@ -92,9 +92,12 @@ def test_quantised_swiglu_equals_library_on_representable_operands(shift):
     X = torch.from_numpy(x)
     for e in range(E):
         lo, hi = offsets[e], offsets[e + 1]
+        if hi == lo:
+            continue
         au = X[lo:hi] @ torch.from_numpy(W1[e]).T
         ref_h = torch.nn.functional.silu(au[:, :f]) * au[:, f:]
-        assert np.allclose(h[lo:hi], ref_h.numpy(), rtol=1e-12, atol=0)
+        ref = ref_h.numpy()
+        assert np.abs(h[lo:hi] - ref).max() <= 1e-12 * np.abs(ref).max()
         Hd = torch.from_numpy(F8.dequantize(hq, sh)[lo:hi])
         assert np.allclose(y[lo:hi], (Hd @ torch.from_numpy(W2[e]).T).numpy(), rtol=1e-12, atol=0)
 
