@@ -192,6 +192,33 @@ int moe_grouped_swiglu_bwd_gathered(const moe_cfg* cfg, const void* x,
                                     float* dW1, float* dW2, void* ws, size_t ws_bytes,
                                     void* stream);
 
+/* E4M3 tensorwise quantisation ("Megatron-Bridge 深度剖析", §FP8 训练: FP8 E4M3 with the
+ * "tensorwise" scaling recipe; the pages give no formula, this is the plain reading).  x holds
+ * `groups` consecutive tensors of elems_per_group bf16 values each (an activation matrix is one
+ * group; W1 [E,2f,d] is E groups of 2f*d).  Per group:
+ *   amax[g] = max |x|;  q = E4M3(x * (448 / amax))  (fp32 quotient and product, round to nearest
+ *   even, saturating to +-448; the sign of zero kept);  scale[g] = amax / 448 (dequantisation).
+ * amax = 0 gives inv = scale = 1.  q: uint8 codes, same layout as x; scale, amax: fp32 [groups]
+ * (amax is scratch that also returns the maxima).  elems_per_group must be a multiple of 16.
+ * No moe_cfg: the call only needs the sizes. */
+int moe_quantize_e4m3(const void* x, int64_t elems_per_group, int32_t groups, uint8_t* q,
+                      float* scale, float* amax, void* stream);
+
+/* Grouped SwiGLU forward on E4M3 operands ("Megatron-Bridge 深度剖析", §FP8 训练: FP8 doubles the
+ * tensor-core rate and halves the bytes of the 128-expert grouped GEMM).  For rows s of expert e:
+ *   [a | u] = x_scale * W1_scale[e] * (dec(x_perm_q[s]) . dec(W1_q[e])^T)   (fp32 accumulation)
+ *   h = SiLU(a) * u  (bf16, and [a | u] in act unless NULL);  h is quantised as one tensor
+ *   (moe_quantize_e4m3) into h_q, h_scale[0] (h_amax[0]: its amax);
+ *   y_perm[s] = h_scale * W2_scale[e] * (dec(h_q[s]) . dec(W2_q[e])^T)  (bf16).
+ * x_perm_q [N,d], W1_q [E,2f,d], W2_q [E,d,f]: uint8 E4M3 codes from moe_quantize_e4m3 (W1_q and
+ * W2_q with E groups, x_perm_q with one); scales fp32 device values.  d and f must be multiples
+ * of 16; cfg->dtype must be MOE_DTYPE_BF16.  Forward only (the backward stays bf16). */
+int moe_grouped_swiglu_fwd_fp8(const moe_cfg* cfg, const uint8_t* x_perm_q, const float* x_scale,
+                               const int32_t* offsets, const uint8_t* W1_q, const float* W1_scale,
+                               const uint8_t* W2_q, const float* W2_scale, void* h, void* act,
+                               uint8_t* h_q, float* h_scale, float* h_amax, void* y_perm,
+                               void* stream);
+
 /* Unpermute + weighted combine: "Megatron-Bridge 深度剖析", §Expert Parallel 基础 (Step 3,
  * results sent back to token order) and §Shared Expert Overlap (shared output added).
  *   y[t] = sum_{j<k} gate[t,j] * y_perm[slot_of_pair[t,j]]  (+ c_t * shared_out[t])

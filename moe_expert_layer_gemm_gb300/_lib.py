@@ -47,8 +47,10 @@ _SIGS = {
     "moe_permute": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP]),
     "moe_grouped_swiglu_fwd": (ctypes.c_int, [_CFG] + [_VP] * 8 + [_SZ, _VP]),
     "moe_grouped_swiglu_bwd": (ctypes.c_int, [_CFG] + [_VP] * 11 + [_SZ, _VP]),
-    "moe_grouped_swiglu_fwd_gathered": (ctypes.c_int, [_CFG] + [_VP] * 8 + [_SZ, _VP]),
-    "moe_grouped_swiglu_bwd_gathered": (ctypes.c_int, [_CFG] + [_VP] * 11 + [_SZ, _VP]),
+    "moe_grouped_swiglu_fwd_gathered": (ctypes.c_int, [_CFG] + [_VP] * 9 + [_SZ, _VP]),
+    "moe_grouped_swiglu_bwd_gathered": (ctypes.c_int, [_CFG] + [_VP] * 12 + [_SZ, _VP]),
+    "moe_quantize_e4m3": (ctypes.c_int, [_VP, ctypes.c_int64, ctypes.c_int32, _VP, _VP, _VP, _VP]),
+    "moe_grouped_swiglu_fwd_fp8": (ctypes.c_int, [_CFG] + [_VP] * 14),
     "moe_unpermute_combine": (ctypes.c_int, [_CFG] + [_VP] * 7),
     "moe_unpermute_combine_bwd": (ctypes.c_int, [_CFG] + [_VP] * 11),
     "moe_layer_fwd": (ctypes.c_int, [_CFG] + [_VP] * 9 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP]),
@@ -184,6 +186,20 @@ def moe_grouped_swiglu_bwd_gathered(cfg, x, token_of_slot, offsets, W1, W2, act,
         ctypes.byref(cfg), _p(x), _p(token_of_slot), _p(offsets), _p(W1), _p(W2), _p(act), _p(h),
         _p(dy_perm), _p(dx_perm), _p(dW1), _p(dW2), _p(ws), 0 if ws is None else ws.numel(),
         _stream(stream)), "moe_grouped_swiglu_bwd_gathered")
+
+
+def moe_quantize_e4m3(x, groups, q, scale, amax, stream=None):
+    """E4M3 codes (uint8 tensor shaped like x) and per-group scales of the bf16 tensor x."""
+    _check(lib().moe_quantize_e4m3(_p(x), x.numel() // groups, groups, _p(q), _p(scale), _p(amax),
+                                   _stream(stream)), "moe_quantize_e4m3")
+
+
+def moe_grouped_swiglu_fwd_fp8(cfg, x_perm_q, x_scale, offsets, W1_q, W1_scale, W2_q, W2_scale, h,
+                               act, h_q, h_scale, h_amax, y_perm, stream=None):
+    _check(lib().moe_grouped_swiglu_fwd_fp8(
+        ctypes.byref(cfg), _p(x_perm_q), _p(x_scale), _p(offsets), _p(W1_q), _p(W1_scale),
+        _p(W2_q), _p(W2_scale), _p(h), _p(act), _p(h_q), _p(h_scale), _p(h_amax), _p(y_perm),
+        _stream(stream)), "moe_grouped_swiglu_fwd_fp8")
 
 
 def moe_unpermute_combine(cfg, y_perm, gate, slot_of_pair, shared_out, shared_coef, y, stream=None):

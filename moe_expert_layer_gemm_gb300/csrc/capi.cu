@@ -713,6 +713,93 @@ int moe_grouped_swiglu_bwd_gathered(const moe_cfg* c, const void* x,
                       dW1, dW2, sched, st, token_of_slot, c->T);
 }
 
+int moe_quantize_e4m3(const void* x, int64_t elems_per_group, int32_t groups, uint8_t* q,
+                      float* scale, float* amax, void* stream) {
+  if (groups < 1 || elems_per_group < 0)
+    return fail(MOE_ERR_INVALID_ARG, "groups=%d elems_per_group=%lld", groups,
+                static_cast<long long>(elems_per_group));
+  if (elems_per_group % 16)
+    return fail(MOE_ERR_UNSUPPORTED, "elems_per_group must be a multiple of 16");
+  MOE_TRY(check_ptr(x, "x", true));
+  MOE_TRY(check_ptr(q, "q", true));
+  MOE_TRY(check_ptr(scale, "scale", true));
+  MOE_TRY(check_ptr(amax, "amax", true));
+  return launch_quantize_e4m3(x, elems_per_group, groups, q, scale, amax, S(stream));
+}
+
+int moe_grouped_swiglu_fwd_fp8(const moe_cfg* c, const uint8_t* x_perm_q, const float* x_scale,
+                               const int32_t* offsets, const uint8_t* W1_q, const float* W1_scale,
+                               const uint8_t* W2_q, const float* W2_scale, void* h, void* act,
+                               uint8_t* h_q, float* h_scale, float* h_amax, void* y_perm,
+                               void* stream) {
+  MOE_TRY(check_cfg(c));
+  if (c->dtype != MOE_DTYPE_BF16)
+    return fail(MOE_ERR_UNSUPPORTED, "the FP8 path writes bf16 activations (dtype bf16)");
+  if (c->d % 16 || c->f % 16)
+    return fail(MOE_ERR_UNSUPPORTED, "FP8 rows need d and f multiples of 16 (16-byte rows)");
+  MOE_TRY(check_ptr(x_perm_q, "x_perm_q", true));
+  MOE_TRY(check_ptr(x_scale, "x_scale", true));
+  MOE_TRY(check_ptr(offsets, "offsets", true));
+  MOE_TRY(check_ptr(W1_q, "W1_q", true));
+  MOE_TRY(check_ptr(W1_scale, "W1_scale", true));
+  MOE_TRY(check_ptr(W2_q, "W2_q", true));
+  MOE_TRY(check_ptr(W2_scale, "W2_scale", true));
+  MOE_TRY(check_ptr(h, "h", true));
+  MOE_TRY(check_ptr(act, "act", false));
+  MOE_TRY(check_ptr(h_q, "h_q", true));
+  MOE_TRY(check_ptr(h_scale, "h_scale", true));
+  MOE_TRY(check_ptr(h_amax, "h_amax", true));
+  MOE_TRY(check_ptr(y_perm, "y_perm", true));
+  cudaStream_t st = S(stream);
+  const int64_t N = Nrows(c);
+  if (N == 0) return MOE_OK;
+  const int d = c->d, f = c->f, E = c->E;
+  // fc1 + SwiGLU on E4M3 operands -> h, [a | u] (bf16)
+  GemmDesc g1 = desc0();
+  g1.name = "gemm_fc1_swiglu_fp8";
+  g1.sched = RAGGED_M;
+  g1.epi = EPI_SWIGLU_FWD;
+  g1.G = E;
+  g1.offsets = offsets;
+  g1.M = static_cast<int>(N);
+  g1.N = 2 * f;
+  g1.K = d;
+  g1.A = opnd(x_perm_q, N, d, false);
+  g1.B = opnd(W1_q, static_cast<int64_t>(E) * 2 * f, d, false);
+  g1.b_group_rows = 2 * f;
+  g1.b_up_rows = f;
+  g1.f = f;
+  g1.out = h;
+  g1.ldo = f;
+  g1.out2 = act;
+  g1.ldo2 = 2 * f;
+  g1.fp8 = true;
+  g1.a_scale = x_scale;
+  g1.b_scale = W1_scale;
+  MOE_TRY(gemm_tc(g1, st));
+  // h -> E4M3 (one tensor)
+  MOE_TRY(launch_quantize_e4m3(h, N * f, 1, h_q, h_scale, h_amax, st));
+  // fc2 on E4M3 operands -> y_perm (bf16)
+  GemmDesc g2 = desc0();
+  g2.name = "gemm_fc2_fp8";
+  g2.sched = RAGGED_M;
+  g2.epi = EPI_STORE;
+  g2.G = E;
+  g2.offsets = offsets;
+  g2.M = static_cast<int>(N);
+  g2.N = d;
+  g2.K = f;
+  g2.A = opnd(h_q, N, f, false);
+  g2.B = opnd(W2_q, static_cast<int64_t>(E) * d, f, false);
+  g2.b_group_rows = d;
+  g2.out = y_perm;
+  g2.ldo = d;
+  g2.fp8 = true;
+  g2.a_scale = h_scale;
+  g2.b_scale = W2_scale;
+  return gemm_tc(g2, st);
+}
+
 int moe_unpermute_combine(const moe_cfg* c, const void* y_perm, const float* gate,
                           const int32_t* slot_of_pair, const void* shared_out,
                           const float* shared_coef, void* y, void* stream) {

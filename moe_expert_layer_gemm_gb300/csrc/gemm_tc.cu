@@ -162,6 +162,8 @@ struct KArgs {
   int* tile_ctr;    // run-time scheduling: the next unclaimed tile (zeroed before the launch)
   const int32_t* gather;   // gathered operand: source row of each operand row
   int gather_rows;         // rows of the gathered source tensor
+  const float* a_scale;    // FP8: dequantisation scale of A (one value)
+  const float* b_scale;    // FP8: dequantisation scale of B, one per group
   int* err;
 };
 
@@ -171,7 +173,7 @@ struct TileInfo {
 
 __device__ __forceinline__ float silu_f(float a) { return a / (1.0f + __expf(-a)); }
 
-template <int BN, int SCHED, int EPI, int TBM = BM>
+template <int BN, int SCHED, int EPI, int TBM = BM, int BKE = BK>
 struct Sched {
   // Number of output column tiles.
   __device__ static int n_tiles(const KArgs& p) {
@@ -213,7 +215,7 @@ struct Sched {
       ti.k0 = s_off[ti.g];
       ti.k_end = s_off[ti.g + 1];
     }
-    ti.kblocks = (ti.k_end - ti.k0 + BK - 1) / BK;
+    ti.kblocks = (ti.k_end - ti.k0 + BKE - 1) / BKE;
     return ti;
   }
 };
@@ -247,7 +249,7 @@ __device__ __forceinline__ void slab_store_3d(const CUtensorMap* m, const uint8_
   }
 }
 
-template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, bool GATHER = false>
+template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, bool GATHER = false, bool F8 = false>
 __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
@@ -263,7 +265,12 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
   static_assert(!GATHER || (!MC && ((SCHED == RAGGED_M && !A_MN) || (SCHED == RAGGED_K && B_MN))),
                 "unsupported gathered operand");
   constexpr int TM = MC ? 2 * BM : BM;   // rows of one walker tile (a CTA, or a cluster pair)
-  using S = Sched<BN, SCHED, EPI, TM>;
+  // K elements per stage: 128-byte rows hold 64 bf16 or 128 E4M3 values
+  constexpr int BKE = F8 ? 2 * BK : BK;
+  using S = Sched<BN, SCHED, EPI, TM, BKE>;
+  static_assert(!F8 || (SCHED == RAGGED_M && !A_MN && !B_MN && !GATHER && !MC &&
+                        (EPI == EPI_SWIGLU_FWD || EPI == EPI_STORE)),
+                "FP8 operands: K-major forward products only");
   constexpr int STAGES = C::STAGES;
   constexpr uint32_t STAGE_TX = A_STAGE + C::B_STAGE;
 
@@ -515,7 +522,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
       auto issue = [&](const TileInfo& ti, int kb, int stg) {
         uint8_t* a_dst = sA + stg * A_STAGE;
         uint8_t* b_dst = sB + stg * C::B_STAGE;
-        const int kk = ti.k0 + kb * BK;
+        const int kk = ti.k0 + kb * BKE;
         const int m_cta = ti.m0 + static_cast<int>(rank) * BM;
         const bool live = !(MC && SCHED == RAGGED_M) || m_cta < ti.m_end;
         auto box = [&](void* dst, const CUtensorMap* m, int c0, int c1) {
@@ -612,7 +619,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    constexpr uint32_t IDESC = F8 ? ptx::idesc_e4m3_f32(BM, BN) : ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -670,7 +677,8 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
                                      : ptx::smem_desc_sw128(a_addr + k16 * 32, 16, 1024);
             const uint64_t bd = B_MN ? ptx::smem_desc_sw128(b_addr + k16 * 2048, BK * 128, 1024)
                                      : ptx::smem_desc_sw128(b_addr + k16 * 32, 16, 1024);
-            ptx::umma_bf16(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
+            if (F8) ptx::umma_f8(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
+            else ptx::umma_bf16(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
           }
           // frees the smem stage (in both CTAs of a cluster) when these MMAs finish
           if (MC) ptx::umma_commit_multicast(&empty[stage], 0x3);
@@ -768,6 +776,8 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
       // slab that crosses the end of its expert's rows would overwrite the next expert's: it is
       // written with masked stores instead.
       const bool tma_slab = TMA_OUT && (SCHED == RAGGED_K ? rows_here > 0 : rows_here == 32);
+      // FP8: the accumulator holds products of decoded E4M3 values; both scales apply here
+      const float sc = F8 ? __ldg(p.a_scale) * __ldg(p.b_scale + ti.g) : 1.0f;
       bool aborted = false;
 
       if (rows_here <= 0) {
@@ -787,8 +797,8 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
             float a[8], b[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              a[i] = __uint_as_float(v0[8 * j + i]);
-              b[i] = __uint_as_float(v1[8 * j + i]);
+              a[i] = __uint_as_float(v0[8 * j + i]) * sc;
+              b[i] = __uint_as_float(v1[8 * j + i]) * sc;
             }
             slab_put(slab, lane, j, pack16(a, static_cast<const bf16*>(nullptr)));
             slab_put(slab, lane, 4 + j, pack16(b, static_cast<const bf16*>(nullptr)));
@@ -850,7 +860,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
               float hv[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i)
-                hv[i] = silu_f(__uint_as_float(ga[8 * j + i])) * __uint_as_float(up[8 * j + i]);
+                hv[i] = silu_f(__uint_as_float(ga[8 * j + i]) * sc) * (__uint_as_float(up[8 * j + i]) * sc);
               slab_put(slab, lane, 4 * hf + j, pack16(hv, static_cast<const bf16*>(nullptr)));
             }
           }
@@ -868,7 +878,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
                 for (int j = 0; j < 4; ++j) {
                   float fv[8];
 #pragma unroll
-                  for (int i = 0; i < 8; ++i) fv[i] = __uint_as_float(v[8 * j + i]);
+                  for (int i = 0; i < 8; ++i) fv[i] = __uint_as_float(v[8 * j + i]) * sc;
                   slab_put(s2, lane, 4 * hf + j, pack16(fv, static_cast<const bf16*>(nullptr)));
                 }
               }
@@ -938,8 +948,8 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
               float hv[8], av[8], uv[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
-                av[i] = __uint_as_float(ga[v * 8 + i]);
-                uv[i] = __uint_as_float(up[v * 8 + i]);
+                av[i] = __uint_as_float(ga[v * 8 + i]) * sc;
+                uv[i] = __uint_as_float(up[v * 8 + i]) * sc;
                 hv[i] = silu_f(av[i]) * uv[i];
               }
               st16(hrow + col + v * 8, pack16(hv, static_cast<const bf16*>(nullptr)));
@@ -998,7 +1008,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
                 if (v * 8 >= ncol) break;
                 float fv[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) fv[i] = __uint_as_float(v32[v * 8 + i]);
+                for (int i = 0; i < 8; ++i) fv[i] = __uint_as_float(v32[v * 8 + i]) * sc;
                 st16(o + v * 8, pack16(fv, static_cast<const bf16*>(nullptr)));
               }
             } else {
@@ -1107,16 +1117,25 @@ int map_f32_3d(CUtensorMap* m, const void* base, int64_t G, int64_t rows, int64_
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box);
 }
 
-int map_operand(CUtensorMap* m, const Operand& op, int box_rows) {
-  return map_bf16(m, op.base, op.rows, op.cols, op.ld, box_rows);
+// 8-bit (E4M3) rows x cols with row pitch ld (elements = bytes); box = 128 columns x box_rows.
+int map_u8(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+  cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box);
 }
 
-template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, bool GATHER = false>
+int map_operand(CUtensorMap* m, const Operand& op, int box_rows, bool f8 = false) {
+  return f8 ? map_u8(m, op.base, op.rows, op.cols, op.ld, box_rows)
+            : map_bf16(m, op.base, op.rows, op.cols, op.ld, box_rows);
+}
+
+template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, bool GATHER = false, bool F8 = false>
 int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   const char* name = g.name ? g.name : kind;
   constexpr bool TMA_OUT = OutPath<SCHED, EPI>::tma;
   using C = TileCfg<BN, TMA_OUT, EpiWidth<BN, SCHED, EPI>::warps, EpiWidth<BN, SCHED, EPI>::slabs>;
-  auto kern = tc_gemm_kernel<BN, A_MN, B_MN, SCHED, EPI, GATHER>;
+  auto kern = tc_gemm_kernel<BN, A_MN, B_MN, SCHED, EPI, GATHER, F8>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [&] {
@@ -1129,11 +1148,12 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   CUtensorMap ma, mb, mo[3];
   memset(mo, 0, sizeof(mo));
   // gathered operands are read one row per box (four rows per tile::gather4 copy)
-  MOE_TRY(map_operand(&ma, g.A, (GATHER && SCHED == RAGGED_M) ? 1 : (A_MN ? BK : BM)));
+  MOE_TRY(map_operand(&ma, g.A, (GATHER && SCHED == RAGGED_M) ? 1 : (A_MN ? BK : BM), F8));
   MOE_TRY(map_operand(&mb, g.B,
                       (GATHER && SCHED == RAGGED_K) ? 1
                       : B_MN ? BK
-                             : ((EPI == EPI_SWIGLU_FWD || McMode<SCHED, EPI>::on) ? BN / 2 : BN)));
+                             : ((EPI == EPI_SWIGLU_FWD || McMode<SCHED, EPI>::on) ? BN / 2 : BN),
+                      F8));
   const int64_t rows = g.M;   // RAGGED_M: rows of the output (capacity)
   if (EPI == EPI_STORE) {
     MOE_TRY(map_bf16(&mo[0], g.out, rows, g.N, g.ldo, 32));
@@ -1170,6 +1190,12 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   a.tile_ctr = g.tile_ctr;
   a.gather = g.gather;
   a.gather_rows = static_cast<int>(SCHED == RAGGED_M ? g.A.rows : g.B.rows);
+  a.a_scale = g.a_scale;
+  a.b_scale = g.b_scale;
+  if (F8 && (!g.a_scale || !g.b_scale)) {
+    set_error("%s: FP8 operands need their scales", name);
+    return MOE_ERR_INVALID_ARG;
+  }
   a.err = device_error_word();
   if (GATHER != (g.gather != nullptr)) {
     set_error("%s: gathered-operand instantiation does not match the descriptor", name);
@@ -1197,6 +1223,17 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
 int gemm_tc(const GemmDesc& g, cudaStream_t st) {
   if (g.G < 1 || g.G > MAXG) {
     set_error("gemm_tc: group count %d outside [1, %d]", g.G, MAXG);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (g.fp8) {
+    // E4M3 operands (K-major), forward products only
+    if (g.sched == RAGGED_M && !g.A.mn_major && !g.B.mn_major && !g.gather) {
+      if (g.epi == EPI_SWIGLU_FWD)
+        return run<256, false, false, RAGGED_M, EPI_SWIGLU_FWD, false, true>(g, "gemm_fc1_swiglu_fp8", st);
+      if (g.epi == EPI_STORE)
+        return run<256, false, false, RAGGED_M, EPI_STORE, false, true>(g, "gemm_fc2_fp8", st);
+    }
+    set_error("gemm_tc: FP8 operands are supported for the K-major forward products only");
     return MOE_ERR_UNSUPPORTED;
   }
   if (g.sched == RAGGED_M && !g.A.mn_major) {

@@ -158,6 +158,11 @@ struct GemmDesc {
   // Gathered operand (bf16 only): row s of the operand is row gather[s] of the tensor the
   // Operand describes (A for RAGGED_M, with M rows; B for RAGGED_K, with K rows).  Null: plain.
   const int32_t* gather;
+  // FP8 (E4M3) operands: A and B hold E4M3 codes; the product is scaled by a_scale[0] *
+  // b_scale[g] (dequantisation scales) before the epilogue.
+  bool fp8;
+  const float* a_scale;
+  const float* b_scale;
 };
 
 // Argument checks and the routing stages (capi.cu), for entry points defined elsewhere.
@@ -167,6 +172,10 @@ int route_stages(const moe_cfg* c, const void* x, const void* W_r, const float* 
                  const float* logits_in, float* logits_out, int32_t* idx, float* gate,
                  int32_t* counts, int32_t* offsets, int32_t* slot_of_pair, int32_t* token_of_slot,
                  int32_t* hist, int32_t* base, cudaStream_t st);
+
+// E4M3 tensorwise quantisation of `groups` blocks of per_group bf16 values (fp8.cu).
+int launch_quantize_e4m3(const void* x, int64_t per_group, int groups, uint8_t* q, float* scale,
+                         float* amax, cudaStream_t st);
 
 int gemm_tc(const GemmDesc& g, cudaStream_t st);     // bf16 tcgen05 path (gemm_tc.cu)
 int gemm_simt(const GemmDesc& g, cudaStream_t st);   // fp32 CUDA-core path (gemm_simt.cu)

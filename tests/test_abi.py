@@ -98,3 +98,15 @@ def test_router_variant_entry_points_check_arguments():
     assert L.moe_expert_bias_update(ctypes.byref(c), P, None, ctypes.c_float(1e-3), None) == -1
     assert L.moe_expert_bias_update(ctypes.byref(c), P, P, ctypes.c_float(float("nan")), None) == -1
     assert L.moe_last_error()
+
+
+def test_binding_argument_counts_match_the_header():
+    """Every ctypes signature of the binding takes as many arguments as the header declares."""
+    import re
+    hdr = open(moe._lib.HEADER).read()
+    decls = {m.group(1): m.group(2) for m in re.finditer(
+        r"^\s*(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(([^;]*?)\);", hdr, re.M | re.S)}
+    for name, (_, args) in moe._lib._SIGS.items():
+        assert name in decls, name
+        params = [p for p in (q.strip() for q in decls[name].split(",")) if p and p != "void"]
+        assert len(params) == len(args), (name, len(params), len(args))
