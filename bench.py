@@ -358,6 +358,8 @@ def run_gpu(args, lc):
             dist.destroy_process_group()
         return None
 
+    fp8 = None if args.no_fp8 or lc.dtype != "bf16" else fp8_forward(args, lc, cfg, inp, saved, dev)
+
     # ---- roofline of the dominant kernel (largest share of device time in the timed region)
     peaks, peak_src = load_peaks()
     work = kernel_work(lc)
@@ -424,11 +426,80 @@ def run_gpu(args, lc):
         "gpu_launches": int(launches),
         "clocks": clk,
         "cpu_baseline": cpu,
+        "fp8_forward": fp8,
         "kernels": kern,
     }
     if world > 1:
         dist.destroy_process_group()
     return out
+
+
+# ----------------------------------------------------------------------------- FP8 forward
+
+def fp8_forward(args, lc, cfg, inp, saved, dev):
+    """The routed experts' forward (fc1 + SwiGLU, fc2) in bf16 and in FP8 E4M3 on the same
+    routed rows: FP8 weights quantised once (FP8 parameters), activations quantised every step
+    (x_perm before fc1, h inside the call).  Device time per step with CUDA events."""
+    import torch
+    import moe_expert_layer_gemm_gb300 as moe
+    E, d, f, N = lc.E, lc.d, lc.f, lc.N
+    if d % 16 or f % 16:
+        return None
+    u8, bf = torch.uint8, torch.bfloat16
+    x_perm, off = saved["x_perm"], saved["offsets"]
+    W1q = torch.empty(E, 2 * f, d, dtype=u8, device=dev)
+    W2q = torch.empty(E, d, f, dtype=u8, device=dev)
+    s1, s2, a1, a2 = (torch.empty(max(E, 4), device=dev) for _ in range(4))
+    moe.moe_quantize_e4m3(inp["W1"], E, W1q, s1, a1)
+    moe.moe_quantize_e4m3(inp["W2"], E, W2q, s2, a2)
+    xq = torch.empty(N, d, dtype=u8, device=dev)
+    xs, xa, hs, ha = (torch.empty(4, device=dev) for _ in range(4))
+    h = torch.empty(N, f, dtype=bf, device=dev)
+    act = torch.empty(N, 2 * f, dtype=bf, device=dev)
+    hq = torch.empty(N, f, dtype=u8, device=dev)
+    yp = torch.empty(N, d, dtype=bf, device=dev)
+
+    def bf16_step():
+        moe.moe_grouped_swiglu_fwd(cfg, x_perm, off, inp["W1"], inp["W2"], h, act, yp)
+
+    def fp8_step():
+        moe.moe_quantize_e4m3(x_perm, 1, xq, xs, xa)
+        moe.moe_grouped_swiglu_fwd_fp8(cfg, xq, xs, off, W1q, s1, W2q, s2, h, act, hq, hs, ha, yp)
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    n = max(5, min(args.steps, 50))
+    ms_bf16 = timed(bf16_step, n)
+    moe.trace_read()
+    moe.trace_enable(True)
+    ms_fp8 = timed(fp8_step, n)
+    moe.trace_enable(False)
+    tr = moe.trace_read()
+    moe.check_device_error()
+    flops = 6.0 * N * d * f
+    peaks, src = load_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
+    per = {k: round(ms / c, 4) for k, (c, ms) in tr.items() if c}
+    gemm_ms = per.get("gemm_fc1_swiglu_fp8", 0) + per.get("gemm_fc2_fp8", 0)
+    return {"bf16_ms": round(ms_bf16, 4), "fp8_ms": round(ms_fp8, 4),
+            "speedup": round(ms_bf16 / ms_fp8, 3),
+            "fp8_gemm_tflops": round(flops / (gemm_ms / 1e3) / 1e12, 1) if gemm_ms else None,
+            "fp8_gemm_frac": round(flops / (gemm_ms / 1e3) / 1e12 / fp8_peak, 4) if gemm_ms else None,
+            "fp8_peak": f"{fp8_peak:.1f} TFLOP/s = 2 x {src} bf16_tflops_sustained (nominal ratio)",
+            "kernels_ms": per,
+            "scope": "routed fc1+SwiGLU and fc2 forward; E4M3 weights quantised once, x_perm and h "
+                     "quantised every step (included)"}
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -477,6 +548,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=512)
     ap.add_argument("--ref-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 forward comparison")
     ap.add_argument("--e2e-steps", type=int, default=20)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "native" else args.warmup
