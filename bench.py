@@ -437,9 +437,9 @@ def run_gpu(args, lc):
 # ----------------------------------------------------------------------------- FP8 forward
 
 def fp8_forward(args, lc, cfg, inp, saved, dev):
-    """The routed experts' forward (fc1 + SwiGLU, fc2) in bf16 and in FP8 E4M3 on the same
-    routed rows: FP8 weights quantised once (FP8 parameters), activations quantised every step
-    (x_perm before fc1, h inside the call).  Device time per step with CUDA events."""
+    """Permute + the routed experts' forward (fc1 + SwiGLU, fc2) in bf16 and in FP8 E4M3 on the
+    same routed rows: FP8 weights quantised once (FP8 parameters), activations quantised every
+    step (x with the permute, h inside the call).  Device time per step with CUDA events."""
     import torch
     import moe_expert_layer_gemm_gb300 as moe
     E, d, f, N = lc.E, lc.d, lc.f, lc.N
@@ -459,11 +459,14 @@ def fp8_forward(args, lc, cfg, inp, saved, dev):
     hq = torch.empty(N, f, dtype=u8, device=dev)
     yp = torch.empty(N, d, dtype=bf, device=dev)
 
+    sop = saved["slot_of_pair"]
+
     def bf16_step():
+        moe.moe_permute(cfg, inp["x"], sop, x_perm)
         moe.moe_grouped_swiglu_fwd(cfg, x_perm, off, inp["W1"], inp["W2"], h, act, yp)
 
     def fp8_step():
-        moe.moe_quantize_e4m3(x_perm, 1, xq, xs, xa)
+        moe.moe_permute_quantize_e4m3(cfg, inp["x"], sop, xq, xs, xa)
         moe.moe_grouped_swiglu_fwd_fp8(cfg, xq, xs, off, W1q, s1, W2q, s2, h, act, hq, hs, ha, yp)
 
     def timed(fn, n):
@@ -498,8 +501,9 @@ def fp8_forward(args, lc, cfg, inp, saved, dev):
             "fp8_gemm_frac": round(flops / (gemm_ms / 1e3) / 1e12 / fp8_peak, 4) if gemm_ms else None,
             "fp8_peak": f"{fp8_peak:.1f} TFLOP/s = 2 x {src} bf16_tflops_sustained (nominal ratio)",
             "kernels_ms": per,
-            "scope": "routed fc1+SwiGLU and fc2 forward; E4M3 weights quantised once, x_perm and h "
-                     "quantised every step (included)"}
+            "scope": "permute + routed fc1+SwiGLU and fc2 forward; E4M3 weights quantised once, "
+                     "x (fused with the permute) and h (amax in fc1's epilogue) quantised every "
+                     "step (included)"}
 
 
 # ----------------------------------------------------------------------------- reference arm

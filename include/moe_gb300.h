@@ -204,11 +204,19 @@ int moe_grouped_swiglu_bwd_gathered(const moe_cfg* cfg, const void* x,
 int moe_quantize_e4m3(const void* x, int64_t elems_per_group, int32_t groups, uint8_t* q,
                       float* scale, float* amax, void* stream);
 
+/* Permute + E4M3 quantisation in one pass: amax over x [T,d] (every token is routed k >= 1
+ * times, so it is the permuted matrix's amax too), then x_perm_q[slot_of_pair[t,j]] =
+ * E4M3(x[t] * (448 / amax)) as moe_quantize_e4m3 would give for the permuted bf16 matrix;
+ * x_scale[0] = amax / 448, x_amax[0] = amax.  bf16 x, d a multiple of 16. */
+int moe_permute_quantize_e4m3(const moe_cfg* cfg, const void* x, const int32_t* slot_of_pair,
+                              uint8_t* x_perm_q, float* x_scale, float* x_amax, void* stream);
+
 /* Grouped SwiGLU forward on E4M3 operands ("Megatron-Bridge 深度剖析", §FP8 训练: FP8 doubles the
  * tensor-core rate and halves the bytes of the 128-expert grouped GEMM).  For rows s of expert e:
  *   [a | u] = x_scale * W1_scale[e] * (dec(x_perm_q[s]) . dec(W1_q[e])^T)   (fp32 accumulation)
  *   h = SiLU(a) * u  (bf16, and [a | u] in act unless NULL);  h is quantised as one tensor
- *   (moe_quantize_e4m3) into h_q, h_scale[0] (h_amax[0]: its amax);
+ *   (as moe_quantize_e4m3 does, with its amax taken in fc1's epilogue) into h_q, h_scale[0]
+ *   (h_amax[0]: its amax);
  *   y_perm[s] = h_scale * W2_scale[e] * (dec(h_q[s]) . dec(W2_q[e])^T)  (bf16).
  * x_perm_q [N,d], W1_q [E,2f,d], W2_q [E,d,f]: uint8 E4M3 codes from moe_quantize_e4m3 (W1_q and
  * W2_q with E groups, x_perm_q with one); scales fp32 device values.  d and f must be multiples

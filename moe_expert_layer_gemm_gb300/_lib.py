@@ -51,6 +51,7 @@ _SIGS = {
     "moe_grouped_swiglu_bwd_gathered": (ctypes.c_int, [_CFG] + [_VP] * 12 + [_SZ, _VP]),
     "moe_quantize_e4m3": (ctypes.c_int, [_VP, ctypes.c_int64, ctypes.c_int32, _VP, _VP, _VP, _VP]),
     "moe_grouped_swiglu_fwd_fp8": (ctypes.c_int, [_CFG] + [_VP] * 14),
+    "moe_permute_quantize_e4m3": (ctypes.c_int, [_CFG] + [_VP] * 6),
     "moe_unpermute_combine": (ctypes.c_int, [_CFG] + [_VP] * 7),
     "moe_unpermute_combine_bwd": (ctypes.c_int, [_CFG] + [_VP] * 11),
     "moe_layer_fwd": (ctypes.c_int, [_CFG] + [_VP] * 9 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP]),
@@ -192,6 +193,12 @@ def moe_quantize_e4m3(x, groups, q, scale, amax, stream=None):
     """E4M3 codes (uint8 tensor shaped like x) and per-group scales of the bf16 tensor x."""
     _check(lib().moe_quantize_e4m3(_p(x), x.numel() // groups, groups, _p(q), _p(scale), _p(amax),
                                    _stream(stream)), "moe_quantize_e4m3")
+
+
+def moe_permute_quantize_e4m3(cfg, x, slot_of_pair, x_perm_q, x_scale, x_amax, stream=None):
+    _check(lib().moe_permute_quantize_e4m3(ctypes.byref(cfg), _p(x), _p(slot_of_pair), _p(x_perm_q),
+                                           _p(x_scale), _p(x_amax), _stream(stream)),
+           "moe_permute_quantize_e4m3")
 
 
 def moe_grouped_swiglu_fwd_fp8(cfg, x_perm_q, x_scale, offsets, W1_q, W1_scale, W2_q, W2_scale, h,

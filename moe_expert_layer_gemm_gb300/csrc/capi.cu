@@ -727,6 +727,22 @@ int moe_quantize_e4m3(const void* x, int64_t elems_per_group, int32_t groups, ui
   return launch_quantize_e4m3(x, elems_per_group, groups, q, scale, amax, S(stream));
 }
 
+int moe_permute_quantize_e4m3(const moe_cfg* c, const void* x, const int32_t* slot_of_pair,
+                              uint8_t* x_perm_q, float* x_scale, float* x_amax, void* stream) {
+  MOE_TRY(check_cfg(c));
+  if (c->dtype != MOE_DTYPE_BF16)
+    return fail(MOE_ERR_UNSUPPORTED, "E4M3 quantisation reads bf16 activations");
+  if (c->d % 16) return fail(MOE_ERR_UNSUPPORTED, "d must be a multiple of 16 (16-byte rows)");
+  MOE_TRY(check_ptr(x, "x", true));
+  MOE_TRY(check_ptr(slot_of_pair, "slot_of_pair", true));
+  MOE_TRY(check_ptr(x_perm_q, "x_perm_q", true));
+  MOE_TRY(check_ptr(x_scale, "x_scale", true));
+  MOE_TRY(check_ptr(x_amax, "x_amax", true));
+  if (c->T == 0) return MOE_OK;
+  return launch_permute_quant_e4m3(x, slot_of_pair, x_perm_q, x_scale, x_amax, c->T, c->d, c->k,
+                                   S(stream));
+}
+
 int moe_grouped_swiglu_fwd_fp8(const moe_cfg* c, const uint8_t* x_perm_q, const float* x_scale,
                                const int32_t* offsets, const uint8_t* W1_q, const float* W1_scale,
                                const uint8_t* W2_q, const float* W2_scale, void* h, void* act,
@@ -776,9 +792,12 @@ int moe_grouped_swiglu_fwd_fp8(const moe_cfg* c, const uint8_t* x_perm_q, const 
   g1.fp8 = true;
   g1.a_scale = x_scale;
   g1.b_scale = W1_scale;
+  g1.amax_out = h_amax;   // max |h| taken in fc1's epilogue
+  if (cudaMemsetAsync(h_amax, 0, sizeof(float), st) != cudaSuccess)
+    return fail(MOE_ERR_CUDA, "clearing h_amax failed");
   MOE_TRY(gemm_tc(g1, st));
-  // h -> E4M3 (one tensor)
-  MOE_TRY(launch_quantize_e4m3(h, N * f, 1, h_q, h_scale, h_amax, st));
+  // h -> E4M3 (one tensor) with that amax
+  MOE_TRY(launch_quant_e4m3_given_amax(h, N * f, 1, h_q, h_scale, h_amax, st));
   // fc2 on E4M3 operands -> y_perm (bf16)
   GemmDesc g2 = desc0();
   g2.name = "gemm_fc2_fp8";

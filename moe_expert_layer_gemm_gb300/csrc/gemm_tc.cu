@@ -164,6 +164,7 @@ struct KArgs {
   int gather_rows;         // rows of the gathered source tensor
   const float* a_scale;    // FP8: dequantisation scale of A (one value)
   const float* b_scale;    // FP8: dequantisation scale of B, one per group
+  float* amax_out;         // FP8 fc1: max |h| (fp32 bits, atomically raised; zeroed before)
   int* err;
 };
 
@@ -778,6 +779,11 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
       const bool tma_slab = TMA_OUT && (SCHED == RAGGED_K ? rows_here > 0 : rows_here == 32);
       // FP8: the accumulator holds products of decoded E4M3 values; both scales apply here
       const float sc = F8 ? __ldg(p.a_scale) * __ldg(p.b_scale + ti.g) : 1.0f;
+      // FP8 fc1: max |h| over this warp's stored (bf16) values, for h's own quantisation
+      float hmax = 0.f;
+      auto track = [&](float v) {
+        if (F8 && EPI == EPI_SWIGLU_FWD) hmax = fmaxf(hmax, fabsf(__bfloat162float(__float2bfloat16_rn(v))));
+      };
       bool aborted = false;
 
       if (rows_here <= 0) {
@@ -859,8 +865,10 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
             for (int j = 0; j < 4; ++j) {
               float hv[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
+              for (int i = 0; i < 8; ++i) {
                 hv[i] = silu_f(__uint_as_float(ga[8 * j + i]) * sc) * (__uint_as_float(up[8 * j + i]) * sc);
+                if (col + 32 * hf + 8 * j + i < p.f) track(hv[i]);
+              }
               slab_put(slab, lane, 4 * hf + j, pack16(hv, static_cast<const bf16*>(nullptr)));
             }
           }
@@ -951,6 +959,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
                 av[i] = __uint_as_float(ga[v * 8 + i]) * sc;
                 uv[i] = __uint_as_float(up[v * 8 + i]) * sc;
                 hv[i] = silu_f(av[i]) * uv[i];
+                track(hv[i]);
               }
               st16(hrow + col + v * 8, pack16(hv, static_cast<const bf16*>(nullptr)));
               if (p.out2) {
@@ -1036,6 +1045,10 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
             }
           }
         }
+      }
+      if (F8 && EPI == EPI_SWIGLU_FWD && p.amax_out) {
+        const float m = warp_max(hmax);   // non-negative floats order like their bit patterns
+        if (lane == 0 && m > 0.f) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), __float_as_uint(m));
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -1192,6 +1205,7 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   a.gather_rows = static_cast<int>(SCHED == RAGGED_M ? g.A.rows : g.B.rows);
   a.a_scale = g.a_scale;
   a.b_scale = g.b_scale;
+  a.amax_out = g.amax_out;
   if (F8 && (!g.a_scale || !g.b_scale)) {
     set_error("%s: FP8 operands need their scales", name);
     return MOE_ERR_INVALID_ARG;

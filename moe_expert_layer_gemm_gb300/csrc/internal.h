@@ -163,6 +163,7 @@ struct GemmDesc {
   bool fp8;
   const float* a_scale;
   const float* b_scale;
+  float* amax_out;         // FP8 fc1 + SwiGLU: receives max |h| (zeroed by the caller)
 };
 
 // Argument checks and the routing stages (capi.cu), for entry points defined elsewhere.
@@ -176,6 +177,12 @@ int route_stages(const moe_cfg* c, const void* x, const void* W_r, const float* 
 // E4M3 tensorwise quantisation of `groups` blocks of per_group bf16 values (fp8.cu).
 int launch_quantize_e4m3(const void* x, int64_t per_group, int groups, uint8_t* q, float* scale,
                          float* amax, cudaStream_t st);
+// The cast alone, with amax already computed (e.g. by the producing GEMM's epilogue).
+int launch_quant_e4m3_given_amax(const void* x, int64_t per_group, int groups, uint8_t* q,
+                                 float* scale, const float* amax, cudaStream_t st);
+// amax of x [T,d] and the permuted E4M3 rows x_perm_q[slot_of_pair[t,j]] = E4M3(x[t] * inv).
+int launch_permute_quant_e4m3(const void* x, const int32_t* sop, uint8_t* xq, float* scale,
+                              float* amax, int T, int d, int k, cudaStream_t st);
 
 int gemm_tc(const GemmDesc& g, cudaStream_t st);     // bf16 tcgen05 path (gemm_tc.cu)
 int gemm_simt(const GemmDesc& g, cudaStream_t st);   // fp32 CUDA-core path (gemm_simt.cu)

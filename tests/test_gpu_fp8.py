@@ -97,3 +97,23 @@ def test_fp8_grouped_swiglu_forward(T, d, E, k, f):
     e_q = rel_err(np64(yp), y_bf)
     assert e_q < 0.1, e_q
     print(f"act {e_act:.2e} h {e_h:.2e} y {e_y:.2e}; vs unquantised {e_q:.3f}")
+
+
+@pytest.mark.parametrize("T,d,E,k", [(1000, 256, 16, 4), (4097, 2048, 128, 8), (7, 64, 4, 1)])
+def test_permute_quantize_equals_quantizing_the_permuted_matrix(T, d, E, k):
+    r = routed(T, E, k, T)
+    g = torch.Generator().manual_seed(d)
+    x = (torch.randn(T, d, generator=g) * 3).bfloat16().cuda()
+    cfg = moe.make_cfg(T, d, E, k, 64)
+    sop = torch.from_numpy(r["slot_of_pair"]).cuda()
+    xq = torch.empty(T * k, d, dtype=torch.uint8, device="cuda")
+    xs, xa = torch.empty(4, device="cuda"), torch.empty(4, device="cuda")
+    moe.moe_permute_quantize_e4m3(cfg, x, sop, xq, xs, xa)
+    xp = torch.empty(T * k, d, dtype=torch.bfloat16, device="cuda")
+    moe.moe_permute(cfg, x, sop, xp)
+    q2, s2, a2 = quantize_gpu(xp, 1)
+    torch.cuda.synchronize()
+    moe.check_device_error()
+    assert torch.equal(xq, q2) and xs[0].item() == s2[0].item() and xa[0].item() == a2[0].item()
+    rq, rs = F8.quantize_tensorwise(xp.float().cpu().numpy())
+    assert np.array_equal(xq.cpu().numpy(), rq) and xs[0].item() == rs[0]
