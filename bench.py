@@ -269,8 +269,6 @@ def run_gpu(args, lc):
         except (ValueError, IndexError):
             pass
     clocks = ClockSampler(gpu_index)
-    moe.trace_read()   # drop anything recorded before
-    moe.trace_enable(True)
     launches0 = moe.launch_count()
     barrier()
     torch.cuda.synchronize()
@@ -283,10 +281,29 @@ def run_gpu(args, lc):
     torch.cuda.synchronize()
     barrier()
     launches = moe.launch_count() - launches0
-    moe.trace_enable(False)
-    trace = moe.trace_read()
     clk = clocks.stop()
     ms_total = ev0.elapsed_time(ev1)
+    moe.check_device_error()
+
+    # ---- per-kernel attribution: a second timed region with every launch bracketed by CUDA
+    # events on its stream, the shared expert's side stream off (concurrent kernels would share
+    # the SMs and their event times would overlap); identical results, serial order.
+    n_trace = max(3, min(args.steps, 20))
+    prev_overlap = moe.set_stream_overlap(False)
+    moe.trace_read()   # drop anything recorded before
+    moe.trace_enable(True)
+    torch.cuda.synchronize()
+    tr0 = torch.cuda.Event(enable_timing=True)
+    tr1 = torch.cuda.Event(enable_timing=True)
+    tr0.record(stream)
+    for _ in range(n_trace):
+        step(inp["x"], inp["dy"], y, grads["dx"])
+    tr1.record(stream)
+    torch.cuda.synchronize()
+    moe.trace_enable(False)
+    trace = moe.trace_read()
+    moe.set_stream_overlap(prev_overlap)
+    trace_ms_step = tr0.elapsed_time(tr1) / n_trace
     moe.check_device_error()
     ms_max = ms_total
     if world > 1:
@@ -424,6 +441,10 @@ def run_gpu(args, lc):
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
+        "kernel_trace": {"steps": n_trace, "ms_per_step": round(trace_ms_step, 4),
+                         "shared_overlap": False,
+                         "note": "per-kernel CUDA-event times (roofline, kernels) from this "
+                                 "second timed region, run in serial order"},
         "clocks": clk,
         "cpu_baseline": cpu,
         "fp8_forward": fp8,

@@ -331,6 +331,13 @@ int moe_trace_enable(int on);
 /* Fills up to `cap` entries; returns the number of kernel kinds seen (or < 0 on error). */
 int moe_trace_read(char* names, int name_stride, int* launches, double* total_ms, int cap);
 
+/* Side-stream overlap switch for moe_layer_fwd / moe_layer_bwd ("Megatron-Bridge 深度剖析",
+ * §Shared Expert Overlap): 1 (default) runs the shared expert (and, in the backward, the router's
+ * backward) on a library-owned side stream concurrently with the routed experts; 0 runs
+ * everything on the caller's stream in order (useful for per-kernel timing).  Results are
+ * identical either way.  Process-wide; returns the previous setting. */
+int moe_set_stream_overlap(int on);
+
 /* Library version, major*10000 + minor*100 + patch. */
 int moe_version(void);
 

@@ -66,6 +66,7 @@ _SIGS = {
     "moe_trace_read": (ctypes.c_int, [ctypes.c_char_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                       ctypes.POINTER(ctypes.c_double), ctypes.c_int]),
     "moe_version": (ctypes.c_int, []),
+    "moe_set_stream_overlap": (ctypes.c_int, [ctypes.c_int]),
 }
 
 _lib = None
@@ -285,6 +286,11 @@ def moe_layer_bwd(cfg, dy, x, W_r, W1, W2, Ws1, Ws2, w_sg, saved, dx, dW_r, dW1,
                                _p(Ws2), _p(w_sg), ctypes.byref(st), _p(dx), _p(dW_r), _p(dW1),
                                _p(dW2), _p(dWs1), _p(dWs2), _p(dw_sg), _p(ws), ws.numel(),
                                _stream(stream)), "moe_layer_bwd")
+
+
+def set_stream_overlap(on):
+    """Side-stream overlap of the layer calls on (default) or off; returns the previous setting."""
+    return int(lib().moe_set_stream_overlap(1 if on else 0))
 
 
 def check_device_error(stream=None):

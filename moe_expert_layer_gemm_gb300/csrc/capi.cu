@@ -87,6 +87,10 @@ int num_sms() {
 #define MOE_SHARED_OVERLAP_BWD MOE_SHARED_OVERLAP
 #endif
 
+// Runtime switch (moe_set_stream_overlap): 1 = use the side stream (default), 0 = run the
+// forked work on the caller's stream.
+static std::atomic<int> g_overlap{1};
+
 struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
@@ -487,6 +491,12 @@ using namespace moe;
 extern "C" {
 
 int moe_version(void) { return 101; }
+
+int moe_set_stream_overlap(int on) {
+  const int prev = g_overlap.load();
+  g_overlap.store(on ? 1 : 0);
+  return prev;
+}
 
 const char* moe_last_error(void) { return g_errbuf; }
 
@@ -933,7 +943,7 @@ int moe_layer_fwd(const moe_cfg* c, const void* x, const void* W_r, const float*
   RouteWs w = carve_route(cv, c);
   // The shared expert (and its gate) needs only x: it runs on the side stream while the routed
   // path (routing, permute, grouped SwiGLU) runs on `st`; the combine waits for both.
-  SideStream* side = (sh && MOE_SHARED_OVERLAP_FWD) ? side_stream() : nullptr;
+  SideStream* side = (sh && MOE_SHARED_OVERLAP_FWD && g_overlap.load()) ? side_stream() : nullptr;
   std::unique_lock<std::mutex> side_lk(g_side_mu, std::defer_lock);
   auto shared_fwd = [&](cudaStream_t ss) -> int {
     if (gt) MOE_TRY(launch_shared_gate(c->dtype, x, w_sg, s->s_coef, c->T, c->d, ss));
@@ -1018,7 +1028,7 @@ int moe_layer_bwd(const moe_cfg* c, const void* dy, const void* x, const void* W
                              w.dshared, w.dcoef, T, d, k, st));
   // 2.-6. The routed experts run on `st`; the shared expert and the router's backward (which
   // need only combine-backward outputs) run on the side stream concurrently; dx waits for both.
-  SideStream* side = MOE_SHARED_OVERLAP_BWD ? side_stream() : nullptr;
+  SideStream* side = (MOE_SHARED_OVERLAP_BWD && g_overlap.load()) ? side_stream() : nullptr;
   std::unique_lock<std::mutex> side_lk(g_side_mu, std::defer_lock);
   auto side_work = [&](cudaStream_t ss) -> int {
     // shared expert (one group of all T tokens)
