@@ -118,6 +118,27 @@ def layer_flops(lc, backward=True):
     return fl * (3.0 if backward else 1.0)
 
 
+# ----------------------------------------------------------------------------- ranks
+
+def max_over_ranks(value, device=None):
+    """The largest value over all ranks (a job of replicas is as slow as its slowest one);
+    the value itself on a single rank.  device: where the collective's tensor lives (the
+    rank's GPU under NCCL, the CPU under gloo)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(tokens_per_rank_step, steps, world, ms_max):
+    """Whole-job tokens/s of `world` independent replicas, each running `steps` steps of
+    tokens_per_rank_step tokens, timed by the slowest rank (ms_max)."""
+    return tokens_per_rank_step * steps * world / (ms_max / 1e3)
+
+
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -305,14 +326,9 @@ def run_gpu(args, lc):
     moe.set_stream_overlap(prev_overlap)
     trace_ms_step = tr0.elapsed_time(tr1) / n_trace
     moe.check_device_error()
-    ms_max = ms_total
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms_total, dev)
     ms_step = ms_max / args.steps
-    tokens = lc.T * args.steps * world
-    value = tokens / (ms_max / 1e3)
+    value = replica_throughput(lc.T, args.steps, world, ms_max)
 
     # ---- end-to-end: every step copies its inputs (x, dy) in from pinned host memory and its
     # results (y, dx) out to pinned host memory.  Copies run on a second stream, double-
@@ -359,12 +375,8 @@ def run_gpu(args, lc):
     stream.wait_stream(copy)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = lc.T * e2e_steps * world / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    e2e_value = replica_throughput(lc.T, e2e_steps, world, e2e_ms)
     esz = inp["x"].element_size()
     h2d = 2 * lc.T * lc.d * esz
     d2h = 2 * lc.T * lc.d * esz if lc.backward else lc.T * lc.d * esz
