@@ -281,6 +281,32 @@ def run_gpu(args, lc):
     torch.cuda.synchronize()
     moe.check_device_error()
 
+    # One step captured in a CUDA graph (the library allocates nothing and orders its memsets
+    # and side-stream fork/join on the stream, so the whole step is capturable); the timed
+    # region replays it.  --no-graph times the eager calls instead.
+    graph = None
+    if not args.no_graph:
+        cs = torch.cuda.Stream(device=dev)
+        cs.wait_stream(stream)
+        with torch.cuda.stream(cs):
+            step(inp["x"], inp["dy"], y, grads["dx"])
+        stream.wait_stream(cs)
+        graph = torch.cuda.CUDAGraph()
+        before = moe.launch_count()
+        with torch.cuda.graph(graph):
+            step(inp["x"], inp["dy"], y, grads["dx"])
+        graph_launches = moe.launch_count() - before
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+        moe.check_device_error()
+
+    def timed_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step(inp["x"], inp["dy"], y, grads["dx"])
+
     # ---- device-timed region: inputs resident in HBM
     gpu_index = local
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -297,11 +323,12 @@ def run_gpu(args, lc):
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(args.steps):
-        step(inp["x"], inp["dy"], y, grads["dx"])
+        timed_step()
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    launches = moe.launch_count() - launches0
+    # graph replays launch no host calls: count the captured step's launches per replay
+    launches = (moe.launch_count() - launches0) if graph is None else graph_launches * args.steps
     clk = clocks.stop()
     ms_total = ev0.elapsed_time(ev1)
     moe.check_device_error()
@@ -453,6 +480,7 @@ def run_gpu(args, lc):
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
+        "cuda_graph": graph is not None,
         "kernel_trace": {"steps": n_trace, "ms_per_step": round(trace_ms_step, 4),
                          "shared_overlap": False,
                          "note": "per-kernel CUDA-event times (roofline, kernels) from this "
@@ -586,6 +614,7 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 forward comparison")
+    ap.add_argument("--no-graph", action="store_true", help="time eager calls, not a CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=20)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "native" else args.warmup
