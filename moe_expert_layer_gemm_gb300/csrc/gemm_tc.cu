@@ -1072,6 +1072,460 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
   }
 }
 
+// ---------------------------------------------------------------- weight gradients on CTA pairs
+// The same weight-gradient product (dW_g = A_g^T . B_g over each group's reduction rows, fp32
+// blocks) on 2-SM tensor-core instructions (tcgen05 cta_group::2).  A cluster of two CTAs owns
+// a 256 x 256 output tile: each CTA loads its 128 rows of A and its 128 columns of B per
+// k-block (32 KB instead of 48 KB), and the even CTA issues M = 256, N = 256 MMAs that read
+// both CTAs' shared memory and leave rows 0..127 in its TMEM and rows 128..255 in the other's.
+// Per FLOP, each SM takes in a third fewer operand bytes, and the smaller stages make room for
+// six of them instead of four.
+//
+// Protocol (stage s of the ring, tile t):
+//   * the even CTA's producer claims tiles (heaviest experts first, as the one-CTA kernel) and
+//     hands each to both CTAs' consumers through a feed ring written into both CTAs;
+//   * both producers wait for their own empty[s] (released by the even CTA's MMA commit, which
+//     arrives on both CTAs), then load; the odd CTA's copies count their bytes on the even
+//     CTA's full[s] and it arrives there too (full[s] expects two arrivals);
+//   * a group's last k-block, when it runs past the group's end, is loaded by the odd CTA onto
+//     its own barrier, its rows past the end zeroed, and only then does it arrive on the even
+//     CTA's full[s] (the even CTA zeroes its own rows before issuing);
+//   * the MMAs' commit arrives on tfull in both CTAs; each CTA's epilogue stores its own 128
+//     rows and arrives on the even CTA's tempty, which the MMA warp waits on before reusing an
+//     accumulator.
+// Every wait is bounded (abort flag and error word as in the one-CTA kernel).
+// Build option, off by default: parity-green, but slower on GB300 than the one-CTA kernel
+// (fc1 weight gradient of the 128-expert layer 1.90 -> 2.15 ms).  These products are bound by
+// DRAM (about 7 GB per fc1 launch, 5.1 GB of it the fp32 gradient blocks, at ~4 TB/s of mixed
+// read/write traffic), not by the operand bytes each SM takes in, which is what pairs reduce.
+#ifndef MOE_PAIR_WGRAD
+#define MOE_PAIR_WGRAD 0
+#endif
+
+namespace pairk {
+constexpr int BN2 = 256;                       // output columns per pair tile
+constexpr int HB = BN2 / 2;                    // B columns per CTA
+constexpr int A_ST = BM * BK * 2;              // 16 KB
+constexpr int B_ST = HB * BK * 2;              // 16 KB
+constexpr int EW = 4;                          // epilogue warps
+#ifndef MOE_PAIR_SLABS
+#define MOE_PAIR_SLABS 4
+#endif
+constexpr int SLABS_P = MOE_PAIR_SLABS;        // fp32 stores in flight per epilogue warp
+constexpr int STAGING = EW * SLABS_P * SLAB;   // 32 KB
+constexpr int AUX = 3072;
+constexpr int MAX_SMEM = 232448;
+constexpr int FIT = (MAX_SMEM - STAGING - AUX) / (A_ST + B_ST);
+constexpr int STAGES = FIT < 6 ? FIT : 6;
+constexpr int RING = STAGES * (A_ST + B_ST);
+constexpr int SMEM = RING + STAGING + AUX;
+constexpr int THREADS = 64 + 32 * EW;
+constexpr int TMEM_COLS = 512;                 // two accumulators of 256 fp32 columns
+}  // namespace pairk
+
+__global__ void __launch_bounds__(pairk::THREADS, 1)
+    tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmO0, const KArgs p) {
+  using namespace pairk;
+  using S = Sched<BN2, RAGGED_K, EPI_F32, 2 * BM>;
+  constexpr uint32_t IDESC = ptx::idesc_bf16_f32(2 * BM, BN2, true, true);
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_ST;
+  uint8_t* staging = smem + RING;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING + STAGING);
+  uint64_t* empty = full + STAGES;
+  uint64_t* pfull = empty + STAGES;       // odd CTA: its own copies of a group's last k-block
+  uint64_t* tfull = pfull + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* feed_full = tempty + 2;
+  uint64_t* feed_empty = feed_full + FEED;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(feed_empty + FEED);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* s_bad = reinterpret_cast<int*>(tmem_holder + 2);
+  int* s_off = reinterpret_cast<int*>(tmem_holder + 4);
+  int* s_ord = s_off + (MAXG + 1);
+  volatile int* s_feed = s_ord + (MAXG + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool even = rank == 0;
+
+  if ((ptx::smem_u32(smem) & 1023u) != 0) {   // the same in both CTAs: both return
+    if (threadIdx.x == 0) record_error(p.err, DEVERR_SMEM_ALIGN);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      ptx::mbar_init(&full[i], 2);     // even producer (with the bytes) + odd producer
+      ptx::mbar_init(&empty[i], 1);    // the pair's MMA commit
+      ptx::mbar_init(&pfull[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&tfull[i], 1);
+      ptx::mbar_init(&tempty[i], 2 * EW);   // both CTAs' epilogue warps
+    }
+    for (int i = 0; i < FEED; ++i) {
+      ptx::mbar_init(&feed_full[i], 1);
+      ptx::mbar_init(&feed_empty[i], 2 + 2 * EW);   // even MMA + odd producer + all epilogues
+    }
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
+    int v;
+    if (p.offsets) v = p.offsets[i];
+    else v = static_cast<int>((static_cast<int64_t>(p.K) * i) / p.G);
+    s_off[i] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int bad = (s_off[0] < 0 || s_off[p.G] > p.K) ? 1 : 0;
+    for (int i = 0; i < p.G && !bad; ++i) bad = s_off[i + 1] < s_off[i];
+    *s_bad = bad;
+    if (bad && even) record_error(p.err, DEVERR_BAD_OFFSETS);
+  }
+  // groups by row count, most first (ties: lower index first), identical in both CTAs
+  for (int g = threadIdx.x; g < p.G; g += blockDim.x) {
+    const int n = s_off[g + 1] - s_off[g];
+    int r = 0;
+    for (int h = 0; h < p.G; ++h) {
+      const int m = s_off[h + 1] - s_off[h];
+      r += (m > n || (m == n && h < g)) ? 1 : 0;
+    }
+    s_ord[r] = g;
+  }
+  __syncthreads();
+  if (*s_bad) return;                    // the same decision in both CTAs
+  const int total = S::total(p, nullptr);
+  if (total == 0) return;
+  ptx::cluster_sync();                   // both CTAs' barriers exist before either touches them
+
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(tmem_holder, TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  // the even CTA's barriers as seen from the odd CTA
+  auto even_addr = [&](const void* local) { return ptx::mapa(ptx::smem_u32(local), 0); };
+  // rows of this k-block (counted from its start) that belong to the group, if fewer than BK
+  auto tail_rows = [&](const TileInfo& ti, int kb) {
+    return kb == ti.kblocks - 1 ? ti.k_end - (ti.k0 + kb * BK) : BK;
+  };
+  // zero rows [valid, BK) of this CTA's A block (MN-major: row r of chunk c is 128 bytes)
+  auto zero_tail = [&](uint8_t* a_src, int valid) {
+    const int nbytes = (BK - valid) * 128;
+    for (int c = 0; c < BM / 64; ++c) {
+      uint8_t* base = a_src + c * (BK * 128) + valid * 128;
+      for (int o = lane * 16; o < nbytes; o += 32 * 16)
+        *reinterpret_cast<uint4*>(base + o) = make_uint4(0, 0, 0, 0);
+    }
+    ptx::fence_proxy_async_smem();
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producers
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t pph = 0;                    // odd CTA: parity of each stage's pfull barrier
+    int fslot = 0;
+    uint32_t fphase = 0;
+    bool ok = true;
+    int armed[STAGES];
+    for (int i = 0; i < STAGES; ++i) armed[i] = -1;
+    int tail_pending = -1;               // odd CTA: a pfull stage whose copies may be in flight
+    const int m_off = static_cast<int>(rank) * BM;    // this CTA's rows of the pair tile
+    const int n_off = static_cast<int>(rank) * HB;    // this CTA's columns of B
+    int next = (even && lane == 0) ? atomicAdd(p.tile_ctr, 1) : 0;
+    for (;;) {
+      // -------- the tile: claimed and published by the even CTA, received by the odd one
+      int tile = 0;
+      bool w = true;
+      if (lane == 0) {
+        if (even) {
+          tile = next < total ? next : -1;
+          w = ptx::mbar_wait_cluster(&feed_empty[fslot], fphase ^ 1u, abort_flag, p.err);
+          if (w) {
+            s_feed[fslot] = tile;
+            ptx::st_cluster_u32(ptx::mapa(ptx::smem_u32(const_cast<int*>(&s_feed[fslot])), 1),
+                                static_cast<uint32_t>(tile));
+            ptx::mbar_arrive(&feed_full[fslot]);
+            ptx::mbar_arrive_remote(ptx::mapa(ptx::smem_u32(&feed_full[fslot]), 1));
+            if (tile >= 0) next = atomicAdd(p.tile_ctr, 1);
+          }
+        } else {
+          w = ptx::mbar_wait_cluster(&feed_full[fslot], fphase, abort_flag, p.err);
+          if (w) {
+            tile = s_feed[fslot];
+            ptx::mbar_arrive_remote(even_addr(&feed_empty[fslot]));
+          }
+        }
+      }
+      w = __shfl_sync(0xffffffffu, w, 0);
+      tile = __shfl_sync(0xffffffffu, tile, 0);
+      if (!w) { ok = false; break; }
+      if (++fslot == FEED) { fslot = 0; fphase ^= 1u; }
+      if (tile < 0) break;
+      const TileInfo ti = S::decode(p, s_off, nullptr, s_ord, tile);
+      for (int kb = 0; kb < ti.kblocks; ++kb) {
+        const int kk = ti.k0 + kb * BK;
+        const int valid = tail_rows(ti, kb);
+        const bool tail = valid < BK;
+        uint8_t* a_dst = sA + stage * A_ST;
+        uint8_t* b_dst = sB + stage * B_ST;
+        // (stage release by the MMA commit: CTA-scope waits, as for any tensor-core arrival)
+        if (lane == 0) w = ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err);
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (!w) { ok = false; break; }
+        if (even) {
+          if (lane == 0) {
+            // own bytes, and the odd CTA's unless this is a short last k-block
+            ptx::mbar_arrive_expect_tx(&full[stage], tail ? A_ST + B_ST : 2 * (A_ST + B_ST));
+            armed[stage] = static_cast<int>(phase);
+#pragma unroll
+            for (int c = 0; c < BM / 64; ++c)
+              ptx::tma_load_2d(a_dst + c * (BK * 128), &tmA, &full[stage], ti.m0 + m_off + 64 * c, kk);
+#pragma unroll
+            for (int c = 0; c < HB / 64; ++c)
+              ptx::tma_load_2d(b_dst + c * (BK * 128), &tmB, &full[stage], ti.n0 + n_off + 64 * c, kk);
+          }
+        } else if (!tail) {
+          if (lane == 0) {
+            const uint32_t fb = even_addr(&full[stage]);
+#pragma unroll
+            for (int c = 0; c < BM / 64; ++c)
+              ptx::tma_load_2d_pair(a_dst + c * (BK * 128), &tmA, fb, ti.m0 + m_off + 64 * c, kk);
+#pragma unroll
+            for (int c = 0; c < HB / 64; ++c)
+              ptx::tma_load_2d_pair(b_dst + c * (BK * 128), &tmB, fb, ti.n0 + n_off + 64 * c, kk);
+            // the bytes are ordered by the copies' own completion on full[stage]: this arrival
+            // only counts (a release here would wait for the copies just issued)
+            ptx::mbar_arrive_remote_relaxed(fb);
+          }
+        } else {
+          // short last k-block: land on our own barrier, zero the rows past the group, then
+          // release it to the even CTA
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(&pfull[stage], A_ST + B_ST);
+            tail_pending = stage;
+#pragma unroll
+            for (int c = 0; c < BM / 64; ++c)
+              ptx::tma_load_2d(a_dst + c * (BK * 128), &tmA, &pfull[stage], ti.m0 + m_off + 64 * c, kk);
+#pragma unroll
+            for (int c = 0; c < HB / 64; ++c)
+              ptx::tma_load_2d(b_dst + c * (BK * 128), &tmB, &pfull[stage], ti.n0 + n_off + 64 * c, kk);
+            w = ptx::mbar_wait(&pfull[stage], (pph >> stage) & 1u, abort_flag, p.err);
+          }
+          w = __shfl_sync(0xffffffffu, w, 0);
+          if (!w) { ok = false; break; }
+          pph ^= 1u << stage;
+          tail_pending = -1;
+          zero_tail(a_dst, valid);
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive_remote(even_addr(&full[stage]));
+        }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+    }
+    if (!ok && lane == 0) {
+      // Unwinding: let this CTA's copies land before the CTA exits (bounded).
+      const uint64_t t0 = ptx::globaltimer();
+      if (even) {
+        for (int i = 0; i < STAGES; ++i) {
+          if (armed[i] < 0) continue;
+          while (!ptx::mbar_try_wait_acq_cluster(&full[i], static_cast<uint32_t>(armed[i])) &&
+                 ptx::globaltimer() - t0 < 100000000ull) {
+          }
+        }
+      } else if (tail_pending >= 0) {
+        while (!ptx::mbar_try_wait(&pfull[tail_pending], (pph >> tail_pending) & 1u) &&
+               ptx::globaltimer() - t0 < 100000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (even) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      int fslot = 0;
+      uint32_t fphase = 0;
+      bool ok = true;
+      for (;;) {
+        if (!ptx::mbar_wait(&feed_full[fslot], fphase, abort_flag, p.err)) break;
+        const int tile = s_feed[fslot];
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&feed_empty[fslot]);
+        if (++fslot == FEED) { fslot = 0; fphase ^= 1u; }
+        if (tile < 0) break;
+        const TileInfo ti = S::decode(p, s_off, nullptr, s_ord, tile);
+        if (ti.kblocks == 0) continue;
+        if (!ptx::mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err)) break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN2);
+        for (int kb = 0; kb < ti.kblocks; ++kb) {
+          const int valid = tail_rows(ti, kb);
+          // a short last k-block carries the odd CTA's ordinary stores (its zeroed rows):
+          // cluster-scope acquire; the other stages complete on TMA bytes alone
+          const bool got = valid < BK
+                               ? ptx::mbar_wait_cluster(&full[stage], phase, abort_flag, p.err)
+                               : ptx::mbar_wait(&full[stage], phase, abort_flag, p.err);
+          if (!got) { ok = false; break; }
+          uint8_t* a_src = sA + stage * A_ST;
+          uint8_t* b_src = sB + stage * B_ST;
+          if (valid < BK) zero_tail(a_src, valid);
+          __syncwarp();
+          ptx::tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a_addr = ptx::smem_u32(a_src), b_addr = ptx::smem_u32(b_src);
+#pragma unroll
+            for (int k16 = 0; k16 < BK / 16; ++k16) {
+              const uint64_t ad = ptx::smem_desc_sw128(a_addr + k16 * 2048, BK * 128, 1024);
+              const uint64_t bd = ptx::smem_desc_sw128(b_addr + k16 * 2048, BK * 128, 1024);
+              ptx::umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
+            }
+            ptx::umma_commit_pair(&empty[stage], 0x3);   // frees the stage in both CTAs
+          }
+          __syncwarp();
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        if (lane == 0) ptx::umma_commit_pair(&tfull[acc], 0x3);   // both CTAs' epilogues
+        __syncwarp();
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int e = warp - 2;
+    const int q = warp & 3;
+    uint8_t* slabs = staging + e * (SLABS_P * SLAB);
+    int slab_sel = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int fslot = 0;
+    uint32_t fphase = 0;
+    auto next_slab = [&]() -> uint8_t* {
+      if (lane == 0) ptx::bulk_wait_read<SLABS_P - 1>();
+      __syncwarp();
+      uint8_t* s = slabs + slab_sel * SLAB;
+      if (++slab_sel == SLABS_P) slab_sel = 0;
+      return s;
+    };
+    auto store = [&](const uint8_t* src, int col, int row, int g) {
+      if (MOE_WGRAD_STORE_HINT)
+        ptx::tma_store_3d_hint(&tmO0, src, col, row, g, ptx::policy_evict_first());
+      else
+        ptx::tma_store_3d(&tmO0, src, col, row, g);
+    };
+    for (;;) {
+      const bool got = even ? ptx::mbar_wait(&feed_full[fslot], fphase, abort_flag, p.err)
+                            : ptx::mbar_wait_cluster(&feed_full[fslot], fphase, abort_flag, p.err);
+      if (!got) break;
+      const int tile = s_feed[fslot];
+      __syncwarp();
+      if (lane == 0) {
+        if (even) ptx::mbar_arrive(&feed_empty[fslot]);
+        else ptx::mbar_arrive_remote(even_addr(&feed_empty[fslot]));
+      }
+      if (++fslot == FEED) { fslot = 0; fphase ^= 1u; }
+      if (tile < 0) break;
+      const TileInfo ti = S::decode(p, s_off, nullptr, s_ord, tile);
+      const int row0 = ti.m0 + static_cast<int>(rank) * BM + q * 32;
+      const int rows_here = min(32, ti.m_end - row0);
+      if (ti.kblocks == 0) {
+        // a group without rows: its block is zero (one zeroed slab stored everywhere)
+        if (rows_here > 0) {
+          uint8_t* z = next_slab();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) slab_put(z, lane, j, make_uint4(0, 0, 0, 0));
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            for (int c = 0; c < BN2; c += 32) {
+              if (ti.n0 + c >= p.N) break;
+              store(z, ti.n0 + c, row0, ti.g);
+              ptx::bulk_commit();
+            }
+          }
+          __syncwarp();
+        }
+        continue;
+      }
+      if (!ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err)) break;
+      ptx::tc_fence_after();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * BN2);
+      if (rows_here > 0) {
+        auto put = [&](const uint32_t (&v)[32], int col) {
+          uint8_t* slab = next_slab();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            slab_put(slab, lane, j, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            store(slab, col, row0, ti.g);
+            ptx::bulk_commit();
+          }
+        };
+        auto has = [&](int c) { return c < BN2 && ti.n0 + c < p.N; };
+        uint32_t va[32], vb[32];
+        int c = 0;
+        if (has(c)) {
+          ptx::tmem_ld32(t_row + c, va);
+          ptx::tmem_ld_wait(va);
+        }
+#pragma unroll 1
+        while (has(c)) {
+          const bool nb = has(c + 32);
+          if (nb) ptx::tmem_ld32(t_row + c + 32, vb);
+          put(va, ti.n0 + c);
+          if (!nb) break;
+          ptx::tmem_ld_wait(vb);
+          c += 32;
+          const bool na = has(c + 32);
+          if (na) ptx::tmem_ld32(t_row + c + 32, va);
+          put(vb, ti.n0 + c);
+          if (!na) break;
+          ptx::tmem_ld_wait(va);
+          c += 32;
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (even) ptx::mbar_arrive(&tempty[acc]);
+        else ptx::mbar_arrive_remote(even_addr(&tempty[acc]));
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) ptx::bulk_wait_all();
+    __syncwarp();
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();   // neither CTA leaves while the other may still use its barriers or TMEM
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -1232,6 +1686,48 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
                 mo[2], a);
 }
 
+// Weight gradient on CTA pairs (tc_wgrad_pair_kernel).
+int run_wgrad_pair(const GemmDesc& g, cudaStream_t st) {
+  using namespace pairk;
+  const char* name = g.name ? g.name : "gemm_wgrad";
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [&] {
+    attr_err = cudaFuncSetAttribute(tc_wgrad_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    SMEM);
+  });
+  if (attr_err != cudaSuccess) {
+    set_error("cudaFuncSetAttribute(%s, %d bytes): %s", name, SMEM, cudaGetErrorString(attr_err));
+    return MOE_ERR_CUDA;
+  }
+  if (!g.tile_ctr) {
+    set_error("%s: run-time tile scheduling needs its counter (GemmDesc.tile_ctr)", name);
+    return MOE_ERR_INVALID_ARG;
+  }
+  CUtensorMap ma, mb, mo;
+  MOE_TRY(map_operand(&ma, g.A, BK));
+  MOE_TRY(map_operand(&mb, g.B, BK));
+  MOE_TRY(map_f32_3d(&mo, g.out, g.G, g.M, g.N, g.ldo, g.out_group_stride));
+  KArgs a;
+  memset(&a, 0, sizeof(a));
+  a.G = g.G;
+  a.offsets = g.offsets;
+  a.M = g.M;
+  a.N = g.N;
+  a.K = g.K;
+  a.out = g.out;
+  a.ldo = g.ldo;
+  a.out_group_stride = g.out_group_stride;
+  a.tile_ctr = g.tile_ctr;
+  a.err = device_error_word();
+  if (cudaMemsetAsync(g.tile_ctr, 0, sizeof(int), st) != cudaSuccess) {
+    set_error("%s: clearing the tile counter failed", name);
+    return MOE_ERR_CUDA;
+  }
+  return launch_clusters(name, tc_wgrad_pair_kernel, dim3(num_sms() & ~1), dim3(THREADS), SMEM, 2,
+                         st, ma, mb, mo, a);
+}
+
 }  // namespace
 
 int gemm_tc(const GemmDesc& g, cudaStream_t st) {
@@ -1276,9 +1772,11 @@ int gemm_tc(const GemmDesc& g, cudaStream_t st) {
       return run<256, false, false, RAGGED_M, EPI_F32>(g, "gemm_router", st);
     }
   }
-  if (g.sched == RAGGED_K && g.A.mn_major && g.B.mn_major && g.epi == EPI_F32)
-    return g.gather ? run<256, true, true, RAGGED_K, EPI_F32, true>(g, "gemm_wgrad", st)
-                    : run<256, true, true, RAGGED_K, EPI_F32>(g, "gemm_wgrad", st);
+  if (g.sched == RAGGED_K && g.A.mn_major && g.B.mn_major && g.epi == EPI_F32) {
+    if (g.gather) return run<256, true, true, RAGGED_K, EPI_F32, true>(g, "gemm_wgrad", st);
+    if (MOE_PAIR_WGRAD) return run_wgrad_pair(g, st);
+    return run<256, true, true, RAGGED_K, EPI_F32>(g, "gemm_wgrad", st);
+  }
   set_error("gemm_tc: unsupported combination sched=%d epi=%d a_mn=%d b_mn=%d", g.sched, g.epi,
             (int)g.A.mn_major, (int)g.B.mn_major);
   return MOE_ERR_UNSUPPORTED;
