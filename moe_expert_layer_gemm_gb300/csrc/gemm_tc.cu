@@ -99,6 +99,15 @@ template <int SCHED, int EPI> struct McMode {
 // 192-column output tiles where they pad the product's width less than 256 (build option:
 // measured slower on GB300 -- fc1 dgrad 1.38 -> 1.55 ms, fc2 dgrad 0.97 -> 1.15 ms at d = 2688,
 // f = 1856 -- the per-FLOP operand traffic and per-tile costs outweigh the saved padding).
+// Weight-gradient fp32 blocks through the load/store units instead of TMA (the staged slab read
+// back so that each warp store writes four whole 128-byte lines).  It tests whether the SM's TMA
+// unit, which also brings in every operand k-block, is what the stores contend for.  Interleaved
+// on GB300 it is no faster on uniform or 16-hot routing and 9% slower on the DeepSeek-style
+// routing: the contention is further out (L2 / DRAM), so the stores stay on TMA.
+#ifndef MOE_WGRAD_LSU_STORE
+#define MOE_WGRAD_LSU_STORE 0
+#endif
+
 #ifndef MOE_TILE192
 #define MOE_TILE192 0
 #endif
@@ -718,6 +727,22 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
       else
         ptx::tma_store_3d(&tmO0, src, col, row, g);
     };
+    // fp32 slab (32 rows x 32 columns, swizzled) -> [g][row0 + r][col ..] with warp-wide
+    // coalesced stores: lanes 8i..8i+7 write one 128-byte row segment; rows past `rows`
+    // (the output's end) are skipped.  v == nullptr stores zeros.
+    auto lsu_store = [&](const uint8_t* slab, int col, int row, int g, int rows) {
+      float* base = static_cast<float*>(p.out) + static_cast<int64_t>(g) * p.out_group_stride;
+      const int ch = lane & 7;
+      const int c4 = col + ch * 4;
+      if (c4 >= p.N) return;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = 4 * i + (lane >> 3);
+        if (r >= rows) break;
+        const uint4 v = slab ? slab_get(slab, r, ch) : make_uint4(0, 0, 0, 0);
+        st16_cs(base + static_cast<int64_t>(row + r) * p.ldo + c4, v);
+      }
+    };
     // Next free staging slab of this warp: at most SLABS-1 earlier stores may still read theirs.
     auto next_slab = [&]() -> uint8_t* {
       if (lane == 0) {
@@ -752,7 +777,12 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
       if (ti.kblocks == 0) {
         // Empty reduction (an expert with no rows): its weight-gradient block is zero.  One
         // zeroed slab is stored to every 32-column chunk of this warp's rows.
-        if (EPI == EPI_F32 && SCHED == RAGGED_K && TMA_OUT && rows_here > 0) {
+        if (EPI == EPI_F32 && SCHED == RAGGED_K && MOE_WGRAD_LSU_STORE && rows_here > 0) {
+          for (int c = c_lo; c < c_hi; c += 32) {
+            if (ti.n0 + c >= p.N) break;
+            lsu_store(nullptr, ti.n0 + c, row0, ti.g, rows_here);
+          }
+        } else if (EPI == EPI_F32 && SCHED == RAGGED_K && TMA_OUT && rows_here > 0) {
           uint8_t* z = next_slab();
 #pragma unroll
           for (int j = 0; j < 8; ++j) slab_put(z, lane, j, make_uint4(0, 0, 0, 0));
@@ -815,6 +845,16 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
         // 32-column chunks; the TMEM load of chunk i+1 is in flight while chunk i is staged
         // and stored (two register sets, alternating).
         auto put = [&](const uint32_t (&v)[32], int col) {
+          if (SCHED == RAGGED_K && MOE_WGRAD_LSU_STORE) {
+            // one slab: written, read back by the whole warp, then free again
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              slab_put(slabs, lane, j, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+            __syncwarp();
+            lsu_store(slabs, col, row0, ti.g, rows_here);
+            __syncwarp();
+            return;
+          }
           uint8_t* slab = next_slab();
 #pragma unroll
           for (int j = 0; j < 8; ++j)
