@@ -14,13 +14,19 @@ GEMM moves.  Readings where they are silent:
   * activations are one tensor (one scale); each expert's fc1 and fc2 weight is its own tensor
     (one scale per expert), as the pages' per-parameter "tensorwise" recipe implies;
   * the GEMM multiplies the decoded values and applies both scales to the fp32 result; the
-    SwiGLU input h is quantised again (its own tensorwise scale) before fc2.
+    SwiGLU input h is quantised again (its own tensorwise scale) before fc2;
+  * backward ("fp8_wgrad": weight gradients in FP8 too; "e4m3" for every tensor): the upstream
+    gradient dy_perm is one tensor, quantised like the activations; fc2's data gradient and the
+    SwiGLU backward give [da | du] in bf16, which is quantised as one tensor before fc1's data
+    gradient and fc1's weight gradient; the weight gradients multiply the quantised tensors the
+    forward made (x_perm_q, h_q) with the quantised gradients, the weights' codes are reused as
+    stored.
 """
 from __future__ import annotations
 
 import numpy as np
 
-from .moe_oracle import silu
+from .moe_oracle import silu, silu_grad
 
 E4M3_MAX = 448.0
 
@@ -113,3 +119,82 @@ def fc2_fp8(hq, sh, W2q, sw2, offsets):
         if hi > lo:
             y[lo:hi] = H[lo:hi] @ (e4m3_decode(W2q[e]) * float(sw2[e])).T
     return y
+
+
+# ----------------------------------------------------------------------------- backward
+
+def _rows(offsets, e):
+    return int(offsets[e]), int(offsets[e + 1])
+
+
+def fc2_dgrad_fp8(dyq, sdy, W2q, sw2, offsets):
+    """dh[s] = (dec(dyq[s]) * sdy) . (dec(W2q[e]) * sw2[e]) for rows s of expert e ([d] . [d, f]).
+    fp64."""
+    E, _, f = W2q.shape
+    D = dequantize(dyq, sdy)
+    dh = np.zeros((D.shape[0], f))
+    for e in range(E):
+        lo, hi = _rows(offsets, e)
+        if hi > lo:
+            dh[lo:hi] = D[lo:hi] @ (e4m3_decode(W2q[e]) * float(sw2[e]))
+    return dh
+
+
+def swiglu_backward(dh, act):
+    """[da | du] of h = SiLU(a) * u at the saved pre-activations act = [a | u]:
+    da = dh * u * SiLU'(a), du = dh * SiLU(a).  fp64."""
+    f = dh.shape[1]
+    a, u = np.asarray(act, np.float64)[:, :f], np.asarray(act, np.float64)[:, f:]
+    return np.concatenate([dh * u * silu_grad(a), dh * silu(a)], axis=1)
+
+
+def fc1_dgrad_fp8(dH1q, sdh, W1q, sw1, offsets):
+    """dx[s] = (dec(dH1q[s]) * sdh) . (dec(W1q[e]) * sw1[e]) for rows s of expert e
+    ([2f] . [2f, d]).  fp64."""
+    E, _, d = W1q.shape
+    G = dequantize(dH1q, sdh)
+    dx = np.zeros((G.shape[0], d))
+    for e in range(E):
+        lo, hi = _rows(offsets, e)
+        if hi > lo:
+            dx[lo:hi] = G[lo:hi] @ (e4m3_decode(W1q[e]) * float(sw1[e]))
+    return dx
+
+
+def wgrad_fp8(Aq, sa, Bq, sb, offsets):
+    """dW[e] = (dec(Aq[rows of e]) * sa)^T . (dec(Bq[rows of e]) * sb): [m, n] per expert, zero for
+    an expert without rows.  fp64."""
+    E = len(offsets) - 1
+    A = dequantize(Aq, sa)
+    B = dequantize(Bq, sb)
+    dW = np.zeros((E, A.shape[1], B.shape[1]))
+    for e in range(E):
+        lo, hi = _rows(offsets, e)
+        if hi > lo:
+            dW[e] = A[lo:hi].T @ B[lo:hi]
+    return dW
+
+
+def bf16_round(x):
+    """x rounded to bfloat16 (round to nearest even) and returned as fp64 (via torch, a library
+    implementation of the format)."""
+    import torch
+    return torch.from_numpy(np.asarray(x, np.float64)).to(torch.bfloat16).double().numpy()
+
+
+def grouped_swiglu_bwd_fp8(xq, sx, W1q, sw1, W2q, sw2, act, hq, sh, dy_perm, offsets):
+    """The backward of the FP8 grouped SwiGLU, stage by stage:
+      dy_perm -> (dyq, sdy) one tensor;  dh = fc2_dgrad_fp8;  dH1 = SwiGLU backward, stored in
+      bf16 and quantised as one tensor -> (dH1q, sdh);  dx = fc1_dgrad_fp8;
+      dW1 = wgrad_fp8(dH1q, x);  dW2 = wgrad_fp8(dyq, h).
+    Returns a dict with every intermediate."""
+    dyq, sdy = quantize_tensorwise(np.asarray(dy_perm, np.float32))
+    dh = fc2_dgrad_fp8(dyq, sdy, W2q, sw2, offsets)
+    dH1 = bf16_round(swiglu_backward(dh, act))
+    dH1q, sdh = quantize_tensorwise(dH1.astype(np.float32))
+    return {
+        "dy_q": dyq, "dy_scale": sdy, "dh": dh, "dH1": dH1, "dH1_q": dH1q, "dH1_scale": sdh,
+        "dx": fc1_dgrad_fp8(dH1q, sdh, W1q, sw1, offsets),
+        "dW1": wgrad_fp8(dH1q, sdh, xq, sx, offsets),
+        "dW2": wgrad_fp8(dyq, sdy, hq, sh, offsets),
+    }
