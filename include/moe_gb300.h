@@ -97,7 +97,8 @@ enum {
   MOE_WS_FFN_FWD = 1,     /* moe_grouped_swiglu_fwd                   */
   MOE_WS_FFN_BWD = 2,     /* moe_grouped_swiglu_bwd                   */
   MOE_WS_LAYER_FWD = 3,   /* moe_layer_fwd                            */
-  MOE_WS_LAYER_BWD = 4    /* moe_layer_bwd                            */
+  MOE_WS_LAYER_BWD = 4,   /* moe_layer_bwd                            */
+  MOE_WS_FFN_BWD_FP8 = 5  /* moe_grouped_swiglu_bwd_fp8               */
 };
 
 /* Bytes of caller workspace the call `which` needs for cfg (0 if cfg is invalid). */
@@ -220,12 +221,37 @@ int moe_permute_quantize_e4m3(const moe_cfg* cfg, const void* x, const int32_t* 
  *   y_perm[s] = h_scale * W2_scale[e] * (dec(h_q[s]) . dec(W2_q[e])^T)  (bf16).
  * x_perm_q [N,d], W1_q [E,2f,d], W2_q [E,d,f]: uint8 E4M3 codes from moe_quantize_e4m3 (W1_q and
  * W2_q with E groups, x_perm_q with one); scales fp32 device values.  d and f must be multiples
- * of 16; cfg->dtype must be MOE_DTYPE_BF16.  Forward only (the backward stays bf16). */
+ * of 16; cfg->dtype must be MOE_DTYPE_BF16.  moe_grouped_swiglu_bwd_fp8 is its backward. */
 int moe_grouped_swiglu_fwd_fp8(const moe_cfg* cfg, const uint8_t* x_perm_q, const float* x_scale,
                                const int32_t* offsets, const uint8_t* W1_q, const float* W1_scale,
                                const uint8_t* W2_q, const float* W2_scale, void* h, void* act,
                                uint8_t* h_q, float* h_scale, float* h_amax, void* y_perm,
                                void* stream);
+
+/* Grouped SwiGLU backward on E4M3 operands ("Megatron-Bridge 深度剖析", §FP8 训练: E4M3 with
+ * tensorwise scaling, weight gradients in FP8 as well).  Takes the forward's quantised tensors
+ * (x_perm_q, h_q with their scales; W1_q, W2_q with one scale per expert) and its bf16 [a | u]
+ * (act [N,2f]); for rows s of expert e:
+ *   dy_perm [N,d] (bf16) is quantised as one tensor (moe_quantize_e4m3) into dy_q, dy_scale[0],
+ *     dy_amax[0];
+ *   dh[s] = dy_scale * W2_scale[e] * (dec(dy_q[s]) . dec(W2_q[e]))          (fp32 accumulation)
+ *   dH1[s] = [da | du] = SwiGLU backward of dh[s] at act[s] (bf16 [N,2f], as moe_grouped_swiglu_bwd);
+ *     dH1 is quantised as one tensor (its amax taken in the same epilogue, dH1_amax[0]) into
+ *     dH1_q [N,2f], dH1_scale[0];
+ *   dx_perm[s] = dH1_scale * W1_scale[e] * (dec(dH1_q[s]) . dec(W1_q[e]))   (bf16 [N,d])
+ *   dW1[e] = dH1_scale * x_scale * dec(dH1_q[rows of e])^T . dec(x_perm_q[rows of e])  (fp32)
+ *   dW2[e] = dy_scale * h_scale * dec(dy_q[rows of e])^T . dec(h_q[rows of e])         (fp32)
+ * The weights' codes are read in their stored [E,2f,d] / [E,d,f] layouts (no transposed copies);
+ * experts without rows get zero weight gradients.  dy_q [N,d] and dH1_q are caller buffers of
+ * uint8; scales and amaxes one fp32 each.  Workspace MOE_WS_FFN_BWD_FP8.  d and f multiples of
+ * 16; cfg->dtype MOE_DTYPE_BF16. */
+int moe_grouped_swiglu_bwd_fp8(const moe_cfg* cfg, const uint8_t* x_perm_q, const float* x_scale,
+                               const int32_t* offsets, const uint8_t* W1_q, const float* W1_scale,
+                               const uint8_t* W2_q, const float* W2_scale, const void* act,
+                               const uint8_t* h_q, const float* h_scale, const void* dy_perm,
+                               uint8_t* dy_q, float* dy_scale, float* dy_amax, void* dH1,
+                               uint8_t* dH1_q, float* dH1_scale, float* dH1_amax, void* dx_perm,
+                               float* dW1, float* dW2, void* ws, size_t ws_bytes, void* stream);
 
 /* Unpermute + weighted combine: "Megatron-Bridge 深度剖析", §Expert Parallel 基础 (Step 3,
  * results sent back to token order) and §Shared Expert Overlap (shared output added).

@@ -22,7 +22,7 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3:
 SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 DTYPE_BF16, DTYPE_F32 = 0, 1
 BIAS_LOGIT, BIAS_SELECT = 0, 1
-WS_ROUTE, WS_FFN_FWD, WS_FFN_BWD, WS_LAYER_FWD, WS_LAYER_BWD = range(5)
+WS_ROUTE, WS_FFN_FWD, WS_FFN_BWD, WS_LAYER_FWD, WS_LAYER_BWD, WS_FFN_BWD_FP8 = range(6)
 
 
 class MoeCfg(ctypes.Structure):
@@ -51,6 +51,7 @@ _SIGS = {
     "moe_grouped_swiglu_bwd_gathered": (ctypes.c_int, [_CFG] + [_VP] * 12 + [_SZ, _VP]),
     "moe_quantize_e4m3": (ctypes.c_int, [_VP, ctypes.c_int64, ctypes.c_int32, _VP, _VP, _VP, _VP]),
     "moe_grouped_swiglu_fwd_fp8": (ctypes.c_int, [_CFG] + [_VP] * 14),
+    "moe_grouped_swiglu_bwd_fp8": (ctypes.c_int, [_CFG] + [_VP] * 22 + [_SZ, _VP]),
     "moe_permute_quantize_e4m3": (ctypes.c_int, [_CFG] + [_VP] * 6),
     "moe_unpermute_combine": (ctypes.c_int, [_CFG] + [_VP] * 7),
     "moe_unpermute_combine_bwd": (ctypes.c_int, [_CFG] + [_VP] * 11),
@@ -208,6 +209,17 @@ def moe_grouped_swiglu_fwd_fp8(cfg, x_perm_q, x_scale, offsets, W1_q, W1_scale, 
         ctypes.byref(cfg), _p(x_perm_q), _p(x_scale), _p(offsets), _p(W1_q), _p(W1_scale),
         _p(W2_q), _p(W2_scale), _p(h), _p(act), _p(h_q), _p(h_scale), _p(h_amax), _p(y_perm),
         _stream(stream)), "moe_grouped_swiglu_fwd_fp8")
+
+
+def moe_grouped_swiglu_bwd_fp8(cfg, x_perm_q, x_scale, offsets, W1_q, W1_scale, W2_q, W2_scale, act,
+                               h_q, h_scale, dy_perm, dy_q, dy_scale, dy_amax, dH1, dH1_q,
+                               dH1_scale, dH1_amax, dx_perm, dW1, dW2, ws, stream=None):
+    _check(lib().moe_grouped_swiglu_bwd_fp8(
+        ctypes.byref(cfg), _p(x_perm_q), _p(x_scale), _p(offsets), _p(W1_q), _p(W1_scale),
+        _p(W2_q), _p(W2_scale), _p(act), _p(h_q), _p(h_scale), _p(dy_perm), _p(dy_q), _p(dy_scale),
+        _p(dy_amax), _p(dH1), _p(dH1_q), _p(dH1_scale), _p(dH1_amax), _p(dx_perm), _p(dW1),
+        _p(dW2), _p(ws), 0 if ws is None else ws.numel(), _stream(stream)),
+        "moe_grouped_swiglu_bwd_fp8")
 
 
 def moe_unpermute_combine(cfg, y_perm, gate, slot_of_pair, shared_out, shared_coef, y, stream=None):

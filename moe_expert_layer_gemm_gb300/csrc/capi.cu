@@ -490,7 +490,7 @@ using namespace moe;
 // ====================================================================== C ABI
 extern "C" {
 
-int moe_version(void) { return 101; }
+int moe_version(void) { return 102; }
 
 int moe_set_stream_overlap(int on) {
   const int prev = g_overlap.load();
@@ -575,6 +575,9 @@ size_t moe_workspace_bytes(const moe_cfg* c, int which) {
       break;
     case MOE_WS_LAYER_BWD:
       carve_bwd(cv, c);
+      break;
+    case MOE_WS_FFN_BWD_FP8:
+      cv.take(2 * 4 * sizeof(int));
       break;
     default:
       return 0;
@@ -827,6 +830,131 @@ int moe_grouped_swiglu_fwd_fp8(const moe_cfg* c, const uint8_t* x_perm_q, const 
   g2.a_scale = h_scale;
   g2.b_scale = W2_scale;
   return gemm_tc(g2, st);
+}
+
+int moe_grouped_swiglu_bwd_fp8(const moe_cfg* c, const uint8_t* x_perm_q, const float* x_scale,
+                               const int32_t* offsets, const uint8_t* W1_q, const float* W1_scale,
+                               const uint8_t* W2_q, const float* W2_scale, const void* act,
+                               const uint8_t* h_q, const float* h_scale, const void* dy_perm,
+                               uint8_t* dy_q, float* dy_scale, float* dy_amax, void* dH1,
+                               uint8_t* dH1_q, float* dH1_scale, float* dH1_amax, void* dx_perm,
+                               float* dW1, float* dW2, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_cfg(c));
+  if (c->dtype != MOE_DTYPE_BF16)
+    return fail(MOE_ERR_UNSUPPORTED, "the FP8 path reads and writes bf16 activations (dtype bf16)");
+  if (c->d % 16 || c->f % 16)
+    return fail(MOE_ERR_UNSUPPORTED, "FP8 rows need d and f multiples of 16 (16-byte rows)");
+  const struct { const void* p; const char* n; } req[] = {
+      {x_perm_q, "x_perm_q"}, {x_scale, "x_scale"}, {offsets, "offsets"}, {W1_q, "W1_q"},
+      {W1_scale, "W1_scale"}, {W2_q, "W2_q"}, {W2_scale, "W2_scale"}, {act, "act"},
+      {h_q, "h_q"}, {h_scale, "h_scale"}, {dy_perm, "dy_perm"}, {dy_q, "dy_q"},
+      {dy_scale, "dy_scale"}, {dy_amax, "dy_amax"}, {dH1, "dH1"}, {dH1_q, "dH1_q"},
+      {dH1_scale, "dH1_scale"}, {dH1_amax, "dH1_amax"}, {dx_perm, "dx_perm"}, {dW1, "dW1"},
+      {dW2, "dW2"}};
+  for (const auto& r : req) MOE_TRY(check_ptr(r.p, r.n, true));
+  MOE_TRY(check_ws(c, MOE_WS_FFN_BWD_FP8, ws, ws_bytes));
+  cudaStream_t st = S(stream);
+  const int64_t N = Nrows(c);
+  const int d = c->d, f = c->f, E = c->E;
+  if (N == 0) {
+    if (cudaMemsetAsync(dW1, 0, sizeof(float) * E * 2 * f * d, st) != cudaSuccess ||
+        cudaMemsetAsync(dW2, 0, sizeof(float) * E * d * f, st) != cudaSuccess)
+      return fail(MOE_ERR_CUDA, "cudaMemsetAsync failed");
+    return MOE_OK;
+  }
+  Carve cv(ws);
+  int* sched = static_cast<int*>(cv.take(2 * 4 * sizeof(int)));
+  // dy_perm -> E4M3 (one tensor)
+  MOE_TRY(launch_quantize_e4m3(dy_perm, N * d, 1, dy_q, dy_scale, dy_amax, st));
+  // dh = dy . W2_e on E4M3 operands (W2_q read MN-major: no transposed copy), SwiGLU backward
+  // -> dH1 = [da | du] (bf16) with its amax
+  GemmDesc a = desc0();
+  a.name = "gemm_fc2_dgrad_fp8";
+  a.sched = RAGGED_M;
+  a.epi = EPI_SWIGLU_BWD;
+  a.G = E;
+  a.offsets = offsets;
+  a.M = static_cast<int>(N);
+  a.N = f;
+  a.K = d;
+  a.A = opnd(dy_q, N, d, false);
+  a.B = opnd(W2_q, static_cast<int64_t>(E) * d, f, true);
+  a.b_group_rows = d;
+  a.f = f;
+  a.out = dH1;
+  a.ldo = 2 * f;
+  a.aux = act;
+  a.ld_aux = 2 * f;
+  a.fp8 = true;
+  a.a_scale = dy_scale;
+  a.b_scale = W2_scale;
+  a.amax_out = dH1_amax;
+  if (cudaMemsetAsync(dH1_amax, 0, sizeof(float), st) != cudaSuccess)
+    return fail(MOE_ERR_CUDA, "clearing dH1_amax failed");
+  MOE_TRY(gemm_tc(a, st));
+  // dH1 -> E4M3 (one tensor) with that amax
+  MOE_TRY(launch_quant_e4m3_given_amax(dH1, N * 2 * f, 1, dH1_q, dH1_scale, dH1_amax, st));
+  // dW2_e = dy_e^T . h_e (both MN-major over the expert's rows)
+  GemmDesc b = desc0();
+  b.name = "gemm_fc2_wgrad_fp8";
+  b.sched = RAGGED_K;
+  b.epi = EPI_F32;
+  b.G = E;
+  b.offsets = offsets;
+  b.M = d;
+  b.N = f;
+  b.K = static_cast<int>(N);
+  b.A = opnd(dy_q, N, d, true);
+  b.B = opnd(h_q, N, f, true);
+  b.out = dW2;
+  b.ldo = f;
+  b.out_group_stride = static_cast<int64_t>(d) * f;
+  b.tile_ctr = sched;
+  b.fp8 = true;
+  b.a_scale = dy_scale;
+  b.b_scale = h_scale;
+  b.b_scale_scalar = true;
+  MOE_TRY(gemm_tc(b, st));
+  // dx_perm = dH1 . W1_e
+  GemmDesc e = desc0();
+  e.name = "gemm_fc1_dgrad_fp8";
+  e.sched = RAGGED_M;
+  e.epi = EPI_STORE;
+  e.G = E;
+  e.offsets = offsets;
+  e.M = static_cast<int>(N);
+  e.N = d;
+  e.K = 2 * f;
+  e.A = opnd(dH1_q, N, 2 * f, false);
+  e.B = opnd(W1_q, static_cast<int64_t>(E) * 2 * f, d, true);
+  e.b_group_rows = 2 * f;
+  e.out = dx_perm;
+  e.ldo = d;
+  e.fp8 = true;
+  e.a_scale = dH1_scale;
+  e.b_scale = W1_scale;
+  MOE_TRY(gemm_tc(e, st));
+  // dW1_e = dH1_e^T . x_perm_e
+  GemmDesc w = desc0();
+  w.name = "gemm_fc1_wgrad_fp8";
+  w.sched = RAGGED_K;
+  w.epi = EPI_F32;
+  w.G = E;
+  w.offsets = offsets;
+  w.M = 2 * f;
+  w.N = d;
+  w.K = static_cast<int>(N);
+  w.A = opnd(dH1_q, N, 2 * f, true);
+  w.B = opnd(x_perm_q, N, d, true);
+  w.out = dW1;
+  w.ldo = d;
+  w.out_group_stride = static_cast<int64_t>(2) * f * d;
+  w.tile_ctr = sched + 4;
+  w.fp8 = true;
+  w.a_scale = dH1_scale;
+  w.b_scale = x_scale;
+  w.b_scale_scalar = true;
+  return gemm_tc(w, st);
 }
 
 int moe_unpermute_combine(const moe_cfg* c, const void* y_perm, const float* gate,

@@ -173,7 +173,8 @@ struct KArgs {
   int gather_rows;         // rows of the gathered source tensor
   const float* a_scale;    // FP8: dequantisation scale of A (one value)
   const float* b_scale;    // FP8: dequantisation scale of B, one per group
-  float* amax_out;         // FP8 fc1: max |h| (fp32 bits, atomically raised; zeroed before)
+  int b_scale_per_group;   // FP8: 0 -> b_scale[0] for every group
+  float* amax_out;         // FP8 SwiGLU epilogues: max |h| or |[da | du]| (fp32 bits, raised)
   int* err;
 };
 
@@ -278,9 +279,10 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
   // K elements per stage: 128-byte rows hold 64 bf16 or 128 E4M3 values
   constexpr int BKE = F8 ? 2 * BK : BK;
   using S = Sched<BN, SCHED, EPI, TM, BKE>;
-  static_assert(!F8 || (SCHED == RAGGED_M && !A_MN && !B_MN && !GATHER && !MC &&
-                        (EPI == EPI_SWIGLU_FWD || EPI == EPI_STORE)),
-                "FP8 operands: K-major forward products only");
+  // MN-major operand tiles are chunks of 128-byte rows along K: 64 bf16 or 128 E4M3 of M/N each
+  constexpr int MNW = F8 ? 128 : 64;
+  constexpr int MN_CHUNK = BKE * 128;   // bytes of one such chunk in a stage
+  static_assert(!F8 || (!GATHER && !MC), "FP8 operands: no gathered or cluster-shared loads");
   constexpr int STAGES = C::STAGES;
   constexpr uint32_t STAGE_TX = A_STAGE + C::B_STAGE;
 
@@ -545,7 +547,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
           if (live) box(a_dst, &tmA, kk, m_cta);
         } else {
 #pragma unroll
-          for (int c = 0; c < BM / 64; ++c) box(a_dst + c * (BK * 128), &tmA, m_cta + 64 * c, kk);
+          for (int c = 0; c < BM / MNW; ++c) box(a_dst + c * MN_CHUNK, &tmA, m_cta + MNW * c, kk);
         }
         if (!B_MN) {
           const int brow = static_cast<int>(ti.g * p.b_group_rows) + ti.n0;
@@ -576,7 +578,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
             }
           } else {
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c) box(b_dst + c * (BK * 128), &tmB, ti.n0 + 64 * c, krow);
+            for (int c = 0; c < BN / MNW; ++c) box(b_dst + c * MN_CHUNK, &tmB, ti.n0 + MNW * c, krow);
           }
         }
       };
@@ -629,7 +631,8 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t IDESC = F8 ? ptx::idesc_e4m3_f32(BM, BN) : ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    constexpr uint32_t IDESC =
+        F8 ? ptx::idesc_e4m3_f32(BM, BN, A_MN, B_MN) : ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -665,11 +668,11 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
         if (SCHED == RAGGED_K && kb == ti.kblocks - 1) {
           // Rows of this k-block past the group's end belong to the next group: zero them in
           // the A tile (MN-major: row r of chunk c is 128 contiguous bytes).
-          const int valid = ti.k_end - (ti.k0 + kb * BK);
-          if (valid < BK) {
-            const int nbytes = (BK - valid) * 128;
-            for (int c = 0; c < BM / 64; ++c) {
-              uint8_t* base = a_src + c * (BK * 128) + valid * 128;
+          const int valid = ti.k_end - (ti.k0 + kb * BKE);
+          if (valid < BKE) {
+            const int nbytes = (BKE - valid) * 128;
+            for (int c = 0; c < BM / MNW; ++c) {
+              uint8_t* base = a_src + c * MN_CHUNK + valid * 128;
               for (int o = lane * 16; o < nbytes; o += 32 * 16)
                 *reinterpret_cast<uint4*>(base + o) = make_uint4(0, 0, 0, 0);
             }
@@ -683,9 +686,12 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
 #pragma unroll
           for (int k16 = 0; k16 < BK / 16; ++k16) {
             if (!a_live) break;
-            const uint64_t ad = A_MN ? ptx::smem_desc_sw128(a_addr + k16 * 2048, BK * 128, 1024)
+            // one instruction takes 32 bytes of K: 16 bf16 or 32 E4M3 -- along a K-major row, or
+            // that many 128-byte rows of an MN-major chunk
+            constexpr uint32_t MN_KSTEP = (F8 ? 32 : 16) * 128;
+            const uint64_t ad = A_MN ? ptx::smem_desc_sw128(a_addr + k16 * MN_KSTEP, MN_CHUNK, 1024)
                                      : ptx::smem_desc_sw128(a_addr + k16 * 32, 16, 1024);
-            const uint64_t bd = B_MN ? ptx::smem_desc_sw128(b_addr + k16 * 2048, BK * 128, 1024)
+            const uint64_t bd = B_MN ? ptx::smem_desc_sw128(b_addr + k16 * MN_KSTEP, MN_CHUNK, 1024)
                                      : ptx::smem_desc_sw128(b_addr + k16 * 32, 16, 1024);
             if (F8) ptx::umma_f8(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
             else ptx::umma_bf16(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
@@ -808,11 +814,13 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
       // written with masked stores instead.
       const bool tma_slab = TMA_OUT && (SCHED == RAGGED_K ? rows_here > 0 : rows_here == 32);
       // FP8: the accumulator holds products of decoded E4M3 values; both scales apply here
-      const float sc = F8 ? __ldg(p.a_scale) * __ldg(p.b_scale + ti.g) : 1.0f;
-      // FP8 fc1: max |h| over this warp's stored (bf16) values, for h's own quantisation
+      const float sc = F8 ? __ldg(p.a_scale) * __ldg(p.b_scale + (p.b_scale_per_group ? ti.g : 0)) : 1.0f;
+      // FP8 SwiGLU epilogues: max |.| over this warp's stored (bf16) values of h (forward) or
+      // [da | du] (backward), for that tensor's own quantisation
+      constexpr bool AMAX = F8 && (EPI == EPI_SWIGLU_FWD || EPI == EPI_SWIGLU_BWD);
       float hmax = 0.f;
       auto track = [&](float v) {
-        if (F8 && EPI == EPI_SWIGLU_FWD) hmax = fmaxf(hmax, fabsf(__bfloat162float(__float2bfloat16_rn(v))));
+        if (AMAX) hmax = fmaxf(hmax, fabsf(__bfloat162float(__float2bfloat16_rn(v))));
       };
       bool aborted = false;
 
@@ -845,11 +853,13 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
         // 32-column chunks; the TMEM load of chunk i+1 is in flight while chunk i is staged
         // and stored (two register sets, alternating).
         auto put = [&](const uint32_t (&v)[32], int col) {
+          // FP8: both dequantisation scales applied to the fp32 result
+          auto w = [&](int i) { return F8 ? __float_as_uint(__uint_as_float(v[i]) * sc) : v[i]; };
           if (SCHED == RAGGED_K && MOE_WGRAD_LSU_STORE) {
             // one slab: written, read back by the whole warp, then free again
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              slab_put(slabs, lane, j, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+              slab_put(slabs, lane, j, make_uint4(w(4 * j), w(4 * j + 1), w(4 * j + 2), w(4 * j + 3)));
             __syncwarp();
             lsu_store(slabs, col, row0, ti.g, rows_here);
             __syncwarp();
@@ -858,7 +868,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
           uint8_t* slab = next_slab();
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            slab_put(slab, lane, j, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+            slab_put(slab, lane, j, make_uint4(w(4 * j), w(4 * j + 1), w(4 * j + 2), w(4 * j + 3)));
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -964,10 +974,12 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
               unpack16(slab_get(su, lane, 4 * hf + j), uv, static_cast<const bf16*>(nullptr));
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
-                const float g = __uint_as_float(dh[8 * j + i]);
+                const float g = __uint_as_float(dh[8 * j + i]) * sc;
                 const float s = 1.0f / (1.0f + __expf(-av[i]));
                 da[i] = g * uv[i] * (s + av[i] * s * (1.0f - s));
                 du[i] = g * av[i] * s;
+                track(da[i]);
+                track(du[i]);
               }
               slab_put(sa, lane, 4 * hf + j, pack16(da, static_cast<const bf16*>(nullptr)));
               slab_put(su, lane, 4 * hf + j, pack16(du, static_cast<const bf16*>(nullptr)));
@@ -1029,10 +1041,12 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
               unpack16(ld16(act + p.f + col + v * 8), uv, static_cast<const bf16*>(nullptr));
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
-                const float g = __uint_as_float(dh[v * 8 + i]);
+                const float g = __uint_as_float(dh[v * 8 + i]) * sc;
                 const float s = 1.0f / (1.0f + __expf(-av[i]));
                 da[i] = g * uv[i] * (s + av[i] * s * (1.0f - s));
                 du[i] = g * av[i] * s;
+                track(da[i]);
+                track(du[i]);
               }
               st16(drow + col + v * 8, pack16(da, static_cast<const bf16*>(nullptr)));
               st16(drow + p.f + col + v * 8, pack16(du, static_cast<const bf16*>(nullptr)));
@@ -1086,7 +1100,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
           }
         }
       }
-      if (F8 && EPI == EPI_SWIGLU_FWD && p.amax_out) {
+      if (AMAX && p.amax_out) {
         const float m = warp_max(hmax);   // non-negative floats order like their bit patterns
         if (lane == 0 && m > 0.f) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), __float_as_uint(m));
       }
@@ -1655,10 +1669,12 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   CUtensorMap ma, mb, mo[3];
   memset(mo, 0, sizeof(mo));
   // gathered operands are read one row per box (four rows per tile::gather4 copy)
-  MOE_TRY(map_operand(&ma, g.A, (GATHER && SCHED == RAGGED_M) ? 1 : (A_MN ? BK : BM), F8));
+  // an MN-major box is one stage's K rows: 64 (bf16) or 128 (E4M3) of them
+  constexpr int KROWS = F8 ? 2 * BK : BK;
+  MOE_TRY(map_operand(&ma, g.A, (GATHER && SCHED == RAGGED_M) ? 1 : (A_MN ? KROWS : BM), F8));
   MOE_TRY(map_operand(&mb, g.B,
                       (GATHER && SCHED == RAGGED_K) ? 1
-                      : B_MN ? BK
+                      : B_MN ? KROWS
                              : ((EPI == EPI_SWIGLU_FWD || McMode<SCHED, EPI>::on) ? BN / 2 : BN),
                       F8));
   const int64_t rows = g.M;   // RAGGED_M: rows of the output (capacity)
@@ -1699,6 +1715,7 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   a.gather_rows = static_cast<int>(SCHED == RAGGED_M ? g.A.rows : g.B.rows);
   a.a_scale = g.a_scale;
   a.b_scale = g.b_scale;
+  a.b_scale_per_group = g.b_scale_scalar ? 0 : 1;
   a.amax_out = g.amax_out;
   if (F8 && (!g.a_scale || !g.b_scale)) {
     set_error("%s: FP8 operands need their scales", name);
@@ -1776,14 +1793,21 @@ int gemm_tc(const GemmDesc& g, cudaStream_t st) {
     return MOE_ERR_UNSUPPORTED;
   }
   if (g.fp8) {
-    // E4M3 operands (K-major), forward products only
-    if (g.sched == RAGGED_M && !g.A.mn_major && !g.B.mn_major && !g.gather) {
-      if (g.epi == EPI_SWIGLU_FWD)
+    // E4M3 operands: the expert products of the forward and the backward
+    if (!g.gather && g.sched == RAGGED_M && !g.A.mn_major) {
+      if (g.epi == EPI_SWIGLU_FWD && !g.B.mn_major)
         return run<256, false, false, RAGGED_M, EPI_SWIGLU_FWD, false, true>(g, "gemm_fc1_swiglu_fp8", st);
-      if (g.epi == EPI_STORE)
+      if (g.epi == EPI_STORE && !g.B.mn_major)
         return run<256, false, false, RAGGED_M, EPI_STORE, false, true>(g, "gemm_fc2_fp8", st);
+      if (g.epi == EPI_SWIGLU_BWD && g.B.mn_major)
+        return run<256, false, true, RAGGED_M, EPI_SWIGLU_BWD, false, true>(g, "gemm_fc2_dgrad_fp8", st);
+      if (g.epi == EPI_STORE && g.B.mn_major)
+        return run<256, false, true, RAGGED_M, EPI_STORE, false, true>(g, "gemm_fc1_dgrad_fp8", st);
     }
-    set_error("gemm_tc: FP8 operands are supported for the K-major forward products only");
+    if (!g.gather && g.sched == RAGGED_K && g.A.mn_major && g.B.mn_major && g.epi == EPI_F32)
+      return run<256, true, true, RAGGED_K, EPI_F32, false, true>(g, "gemm_wgrad_fp8", st);
+    set_error("gemm_tc: unsupported FP8 combination sched=%d epi=%d a_mn=%d b_mn=%d", g.sched, g.epi,
+              (int)g.A.mn_major, (int)g.B.mn_major);
     return MOE_ERR_UNSUPPORTED;
   }
   if (g.sched == RAGGED_M && !g.A.mn_major) {

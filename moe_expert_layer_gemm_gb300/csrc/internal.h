@@ -159,11 +159,14 @@ struct GemmDesc {
   // Operand describes (A for RAGGED_M, with M rows; B for RAGGED_K, with K rows).  Null: plain.
   const int32_t* gather;
   // FP8 (E4M3) operands: A and B hold E4M3 codes; the product is scaled by a_scale[0] *
-  // b_scale[g] (dequantisation scales) before the epilogue.
+  // b_scale[g] (b_scale[0] with b_scale_scalar: both operands one tensor each, as in a weight
+  // gradient) before the epilogue.
   bool fp8;
   const float* a_scale;
   const float* b_scale;
-  float* amax_out;         // FP8 fc1 + SwiGLU: receives max |h| (zeroed by the caller)
+  bool b_scale_scalar;
+  float* amax_out;         // FP8 SwiGLU forward / backward: receives max |h| or max |[da | du]|
+                           // over the bf16 values written (zeroed by the caller)
 };
 
 // Argument checks and the routing stages (capi.cu), for entry points defined elsewhere.

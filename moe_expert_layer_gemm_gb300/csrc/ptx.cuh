@@ -278,11 +278,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
-// Instruction descriptor of tcgen05.mma.kind::f8f6f4: E4M3 x E4M3 -> fp32, M x N, K-major A/B.
-__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+// Instruction descriptor of tcgen05.mma.kind::f8f6f4: E4M3 x E4M3 -> fp32, M x N (8-bit
+// operands may be K- or MN-major, like the 16-bit ones).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn, bool b_mn) {
   return (1u << 4)                                   // D format: f32
          | (0u << 7)                                 // A format: E4M3
          | (0u << 10)                                // B format: E4M3
+         | ((a_mn ? 1u : 0u) << 15)                  // A major: 0 K, 1 MN
+         | ((b_mn ? 1u : 0u) << 16)                  // B major
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
