@@ -414,7 +414,7 @@ def run_gpu(args, lc):
             dist.destroy_process_group()
         return None
 
-    fp8 = None if args.no_fp8 or lc.dtype != "bf16" else fp8_forward(args, lc, cfg, inp, saved, dev)
+    fp8 = None if args.no_fp8 or lc.dtype != "bf16" else fp8_experts(args, lc, cfg, inp, saved, dev)
 
     # ---- roofline of the dominant kernel (largest share of device time in the timed region)
     peaks, peak_src = load_peaks()
@@ -487,7 +487,7 @@ def run_gpu(args, lc):
                                  "second timed region, run in serial order"},
         "clocks": clk,
         "cpu_baseline": cpu,
-        "fp8_forward": fp8,
+        "fp8": fp8,
         "kernels": kern,
     }
     if world > 1:
@@ -495,12 +495,14 @@ def run_gpu(args, lc):
     return out
 
 
-# ----------------------------------------------------------------------------- FP8 forward
+# ----------------------------------------------------------------------------- FP8 experts
 
-def fp8_forward(args, lc, cfg, inp, saved, dev):
-    """Permute + the routed experts' forward (fc1 + SwiGLU, fc2) in bf16 and in FP8 E4M3 on the
-    same routed rows: FP8 weights quantised once (FP8 parameters), activations quantised every
-    step (x with the permute, h inside the call).  Device time per step with CUDA events."""
+def fp8_experts(args, lc, cfg, inp, saved, dev):
+    """The routed experts in bf16 and in FP8 E4M3 on the same routed rows, forward and backward.
+    Forward: permute + fc1 + SwiGLU + fc2; backward: the expert backward (both data gradients, both
+    weight gradients).  FP8 weights are quantised once (FP8 parameters); activations and gradients
+    are quantised every step (x with the permute, h and [da | du] from their GEMMs' epilogues, dy
+    inside the backward call).  Device time per step with CUDA events."""
     import torch
     import moe_expert_layer_gemm_gb300 as moe
     E, d, f, N = lc.E, lc.d, lc.f, lc.N
@@ -514,21 +516,38 @@ def fp8_forward(args, lc, cfg, inp, saved, dev):
     moe.moe_quantize_e4m3(inp["W1"], E, W1q, s1, a1)
     moe.moe_quantize_e4m3(inp["W2"], E, W2q, s2, a2)
     xq = torch.empty(N, d, dtype=u8, device=dev)
-    xs, xa, hs, ha = (torch.empty(4, device=dev) for _ in range(4))
+    xs, xa, hs, ha, dys, dya, gs, ga = (torch.empty(4, device=dev) for _ in range(8))
     h = torch.empty(N, f, dtype=bf, device=dev)
     act = torch.empty(N, 2 * f, dtype=bf, device=dev)
     hq = torch.empty(N, f, dtype=u8, device=dev)
     yp = torch.empty(N, d, dtype=bf, device=dev)
-
+    g = torch.Generator(device=dev).manual_seed(11)
+    dyp = (torch.randn(N, d, device=dev, generator=g) * 0.01).to(bf)
+    dyq = torch.empty(N, d, dtype=u8, device=dev)
+    dH1 = torch.empty(N, 2 * f, dtype=bf, device=dev)
+    dH1q = torch.empty(N, 2 * f, dtype=u8, device=dev)
+    dxp = torch.empty(N, d, dtype=bf, device=dev)
+    dW1 = torch.empty(E, 2 * f, d, device=dev)
+    dW2 = torch.empty(E, d, f, device=dev)
+    ws16 = moe.workspace(cfg, moe.WS_FFN_BWD, dev)
+    ws8 = moe.workspace(cfg, moe.WS_FFN_BWD_FP8, dev)
     sop = saved["slot_of_pair"]
 
-    def bf16_step():
+    def fwd16():
         moe.moe_permute(cfg, inp["x"], sop, x_perm)
         moe.moe_grouped_swiglu_fwd(cfg, x_perm, off, inp["W1"], inp["W2"], h, act, yp)
 
-    def fp8_step():
+    def fwd8():
         moe.moe_permute_quantize_e4m3(cfg, inp["x"], sop, xq, xs, xa)
         moe.moe_grouped_swiglu_fwd_fp8(cfg, xq, xs, off, W1q, s1, W2q, s2, h, act, hq, hs, ha, yp)
+
+    def bwd16():
+        moe.moe_grouped_swiglu_bwd(cfg, x_perm, off, inp["W1"], inp["W2"], act, h, dyp, dxp, dW1,
+                                   dW2, ws16)
+
+    def bwd8():
+        moe.moe_grouped_swiglu_bwd_fp8(cfg, xq, xs, off, W1q, s1, W2q, s2, act, hq, hs, dyp, dyq,
+                                       dys, dya, dH1, dH1q, gs, ga, dxp, dW1, dW2, ws8)
 
     def timed(fn, n):
         for _ in range(3):
@@ -544,27 +563,37 @@ def fp8_forward(args, lc, cfg, inp, saved, dev):
         return e0.elapsed_time(e1) / n
 
     n = max(5, min(args.steps, 50))
-    ms_bf16 = timed(bf16_step, n)
-    moe.trace_read()
-    moe.trace_enable(True)
-    ms_fp8 = timed(fp8_step, n)
-    moe.trace_enable(False)
-    tr = moe.trace_read()
-    moe.check_device_error()
-    flops = 6.0 * N * d * f
     peaks, src = load_peaks()
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
-    per = {k: round(ms / c, 4) for k, (c, ms) in tr.items() if c}
-    gemm_ms = per.get("gemm_fc1_swiglu_fp8", 0) + per.get("gemm_fc2_fp8", 0)
-    return {"bf16_ms": round(ms_bf16, 4), "fp8_ms": round(ms_fp8, 4),
-            "speedup": round(ms_bf16 / ms_fp8, 3),
-            "fp8_gemm_tflops": round(flops / (gemm_ms / 1e3) / 1e12, 1) if gemm_ms else None,
-            "fp8_gemm_frac": round(flops / (gemm_ms / 1e3) / 1e12 / fp8_peak, 4) if gemm_ms else None,
-            "fp8_peak": f"{fp8_peak:.1f} TFLOP/s = 2 x {src} bf16_tflops_sustained (nominal ratio)",
-            "kernels_ms": per,
-            "scope": "permute + routed fc1+SwiGLU and fc2 forward; E4M3 weights quantised once, "
-                     "x (fused with the permute) and h (amax in fc1's epilogue) quantised every "
-                     "step (included)"}
+    out = {"fp8_peak": f"{fp8_peak:.1f} TFLOP/s = 2 x {src} bf16_tflops_sustained (nominal ratio)"}
+    for part, f16, f8, flops, gemms, scope in (
+            ("forward", fwd16, fwd8, 6.0 * N * d * f, ("gemm_fc1_swiglu_fp8", "gemm_fc2_fp8"),
+             "permute + routed fc1+SwiGLU and fc2; x quantised with the permute, h from fc1's "
+             "epilogue amax (included)"),
+            ("backward", bwd16, bwd8, 12.0 * N * d * f,
+             ("gemm_fc2_dgrad_fp8", "gemm_fc2_wgrad_fp8", "gemm_fc1_dgrad_fp8", "gemm_fc1_wgrad_fp8"),
+             "routed expert backward: dy quantised, fc2 dgrad + SwiGLU backward, [da | du] "
+             "quantised, fc1 dgrad, fc1 and fc2 weight gradients (fp32)")):
+        if part == "backward":
+            fwd8()          # the backward reads the FP8 forward's h codes and [a | u]
+        ms16 = timed(f16, n)
+        if part == "backward":
+            fwd8()
+        moe.trace_read()
+        moe.trace_enable(True)
+        ms8 = timed(f8, n)
+        moe.trace_enable(False)
+        tr = moe.trace_read()
+        moe.check_device_error()
+        per = {k: round(ms / c, 4) for k, (c, ms) in tr.items() if c}
+        gemm_ms = sum(per.get(k, 0) for k in gemms)
+        out[part] = {"bf16_ms": round(ms16, 4), "fp8_ms": round(ms8, 4),
+                     "speedup": round(ms16 / ms8, 3),
+                     "fp8_gemm_tflops": round(flops / (gemm_ms / 1e3) / 1e12, 1) if gemm_ms else None,
+                     "fp8_gemm_frac": round(flops / (gemm_ms / 1e3) / 1e12 / fp8_peak, 4)
+                     if gemm_ms else None,
+                     "kernels_ms": per, "scope": scope}
+    return out
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -613,7 +642,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=512)
     ap.add_argument("--ref-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 forward comparison")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 expert comparison")
     ap.add_argument("--no-graph", action="store_true", help="time eager calls, not a CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=20)
     args = ap.parse_args()

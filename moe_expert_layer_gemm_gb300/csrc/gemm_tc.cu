@@ -972,14 +972,18 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
               float av[8], uv[8], da[8], du[8];
               unpack16(slab_get(sa, lane, 4 * hf + j), av, static_cast<const bf16*>(nullptr));
               unpack16(slab_get(su, lane, 4 * hf + j), uv, static_cast<const bf16*>(nullptr));
+              // columns past f (an edge tile) are never stored: keep them out of the amax
+              const bool live = col + 32 * hf + 8 * j < p.f;
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 const float g = __uint_as_float(dh[8 * j + i]) * sc;
                 const float s = 1.0f / (1.0f + __expf(-av[i]));
                 da[i] = g * uv[i] * (s + av[i] * s * (1.0f - s));
                 du[i] = g * av[i] * s;
-                track(da[i]);
-                track(du[i]);
+                if (live) {
+                  track(da[i]);
+                  track(du[i]);
+                }
               }
               slab_put(sa, lane, 4 * hf + j, pack16(da, static_cast<const bf16*>(nullptr)));
               slab_put(su, lane, 4 * hf + j, pack16(du, static_cast<const bf16*>(nullptr)));
