@@ -98,7 +98,8 @@ enum {
   MOE_WS_FFN_BWD = 2,     /* moe_grouped_swiglu_bwd                   */
   MOE_WS_LAYER_FWD = 3,   /* moe_layer_fwd                            */
   MOE_WS_LAYER_BWD = 4,   /* moe_layer_bwd                            */
-  MOE_WS_FFN_BWD_FP8 = 5  /* moe_grouped_swiglu_bwd_fp8               */
+  MOE_WS_FFN_BWD_FP8 = 5, /* moe_grouped_swiglu_bwd_fp8               */
+  MOE_WS_LAYER_BWD_FP8 = 6 /* moe_layer_bwd_fp8                       */
 };
 
 /* Bytes of caller workspace the call `which` needs for cfg (0 if cfg is invalid). */
@@ -339,6 +340,44 @@ int moe_layer_bwd(const moe_cfg* cfg, const void* dy, const void* x, const void*
                   const void* w_sg, const moe_saved* saved, void* dx, float* dW_r, float* dW1,
                   float* dW2, float* dWs1, float* dWs2, float* dw_sg, void* ws, size_t ws_bytes,
                   void* stream);
+
+/* The routed experts of a layer in FP8 ("Megatron-Bridge 深度剖析", §FP8 训练: E4M3, tensorwise
+ * scaling, FP8 parameters, weight gradients in FP8).  Caller-owned device buffers:
+ *   W1_q [E,2f,d], W2_q [E,d,f]: E4M3 codes of the experts' weights with one fp32 scale per
+ *     expert (W1_scale [E], W2_scale [E]) -- moe_quantize_e4m3 with E groups; read only;
+ *   x_perm_q [N,d], h_q [N,f]: the E4M3 activations moe_layer_fwd_fp8 leaves for the backward;
+ *   scales [8] fp32: written by the calls -- [0] x scale, [1] x amax, [2] h scale, [3] h amax
+ *     (forward), [4] dy_perm scale, [5] its amax, [6] [da | du] scale, [7] its amax (backward). */
+typedef struct moe_fp8_experts {
+  const uint8_t* W1_q;
+  const float* W1_scale;
+  const uint8_t* W2_q;
+  const float* W2_scale;
+  uint8_t* x_perm_q;
+  uint8_t* h_q;
+  float* scales;
+} moe_fp8_experts;
+
+/* moe_layer_fwd with the routed experts on E4M3 operands: x is permuted and quantised in one
+ * pass (moe_permute_quantize_e4m3) and the experts run as moe_grouped_swiglu_fwd_fp8 does, with
+ * fp8's weights; routing, the shared expert and the combine are those of moe_layer_fwd.  saved
+ * is filled as by moe_layer_fwd except saved.x_perm (unused, may be NULL); fp8's x_perm_q, h_q
+ * and scales[0..3] are written.  Workspace MOE_WS_LAYER_FWD.  cfg->dtype MOE_DTYPE_BF16, d and
+ * f multiples of 16. */
+int moe_layer_fwd_fp8(const moe_cfg* cfg, const void* x, const void* W_r, const float* b_r,
+                      const moe_fp8_experts* fp8, const void* Ws1, const void* Ws2,
+                      const void* w_sg, void* y, const moe_saved* saved, void* ws, size_t ws_bytes,
+                      void* stream);
+
+/* moe_layer_bwd after moe_layer_fwd_fp8: the routed experts' backward runs as
+ * moe_grouped_swiglu_bwd_fp8 does (dy_perm and [da | du] quantised, both data gradients and
+ * both weight gradients on E4M3 operands); the rest is that of moe_layer_bwd.  Outputs as
+ * moe_layer_bwd; fp8.scales[4..7] are written.  Workspace MOE_WS_LAYER_BWD_FP8. */
+int moe_layer_bwd_fp8(const moe_cfg* cfg, const void* dy, const void* x, const void* W_r,
+                      const moe_fp8_experts* fp8, const void* Ws1, const void* Ws2,
+                      const void* w_sg, const moe_saved* saved, void* dx, float* dW_r, float* dW1,
+                      float* dW2, float* dWs1, float* dWs2, float* dw_sg, void* ws,
+                      size_t ws_bytes, void* stream);
 
 /* Message of the last error on this host thread ("" if none). */
 const char* moe_last_error(void);

@@ -22,7 +22,7 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3:
 SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 DTYPE_BF16, DTYPE_F32 = 0, 1
 BIAS_LOGIT, BIAS_SELECT = 0, 1
-WS_ROUTE, WS_FFN_FWD, WS_FFN_BWD, WS_LAYER_FWD, WS_LAYER_BWD, WS_FFN_BWD_FP8 = range(6)
+WS_ROUTE, WS_FFN_FWD, WS_FFN_BWD, WS_LAYER_FWD, WS_LAYER_BWD, WS_FFN_BWD_FP8, WS_LAYER_BWD_FP8 = range(7)
 
 
 class MoeCfg(ctypes.Structure):
@@ -35,6 +35,11 @@ class MoeSaved(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("logits", "idx", "gate", "counts", "offsets", "slot_of_pair", "token_of_slot",
                  "x_perm", "act", "h", "y_perm", "s_act", "s_h", "s_out", "s_coef", "aux_loss")]
+
+
+class MoeFp8Experts(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("W1_q", "W1_scale", "W2_q", "W2_scale", "x_perm_q", "h_q", "scales")]
 
 
 _VP = ctypes.c_void_p
@@ -56,6 +61,10 @@ _SIGS = {
     "moe_unpermute_combine": (ctypes.c_int, [_CFG] + [_VP] * 7),
     "moe_unpermute_combine_bwd": (ctypes.c_int, [_CFG] + [_VP] * 11),
     "moe_layer_fwd": (ctypes.c_int, [_CFG] + [_VP] * 9 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP]),
+    "moe_layer_fwd_fp8": (ctypes.c_int, [_CFG] + [_VP] * 3 + [ctypes.POINTER(MoeFp8Experts)]
+                          + [_VP] * 4 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP]),
+    "moe_layer_bwd_fp8": (ctypes.c_int, [_CFG] + [_VP] * 3 + [ctypes.POINTER(MoeFp8Experts)]
+                          + [_VP] * 3 + [ctypes.POINTER(MoeSaved)] + [_VP] * 8 + [_SZ, _VP]),
     "moe_layer_bwd": (ctypes.c_int, [_CFG] + [_VP] * 8 + [ctypes.POINTER(MoeSaved)] + [_VP] * 8
                       + [_SZ, _VP]),
     "moe_router_aux_loss": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP, _SZ, _VP]),
@@ -298,6 +307,47 @@ def moe_layer_bwd(cfg, dy, x, W_r, W1, W2, Ws1, Ws2, w_sg, saved, dx, dW_r, dW1,
                                _p(Ws2), _p(w_sg), ctypes.byref(st), _p(dx), _p(dW_r), _p(dW1),
                                _p(dW2), _p(dWs1), _p(dWs2), _p(dw_sg), _p(ws), ws.numel(),
                                _stream(stream)), "moe_layer_bwd")
+
+
+def alloc_fp8_experts(cfg, W1, W2, device="cuda", stream=None):
+    """FP8 state of the routed experts (torch tensors): W1 and W2 quantised once to E4M3 with
+    one scale per expert (FP8 parameters), and the buffers the FP8 layer calls write."""
+    import torch
+    E, d, f = cfg.E, cfg.d, cfg.f
+    N = max(cfg.T, 1) * cfg.k
+    u8, f32 = torch.uint8, torch.float32
+    q = dict(W1_q=torch.empty(E, 2 * f, d, dtype=u8, device=device),
+             W1_scale=torch.empty(E, dtype=f32, device=device),
+             W2_q=torch.empty(E, d, f, dtype=u8, device=device),
+             W2_scale=torch.empty(E, dtype=f32, device=device),
+             x_perm_q=torch.empty(N, d, dtype=u8, device=device),
+             h_q=torch.empty(N, f, dtype=u8, device=device),
+             scales=torch.zeros(8, dtype=f32, device=device))
+    amax = torch.empty(E, dtype=f32, device=device)
+    moe_quantize_e4m3(W1, E, q["W1_q"], q["W1_scale"], amax, stream)
+    moe_quantize_e4m3(W2, E, q["W2_q"], q["W2_scale"], amax, stream)
+    return q
+
+
+def fp8_struct(q):
+    return MoeFp8Experts(*[None if q.get(n) is None else q[n].data_ptr()
+                           for n, _ in MoeFp8Experts._fields_])
+
+
+def moe_layer_fwd_fp8(cfg, x, W_r, b_r, fp8, Ws1, Ws2, w_sg, y, saved, ws, stream=None):
+    st, qs = saved_struct(saved), fp8_struct(fp8)
+    _check(lib().moe_layer_fwd_fp8(ctypes.byref(cfg), _p(x), _p(W_r), _p(b_r), ctypes.byref(qs),
+                                   _p(Ws1), _p(Ws2), _p(w_sg), _p(y), ctypes.byref(st), _p(ws),
+                                   ws.numel(), _stream(stream)), "moe_layer_fwd_fp8")
+
+
+def moe_layer_bwd_fp8(cfg, dy, x, W_r, fp8, Ws1, Ws2, w_sg, saved, dx, dW_r, dW1, dW2, dWs1, dWs2,
+                      dw_sg, ws, stream=None):
+    st, qs = saved_struct(saved), fp8_struct(fp8)
+    _check(lib().moe_layer_bwd_fp8(ctypes.byref(cfg), _p(dy), _p(x), _p(W_r), ctypes.byref(qs),
+                                   _p(Ws1), _p(Ws2), _p(w_sg), ctypes.byref(st), _p(dx), _p(dW_r),
+                                   _p(dW1), _p(dW2), _p(dWs1), _p(dWs2), _p(dw_sg), _p(ws),
+                                   ws.numel(), _stream(stream)), "moe_layer_bwd_fp8")
 
 
 def set_stream_overlap(on):

@@ -483,6 +483,168 @@ static int ffn_bwd_impl(const moe_cfg* c, int G, const int32_t* offsets, int64_t
   return gemm(c, w, st);
 }
 
+// The routed experts' forward on E4M3 operands (fc1 + SwiGLU with h's amax, h quantised, fc2).
+static int ffn_fwd_fp8_impl(const moe_cfg* c, const int32_t* offsets, const uint8_t* x_perm_q,
+                            const float* x_scale, const uint8_t* W1_q, const float* W1_scale,
+                            const uint8_t* W2_q, const float* W2_scale, void* h, void* act,
+                            uint8_t* h_q, float* h_scale, float* h_amax, void* y_perm,
+                            cudaStream_t st) {
+  const int64_t N = Nrows(c);
+  const int d = c->d, f = c->f, E = c->E;
+  // fc1 + SwiGLU on E4M3 operands -> h, [a | u] (bf16)
+  GemmDesc g1 = desc0();
+  g1.name = "gemm_fc1_swiglu_fp8";
+  g1.sched = RAGGED_M;
+  g1.epi = EPI_SWIGLU_FWD;
+  g1.G = E;
+  g1.offsets = offsets;
+  g1.M = static_cast<int>(N);
+  g1.N = 2 * f;
+  g1.K = d;
+  g1.A = opnd(x_perm_q, N, d, false);
+  g1.B = opnd(W1_q, static_cast<int64_t>(E) * 2 * f, d, false);
+  g1.b_group_rows = 2 * f;
+  g1.b_up_rows = f;
+  g1.f = f;
+  g1.out = h;
+  g1.ldo = f;
+  g1.out2 = act;
+  g1.ldo2 = 2 * f;
+  g1.fp8 = true;
+  g1.a_scale = x_scale;
+  g1.b_scale = W1_scale;
+  g1.amax_out = h_amax;   // max |h| taken in fc1's epilogue
+  if (cudaMemsetAsync(h_amax, 0, sizeof(float), st) != cudaSuccess)
+    return fail(MOE_ERR_CUDA, "clearing h_amax failed");
+  MOE_TRY(gemm_tc(g1, st));
+  // h -> E4M3 (one tensor) with that amax
+  MOE_TRY(launch_quant_e4m3_given_amax(h, N * f, 1, h_q, h_scale, h_amax, st));
+  // fc2 on E4M3 operands -> y_perm (bf16)
+  GemmDesc g2 = desc0();
+  g2.name = "gemm_fc2_fp8";
+  g2.sched = RAGGED_M;
+  g2.epi = EPI_STORE;
+  g2.G = E;
+  g2.offsets = offsets;
+  g2.M = static_cast<int>(N);
+  g2.N = d;
+  g2.K = f;
+  g2.A = opnd(h_q, N, f, false);
+  g2.B = opnd(W2_q, static_cast<int64_t>(E) * d, f, false);
+  g2.b_group_rows = d;
+  g2.out = y_perm;
+  g2.ldo = d;
+  g2.fp8 = true;
+  g2.a_scale = h_scale;
+  g2.b_scale = W2_scale;
+  return gemm_tc(g2, st);
+}
+
+// The routed experts' backward on E4M3 operands: dy quantised, fc2 dgrad + SwiGLU backward
+// (with [da | du]'s amax), [da | du] quantised, fc2 wgrad, fc1 dgrad, fc1 wgrad.  dx_perm may
+// alias dy_perm (dy_perm is read only by the first quantisation).
+static int ffn_bwd_fp8_impl(const moe_cfg* c, const int32_t* offsets, const uint8_t* x_perm_q,
+                            const float* x_scale, const uint8_t* W1_q, const float* W1_scale,
+                            const uint8_t* W2_q, const float* W2_scale, const void* act,
+                            const uint8_t* h_q, const float* h_scale, const void* dy_perm,
+                            uint8_t* dy_q, float* dy_scale, float* dy_amax, void* dH1,
+                            uint8_t* dH1_q, float* dH1_scale, float* dH1_amax, void* dx_perm,
+                            float* dW1, float* dW2, int* sched, cudaStream_t st) {
+  const int64_t N = Nrows(c);
+  const int d = c->d, f = c->f, E = c->E;
+  // dy_perm -> E4M3 (one tensor)
+  MOE_TRY(launch_quantize_e4m3(dy_perm, N * d, 1, dy_q, dy_scale, dy_amax, st));
+  // dh = dy . W2_e on E4M3 operands (W2_q read MN-major: no transposed copy), SwiGLU backward
+  // -> dH1 = [da | du] (bf16) with its amax
+  GemmDesc a = desc0();
+  a.name = "gemm_fc2_dgrad_fp8";
+  a.sched = RAGGED_M;
+  a.epi = EPI_SWIGLU_BWD;
+  a.G = E;
+  a.offsets = offsets;
+  a.M = static_cast<int>(N);
+  a.N = f;
+  a.K = d;
+  a.A = opnd(dy_q, N, d, false);
+  a.B = opnd(W2_q, static_cast<int64_t>(E) * d, f, true);
+  a.b_group_rows = d;
+  a.f = f;
+  a.out = dH1;
+  a.ldo = 2 * f;
+  a.aux = act;
+  a.ld_aux = 2 * f;
+  a.fp8 = true;
+  a.a_scale = dy_scale;
+  a.b_scale = W2_scale;
+  a.amax_out = dH1_amax;
+  if (cudaMemsetAsync(dH1_amax, 0, sizeof(float), st) != cudaSuccess)
+    return fail(MOE_ERR_CUDA, "clearing dH1_amax failed");
+  MOE_TRY(gemm_tc(a, st));
+  // dH1 -> E4M3 (one tensor) with that amax
+  MOE_TRY(launch_quant_e4m3_given_amax(dH1, N * 2 * f, 1, dH1_q, dH1_scale, dH1_amax, st));
+  // dW2_e = dy_e^T . h_e (both MN-major over the expert's rows)
+  GemmDesc b = desc0();
+  b.name = "gemm_fc2_wgrad_fp8";
+  b.sched = RAGGED_K;
+  b.epi = EPI_F32;
+  b.G = E;
+  b.offsets = offsets;
+  b.M = d;
+  b.N = f;
+  b.K = static_cast<int>(N);
+  b.A = opnd(dy_q, N, d, true);
+  b.B = opnd(h_q, N, f, true);
+  b.out = dW2;
+  b.ldo = f;
+  b.out_group_stride = static_cast<int64_t>(d) * f;
+  b.tile_ctr = sched;
+  b.fp8 = true;
+  b.a_scale = dy_scale;
+  b.b_scale = h_scale;
+  b.b_scale_scalar = true;
+  MOE_TRY(gemm_tc(b, st));
+  // dx_perm = dH1 . W1_e
+  GemmDesc e = desc0();
+  e.name = "gemm_fc1_dgrad_fp8";
+  e.sched = RAGGED_M;
+  e.epi = EPI_STORE;
+  e.G = E;
+  e.offsets = offsets;
+  e.M = static_cast<int>(N);
+  e.N = d;
+  e.K = 2 * f;
+  e.A = opnd(dH1_q, N, 2 * f, false);
+  e.B = opnd(W1_q, static_cast<int64_t>(E) * 2 * f, d, true);
+  e.b_group_rows = 2 * f;
+  e.out = dx_perm;
+  e.ldo = d;
+  e.fp8 = true;
+  e.a_scale = dH1_scale;
+  e.b_scale = W1_scale;
+  MOE_TRY(gemm_tc(e, st));
+  // dW1_e = dH1_e^T . x_perm_e
+  GemmDesc w = desc0();
+  w.name = "gemm_fc1_wgrad_fp8";
+  w.sched = RAGGED_K;
+  w.epi = EPI_F32;
+  w.G = E;
+  w.offsets = offsets;
+  w.M = 2 * f;
+  w.N = d;
+  w.K = static_cast<int>(N);
+  w.A = opnd(dH1_q, N, 2 * f, true);
+  w.B = opnd(x_perm_q, N, d, true);
+  w.out = dW1;
+  w.ldo = d;
+  w.out_group_stride = static_cast<int64_t>(2) * f * d;
+  w.tile_ctr = sched + 4;
+  w.fp8 = true;
+  w.a_scale = dH1_scale;
+  w.b_scale = x_scale;
+  w.b_scale_scalar = true;
+  return gemm_tc(w, st);
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -578,6 +740,11 @@ size_t moe_workspace_bytes(const moe_cfg* c, int which) {
       break;
     case MOE_WS_FFN_BWD_FP8:
       cv.take(2 * 4 * sizeof(int));
+      break;
+    case MOE_WS_LAYER_BWD_FP8:
+      carve_bwd(cv, c);
+      cv.take(static_cast<size_t>(Nrows(c)) * c->d);
+      cv.take(static_cast<size_t>(Nrows(c)) * 2 * c->f);
       break;
     default:
       return 0;
@@ -782,54 +949,8 @@ int moe_grouped_swiglu_fwd_fp8(const moe_cfg* c, const uint8_t* x_perm_q, const 
   cudaStream_t st = S(stream);
   const int64_t N = Nrows(c);
   if (N == 0) return MOE_OK;
-  const int d = c->d, f = c->f, E = c->E;
-  // fc1 + SwiGLU on E4M3 operands -> h, [a | u] (bf16)
-  GemmDesc g1 = desc0();
-  g1.name = "gemm_fc1_swiglu_fp8";
-  g1.sched = RAGGED_M;
-  g1.epi = EPI_SWIGLU_FWD;
-  g1.G = E;
-  g1.offsets = offsets;
-  g1.M = static_cast<int>(N);
-  g1.N = 2 * f;
-  g1.K = d;
-  g1.A = opnd(x_perm_q, N, d, false);
-  g1.B = opnd(W1_q, static_cast<int64_t>(E) * 2 * f, d, false);
-  g1.b_group_rows = 2 * f;
-  g1.b_up_rows = f;
-  g1.f = f;
-  g1.out = h;
-  g1.ldo = f;
-  g1.out2 = act;
-  g1.ldo2 = 2 * f;
-  g1.fp8 = true;
-  g1.a_scale = x_scale;
-  g1.b_scale = W1_scale;
-  g1.amax_out = h_amax;   // max |h| taken in fc1's epilogue
-  if (cudaMemsetAsync(h_amax, 0, sizeof(float), st) != cudaSuccess)
-    return fail(MOE_ERR_CUDA, "clearing h_amax failed");
-  MOE_TRY(gemm_tc(g1, st));
-  // h -> E4M3 (one tensor) with that amax
-  MOE_TRY(launch_quant_e4m3_given_amax(h, N * f, 1, h_q, h_scale, h_amax, st));
-  // fc2 on E4M3 operands -> y_perm (bf16)
-  GemmDesc g2 = desc0();
-  g2.name = "gemm_fc2_fp8";
-  g2.sched = RAGGED_M;
-  g2.epi = EPI_STORE;
-  g2.G = E;
-  g2.offsets = offsets;
-  g2.M = static_cast<int>(N);
-  g2.N = d;
-  g2.K = f;
-  g2.A = opnd(h_q, N, f, false);
-  g2.B = opnd(W2_q, static_cast<int64_t>(E) * d, f, false);
-  g2.b_group_rows = d;
-  g2.out = y_perm;
-  g2.ldo = d;
-  g2.fp8 = true;
-  g2.a_scale = h_scale;
-  g2.b_scale = W2_scale;
-  return gemm_tc(g2, st);
+  return ffn_fwd_fp8_impl(c, offsets, x_perm_q, x_scale, W1_q, W1_scale, W2_q, W2_scale, h, act,
+                          h_q, h_scale, h_amax, y_perm, st);
 }
 
 int moe_grouped_swiglu_bwd_fp8(const moe_cfg* c, const uint8_t* x_perm_q, const float* x_scale,
@@ -864,97 +985,9 @@ int moe_grouped_swiglu_bwd_fp8(const moe_cfg* c, const uint8_t* x_perm_q, const 
   }
   Carve cv(ws);
   int* sched = static_cast<int*>(cv.take(2 * 4 * sizeof(int)));
-  // dy_perm -> E4M3 (one tensor)
-  MOE_TRY(launch_quantize_e4m3(dy_perm, N * d, 1, dy_q, dy_scale, dy_amax, st));
-  // dh = dy . W2_e on E4M3 operands (W2_q read MN-major: no transposed copy), SwiGLU backward
-  // -> dH1 = [da | du] (bf16) with its amax
-  GemmDesc a = desc0();
-  a.name = "gemm_fc2_dgrad_fp8";
-  a.sched = RAGGED_M;
-  a.epi = EPI_SWIGLU_BWD;
-  a.G = E;
-  a.offsets = offsets;
-  a.M = static_cast<int>(N);
-  a.N = f;
-  a.K = d;
-  a.A = opnd(dy_q, N, d, false);
-  a.B = opnd(W2_q, static_cast<int64_t>(E) * d, f, true);
-  a.b_group_rows = d;
-  a.f = f;
-  a.out = dH1;
-  a.ldo = 2 * f;
-  a.aux = act;
-  a.ld_aux = 2 * f;
-  a.fp8 = true;
-  a.a_scale = dy_scale;
-  a.b_scale = W2_scale;
-  a.amax_out = dH1_amax;
-  if (cudaMemsetAsync(dH1_amax, 0, sizeof(float), st) != cudaSuccess)
-    return fail(MOE_ERR_CUDA, "clearing dH1_amax failed");
-  MOE_TRY(gemm_tc(a, st));
-  // dH1 -> E4M3 (one tensor) with that amax
-  MOE_TRY(launch_quant_e4m3_given_amax(dH1, N * 2 * f, 1, dH1_q, dH1_scale, dH1_amax, st));
-  // dW2_e = dy_e^T . h_e (both MN-major over the expert's rows)
-  GemmDesc b = desc0();
-  b.name = "gemm_fc2_wgrad_fp8";
-  b.sched = RAGGED_K;
-  b.epi = EPI_F32;
-  b.G = E;
-  b.offsets = offsets;
-  b.M = d;
-  b.N = f;
-  b.K = static_cast<int>(N);
-  b.A = opnd(dy_q, N, d, true);
-  b.B = opnd(h_q, N, f, true);
-  b.out = dW2;
-  b.ldo = f;
-  b.out_group_stride = static_cast<int64_t>(d) * f;
-  b.tile_ctr = sched;
-  b.fp8 = true;
-  b.a_scale = dy_scale;
-  b.b_scale = h_scale;
-  b.b_scale_scalar = true;
-  MOE_TRY(gemm_tc(b, st));
-  // dx_perm = dH1 . W1_e
-  GemmDesc e = desc0();
-  e.name = "gemm_fc1_dgrad_fp8";
-  e.sched = RAGGED_M;
-  e.epi = EPI_STORE;
-  e.G = E;
-  e.offsets = offsets;
-  e.M = static_cast<int>(N);
-  e.N = d;
-  e.K = 2 * f;
-  e.A = opnd(dH1_q, N, 2 * f, false);
-  e.B = opnd(W1_q, static_cast<int64_t>(E) * 2 * f, d, true);
-  e.b_group_rows = 2 * f;
-  e.out = dx_perm;
-  e.ldo = d;
-  e.fp8 = true;
-  e.a_scale = dH1_scale;
-  e.b_scale = W1_scale;
-  MOE_TRY(gemm_tc(e, st));
-  // dW1_e = dH1_e^T . x_perm_e
-  GemmDesc w = desc0();
-  w.name = "gemm_fc1_wgrad_fp8";
-  w.sched = RAGGED_K;
-  w.epi = EPI_F32;
-  w.G = E;
-  w.offsets = offsets;
-  w.M = 2 * f;
-  w.N = d;
-  w.K = static_cast<int>(N);
-  w.A = opnd(dH1_q, N, 2 * f, true);
-  w.B = opnd(x_perm_q, N, d, true);
-  w.out = dW1;
-  w.ldo = d;
-  w.out_group_stride = static_cast<int64_t>(2) * f * d;
-  w.tile_ctr = sched + 4;
-  w.fp8 = true;
-  w.a_scale = dH1_scale;
-  w.b_scale = x_scale;
-  w.b_scale_scalar = true;
-  return gemm_tc(w, st);
+  return ffn_bwd_fp8_impl(c, offsets, x_perm_q, x_scale, W1_q, W1_scale, W2_q, W2_scale, act, h_q,
+                          h_scale, dy_perm, dy_q, dy_scale, dy_amax, dH1, dH1_q, dH1_scale,
+                          dH1_amax, dx_perm, dW1, dW2, sched, st);
 }
 
 int moe_unpermute_combine(const moe_cfg* c, const void* y_perm, const float* gate,
@@ -1020,7 +1053,22 @@ int moe_expert_bias_update(const moe_cfg* c, const int32_t* counts, float* e_bia
   return launch_bias_update(counts, e_bias, c->T, c->k, c->E, rate, S(stream));
 }
 
-static int check_saved(const moe_cfg* c, const moe_saved* s) {
+static int check_fp8_experts(const moe_cfg* c, const moe_fp8_experts* q) {
+  if (c->dtype != MOE_DTYPE_BF16)
+    return fail(MOE_ERR_UNSUPPORTED, "the FP8 experts read and write bf16 activations (dtype bf16)");
+  if (c->d % 16 || c->f % 16)
+    return fail(MOE_ERR_UNSUPPORTED, "FP8 rows need d and f multiples of 16 (16-byte rows)");
+  MOE_TRY(check_ptr(q->W1_q, "fp8.W1_q", true));
+  MOE_TRY(check_ptr(q->W1_scale, "fp8.W1_scale", true));
+  MOE_TRY(check_ptr(q->W2_q, "fp8.W2_q", true));
+  MOE_TRY(check_ptr(q->W2_scale, "fp8.W2_scale", true));
+  MOE_TRY(check_ptr(q->x_perm_q, "fp8.x_perm_q", true));
+  MOE_TRY(check_ptr(q->h_q, "fp8.h_q", true));
+  MOE_TRY(check_ptr(q->scales, "fp8.scales", true));
+  return MOE_OK;
+}
+
+static int check_saved(const moe_cfg* c, const moe_saved* s, bool fp8 = false) {
   if (!s) return fail(MOE_ERR_INVALID_ARG, "saved is NULL");
   MOE_TRY(check_ptr(s->logits, "saved.logits", true));
   MOE_TRY(check_ptr(s->idx, "saved.idx", true));
@@ -1029,7 +1077,7 @@ static int check_saved(const moe_cfg* c, const moe_saved* s) {
   MOE_TRY(check_ptr(s->offsets, "saved.offsets", true));
   MOE_TRY(check_ptr(s->slot_of_pair, "saved.slot_of_pair", true));
   MOE_TRY(check_ptr(s->token_of_slot, "saved.token_of_slot", true));
-  MOE_TRY(check_ptr(s->x_perm, "saved.x_perm", !permute_fused(c)));
+  MOE_TRY(check_ptr(s->x_perm, "saved.x_perm", !fp8 && !permute_fused(c)));
   MOE_TRY(check_ptr(s->act, "saved.act", true));
   MOE_TRY(check_ptr(s->h, "saved.h", true));
   MOE_TRY(check_ptr(s->y_perm, "saved.y_perm", true));
@@ -1042,22 +1090,24 @@ static int check_saved(const moe_cfg* c, const moe_saved* s) {
   return MOE_OK;
 }
 
-int moe_layer_fwd(const moe_cfg* c, const void* x, const void* W_r, const float* b_r,
-                  const void* W1, const void* W2, const void* Ws1, const void* Ws2,
-                  const void* w_sg, void* y, const moe_saved* s, void* ws, size_t ws_bytes,
-                  void* stream) {
+// The layer forward; with q the routed experts run on E4M3 operands (q's weights and buffers).
+static int layer_fwd_impl(const moe_cfg* c, const void* x, const void* W_r, const float* b_r,
+                          const void* W1, const void* W2, const moe_fp8_experts* q,
+                          const void* Ws1, const void* Ws2, const void* w_sg, void* y,
+                          const moe_saved* s, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(check_cfg(c));
   MOE_TRY(check_ptr(x, "x", true));
   MOE_TRY(check_ptr(W_r, "W_r", true));
   MOE_TRY(check_ptr(b_r, "b_r", false));
-  MOE_TRY(check_ptr(W1, "W1", true));
-  MOE_TRY(check_ptr(W2, "W2", true));
+  MOE_TRY(check_ptr(W1, "W1", !q));
+  MOE_TRY(check_ptr(W2, "W2", !q));
+  if (q) MOE_TRY(check_fp8_experts(c, q));
   const bool sh = c->f_shared > 0, gt = c->shared_gate != 0;
   MOE_TRY(check_ptr(Ws1, "Ws1", sh));
   MOE_TRY(check_ptr(Ws2, "Ws2", sh));
   MOE_TRY(check_ptr(w_sg, "w_sg", gt));
   MOE_TRY(check_ptr(y, "y", true));
-  MOE_TRY(check_saved(c, s));
+  MOE_TRY(check_saved(c, s, q != nullptr));
   MOE_TRY(check_ws(c, MOE_WS_LAYER_FWD, ws, ws_bytes));
   cudaStream_t st = S(stream);
   if (c->T == 0) {
@@ -1092,7 +1142,14 @@ int moe_layer_fwd(const moe_cfg* c, const void* x, const void* W_r, const float*
   if (c->aux_coeff > 0.0f)
     MOE_TRY(launch_aux_loss(s->logits, s->counts, c->T, c->E, c->k, c->score_fn, c->aux_coeff,
                             w.aux, s->aux_loss, st));
-  if (permute_fused(c)) {
+  if (q) {
+    // "Megatron-Bridge 深度剖析", §FP8 训练: x permuted and quantised in one pass, E4M3 experts
+    MOE_TRY(launch_permute_quant_e4m3(x, s->slot_of_pair, q->x_perm_q, q->scales + 0,
+                                      q->scales + 1, c->T, c->d, c->k, st));
+    MOE_TRY(ffn_fwd_fp8_impl(c, s->offsets, q->x_perm_q, q->scales + 0, q->W1_q, q->W1_scale,
+                             q->W2_q, q->W2_scale, s->h, s->act, q->h_q, q->scales + 2,
+                             q->scales + 3, s->y_perm, st));
+  } else if (permute_fused(c)) {
     // "Megatron-Bridge 深度剖析", §Permute Fusion: fc1 gathers its rows from x by token_of_slot
     MOE_TRY(ffn_fwd_impl(c, c->E, s->offsets, Nrows(c), c->f, x, W1, W2, s->h, s->act,
                          s->y_perm, st, s->token_of_slot, c->T));
@@ -1112,22 +1169,24 @@ int moe_layer_fwd(const moe_cfg* c, const void* x, const void* W_r, const float*
                         gt ? s->s_coef : nullptr, y, c->T, c->d, c->k, st);
 }
 
-int moe_layer_bwd(const moe_cfg* c, const void* dy, const void* x, const void* W_r,
-                  const void* W1, const void* W2, const void* Ws1, const void* Ws2,
-                  const void* w_sg, const moe_saved* s, void* dx, float* dW_r, float* dW1,
-                  float* dW2, float* dWs1, float* dWs2, float* dw_sg, void* ws, size_t ws_bytes,
-                  void* stream) {
+// The layer backward; with q the routed experts' backward runs on E4M3 operands.
+static int layer_bwd_impl(const moe_cfg* c, const void* dy, const void* x, const void* W_r,
+                          const void* W1, const void* W2, const moe_fp8_experts* q,
+                          const void* Ws1, const void* Ws2, const void* w_sg, const moe_saved* s,
+                          void* dx, float* dW_r, float* dW1, float* dW2, float* dWs1,
+                          float* dWs2, float* dw_sg, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(check_cfg(c));
   const bool sh = c->f_shared > 0, gt = c->shared_gate != 0;
   MOE_TRY(check_ptr(dy, "dy", true));
   MOE_TRY(check_ptr(x, "x", true));
   MOE_TRY(check_ptr(W_r, "W_r", true));
-  MOE_TRY(check_ptr(W1, "W1", true));
-  MOE_TRY(check_ptr(W2, "W2", true));
+  MOE_TRY(check_ptr(W1, "W1", !q));
+  MOE_TRY(check_ptr(W2, "W2", !q));
+  if (q) MOE_TRY(check_fp8_experts(c, q));
   MOE_TRY(check_ptr(Ws1, "Ws1", sh));
   MOE_TRY(check_ptr(Ws2, "Ws2", sh));
   MOE_TRY(check_ptr(w_sg, "w_sg", gt));
-  MOE_TRY(check_saved(c, s));
+  MOE_TRY(check_saved(c, s, q != nullptr));
   MOE_TRY(check_ptr(dx, "dx", true));
   MOE_TRY(check_ptr(dW_r, "dW_r", true));
   MOE_TRY(check_ptr(dW1, "dW1", true));
@@ -1135,7 +1194,7 @@ int moe_layer_bwd(const moe_cfg* c, const void* dy, const void* x, const void* W
   MOE_TRY(check_ptr(dWs1, "dWs1", sh));
   MOE_TRY(check_ptr(dWs2, "dWs2", sh));
   MOE_TRY(check_ptr(dw_sg, "dw_sg", gt));
-  MOE_TRY(check_ws(c, MOE_WS_LAYER_BWD, ws, ws_bytes));
+  MOE_TRY(check_ws(c, q ? MOE_WS_LAYER_BWD_FP8 : MOE_WS_LAYER_BWD, ws, ws_bytes));
   cudaStream_t st = S(stream);
   const int T = c->T, d = c->d, E = c->E, k = c->k;
   if (T == 0) {
@@ -1150,6 +1209,9 @@ int moe_layer_bwd(const moe_cfg* c, const void* dy, const void* x, const void* W
   }
   Carve cv(ws);
   BwdWs w = carve_bwd(cv, c);
+  uint8_t* dy_q = q ? static_cast<uint8_t*>(cv.take(static_cast<size_t>(Nrows(c)) * d)) : nullptr;
+  uint8_t* dH1_q =
+      q ? static_cast<uint8_t*>(cv.take(static_cast<size_t>(Nrows(c)) * 2 * c->f)) : nullptr;
   // 1. combine backward
   MOE_TRY(launch_combine_bwd(c->dtype, dy, s->y_perm, s->gate, s->slot_of_pair,
                              sh ? s->s_out : nullptr, gt ? s->s_coef : nullptr, w.dy_perm, w.dgate,
@@ -1217,7 +1279,12 @@ int moe_layer_bwd(const moe_cfg* c, const void* dy, const void* x, const void* W
       return fail(MOE_ERR_CUDA, "recording the side stream's completion failed");
   }
   // routed experts (dx_perm overwrites dy_perm once it is no longer read)
-  if (permute_fused(c))
+  if (q)
+    MOE_TRY(ffn_bwd_fp8_impl(c, s->offsets, q->x_perm_q, q->scales + 0, q->W1_q, q->W1_scale,
+                             q->W2_q, q->W2_scale, s->act, q->h_q, q->scales + 2, w.dy_perm, dy_q,
+                             q->scales + 4, q->scales + 5, w.dH1, dH1_q, q->scales + 6,
+                             q->scales + 7, w.dy_perm, dW1, dW2, w.sched, st));
+  else if (permute_fused(c))
     MOE_TRY(ffn_bwd_impl(c, E, s->offsets, Nrows(c), c->f, x, W1, W2, s->act, s->h, w.dy_perm,
                          w.dH1, w.dy_perm, dW1, dW2, w.sched, st, s->token_of_slot, T));
   else
@@ -1233,6 +1300,42 @@ int moe_layer_bwd(const moe_cfg* c, const void* dy, const void* x, const void* W
   // 7. dx = sum_j dx_perm[slot(t,j)] + dx_shared + dx_router + dz * w_sg
   return launch_gather_sum(c->dtype, w.dy_perm, s->slot_of_pair, sh ? w.dx_shared : nullptr,
                            w.dx_router, gt ? w.dz : nullptr, gt ? w_sg : nullptr, dx, T, d, k, st);
+}
+
+int moe_layer_fwd(const moe_cfg* c, const void* x, const void* W_r, const float* b_r,
+                  const void* W1, const void* W2, const void* Ws1, const void* Ws2,
+                  const void* w_sg, void* y, const moe_saved* s, void* ws, size_t ws_bytes,
+                  void* stream) {
+  return layer_fwd_impl(c, x, W_r, b_r, W1, W2, nullptr, Ws1, Ws2, w_sg, y, s, ws, ws_bytes,
+                        stream);
+}
+
+int moe_layer_fwd_fp8(const moe_cfg* c, const void* x, const void* W_r, const float* b_r,
+                      const moe_fp8_experts* q, const void* Ws1, const void* Ws2,
+                      const void* w_sg, void* y, const moe_saved* s, void* ws, size_t ws_bytes,
+                      void* stream) {
+  if (!q) return fail(MOE_ERR_INVALID_ARG, "fp8 is NULL");
+  return layer_fwd_impl(c, x, W_r, b_r, nullptr, nullptr, q, Ws1, Ws2, w_sg, y, s, ws, ws_bytes,
+                        stream);
+}
+
+int moe_layer_bwd(const moe_cfg* c, const void* dy, const void* x, const void* W_r,
+                  const void* W1, const void* W2, const void* Ws1, const void* Ws2,
+                  const void* w_sg, const moe_saved* s, void* dx, float* dW_r, float* dW1,
+                  float* dW2, float* dWs1, float* dWs2, float* dw_sg, void* ws, size_t ws_bytes,
+                  void* stream) {
+  return layer_bwd_impl(c, dy, x, W_r, W1, W2, nullptr, Ws1, Ws2, w_sg, s, dx, dW_r, dW1, dW2,
+                        dWs1, dWs2, dw_sg, ws, ws_bytes, stream);
+}
+
+int moe_layer_bwd_fp8(const moe_cfg* c, const void* dy, const void* x, const void* W_r,
+                      const moe_fp8_experts* q, const void* Ws1, const void* Ws2,
+                      const void* w_sg, const moe_saved* s, void* dx, float* dW_r, float* dW1,
+                      float* dW2, float* dWs1, float* dWs2, float* dw_sg, void* ws,
+                      size_t ws_bytes, void* stream) {
+  if (!q) return fail(MOE_ERR_INVALID_ARG, "fp8 is NULL");
+  return layer_bwd_impl(c, dy, x, W_r, nullptr, nullptr, q, Ws1, Ws2, w_sg, s, dx, dW_r, dW1, dW2,
+                        dWs1, dWs2, dw_sg, ws, ws_bytes, stream);
 }
 
 }  // extern "C"
