@@ -415,6 +415,8 @@ def run_gpu(args, lc):
         return None
 
     fp8 = None if args.no_fp8 or lc.dtype != "bf16" else fp8_experts(args, lc, cfg, inp, saved, dev)
+    if fp8 is not None:
+        fp8["layer"] = fp8_layer(args, lc, cfg, inp, dev, ms_step)
 
     # ---- roofline of the dominant kernel (largest share of device time in the timed region)
     peaks, peak_src = load_peaks()
@@ -594,6 +596,69 @@ def fp8_experts(args, lc, cfg, inp, saved, dev):
                      if gemm_ms else None,
                      "kernels_ms": per, "scope": scope}
     return out
+
+
+def fp8_layer(args, lc, cfg, inp, dev, ms_bf16):
+    """The whole layer step with FP8 routed experts (moe_layer_fwd_fp8 / moe_layer_bwd_fp8: router,
+    shared expert and combine as in bf16; E4M3 weights quantised once as FP8 parameters, x,
+    h, dy_perm and [da | du] quantised inside the step), replayed from a CUDA graph like the
+    bf16 step it is compared with."""
+    import torch
+    import moe_expert_layer_gemm_gb300 as moe
+    saved = moe.alloc_saved(cfg, dev)
+    saved["x_perm"] = None
+    q = moe.alloc_fp8_experts(cfg, inp["W1"], inp["W2"], dev)
+    f32 = torch.float32
+    y = torch.empty_like(inp["x"])
+    g = dict(dx=torch.empty_like(inp["x"]), dW_r=torch.empty(lc.E, lc.d, dtype=f32, device=dev),
+             dW1=torch.empty(lc.E, 2 * lc.f, lc.d, dtype=f32, device=dev),
+             dW2=torch.empty(lc.E, lc.d, lc.f, dtype=f32, device=dev),
+             dWs1=torch.empty(2 * lc.f_shared, lc.d, dtype=f32, device=dev) if lc.f_shared else None,
+             dWs2=torch.empty(lc.d, lc.f_shared, dtype=f32, device=dev) if lc.f_shared else None,
+             dw_sg=torch.empty(lc.d, dtype=f32, device=dev) if lc.shared_gate else None)
+    ws_f = moe.workspace(cfg, moe.WS_LAYER_FWD, dev)
+    ws_b = moe.workspace(cfg, moe.WS_LAYER_BWD_FP8, dev)
+
+    def step():
+        moe.moe_layer_fwd_fp8(cfg, inp["x"], inp["W_r"], inp["b_r"], q, inp["Ws1"], inp["Ws2"],
+                              inp["w_sg"], y, saved, ws_f)
+        if lc.backward:
+            moe.moe_layer_bwd_fp8(cfg, inp["dy"], inp["x"], inp["W_r"], q, inp["Ws1"], inp["Ws2"],
+                                  inp["w_sg"], saved, g["dx"], g["dW_r"], g["dW1"], g["dW2"],
+                                  g["dWs1"], g["dWs2"], g["dw_sg"], ws_b)
+
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    moe.check_device_error()
+    graph = None
+    if not args.no_graph:
+        cs = torch.cuda.Stream(device=dev)
+        cs.wait_stream(stream)
+        with torch.cuda.stream(cs):
+            step()
+        stream.wait_stream(cs)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        graph.replay()
+        torch.cuda.synchronize()
+    n = max(5, min(args.steps, 50))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        graph.replay() if graph is not None else step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    moe.check_device_error()
+    ms = e0.elapsed_time(e1) / n
+    return {"ms_per_step": round(ms, 4), "tokens_per_s": round(lc.T / (ms / 1e3), 1),
+            "bf16_ms_per_step": round(ms_bf16, 4), "speedup": round(ms_bf16 / ms, 3),
+            "steps": n, "cuda_graph": graph is not None,
+            "scope": "whole layer " + ("fwd+bwd" if lc.backward else "fwd") + " with the routed "
+                     "experts in E4M3 (router, shared expert and combine in bf16)"}
 
 
 # ----------------------------------------------------------------------------- reference arm
