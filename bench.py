@@ -599,15 +599,15 @@ def fp8_experts(args, lc, cfg, inp, saved, dev):
 
 
 def fp8_layer(args, lc, cfg, inp, dev, ms_bf16):
-    """The whole layer step with FP8 routed experts (moe_layer_fwd_fp8 / moe_layer_bwd_fp8: router,
-    shared expert and combine as in bf16; E4M3 weights quantised once as FP8 parameters, x,
-    h, dy_perm and [da | du] quantised inside the step), replayed from a CUDA graph like the
-    bf16 step it is compared with."""
+    """The whole layer step with FP8 experts (moe_layer_fwd_fp8 / moe_layer_bwd_fp8: routed and
+    shared experts on E4M3 operands, router, gate and combine as in bf16; E4M3 weights quantised
+    once as FP8 parameters, activations and gradients quantised inside the step), replayed from a
+    CUDA graph like the bf16 step it is compared with."""
     import torch
     import moe_expert_layer_gemm_gb300 as moe
     saved = moe.alloc_saved(cfg, dev)
     saved["x_perm"] = None
-    q = moe.alloc_fp8_experts(cfg, inp["W1"], inp["W2"], dev)
+    q = moe.alloc_fp8_experts(cfg, inp["W1"], inp["W2"], dev, Ws1=inp["Ws1"], Ws2=inp["Ws2"])
     f32 = torch.float32
     y = torch.empty_like(inp["x"])
     g = dict(dx=torch.empty_like(inp["x"]), dW_r=torch.empty(lc.E, lc.d, dtype=f32, device=dev),
@@ -658,7 +658,7 @@ def fp8_layer(args, lc, cfg, inp, dev, ms_bf16):
             "bf16_ms_per_step": round(ms_bf16, 4), "speedup": round(ms_bf16 / ms, 3),
             "steps": n, "cuda_graph": graph is not None,
             "scope": "whole layer " + ("fwd+bwd" if lc.backward else "fwd") + " with the routed "
-                     "experts in E4M3 (router, shared expert and combine in bf16)"}
+                     "and shared experts in E4M3 (router, shared gate and combine in bf16)"}
 
 
 # ----------------------------------------------------------------------------- reference arm

@@ -341,13 +341,18 @@ int moe_layer_bwd(const moe_cfg* cfg, const void* dy, const void* x, const void*
                   float* dW2, float* dWs1, float* dWs2, float* dw_sg, void* ws, size_t ws_bytes,
                   void* stream);
 
-/* The routed experts of a layer in FP8 ("Megatron-Bridge 深度剖析", §FP8 训练: E4M3, tensorwise
+/* The experts of a layer in FP8 ("Megatron-Bridge 深度剖析", §FP8 训练: E4M3, tensorwise
  * scaling, FP8 parameters, weight gradients in FP8).  Caller-owned device buffers:
- *   W1_q [E,2f,d], W2_q [E,d,f]: E4M3 codes of the experts' weights with one fp32 scale per
- *     expert (W1_scale [E], W2_scale [E]) -- moe_quantize_e4m3 with E groups; read only;
+ *   W1_q [E,2f,d], W2_q [E,d,f]: E4M3 codes of the routed experts' weights with one fp32 scale
+ *     per expert (W1_scale [E], W2_scale [E]) -- moe_quantize_e4m3 with E groups; read only;
  *   x_perm_q [N,d], h_q [N,f]: the E4M3 activations moe_layer_fwd_fp8 leaves for the backward;
- *   scales [8] fp32: written by the calls -- [0] x scale, [1] x amax, [2] h scale, [3] h amax
- *     (forward), [4] dy_perm scale, [5] its amax, [6] [da | du] scale, [7] its amax (backward). */
+ *   scales [16] fp32, written by the calls, scale then amax of: [0] x, [2] h, [4] dy_perm,
+ *     [6] [da | du] (routed), [8] the shared expert's h, [10] its upstream gradient, [12] its
+ *     [da | du];
+ *   Ws1_q [2f_s,d], Ws2_q [d,f_s] with Ws1_scale [1], Ws2_scale [1]: the shared expert's E4M3
+ *     weights, or Ws1_q = NULL to keep the shared expert in bf16 (then the layer calls take Ws1,
+ *     Ws2); with them, x_q [T,d] (x's codes in token order, same scale) and s_h_q [T,f_s] are
+ *     written by the forward. */
 typedef struct moe_fp8_experts {
   const uint8_t* W1_q;
   const float* W1_scale;
@@ -356,14 +361,20 @@ typedef struct moe_fp8_experts {
   uint8_t* x_perm_q;
   uint8_t* h_q;
   float* scales;
+  const uint8_t* Ws1_q;
+  const float* Ws1_scale;
+  const uint8_t* Ws2_q;
+  const float* Ws2_scale;
+  uint8_t* x_q;
+  uint8_t* s_h_q;
 } moe_fp8_experts;
 
 /* moe_layer_fwd with the routed experts on E4M3 operands: x is permuted and quantised in one
  * pass (moe_permute_quantize_e4m3) and the experts run as moe_grouped_swiglu_fwd_fp8 does, with
- * fp8's weights; routing, the shared expert and the combine are those of moe_layer_fwd.  saved
- * is filled as by moe_layer_fwd except saved.x_perm (unused, may be NULL); fp8's x_perm_q, h_q
- * and scales[0..3] are written.  Workspace MOE_WS_LAYER_FWD.  cfg->dtype MOE_DTYPE_BF16, d and
- * f multiples of 16. */
+ * fp8's weights -- the shared expert too when fp8 holds its weights (an FP8 dense SwiGLU on
+ * x_q); routing, the shared gate and the combine are those of moe_layer_fwd.  saved is filled
+ * as by moe_layer_fwd except saved.x_perm (unused, may be NULL).  Workspace MOE_WS_LAYER_FWD.
+ * cfg->dtype MOE_DTYPE_BF16; d, f (and f_s for an FP8 shared expert) multiples of 16. */
 int moe_layer_fwd_fp8(const moe_cfg* cfg, const void* x, const void* W_r, const float* b_r,
                       const moe_fp8_experts* fp8, const void* Ws1, const void* Ws2,
                       const void* w_sg, void* y, const moe_saved* saved, void* ws, size_t ws_bytes,
@@ -371,8 +382,9 @@ int moe_layer_fwd_fp8(const moe_cfg* cfg, const void* x, const void* W_r, const 
 
 /* moe_layer_bwd after moe_layer_fwd_fp8: the routed experts' backward runs as
  * moe_grouped_swiglu_bwd_fp8 does (dy_perm and [da | du] quantised, both data gradients and
- * both weight gradients on E4M3 operands); the rest is that of moe_layer_bwd.  Outputs as
- * moe_layer_bwd; fp8.scales[4..7] are written.  Workspace MOE_WS_LAYER_BWD_FP8. */
+ * both weight gradients on E4M3 operands), the shared expert's likewise when it is in FP8;
+ * the rest is that of moe_layer_bwd.  Outputs as moe_layer_bwd.  Workspace
+ * MOE_WS_LAYER_BWD_FP8. */
 int moe_layer_bwd_fp8(const moe_cfg* cfg, const void* dy, const void* x, const void* W_r,
                       const moe_fp8_experts* fp8, const void* Ws1, const void* Ws2,
                       const void* w_sg, const moe_saved* saved, void* dx, float* dW_r, float* dW1,

@@ -39,7 +39,8 @@ class MoeSaved(ctypes.Structure):
 
 class MoeFp8Experts(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("W1_q", "W1_scale", "W2_q", "W2_scale", "x_perm_q", "h_q", "scales")]
+                ("W1_q", "W1_scale", "W2_q", "W2_scale", "x_perm_q", "h_q", "scales",
+                 "Ws1_q", "Ws1_scale", "Ws2_q", "Ws2_scale", "x_q", "s_h_q")]
 
 
 _VP = ctypes.c_void_p
@@ -309,12 +310,14 @@ def moe_layer_bwd(cfg, dy, x, W_r, W1, W2, Ws1, Ws2, w_sg, saved, dx, dW_r, dW1,
                                _stream(stream)), "moe_layer_bwd")
 
 
-def alloc_fp8_experts(cfg, W1, W2, device="cuda", stream=None):
-    """FP8 state of the routed experts (torch tensors): W1 and W2 quantised once to E4M3 with
-    one scale per expert (FP8 parameters), and the buffers the FP8 layer calls write."""
+def alloc_fp8_experts(cfg, W1, W2, device="cuda", stream=None, Ws1=None, Ws2=None):
+    """FP8 state of the experts (torch tensors): W1 and W2 (and the shared expert's Ws1, Ws2 when
+    given) quantised once to E4M3 with one scale per expert (FP8 parameters), and the buffers
+    the FP8 layer calls write."""
     import torch
-    E, d, f = cfg.E, cfg.d, cfg.f
-    N = max(cfg.T, 1) * cfg.k
+    E, d, f, fs = cfg.E, cfg.d, cfg.f, cfg.f_shared
+    T = max(cfg.T, 1)
+    N = T * cfg.k
     u8, f32 = torch.uint8, torch.float32
     q = dict(W1_q=torch.empty(E, 2 * f, d, dtype=u8, device=device),
              W1_scale=torch.empty(E, dtype=f32, device=device),
@@ -322,10 +325,19 @@ def alloc_fp8_experts(cfg, W1, W2, device="cuda", stream=None):
              W2_scale=torch.empty(E, dtype=f32, device=device),
              x_perm_q=torch.empty(N, d, dtype=u8, device=device),
              h_q=torch.empty(N, f, dtype=u8, device=device),
-             scales=torch.zeros(8, dtype=f32, device=device))
-    amax = torch.empty(E, dtype=f32, device=device)
+             scales=torch.zeros(16, dtype=f32, device=device))
+    amax = torch.empty(max(E, 4), dtype=f32, device=device)
     moe_quantize_e4m3(W1, E, q["W1_q"], q["W1_scale"], amax, stream)
     moe_quantize_e4m3(W2, E, q["W2_q"], q["W2_scale"], amax, stream)
+    if fs and Ws1 is not None:
+        q.update(Ws1_q=torch.empty(2 * fs, d, dtype=u8, device=device),
+                 Ws1_scale=torch.empty(4, dtype=f32, device=device),
+                 Ws2_q=torch.empty(d, fs, dtype=u8, device=device),
+                 Ws2_scale=torch.empty(4, dtype=f32, device=device),
+                 x_q=torch.empty(T, d, dtype=u8, device=device),
+                 s_h_q=torch.empty(T, fs, dtype=u8, device=device))
+        moe_quantize_e4m3(Ws1, 1, q["Ws1_q"], q["Ws1_scale"], amax, stream)
+        moe_quantize_e4m3(Ws2, 1, q["Ws2_q"], q["Ws2_scale"], amax, stream)
     return q
 
 

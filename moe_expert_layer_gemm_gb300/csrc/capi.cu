@@ -484,16 +484,19 @@ static int ffn_bwd_impl(const moe_cfg* c, int G, const int32_t* offsets, int64_t
 }
 
 // The routed experts' forward on E4M3 operands (fc1 + SwiGLU with h's amax, h quantised, fc2).
-static int ffn_fwd_fp8_impl(const moe_cfg* c, const int32_t* offsets, const uint8_t* x_perm_q,
+// G groups of rows (offsets NULL: one group of all rows -- the shared expert), ffn width f.
+static int ffn_fwd_fp8_impl(const moe_cfg* c, int G, const int32_t* offsets, int64_t rows, int f,
+                            const uint8_t* x_perm_q,
                             const float* x_scale, const uint8_t* W1_q, const float* W1_scale,
                             const uint8_t* W2_q, const float* W2_scale, void* h, void* act,
                             uint8_t* h_q, float* h_scale, float* h_amax, void* y_perm,
                             cudaStream_t st) {
-  const int64_t N = Nrows(c);
-  const int d = c->d, f = c->f, E = c->E;
+  const int64_t N = rows;
+  const int d = c->d, E = G;
+  const bool shared = offsets == nullptr;
   // fc1 + SwiGLU on E4M3 operands -> h, [a | u] (bf16)
   GemmDesc g1 = desc0();
-  g1.name = "gemm_fc1_swiglu_fp8";
+  g1.name = shared ? "gemm_shared_fc1_swiglu_fp8" : "gemm_fc1_swiglu_fp8";
   g1.sched = RAGGED_M;
   g1.epi = EPI_SWIGLU_FWD;
   g1.G = E;
@@ -521,7 +524,7 @@ static int ffn_fwd_fp8_impl(const moe_cfg* c, const int32_t* offsets, const uint
   MOE_TRY(launch_quant_e4m3_given_amax(h, N * f, 1, h_q, h_scale, h_amax, st));
   // fc2 on E4M3 operands -> y_perm (bf16)
   GemmDesc g2 = desc0();
-  g2.name = "gemm_fc2_fp8";
+  g2.name = shared ? "gemm_shared_fc2_fp8" : "gemm_fc2_fp8";
   g2.sched = RAGGED_M;
   g2.epi = EPI_STORE;
   g2.G = E;
@@ -543,21 +546,23 @@ static int ffn_fwd_fp8_impl(const moe_cfg* c, const int32_t* offsets, const uint
 // The routed experts' backward on E4M3 operands: dy quantised, fc2 dgrad + SwiGLU backward
 // (with [da | du]'s amax), [da | du] quantised, fc2 wgrad, fc1 dgrad, fc1 wgrad.  dx_perm may
 // alias dy_perm (dy_perm is read only by the first quantisation).
-static int ffn_bwd_fp8_impl(const moe_cfg* c, const int32_t* offsets, const uint8_t* x_perm_q,
+static int ffn_bwd_fp8_impl(const moe_cfg* c, int G, const int32_t* offsets, int64_t rows, int f,
+                            const uint8_t* x_perm_q,
                             const float* x_scale, const uint8_t* W1_q, const float* W1_scale,
                             const uint8_t* W2_q, const float* W2_scale, const void* act,
                             const uint8_t* h_q, const float* h_scale, const void* dy_perm,
                             uint8_t* dy_q, float* dy_scale, float* dy_amax, void* dH1,
                             uint8_t* dH1_q, float* dH1_scale, float* dH1_amax, void* dx_perm,
                             float* dW1, float* dW2, int* sched, cudaStream_t st) {
-  const int64_t N = Nrows(c);
-  const int d = c->d, f = c->f, E = c->E;
+  const int64_t N = rows;
+  const int d = c->d, E = G;
+  const bool shared = offsets == nullptr;
   // dy_perm -> E4M3 (one tensor)
   MOE_TRY(launch_quantize_e4m3(dy_perm, N * d, 1, dy_q, dy_scale, dy_amax, st));
   // dh = dy . W2_e on E4M3 operands (W2_q read MN-major: no transposed copy), SwiGLU backward
   // -> dH1 = [da | du] (bf16) with its amax
   GemmDesc a = desc0();
-  a.name = "gemm_fc2_dgrad_fp8";
+  a.name = shared ? "gemm_shared_fc2_dgrad_fp8" : "gemm_fc2_dgrad_fp8";
   a.sched = RAGGED_M;
   a.epi = EPI_SWIGLU_BWD;
   a.G = E;
@@ -584,7 +589,7 @@ static int ffn_bwd_fp8_impl(const moe_cfg* c, const int32_t* offsets, const uint
   MOE_TRY(launch_quant_e4m3_given_amax(dH1, N * 2 * f, 1, dH1_q, dH1_scale, dH1_amax, st));
   // dW2_e = dy_e^T . h_e (both MN-major over the expert's rows)
   GemmDesc b = desc0();
-  b.name = "gemm_fc2_wgrad_fp8";
+  b.name = shared ? "gemm_shared_fc2_wgrad_fp8" : "gemm_fc2_wgrad_fp8";
   b.sched = RAGGED_K;
   b.epi = EPI_F32;
   b.G = E;
@@ -605,7 +610,7 @@ static int ffn_bwd_fp8_impl(const moe_cfg* c, const int32_t* offsets, const uint
   MOE_TRY(gemm_tc(b, st));
   // dx_perm = dH1 . W1_e
   GemmDesc e = desc0();
-  e.name = "gemm_fc1_dgrad_fp8";
+  e.name = shared ? "gemm_shared_fc1_dgrad_fp8" : "gemm_fc1_dgrad_fp8";
   e.sched = RAGGED_M;
   e.epi = EPI_STORE;
   e.G = E;
@@ -624,7 +629,7 @@ static int ffn_bwd_fp8_impl(const moe_cfg* c, const int32_t* offsets, const uint
   MOE_TRY(gemm_tc(e, st));
   // dW1_e = dH1_e^T . x_perm_e
   GemmDesc w = desc0();
-  w.name = "gemm_fc1_wgrad_fp8";
+  w.name = shared ? "gemm_shared_fc1_wgrad_fp8" : "gemm_fc1_wgrad_fp8";
   w.sched = RAGGED_K;
   w.epi = EPI_F32;
   w.G = E;
@@ -745,6 +750,10 @@ size_t moe_workspace_bytes(const moe_cfg* c, int which) {
       carve_bwd(cv, c);
       cv.take(static_cast<size_t>(Nrows(c)) * c->d);
       cv.take(static_cast<size_t>(Nrows(c)) * 2 * c->f);
+      if (c->f_shared > 0) {   // room for an FP8 shared expert's gradient codes
+        cv.take(static_cast<size_t>(c->T) * c->d);
+        cv.take(static_cast<size_t>(c->T) * 2 * c->f_shared);
+      }
       break;
     default:
       return 0;
@@ -919,8 +928,8 @@ int moe_permute_quantize_e4m3(const moe_cfg* c, const void* x, const int32_t* sl
   MOE_TRY(check_ptr(x_scale, "x_scale", true));
   MOE_TRY(check_ptr(x_amax, "x_amax", true));
   if (c->T == 0) return MOE_OK;
-  return launch_permute_quant_e4m3(x, slot_of_pair, x_perm_q, x_scale, x_amax, c->T, c->d, c->k,
-                                   S(stream));
+  return launch_permute_quant_e4m3(x, slot_of_pair, x_perm_q, nullptr, x_scale, x_amax, c->T, c->d,
+                                   c->k, S(stream));
 }
 
 int moe_grouped_swiglu_fwd_fp8(const moe_cfg* c, const uint8_t* x_perm_q, const float* x_scale,
@@ -949,7 +958,7 @@ int moe_grouped_swiglu_fwd_fp8(const moe_cfg* c, const uint8_t* x_perm_q, const 
   cudaStream_t st = S(stream);
   const int64_t N = Nrows(c);
   if (N == 0) return MOE_OK;
-  return ffn_fwd_fp8_impl(c, offsets, x_perm_q, x_scale, W1_q, W1_scale, W2_q, W2_scale, h, act,
+  return ffn_fwd_fp8_impl(c, c->E, offsets, Nrows(c), c->f, x_perm_q, x_scale, W1_q, W1_scale, W2_q, W2_scale, h, act,
                           h_q, h_scale, h_amax, y_perm, st);
 }
 
@@ -985,7 +994,7 @@ int moe_grouped_swiglu_bwd_fp8(const moe_cfg* c, const uint8_t* x_perm_q, const 
   }
   Carve cv(ws);
   int* sched = static_cast<int*>(cv.take(2 * 4 * sizeof(int)));
-  return ffn_bwd_fp8_impl(c, offsets, x_perm_q, x_scale, W1_q, W1_scale, W2_q, W2_scale, act, h_q,
+  return ffn_bwd_fp8_impl(c, c->E, offsets, Nrows(c), c->f, x_perm_q, x_scale, W1_q, W1_scale, W2_q, W2_scale, act, h_q,
                           h_scale, dy_perm, dy_q, dy_scale, dy_amax, dH1, dH1_q, dH1_scale,
                           dH1_amax, dx_perm, dW1, dW2, sched, st);
 }
@@ -1065,7 +1074,19 @@ static int check_fp8_experts(const moe_cfg* c, const moe_fp8_experts* q) {
   MOE_TRY(check_ptr(q->x_perm_q, "fp8.x_perm_q", true));
   MOE_TRY(check_ptr(q->h_q, "fp8.h_q", true));
   MOE_TRY(check_ptr(q->scales, "fp8.scales", true));
+  const bool sq = c->f_shared > 0 && q->Ws1_q;   // the shared expert in FP8 too
+  if (sq && c->f_shared % 16)
+    return fail(MOE_ERR_UNSUPPORTED, "an FP8 shared expert needs f_shared a multiple of 16");
+  MOE_TRY(check_ptr(q->Ws1_scale, "fp8.Ws1_scale", sq));
+  MOE_TRY(check_ptr(q->Ws2_q, "fp8.Ws2_q", sq));
+  MOE_TRY(check_ptr(q->Ws2_scale, "fp8.Ws2_scale", sq));
+  MOE_TRY(check_ptr(q->x_q, "fp8.x_q", sq));
+  MOE_TRY(check_ptr(q->s_h_q, "fp8.s_h_q", sq));
   return MOE_OK;
+}
+
+static bool shared_fp8(const moe_cfg* c, const moe_fp8_experts* q) {
+  return q && c->f_shared > 0 && q->Ws1_q;
 }
 
 static int check_saved(const moe_cfg* c, const moe_saved* s, bool fp8 = false) {
@@ -1103,8 +1124,9 @@ static int layer_fwd_impl(const moe_cfg* c, const void* x, const void* W_r, cons
   MOE_TRY(check_ptr(W2, "W2", !q));
   if (q) MOE_TRY(check_fp8_experts(c, q));
   const bool sh = c->f_shared > 0, gt = c->shared_gate != 0;
-  MOE_TRY(check_ptr(Ws1, "Ws1", sh));
-  MOE_TRY(check_ptr(Ws2, "Ws2", sh));
+  const bool sq = shared_fp8(c, q);
+  MOE_TRY(check_ptr(Ws1, "Ws1", sh && !sq));
+  MOE_TRY(check_ptr(Ws2, "Ws2", sh && !sq));
   MOE_TRY(check_ptr(w_sg, "w_sg", gt));
   MOE_TRY(check_ptr(y, "y", true));
   MOE_TRY(check_saved(c, s, q != nullptr));
@@ -1125,11 +1147,20 @@ static int layer_fwd_impl(const moe_cfg* c, const void* x, const void* W_r, cons
   std::unique_lock<std::mutex> side_lk(g_side_mu, std::defer_lock);
   auto shared_fwd = [&](cudaStream_t ss) -> int {
     if (gt) MOE_TRY(launch_shared_gate(c->dtype, x, w_sg, s->s_coef, c->T, c->d, ss));
+    if (sq)
+      return ffn_fwd_fp8_impl(c, 1, nullptr, c->T, c->f_shared, q->x_q, q->scales + 0, q->Ws1_q,
+                              q->Ws1_scale, q->Ws2_q, q->Ws2_scale, s->s_h, s->s_act, q->s_h_q,
+                              q->scales + 8, q->scales + 9, s->s_out, ss);
     return ffn_fwd_impl(c, 1, nullptr, c->T, c->f_shared, x, Ws1, Ws2, s->s_h, s->s_act,
                         s->s_out, ss);
   };
   MOE_TRY(route_impl(c, x, W_r, b_r, nullptr, s->logits, s->idx, s->gate, s->counts, s->offsets,
                      s->slot_of_pair, s->token_of_slot, w, st));
+  // FP8: x permuted and quantised in one pass ("Megatron-Bridge 深度剖析", §FP8 训练), also in
+  // token order for an FP8 shared expert -- before the side stream forks, which reads those codes
+  if (q)
+    MOE_TRY(launch_permute_quant_e4m3(x, s->slot_of_pair, q->x_perm_q, sq ? q->x_q : nullptr,
+                                      q->scales + 0, q->scales + 1, c->T, c->d, c->k, st));
   if (side) {
     side_lk.lock();
     if (cudaEventRecord(side->fork, st) != cudaSuccess ||
@@ -1143,10 +1174,8 @@ static int layer_fwd_impl(const moe_cfg* c, const void* x, const void* W_r, cons
     MOE_TRY(launch_aux_loss(s->logits, s->counts, c->T, c->E, c->k, c->score_fn, c->aux_coeff,
                             w.aux, s->aux_loss, st));
   if (q) {
-    // "Megatron-Bridge 深度剖析", §FP8 训练: x permuted and quantised in one pass, E4M3 experts
-    MOE_TRY(launch_permute_quant_e4m3(x, s->slot_of_pair, q->x_perm_q, q->scales + 0,
-                                      q->scales + 1, c->T, c->d, c->k, st));
-    MOE_TRY(ffn_fwd_fp8_impl(c, s->offsets, q->x_perm_q, q->scales + 0, q->W1_q, q->W1_scale,
+    // E4M3 experts on the codes made above
+    MOE_TRY(ffn_fwd_fp8_impl(c, c->E, s->offsets, Nrows(c), c->f, q->x_perm_q, q->scales + 0, q->W1_q, q->W1_scale,
                              q->W2_q, q->W2_scale, s->h, s->act, q->h_q, q->scales + 2,
                              q->scales + 3, s->y_perm, st));
   } else if (permute_fused(c)) {
@@ -1183,8 +1212,9 @@ static int layer_bwd_impl(const moe_cfg* c, const void* dy, const void* x, const
   MOE_TRY(check_ptr(W1, "W1", !q));
   MOE_TRY(check_ptr(W2, "W2", !q));
   if (q) MOE_TRY(check_fp8_experts(c, q));
-  MOE_TRY(check_ptr(Ws1, "Ws1", sh));
-  MOE_TRY(check_ptr(Ws2, "Ws2", sh));
+  const bool sq = shared_fp8(c, q);
+  MOE_TRY(check_ptr(Ws1, "Ws1", sh && !sq));
+  MOE_TRY(check_ptr(Ws2, "Ws2", sh && !sq));
   MOE_TRY(check_ptr(w_sg, "w_sg", gt));
   MOE_TRY(check_saved(c, s, q != nullptr));
   MOE_TRY(check_ptr(dx, "dx", true));
@@ -1212,6 +1242,9 @@ static int layer_bwd_impl(const moe_cfg* c, const void* dy, const void* x, const
   uint8_t* dy_q = q ? static_cast<uint8_t*>(cv.take(static_cast<size_t>(Nrows(c)) * d)) : nullptr;
   uint8_t* dH1_q =
       q ? static_cast<uint8_t*>(cv.take(static_cast<size_t>(Nrows(c)) * 2 * c->f)) : nullptr;
+  uint8_t* ds_q = sq ? static_cast<uint8_t*>(cv.take(static_cast<size_t>(T) * d)) : nullptr;
+  uint8_t* s_dH1_q =
+      sq ? static_cast<uint8_t*>(cv.take(static_cast<size_t>(T) * 2 * c->f_shared)) : nullptr;
   // 1. combine backward
   MOE_TRY(launch_combine_bwd(c->dtype, dy, s->y_perm, s->gate, s->slot_of_pair,
                              sh ? s->s_out : nullptr, gt ? s->s_coef : nullptr, w.dy_perm, w.dgate,
@@ -1222,7 +1255,13 @@ static int layer_bwd_impl(const moe_cfg* c, const void* dy, const void* x, const
   std::unique_lock<std::mutex> side_lk(g_side_mu, std::defer_lock);
   auto side_work = [&](cudaStream_t ss) -> int {
     // shared expert (one group of all T tokens)
-    if (sh)
+    if (sq)
+      MOE_TRY(ffn_bwd_fp8_impl(c, 1, nullptr, T, c->f_shared, q->x_q, q->scales + 0, q->Ws1_q,
+                               q->Ws1_scale, q->Ws2_q, q->Ws2_scale, s->s_act, q->s_h_q,
+                               q->scales + 8, w.dshared, ds_q, q->scales + 10, q->scales + 11,
+                               w.s_dH1, s_dH1_q, q->scales + 12, q->scales + 13, w.dx_shared,
+                               dWs1, dWs2, w.sched + 8, ss));
+    else if (sh)
       MOE_TRY(ffn_bwd_impl(c, 1, nullptr, T, c->f_shared, x, Ws1, Ws2, s->s_act, s->s_h,
                            w.dshared, w.s_dH1, w.dx_shared, dWs1, dWs2, w.sched + 8, ss));
     // router: dlogits (+ shared gate dz in column E), with the balancing loss's gradient
@@ -1280,7 +1319,7 @@ static int layer_bwd_impl(const moe_cfg* c, const void* dy, const void* x, const
   }
   // routed experts (dx_perm overwrites dy_perm once it is no longer read)
   if (q)
-    MOE_TRY(ffn_bwd_fp8_impl(c, s->offsets, q->x_perm_q, q->scales + 0, q->W1_q, q->W1_scale,
+    MOE_TRY(ffn_bwd_fp8_impl(c, c->E, s->offsets, Nrows(c), c->f, q->x_perm_q, q->scales + 0, q->W1_q, q->W1_scale,
                              q->W2_q, q->W2_scale, s->act, q->h_q, q->scales + 2, w.dy_perm, dy_q,
                              q->scales + 4, q->scales + 5, w.dH1, dH1_q, q->scales + 6,
                              q->scales + 7, w.dy_perm, dW1, dW2, w.sched, st));

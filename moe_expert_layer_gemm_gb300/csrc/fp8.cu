@@ -73,13 +73,15 @@ __global__ void __launch_bounds__(256) quant_kernel(const bf16* __restrict__ x, 
   }
 }
 
-// Permute + quantise: x_perm_q[slot(t, j)] = E4M3(x[t] * inv) for every pair (t, j); x is
-// read once per token (one warp per token), the codes written k times.  Same codes as
-// quantising the permuted matrix: the pairs' rows are exact copies of x's rows.
+// Permute + quantise: x_perm_q[slot(t, j)] = E4M3(x[t] * inv) for every pair (t, j), and
+// x_q[t] the same codes in token order if x_q is given (the shared expert's input); x is read
+// once per token (one warp per token).  Same codes as quantising the permuted matrix: the pairs'
+// rows are exact copies of x's rows.
 __global__ void __launch_bounds__(256) permute_quant_kernel(const bf16* __restrict__ x,
                                                             const int32_t* __restrict__ sop,
                                                             const unsigned int* __restrict__ amax_bits,
                                                             uint8_t* __restrict__ xq,
+                                                            uint8_t* __restrict__ xq_tok,
                                                             float* __restrict__ scale, int Tn,
                                                             int d, int k, int* err) {
   const float amax = __uint_as_float(amax_bits[0]);
@@ -118,6 +120,8 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(const bf16* __restri
         if (slot[j] >= 0)
           *reinterpret_cast<uint2*>(xq + static_cast<int64_t>(slot[j]) * d + c) = make_uint2(w[0], w[1]);
       }
+      if (xq_tok)
+        *reinterpret_cast<uint2*>(xq_tok + static_cast<int64_t>(t) * d + c) = make_uint2(w[0], w[1]);
     }
   }
 }
@@ -135,8 +139,8 @@ int launch_quant_e4m3_given_amax(const void* x, int64_t per_group, int groups, u
                 per_group, reinterpret_cast<const unsigned int*>(amax), q, scale);
 }
 
-int launch_permute_quant_e4m3(const void* x, const int32_t* sop, uint8_t* xq, float* scale,
-                              float* amax, int T, int d, int k, cudaStream_t st) {
+int launch_permute_quant_e4m3(const void* x, const int32_t* sop, uint8_t* xq, uint8_t* xq_tok,
+                              float* scale, float* amax, int T, int d, int k, cudaStream_t st) {
   if (cudaMemsetAsync(amax, 0, sizeof(float), st) != cudaSuccess) {
     set_error("clearing the amax buffer failed");
     return MOE_ERR_CUDA;
@@ -151,7 +155,7 @@ int launch_permute_quant_e4m3(const void* x, const int32_t* sop, uint8_t* xq, fl
   if (rb > num_sms() * 8) rb = num_sms() * 8;
   return launch("fp8_permute_quantize", permute_quant_kernel, dim3(rb), dim3(256), 0, st,
                 static_cast<const bf16*>(x), sop, reinterpret_cast<const unsigned int*>(amax), xq,
-                scale, T, d, k, device_error_word());
+                xq_tok, scale, T, d, k, device_error_word());
 }
 
 int launch_quantize_e4m3(const void* x, int64_t per_group, int groups, uint8_t* q, float* scale,

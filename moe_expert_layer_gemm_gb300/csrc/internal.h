@@ -183,9 +183,10 @@ int launch_quantize_e4m3(const void* x, int64_t per_group, int groups, uint8_t* 
 // The cast alone, with amax already computed (e.g. by the producing GEMM's epilogue).
 int launch_quant_e4m3_given_amax(const void* x, int64_t per_group, int groups, uint8_t* q,
                                  float* scale, const float* amax, cudaStream_t st);
-// amax of x [T,d] and the permuted E4M3 rows x_perm_q[slot_of_pair[t,j]] = E4M3(x[t] * inv).
-int launch_permute_quant_e4m3(const void* x, const int32_t* sop, uint8_t* xq, float* scale,
-                              float* amax, int T, int d, int k, cudaStream_t st);
+// amax of x [T,d] and the permuted E4M3 rows x_perm_q[slot_of_pair[t,j]] = E4M3(x[t] * inv)
+// (and x_q[t], the same codes in token order, if x_q is not NULL).
+int launch_permute_quant_e4m3(const void* x, const int32_t* sop, uint8_t* xq, uint8_t* x_q,
+                              float* scale, float* amax, int T, int d, int k, cudaStream_t st);
 
 int gemm_tc(const GemmDesc& g, cudaStream_t st);     // bf16 tcgen05 path (gemm_tc.cu)
 int gemm_simt(const GemmDesc& g, cudaStream_t st);   // fp32 CUDA-core path (gemm_simt.cu)

@@ -5,8 +5,10 @@ The FP8 expert stages are checked against the oracle in test_gpu_fp8.py; here th
   * every FP8 buffer and output bit-identical to the stage calls composed by hand on the
     layer's own routing (permute + quantise, FP8 experts, combine; combine backward, FP8 expert
     backward);
-  * router and shared-expert gradients bit-identical to the bf16 layer backward run on the same
-    saved forward state (they do not depend on the routed experts' backward);
+  * with the shared expert in FP8: its outputs, codes and weight gradients bit-identical to the
+    FP8 stage calls on one group of all tokens (x's codes in token order);
+  * router gradients (and a bf16 shared expert's) bit-identical to the bf16 layer backward run on
+    the same saved forward state (they do not depend on the routed experts' backward);
   * y and dx within the E4M3 rounding bound of the unquantised fp64 oracle layer.
 """
 import numpy as np
@@ -30,11 +32,12 @@ CASES = [
 ]
 
 
-def run_fp8_layer(lc, inp, cfg):
+def run_fp8_layer(lc, inp, cfg, sfp8=False):
     dev = inp["x"].device
     saved = moe.alloc_saved(cfg, dev)
     saved["x_perm"] = None                              # the FP8 layer does not use it
-    q = moe.alloc_fp8_experts(cfg, inp["W1"], inp["W2"], dev)
+    q = moe.alloc_fp8_experts(cfg, inp["W1"], inp["W2"], dev,
+                              Ws1=inp["Ws1"] if sfp8 else None, Ws2=inp["Ws2"] if sfp8 else None)
     y = torch.empty_like(inp["x"])
     moe.moe_layer_fwd_fp8(cfg, inp["x"], inp["W_r"], inp["b_r"], q, inp["Ws1"], inp["Ws2"],
                           inp["w_sg"], y, saved, moe.workspace(cfg, moe.WS_LAYER_FWD, dev))
@@ -54,12 +57,17 @@ def run_fp8_layer(lc, inp, cfg):
     return y, saved, q, g
 
 
-@pytest.mark.parametrize("lc", CASES, ids=lambda c: c.name.split()[0])
-def test_fp8_layer(lc):
+PARAMS = [(lc, False) for lc in CASES] + [(lc, True) for lc in CASES if lc.f_shared]
+
+
+@pytest.mark.parametrize("lc,sfp8", PARAMS,
+                         ids=lambda v: v.name.split()[0] if hasattr(v, "name") else
+                         ("shared-fp8" if v else "shared-bf16"))
+def test_fp8_layer(lc, sfp8):
     cpu_inp, _ = clean_inputs(lc)
     inp = inputs_to(cpu_inp, "cuda")
     cfg = moe.cfg_from(lc)
-    y, saved, q, g = run_fp8_layer(lc, inp, cfg)
+    y, saved, q, g = run_fp8_layer(lc, inp, cfg, sfp8)
     dev = "cuda"
     N, d, f, E = lc.N, lc.d, lc.f, lc.E
     bf, u8 = torch.bfloat16, torch.uint8
@@ -109,7 +117,7 @@ def test_fp8_layer(lc):
     torch.cuda.synchronize()
     moe.check_device_error()
     assert torch.equal(g["dW1"], dW1) and torch.equal(g["dW2"], dW2)
-    assert torch.equal(q["scales"][4:], torch.stack([sc[0][0], sc[1][0], sc[2][0], sc[3][0]]))
+    assert torch.equal(q["scales"][4:8], torch.stack([sc[0][0], sc[1][0], sc[2][0], sc[3][0]]))
 
     # router and shared-expert gradients: the bf16 backward on the same saved forward state
     saved16 = dict(saved)
@@ -122,9 +130,40 @@ def test_fp8_layer(lc):
                       moe.workspace(cfg, moe.WS_LAYER_BWD))
     torch.cuda.synchronize()
     moe.check_device_error()
-    for n in ("dW_r", "dWs1", "dWs2", "dw_sg"):
+    for n in ("dW_r", "dw_sg") + (() if sfp8 else ("dWs1", "dWs2")):
         if g[n] is not None:
             assert torch.equal(g[n], g16[n]), n
+
+    if sfp8:
+        # the shared expert: FP8 stage calls on one group of all T tokens
+        T, fs = lc.T, lc.f_shared
+        tos = saved["token_of_slot"][:N].long()
+        assert torch.equal(q["x_q"][tos], q["x_perm_q"])         # x's codes in token order
+        cfg1 = moe.make_cfg(T, d, 1, 1, fs)
+        off1 = torch.tensor([0, T], dtype=torch.int32, device=dev)
+        x_scale = q["scales"][0:1].clone()
+        sh_, sa_ = torch.empty(T, fs, dtype=bf, device=dev), torch.empty(T, 2 * fs, dtype=bf, device=dev)
+        shq = torch.empty(T, fs, dtype=u8, device=dev)
+        shs, sha = torch.empty(4, device=dev), torch.empty(4, device=dev)
+        so = torch.empty(T, d, dtype=bf, device=dev)
+        moe.moe_grouped_swiglu_fwd_fp8(cfg1, q["x_q"], x_scale, off1, q["Ws1_q"], q["Ws1_scale"],
+                                       q["Ws2_q"], q["Ws2_scale"], sh_, sa_, shq, shs, sha, so)
+        sdyq, sdH1q = torch.empty(T, d, dtype=u8, device=dev), torch.empty(T, 2 * fs, dtype=u8, device=dev)
+        sdH1, sdx = torch.empty(T, 2 * fs, dtype=bf, device=dev), torch.empty(T, d, dtype=bf, device=dev)
+        ssc = [torch.empty(4, device=dev) for _ in range(4)]
+        dWs1, dWs2 = torch.empty_like(g["dWs1"]), torch.empty_like(g["dWs2"])
+        moe.moe_grouped_swiglu_bwd_fp8(cfg1, q["x_q"], x_scale, off1, q["Ws1_q"], q["Ws1_scale"],
+                                       q["Ws2_q"], q["Ws2_scale"], sa_, shq, shs, dsh, sdyq,
+                                       ssc[0], ssc[1], sdH1, sdH1q, ssc[2], ssc[3], sdx, dWs1, dWs2,
+                                       moe.workspace(cfg1, moe.WS_FFN_BWD_FP8))
+        torch.cuda.synchronize()
+        moe.check_device_error()
+        for a, b, n in ((saved["s_h"], sh_, "s_h"), (saved["s_act"], sa_, "s_act"),
+                        (saved["s_out"], so, "s_out"), (q["s_h_q"], shq, "s_h_q"),
+                        (g["dWs1"], dWs1, "dWs1"), (g["dWs2"], dWs2, "dWs2")):
+            assert torch.equal(a, b), n
+        assert torch.equal(q["scales"][8:14], torch.stack(
+            [shs[0], sha[0], ssc[0][0], ssc[1][0], ssc[2][0], ssc[3][0]]))
 
     # against the unquantised fp64 layer: E4M3 rounding (3 mantissa bits) of x, h, the
     # weights, dy_perm and [da | du]
@@ -132,6 +171,9 @@ def test_fp8_layer(lc):
     e = {"y": rel_err(np64(y), ref["fwd"]["y"]), "dx": rel_err(np64(g["dx"]), ref["bwd"]["dx"]),
          "dW1": rel_err(np64(g["dW1"]), ref["bwd"]["dW1"]),
          "dW2": rel_err(np64(g["dW2"]), ref["bwd"]["dW2"])}
+    if sfp8:
+        e.update(dWs1=rel_err(np64(g["dWs1"]), ref["bwd"]["dWs1"]),
+                 dWs2=rel_err(np64(g["dWs2"]), ref["bwd"]["dWs2"]))
     assert max(e.values()) < 0.15, e
     print(lc.name, {k: round(v, 4) for k, v in e.items()})
 
@@ -141,7 +183,7 @@ def test_fp8_layer_zero_tokens():
     cfg = moe.cfg_from(lc)
     # buffers of one row, a layer of zero tokens: nothing may be read or written per token
     inp = inputs_to(moe_inputs.make_layer_inputs(lc.replace(T=1), seed=1), "cuda")
-    y, saved, q, g = run_fp8_layer(lc, inp, cfg)
+    y, saved, q, g = run_fp8_layer(lc, inp, cfg, sfp8=True)
     assert int(saved["offsets"].abs().sum()) == 0
     for n in ("dW_r", "dW1", "dW2", "dWs1", "dWs2", "dw_sg"):
         assert not g[n].any(), n
