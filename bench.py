@@ -43,10 +43,13 @@ def load_peaks():
 
 # ----------------------------------------------------------------------------- work per kernel
 
-def kernel_work(lc):
+def kernel_work(lc, trace=None, steps=1):
     """Algorithmic work of one launch of each kernel kind: ('tensor', FLOPs) or ('hbm', bytes).
     FLOPs count 2 per multiply-add of the products the method needs (no padding, no dense
-    all-expert work); bytes count each operand the kernel must read or write once."""
+    all-expert work); bytes count each operand the kernel must read or write once.  The FP8
+    layer's E4M3 products (names ending in _fp8) do the same FLOPs as their bf16 twins; its
+    quantisation kernels serve several tensors a step, so their bytes per launch are the step's
+    total times `steps` over the launches `trace` saw in that many steps."""
     T, d, E, k, f, fs = lc.T, lc.d, lc.E, lc.k, lc.f, lc.f_shared
     N = T * k
     b = 2 if lc.dtype == "bf16" else 4
@@ -82,7 +85,39 @@ def kernel_work(lc):
             "gemm_shared_fc1_dgrad": ("tensor", 4.0 * T * d * fs),
             "gemm_shared_fc1_wgrad": ("tensor", 4.0 * T * d * fs),
         })
+    for n in [n for n in w if n.startswith("gemm_") and "router" not in n]:
+        w[n + "_fp8"] = w[n]
+    # E4M3 quantisation (bf16 in, one byte out): amax passes read, quantise passes read + write
+    amax_bytes = T * d * 2 + (N * d * 2 if lc.backward else 0) + \
+        (T * d * 2 if fs and lc.backward else 0)
+    quant_bytes = N * f * 3 + (T * fs * 3 if fs else 0)
+    if lc.backward:
+        quant_bytes += N * d * 3 + N * 2 * f * 3 + ((T * d * 3 + T * 2 * fs * 3) if fs else 0)
+    per = lambda name, total: total * steps / max(1, (trace or {}).get(name, (steps, 0))[0])  # noqa: E731
+    w["fp8_amax"] = ("hbm", per("fp8_amax", amax_bytes))
+    w["fp8_quantize"] = ("hbm", per("fp8_quantize", quant_bytes))
+    w["fp8_permute_quantize"] = ("hbm", T * d * 2 + N * d + (T * d if fs else 0) + N * 4)
     return w
+
+
+def gemm_bytes(lc):
+    """Algorithmic DRAM bytes of one launch of each expert GEMM: every operand read once, every
+    result written once (bf16 activations out, fp32 weight gradients; E4M3 operands of the _fp8
+    kinds one byte each).  A GEMM whose bytes at the measured copy bandwidth take longer than its
+    FLOPs at the tensor peak is HBM-bound, and its roofline is the bandwidth."""
+    T, d, E, k, f, fs = lc.T, lc.d, lc.E, lc.k, lc.f, lc.f_shared
+    out = {}
+    for pre, rows, G, ff in (("gemm_", T * k, E, f), ("gemm_shared_", T, 1, fs)):
+        if ff == 0:
+            continue
+        for sfx, b in (("", 2), ("_fp8", 1)):
+            out[pre + "fc1_swiglu" + sfx] = rows * d * b + G * 2 * ff * d * b + rows * 3 * ff * 2
+            out[pre + "fc2" + sfx] = rows * ff * b + G * d * ff * b + rows * d * 2
+            out[pre + "fc2_dgrad" + sfx] = rows * d * b + G * d * ff * b + rows * 4 * ff * 2
+            out[pre + "fc2_wgrad" + sfx] = rows * d * b + rows * ff * b + G * d * ff * 4
+            out[pre + "fc1_dgrad" + sfx] = rows * 2 * ff * b + G * 2 * ff * d * b + rows * d * 2
+            out[pre + "fc1_wgrad" + sfx] = rows * 2 * ff * b + rows * d * b + G * 2 * ff * d * 4
+    return out
 
 
 def kernel_source_hash():
@@ -261,10 +296,23 @@ def run_gpu(args, lc):
         dw_sg=torch.empty(lc.d, dtype=f32, device=dev) if lc.shared_gate else None,
     )
     ws_f = moe.workspace(cfg, moe.WS_LAYER_FWD, dev)
-    ws_b = moe.workspace(cfg, moe.WS_LAYER_BWD, dev)
+    ws_b = moe.workspace(cfg, moe.WS_LAYER_BWD_FP8 if args.fp8 else moe.WS_LAYER_BWD, dev)
     stream = torch.cuda.current_stream()
+    fp8q = None
+    if args.fp8:
+        # E4M3 weights quantised once (FP8 parameters); saved.x_perm is not used
+        fp8q = moe.alloc_fp8_experts(cfg, inp["W1"], inp["W2"], dev, Ws1=inp["Ws1"], Ws2=inp["Ws2"])
+        saved["x_perm"] = None
 
     def step(x, dy, yout, dxout):
+        if fp8q is not None:
+            moe.moe_layer_fwd_fp8(cfg, x, inp["W_r"], inp["b_r"], fp8q, inp["Ws1"], inp["Ws2"],
+                                  inp["w_sg"], yout, saved, ws_f)
+            if lc.backward:
+                moe.moe_layer_bwd_fp8(cfg, dy, x, inp["W_r"], fp8q, inp["Ws1"], inp["Ws2"],
+                                      inp["w_sg"], saved, dxout, grads["dW_r"], grads["dW1"],
+                                      grads["dW2"], grads["dWs1"], grads["dWs2"], grads["dw_sg"], ws_b)
+            return
         moe.moe_layer_fwd(cfg, x, inp["W_r"], inp["b_r"], inp["W1"], inp["W2"], inp["Ws1"],
                           inp["Ws2"], inp["w_sg"], yout, saved, ws_f)
         if lc.backward:
@@ -414,20 +462,33 @@ def run_gpu(args, lc):
             dist.destroy_process_group()
         return None
 
-    fp8 = None if args.no_fp8 or lc.dtype != "bf16" else fp8_experts(args, lc, cfg, inp, saved, dev)
+    fp8 = None if args.no_fp8 or args.fp8 or lc.dtype != "bf16" else \
+        fp8_experts(args, lc, cfg, inp, saved, dev)
     if fp8 is not None:
         fp8["layer"] = fp8_layer(args, lc, cfg, inp, dev, ms_step)
 
     # ---- roofline of the dominant kernel (largest share of device time in the timed region)
     peaks, peak_src = load_peaks()
-    work = kernel_work(lc)
+    work = kernel_work(lc, trace, n_trace)
+    flops_of = dict(work)      # FLOPs of the GEMMs, whatever bound their roofline takes
+    bf16_peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+
+    def tensor_peak(name):
+        # E4M3 products: twice the measured bf16 rate (the nominal dense fp8 : bf16 ratio)
+        return 2.0 * bf16_peak if name.endswith("_fp8") else bf16_peak
+
+    gbytes = gemm_bytes(lc) if lc.dtype == "bf16" else {}
     kern = {}
     for name, (n_launch, ms) in trace.items():
         kind, amount = work.get(name, ("hbm", 0.0))
+        if kind == "tensor" and name in gbytes and \
+                gbytes[name] / (peaks["hbm_gbs"] * 1e9) > amount / (tensor_peak(name) * 1e12):
+            kind, amount = "hbm", gbytes[name]      # bound by its bytes, not its FLOPs
+        work[name] = (kind, amount)
         avg_ms = ms / max(1, n_launch)
         if kind == "tensor":
             ach = amount / (avg_ms / 1e3) / 1e12
-            unit, peak = "TFLOP/s", peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+            unit, peak = "TFLOP/s", tensor_peak(name)
         else:
             ach = amount / (avg_ms / 1e3) / 1e9
             unit, peak = "GB/s", peaks["hbm_gbs"]
@@ -443,12 +504,16 @@ def run_gpu(args, lc):
         kd = kern[dom]
         kind = work.get(dom, ("hbm", 0))[0]
         traffic = captured_traffic(lc.name, dom)
+        fp8_dom = kind == "tensor" and dom.endswith("_fp8")
         roof = {"bound": kind, "kernel": dom, "achieved": kd["achieved"],
-                "peak": peaks.get("bf16_tflops_sustained") if kind == "tensor" else peaks["hbm_gbs"],
+                "peak": tensor_peak(dom) if kind == "tensor" else peaks["hbm_gbs"],
                 "unit": kd["unit"], "frac": kd["frac"], "traffic": traffic,
-                "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if kind == 'tensor' else 'hbm_gbs'})"}
+                "peak_source": f"{peak_src} (" + ("2 x bf16_tflops_sustained, nominal fp8:bf16 ratio"
+                                                  if fp8_dom else "bf16_tflops_sustained"
+                                                  if kind == "tensor" else "hbm_gbs") + ")"}
     gemm_ms = sum(ms for n, (_, ms) in trace.items() if n.startswith("gemm_"))
-    gemm_flops = sum(work[n][1] * trace[n][0] for n in trace if n.startswith("gemm_") and n in work)
+    gemm_flops = sum(flops_of[n][1] * trace[n][0] for n in trace
+                     if n.startswith("gemm_") and n in flops_of)
     gemm_tflops = gemm_flops / (gemm_ms / 1e3) / 1e12 if gemm_ms else None
 
     # ---- CPU oracle on a bounded sample (rank 0, N = 1 only)
@@ -466,7 +531,8 @@ def run_gpu(args, lc):
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": lc.dtype,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": ("e4m3 experts, bf16 router/combine" if args.fp8 else lc.dtype),
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights, random init)",
         "config": {"workload": lc.name, "T": lc.T, "d_model": lc.d, "experts": lc.E, "top_k": lc.k,
                    "ffn": lc.f, "shared_ffn": lc.f_shared,
@@ -709,6 +775,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 expert comparison")
     ap.add_argument("--no-graph", action="store_true", help="time eager calls, not a CUDA graph")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time the layer with its experts in FP8 E4M3 (moe_layer_fwd_fp8 / "
+                         "moe_layer_bwd_fp8) instead of bf16")
     ap.add_argument("--e2e-steps", type=int, default=20)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "native" else args.warmup
