@@ -41,9 +41,6 @@ template <int SCHED, int EPI> struct OutPath {
   static constexpr bool tma = !(SCHED == RAGGED_M && EPI == EPI_F32);
 };
 
-#ifndef MOE_EPI8_WGRAD
-#define MOE_EPI8_WGRAD 0
-#endif
 #ifndef MOE_EPI8_SWIGLU_BWD
 #define MOE_EPI8_SWIGLU_BWD 1
 #endif
@@ -127,15 +124,23 @@ template <int SCHED, int EPI, int EPI_WARPS> struct SlabsPerWarp {
 };
 
 // Epilogue width: 4 warps (one per TMEM lane quadrant) or 8 (two per quadrant, each on half
-// of the tile's columns) for products whose epilogue is long relative to their MMAs (weight
-// gradients, SwiGLU backward); 8 epilogue warps trade one pipeline stage for staging slabs.
+// of the tile's columns) for products whose epilogue is long relative to their MMAs (the
+// SwiGLU backward; the E4M3 SwiGLU forward, whose MMAs take half the bf16 time: 0.97 -> 0.82 ms
+// on the 128-expert layer); 8 epilogue warps trade one pipeline stage for staging slabs.
 // (8 warps split a tile's columns in two halves of 64-column steps: BN a multiple of 128.)
-template <int BN, int SCHED, int EPI> struct EpiWidth {
+// Weight gradients keep 4: with 8 they were slower (fc1 1.86 -> 2.04 ms) and their fp32
+// blocks differed between runs on the 128-expert routing, so that form was removed.
+#ifndef MOE_EPI8_F8_FWD
+#define MOE_EPI8_F8_FWD 1
+#endif
+template <int BN, int SCHED, int EPI, bool F8 = false> struct EpiWidth {
   static constexpr int warps =
       (!OutPath<SCHED, EPI>::tma || BN % 128 != 0) ? 4
-      : (SCHED == RAGGED_K ? (MOE_EPI8_WGRAD ? 8 : 4)
+      : (SCHED == RAGGED_K ? 4
                            : (EPI == EPI_SWIGLU_BWD ? (MOE_EPI8_SWIGLU_BWD ? 8 : 4)
-                                                    : (MOE_EPI8_OTHER ? 8 : 4)));
+                                                    : ((F8 && EPI == EPI_SWIGLU_FWD ? MOE_EPI8_F8_FWD
+                                                                                    : MOE_EPI8_OTHER)
+                                                           ? 8 : 4)));
   static constexpr int slabs = SlabsPerWarp<SCHED, EPI, warps>::n;
 };
 
@@ -261,13 +266,13 @@ __device__ __forceinline__ void slab_store_3d(const CUtensorMap* m, const uint8_
 }
 
 template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, bool GATHER = false, bool F8 = false>
-__global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI>::warps, 1)
+__global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
                    const __grid_constant__ CUtensorMap tmO2, const KArgs p) {
   constexpr bool TMA_OUT = OutPath<SCHED, EPI>::tma;
-  constexpr int EPI_WARPS = EpiWidth<BN, SCHED, EPI>::warps;
-  constexpr int SLABS = EpiWidth<BN, SCHED, EPI>::slabs;
+  constexpr int EPI_WARPS = EpiWidth<BN, SCHED, EPI, F8>::warps;
+  constexpr int SLABS = EpiWidth<BN, SCHED, EPI, F8>::slabs;
   using C = TileCfg<BN, TMA_OUT, EPI_WARPS, SLABS>;
   constexpr bool MC = McMode<SCHED, EPI>::on;
   constexpr bool DYN = DynMode<SCHED, EPI>::on;
@@ -1659,7 +1664,8 @@ template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, bool GATHER = false,
 int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   const char* name = g.name ? g.name : kind;
   constexpr bool TMA_OUT = OutPath<SCHED, EPI>::tma;
-  using C = TileCfg<BN, TMA_OUT, EpiWidth<BN, SCHED, EPI>::warps, EpiWidth<BN, SCHED, EPI>::slabs>;
+  using C = TileCfg<BN, TMA_OUT, EpiWidth<BN, SCHED, EPI, F8>::warps,
+                    EpiWidth<BN, SCHED, EPI, F8>::slabs>;
   auto kern = tc_gemm_kernel<BN, A_MN, B_MN, SCHED, EPI, GATHER, F8>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;

@@ -9,7 +9,9 @@ compute one piece at a time:
   * counts, offsets and both slot maps exactly the stable counting sort of the selection;
   * y and dx on sampled tokens (whole forward and backward of those tokens, their experts,
     the shared expert and the router);
-  * dW1, dW2 of sampled experts (all of an expert's rows, when none of them is a near tie).
+  * dW1, dW2 of sampled experts (all of an expert's rows, when none of them is a near tie);
+  * a second run of the same step gives bit-identical outputs (no float atomics, fixed-order
+    sums, tiles claimed at run time but each reduced by one CTA).
 """
 import numpy as np
 import pytest
@@ -18,7 +20,7 @@ import torch
 import moe_inputs
 import oracle.moe_oracle as O
 
-from .helpers import TOL, assert_close, np64, run_layer
+from .helpers import GRAD_NAMES, TOL, assert_close, np64, run_layer
 
 pytestmark = pytest.mark.gpu
 
@@ -116,3 +118,13 @@ def test_fullsize_sampled_expert_weight_gradients(full_run):
         _, dW1e, dW2e = O.swiglu_ffn_backward(host["W1"][e], host["W2"][e], X, a, u, h, do)
         assert_close(f"dW1[{e}] ({len(t_list)} rows)", np64(gpu["dW1"][e]), dW1e, TOL[lc.dtype])
         assert_close(f"dW2[{e}] ({len(t_list)} rows)", np64(gpu["dW2"][e]), dW2e, TOL[lc.dtype])
+
+
+def test_fullsize_rerun_is_bit_identical(full_run):
+    lc, inp, gpu, host = full_run
+    again = run_layer(lc, inp, backward=lc.backward)
+    for n in ["y"] + (GRAD_NAMES if lc.backward else []):
+        if gpu.get(n) is not None:
+            assert torch.equal(gpu[n], again[n]), n
+    for n in ("act", "h", "y_perm"):
+        assert torch.equal(gpu["saved"][n], again["saved"][n]), n
