@@ -87,9 +87,9 @@ def kernel_work(lc, trace=None, steps=1):
         })
     for n in [n for n in w if n.startswith("gemm_") and "router" not in n]:
         w[n + "_fp8"] = w[n]
-    # E4M3 quantisation (bf16 in, one byte out): amax passes read, quantise passes read + write
-    amax_bytes = T * d * 2 + (N * d * 2 if lc.backward else 0) + \
-        (T * d * 2 if fs and lc.backward else 0)
+    # E4M3 quantisation (bf16 in, one byte out): amax passes read (only x's in the layer: the
+    # gradients' amaxes come out of the combine backward), quantise passes read + write
+    amax_bytes = T * d * 2
     quant_bytes = N * f * 3 + (T * fs * 3 if fs else 0)
     if lc.backward:
         quant_bytes += N * d * 3 + N * 2 * f * 3 + ((T * d * 3 + T * 2 * fs * 3) if fs else 0)

@@ -553,12 +553,16 @@ static int ffn_bwd_fp8_impl(const moe_cfg* c, int G, const int32_t* offsets, int
                             const uint8_t* h_q, const float* h_scale, const void* dy_perm,
                             uint8_t* dy_q, float* dy_scale, float* dy_amax, void* dH1,
                             uint8_t* dH1_q, float* dH1_scale, float* dH1_amax, void* dx_perm,
-                            float* dW1, float* dW2, int* sched, cudaStream_t st) {
+                            float* dW1, float* dW2, int* sched, cudaStream_t st,
+                            bool dy_amax_ready = false) {
   const int64_t N = rows;
   const int d = c->d, E = G;
   const bool shared = offsets == nullptr;
-  // dy_perm -> E4M3 (one tensor)
-  MOE_TRY(launch_quantize_e4m3(dy_perm, N * d, 1, dy_q, dy_scale, dy_amax, st));
+  // dy_perm -> E4M3 (one tensor; its amax already reduced by the producer of dy_perm, or here)
+  if (dy_amax_ready)
+    MOE_TRY(launch_quant_e4m3_given_amax(dy_perm, N * d, 1, dy_q, dy_scale, dy_amax, st));
+  else
+    MOE_TRY(launch_quantize_e4m3(dy_perm, N * d, 1, dy_q, dy_scale, dy_amax, st));
   // dh = dy . W2_e on E4M3 operands (W2_q read MN-major: no transposed copy), SwiGLU backward
   // -> dH1 = [da | du] (bf16) with its amax
   GemmDesc a = desc0();
@@ -1245,10 +1249,15 @@ static int layer_bwd_impl(const moe_cfg* c, const void* dy, const void* x, const
   uint8_t* ds_q = sq ? static_cast<uint8_t*>(cv.take(static_cast<size_t>(T) * d)) : nullptr;
   uint8_t* s_dH1_q =
       sq ? static_cast<uint8_t*>(cv.take(static_cast<size_t>(T) * 2 * c->f_shared)) : nullptr;
-  // 1. combine backward
+  // 1. combine backward (FP8: it also reduces the amax of dy_perm, and of the shared expert's
+  // upstream gradient, as it stores them)
+  if (q && (cudaMemsetAsync(q->scales + 5, 0, sizeof(float), st) != cudaSuccess ||
+            (sq && cudaMemsetAsync(q->scales + 11, 0, sizeof(float), st) != cudaSuccess)))
+    return fail(MOE_ERR_CUDA, "clearing the gradient amaxes failed");
   MOE_TRY(launch_combine_bwd(c->dtype, dy, s->y_perm, s->gate, s->slot_of_pair,
                              sh ? s->s_out : nullptr, gt ? s->s_coef : nullptr, w.dy_perm, w.dgate,
-                             w.dshared, w.dcoef, T, d, k, st));
+                             w.dshared, w.dcoef, T, d, k, st, q ? q->scales + 5 : nullptr,
+                             sq ? q->scales + 11 : nullptr));
   // 2.-6. The routed experts run on `st`; the shared expert and the router's backward (which
   // need only combine-backward outputs) run on the side stream concurrently; dx waits for both.
   SideStream* side = (MOE_SHARED_OVERLAP_BWD && g_overlap.load()) ? side_stream() : nullptr;
@@ -1260,7 +1269,7 @@ static int layer_bwd_impl(const moe_cfg* c, const void* dy, const void* x, const
                                q->Ws1_scale, q->Ws2_q, q->Ws2_scale, s->s_act, q->s_h_q,
                                q->scales + 8, w.dshared, ds_q, q->scales + 10, q->scales + 11,
                                w.s_dH1, s_dH1_q, q->scales + 12, q->scales + 13, w.dx_shared,
-                               dWs1, dWs2, w.sched + 8, ss));
+                               dWs1, dWs2, w.sched + 8, ss, true));
     else if (sh)
       MOE_TRY(ffn_bwd_impl(c, 1, nullptr, T, c->f_shared, x, Ws1, Ws2, s->s_act, s->s_h,
                            w.dshared, w.s_dH1, w.dx_shared, dWs1, dWs2, w.sched + 8, ss));
@@ -1322,7 +1331,7 @@ static int layer_bwd_impl(const moe_cfg* c, const void* dy, const void* x, const
     MOE_TRY(ffn_bwd_fp8_impl(c, c->E, s->offsets, Nrows(c), c->f, q->x_perm_q, q->scales + 0, q->W1_q, q->W1_scale,
                              q->W2_q, q->W2_scale, s->act, q->h_q, q->scales + 2, w.dy_perm, dy_q,
                              q->scales + 4, q->scales + 5, w.dH1, dH1_q, q->scales + 6,
-                             q->scales + 7, w.dy_perm, dW1, dW2, w.sched, st));
+                             q->scales + 7, w.dy_perm, dW1, dW2, w.sched, st, true));
   else if (permute_fused(c))
     MOE_TRY(ffn_bwd_impl(c, E, s->offsets, Nrows(c), c->f, x, W1, W2, s->act, s->h, w.dy_perm,
                          w.dH1, w.dy_perm, dW1, dW2, w.sched, st, s->token_of_slot, T));

@@ -67,6 +67,12 @@ __device__ __forceinline__ uint4 pack16(const float* f, const float*) {
                     __float_as_uint(f[3]));
 }
 
+// A float as it reads back after being stored as T (round to nearest even for bf16).
+__device__ __forceinline__ float as_stored(float v, const bf16*) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+__device__ __forceinline__ float as_stored(float v, const float*) { return v; }
+
 __device__ __forceinline__ uint4 ld_nc16(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -97,7 +97,8 @@ int launch_combine(int dtype, const void* y_perm, const float* gate, const int32
 int launch_combine_bwd(int dtype, const void* dy, const void* y_perm, const float* gate,
                        const int32_t* slot_of_pair, const void* shared_out,
                        const float* shared_coef, void* dy_perm, float* dgate, void* dshared,
-                       float* dcoef, int T, int d, int k, cudaStream_t st);
+                       float* dcoef, int T, int d, int k, cudaStream_t st, float* amax_dy = nullptr,
+                       float* amax_ds = nullptr);
 int launch_gather_sum(int dtype, const void* dx_perm, const int32_t* slot_of_pair,
                       const void* dx_shared, const void* dx_router, const float* dz,
                       const void* w_sg, void* dx, int T, int d, int k, cudaStream_t st);

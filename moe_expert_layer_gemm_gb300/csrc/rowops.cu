@@ -144,12 +144,16 @@ __global__ void __launch_bounds__(ROW_THREADS) combine_bwd_kernel(
     const T* __restrict__ dy, const T* __restrict__ y_perm, const float* __restrict__ gate,
     const int32_t* __restrict__ sop, const T* __restrict__ shared_out,
     const float* __restrict__ shared_coef, T* __restrict__ dy_perm, float* __restrict__ dgate,
-    T* __restrict__ dshared, float* __restrict__ dcoef, int Tn, int d, int k, int* err) {
+    T* __restrict__ dshared, float* __restrict__ dcoef, int Tn, int d, int k, int* err,
+    unsigned int* __restrict__ amax_dy, unsigned int* __restrict__ amax_ds) {
   constexpr int VE = Vec16<T>::n;
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   const int vpr = d / VE;
+  // FP8 backward: max |value| of dy_perm and of dshared as stored (after rounding to T)
+  float mdy = 0.f, mds = 0.f;
+  auto stored = [](float v) { return fabsf(as_stored(v, static_cast<const T*>(nullptr))); };
   for (int t = gw; t < Tn; t += nw) {
     const int64_t pk = static_cast<int64_t>(t) * k;
     const int my_slot = lane < k ? checked_slot(sop[pk + lane], Tn, k, err) : 0;
@@ -191,10 +195,15 @@ __global__ void __launch_bounds__(ROW_THREADS) combine_bwd_kernel(
             dot[j] = fmaf(g_in[i], yv[i], dot[j]);
             o[i] = g * g_in[i];
           }
-          if (s >= 0)
+          if (s >= 0) {
             st16(reinterpret_cast<char*>(dy_perm + static_cast<int64_t>(s) * d) +
                      static_cast<int64_t>(v) * 16,
                  pack16(o, static_cast<const T*>(nullptr)));
+            if (amax_dy) {
+#pragma unroll
+              for (int i = 0; i < VE; ++i) mdy = fmaxf(mdy, stored(o[i]));
+            }
+          }
         }
       }
       if (shared_out) {
@@ -213,6 +222,10 @@ __global__ void __launch_bounds__(ROW_THREADS) combine_bwd_kernel(
           st16(reinterpret_cast<char*>(dshared + static_cast<int64_t>(t) * d) +
                    static_cast<int64_t>(v) * 16,
                pack16(o, static_cast<const T*>(nullptr)));
+          if (amax_ds) {
+#pragma unroll
+            for (int i = 0; i < VE; ++i) mds = fmaxf(mds, stored(o[i]));
+          }
         }
       }
     }
@@ -227,6 +240,15 @@ __global__ void __launch_bounds__(ROW_THREADS) combine_bwd_kernel(
       const float s = warp_sum(dotc);
       if (lane == 0) dcoef[t] = s;
     }
+  }
+  // non-negative floats order like their bit patterns
+  if (amax_dy) {
+    const float m = warp_max(mdy);
+    if (lane == 0 && m > 0.f) atomicMax(amax_dy, __float_as_uint(m));
+  }
+  if (amax_ds) {
+    const float m = warp_max(mds);
+    if (lane == 0 && m > 0.f) atomicMax(amax_ds, __float_as_uint(m));
   }
 }
 
@@ -501,16 +523,18 @@ int launch_combine(int dtype, const void* y_perm, const float* gate, const int32
 int launch_combine_bwd(int dtype, const void* dy, const void* y_perm, const float* gate,
                        const int32_t* sop, const void* shared_out, const float* shared_coef,
                        void* dy_perm, float* dgate, void* dshared, float* dcoef, int T, int d, int k,
-                       cudaStream_t st) {
+                       cudaStream_t st, float* amax_dy, float* amax_ds) {
+  auto* ady = reinterpret_cast<unsigned int*>(amax_dy);
+  auto* ads = reinterpret_cast<unsigned int*>(amax_ds);
   if (dtype == MOE_DTYPE_BF16)
     return launch("combine_bwd", combine_bwd_kernel<bf16>, row_grid(T), dim3(ROW_THREADS), 0, st,
                   (const bf16*)dy, (const bf16*)y_perm, gate, sop, (const bf16*)shared_out,
                   shared_coef, (bf16*)dy_perm, dgate, (bf16*)dshared, dcoef, T, d, k,
-                  device_error_word());
+                  device_error_word(), ady, ads);
   return launch("combine_bwd", combine_bwd_kernel<float>, row_grid(T), dim3(ROW_THREADS), 0, st,
                 (const float*)dy, (const float*)y_perm, gate, sop, (const float*)shared_out,
                 shared_coef, (float*)dy_perm, dgate, (float*)dshared, dcoef, T, d, k,
-                device_error_word());
+                device_error_word(), ady, ads);
 }
 
 int launch_gather_sum(int dtype, const void* dx_perm, const int32_t* sop, const void* dx_shared,
