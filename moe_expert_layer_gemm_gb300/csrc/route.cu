@@ -7,8 +7,9 @@
 //   slot(t, j) = offsets[e] + #{t' < t : t' picked e},  e = idx[t, j].
 //
 // Four launches:
-//   topk  -- one warp per token (grid-stride over all tokens): k rounds of a warp-wide argmax
-//            over fp32 keys (ties -> lower expert index), gates in fp32.  The key is the logit,
+//   topk  -- one warp per token (grid-stride over all tokens): k rounds of a warp-wide max
+//            (fp32 key, ties to the lower expert index), gates in fp32, lane j computing pair
+//            j's.  The key is the logit,
 //            or, with a selection-only expert bias ("Megatron-Bridge 深度剖析",
 //            §Nemotron-3-Nano 配置: sigmoid routing with expert-bias correction as in DeepSeek
 //            V3), the fp32 score (softmax over E, or sigmoid) plus the expert's bias.
@@ -19,6 +20,8 @@
 //            the block's tokens of expert e is the popcount of the mask bits below t.
 // All integer, so the result is exact and independent of scheduling.
 #include <limits.h>
+
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -88,64 +91,72 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
       for (int q = 0; q < EPL; ++q) key[q] = cur[q];
     }
 
-    // ---- selection: k rounds of warp argmax, order (key desc, expert asc); the selected
-    // experts' logits travel with them for the gates
-    uint32_t taken = 0u;
-    float sel_v[MAXK];
-    int sel_e[MAXK];
+    // ---- selection: k rounds of a warp-wide max, order (key desc, expert asc).  Each lane first
+    // sorts its EPL (key, expert) pairs, so a round compares only the lanes' heads: a float max,
+    // then the lowest expert among the lanes holding it (a ballot; a second reduction only when
+    // lanes tie).  The winning lane moves on to its next pair.
+    float hk[EPL];
+    int he[EPL];
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) {
+      const int e = q * 32 + lane;
+      hk[q] = e < E ? key[q] : NEG_INF;
+      he[q] = e < E ? e : INT_MAX;
+    }
+#pragma unroll
+    for (int i = 1; i < EPL; ++i)          // insertion sort, (key desc, expert asc)
+#pragma unroll
+      for (int q = i; q > 0; --q)
+        if (hk[q] > hk[q - 1] || (hk[q] == hk[q - 1] && he[q] < he[q - 1])) {
+          const float tk = hk[q];
+          hk[q] = hk[q - 1];
+          hk[q - 1] = tk;
+          const int te = he[q];
+          he[q] = he[q - 1];
+          he[q - 1] = te;
+        }
+    int my_e = 0;                          // lane j: the j-th selected expert
 #pragma unroll
     for (int j = 0; j < MAXK; ++j) {
-      sel_v[j] = NEG_INF;
-      sel_e[j] = 0;
       if (j < k) {
-        float bv = NEG_INF, bl = NEG_INF;
-        int be = INT_MAX;
+        const float m = warp_max(hk[0]);   // -0 and +0 compare equal, as in the oracle
+        const unsigned tied = __ballot_sync(0xffffffffu, hk[0] == m);
+        int e;
+        if ((tied & (tied - 1u)) == 0u) {
+          e = __shfl_sync(0xffffffffu, he[0], __ffs(tied) - 1);
+        } else {
+          int c = hk[0] == m ? he[0] : INT_MAX;
 #pragma unroll
-        for (int q = 0; q < EPL; ++q) {
-          const int e = q * 32 + lane;
-          if (!((taken >> q) & 1u) && e < E && (key[q] > bv || (key[q] == bv && e < be))) {
-            bv = key[q];
-            be = e;
-            bl = cur[q];
-          }
+          for (int o = 16; o > 0; o >>= 1) c = min(c, __shfl_xor_sync(0xffffffffu, c, o));
+          e = c;
         }
+        if (lane == j) my_e = e;
+        if ((e & 31) == lane) {            // the winner drops its head
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-          const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
-          if (ov > bv || (ov == bv && oe < be)) {
-            bv = ov;
-            be = oe;
-            bl = ol;
+          for (int q = 0; q + 1 < EPL; ++q) {
+            hk[q] = hk[q + 1];
+            he[q] = he[q + 1];
           }
+          hk[EPL - 1] = NEG_INF;
+          he[EPL - 1] = INT_MAX;
         }
-        sel_v[j] = bl;
-        sel_e[j] = be;
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
       }
     }
 
-    // ---- gates (fp32)
-    float g[MAXK];
+    // ---- gates (fp32), lane j for pair j: the selected expert's logit (in L1 from the row load)
+    const float lv = lane < k ? __ldg(logits + static_cast<int64_t>(t) * E + my_e) : NEG_INF;
+    float g;
     if (score_fn == MOE_SCORE_SOFTMAX) {
       // shift: the row maximum (over all E without renorm, over the selected with it); without
       // a selection bias the top-1 logit is both
-      float m = sel_v[0];
-      if (sel_bias) {
-        if (renorm) {
-#pragma unroll
-          for (int j = 1; j < MAXK; ++j)
-            if (j < k) m = fmaxf(m, sel_v[j]);
-        } else {
-          m = rmax;
-        }
-      }
-      float denom = 0.f;
+      float m;
+      if (!sel_bias) m = __shfl_sync(0xffffffffu, lv, 0);
+      else if (renorm) m = __shfl_sync(0xffffffffu, warp_max(lv), 0);
+      else m = rmax;
+      const float ex = lane < k ? expf(lv - m) : 0.f;
+      float denom;
       if (renorm) {
-#pragma unroll
-        for (int j = 0; j < MAXK; ++j)
-          if (j < k) denom += expf(sel_v[j] - m);
+        denom = warp_sum(ex);
       } else {
         float part = 0.f;
 #pragma unroll
@@ -153,30 +164,20 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
           if (q * 32 + lane < E) part += expf(cur[q] - m);
         denom = warp_sum(part);
       }
-      const float inv = 1.0f / denom;
-#pragma unroll
-      for (int j = 0; j < MAXK; ++j) g[j] = expf(sel_v[j] - m) * inv;
+      denom = __shfl_sync(0xffffffffu, denom, 0);   // one value for every lane
+      g = ex * (1.0f / denom);
     } else {
-      float sum = 0.f;
-#pragma unroll
-      for (int j = 0; j < MAXK; ++j) {
-        g[j] = sigmoid_f(sel_v[j]);
-        if (j < k) sum += g[j];
-      }
+      g = lane < k ? sigmoid_f(lv) : 0.f;
       if (renorm) {
-        const float inv = 1.0f / sum;
-#pragma unroll
-        for (int j = 0; j < MAXK; ++j) g[j] *= inv;
+        const float sum = __shfl_sync(0xffffffffu, warp_sum(g), 0);
+        g *= 1.0f / sum;
       }
     }
 
     // ---- outputs: lane j writes pair j
-#pragma unroll
-    for (int j = 0; j < MAXK; ++j) {
-      if (j < k && lane == j) {
-        idx[static_cast<int64_t>(t) * k + j] = sel_e[j];
-        gate[static_cast<int64_t>(t) * k + j] = g[j];
-      }
+    if (lane < k) {
+      idx[static_cast<int64_t>(t) * k + lane] = my_e;
+      gate[static_cast<int64_t>(t) * k + lane] = g;
     }
 #pragma unroll
     for (int q = 0; q < EPL; ++q) cur[q] = nxt[q];
@@ -203,54 +204,85 @@ __global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ i
   for (int e = tid; e < E; e += blockDim.x) hist[static_cast<int64_t>(e) * nblk + blockIdx.x] = cnt[e];
 }
 
-// Exclusive prefix sum over hist[E][nblk] (expert-major) by one block of 1024 threads.
-__global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ hist, int E,
-                                                    int nblk, int32_t* __restrict__ base,
-                                                    int32_t* __restrict__ counts,
-                                                    int32_t* __restrict__ offsets) {
-  __shared__ int warp_tot[32];
+// Exclusive prefix sum over hist[E][nblk] (expert-major) by one block of 1024 threads.  Up to
+// SCAN_CHUNK entries are read into shared memory at once (coalesced, every load in flight
+// together), then scanned there in tiles of SCAN_TILE: every thread scans 8 consecutive
+// entries, a block-wide scan of the threads' sums gives their starts; the chunk is written back
+// coalesced (plus offsets[e] where row e of hist begins).
+constexpr int SCAN_THREADS = 1024;
+constexpr int SCAN_PER = 8;
+constexpr int SCAN_TILE = SCAN_THREADS * SCAN_PER;
+constexpr int SCAN_CHUNK = 5 * SCAN_TILE;   // 160 KB of dynamic shared memory at most
+
+inline int scan_smem_bytes(int L) {
+  const int n = L < SCAN_CHUNK ? L : SCAN_CHUNK;
+  return ((n + SCAN_TILE - 1) / SCAN_TILE) * SCAN_TILE * static_cast<int>(sizeof(int));
+}
+
+__global__ void __launch_bounds__(SCAN_THREADS) scan_kernel(const int32_t* __restrict__ hist, int E,
+                                                            int nblk, int32_t* __restrict__ base,
+                                                            int32_t* __restrict__ counts,
+                                                            int32_t* __restrict__ offsets) {
+  extern __shared__ int buf[];
+  __shared__ int warp_tot[SCAN_THREADS / 32];
+  __shared__ int tile_tot;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int L = E * nblk;
-  const int chunk = (L + blockDim.x - 1) / blockDim.x;
-  const int lo = min(L, tid * chunk), hi = min(L, lo + chunk);
-  int local = 0;
-  for (int i = lo; i < hi; ++i) local += hist[i];
-  // block-wide exclusive scan of `local`
-  int incl = local;
+  int carry = 0;   // sum of all earlier entries (the same in every thread)
+  for (int c0 = 0; c0 < L; c0 += SCAN_CHUNK) {
+    const int n = min(SCAN_CHUNK, L - c0);
+    const int ntile = (n + SCAN_TILE - 1) / SCAN_TILE;
+    for (int i = tid; i < ntile * SCAN_TILE; i += SCAN_THREADS) buf[i] = i < n ? hist[c0 + i] : 0;
+    __syncthreads();
+    for (int tt = 0; tt < ntile; ++tt) {
+      int* tb = buf + tt * SCAN_TILE;
+      int v[SCAN_PER];
+      int local = 0;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int nw = blockDim.x >> 5;
-    int v = lane < nw ? warp_tot[lane] : 0;
-    int s = v;
+      for (int i = 0; i < SCAN_PER; ++i) {
+        v[i] = tb[tid * SCAN_PER + i];
+        local += v[i];
+      }
+      int incl = local;   // block-wide inclusive scan of the threads' sums
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += u;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      if (lane == 31) warp_tot[warp] = incl;
+      __syncthreads();
+      if (warp == 0) {
+        const int w = warp_tot[lane];
+        int sc = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(0xffffffffu, sc, o);
+          if (lane >= o) sc += u;
+        }
+        warp_tot[lane] = sc - w;   // exclusive prefix of the warp totals
+        if (lane == 31) tile_tot = sc;
+      }
+      __syncthreads();
+      int run = carry + warp_tot[warp] + incl - local;
+#pragma unroll
+      for (int i = 0; i < SCAN_PER; ++i) {
+        tb[tid * SCAN_PER + i] = run;   // this thread's own entries: no one else reads them
+        run += v[i];
+      }
+      carry += tile_tot;
+      __syncthreads();   // warp_tot and tile_tot are rewritten by the next tile
     }
-    if (lane < nw) warp_tot[lane] = s - v;   // exclusive prefix of warp totals
+    for (int i = tid; i < n; i += SCAN_THREADS) {
+      const int g = c0 + i;
+      const int b = buf[i];
+      base[g] = b;
+      if (g % nblk == 0) offsets[g / nblk] = b;
+    }
+    __syncthreads();   // buf is refilled by the next chunk
   }
-  __syncthreads();
-  int run = warp_tot[warp] + incl - local;
-  for (int i = lo; i < hi; ++i) {
-    base[i] = run;
-    run += hist[i];
-  }
-  __syncthreads();
-  int total = 0;
-  if (L > 0) total = base[L - 1] + hist[L - 1];
-  for (int e = tid; e < E; e += blockDim.x) {
-    const int start = base[static_cast<int64_t>(e) * nblk];
-    const int end = (e + 1 < E) ? base[static_cast<int64_t>(e + 1) * nblk] : total;
-    counts[e] = end - start;
-    offsets[e] = start;
-  }
-  if (tid == 0) offsets[E] = total;
+  if (tid == 0) offsets[E] = carry;
+  __syncthreads();     // offsets (global, written by this block) are read back below
+  for (int e = tid; e < E; e += blockDim.x) counts[e] = offsets[e + 1] - offsets[e];
 }
 
 __global__ void __launch_bounds__(256) slots_kernel(const int32_t* __restrict__ idx, int T, int k,
@@ -435,8 +467,19 @@ int launch_topk(const float* logits, int T, int E, int k, int score_fn, int reno
 
 int launch_scan(const int32_t* hist, int E, int nblk, int32_t* base, int32_t* counts,
                 int32_t* offsets, cudaStream_t st) {
-  return launch("route_scan", scan_kernel, dim3(1), dim3(1024), 0, st, hist, E, nblk, base,
-                counts, offsets);
+  const int smem = scan_smem_bytes(E * nblk);
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    SCAN_CHUNK * static_cast<int>(sizeof(int)));
+  });
+  if (attr_err != cudaSuccess) {
+    set_error("cudaFuncSetAttribute(route_scan): %s", cudaGetErrorString(attr_err));
+    return MOE_ERR_CUDA;
+  }
+  return launch("route_scan", scan_kernel, dim3(1), dim3(SCAN_THREADS), smem, st, hist, E, nblk,
+                base, counts, offsets);
 }
 
 int launch_slots(const int32_t* idx, int T, int k, int E, const int32_t* base,
