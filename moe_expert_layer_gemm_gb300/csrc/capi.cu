@@ -351,8 +351,8 @@ static int route_impl(const moe_cfg* c, const void* x, const void* W_r, const fl
   }
   MOE_TRY(launch_topk(logits, c->T, c->E, c->k, c->score_fn, c->renorm,
                       select_bias ? b_r : nullptr, idx, gate, w.hist, st));
-  MOE_TRY(launch_scan(w.hist, c->E, route_blocks(c->T), w.base, counts, offsets, st));
-  MOE_TRY(launch_slots(idx, c->T, c->k, c->E, w.base, sop, tos, st));
+  MOE_TRY(launch_scan(w.hist, c->E, route_blocks(c->T), w.base, counts, st));
+  MOE_TRY(launch_slots(idx, c->T, c->k, c->E, w.base, counts, offsets, sop, tos, st));
   return MOE_OK;
 }
 

@@ -83,10 +83,14 @@ int launch_aux_loss(const float* logits, const int32_t* counts, int T, int E, in
                     float coeff, float* partial, float* out, cudaStream_t st);
 int launch_bias_update(const int32_t* counts, float* bias, int T, int k, int E, float rate,
                        cudaStream_t st);
+// Per expert: exclusive prefix of its row of hist (base[e][b], from the expert's first slot) and
+// counts[e].
 int launch_scan(const int32_t* hist, int E, int nblk, int32_t* base, int32_t* counts,
-                int32_t* offsets, cudaStream_t st);
+                cudaStream_t st);
+// offsets (the exclusive scan of counts, E+1 entries) and both slot maps.
 int launch_slots(const int32_t* idx, int T, int k, int E, const int32_t* base,
-                 int32_t* slot_of_pair, int32_t* token_of_slot, cudaStream_t st);
+                 const int32_t* counts, int32_t* offsets, int32_t* slot_of_pair,
+                 int32_t* token_of_slot, cudaStream_t st);
 
 // ------------------------------------------------------------------ row kernels (rowops.cu)
 int launch_permute(int dtype, const void* x, const int32_t* slot_of_pair, void* x_perm, int T,

@@ -14,14 +14,14 @@
 //            §Nemotron-3-Nano 配置: sigmoid routing with expert-bias correction as in DeepSeek
 //            V3), the fp32 score (softmax over E, or sigmoid) plus the expert's bias.
 //   hist  -- one block per 256 tokens: per-expert counts of the block, hist[e][block].
-//   scan  -- one block: exclusive prefix over hist in expert-major order gives, for every
-//            (expert, block), the first slot of that block's tokens of that expert.
-//   slots -- per block: per-expert bitmasks of the block's tokens; the rank of token t among
-//            the block's tokens of expert e is the popcount of the mask bits below t.
+//   scan  -- one block per expert: the exclusive prefix of its row of hist (the first slot of
+//            each block's tokens of that expert, counted from the expert's first slot) and
+//            its count.
+//   slots -- per block: offsets = the exclusive scan of counts (formed by every block, written
+//            out by block 0); per-expert bitmasks of the block's tokens; the rank of token t
+//            among the block's tokens of expert e is the popcount of the mask bits below t.
 // All integer, so the result is exact and independent of scheduling.
 #include <limits.h>
-
-#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -204,96 +204,103 @@ __global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ i
   for (int e = tid; e < E; e += blockDim.x) hist[static_cast<int64_t>(e) * nblk + blockIdx.x] = cnt[e];
 }
 
-// Exclusive prefix sum over hist[E][nblk] (expert-major) by one block of 1024 threads.  Up to
-// SCAN_CHUNK entries are read into shared memory at once (coalesced, every load in flight
-// together), then scanned there in tiles of SCAN_TILE: every thread scans 8 consecutive
-// entries, a block-wide scan of the threads' sums gives their starts; the chunk is written back
-// coalesced (plus offsets[e] where row e of hist begins).
-constexpr int SCAN_THREADS = 1024;
-constexpr int SCAN_PER = 8;
-constexpr int SCAN_TILE = SCAN_THREADS * SCAN_PER;
-constexpr int SCAN_CHUNK = 5 * SCAN_TILE;   // 160 KB of dynamic shared memory at most
+// Per expert e (one block each): the exclusive prefix of hist[e][0..nblk) -- the first slot of
+// block b's tokens of expert e, counted from the expert's first slot -- and the row total
+// counts[e].  Each thread takes 8 consecutive entries; a block-wide scan of the threads' sums
+// gives their starts.  The experts' own offsets are the scan of counts, which every slots block
+// forms itself (it needs all of them).
+constexpr int RSCAN_THREADS = 256;
+constexpr int RSCAN_PER = 8;
 
-inline int scan_smem_bytes(int L) {
-  const int n = L < SCAN_CHUNK ? L : SCAN_CHUNK;
-  return ((n + SCAN_TILE - 1) / SCAN_TILE) * SCAN_TILE * static_cast<int>(sizeof(int));
-}
-
-__global__ void __launch_bounds__(SCAN_THREADS) scan_kernel(const int32_t* __restrict__ hist, int E,
-                                                            int nblk, int32_t* __restrict__ base,
-                                                            int32_t* __restrict__ counts,
-                                                            int32_t* __restrict__ offsets) {
-  extern __shared__ int buf[];
-  __shared__ int warp_tot[SCAN_THREADS / 32];
-  __shared__ int tile_tot;
+__global__ void __launch_bounds__(RSCAN_THREADS) row_scan_kernel(const int32_t* __restrict__ hist,
+                                                                 int nblk,
+                                                                 int32_t* __restrict__ rowpre,
+                                                                 int32_t* __restrict__ counts) {
+  __shared__ int warp_tot[RSCAN_THREADS / 32];
+  __shared__ int chunk_tot;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int L = E * nblk;
-  int carry = 0;   // sum of all earlier entries (the same in every thread)
-  for (int c0 = 0; c0 < L; c0 += SCAN_CHUNK) {
-    const int n = min(SCAN_CHUNK, L - c0);
-    const int ntile = (n + SCAN_TILE - 1) / SCAN_TILE;
-    for (int i = tid; i < ntile * SCAN_TILE; i += SCAN_THREADS) buf[i] = i < n ? hist[c0 + i] : 0;
+  const int32_t* row = hist + static_cast<int64_t>(blockIdx.x) * nblk;
+  int32_t* out = rowpre + static_cast<int64_t>(blockIdx.x) * nblk;
+  int carry = 0;
+  for (int c0 = 0; c0 < nblk; c0 += RSCAN_THREADS * RSCAN_PER) {
+    const int i0 = c0 + tid * RSCAN_PER;
+    int v[RSCAN_PER];
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < RSCAN_PER; ++i) {
+      v[i] = i0 + i < nblk ? row[i0 + i] : 0;
+      local += v[i];
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
-    for (int tt = 0; tt < ntile; ++tt) {
-      int* tb = buf + tt * SCAN_TILE;
-      int v[SCAN_PER];
-      int local = 0;
-#pragma unroll
-      for (int i = 0; i < SCAN_PER; ++i) {
-        v[i] = tb[tid * SCAN_PER + i];
-        local += v[i];
+    if (tid == 0) {
+      int run = 0;
+      for (int w = 0; w < RSCAN_THREADS / 32; ++w) {
+        const int t = warp_tot[w];
+        warp_tot[w] = run;
+        run += t;
       }
-      int incl = local;   // block-wide inclusive scan of the threads' sums
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
-      }
-      if (lane == 31) warp_tot[warp] = incl;
-      __syncthreads();
-      if (warp == 0) {
-        const int w = warp_tot[lane];
-        int sc = w;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int u = __shfl_up_sync(0xffffffffu, sc, o);
-          if (lane >= o) sc += u;
-        }
-        warp_tot[lane] = sc - w;   // exclusive prefix of the warp totals
-        if (lane == 31) tile_tot = sc;
-      }
-      __syncthreads();
-      int run = carry + warp_tot[warp] + incl - local;
-#pragma unroll
-      for (int i = 0; i < SCAN_PER; ++i) {
-        tb[tid * SCAN_PER + i] = run;   // this thread's own entries: no one else reads them
-        run += v[i];
-      }
-      carry += tile_tot;
-      __syncthreads();   // warp_tot and tile_tot are rewritten by the next tile
+      chunk_tot = run;
     }
-    for (int i = tid; i < n; i += SCAN_THREADS) {
-      const int g = c0 + i;
-      const int b = buf[i];
-      base[g] = b;
-      if (g % nblk == 0) offsets[g / nblk] = b;
+    __syncthreads();
+    int run = carry + warp_tot[warp] + incl - local;
+#pragma unroll
+    for (int i = 0; i < RSCAN_PER; ++i) {
+      if (i0 + i < nblk) out[i0 + i] = run;
+      run += v[i];
     }
-    __syncthreads();   // buf is refilled by the next chunk
+    carry += chunk_tot;
+    __syncthreads();   // warp_tot and chunk_tot are rewritten by the next chunk
   }
-  if (tid == 0) offsets[E] = carry;
-  __syncthreads();     // offsets (global, written by this block) are read back below
-  for (int e = tid; e < E; e += blockDim.x) counts[e] = offsets[e + 1] - offsets[e];
+  if (tid == 0) counts[blockIdx.x] = carry;
 }
 
 __global__ void __launch_bounds__(256) slots_kernel(const int32_t* __restrict__ idx, int T, int k,
-                                                    int E, const int32_t* __restrict__ base,
-                                                    int nblk, int32_t* __restrict__ slot_of_pair,
+                                                    int E, const int32_t* __restrict__ rowpre,
+                                                    const int32_t* __restrict__ counts,
+                                                    int32_t* __restrict__ offsets, int nblk,
+                                                    int32_t* __restrict__ slot_of_pair,
                                                     int32_t* __restrict__ token_of_slot,
                                                     int* err) {
   __shared__ uint32_t mask[MOE_MAX_EXPERTS * MASK_WORDS];
+  __shared__ int s_off[MOE_MAX_EXPERTS + 1];
   const int tid = threadIdx.x;
   for (int i = tid; i < E * MASK_WORDS; i += blockDim.x) mask[i] = 0u;
+  if (tid < 32) {
+    // offsets = exclusive scan of counts (E <= 256: 8 experts per lane, in expert order)
+    constexpr int PER = MOE_MAX_EXPERTS / 32;
+    int v[PER];
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = tid * PER + i;
+      v[i] = e < E ? counts[e] : 0;
+      local += v[i];
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (tid >= o) incl += u;
+    }
+    int run = incl - local;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = tid * PER + i;
+      if (e < E) s_off[e] = run;
+      run += v[i];
+    }
+    if (tid == 31) s_off[E] = incl;
+  }
   __syncthreads();
+  if (blockIdx.x == 0)
+    for (int e = tid; e <= E; e += blockDim.x) offsets[e] = s_off[e];
   const int t = blockIdx.x * TPB + tid;
   const int w = tid >> 5, bit = tid & 31;
   int ev[MAXK];
@@ -319,7 +326,7 @@ __global__ void __launch_bounds__(256) slots_kernel(const int32_t* __restrict__ 
     if (e < 0) continue;
     int rank = __popc(mask[e * MASK_WORDS + w] & ((1u << bit) - 1u));
     for (int ww = 0; ww < w; ++ww) rank += __popc(mask[e * MASK_WORDS + ww]);
-    const int s = base[static_cast<int64_t>(e) * nblk + blockIdx.x] + rank;
+    const int s = s_off[e] + rowpre[static_cast<int64_t>(e) * nblk + blockIdx.x] + rank;
     if (s < 0 || s >= N) {
       record_error(err, DEVERR_BAD_SLOT);
       continue;
@@ -466,27 +473,17 @@ int launch_topk(const float* logits, int T, int E, int k, int score_fn, int reno
 }
 
 int launch_scan(const int32_t* hist, int E, int nblk, int32_t* base, int32_t* counts,
-                int32_t* offsets, cudaStream_t st) {
-  const int smem = scan_smem_bytes(E * nblk);
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    SCAN_CHUNK * static_cast<int>(sizeof(int)));
-  });
-  if (attr_err != cudaSuccess) {
-    set_error("cudaFuncSetAttribute(route_scan): %s", cudaGetErrorString(attr_err));
-    return MOE_ERR_CUDA;
-  }
-  return launch("route_scan", scan_kernel, dim3(1), dim3(SCAN_THREADS), smem, st, hist, E, nblk,
-                base, counts, offsets);
+                cudaStream_t st) {
+  return launch("route_scan", row_scan_kernel, dim3(E), dim3(RSCAN_THREADS), 0, st, hist, nblk,
+                base, counts);
 }
 
 int launch_slots(const int32_t* idx, int T, int k, int E, const int32_t* base,
-                 int32_t* slot_of_pair, int32_t* token_of_slot, cudaStream_t st) {
+                 const int32_t* counts, int32_t* offsets, int32_t* slot_of_pair,
+                 int32_t* token_of_slot, cudaStream_t st) {
   const int nblk = route_blocks(T);
   return launch("route_slots", slots_kernel, dim3(nblk), dim3(256), 0, st, idx, T, k, E, base,
-                nblk, slot_of_pair, token_of_slot, device_error_word());
+                counts, offsets, nblk, slot_of_pair, token_of_slot, device_error_word());
 }
 
 }  // namespace moe
