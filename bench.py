@@ -406,8 +406,9 @@ def run_gpu(args, lc):
     value = replica_throughput(lc.T, args.steps, world, ms_max)
 
     # ---- end-to-end: every step copies its inputs (x, dy) in from pinned host memory and its
-    # results (y, dx) out to pinned host memory.  Copies run on a second stream, double-
-    # buffered, so that step i+1's upload and step i's download overlap step i's compute.
+    # results (y, dx) out to pinned host memory.  Uploads and downloads run on two copy streams
+    # (two copy engines), double-buffered, so that step i+1's upload and step i's download
+    # overlap step i's compute; events order every buffer's reuse.
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
     x_h = [inp["x"].cpu().pin_memory() for _ in range(2)]
     dy_h = [inp["dy"].cpu().pin_memory() for _ in range(2)]
@@ -417,7 +418,8 @@ def run_gpu(args, lc):
     dy_d = [torch.empty_like(inp["dy"]) for _ in range(2)]
     y_d = [torch.empty_like(inp["x"]) for _ in range(2)]
     dx_d = [torch.empty_like(inp["x"]) for _ in range(2)]
-    copy = torch.cuda.Stream(device=dev)
+    up_s = torch.cuda.Stream(device=dev)
+    down_s = torch.cuda.Stream(device=dev)
     uploaded = [torch.cuda.Event() for _ in range(2)]
     computed = [torch.cuda.Event() for _ in range(2)]
     downloaded = [torch.cuda.Event() for _ in range(2)]
@@ -426,28 +428,35 @@ def run_gpu(args, lc):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    with torch.cuda.stream(copy):
+    up_s.wait_stream(stream)
+    down_s.wait_stream(stream)
+    with torch.cuda.stream(up_s):
         x_d[0].copy_(x_h[0], non_blocking=True)
         dy_d[0].copy_(dy_h[0], non_blocking=True)
-        uploaded[0].record(copy)
+        uploaded[0].record(up_s)
     for i in range(e2e_steps):
         b = i & 1
         stream.wait_event(uploaded[b])
+        if i >= 2:
+            stream.wait_event(downloaded[b])      # step i-2's results are out of y_d[b], dx_d[b]
         step(x_d[b], dy_d[b], y_d[b], dx_d[b])
         computed[b].record(stream)
-        with torch.cuda.stream(copy):
-            if i + 1 < e2e_steps:
-                nb = b ^ 1
+        if i + 1 < e2e_steps:
+            nb = b ^ 1
+            with torch.cuda.stream(up_s):
                 if i >= 1:
-                    copy.wait_event(downloaded[nb])   # buffers of step i-1 are out
+                    up_s.wait_event(computed[nb])  # step i-1 no longer reads x_d[nb], dy_d[nb]
                 x_d[nb].copy_(x_h[nb], non_blocking=True)
                 dy_d[nb].copy_(dy_h[nb], non_blocking=True)
-                uploaded[nb].record(copy)
-            copy.wait_event(computed[b])
+                uploaded[nb].record(up_s)
+        with torch.cuda.stream(down_s):
+            down_s.wait_event(computed[b])
             y_h[b].copy_(y_d[b], non_blocking=True)
-            dx_h[b].copy_(dx_d[b], non_blocking=True)
-            downloaded[b].record(copy)
-    stream.wait_stream(copy)
+            if lc.backward:
+                dx_h[b].copy_(dx_d[b], non_blocking=True)
+            downloaded[b].record(down_s)
+    stream.wait_stream(up_s)
+    stream.wait_stream(down_s)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)

@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
                                                    int k, int score_fn, int renorm,
                                                    const float* __restrict__ sel_bias,
                                                    int32_t* __restrict__ idx,
-                                                   float* __restrict__ gate) {
+                                                   float* __restrict__ gate, int* err) {
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
@@ -100,7 +100,9 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 #pragma unroll
     for (int q = 0; q < EPL; ++q) {
       const int e = q * 32 + lane;
-      hk[q] = e < E ? key[q] : NEG_INF;
+      // a NaN key (outside the inputs' contract) ranks as -inf, so every round still has a
+      // maximum that some lane holds and the selection stays within [0, E)
+      hk[q] = (e < E && key[q] == key[q]) ? key[q] : NEG_INF;
       he[q] = e < E ? e : INT_MAX;
     }
 #pragma unroll
@@ -144,6 +146,10 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     }
 
     // ---- gates (fp32), lane j for pair j: the selected expert's logit (in L1 from the row load)
+    if (lane < k && (my_e < 0 || my_e >= E)) {   // cannot happen; never index with it
+      record_error(err, DEVERR_BAD_EXPERT);
+      my_e = 0;
+    }
     const float lv = lane < k ? __ldg(logits + static_cast<int64_t>(t) * E + my_e) : NEG_INF;
     float g;
     if (score_fn == MOE_SCORE_SOFTMAX) {
@@ -457,16 +463,16 @@ int launch_topk(const float* logits, int T, int E, int k, int score_fn, int reno
   int rc;
   if (E <= 32)
     rc = launch("route_topk", topk_kernel<1>, grid, block, 0, st, logits, T, E, k, score_fn, renorm,
-                sel_bias, idx, gate);
+                sel_bias, idx, gate, device_error_word());
   else if (E <= 64)
     rc = launch("route_topk", topk_kernel<2>, grid, block, 0, st, logits, T, E, k, score_fn, renorm,
-                sel_bias, idx, gate);
+                sel_bias, idx, gate, device_error_word());
   else if (E <= 128)
     rc = launch("route_topk", topk_kernel<4>, grid, block, 0, st, logits, T, E, k, score_fn, renorm,
-                sel_bias, idx, gate);
+                sel_bias, idx, gate, device_error_word());
   else
     rc = launch("route_topk", topk_kernel<8>, grid, block, 0, st, logits, T, E, k, score_fn, renorm,
-                sel_bias, idx, gate);
+                sel_bias, idx, gate, device_error_word());
   MOE_TRY(rc);
   return launch("route_hist", hist_kernel, dim3(nblk), dim3(TPB), 0, st, idx, T, k, E, hist, nblk,
                 device_error_word());

@@ -74,3 +74,24 @@ def test_route_stress_full_size(case):
 def test_route_token_counts_around_block_edges(T):
     lg = torch.randint(0, 3, (T, 16), generator=torch.Generator().manual_seed(T)).float()
     check_route(T, 16, 4, 1, 1, lg)
+
+
+@pytest.mark.parametrize("E,k", [(64, 4), (128, 8)])
+def test_route_nan_logits_stay_in_range(E, k):
+    """NaN logits are outside the inputs' contract, but routing must stay memory-safe: a NaN key
+    ranks as -inf, so every selected expert is in [0, E), each row's set is distinct, and the
+    maps remain a bijection.  Rows without NaN are routed as the oracle routes them."""
+    T = 300
+    lg = torch.randn(T, E, generator=torch.Generator().manual_seed(E + k)) * 2.0
+    lg[:10] = float("nan")                      # whole rows
+    lg[10:20, ::2] = float("nan")               # half rows
+    g = route_gpu(T, E, k, 1, 1, lg.cuda())
+    idx = g["idx"]
+    assert ((idx >= 0) & (idx < E)).all()
+    assert all(len(set(r)) == k for r in idx.tolist())
+    assert g["counts"].sum() == T * k and g["offsets"][-1] == T * k
+    assert np.array_equal(np.sort(g["token_of_slot"][: T * k]), np.repeat(np.arange(T), k))
+    r = O.route(lg[20:].numpy(), k, E, 1, 1)
+    assert (idx[20:] == r["idx"]).all()
+    # whole-NaN rows: every key ranks as -inf, ties go to the lowest experts
+    assert (idx[:10] == np.arange(k)).all()
