@@ -396,7 +396,9 @@ const char* moe_last_error(void);
 
 /* Synchronises `stream`, reads and clears the device error word of the current device.
  * Returns MOE_OK, MOE_ERR_DEVICE_CHECK (with the kernel's code in *code if code != NULL),
- * or MOE_ERR_CUDA. */
+ * or MOE_ERR_CUDA.  Codes (the first one recorded wins): 1 a bounded wait ran out, 2 an expert
+ * index outside [0, E), 3 a slot outside [0, N), 4 offsets not monotone or not ending at N,
+ * 5 dynamic shared memory not 1024-byte aligned, 6 a gathered token index outside [0, T). */
 int moe_check_device_error(void* stream, int32_t* code);
 
 /* Launch accounting and per-kernel timing (tracing).  moe_trace_enable(1) makes every
@@ -414,6 +416,16 @@ int moe_trace_read(char* names, int name_stride, int* launches, double* total_ms
  * everything on the caller's stream in order (useful for per-kernel timing).  Results are
  * identical either way.  Process-wide; returns the previous setting. */
 int moe_set_stream_overlap(int on);
+
+/* Self-test of the failure path of the pipelined kernels: launches one block that waits, through
+ * the same bounded mbarrier wait as every GEMM pipeline (here with a 50 ms limit), on a barrier
+ * that nothing arrives on.  The wait gives up, the kernel raises its abort flag, records
+ * device error code 1 (a bounded wait ran out) in the device error word and returns.
+ *   observed (device int32): bit 0 = the wait reported success (expected 0), bit 1 = the abort
+ *   flag was raised (expected 1).
+ * The caller then reads the code with moe_check_device_error (which clears it); the context stays
+ * usable. */
+int moe_selftest_wait_timeout(int32_t* observed, void* stream);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int moe_version(void);

@@ -62,6 +62,7 @@ _SIGS = {
     "moe_unpermute_combine": (ctypes.c_int, [_CFG] + [_VP] * 7),
     "moe_unpermute_combine_bwd": (ctypes.c_int, [_CFG] + [_VP] * 11),
     "moe_layer_fwd": (ctypes.c_int, [_CFG] + [_VP] * 9 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP]),
+    "moe_selftest_wait_timeout": (ctypes.c_int, [_VP, _VP]),
     "moe_layer_fwd_fp8": (ctypes.c_int, [_CFG] + [_VP] * 3 + [ctypes.POINTER(MoeFp8Experts)]
                           + [_VP] * 4 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP]),
     "moe_layer_bwd_fp8": (ctypes.c_int, [_CFG] + [_VP] * 3 + [ctypes.POINTER(MoeFp8Experts)]
@@ -360,6 +361,11 @@ def moe_layer_bwd_fp8(cfg, dy, x, W_r, fp8, Ws1, Ws2, w_sg, saved, dx, dW_r, dW1
                                    _p(Ws1), _p(Ws2), _p(w_sg), ctypes.byref(st), _p(dx), _p(dW_r),
                                    _p(dW1), _p(dW2), _p(dWs1), _p(dWs2), _p(dw_sg), _p(ws),
                                    ws.numel(), _stream(stream)), "moe_layer_bwd_fp8")
+
+
+def moe_selftest_wait_timeout(observed, stream=None):
+    """Run the bounded-wait self-test (see include/moe_gb300.h); observed: int32 device tensor."""
+    _check(lib().moe_selftest_wait_timeout(_p(observed), _stream(stream)), "moe_selftest_wait_timeout")
 
 
 def set_stream_overlap(on):

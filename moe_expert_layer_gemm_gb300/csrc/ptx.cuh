@@ -57,7 +57,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Waits until the phase with the given parity has completed.  Returns false if the CTA's
 // abort flag is raised (by this or another thread) or the wait ran out of time.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* err) {
+                                          int* err, uint64_t limit_ns = MOE_WAIT_TIMEOUT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   uint32_t spins = 0;
@@ -65,7 +65,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try_wait(bar, parity)) return true;
     if ((++spins & 63u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > MOE_WAIT_TIMEOUT_NS) {
+      if (globaltimer() - t0 > limit_ns) {
         *abort_flag = 1;
         record_error(err, DEVERR_WAIT_TIMEOUT);
         return false;
