@@ -110,3 +110,40 @@ def test_binding_argument_counts_match_the_header():
         assert name in decls, name
         params = [p for p in (q.strip() for q in decls[name].split(",")) if p and p != "void"]
         assert len(params) == len(args), (name, len(params), len(args))
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include "moe_gb300.h"
+int main(void) {
+  moe_cfg c = {256, 128, 8, 2, 256, 0, MOE_SCORE_SOFTMAX, 1, 0, MOE_DTYPE_BF16, MOE_BIAS_LOGIT,
+               0.0f};
+  size_t ws = moe_workspace_bytes(&c, MOE_WS_LAYER_BWD);
+  int rc = moe_route_topk(NULL, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0);
+  printf("%d %zu %d %s\n", moe_version(), ws, rc, moe_last_error());
+  return (ws > 0 && rc == MOE_ERR_INVALID_ARG) ? 0 : 1;
+}
+"""
+
+
+def test_plain_c_client_builds_against_the_header_and_links(tmp_path):
+    """The header is strict C11 and the library links into a plain C program (no C++, no Python),
+    which sizes a workspace and gets a host-side argument error back."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    libdir = os.path.dirname(moe._lib.LIB_PATH)
+    exe = tmp_path / "client"
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                        "-I" + os.path.join(root, "include"), str(src), "-L" + libdir,
+                        "-lmoe_gb300", "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    env = dict(os.environ, LD_LIBRARY_PATH=libdir)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, env=env, timeout=120)
+    assert r.returncode == 0, (r.stdout, r.stderr)
+    assert "cfg is NULL" in r.stdout
