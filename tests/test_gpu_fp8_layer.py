@@ -29,6 +29,8 @@ CASES = [
                                 T=384, d=128, E=32, k=8, f=64, f_shared=64),
     moe_inputs.QWEN3_30B_A3B.replace(name="qwen3-style small T300 d384 E24 top4 f144",
                                      T=300, d=384, E=24, k=4, f=144, backward=True),
+    moe_inputs.MTP_256E.replace(name="mtp-e256 small T400 d128 E256 top8 f64 s64 gate",
+                                T=400, d=128, E=256, k=8, f=64, f_shared=64),
 ]
 
 
