@@ -1,0 +1,103 @@
+"""Oracle for the MXFP8 (microscaling FP8) expert GEMMs: block quantisation and the grouped
+SwiGLU forward on block-scaled operands (fp64 CPU).
+
+TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's CPU leg may import this
+module; it imports nothing of the CUDA library and shares no code with it.
+
+What the pages fix ("Megatron-Bridge 深度剖析", §新硬件适配): Blackwell brings a microscaling
+FP8 whose scale factors are finer grained than FP8's per-tensor ones (and an FP4 beside it).
+The pages stop there; the format is the Open Compute Project's Microscaling (MX) one, whose
+MXFP8 variant pairs E4M3 elements with one shared E8M0 (power-of-two) scale per block.
+Readings where the pages are silent:
+  * a block is 32 consecutive elements along the product's reduction dimension K (d for fc1,
+    f for fc2), so every row of an operand has K/32 scales;
+  * the shared exponent of a block is floor(log2(amax)) - 8, where 8 is the exponent of E4M3's
+    largest normal (448 = 1.75 * 2^8) and amax the block's largest magnitude; it is clamped to
+    [-127, 127] and amax = 0 gives -127; the stored E8M0 byte is exponent + 127;
+  * an element's code is E4M3(x / 2^e), round to nearest even; magnitudes in [448, 512) * 2^e
+    saturate to 448 (the MX rule of clamping to the element format's largest normal);
+  * the GEMM multiplies decoded values (code value times its block's scale) and accumulates;
+    h is quantised again, in blocks of 32 along f, before fc2, from its bf16 value;
+  * each expert's weights are quantised along their own K: W1 [2f, d] in blocks along d, W2
+    [d, f] in blocks along f.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .fp8_oracle import bf16_round, e4m3_decode, e4m3_encode  # noqa: F401 (bf16_round: re-export)
+from .moe_oracle import silu
+
+BLOCK = 32
+E4M3_EMAX = 8          # exponent of the largest normal E4M3 value, 448 = 1.75 * 2^8
+SCALE_BIAS = 127       # E8M0: the byte is the exponent plus 127
+
+
+def shared_exponent(amax):
+    """Shared block exponent floor(log2(amax)) - 8, clamped to [-127, 127]; -127 for amax = 0.
+    floor(log2(.)) is read off frexp (exact): amax = m * 2^p with m in [0.5, 1) -> p - 1."""
+    a = np.asarray(amax, dtype=np.float64)
+    _, p = np.frexp(a)
+    e = np.where(a > 0, (p.astype(np.int64) - 1) - E4M3_EMAX, -127)
+    return np.clip(e, -127, 127).astype(np.int64)
+
+
+def mx_quantize(x, block=BLOCK):
+    """MXFP8 codes of x along its last axis (whose length must be a multiple of `block`).
+    Returns (codes uint8 with x's shape, scale bytes uint8 [..., K / block])."""
+    x64 = np.asarray(x, dtype=np.float64)
+    K = x64.shape[-1]
+    if K % block:
+        raise ValueError("the blocked axis must be a multiple of the block size")
+    blocks = x64.reshape(x64.shape[:-1] + (K // block, block))
+    amax = np.abs(blocks).max(axis=-1)
+    e = shared_exponent(amax)
+    # x / 2^e is exact in fp64; as fp32 it is exact too for the magnitudes that can round to a
+    # nonzero E4M3 value (2^e * 2^-10 and up), which is all e4m3_encode looks at
+    scaled = np.ldexp(blocks, -e[..., None]).astype(np.float32)
+    codes = e4m3_encode(scaled).reshape(x64.shape)
+    return codes, (e + SCALE_BIAS).astype(np.uint8)
+
+
+def mx_decode(codes, scales, block=BLOCK):
+    """Decoded values: each code's E4M3 value times 2^(its block's byte - 127) (fp64)."""
+    c = np.asarray(codes)
+    s = np.asarray(scales, dtype=np.int64)
+    K = c.shape[-1]
+    v = e4m3_decode(c).reshape(c.shape[:-1] + (K // block, block))
+    v = np.ldexp(v, (s - SCALE_BIAS)[..., None])
+    return v.reshape(c.shape)
+
+
+def fc1_swiglu_mx(xq, xs, W1q, W1s, offsets):
+    """fc1 + SwiGLU of every expert on MXFP8 operands: for the rows s of expert e,
+    [a | u] = dec(xq[s], xs[s]) . dec(W1q[e], W1s[e])^T and h = SiLU(a) * u.  fp64.
+    Returns (h [N, f], act = [a | u] [N, 2f])."""
+    E = W1q.shape[0]
+    f = W1q.shape[1] // 2
+    X = mx_decode(xq, xs)
+    N = X.shape[0]
+    h = np.zeros((N, f))
+    act = np.zeros((N, 2 * f))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi == lo:
+            continue
+        au = X[lo:hi] @ mx_decode(W1q[e], W1s[e]).T
+        act[lo:hi] = au
+        h[lo:hi] = silu(au[:, :f]) * au[:, f:]
+    return h, act
+
+
+def fc2_mx(hq, hs, W2q, W2s, offsets):
+    """fc2 of every expert on MXFP8 operands: y[s] = dec(hq[s], hs[s]) . dec(W2q[e], W2s[e])^T
+    for the rows s of expert e.  fp64."""
+    E = W2q.shape[0]
+    H = mx_decode(hq, hs)
+    y = np.zeros((H.shape[0], W2q.shape[1]))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            y[lo:hi] = H[lo:hi] @ mx_decode(W2q[e], W2s[e]).T
+    return y
+
