@@ -254,6 +254,62 @@ int moe_grouped_swiglu_bwd_fp8(const moe_cfg* cfg, const uint8_t* x_perm_q, cons
                                uint8_t* dH1_q, float* dH1_scale, float* dH1_amax, void* dx_perm,
                                float* dW1, float* dW2, void* ws, size_t ws_bytes, void* stream);
 
+/* MXFP8: microscaled FP8 ("Megatron-Bridge 深度剖析", §新硬件适配: Blackwell's microscaling FP8,
+ * with scale factors finer grained than per tensor; element and scale formats are the OCP
+ * Microscaling ones).  A block is 32 consecutive elements along a product's reduction dimension:
+ *   e = floor(log2(max |x| over the block)) - 8, clamped to [-127, 127] (-127 for an all-zero
+ *   block); code = E4M3(x * 2^-e) (round to nearest even, saturating at +-448); scale byte
+ *   (E8M0) = e + 127, so x ~ E4M3value(code) * 2^(byte - 127).
+ * The GEMMs read block scales in packed layouts sized by moe_mxfp8_scale_bytes:
+ *   MOE_MX_SCALES_X / _H: the permuted activations x_perm [N,d] / h [N,f], in 512-byte chunks of
+ *     128 rows x 128 elements.  Chunk (mt, kc) starts at (mt * ceil(K/128) + kc) * 512, where the
+ *     row tile mt of slot s (expert e, rows [off_e, off_e+1)) is sum_{e'<e} ceil(n_e'/128) +
+ *     (s - off_e) / 128, and the scale of the tile's row r, block j (of the chunk's four) is byte
+ *     (r % 32) * 16 + (r / 32) * 4 + j.  Rows past an expert's end are left unwritten; blocks past K
+ *     are 127.
+ *   MOE_MX_SCALES_W1 / _W2: each expert's weights, per output tile of 192 B-rows (fc1 tile t: gate
+ *     rows 96t..96t+95 then up rows f+96t..f+96t+95; fc2 tile t: rows 192t..192t+191) and per
+ *     128-element K chunk kc, two such chunks (tile rows 0..127, 128..255) at
+ *     ((e * tiles + t) * ceil(K/128) + kc) * 1024; rows and blocks past the weight are 127. */
+enum { MOE_MX_SCALES_X = 0, MOE_MX_SCALES_H = 1, MOE_MX_SCALES_W1 = 2, MOE_MX_SCALES_W2 = 3 };
+/* Bytes of one packed scale buffer for cfg (0 for an invalid cfg or `which`). */
+size_t moe_mxfp8_scale_bytes(const moe_cfg* cfg, int which);
+
+/* MXFP8 quantisation of `rows` rows of `cols` bf16 values along each row (cols a multiple of
+ * 32): q uint8 codes in x's layout, scales uint8 [rows, cols/32] row-major (plain layout, not
+ * packed).  Quantise a weight along its reduction dimension: W1 [E,2f,d] as E*2f rows of d, W2
+ * [E,d,f] as E*d rows of f.  All pointers device, 16-byte aligned. */
+int moe_quantize_mxfp8(const void* x, int64_t rows, int32_t cols, uint8_t* q, uint8_t* scales,
+                       void* stream);
+
+/* Row-major expert weight scales (from moe_quantize_mxfp8: W1_s [E,2f,d/32], W2_s [E,d,f/32]) ->
+ * the packed layouts MOE_MX_SCALES_W1 (W1_sp) and MOE_MX_SCALES_W2 (W2_sp).  Done once per
+ * weight update; the codes keep their [E,2f,d] / [E,d,f] layouts. */
+int moe_mxfp8_pack_expert_scales(const moe_cfg* cfg, const uint8_t* W1_s, const uint8_t* W2_s,
+                                 uint8_t* W1_sp, uint8_t* W2_sp, void* stream);
+
+/* Permute + MXFP8 quantisation in one pass: x_perm_q[slot_of_pair[t,j]] = the codes of x[t]
+ * (moe_quantize_mxfp8 of row t), the scales into x_perm_s in the MOE_MX_SCALES_X layout (row tiles
+ * from offsets [E+1], the routing's).  bf16 x [T,d]; d a multiple of 32. */
+int moe_permute_quantize_mxfp8(const moe_cfg* cfg, const void* x, const int32_t* slot_of_pair,
+                               const int32_t* offsets, uint8_t* x_perm_q, uint8_t* x_perm_s,
+                               void* stream);
+
+/* Grouped SwiGLU forward on MXFP8 operands, block-scaled tensor-core products (every K-block of
+ * 32 carries its A-row and B-row scales).  For rows s of expert e:
+ *   [a | u] = dec(x_perm_q[s], x_perm_s) . dec(W1_q[e], W1_sp)^T   (fp32 accumulation)
+ *   h = SiLU(a) * u, rounded to bf16 (written to h [N,f] unless NULL; [a | u] to act [N,2f] unless
+ *     NULL), then quantised to MXFP8 along f in the same epilogue: codes h_q [N,f], scales h_s in
+ *     the MOE_MX_SCALES_H layout;
+ *   y_perm[s] = dec(h_q[s], h_s) . dec(W2_q[e], W2_sp)^T                 (bf16 [N,d])
+ * W1_q [E,2f,d] and W2_q [E,d,f] are codes from moe_quantize_mxfp8, W1_sp / W2_sp their packed
+ * scales (moe_mxfp8_pack_expert_scales).  d and f multiples of 32; cfg->dtype MOE_DTYPE_BF16. */
+int moe_grouped_swiglu_fwd_mxfp8(const moe_cfg* cfg, const uint8_t* x_perm_q,
+                                 const uint8_t* x_perm_s, const int32_t* offsets,
+                                 const uint8_t* W1_q, const uint8_t* W1_sp, const uint8_t* W2_q,
+                                 const uint8_t* W2_sp, void* h, void* act, uint8_t* h_q,
+                                 uint8_t* h_s, void* y_perm, void* stream);
+
 /* Unpermute + weighted combine: "Megatron-Bridge 深度剖析", §Expert Parallel 基础 (Step 3,
  * results sent back to token order) and §Shared Expert Overlap (shared output added).
  *   y[t] = sum_{j<k} gate[t,j] * y_perm[slot_of_pair[t,j]]  (+ c_t * shared_out[t])

@@ -23,6 +23,7 @@ SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 DTYPE_BF16, DTYPE_F32 = 0, 1
 BIAS_LOGIT, BIAS_SELECT = 0, 1
 WS_ROUTE, WS_FFN_FWD, WS_FFN_BWD, WS_LAYER_FWD, WS_LAYER_BWD, WS_FFN_BWD_FP8, WS_LAYER_BWD_FP8 = range(7)
+MX_SCALES_X, MX_SCALES_H, MX_SCALES_W1, MX_SCALES_W2 = range(4)
 
 
 class MoeCfg(ctypes.Structure):
@@ -59,6 +60,11 @@ _SIGS = {
     "moe_grouped_swiglu_fwd_fp8": (ctypes.c_int, [_CFG] + [_VP] * 14),
     "moe_grouped_swiglu_bwd_fp8": (ctypes.c_int, [_CFG] + [_VP] * 22 + [_SZ, _VP]),
     "moe_permute_quantize_e4m3": (ctypes.c_int, [_CFG] + [_VP] * 6),
+    "moe_mxfp8_scale_bytes": (_SZ, [_CFG, ctypes.c_int]),
+    "moe_quantize_mxfp8": (ctypes.c_int, [_VP, ctypes.c_int64, ctypes.c_int32, _VP, _VP, _VP]),
+    "moe_mxfp8_pack_expert_scales": (ctypes.c_int, [_CFG] + [_VP] * 5),
+    "moe_permute_quantize_mxfp8": (ctypes.c_int, [_CFG] + [_VP] * 6),
+    "moe_grouped_swiglu_fwd_mxfp8": (ctypes.c_int, [_CFG] + [_VP] * 13),
     "moe_unpermute_combine": (ctypes.c_int, [_CFG] + [_VP] * 7),
     "moe_unpermute_combine_bwd": (ctypes.c_int, [_CFG] + [_VP] * 11),
     "moe_layer_fwd": (ctypes.c_int, [_CFG] + [_VP] * 9 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP]),
@@ -231,6 +237,62 @@ def moe_grouped_swiglu_bwd_fp8(cfg, x_perm_q, x_scale, offsets, W1_q, W1_scale, 
         _p(dy_amax), _p(dH1), _p(dH1_q), _p(dH1_scale), _p(dH1_amax), _p(dx_perm), _p(dW1),
         _p(dW2), _p(ws), 0 if ws is None else ws.numel(), _stream(stream)),
         "moe_grouped_swiglu_bwd_fp8")
+
+
+def mxfp8_scale_bytes(cfg, which):
+    return lib().moe_mxfp8_scale_bytes(ctypes.byref(cfg), which)
+
+
+def moe_quantize_mxfp8(x, q, scales, stream=None):
+    """MXFP8 codes (uint8, x's shape) and row-major block scales (uint8 [..., cols/32]) of the bf16
+    tensor x along its last dimension."""
+    cols = x.shape[-1]
+    _check(lib().moe_quantize_mxfp8(_p(x), x.numel() // max(cols, 1), cols, _p(q), _p(scales),
+                                    _stream(stream)), "moe_quantize_mxfp8")
+
+
+def moe_mxfp8_pack_expert_scales(cfg, W1_s, W2_s, W1_sp, W2_sp, stream=None):
+    _check(lib().moe_mxfp8_pack_expert_scales(ctypes.byref(cfg), _p(W1_s), _p(W2_s), _p(W1_sp),
+                                              _p(W2_sp), _stream(stream)),
+           "moe_mxfp8_pack_expert_scales")
+
+
+def moe_permute_quantize_mxfp8(cfg, x, slot_of_pair, offsets, x_perm_q, x_perm_s, stream=None):
+    _check(lib().moe_permute_quantize_mxfp8(ctypes.byref(cfg), _p(x), _p(slot_of_pair), _p(offsets),
+                                            _p(x_perm_q), _p(x_perm_s), _stream(stream)),
+           "moe_permute_quantize_mxfp8")
+
+
+def moe_grouped_swiglu_fwd_mxfp8(cfg, x_perm_q, x_perm_s, offsets, W1_q, W1_sp, W2_q, W2_sp, h, act,
+                                 h_q, h_s, y_perm, stream=None):
+    _check(lib().moe_grouped_swiglu_fwd_mxfp8(
+        ctypes.byref(cfg), _p(x_perm_q), _p(x_perm_s), _p(offsets), _p(W1_q), _p(W1_sp), _p(W2_q),
+        _p(W2_sp), _p(h), _p(act), _p(h_q), _p(h_s), _p(y_perm), _stream(stream)),
+        "moe_grouped_swiglu_fwd_mxfp8")
+
+
+def alloc_mxfp8_experts(cfg, W1, W2, device="cuda", stream=None):
+    """MXFP8 state of the routed experts (torch tensors): W1 and W2 quantised once along their
+    reduction dimensions (codes, row-major scales and the packed scales the GEMMs read), and the
+    buffers the MXFP8 stage calls write."""
+    import torch
+    E, d, f = cfg.E, cfg.d, cfg.f
+    N = max(cfg.T, 1) * cfg.k
+    u8 = torch.uint8
+    m = dict(W1_q=torch.empty(E, 2 * f, d, dtype=u8, device=device),
+             W1_s=torch.empty(E, 2 * f, d // 32, dtype=u8, device=device),
+             W2_q=torch.empty(E, d, f, dtype=u8, device=device),
+             W2_s=torch.empty(E, d, f // 32, dtype=u8, device=device),
+             W1_sp=torch.empty(mxfp8_scale_bytes(cfg, MX_SCALES_W1), dtype=u8, device=device),
+             W2_sp=torch.empty(mxfp8_scale_bytes(cfg, MX_SCALES_W2), dtype=u8, device=device),
+             x_perm_q=torch.empty(N, d, dtype=u8, device=device),
+             x_perm_s=torch.empty(mxfp8_scale_bytes(cfg, MX_SCALES_X), dtype=u8, device=device),
+             h_q=torch.empty(N, f, dtype=u8, device=device),
+             h_s=torch.empty(mxfp8_scale_bytes(cfg, MX_SCALES_H), dtype=u8, device=device))
+    moe_quantize_mxfp8(W1, m["W1_q"], m["W1_s"], stream)
+    moe_quantize_mxfp8(W2, m["W2_q"], m["W2_s"], stream)
+    moe_mxfp8_pack_expert_scales(cfg, m["W1_s"], m["W2_s"], m["W1_sp"], m["W2_sp"], stream)
+    return m
 
 
 def moe_unpermute_combine(cfg, y_perm, gate, slot_of_pair, shared_out, shared_coef, y, stream=None):

@@ -661,7 +661,7 @@ using namespace moe;
 // ====================================================================== C ABI
 extern "C" {
 
-int moe_version(void) { return 102; }
+int moe_version(void) { return 103; }
 
 int moe_set_stream_overlap(int on) {
   const int prev = g_overlap.load();
@@ -964,6 +964,132 @@ int moe_grouped_swiglu_fwd_fp8(const moe_cfg* c, const uint8_t* x_perm_q, const 
   if (N == 0) return MOE_OK;
   return ffn_fwd_fp8_impl(c, c->E, offsets, Nrows(c), c->f, x_perm_q, x_scale, W1_q, W1_scale, W2_q, W2_scale, h, act,
                           h_q, h_scale, h_amax, y_perm, st);
+}
+
+// ------------------------------------------------------------------ MXFP8
+static int check_mx_cfg(const moe_cfg* c) {
+  MOE_TRY(check_cfg(c));
+  if (c->dtype != MOE_DTYPE_BF16)
+    return fail(MOE_ERR_UNSUPPORTED, "the MXFP8 path reads and writes bf16 activations (dtype bf16)");
+  if (c->d % 32 || c->f % 32)
+    return fail(MOE_ERR_UNSUPPORTED, "MXFP8 blocks need d and f multiples of 32");
+  return MOE_OK;
+}
+
+size_t moe_mxfp8_scale_bytes(const moe_cfg* c, int which) {
+  if (validate_cfg(c) != MOE_OK) return 0;
+  const int64_t N = Nrows(c);
+  switch (which) {
+    case MOE_MX_SCALES_X: return static_cast<size_t>(mx_act_scale_bytes(N, c->E, c->d));
+    case MOE_MX_SCALES_H: return static_cast<size_t>(mx_act_scale_bytes(N, c->E, c->f));
+    case MOE_MX_SCALES_W1:
+      return static_cast<size_t>(c->E) * mx_fc1_tiles(c->f) * mx_kch(c->d) * MX_SFB_BYTES;
+    case MOE_MX_SCALES_W2:
+      return static_cast<size_t>(c->E) * mx_fc2_tiles(c->d) * mx_kch(c->f) * MX_SFB_BYTES;
+    default: return 0;
+  }
+}
+
+int moe_quantize_mxfp8(const void* x, int64_t rows, int32_t cols, uint8_t* q, uint8_t* scales,
+                       void* stream) {
+  if (rows < 0 || cols < 0)
+    return fail(MOE_ERR_INVALID_ARG, "rows=%lld cols=%d", static_cast<long long>(rows), cols);
+  if (cols % 32) return fail(MOE_ERR_UNSUPPORTED, "cols must be a multiple of 32 (MXFP8 blocks)");
+  MOE_TRY(check_ptr(x, "x", true));
+  MOE_TRY(check_ptr(q, "q", true));
+  MOE_TRY(validate_ptr(scales, "scales", true));
+  return launch_mx_quantize(x, rows, cols, q, scales, S(stream));
+}
+
+int moe_mxfp8_pack_expert_scales(const moe_cfg* c, const uint8_t* W1_s, const uint8_t* W2_s,
+                                 uint8_t* W1_sp, uint8_t* W2_sp, void* stream) {
+  MOE_TRY(check_mx_cfg(c));
+  MOE_TRY(validate_ptr(W1_s, "W1_s", true));
+  MOE_TRY(validate_ptr(W2_s, "W2_s", true));
+  MOE_TRY(check_ptr(W1_sp, "W1_sp", true));
+  MOE_TRY(check_ptr(W2_sp, "W2_sp", true));
+  cudaStream_t st = S(stream);
+  MOE_TRY(launch_mx_pack_weight_scales(W1_s, c->E, 2 * c->f, c->d, c->f, W1_sp, st));
+  return launch_mx_pack_weight_scales(W2_s, c->E, c->d, c->f, 0, W2_sp, st);
+}
+
+int moe_permute_quantize_mxfp8(const moe_cfg* c, const void* x, const int32_t* slot_of_pair,
+                               const int32_t* offsets, uint8_t* x_perm_q, uint8_t* x_perm_s,
+                               void* stream) {
+  MOE_TRY(check_mx_cfg(c));
+  MOE_TRY(check_ptr(x, "x", true));
+  MOE_TRY(check_ptr(slot_of_pair, "slot_of_pair", true));
+  MOE_TRY(check_ptr(offsets, "offsets", true));
+  MOE_TRY(check_ptr(x_perm_q, "x_perm_q", true));
+  MOE_TRY(check_ptr(x_perm_s, "x_perm_s", true));
+  if (c->T == 0) return MOE_OK;
+  return launch_permute_quant_mx(x, slot_of_pair, offsets, x_perm_q, x_perm_s, c->T, c->d, c->k,
+                                 c->E, S(stream));
+}
+
+int moe_grouped_swiglu_fwd_mxfp8(const moe_cfg* c, const uint8_t* x_perm_q,
+                                 const uint8_t* x_perm_s, const int32_t* offsets,
+                                 const uint8_t* W1_q, const uint8_t* W1_sp, const uint8_t* W2_q,
+                                 const uint8_t* W2_sp, void* h, void* act, uint8_t* h_q,
+                                 uint8_t* h_s, void* y_perm, void* stream) {
+  MOE_TRY(check_mx_cfg(c));
+  const struct { const void* p; const char* n; } req[] = {
+      {x_perm_q, "x_perm_q"}, {x_perm_s, "x_perm_s"}, {offsets, "offsets"}, {W1_q, "W1_q"},
+      {W1_sp, "W1_sp"},       {W2_q, "W2_q"},         {W2_sp, "W2_sp"},     {h_q, "h_q"},
+      {h_s, "h_s"},           {y_perm, "y_perm"}};
+  for (const auto& r : req) MOE_TRY(check_ptr(r.p, r.n, true));
+  MOE_TRY(check_ptr(h, "h", false));
+  MOE_TRY(check_ptr(act, "act", false));
+  cudaStream_t st = S(stream);
+  const int64_t N = Nrows(c);
+  if (N == 0) return MOE_OK;
+  const int d = c->d, f = c->f, E = c->E;
+  // fc1 + SwiGLU on MXFP8 operands -> h codes and block scales (and bf16 h, [a | u] if asked)
+  GemmDesc g1 = desc0();
+  g1.name = "gemm_fc1_swiglu_mxfp8";
+  g1.sched = RAGGED_M;
+  g1.epi = EPI_SWIGLU_FWD;
+  g1.G = E;
+  g1.offsets = offsets;
+  g1.M = static_cast<int>(N);
+  g1.N = 2 * f;
+  g1.K = d;
+  g1.A = opnd(x_perm_q, N, d, false);
+  g1.B = opnd(W1_q, static_cast<int64_t>(E) * 2 * f, d, false);
+  g1.b_group_rows = 2 * f;
+  g1.b_up_rows = f;
+  g1.f = f;
+  g1.out = h;
+  g1.ldo = f;
+  g1.out2 = act;
+  g1.ldo2 = 2 * f;
+  g1.fp8 = true;
+  g1.mx = true;
+  g1.sfa = x_perm_s;
+  g1.sfb = W1_sp;
+  g1.q_out = h_q;
+  g1.q_sf = h_s;
+  MOE_TRY(gemm_tc(g1, st));
+  // fc2 on MXFP8 operands -> y_perm (bf16)
+  GemmDesc g2 = desc0();
+  g2.name = "gemm_fc2_mxfp8";
+  g2.sched = RAGGED_M;
+  g2.epi = EPI_STORE;
+  g2.G = E;
+  g2.offsets = offsets;
+  g2.M = static_cast<int>(N);
+  g2.N = d;
+  g2.K = f;
+  g2.A = opnd(h_q, N, f, false);
+  g2.B = opnd(W2_q, static_cast<int64_t>(E) * d, f, false);
+  g2.b_group_rows = d;
+  g2.out = y_perm;
+  g2.ldo = d;
+  g2.fp8 = true;
+  g2.mx = true;
+  g2.sfa = h_s;
+  g2.sfb = W2_sp;
+  return gemm_tc(g2, st);
 }
 
 int moe_grouped_swiglu_bwd_fp8(const moe_cfg* c, const uint8_t* x_perm_q, const float* x_scale,

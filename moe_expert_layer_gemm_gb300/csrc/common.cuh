@@ -107,4 +107,25 @@ __device__ __forceinline__ float warp_max(float v) {
 
 __device__ __forceinline__ float sigmoid_f(float z) { return 1.0f / (1.0f + expf(-z)); }
 
+// Two fp32 values -> two E4M3 codes (lo in the low byte): round to nearest even, saturating at
+// +-448.
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Shared exponent of an MXFP8 block with largest magnitude amax: floor(log2(amax)) - 8 (8: the
+// exponent of E4M3's largest normal, 448 = 1.75 * 2^8), clamped to [-127, 127]; -127 for 0 (and
+// for subnormal amax, whose floor(log2) is below -126).  Read off the fp32 exponent field.
+__device__ __forceinline__ int mx_exponent(float amax) {
+  const int fe = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+  return fe == 0 ? -127 : max(fe - 135, -127);
+}
+// 2^-e for a shared exponent e from mx_exponent of a finite amax (e in [-127, 119]): an exact
+// power of two and a normal fp32 value.
+__device__ __forceinline__ float mx_inv_scale(int e) {
+  return __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+}
+
 }  // namespace moe

@@ -15,13 +15,6 @@ namespace {
 
 constexpr float E4M3_MAX = 448.0f;
 
-// Two fp32 values -> two E4M3 codes (lo in the low byte).
-__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 // amax of each group: grid (blocks, groups); 8 bf16 per 16-byte load.
 __global__ void __launch_bounds__(256) amax_kernel(const bf16* __restrict__ x, int64_t per_group,
                                                    unsigned int* __restrict__ amax_bits) {

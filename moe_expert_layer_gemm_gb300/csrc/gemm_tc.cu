@@ -144,20 +144,39 @@ template <int BN, int SCHED, int EPI, bool F8 = false> struct EpiWidth {
   static constexpr int slabs = SlabsPerWarp<SCHED, EPI, warps>::n;
 };
 
-template <int BN, bool TMA_OUT, int EPI_WARPS, int SLABS> struct TileCfg {
+// SFS: bytes of MXFP8 block scales per stage (0 without); MAXST: most stages the ring may have.
+template <int BN, bool TMA_OUT, int EPI_WARPS, int SLABS, int SFS = 0, int MAXST = 6>
+struct TileCfg {
   static constexpr int B_STAGE = BN * BK * 2;
   static constexpr int STAGING = TMA_OUT ? EPI_WARPS * SLABS * SLAB : 0;
   static constexpr int AUX = 3072;   // barriers, TMEM address, flags, group tables
   static constexpr int MAX_SMEM = 232448;   // opt-in dynamic shared memory per block
-  static constexpr int FIT = (MAX_SMEM - STAGING - AUX) / (A_STAGE + B_STAGE);
-  static constexpr int STAGES = FIT < 6 ? FIT : 6;
+  static constexpr int FIT = (MAX_SMEM - STAGING - AUX) / (A_STAGE + B_STAGE + SFS);
+  static constexpr int STAGES = FIT < MAXST ? FIT : MAXST;
   static constexpr int RING = STAGES * (A_STAGE + B_STAGE);
-  static constexpr int SMEM = RING + STAGING + AUX;
+  static constexpr int SF_RING = STAGES * SFS;   // after the staging slabs
+  static constexpr int SMEM = RING + STAGING + SF_RING + AUX;
   // two accumulators of BN columns; allocations are powers of two of at least 32 columns
   static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
                                  : 2 * BN <= 256 ? 256 : 512;
   static constexpr int ACC_STRIDE = TMEM_COLS / 2;   // column of accumulator 1 (aligned)
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+};
+
+// MXFP8 tiles: two accumulators of BN columns, then a 16-column TMEM slot per ring stage for the
+// stage's block scales (A: 4 columns, B: 4 per 128 rows of the tile, at +8).  With BN = 192 the
+// 512 columns hold both accumulators (0..191, 256..447) and four stages' scales (448..511).
+constexpr int MX_SF_COLS = 16;
+template <int BN> struct MxCfg {
+  static constexpr int SF_STAGE = MX_CHUNK + MX_SFB_BYTES;   // A chunk, then B chunks
+  static constexpr int ACC_STRIDE = 2 * BN <= 256 ? 128 : 256;
+  static constexpr int SF_COL0 = ACC_STRIDE + BN;
+  static constexpr int MAX_STAGES = (512 - SF_COL0) / MX_SF_COLS;
+};
+template <int BN, int SCHED, int EPI, bool F8, bool MX> struct CfgOf {
+  using type = TileCfg<BN, OutPath<SCHED, EPI>::tma, EpiWidth<BN, SCHED, EPI, F8>::warps,
+                       EpiWidth<BN, SCHED, EPI, F8>::slabs, MX ? MxCfg<BN>::SF_STAGE : 0,
+                       MX ? MxCfg<BN>::MAX_STAGES : 6>;
 };
 
 struct KArgs {
@@ -180,11 +199,18 @@ struct KArgs {
   const float* b_scale;    // FP8: dequantisation scale of B, one per group
   int b_scale_per_group;   // FP8: 0 -> b_scale[0] for every group
   float* amax_out;         // FP8 SwiGLU epilogues: max |h| or |[da | du]| (fp32 bits, raised)
+  const uint8_t* sfa;      // MXFP8: packed block scales of A (activation layout)
+  const uint8_t* sfb;      // MXFP8: packed block scales of B (weight layout)
+  uint8_t* q_out;          // MXFP8 SwiGLU forward: h codes [rows, f]
+  uint8_t* q_sf;           // MXFP8 SwiGLU forward: h block scales (activation layout)
+  int kch;                 // MXFP8: 128-element K chunks of the operands
+  int kch_out;             // MXFP8 SwiGLU forward: 128-element chunks of h's rows
   int* err;
 };
 
 struct TileInfo {
   int g, m0, m_end, n0, k0, k_end, kblocks;
+  int mt, nt;   // RAGGED_M: row tile (over all groups) and column tile
 };
 
 __device__ __forceinline__ float silu_f(float a) { return a / (1.0f + __expf(-a)); }
@@ -230,6 +256,8 @@ struct Sched {
       ti.n0 = nt * (EPI == EPI_SWIGLU_FWD ? BN / 2 : BN);
       ti.k0 = 0;
       ti.k_end = p.K;
+      ti.mt = mt;
+      ti.nt = nt;
     } else {
       const int mtc = (p.M + TBM - 1) / TBM;
       const int per = mtc * nt_count;
@@ -242,6 +270,8 @@ struct Sched {
       ti.n0 = nt * BN;
       ti.k0 = s_off[ti.g];
       ti.k_end = s_off[ti.g + 1];
+      ti.mt = mt;
+      ti.nt = nt;
     }
     ti.kblocks = (ti.k_end - ti.k0 + BKE - 1) / BKE;
     return ti;
@@ -277,7 +307,8 @@ __device__ __forceinline__ void slab_store_3d(const CUtensorMap* m, const uint8_
   }
 }
 
-template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, bool GATHER = false, bool F8 = false>
+template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, bool GATHER = false, bool F8 = false,
+          bool MX = false>
 __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
@@ -285,7 +316,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
   constexpr bool TMA_OUT = OutPath<SCHED, EPI>::tma;
   constexpr int EPI_WARPS = EpiWidth<BN, SCHED, EPI, F8>::warps;
   constexpr int SLABS = EpiWidth<BN, SCHED, EPI, F8>::slabs;
-  using C = TileCfg<BN, TMA_OUT, EPI_WARPS, SLABS>;
+  using C = typename CfgOf<BN, SCHED, EPI, F8, MX>::type;
   constexpr bool MC = McMode<SCHED, EPI>::on;
   constexpr bool DYN = DynMode<SCHED, EPI>::on;
   static_assert(!MC || BN % 128 == 0, "cluster pairs split B in 128-row halves");
@@ -300,14 +331,20 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
   constexpr int MNW = F8 ? 128 : 64;
   constexpr int MN_CHUNK = BKE * 128;   // bytes of one such chunk in a stage
   static_assert(!F8 || (!GATHER && !MC), "FP8 operands: no gathered or cluster-shared loads");
+  // MXFP8: K-major E4M3 operands of a row-ragged product; one stage is one 128-element K chunk
+  static_assert(!MX || (F8 && SCHED == RAGGED_M && !A_MN && !B_MN && BN <= 256 &&
+                        C::ACC_STRIDE == MxCfg<BN>::ACC_STRIDE &&
+                        MxCfg<BN>::SF_COL0 + C::STAGES * MX_SF_COLS <= C::TMEM_COLS),
+                "MXFP8 tile configuration");
   constexpr int STAGES = C::STAGES;
-  constexpr uint32_t STAGE_TX = A_STAGE + C::B_STAGE;
+  constexpr uint32_t STAGE_TX = A_STAGE + C::B_STAGE + (MX ? MxCfg<BN>::SF_STAGE : 0);
 
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_STAGE;
   uint8_t* staging = smem + C::RING;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING + C::STAGING);
+  uint8_t* sSF = smem + C::RING + C::STAGING;   // MXFP8 block scales, one slot per stage
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING + C::STAGING + C::SF_RING);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -598,6 +635,15 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
             for (int c = 0; c < BN / MNW; ++c) box(b_dst + c * MN_CHUNK, &tmB, ti.n0 + MNW * c, krow);
           }
         }
+        if (MX) {
+          // this K chunk's block scales: the A row tile's chunk, then the B tile's chunks
+          uint8_t* sf_dst = sSF + stg * MxCfg<BN>::SF_STAGE;
+          ptx::bulk_load(sf_dst, p.sfa + (static_cast<int64_t>(ti.mt) * p.kch + kb) * MX_CHUNK,
+                         MX_CHUNK, &full[stg]);
+          const int64_t wt = static_cast<int64_t>(ti.g) * S::n_tiles(p) + ti.nt;
+          ptx::bulk_load(sf_dst + MX_CHUNK, p.sfb + (wt * p.kch + kb) * MX_SFB_BYTES, MX_SFB_BYTES,
+                         &full[stg]);
+        }
       };
       // Run-time tiles: the next tile is claimed before the current one's loads are issued,
       // hiding the atomic's latency; -1 once the list is exhausted.
@@ -700,6 +746,18 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
         ptx::tc_fence_after();
         if (lane == 0) {
           const uint32_t a_addr = ptx::smem_u32(a_src), b_addr = ptx::smem_u32(b_src);
+          // MXFP8: the stage's block scales into its TMEM slot (the copies and the MMAs below
+          // execute in issue order; the slot's previous MMAs finished before this stage was
+          // refilled, as they released it)
+          const uint32_t sf_t = tmem_base + static_cast<uint32_t>(MX ? MxCfg<BN>::SF_COL0 + stage * MX_SF_COLS : 0);
+          if (MX) {
+            const uint32_t sf_s = ptx::smem_u32(sSF + stage * MxCfg<BN>::SF_STAGE);
+            ptx::tmem_cp_32x128_x4(sf_t, ptx::smem_desc_plain(sf_s, 128));
+#pragma unroll
+            for (int ch = 0; ch < MX_SFB_CHUNKS; ++ch)
+              ptx::tmem_cp_32x128_x4(sf_t + 8 + 4 * ch,
+                                     ptx::smem_desc_plain(sf_s + MX_CHUNK * (1 + ch), 128));
+          }
 #pragma unroll
           for (int k16 = 0; k16 < BK / 16; ++k16) {
             if (!a_live) break;
@@ -710,7 +768,10 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
                                      : ptx::smem_desc_sw128(a_addr + k16 * 32, 16, 1024);
             const uint64_t bd = B_MN ? ptx::smem_desc_sw128(b_addr + k16 * MN_KSTEP, MN_CHUNK, 1024)
                                      : ptx::smem_desc_sw128(b_addr + k16 * 32, 16, 1024);
-            if (F8) ptx::umma_f8(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
+            if (MX)   // K slice k16 of the chunk: byte k16 of each row's scale column
+              ptx::umma_mx(d_tmem, ad, bd, ptx::idesc_mx_e4m3(BM, BN, A_MN, B_MN, k16, k16), sf_t,
+                           sf_t + 8, (kb | k16) != 0 ? 1u : 0u);
+            else if (F8) ptx::umma_f8(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
             else ptx::umma_bf16(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
           }
           // frees the smem stage (in both CTAs of a cluster) when these MMAs finish
@@ -831,10 +892,11 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
       // written with masked stores instead.
       const bool tma_slab = TMA_OUT && (SCHED == RAGGED_K ? rows_here > 0 : rows_here == 32);
       // FP8: the accumulator holds products of decoded E4M3 values; both scales apply here
-      const float sc = F8 ? __ldg(p.a_scale) * __ldg(p.b_scale + (p.b_scale_per_group ? ti.g : 0)) : 1.0f;
+      // (MXFP8: the block scales were applied by the MMAs)
+      const float sc = F8 && !MX ? __ldg(p.a_scale) * __ldg(p.b_scale + (p.b_scale_per_group ? ti.g : 0)) : 1.0f;
       // FP8 SwiGLU epilogues: max |.| over this warp's stored (bf16) values of h (forward) or
       // [da | du] (backward), for that tensor's own quantisation
-      constexpr bool AMAX = F8 && (EPI == EPI_SWIGLU_FWD || EPI == EPI_SWIGLU_BWD);
+      constexpr bool AMAX = F8 && !MX && (EPI == EPI_SWIGLU_FWD || EPI == EPI_SWIGLU_BWD);
       float hmax = 0.f;
       auto track = [&](float v) {
         if (AMAX) hmax = fmaxf(hmax, fabsf(__bfloat162float(__float2bfloat16_rn(v))));
@@ -843,6 +905,69 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
 
       if (rows_here <= 0) {
         // no row of this slab exists
+      } else if (MX && EPI == EPI_SWIGLU_FWD) {
+        // h quantised to MXFP8 where it is made: a thread holds 32 consecutive h values of its
+        // row (one block along f, fc2's reduction dimension), rounded to bf16 first.  Codes and
+        // the block's scale byte go straight out (32 bytes and 1 byte per block); bf16 h and
+        // [a | u] only if asked for.
+        bf16* hrow = p.out ? static_cast<bf16*>(p.out) + row * p.ldo : nullptr;
+        bf16* arow = p.out2 ? static_cast<bf16*>(p.out2) + row * p.ldo2 : nullptr;
+        uint8_t* qrow = p.q_out + static_cast<int64_t>(row) * p.f;
+        uint8_t* sfrow = p.q_sf + static_cast<int64_t>(ti.mt) * p.kch_out * MX_CHUNK + (r & 31) * 16 +
+                         (r >> 5) * 4;
+#pragma unroll 1
+        for (int c = c_lo; c < c_hi; c += 32) {
+          const int col = ti.n0 + c;
+          if (col >= p.f) break;
+          uint32_t ga[32], up[32];
+          ptx::tmem_ld32(t_row + c, ga);
+          ptx::tmem_ld32(t_row + BN / 2 + c, up);
+          ptx::tmem_ld_wait();
+          if (!valid) continue;
+          float hv[32];
+          float am = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            hv[i] = __bfloat162float(__float2bfloat16_rn(
+                silu_f(__uint_as_float(ga[i])) * __uint_as_float(up[i])));
+            am = fmaxf(am, fabsf(hv[i]));
+          }
+          const int ex = mx_exponent(am);
+          const float inv = mx_inv_scale(ex);
+          uint32_t w[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t lo = cvt_e4m3x2(hv[4 * j] * inv, hv[4 * j + 1] * inv);
+            const uint32_t hi = cvt_e4m3x2(hv[4 * j + 2] * inv, hv[4 * j + 3] * inv);
+            w[j] = lo | (hi << 16);
+          }
+          *reinterpret_cast<uint4*>(qrow + col) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(qrow + col + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+          const int blk = col >> 5;
+          uint8_t* sf = sfrow + (blk >> 2) * MX_CHUNK;
+          sf[blk & 3] = static_cast<uint8_t>(ex + 127);
+          if (col + 32 >= p.f) {
+            for (int j = (blk & 3) + 1; j < 4; ++j) sf[j] = 127;   // blocks past f: 2^0
+          }
+          if (hrow) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              st16(hrow + col + v * 8, pack16(hv + 8 * v, static_cast<const bf16*>(nullptr)));
+          }
+          if (arow) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float av[8], uv[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                av[i] = __uint_as_float(ga[8 * v + i]);
+                uv[i] = __uint_as_float(up[8 * v + i]);
+              }
+              st16(arow + col + v * 8, pack16(av, static_cast<const bf16*>(nullptr)));
+              st16(arow + p.f + col + v * 8, pack16(uv, static_cast<const bf16*>(nullptr)));
+            }
+          }
+        }
       } else if (tma_slab && EPI == EPI_STORE) {
 #pragma unroll 1
         for (int c = c_lo; c < c_hi; c += 64) {
@@ -1672,13 +1797,12 @@ int map_operand(CUtensorMap* m, const Operand& op, int box_rows, bool f8 = false
             : map_bf16(m, op.base, op.rows, op.cols, op.ld, box_rows);
 }
 
-template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, bool GATHER = false, bool F8 = false>
+template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, bool GATHER = false, bool F8 = false,
+          bool MX = false>
 int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   const char* name = g.name ? g.name : kind;
-  constexpr bool TMA_OUT = OutPath<SCHED, EPI>::tma;
-  using C = TileCfg<BN, TMA_OUT, EpiWidth<BN, SCHED, EPI, F8>::warps,
-                    EpiWidth<BN, SCHED, EPI, F8>::slabs>;
-  auto kern = tc_gemm_kernel<BN, A_MN, B_MN, SCHED, EPI, GATHER, F8>;
+  using C = typename CfgOf<BN, SCHED, EPI, F8, MX>::type;
+  auto kern = tc_gemm_kernel<BN, A_MN, B_MN, SCHED, EPI, GATHER, F8, MX>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [&] {
@@ -1704,7 +1828,7 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
     MOE_TRY(map_bf16(&mo[0], g.out, rows, g.N, g.ldo, 32));
   } else if (EPI == EPI_F32 && SCHED == RAGGED_K) {
     MOE_TRY(map_f32_3d(&mo[0], g.out, g.G, g.M, g.N, g.ldo, g.out_group_stride));
-  } else if (EPI == EPI_SWIGLU_FWD) {
+  } else if (EPI == EPI_SWIGLU_FWD && !MX) {   // (MXFP8: direct stores, no maps)
     MOE_TRY(map_bf16(&mo[0], g.out, rows, g.f, g.ldo, 32));
     if (g.out2) {
       MOE_TRY(map_bf16(&mo[1], g.out2, rows, g.f, g.ldo2, 32));
@@ -1739,9 +1863,26 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   a.b_scale = g.b_scale;
   a.b_scale_per_group = g.b_scale_scalar ? 0 : 1;
   a.amax_out = g.amax_out;
-  if (F8 && (!g.a_scale || !g.b_scale)) {
+  a.sfa = g.sfa;
+  a.sfb = g.sfb;
+  a.q_out = g.q_out;
+  a.q_sf = g.q_sf;
+  a.kch = static_cast<int>(mx_kch(g.K));
+  a.kch_out = static_cast<int>(mx_kch(g.f));
+  if (F8 && !MX && (!g.a_scale || !g.b_scale)) {
     set_error("%s: FP8 operands need their scales", name);
     return MOE_ERR_INVALID_ARG;
+  }
+  if (MX) {
+    const bool aligned = (reinterpret_cast<uintptr_t>(g.sfa) & 15u) == 0 &&
+                         (reinterpret_cast<uintptr_t>(g.sfb) & 15u) == 0;
+    if (!g.sfa || !g.sfb || !aligned || g.K % 32 != 0 ||
+        (EPI == EPI_SWIGLU_FWD && (!g.q_out || !g.q_sf || g.f % 32 != 0 ||
+                                   (reinterpret_cast<uintptr_t>(g.q_out) & 15u) != 0))) {
+      set_error("%s: MXFP8 operands need 16-byte aligned block scales, K (and f) multiples of 32 "
+                "and, for SwiGLU, h's code and scale buffers", name);
+      return MOE_ERR_INVALID_ARG;
+    }
   }
   a.err = device_error_word();
   if (GATHER != (g.gather != nullptr)) {
@@ -1812,6 +1953,20 @@ int run_wgrad_pair(const GemmDesc& g, cudaStream_t st) {
 int gemm_tc(const GemmDesc& g, cudaStream_t st) {
   if (g.G < 1 || g.G > MAXG) {
     set_error("gemm_tc: group count %d outside [1, %d]", g.G, MAXG);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (g.fp8 && g.mx) {
+    // MXFP8 operands: the expert products of the forward
+    if (!g.gather && g.sched == RAGGED_M && !g.A.mn_major && !g.B.mn_major) {
+      if (g.epi == EPI_SWIGLU_FWD)
+        return run<MX_BN, false, false, RAGGED_M, EPI_SWIGLU_FWD, false, true, true>(
+            g, "gemm_fc1_swiglu_mxfp8", st);
+      if (g.epi == EPI_STORE)
+        return run<MX_BN, false, false, RAGGED_M, EPI_STORE, false, true, true>(g, "gemm_fc2_mxfp8",
+                                                                               st);
+    }
+    set_error("gemm_tc: unsupported MXFP8 combination sched=%d epi=%d a_mn=%d b_mn=%d", g.sched,
+              g.epi, (int)g.A.mn_major, (int)g.B.mn_major);
     return MOE_ERR_UNSUPPORTED;
   }
   if (g.fp8) {

@@ -172,7 +172,43 @@ struct GemmDesc {
   bool b_scale_scalar;
   float* amax_out;         // FP8 SwiGLU forward / backward: receives max |h| or max |[da | du]|
                            // over the bf16 values written (zeroed by the caller)
+  // MXFP8 operands (with fp8): E4M3 codes whose E8M0 block scales (one per 32 K-elements of each
+  // row) sfa / sfb hold in the packed layouts below; the MMAs apply them, the epilogue none.
+  bool mx;
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  // MXFP8 SwiGLU forward: h as MXFP8 codes [rows, f] and its packed block scales (the A-operand
+  // layout, row tiles as this product's); `out` (bf16 h) and `out2` ([a | u]) may be null.
+  uint8_t* q_out;
+  uint8_t* q_sf;
 };
+
+// ------------------------------------------------------------------ MXFP8 packed scales
+// Block scales of 128 operand rows x 128 K-elements (four 32-blocks per row) form one 512-byte
+// chunk in the order the tensor cores read them from TMEM: the scale of row r, block j sits at
+// byte (r % 32) * 16 + (r / 32) * 4 + j.
+//   activation operand [N rows, K]: chunk (mt, kc) at (mt * kch + kc) * 512, where mt is the row
+//     tile -- the tiles of earlier experts (sum of ceil(rows_e / 128)) plus the row's offset
+//     inside its expert / 128 -- and kc = K-element / 128, kch = ceil(K / 128);
+//   weight operand: per expert e and output tile nt, for every kc, MX_SFB_CHUNKS chunks (tile rows
+//     0..127, 128..255) at ((e * NT + nt) * kch + kc) * MX_SFB_BYTES.  fc1 tile nt holds gate rows
+//     nt*96 .. +95 then up rows f + nt*96 .. +95 (NT = ceil(f / 96)); fc2 tile nt holds rows
+//     nt*192 .. +191 (NT = ceil(d / 192)).
+// Scales of rows or blocks past the operand's end are 127 (2^0) in weight chunks; activation
+// chunks leave rows past an expert's end unwritten (their products are never stored) and set
+// blocks past K to 127.
+constexpr int MX_BN = 192;                 // output columns of an MXFP8 tile
+constexpr int MX_CHUNK = 512;
+constexpr int MX_SFB_CHUNKS = (MX_BN + 127) / 128;
+constexpr int MX_SFB_BYTES = MX_SFB_CHUNKS * MX_CHUNK;
+inline int64_t mx_kch(int64_t K) { return (K + 127) / 128; }
+// an upper bound of sum_e ceil(rows_e / 128) for N rows over E experts
+inline int64_t mx_row_tiles(int64_t N, int E) { return (N + 127 * static_cast<int64_t>(E)) / 128 + 1; }
+inline int64_t mx_act_scale_bytes(int64_t N, int E, int64_t K) {
+  return mx_row_tiles(N, E) * mx_kch(K) * MX_CHUNK;
+}
+inline int64_t mx_fc1_tiles(int f) { return (f + MX_BN / 2 - 1) / (MX_BN / 2); }
+inline int64_t mx_fc2_tiles(int d) { return (d + MX_BN - 1) / MX_BN; }
 
 // Argument checks and the routing stages (capi.cu), for entry points defined elsewhere.
 int validate_cfg(const moe_cfg* c);
@@ -192,6 +228,19 @@ int launch_quant_e4m3_given_amax(const void* x, int64_t per_group, int groups, u
 // (and x_q[t], the same codes in token order, if x_q is not NULL).
 int launch_permute_quant_e4m3(const void* x, const int32_t* sop, uint8_t* xq, uint8_t* x_q,
                               float* scale, float* amax, int T, int d, int k, cudaStream_t st);
+
+// MXFP8 quantisation (mxfp8.cu).  Rows of `cols` bf16 values (cols % 32 == 0) -> E4M3 codes and
+// row-major E8M0 scales [rows, cols / 32].
+int launch_mx_quantize(const void* x, int64_t rows, int cols, uint8_t* q, uint8_t* s,
+                       cudaStream_t st);
+// Row-major weight scales [E, R, K / 32] -> the packed weight layout; swiglu_f > 0: fc1 tiles
+// over R = 2 * swiglu_f rows, 0: fc2 tiles over R rows.
+int launch_mx_pack_weight_scales(const uint8_t* s, int E, int R, int K, int swiglu_f,
+                                 uint8_t* packed, cudaStream_t st);
+// Permute + quantise: x_perm_q[slot(t, j)] = MXFP8 codes of x[t], scales in the packed
+// activation layout (row tiles from the routing offsets).
+int launch_permute_quant_mx(const void* x, const int32_t* sop, const int32_t* offsets,
+                            uint8_t* xq, uint8_t* xs, int T, int d, int k, int E, cudaStream_t st);
 
 int gemm_tc(const GemmDesc& g, cudaStream_t st);     // bf16 tcgen05 path (gemm_tc.cu)
 int gemm_simt(const GemmDesc& g, cudaStream_t st);   // fp32 CUDA-core path (gemm_simt.cu)

@@ -228,6 +228,16 @@ __device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const void* des
       "l"(reinterpret_cast<uint64_t>(desc)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "l"(policy)
       : "memory");
 }
+// Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
+// to shared memory, completing on `bar`'s transaction count.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -288,6 +298,55 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn, b
          | ((b_mn ? 1u : 0u) << 16)                  // B major
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale: E4M3 x E4M3 -> fp32 with
+// one E8M0 scale per 32 K-elements of every row of A and of B.  The accumulator is always fp32
+// (no D-format field); bits 4-5 and 29-30 pick the byte of each 32-bit scale column that this
+// instruction's K = 32 slice uses, bit 23 selects E8M0 scales.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N, bool a_mn, bool b_mn,
+                                                     int sfa_id, int sfb_id) {
+  return (static_cast<uint32_t>(sfb_id) << 4)       // B scale byte
+         | (0u << 7)                                 // A format: E4M3
+         | (0u << 10)                                // B format: E4M3
+         | ((a_mn ? 1u : 0u) << 15)                  // A major: 0 K, 1 MN
+         | ((b_mn ? 1u : 0u) << 16)                  // B major
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (1u << 23)                                // scale format: E8M0
+         | (static_cast<uint32_t>(M >> 4) << 24)     // M / 16
+         | (static_cast<uint32_t>(sfa_id) << 29);    // A scale byte
+}
+
+// Shared-memory descriptor of an unswizzled K-major block of 16-byte rows (8-row core matrices,
+// SBO bytes apart): the source of tcgen05.cp.
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t addr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;   // descriptor version for tcgen05
+  return d;
+}
+
+// Copy 32 rows x 16 bytes of shared memory into 4 TMEM columns of lanes 0-31, replicated into
+// the other three lane quadrants (the layout block-scaled MMAs read their scales from: scale
+// byte j of row r of a 128-row group sits in lane r % 32, column r / 32, byte j).
+__device__ __forceinline__ void tmem_cp_32x128_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// D(tmem) (+)= (A . diag-blocks(sfa)) x (B . diag-blocks(sfb))^T on E4M3 with E8M0 block scales
+// read from TMEM (K = 32 per instruction), one thread.
+__device__ __forceinline__ void umma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* smem_result, uint32_t ncols) {

@@ -165,3 +165,61 @@ def compare_layer(lc, gpu, ref, tol, backward=True, order_keys=None):
                 continue
             errs[n] = assert_close(n, np64(gpu[n]), b[n], tol)
     return errs
+
+
+# ----------------------------------------------------------------------------- MXFP8 layouts
+# The packed block-scale layouts of the C ABI (include/moe_gb300.h, MOE_MX_SCALES_*), restated
+# here from that documentation to read the GPU's buffers back into row-major [rows, K/32] scales.
+
+def mx_unpack_act_scales(packed, offsets, N, K):
+    """Row-major scales [N, K/32] of the permuted rows from the MOE_MX_SCALES_X/_H layout."""
+    packed = np.asarray(packed)
+    off = np.asarray(offsets, np.int64)
+    kch, nb = (K + 127) // 128, K // 32
+    pre = np.concatenate([[0], np.cumsum((np.diff(off) + 127) // 128)])
+    s = np.arange(N)
+    e = np.searchsorted(off, s, side="right") - 1          # the expert that holds row s
+    rr = s - off[e]
+    mt = pre[e] + rr // 128
+    b = np.arange(nb)
+    r = rr % 128
+    idx = (mt[:, None] * kch + b[None, :] // 4) * 512 + (r % 32)[:, None] * 16 + \
+        (r // 32)[:, None] * 4 + (b % 4)[None, :]
+    return packed[idx]
+
+
+def mx_act_pad_bytes(packed, offsets, N, K):
+    """The bytes of blocks past K in every row's last chunk (must all be 127)."""
+    off = np.asarray(offsets, np.int64)
+    kch, nb = (K + 127) // 128, K // 32
+    if nb % 4 == 0:
+        return np.array([127], np.uint8)
+    pre = np.concatenate([[0], np.cumsum((np.diff(off) + 127) // 128)])
+    s = np.arange(N)
+    e = np.searchsorted(off, s, side="right") - 1
+    rr = s - off[e]
+    mt = pre[e] + rr // 128
+    b = np.arange(nb % 4, 4)
+    idx = (mt[:, None] * kch + kch - 1) * 512 + ((rr % 128) % 32)[:, None] * 16 + \
+        ((rr % 128) // 32)[:, None] * 4 + b[None, :]
+    return np.asarray(packed)[idx]
+
+
+def mx_weight_index(E, R, K, swiglu_f):
+    """Index [E, R, K/32] into the packed weight layout (MOE_MX_SCALES_W1 with swiglu_f = f, R = 2f;
+    MOE_MX_SCALES_W2 with swiglu_f = 0)."""
+    kch, nb = (K + 127) // 128, K // 32
+    q = np.arange(R)
+    if swiglu_f:
+        hc = np.where(q < swiglu_f, q, q - swiglu_f)
+        t = hc // 96
+        rt = np.where(q < swiglu_f, hc % 96, 96 + hc % 96)
+        NT = (swiglu_f + 95) // 96
+    else:
+        t, rt = q // 192, q % 192
+        NT = (R + 191) // 192
+    e = np.arange(E)[:, None, None]
+    b = np.arange(nb)[None, None, :]
+    t, rt = t[None, :, None], rt[None, :, None]
+    return ((e * NT + t) * kch + b // 4) * 1024 + (rt // 128) * 512 + (rt % 32) * 16 + \
+        ((rt % 128) // 32) * 4 + b % 4

@@ -1,0 +1,189 @@
+"""MXFP8 (block-scaled E4M3) path on the GPU against the MXFP8 oracle, through the C ABI.
+
+  * moe_quantize_mxfp8: codes and E8M0 scale bytes bit-identical to the oracle's block
+    quantisation of the same bf16 values (the decisions are exact: a power-of-two division and
+    one E4M3 rounding);
+  * moe_mxfp8_pack_expert_scales: every scale at its documented place in the packed layout, and
+    every other byte 127;
+  * moe_permute_quantize_mxfp8: the codes of every permuted row equal the oracle's codes of its
+    token's row, and the packed scales read back equal the oracle's;
+  * moe_grouped_swiglu_fwd_mxfp8: [a | u] and h within the bf16 output tolerance of the oracle's
+    fp64 product of the same decoded operands; h's codes and scales bit-identical to the oracle's
+    quantisation of the GPU's bf16 h; y_perm within tolerance of the oracle's fc2 on those codes;
+    and against the unquantised bf16 experts within the format's rounding bound.
+Shapes cover several tiles with ragged tails, experts without rows, K not a multiple of 128 (a
+partial last scale chunk) and f not a multiple of the 96-column SwiGLU tile.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_expert_layer_gemm_gb300 as moe
+import oracle.moe_oracle as O
+import oracle.mxfp8_oracle as MX
+
+from .helpers import (assert_close, mx_act_pad_bytes, mx_unpack_act_scales, mx_weight_index, np64,
+                      rel_err)
+
+pytestmark = pytest.mark.gpu
+
+TOL_OUT = 1e-2   # bf16 outputs of an fp32-accumulated product of exact block-scaled E4M3 values
+
+
+def sync():
+    torch.cuda.synchronize()
+    moe.check_device_error()
+
+
+def varied(shape, seed, spread=4.0):
+    """bf16 values whose magnitude changes from one 32-block to the next (2^-spread .. 2^spread),
+    with some all-zero blocks."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(*shape, generator=g)
+    nb = shape[-1] // 32
+    mag = torch.exp2(torch.empty(*shape[:-1], nb).uniform_(-spread, spread, generator=g))
+    mag[..., ::7] = 0 if nb > 3 else mag[..., ::7]
+    return (x * mag.repeat_interleave(32, dim=-1)).bfloat16()
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 32), (100, 96), (513, 2688), (64, 1856)])
+def test_quantize_codes_and_scales_are_exact(rows, cols):
+    x = varied((rows, cols), rows + cols)
+    x[0, :4] = torch.tensor([480.0, -448.0, 1e-30, 0.0]).bfloat16()   # saturation, tiny, zero
+    q = torch.empty(rows, cols, dtype=torch.uint8, device="cuda")
+    s = torch.empty(rows, cols // 32, dtype=torch.uint8, device="cuda")
+    moe.moe_quantize_mxfp8(x.cuda(), q, s)
+    sync()
+    rq, rs = MX.mx_quantize(x.double().numpy())
+    assert np.array_equal(s.cpu().numpy(), rs)
+    assert np.array_equal(q.cpu().numpy(), rq)
+
+
+def mx_experts(cfg, seed, scale=0.05):
+    E, d, f = cfg.E, cfg.d, cfg.f
+    W1 = (varied((E, 2 * f, d), seed, 2.0).float() * scale).bfloat16().cuda()
+    W2 = (varied((E, d, f), seed + 1, 2.0).float() * scale).bfloat16().cuda()
+    m = moe.alloc_mxfp8_experts(cfg, W1, W2)
+    sync()
+    return W1, W2, m
+
+
+@pytest.mark.parametrize("E,d,f", [(3, 256, 160), (2, 2688, 1856), (4, 384, 96)])
+def test_packed_weight_scales_are_at_their_places(E, d, f):
+    cfg = moe.make_cfg(64, d, E, 2, f)
+    W1, W2, m = mx_experts(cfg, E + d)
+    rq1, rs1 = MX.mx_quantize(W1.double().cpu().numpy())
+    rq2, rs2 = MX.mx_quantize(W2.double().cpu().numpy())
+    assert np.array_equal(m["W1_q"].cpu().numpy(), rq1) and np.array_equal(m["W1_s"].cpu().numpy(), rs1)
+    assert np.array_equal(m["W2_q"].cpu().numpy(), rq2) and np.array_equal(m["W2_s"].cpu().numpy(), rs2)
+    for packed, rs, R, K, sf in ((m["W1_sp"], rs1, 2 * f, d, f), (m["W2_sp"], rs2, d, f, 0)):
+        p = packed.cpu().numpy()
+        idx = mx_weight_index(E, R, K, sf)
+        assert np.array_equal(p[idx], rs)
+        rest = np.ones(p.size, bool)
+        rest[idx.ravel()] = False
+        assert (p[rest] == 127).all()
+
+
+def routed(T, E, k, seed, empty=0):
+    g = torch.Generator().manual_seed(seed)
+    lg = torch.randn(T, E, generator=g)
+    if empty:
+        lg[:, E - empty:] = -1e4      # the last `empty` experts receive nothing
+    return O.route(lg.numpy(), k, E, O.SOFTMAX, 1)
+
+
+@pytest.mark.parametrize("T,d,E,k,empty", [(1000, 256, 16, 4, 3), (4097, 2048, 128, 8, 0),
+                                           (7, 64, 4, 1, 0), (300, 2688, 8, 6, 1)])
+def test_permute_quantize_mx(T, d, E, k, empty):
+    r = routed(T, E, k, T, empty)
+    x = varied((T, d), d).cuda()
+    cfg = moe.make_cfg(T, d, E, k, 64)
+    N = T * k
+    sop = torch.from_numpy(r["slot_of_pair"]).cuda()
+    off = torch.from_numpy(r["offsets"]).cuda()
+    xq = torch.empty(N, d, dtype=torch.uint8, device="cuda")
+    xs = torch.full((moe.mxfp8_scale_bytes(cfg, moe.MX_SCALES_X),), 0xEE, dtype=torch.uint8,
+                    device="cuda")
+    moe.moe_permute_quantize_mxfp8(cfg, x, sop, off, xq, xs)
+    sync()
+    rq, rs = MX.mx_quantize(x.double().cpu().numpy())
+    tos = r["token_of_slot"]
+    assert np.array_equal(xq.cpu().numpy(), rq[tos])
+    p = xs.cpu().numpy()
+    assert np.array_equal(mx_unpack_act_scales(p, r["offsets"], N, d), rs[tos])
+    assert (mx_act_pad_bytes(p, r["offsets"], N, d) == 127).all()
+
+
+@pytest.mark.parametrize("T,d,E,k,f,empty", [(600, 256, 8, 2, 160, 2), (1024, 2048, 128, 8, 768, 0),
+                                             (300, 384, 16, 4, 96, 5), (257, 2688, 8, 6, 1856, 0)])
+def test_mxfp8_grouped_swiglu_forward(T, d, E, k, f, empty):
+    r = routed(T, E, k, d + f, empty)
+    N = T * k
+    o = r["offsets"]
+    cfg = moe.make_cfg(T, d, E, k, f)
+    x = varied((T, d), T).cuda()
+    W1, W2, m = mx_experts(cfg, d)
+    sop = torch.from_numpy(r["slot_of_pair"]).cuda()
+    off = torch.from_numpy(o).cuda()
+    moe.moe_permute_quantize_mxfp8(cfg, x, sop, off, m["x_perm_q"], m["x_perm_s"])
+    bf = torch.bfloat16
+    h = torch.empty(N, f, dtype=bf, device="cuda")
+    act = torch.empty(N, 2 * f, dtype=bf, device="cuda")
+    yp = torch.empty(N, d, dtype=bf, device="cuda")
+    moe.moe_grouped_swiglu_fwd_mxfp8(cfg, m["x_perm_q"], m["x_perm_s"], off, m["W1_q"], m["W1_sp"],
+                                     m["W2_q"], m["W2_sp"], h, act, m["h_q"], m["h_s"], yp)
+    sync()
+    xq = m["x_perm_q"].cpu().numpy()
+    xs = mx_unpack_act_scales(m["x_perm_s"].cpu().numpy(), o, N, d)
+    W1q, W1s = m["W1_q"].cpu().numpy(), m["W1_s"].cpu().numpy()
+    W2q, W2s = m["W2_q"].cpu().numpy(), m["W2_s"].cpu().numpy()
+    ref_h, ref_act = MX.fc1_swiglu_mx(xq, xs, W1q, W1s, o)
+    e_act = assert_close("act", np64(act), ref_act, TOL_OUT)
+    e_h = assert_close("h", np64(h), ref_h, TOL_OUT)
+    # h's codes and scales: the oracle's block quantisation of the GPU's (bf16) h
+    rq, rs = MX.mx_quantize(np64(h))
+    assert np.array_equal(m["h_q"].cpu().numpy(), rq)
+    hs = m["h_s"].cpu().numpy()
+    assert np.array_equal(mx_unpack_act_scales(hs, o, N, f), rs)
+    assert (mx_act_pad_bytes(hs, o, N, f) == 127).all()
+    ref_y = MX.fc2_mx(rq, rs, W2q, W2s, o)
+    e_y = assert_close("y_perm", np64(yp), ref_y, TOL_OUT)
+    # against the unquantised experts: four E4M3 roundings (x, W1, h, W2), each within 2^-4
+    # of its value (3 mantissa bits); on these inputs the result moves by 6-10%
+    X = np64(x)[r["token_of_slot"]]
+    y_bf = np.zeros((N, d))
+    for e in range(E):
+        sl = slice(o[e], o[e + 1])
+        if o[e + 1] > o[e]:
+            y_bf[sl] = O.swiglu_ffn(np64(W1[e]), np64(W2[e]), X[sl])[0]
+    e_q = rel_err(np64(yp), y_bf)
+    assert e_q < 0.25, e_q
+    print(f"act {e_act:.2e} h {e_h:.2e} y {e_y:.2e}; vs unquantised {e_q:.3f}")
+
+
+def test_mxfp8_forward_without_bf16_side_outputs_and_zero_tokens():
+    """h and [a | u] are optional (NULL): the codes and y_perm are the same; T = 0 is a no-op."""
+    T, d, E, k, f = 200, 256, 8, 2, 128
+    r = routed(T, E, k, 3)
+    cfg = moe.make_cfg(T, d, E, k, f)
+    x = varied((T, d), 5).cuda()
+    W1, W2, m = mx_experts(cfg, 9)
+    sop = torch.from_numpy(r["slot_of_pair"]).cuda()
+    off = torch.from_numpy(r["offsets"]).cuda()
+    moe.moe_permute_quantize_mxfp8(cfg, x, sop, off, m["x_perm_q"], m["x_perm_s"])
+    N = T * k
+    outs = []
+    for with_h in (True, False):
+        h = torch.empty(N, f, dtype=torch.bfloat16, device="cuda") if with_h else None
+        yp = torch.empty(N, d, dtype=torch.bfloat16, device="cuda")
+        moe.moe_grouped_swiglu_fwd_mxfp8(cfg, m["x_perm_q"], m["x_perm_s"], off, m["W1_q"],
+                                         m["W1_sp"], m["W2_q"], m["W2_sp"], h, None, m["h_q"],
+                                         m["h_s"], yp)
+        sync()
+        outs.append((m["h_q"].clone(), yp))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    cfg0 = moe.make_cfg(0, d, E, k, f)
+    moe.moe_grouped_swiglu_fwd_mxfp8(cfg0, m["x_perm_q"], m["x_perm_s"], off, m["W1_q"], m["W1_sp"],
+                                     m["W2_q"], m["W2_sp"], None, None, m["h_q"], m["h_s"], outs[0][1])
+    sync()
