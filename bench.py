@@ -609,6 +609,10 @@ def fp8_experts(args, lc, cfg, inp, saved, dev):
     ws16 = moe.workspace(cfg, moe.WS_FFN_BWD, dev)
     ws8 = moe.workspace(cfg, moe.WS_FFN_BWD_FP8, dev)
     sop = saved["slot_of_pair"]
+    # MXFP8 (one E8M0 scale per 32 elements along K): weights quantised once, x with the
+    # permute, h in fc1's epilogue; [a | u] saved as for training, bf16 h not written
+    mx = moe.alloc_mxfp8_experts(cfg, inp["W1"], inp["W2"], dev) if d % 32 == 0 and f % 32 == 0 \
+        else None
 
     def fwd16():
         moe.moe_permute(cfg, inp["x"], sop, x_perm)
@@ -617,6 +621,12 @@ def fp8_experts(args, lc, cfg, inp, saved, dev):
     def fwd8():
         moe.moe_permute_quantize_e4m3(cfg, inp["x"], sop, xq, xs, xa)
         moe.moe_grouped_swiglu_fwd_fp8(cfg, xq, xs, off, W1q, s1, W2q, s2, h, act, hq, hs, ha, yp)
+
+    def fwdmx():
+        moe.moe_permute_quantize_mxfp8(cfg, inp["x"], sop, off, mx["x_perm_q"], mx["x_perm_s"])
+        moe.moe_grouped_swiglu_fwd_mxfp8(cfg, mx["x_perm_q"], mx["x_perm_s"], off, mx["W1_q"],
+                                         mx["W1_sp"], mx["W2_q"], mx["W2_sp"], None, act, mx["h_q"],
+                                         mx["h_s"], yp)
 
     def bwd16():
         moe.moe_grouped_swiglu_bwd(cfg, x_perm, off, inp["W1"], inp["W2"], act, h, dyp, dxp, dW1,
@@ -670,6 +680,24 @@ def fp8_experts(args, lc, cfg, inp, saved, dev):
                      "fp8_gemm_frac": round(flops / (gemm_ms / 1e3) / 1e12 / fp8_peak, 4)
                      if gemm_ms else None,
                      "kernels_ms": per, "scope": scope}
+    if mx is not None:
+        moe.trace_read()
+        moe.trace_enable(True)
+        msmx = timed(fwdmx, n)
+        moe.trace_enable(False)
+        tr = moe.trace_read()
+        moe.check_device_error()
+        per = {k: round(ms / c, 4) for k, (c, ms) in tr.items() if c}
+        gemm_ms = sum(per.get(k, 0) for k in ("gemm_fc1_swiglu_mxfp8", "gemm_fc2_mxfp8"))
+        flops = 6.0 * N * d * f
+        fw = out["forward"]
+        fw.update(mxfp8_ms=round(msmx, 4), mxfp8_speedup=round(fw["bf16_ms"] / msmx, 3),
+                  mxfp8_gemm_tflops=round(flops / (gemm_ms / 1e3) / 1e12, 1) if gemm_ms else None,
+                  mxfp8_gemm_frac=round(flops / (gemm_ms / 1e3) / 1e12 / fp8_peak, 4)
+                  if gemm_ms else None,
+                  mxfp8_kernels_ms=per,
+                  mxfp8_scope="MXFP8 (E8M0 scale per 32 along K): permute + quantise x, fc1 + "
+                              "SwiGLU with h quantised in its epilogue, fc2; [a | u] saved")
     return out
 
 
