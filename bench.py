@@ -475,6 +475,7 @@ def run_gpu(args, lc):
         fp8_experts(args, lc, cfg, inp, saved, dev)
     if fp8 is not None:
         fp8["layer"] = fp8_layer(args, lc, cfg, inp, dev, ms_step)
+        fp8["mxfp8_layer_fwd"] = mxfp8_layer_fwd(args, lc, cfg, inp, dev)
 
     # ---- roofline of the dominant kernel (largest share of device time in the timed region)
     peaks, peak_src = load_peaks()
@@ -701,6 +702,73 @@ def fp8_experts(args, lc, cfg, inp, saved, dev):
     return out
 
 
+def graph_timed(args, step, dev, n):
+    """Device ms per call of step(): 3 eager warm-up calls, then n replays of a CUDA graph of one
+    call (eager calls with --no-graph), timed with CUDA events on the current stream."""
+    import torch
+    import moe_expert_layer_gemm_gb300 as moe
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    moe.check_device_error()
+    graph = None
+    if not args.no_graph:
+        cs = torch.cuda.Stream(device=dev)
+        cs.wait_stream(stream)
+        with torch.cuda.stream(cs):
+            step()
+        stream.wait_stream(cs)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        graph.replay()
+        torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        graph.replay() if graph is not None else step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    moe.check_device_error()
+    return e0.elapsed_time(e1) / n, graph is not None
+
+
+def mxfp8_layer_fwd(args, lc, cfg, inp, dev):
+    """The layer forward with MXFP8 routed experts (moe_layer_fwd_mxfp8: x permuted and
+    block-quantised in one pass, h quantised in fc1's epilogue; router, bf16 shared expert and
+    combine as in bf16) against the bf16 layer forward (moe_layer_fwd), both replayed from CUDA
+    graphs.  MXFP8 weights are quantised once, outside the timed calls."""
+    import torch
+    import moe_expert_layer_gemm_gb300 as moe
+    if lc.d % 32 or lc.f % 32:
+        return None
+    s16 = moe.alloc_saved(cfg, dev)
+    smx = moe.alloc_saved(cfg, dev)
+    smx["x_perm"] = smx["act"] = smx["h"] = None
+    mx = moe.alloc_mxfp8_experts(cfg, inp["W1"], inp["W2"], dev)
+    y = torch.empty_like(inp["x"])
+    ws_f = moe.workspace(cfg, moe.WS_LAYER_FWD, dev)
+
+    def f16():
+        moe.moe_layer_fwd(cfg, inp["x"], inp["W_r"], inp["b_r"], inp["W1"], inp["W2"], inp["Ws1"],
+                          inp["Ws2"], inp["w_sg"], y, s16, ws_f)
+
+    def fmx():
+        moe.moe_layer_fwd_mxfp8(cfg, inp["x"], inp["W_r"], inp["b_r"], mx, inp["Ws1"], inp["Ws2"],
+                                inp["w_sg"], y, smx, ws_f)
+
+    n = max(5, min(args.steps, 50))
+    ms16, graphed = graph_timed(args, f16, dev, n)
+    msmx, _ = graph_timed(args, fmx, dev, n)
+    return {"bf16_fwd_ms": round(ms16, 4), "mxfp8_fwd_ms": round(msmx, 4),
+            "speedup": round(ms16 / msmx, 3), "tokens_per_s": round(lc.T / (msmx / 1e3), 1),
+            "steps": n, "cuda_graph": graphed,
+            "scope": "layer forward: routing, permute + quantise, routed experts in MXFP8, "
+                     "shared expert in bf16, combine (bf16 forward: the same with bf16 experts)"}
+
+
 def fp8_layer(args, lc, cfg, inp, dev, ms_bf16):
     """The whole layer step with FP8 experts (moe_layer_fwd_fp8 / moe_layer_bwd_fp8: routed and
     shared experts on E4M3 operands, router, gate and combine as in bf16; E4M3 weights quantised
@@ -730,36 +798,11 @@ def fp8_layer(args, lc, cfg, inp, dev, ms_bf16):
                                   inp["w_sg"], saved, g["dx"], g["dW_r"], g["dW1"], g["dW2"],
                                   g["dWs1"], g["dWs2"], g["dw_sg"], ws_b)
 
-    stream = torch.cuda.current_stream()
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    moe.check_device_error()
-    graph = None
-    if not args.no_graph:
-        cs = torch.cuda.Stream(device=dev)
-        cs.wait_stream(stream)
-        with torch.cuda.stream(cs):
-            step()
-        stream.wait_stream(cs)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step()
-        graph.replay()
-        torch.cuda.synchronize()
     n = max(5, min(args.steps, 50))
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(n):
-        graph.replay() if graph is not None else step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    moe.check_device_error()
-    ms = e0.elapsed_time(e1) / n
+    ms, graphed = graph_timed(args, step, dev, n)
     return {"ms_per_step": round(ms, 4), "tokens_per_s": round(lc.T / (ms / 1e3), 1),
             "bf16_ms_per_step": round(ms_bf16, 4), "speedup": round(ms_bf16 / ms, 3),
-            "steps": n, "cuda_graph": graph is not None,
+            "steps": n, "cuda_graph": graphed,
             "scope": "whole layer " + ("fwd+bwd" if lc.backward else "fwd") + " with the routed "
                      "and shared experts in E4M3 (router, shared gate and combine in bf16)"}
 

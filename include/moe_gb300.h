@@ -310,6 +310,22 @@ int moe_grouped_swiglu_fwd_mxfp8(const moe_cfg* cfg, const uint8_t* x_perm_q,
                                  const uint8_t* W2_sp, void* h, void* act, uint8_t* h_q,
                                  uint8_t* h_s, void* y_perm, void* stream);
 
+/* MXFP8 state of the routed experts for moe_layer_fwd_mxfp8.  Caller-owned device buffers:
+ *   W1_q [E,2f,d], W2_q [E,d,f]: codes from moe_quantize_mxfp8 (W1 blocked along d, W2 along f);
+ *   W1_sp, W2_sp: their packed scales (moe_mxfp8_pack_expert_scales); read only;
+ *   x_perm_q [N,d], x_perm_s (MOE_MX_SCALES_X bytes), h_q [N,f], h_s (MOE_MX_SCALES_H bytes): the
+ *   layer forward's MXFP8 activations, written by the call. */
+typedef struct moe_mxfp8_experts {
+  const uint8_t* W1_q;
+  const uint8_t* W1_sp;
+  const uint8_t* W2_q;
+  const uint8_t* W2_sp;
+  uint8_t* x_perm_q;
+  uint8_t* x_perm_s;
+  uint8_t* h_q;
+  uint8_t* h_s;
+} moe_mxfp8_experts;
+
 /* Unpermute + weighted combine: "Megatron-Bridge 深度剖析", §Expert Parallel 基础 (Step 3,
  * results sent back to token order) and §Shared Expert Overlap (shared output added).
  *   y[t] = sum_{j<k} gate[t,j] * y_perm[slot_of_pair[t,j]]  (+ c_t * shared_out[t])
@@ -424,6 +440,18 @@ typedef struct moe_fp8_experts {
   uint8_t* x_q;
   uint8_t* s_h_q;
 } moe_fp8_experts;
+
+/* The layer forward with its routed experts on MXFP8 operands: moe_layer_fwd, except that x is
+ * permuted and block-quantised in one pass (moe_permute_quantize_mxfp8) and the routed experts run
+ * as moe_grouped_swiglu_fwd_mxfp8 on mx's weights and buffers.  Router, shared expert (bf16 Ws1,
+ * Ws2), shared gate and combine are those of moe_layer_fwd.  There is no MXFP8 backward: saved.act
+ * and saved.h are not written (and may be NULL), saved.x_perm is not used; routing, y_perm and the
+ * shared expert's buffers are written as by moe_layer_fwd.  Workspace MOE_WS_LAYER_FWD; d and f
+ * multiples of 32; cfg->dtype MOE_DTYPE_BF16. */
+int moe_layer_fwd_mxfp8(const moe_cfg* cfg, const void* x, const void* W_r, const float* b_r,
+                        const moe_mxfp8_experts* mx, const void* Ws1, const void* Ws2,
+                        const void* w_sg, void* y, const moe_saved* saved, void* ws,
+                        size_t ws_bytes, void* stream);
 
 /* moe_layer_fwd with the routed experts on E4M3 operands: x is permuted and quantised in one
  * pass (moe_permute_quantize_e4m3) and the experts run as moe_grouped_swiglu_fwd_fp8 does, with

@@ -44,6 +44,11 @@ class MoeFp8Experts(ctypes.Structure):
                  "Ws1_q", "Ws1_scale", "Ws2_q", "Ws2_scale", "x_q", "s_h_q")]
 
 
+class MoeMxfp8Experts(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("W1_q", "W1_sp", "W2_q", "W2_sp", "x_perm_q", "x_perm_s", "h_q", "h_s")]
+
+
 _VP = ctypes.c_void_p
 _SZ = ctypes.c_size_t
 _CFG = ctypes.POINTER(MoeCfg)
@@ -65,6 +70,8 @@ _SIGS = {
     "moe_mxfp8_pack_expert_scales": (ctypes.c_int, [_CFG] + [_VP] * 5),
     "moe_permute_quantize_mxfp8": (ctypes.c_int, [_CFG] + [_VP] * 6),
     "moe_grouped_swiglu_fwd_mxfp8": (ctypes.c_int, [_CFG] + [_VP] * 13),
+    "moe_layer_fwd_mxfp8": (ctypes.c_int, [_CFG] + [_VP] * 3 + [ctypes.POINTER(MoeMxfp8Experts)]
+                            + [_VP] * 4 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP]),
     "moe_unpermute_combine": (ctypes.c_int, [_CFG] + [_VP] * 7),
     "moe_unpermute_combine_bwd": (ctypes.c_int, [_CFG] + [_VP] * 11),
     "moe_layer_fwd": (ctypes.c_int, [_CFG] + [_VP] * 9 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP]),
@@ -293,6 +300,17 @@ def alloc_mxfp8_experts(cfg, W1, W2, device="cuda", stream=None):
     moe_quantize_mxfp8(W2, m["W2_q"], m["W2_s"], stream)
     moe_mxfp8_pack_expert_scales(cfg, m["W1_s"], m["W2_s"], m["W1_sp"], m["W2_sp"], stream)
     return m
+
+
+def mx_struct(m):
+    return MoeMxfp8Experts(*[m[n].data_ptr() for n, _ in MoeMxfp8Experts._fields_])
+
+
+def moe_layer_fwd_mxfp8(cfg, x, W_r, b_r, mx, Ws1, Ws2, w_sg, y, saved, ws, stream=None):
+    st, ms = saved_struct(saved), mx_struct(mx)
+    _check(lib().moe_layer_fwd_mxfp8(ctypes.byref(cfg), _p(x), _p(W_r), _p(b_r), ctypes.byref(ms),
+                                     _p(Ws1), _p(Ws2), _p(w_sg), _p(y), ctypes.byref(st), _p(ws),
+                                     ws.numel(), _stream(stream)), "moe_layer_fwd_mxfp8")
 
 
 def moe_unpermute_combine(cfg, y_perm, gate, slot_of_pair, shared_out, shared_coef, y, stream=None):

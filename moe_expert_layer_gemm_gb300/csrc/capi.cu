@@ -976,6 +976,61 @@ static int check_mx_cfg(const moe_cfg* c) {
   return MOE_OK;
 }
 
+// The routed experts' forward on MXFP8 operands: fc1 + SwiGLU with h quantised to MXFP8 in its
+// epilogue, then fc2 (N rows; bf16 h and [a | u] written only where given).
+static int ffn_fwd_mx_impl(const moe_cfg* c, const int32_t* offsets, int64_t N,
+                           const uint8_t* x_perm_q, const uint8_t* x_perm_s, const uint8_t* W1_q,
+                           const uint8_t* W1_sp, const uint8_t* W2_q, const uint8_t* W2_sp, void* h,
+                           void* act, uint8_t* h_q, uint8_t* h_s, void* y_perm, cudaStream_t st) {
+  const int d = c->d, f = c->f, E = c->E;
+  // fc1 + SwiGLU on MXFP8 operands -> h codes and block scales (and bf16 h, [a | u] if asked)
+  GemmDesc g1 = desc0();
+  g1.name = "gemm_fc1_swiglu_mxfp8";
+  g1.sched = RAGGED_M;
+  g1.epi = EPI_SWIGLU_FWD;
+  g1.G = E;
+  g1.offsets = offsets;
+  g1.M = static_cast<int>(N);
+  g1.N = 2 * f;
+  g1.K = d;
+  g1.A = opnd(x_perm_q, N, d, false);
+  g1.B = opnd(W1_q, static_cast<int64_t>(E) * 2 * f, d, false);
+  g1.b_group_rows = 2 * f;
+  g1.b_up_rows = f;
+  g1.f = f;
+  g1.out = h;
+  g1.ldo = f;
+  g1.out2 = act;
+  g1.ldo2 = 2 * f;
+  g1.fp8 = true;
+  g1.mx = true;
+  g1.sfa = x_perm_s;
+  g1.sfb = W1_sp;
+  g1.q_out = h_q;
+  g1.q_sf = h_s;
+  MOE_TRY(gemm_tc(g1, st));
+  // fc2 on MXFP8 operands -> y_perm (bf16)
+  GemmDesc g2 = desc0();
+  g2.name = "gemm_fc2_mxfp8";
+  g2.sched = RAGGED_M;
+  g2.epi = EPI_STORE;
+  g2.G = E;
+  g2.offsets = offsets;
+  g2.M = static_cast<int>(N);
+  g2.N = d;
+  g2.K = f;
+  g2.A = opnd(h_q, N, f, false);
+  g2.B = opnd(W2_q, static_cast<int64_t>(E) * d, f, false);
+  g2.b_group_rows = d;
+  g2.out = y_perm;
+  g2.ldo = d;
+  g2.fp8 = true;
+  g2.mx = true;
+  g2.sfa = h_s;
+  g2.sfb = W2_sp;
+  return gemm_tc(g2, st);
+}
+
 size_t moe_mxfp8_scale_bytes(const moe_cfg* c, int which) {
   if (validate_cfg(c) != MOE_OK) return 0;
   const int64_t N = Nrows(c);
@@ -1040,56 +1095,10 @@ int moe_grouped_swiglu_fwd_mxfp8(const moe_cfg* c, const uint8_t* x_perm_q,
   for (const auto& r : req) MOE_TRY(check_ptr(r.p, r.n, true));
   MOE_TRY(check_ptr(h, "h", false));
   MOE_TRY(check_ptr(act, "act", false));
-  cudaStream_t st = S(stream);
   const int64_t N = Nrows(c);
   if (N == 0) return MOE_OK;
-  const int d = c->d, f = c->f, E = c->E;
-  // fc1 + SwiGLU on MXFP8 operands -> h codes and block scales (and bf16 h, [a | u] if asked)
-  GemmDesc g1 = desc0();
-  g1.name = "gemm_fc1_swiglu_mxfp8";
-  g1.sched = RAGGED_M;
-  g1.epi = EPI_SWIGLU_FWD;
-  g1.G = E;
-  g1.offsets = offsets;
-  g1.M = static_cast<int>(N);
-  g1.N = 2 * f;
-  g1.K = d;
-  g1.A = opnd(x_perm_q, N, d, false);
-  g1.B = opnd(W1_q, static_cast<int64_t>(E) * 2 * f, d, false);
-  g1.b_group_rows = 2 * f;
-  g1.b_up_rows = f;
-  g1.f = f;
-  g1.out = h;
-  g1.ldo = f;
-  g1.out2 = act;
-  g1.ldo2 = 2 * f;
-  g1.fp8 = true;
-  g1.mx = true;
-  g1.sfa = x_perm_s;
-  g1.sfb = W1_sp;
-  g1.q_out = h_q;
-  g1.q_sf = h_s;
-  MOE_TRY(gemm_tc(g1, st));
-  // fc2 on MXFP8 operands -> y_perm (bf16)
-  GemmDesc g2 = desc0();
-  g2.name = "gemm_fc2_mxfp8";
-  g2.sched = RAGGED_M;
-  g2.epi = EPI_STORE;
-  g2.G = E;
-  g2.offsets = offsets;
-  g2.M = static_cast<int>(N);
-  g2.N = d;
-  g2.K = f;
-  g2.A = opnd(h_q, N, f, false);
-  g2.B = opnd(W2_q, static_cast<int64_t>(E) * d, f, false);
-  g2.b_group_rows = d;
-  g2.out = y_perm;
-  g2.ldo = d;
-  g2.fp8 = true;
-  g2.mx = true;
-  g2.sfa = h_s;
-  g2.sfb = W2_sp;
-  return gemm_tc(g2, st);
+  return ffn_fwd_mx_impl(c, offsets, N, x_perm_q, x_perm_s, W1_q, W1_sp, W2_q, W2_sp, h, act, h_q,
+                         h_s, y_perm, S(stream));
 }
 
 int moe_grouped_swiglu_bwd_fp8(const moe_cfg* c, const uint8_t* x_perm_q, const float* x_scale,
@@ -1219,7 +1228,8 @@ static bool shared_fp8(const moe_cfg* c, const moe_fp8_experts* q) {
   return q && c->f_shared > 0 && q->Ws1_q;
 }
 
-static int check_saved(const moe_cfg* c, const moe_saved* s, bool fp8 = false) {
+static int check_saved(const moe_cfg* c, const moe_saved* s, bool fp8 = false,
+                       bool need_act = true) {
   if (!s) return fail(MOE_ERR_INVALID_ARG, "saved is NULL");
   MOE_TRY(check_ptr(s->logits, "saved.logits", true));
   MOE_TRY(check_ptr(s->idx, "saved.idx", true));
@@ -1229,8 +1239,8 @@ static int check_saved(const moe_cfg* c, const moe_saved* s, bool fp8 = false) {
   MOE_TRY(check_ptr(s->slot_of_pair, "saved.slot_of_pair", true));
   MOE_TRY(check_ptr(s->token_of_slot, "saved.token_of_slot", true));
   MOE_TRY(check_ptr(s->x_perm, "saved.x_perm", !fp8 && !permute_fused(c)));
-  MOE_TRY(check_ptr(s->act, "saved.act", true));
-  MOE_TRY(check_ptr(s->h, "saved.h", true));
+  MOE_TRY(check_ptr(s->act, "saved.act", need_act));
+  MOE_TRY(check_ptr(s->h, "saved.h", need_act));
   MOE_TRY(check_ptr(s->y_perm, "saved.y_perm", true));
   const bool sh = c->f_shared > 0;
   MOE_TRY(check_ptr(s->s_act, "saved.s_act", sh));
@@ -1241,25 +1251,38 @@ static int check_saved(const moe_cfg* c, const moe_saved* s, bool fp8 = false) {
   return MOE_OK;
 }
 
-// The layer forward; with q the routed experts run on E4M3 operands (q's weights and buffers).
+static int check_mx_experts(const moe_cfg* c, const moe_mxfp8_experts* m) {
+  MOE_TRY(check_mx_cfg(c));
+  const struct { const void* p; const char* n; } req[] = {
+      {m->W1_q, "mx.W1_q"},         {m->W1_sp, "mx.W1_sp"}, {m->W2_q, "mx.W2_q"},
+      {m->W2_sp, "mx.W2_sp"},       {m->x_perm_q, "mx.x_perm_q"},
+      {m->x_perm_s, "mx.x_perm_s"}, {m->h_q, "mx.h_q"},     {m->h_s, "mx.h_s"}};
+  for (const auto& r : req) MOE_TRY(check_ptr(r.p, r.n, true));
+  return MOE_OK;
+}
+
+// The layer forward; with q the routed experts run on E4M3 operands (q's weights and buffers),
+// with mx on MXFP8 operands.
 static int layer_fwd_impl(const moe_cfg* c, const void* x, const void* W_r, const float* b_r,
                           const void* W1, const void* W2, const moe_fp8_experts* q,
                           const void* Ws1, const void* Ws2, const void* w_sg, void* y,
-                          const moe_saved* s, void* ws, size_t ws_bytes, void* stream) {
+                          const moe_saved* s, void* ws, size_t ws_bytes, void* stream,
+                          const moe_mxfp8_experts* mx = nullptr) {
   MOE_TRY(check_cfg(c));
   MOE_TRY(check_ptr(x, "x", true));
   MOE_TRY(check_ptr(W_r, "W_r", true));
   MOE_TRY(check_ptr(b_r, "b_r", false));
-  MOE_TRY(check_ptr(W1, "W1", !q));
-  MOE_TRY(check_ptr(W2, "W2", !q));
+  MOE_TRY(check_ptr(W1, "W1", !q && !mx));
+  MOE_TRY(check_ptr(W2, "W2", !q && !mx));
   if (q) MOE_TRY(check_fp8_experts(c, q));
+  if (mx) MOE_TRY(check_mx_experts(c, mx));
   const bool sh = c->f_shared > 0, gt = c->shared_gate != 0;
   const bool sq = shared_fp8(c, q);
   MOE_TRY(check_ptr(Ws1, "Ws1", sh && !sq));
   MOE_TRY(check_ptr(Ws2, "Ws2", sh && !sq));
   MOE_TRY(check_ptr(w_sg, "w_sg", gt));
   MOE_TRY(check_ptr(y, "y", true));
-  MOE_TRY(check_saved(c, s, q != nullptr));
+  MOE_TRY(check_saved(c, s, q != nullptr || mx != nullptr, mx == nullptr));
   MOE_TRY(check_ws(c, MOE_WS_LAYER_FWD, ws, ws_bytes));
   cudaStream_t st = S(stream);
   if (c->T == 0) {
@@ -1291,6 +1314,10 @@ static int layer_fwd_impl(const moe_cfg* c, const void* x, const void* W_r, cons
   if (q)
     MOE_TRY(launch_permute_quant_e4m3(x, s->slot_of_pair, q->x_perm_q, sq ? q->x_q : nullptr,
                                       q->scales + 0, q->scales + 1, c->T, c->d, c->k, st));
+  // MXFP8: x permuted and block-quantised in one pass, its scales in the row tiles of the routing
+  if (mx)
+    MOE_TRY(launch_permute_quant_mx(x, s->slot_of_pair, s->offsets, mx->x_perm_q, mx->x_perm_s,
+                                    c->T, c->d, c->k, c->E, st));
   if (side) {
     side_lk.lock();
     if (cudaEventRecord(side->fork, st) != cudaSuccess ||
@@ -1308,6 +1335,11 @@ static int layer_fwd_impl(const moe_cfg* c, const void* x, const void* W_r, cons
     MOE_TRY(ffn_fwd_fp8_impl(c, c->E, s->offsets, Nrows(c), c->f, q->x_perm_q, q->scales + 0, q->W1_q, q->W1_scale,
                              q->W2_q, q->W2_scale, s->h, s->act, q->h_q, q->scales + 2,
                              q->scales + 3, s->y_perm, st));
+  } else if (mx) {
+    // MXFP8 experts (a forward without a backward: bf16 h and [a | u] are not written)
+    MOE_TRY(ffn_fwd_mx_impl(c, s->offsets, Nrows(c), mx->x_perm_q, mx->x_perm_s, mx->W1_q,
+                            mx->W1_sp, mx->W2_q, mx->W2_sp, nullptr, nullptr, mx->h_q, mx->h_s,
+                            s->y_perm, st));
   } else if (permute_fused(c)) {
     // "Megatron-Bridge 深度剖析", §Permute Fusion: fc1 gathers its rows from x by token_of_slot
     MOE_TRY(ffn_fwd_impl(c, c->E, s->offsets, Nrows(c), c->f, x, W1, W2, s->h, s->act,
@@ -1482,6 +1514,15 @@ int moe_layer_fwd(const moe_cfg* c, const void* x, const void* W_r, const float*
                   void* stream) {
   return layer_fwd_impl(c, x, W_r, b_r, W1, W2, nullptr, Ws1, Ws2, w_sg, y, s, ws, ws_bytes,
                         stream);
+}
+
+int moe_layer_fwd_mxfp8(const moe_cfg* c, const void* x, const void* W_r, const float* b_r,
+                        const moe_mxfp8_experts* mx, const void* Ws1, const void* Ws2,
+                        const void* w_sg, void* y, const moe_saved* saved, void* ws,
+                        size_t ws_bytes, void* stream) {
+  if (!mx) return fail(MOE_ERR_INVALID_ARG, "mx is NULL");
+  return layer_fwd_impl(c, x, W_r, b_r, nullptr, nullptr, nullptr, Ws1, Ws2, w_sg, y, saved, ws,
+                        ws_bytes, stream, mx);
 }
 
 int moe_layer_fwd_fp8(const moe_cfg* c, const void* x, const void* W_r, const float* b_r,

@@ -10,7 +10,9 @@
   * moe_grouped_swiglu_fwd_mxfp8: [a | u] and h within the bf16 output tolerance of the oracle's
     fp64 product of the same decoded operands; h's codes and scales bit-identical to the oracle's
     quantisation of the GPU's bf16 h; y_perm within tolerance of the oracle's fc2 on those codes;
-    and against the unquantised bf16 experts within the format's rounding bound.
+    and against the unquantised bf16 experts within the format's rounding bound;
+  * moe_layer_fwd_mxfp8: routing and shared expert identical to the bf16 layer's, y bit-identical
+    to the composed stage calls, and within the format's rounding of the unquantised layer.
 Shapes cover several tiles with ragged tails, experts without rows, K not a multiple of 128 (a
 partial last scale chunk) and f not a multiple of the 96-column SwiGLU tile.
 """
@@ -19,11 +21,12 @@ import pytest
 import torch
 
 import moe_expert_layer_gemm_gb300 as moe
+import moe_inputs
 import oracle.moe_oracle as O
 import oracle.mxfp8_oracle as MX
 
 from .helpers import (assert_close, mx_act_pad_bytes, mx_unpack_act_scales, mx_weight_index, np64,
-                      rel_err)
+                      oracle_layer, rel_err, run_layer)
 
 pytestmark = pytest.mark.gpu
 
@@ -187,3 +190,60 @@ def test_mxfp8_forward_without_bf16_side_outputs_and_zero_tokens():
     moe.moe_grouped_swiglu_fwd_mxfp8(cfg0, m["x_perm_q"], m["x_perm_s"], off, m["W1_q"], m["W1_sp"],
                                      m["W2_q"], m["W2_sp"], None, None, m["h_q"], m["h_s"], outs[0][1])
     sync()
+
+
+LAYER_CASES = {
+    # the DeepSeek-style layer's kind (sigmoid + renorm, Zipf-biased router, ungated shared
+    # expert) and the MTP kind (softmax, gated shared expert), at sizes the oracle runs quickly
+    "sigmoid-shared": moe_inputs.LayerConfig("mx sigmoid shared", 300, 256, 16, 4, 160, f_shared=128,
+                                             score_fn=O.SIGMOID, renorm=1, router_bias="zipf1.2"),
+    "softmax-gated": moe_inputs.LayerConfig("mx softmax gated", 257, 384, 32, 8, 96, f_shared=64,
+                                            score_fn=O.SOFTMAX, renorm=1, shared_gate=1,
+                                            router_init="uniform"),
+    "no-shared": moe_inputs.LayerConfig("mx plain", 500, 2688, 8, 2, 1856),
+}
+
+
+@pytest.mark.parametrize("name", list(LAYER_CASES))
+def test_mxfp8_layer_forward_is_the_composed_stages(name):
+    """moe_layer_fwd_mxfp8 = the bf16 layer's routing and shared expert + the MXFP8 stage calls +
+    the combine, bit for bit; and within the format's rounding of the unquantised oracle layer."""
+    lc = LAYER_CASES[name]
+    inp = {k: (None if v is None else v.cuda())
+           for k, v in moe_inputs.make_layer_inputs(lc, seed=1).items()}
+    ref16 = run_layer(lc, inp, backward=False)
+    cfg = moe.cfg_from(lc)
+    m = moe.alloc_mxfp8_experts(cfg, inp["W1"], inp["W2"])
+    saved = moe.alloc_saved(cfg)
+    saved["x_perm"] = saved["act"] = saved["h"] = None
+    y = torch.empty_like(inp["x"])
+    moe.moe_layer_fwd_mxfp8(cfg, inp["x"], inp["W_r"], inp["b_r"], m, inp["Ws1"], inp["Ws2"],
+                            inp["w_sg"], y, saved, moe.workspace(cfg, moe.WS_LAYER_FWD))
+    sync()
+    s16 = ref16["saved"]
+    for key in ("logits", "idx", "gate", "counts", "offsets", "slot_of_pair", "token_of_slot"):
+        assert torch.equal(saved[key], s16[key]), key
+    if lc.f_shared:
+        assert torch.equal(saved["s_out"], s16["s_out"])
+    # the same call composed from the stage functions
+    N = lc.T * lc.k
+    xq = torch.empty_like(m["x_perm_q"])
+    xs = torch.empty_like(m["x_perm_s"])
+    moe.moe_permute_quantize_mxfp8(cfg, inp["x"], s16["slot_of_pair"], s16["offsets"], xq, xs)
+    hq, hs = torch.empty_like(m["h_q"]), torch.empty_like(m["h_s"])
+    yp = torch.empty(N, lc.d, dtype=torch.bfloat16, device="cuda")
+    moe.moe_grouped_swiglu_fwd_mxfp8(cfg, xq, xs, s16["offsets"], m["W1_q"], m["W1_sp"], m["W2_q"],
+                                     m["W2_sp"], None, None, hq, hs, yp)
+    yc = torch.empty_like(y)
+    moe.moe_unpermute_combine(cfg, yp, s16["gate"], s16["slot_of_pair"],
+                              s16["s_out"] if lc.f_shared else None,
+                              s16["s_coef"] if lc.shared_gate else None, yc)
+    sync()
+    assert torch.equal(m["x_perm_q"], xq) and torch.equal(m["h_q"], hq)
+    assert torch.equal(saved["y_perm"], yp) and torch.equal(y, yc)
+    # against the unquantised fp64 layer
+    ref = oracle_layer(lc, {k: (None if v is None else v.cpu()) for k, v in inp.items()},
+                       backward=False)
+    e = rel_err(np64(y), ref["fwd"]["y"])
+    assert e < 0.15, e
+    print(f"{name}: y vs unquantised {e:.3f}")
