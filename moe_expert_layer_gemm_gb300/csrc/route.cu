@@ -43,6 +43,23 @@ __device__ __forceinline__ void load_logit_row(const float* __restrict__ logits,
   }
 }
 
+// A float as an unsigned integer with the same order (for single-instruction warp reductions);
+// -0 becomes +0 first, so that the two zeros tie as they compare equal.
+__device__ __forceinline__ unsigned ordered_key(float f) {
+  unsigned b = __float_as_uint(f);
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Sum over lanes 0..7 (k <= 8 pairs live there, the other lanes hold zeros), result in lane 0
+// and every lane of its group of eight.  The same value as a full-warp butterfly over those
+// lanes: the skipped steps would only add zeros.
+__device__ __forceinline__ float sum8(float v) {
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 template <int EPL>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E,
                                                    int k, int score_fn, int renorm,
@@ -92,17 +109,18 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     }
 
     // ---- selection: k rounds of a warp-wide max, order (key desc, expert asc).  Each lane first
-    // sorts its EPL (key, expert) pairs, so a round compares only the lanes' heads: a float max,
-    // then the lowest expert among the lanes holding it (a ballot; a second reduction only when
-    // lanes tie).  The winning lane moves on to its next pair.
-    float hk[EPL];
+    // sorts its EPL (key, expert) pairs, so a round compares only the lanes' heads: the largest
+    // key, then the lowest expert among the lanes holding it -- two single-instruction warp
+    // reductions (redux.sync) on the keys as order-preserving integers.  The winning lane moves
+    // on to its next pair.
+    unsigned hk[EPL];
     int he[EPL];
 #pragma unroll
     for (int q = 0; q < EPL; ++q) {
       const int e = q * 32 + lane;
       // a NaN key (outside the inputs' contract) ranks as -inf, so every round still has a
       // maximum that some lane holds and the selection stays within [0, E)
-      hk[q] = (e < E && key[q] == key[q]) ? key[q] : NEG_INF;
+      hk[q] = ordered_key((e < E && key[q] == key[q]) ? key[q] : NEG_INF);
       he[q] = e < E ? e : INT_MAX;
     }
 #pragma unroll
@@ -110,7 +128,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 #pragma unroll
       for (int q = i; q > 0; --q)
         if (hk[q] > hk[q - 1] || (hk[q] == hk[q - 1] && he[q] < he[q - 1])) {
-          const float tk = hk[q];
+          const unsigned tk = hk[q];
           hk[q] = hk[q - 1];
           hk[q - 1] = tk;
           const int te = he[q];
@@ -121,17 +139,8 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 #pragma unroll
     for (int j = 0; j < MAXK; ++j) {
       if (j < k) {
-        const float m = warp_max(hk[0]);   // -0 and +0 compare equal, as in the oracle
-        const unsigned tied = __ballot_sync(0xffffffffu, hk[0] == m);
-        int e;
-        if ((tied & (tied - 1u)) == 0u) {
-          e = __shfl_sync(0xffffffffu, he[0], __ffs(tied) - 1);
-        } else {
-          int c = hk[0] == m ? he[0] : INT_MAX;
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) c = min(c, __shfl_xor_sync(0xffffffffu, c, o));
-          e = c;
-        }
+        const unsigned m = __reduce_max_sync(0xffffffffu, hk[0]);
+        const int e = __reduce_min_sync(0xffffffffu, hk[0] == m ? he[0] : INT_MAX);
         if (lane == j) my_e = e;
         if ((e & 31) == lane) {            // the winner drops its head
 #pragma unroll
@@ -139,7 +148,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
             hk[q] = hk[q + 1];
             he[q] = he[q + 1];
           }
-          hk[EPL - 1] = NEG_INF;
+          hk[EPL - 1] = 0u;   // below every key (-inf is 0x007FFFFF)
           he[EPL - 1] = INT_MAX;
         }
       }
@@ -162,7 +171,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
       const float ex = lane < k ? expf(lv - m) : 0.f;
       float denom;
       if (renorm) {
-        denom = warp_sum(ex);
+        denom = sum8(ex);   // pairs live in lanes 0..k-1
       } else {
         float part = 0.f;
 #pragma unroll
@@ -175,7 +184,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     } else {
       g = lane < k ? sigmoid_f(lv) : 0.f;
       if (renorm) {
-        const float sum = __shfl_sync(0xffffffffu, warp_sum(g), 0);
+        const float sum = __shfl_sync(0xffffffffu, sum8(g), 0);
         g *= 1.0f / sum;
       }
     }
