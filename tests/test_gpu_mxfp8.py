@@ -97,7 +97,7 @@ def routed(T, E, k, seed, empty=0):
 
 
 @pytest.mark.parametrize("T,d,E,k,empty", [(1000, 256, 16, 4, 3), (4097, 2048, 128, 8, 0),
-                                           (7, 64, 4, 1, 0), (300, 2688, 8, 6, 1)])
+                                           (7, 64, 4, 1, 0), (300, 2688, 8, 6, 1), (900, 224, 256, 8, 30)])
 def test_permute_quantize_mx(T, d, E, k, empty):
     r = routed(T, E, k, T, empty)
     x = varied((T, d), d).cuda()
@@ -119,7 +119,8 @@ def test_permute_quantize_mx(T, d, E, k, empty):
 
 
 @pytest.mark.parametrize("T,d,E,k,f,empty", [(600, 256, 8, 2, 160, 2), (1024, 2048, 128, 8, 768, 0),
-                                             (300, 384, 16, 4, 96, 5), (257, 2688, 8, 6, 1856, 0)])
+                                             (300, 384, 16, 4, 96, 5), (257, 2688, 8, 6, 1856, 0),
+                                             (700, 224, 256, 8, 128, 40), (129, 96, 3, 3, 32, 0)])
 def test_mxfp8_grouped_swiglu_forward(T, d, E, k, f, empty):
     r = routed(T, E, k, d + f, empty)
     N = T * k
