@@ -100,6 +100,36 @@ def test_router_variant_entry_points_check_arguments():
     assert L.moe_last_error()
 
 
+def test_mxfp8_entry_points_check_arguments():
+    """MXFP8 calls reject, on the host and before any launch: d or f not a multiple of 32 (the
+    block), an fp32 layer, a row length not a multiple of 32, missing or misaligned buffers."""
+    c = cfg(d=256, f=160)
+    for which in range(4):
+        assert L.moe_mxfp8_scale_bytes(ctypes.byref(c), which) > 0
+    assert L.moe_mxfp8_scale_bytes(ctypes.byref(c), 7) == 0
+    assert L.moe_mxfp8_scale_bytes(ctypes.byref(cfg(k=9)), moe.MX_SCALES_X) == 0
+    # packed sizes: activations per 128-row tile and 128-element chunk, weights per 192-row tile
+    N, E = 256 * 2, 8
+    assert L.moe_mxfp8_scale_bytes(ctypes.byref(c), moe.MX_SCALES_X) == ((N + 127 * E) // 128 + 1) * 2 * 512
+    assert L.moe_mxfp8_scale_bytes(ctypes.byref(c), moe.MX_SCALES_W1) == E * 2 * 2 * 1024
+    assert L.moe_mxfp8_scale_bytes(ctypes.byref(c), moe.MX_SCALES_W2) == E * 2 * 2 * 1024
+    assert L.moe_quantize_mxfp8(P, 4, 48, P, P, None) == -2          # 48 is not a multiple of 32
+    assert L.moe_quantize_mxfp8(P, -1, 64, P, P, None) == -1
+    assert L.moe_quantize_mxfp8(P, 4, 64, MIS, P, None) == -4
+    bad_f = cfg(d=256, f=144)
+    assert L.moe_permute_quantize_mxfp8(ctypes.byref(bad_f), P, P, P, P, P, None) == -2
+    assert L.moe_permute_quantize_mxfp8(ctypes.byref(cfg(dtype=1)), P, P, P, P, P, None) == -2
+    assert L.moe_permute_quantize_mxfp8(ctypes.byref(c), P, P, None, P, P, None) == -1
+    assert L.moe_mxfp8_pack_expert_scales(ctypes.byref(c), P, P, P, MIS, None) == -4
+    args = [P] * 13
+    assert L.moe_grouped_swiglu_fwd_mxfp8(ctypes.byref(bad_f), *args) == -2
+    args[3] = None                                                     # W1_q
+    assert L.moe_grouped_swiglu_fwd_mxfp8(ctypes.byref(c), *args) == -1
+    assert b"W1_q" in L.moe_last_error()
+    assert L.moe_layer_fwd_mxfp8(ctypes.byref(c), P, P, None, None, None, None, None, P, None, P,
+                                 1 << 30, None) == -1
+
+
 def test_binding_argument_counts_match_the_header():
     """Every ctypes signature of the binding takes as many arguments as the header declares."""
     import re
