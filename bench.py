@@ -97,6 +97,11 @@ def kernel_work(lc, trace=None, steps=1):
     w["fp8_amax"] = ("hbm", per("fp8_amax", amax_bytes))
     w["fp8_quantize"] = ("hbm", per("fp8_quantize", quant_bytes))
     w["fp8_permute_quantize"] = ("hbm", T * d * 2 + N * d + (T * d if fs else 0) + N * 4)
+    # MXFP8 (routed experts): the same products; permute + quantise reads x once and writes every
+    # pair's codes and its block scales (one byte per 32)
+    w["gemm_fc1_swiglu_mxfp8"] = w["gemm_fc1_swiglu"]
+    w["gemm_fc2_mxfp8"] = w["gemm_fc2"]
+    w["mxfp8_permute_quantize"] = ("hbm", T * d * 2 + N * d * 33 / 32 + N * 4)
     return w
 
 
@@ -117,6 +122,11 @@ def gemm_bytes(lc):
             out[pre + "fc2_wgrad" + sfx] = rows * d * b + rows * ff * b + G * d * ff * 4
             out[pre + "fc1_dgrad" + sfx] = rows * 2 * ff * b + G * 2 * ff * d * b + rows * d * 2
             out[pre + "fc1_wgrad" + sfx] = rows * 2 * ff * b + rows * d * b + G * 2 * ff * d * 4
+    # MXFP8 forward (layer call): codes plus one scale byte per 32 in, h's codes and scales out
+    # of fc1 (no bf16 h or [a | u]), bf16 y_perm out of fc2
+    q = 33 / 32
+    out["gemm_fc1_swiglu_mxfp8"] = T * k * d * q + E * 2 * f * d * q + T * k * f * q
+    out["gemm_fc2_mxfp8"] = T * k * f * q + E * d * f * q + T * k * d * 2
     return out
 
 
@@ -247,7 +257,8 @@ def time_oracle(lc_s, host, reps=1):
     t0 = time.perf_counter()
     for _ in range(reps):
         fwd = O.layer_forward(lc_s, host)
-        O.layer_backward(lc_s, host, fwd, host["dy"])
+        if lc_s.backward:
+            O.layer_backward(lc_s, host, fwd, host["dy"])
     return (time.perf_counter() - t0) / reps
 
 
@@ -298,6 +309,12 @@ def run_gpu(args, lc):
     ws_f = moe.workspace(cfg, moe.WS_LAYER_FWD, dev)
     ws_b = moe.workspace(cfg, moe.WS_LAYER_BWD_FP8 if args.fp8 else moe.WS_LAYER_BWD, dev)
     stream = torch.cuda.current_stream()
+    mxq = None
+    if args.mxfp8:
+        # MXFP8 routed experts, forward only (quantised once, outside the timed steps); the
+        # saved state keeps routing and y_perm, no bf16 x_perm, h or [a | u]
+        mxq = moe.alloc_mxfp8_experts(cfg, inp["W1"], inp["W2"], dev)
+        saved["x_perm"] = saved["act"] = saved["h"] = None
     fp8q = None
     if args.fp8:
         # E4M3 weights quantised once (FP8 parameters); saved.x_perm is not used
@@ -305,6 +322,10 @@ def run_gpu(args, lc):
         saved["x_perm"] = None
 
     def step(x, dy, yout, dxout):
+        if mxq is not None:
+            moe.moe_layer_fwd_mxfp8(cfg, x, inp["W_r"], inp["b_r"], mxq, inp["Ws1"], inp["Ws2"],
+                                    inp["w_sg"], yout, saved, ws_f)
+            return
         if fp8q is not None:
             moe.moe_layer_fwd_fp8(cfg, x, inp["W_r"], inp["b_r"], fp8q, inp["Ws1"], inp["Ws2"],
                                   inp["w_sg"], yout, saved, ws_f)
@@ -488,7 +509,7 @@ def run_gpu(args, lc):
             dist.destroy_process_group()
         return None
 
-    fp8 = None if args.no_fp8 or args.fp8 or lc.dtype != "bf16" else \
+    fp8 = None if args.no_fp8 or args.fp8 or args.mxfp8 or lc.dtype != "bf16" else \
         fp8_experts(args, lc, cfg, inp, saved, dev)
     if fp8 is not None:
         fp8["layer"] = fp8_layer(args, lc, cfg, inp, dev, ms_step)
@@ -501,8 +522,9 @@ def run_gpu(args, lc):
     bf16_peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
 
     def tensor_peak(name):
-        # E4M3 products: twice the measured bf16 rate (the nominal dense fp8 : bf16 ratio)
-        return 2.0 * bf16_peak if name.endswith("_fp8") else bf16_peak
+        # E4M3 products (tensorwise or block-scaled): twice the measured bf16 rate (the nominal
+        # dense fp8 : bf16 ratio)
+        return 2.0 * bf16_peak if name.endswith(("_fp8", "_mxfp8")) else bf16_peak
 
     gbytes = gemm_bytes(lc) if lc.dtype == "bf16" else {}
     kern = {}
@@ -531,7 +553,7 @@ def run_gpu(args, lc):
         kd = kern[dom]
         kind = work.get(dom, ("hbm", 0))[0]
         traffic = captured_traffic(lc.name, dom)
-        fp8_dom = kind == "tensor" and dom.endswith("_fp8")
+        fp8_dom = kind == "tensor" and dom.endswith(("_fp8", "_mxfp8"))
         roof = {"bound": kind, "kernel": dom, "achieved": kd["achieved"],
                 "peak": tensor_peak(dom) if kind == "tensor" else peaks["hbm_gbs"],
                 "unit": kd["unit"], "frac": kd["frac"], "traffic": traffic,
@@ -551,15 +573,17 @@ def run_gpu(args, lc):
         dt = time_oracle(lc_s, host)
         cpu = {"value": round(n_tok / dt, 2), "unit": "tokens/s", "cores": cpu_cores(),
                "kind": "oracle",
-               "sample": f"{n_tok} seeded tokens of the workload, all {lc.E} experts, fwd+bwd in "
-                         f"fp64 numpy ({dt:.1f} s)"}
+               "sample": f"{n_tok} seeded tokens of the workload, all {lc.E} experts, "
+                         f"{'fwd+bwd' if lc.backward else 'fwd'} in fp64 numpy ({dt:.1f} s)"}
 
     flops_step = layer_flops(lc, lc.backward)
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("e4m3 experts, bf16 router/combine" if args.fp8 else lc.dtype),
+        "dtype": ("e4m3 experts, bf16 router/combine" if args.fp8 else
+                  "mxfp8 experts (e4m3, e8m0 scale per 32), bf16 router/shared/combine"
+                  if args.mxfp8 else lc.dtype),
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights, random init)",
         "config": {"workload": lc.name, "T": lc.T, "d_model": lc.d, "experts": lc.E, "top_k": lc.k,
                    "ffn": lc.f, "shared_ffn": lc.f_shared,
@@ -845,13 +869,13 @@ def run_reference(args, lc):
     dt = time.perf_counter() - t0
     value = args.ref_tokens * args.steps / dt
     sample = (f"{args.ref_tokens} seeded tokens of the workload per step, all {lc.E} experts, "
-              f"fp64 numpy forward+backward")
+              f"fp64 numpy {'forward+backward' if lc.backward else 'forward'}")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": lc.name, "T": lc.T, "pass": "fwd+bwd"},
+        "data": "synthetic", "config": {"workload": lc.name, "T": lc.T, "pass": "fwd+bwd" if lc.backward else "fwd"},
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cpu_cores(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -875,10 +899,17 @@ def main():
     ap.add_argument("--fp8", action="store_true",
                     help="time the layer with its experts in FP8 E4M3 (moe_layer_fwd_fp8 / "
                          "moe_layer_bwd_fp8) instead of bf16")
+    ap.add_argument("--mxfp8", action="store_true",
+                    help="time the layer forward with MXFP8 routed experts (moe_layer_fwd_mxfp8); "
+                         "forward only, also on workloads whose step includes the backward")
     ap.add_argument("--e2e-steps", type=int, default=20)
     args = ap.parse_args()
+    if args.fp8 and args.mxfp8:
+        ap.error("--fp8 and --mxfp8 are exclusive")
     args.warmup = max(args.warmup, 3) if args.impl == "native" else args.warmup
     lc = moe_inputs.CONFIGS[args.workload]
+    if args.mxfp8:
+        lc = lc.replace(backward=False)     # there is no MXFP8 backward: the step is the forward
     out = run_reference(args, lc) if args.impl == "reference" else run_gpu(args, lc)
     if out is not None:
         print(json.dumps(out), flush=True)
