@@ -311,10 +311,12 @@ def run_gpu(args, lc):
     stream = torch.cuda.current_stream()
     mxq = None
     if args.mxfp8:
-        # MXFP8 routed experts, forward only (quantised once, outside the timed steps); the
-        # saved state keeps routing and y_perm, no bf16 x_perm, h or [a | u]
+        # MXFP8 routed experts (quantised once, outside the timed steps).  Forward-only
+        # configurations keep routing and y_perm alone; with a backward, the forward also saves
+        # the bf16 x_perm, [a | u] and h that the bf16 backward reads
         mxq = moe.alloc_mxfp8_experts(cfg, inp["W1"], inp["W2"], dev)
-        saved["x_perm"] = saved["act"] = saved["h"] = None
+        if not lc.backward:
+            saved["x_perm"] = saved["act"] = saved["h"] = None
     fp8q = None
     if args.fp8:
         # E4M3 weights quantised once (FP8 parameters); saved.x_perm is not used
@@ -325,6 +327,11 @@ def run_gpu(args, lc):
         if mxq is not None:
             moe.moe_layer_fwd_mxfp8(cfg, x, inp["W_r"], inp["b_r"], mxq, inp["Ws1"], inp["Ws2"],
                                     inp["w_sg"], yout, saved, ws_f)
+            if lc.backward:
+                moe.moe_layer_bwd(cfg, dy, x, inp["W_r"], inp["W1"], inp["W2"], inp["Ws1"],
+                                  inp["Ws2"], inp["w_sg"], saved, dxout, grads["dW_r"],
+                                  grads["dW1"], grads["dW2"], grads["dWs1"], grads["dWs2"],
+                                  grads["dw_sg"], ws_b)
             return
         if fp8q is not None:
             moe.moe_layer_fwd_fp8(cfg, x, inp["W_r"], inp["b_r"], fp8q, inp["Ws1"], inp["Ws2"],
@@ -582,7 +589,9 @@ def run_gpu(args, lc):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": ("e4m3 experts, bf16 router/combine" if args.fp8 else
-                  "mxfp8 experts (e4m3, e8m0 scale per 32), bf16 router/shared/combine"
+                  ("mxfp8 experts in the forward (e4m3, e8m0 scale per 32), bf16 backward, "
+                   "bf16 router/shared/combine" if lc.backward else
+                   "mxfp8 experts (e4m3, e8m0 scale per 32), bf16 router/shared/combine")
                   if args.mxfp8 else lc.dtype),
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights, random init)",
         "config": {"workload": lc.name, "T": lc.T, "d_model": lc.d, "experts": lc.E, "top_k": lc.k,
@@ -900,16 +909,19 @@ def main():
                     help="time the layer with its experts in FP8 E4M3 (moe_layer_fwd_fp8 / "
                          "moe_layer_bwd_fp8) instead of bf16")
     ap.add_argument("--mxfp8", action="store_true",
-                    help="time the layer forward with MXFP8 routed experts (moe_layer_fwd_mxfp8); "
-                         "forward only, also on workloads whose step includes the backward")
+                    help="time the layer with MXFP8 routed experts in the forward "
+                         "(moe_layer_fwd_mxfp8) and the bf16 backward (moe_layer_bwd) on its saved "
+                         "state; --mxfp8-forward-only times the forward alone")
+    ap.add_argument("--mxfp8-forward-only", action="store_true",
+                    help="with --mxfp8: the step is the forward, also on workloads with a backward")
     ap.add_argument("--e2e-steps", type=int, default=20)
     args = ap.parse_args()
     if args.fp8 and args.mxfp8:
         ap.error("--fp8 and --mxfp8 are exclusive")
     args.warmup = max(args.warmup, 3) if args.impl == "native" else args.warmup
     lc = moe_inputs.CONFIGS[args.workload]
-    if args.mxfp8:
-        lc = lc.replace(backward=False)     # there is no MXFP8 backward: the step is the forward
+    if args.mxfp8 and args.mxfp8_forward_only:
+        lc = lc.replace(backward=False)
     out = run_reference(args, lc) if args.impl == "reference" else run_gpu(args, lc)
     if out is not None:
         print(json.dumps(out), flush=True)

@@ -444,10 +444,12 @@ typedef struct moe_fp8_experts {
 /* The layer forward with its routed experts on MXFP8 operands: moe_layer_fwd, except that x is
  * permuted and block-quantised in one pass (moe_permute_quantize_mxfp8) and the routed experts run
  * as moe_grouped_swiglu_fwd_mxfp8 on mx's weights and buffers.  Router, shared expert (bf16 Ws1,
- * Ws2), shared gate and combine are those of moe_layer_fwd.  There is no MXFP8 backward: saved.act
- * and saved.h are not written (and may be NULL), saved.x_perm is not used; routing, y_perm and the
- * shared expert's buffers are written as by moe_layer_fwd.  Workspace MOE_WS_LAYER_FWD; d and f
- * multiples of 32; cfg->dtype MOE_DTYPE_BF16. */
+ * Ws2), shared gate and combine are those of moe_layer_fwd.  Routing, y_perm and the shared
+ * expert's buffers are written as by moe_layer_fwd.  saved.x_perm, saved.act and saved.h may be
+ * NULL (inference: not written); when given, the forward writes the permuted bf16 rows of x, the
+ * bf16 [a | u] of the MXFP8 products and the bf16 h, and moe_layer_bwd (the bf16 backward, with
+ * the bf16 weights) then runs on this forward's state: MXFP8 forward, bf16 data and weight
+ * gradients.  Workspace MOE_WS_LAYER_FWD; d and f multiples of 32; cfg->dtype MOE_DTYPE_BF16. */
 int moe_layer_fwd_mxfp8(const moe_cfg* cfg, const void* x, const void* W_r, const float* b_r,
                         const moe_mxfp8_experts* mx, const void* Ws1, const void* Ws2,
                         const void* w_sg, void* y, const moe_saved* saved, void* ws,

@@ -1315,9 +1315,10 @@ static int layer_fwd_impl(const moe_cfg* c, const void* x, const void* W_r, cons
     MOE_TRY(launch_permute_quant_e4m3(x, s->slot_of_pair, q->x_perm_q, sq ? q->x_q : nullptr,
                                       q->scales + 0, q->scales + 1, c->T, c->d, c->k, st));
   // MXFP8: x permuted and block-quantised in one pass, its scales in the row tiles of the routing
+  // (and the permuted bf16 rows into saved.x_perm when given, for a bf16 backward)
   if (mx)
     MOE_TRY(launch_permute_quant_mx(x, s->slot_of_pair, s->offsets, mx->x_perm_q, mx->x_perm_s,
-                                    c->T, c->d, c->k, c->E, st));
+                                    c->T, c->d, c->k, c->E, st, s->x_perm));
   if (side) {
     side_lk.lock();
     if (cudaEventRecord(side->fork, st) != cudaSuccess ||
@@ -1336,9 +1337,10 @@ static int layer_fwd_impl(const moe_cfg* c, const void* x, const void* W_r, cons
                              q->W2_q, q->W2_scale, s->h, s->act, q->h_q, q->scales + 2,
                              q->scales + 3, s->y_perm, st));
   } else if (mx) {
-    // MXFP8 experts (a forward without a backward: bf16 h and [a | u] are not written)
+    // MXFP8 experts; bf16 h and [a | u] written only into the saved buffers given (what the bf16
+    // backward reads)
     MOE_TRY(ffn_fwd_mx_impl(c, s->offsets, Nrows(c), mx->x_perm_q, mx->x_perm_s, mx->W1_q,
-                            mx->W1_sp, mx->W2_q, mx->W2_sp, nullptr, nullptr, mx->h_q, mx->h_s,
+                            mx->W1_sp, mx->W2_q, mx->W2_sp, s->h, s->act, mx->h_q, mx->h_s,
                             s->y_perm, st));
   } else if (permute_fused(c)) {
     // "Megatron-Bridge 深度剖析", §Permute Fusion: fc1 gathers its rows from x by token_of_slot

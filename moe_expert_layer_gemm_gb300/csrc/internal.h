@@ -238,9 +238,10 @@ int launch_mx_quantize(const void* x, int64_t rows, int cols, uint8_t* q, uint8_
 int launch_mx_pack_weight_scales(const uint8_t* s, int E, int R, int K, int swiglu_f,
                                  uint8_t* packed, cudaStream_t st);
 // Permute + quantise: x_perm_q[slot(t, j)] = MXFP8 codes of x[t], scales in the packed
-// activation layout (row tiles from the routing offsets).
+// activation layout (row tiles from the routing offsets); xp (optional): the bf16 rows too.
 int launch_permute_quant_mx(const void* x, const int32_t* sop, const int32_t* offsets,
-                            uint8_t* xq, uint8_t* xs, int T, int d, int k, int E, cudaStream_t st);
+                            uint8_t* xq, uint8_t* xs, int T, int d, int k, int E, cudaStream_t st,
+                            void* xp = nullptr);
 
 int gemm_tc(const GemmDesc& g, cudaStream_t st);     // bf16 tcgen05 path (gemm_tc.cu)
 int gemm_simt(const GemmDesc& g, cudaStream_t st);   // fp32 CUDA-core path (gemm_simt.cu)

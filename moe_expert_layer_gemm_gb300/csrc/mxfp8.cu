@@ -12,7 +12,8 @@
 //                          matrix)
 //   mx_pack_wscales_kernel row-major weight scales -> the packed per-tile layout the GEMMs read
 //   permute_quant_mx_kernel  x [T, d] -> the permuted codes x_perm_q[slot] and its scales in the
-//                          packed activation layout (row tiles from the routing offsets)
+//                          packed activation layout (row tiles from the routing offsets), and
+//                          optionally the permuted bf16 rows themselves (for a bf16 backward)
 #include "common.cuh"
 #include "internal.h"
 
@@ -94,11 +95,13 @@ __global__ void __launch_bounds__(256) mx_pack_wscales_kernel(const uint8_t* __r
 
 // Permute + quantise, one warp per token: lane L quantises columns 8L.. of each 256-column step,
 // four lanes make one 32-block (amax over the four by shuffles).  Codes go to every slot of the
-// token; the block's scale byte to each slot's place in the packed activation layout.
+// token; the block's scale byte to each slot's place in the packed activation layout; with xp,
+// the bf16 row to each slot too.
 constexpr int MXP_THREADS = 256;
 __global__ void __launch_bounds__(MXP_THREADS) permute_quant_mx_kernel(
     const bf16* __restrict__ x, const int32_t* __restrict__ sop, const int32_t* __restrict__ offsets,
-    uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, int Tn, int d, int k, int E, int* err) {
+    uint8_t* __restrict__ xq, uint8_t* __restrict__ xs, bf16* __restrict__ xp, int Tn, int d, int k,
+    int E, int* err) {
   __shared__ int s_off[MOE_MAX_EXPERTS + 1];
   __shared__ int s_pre[MOE_MAX_EXPERTS + 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -159,7 +162,8 @@ __global__ void __launch_bounds__(MXP_THREADS) permute_quant_mx_kernel(
       const int c = c0 + lane * 8;
       const bool act = c < d;   // d % 32 == 0: a 4-lane group is all in or all out
       float f[8];
-      if (act) unpack16(ld_nc16(src + c), f, static_cast<const bf16*>(nullptr));
+      const uint4 raw = act ? ld_nc16(src + c) : make_uint4(0, 0, 0, 0);
+      unpack16(raw, f, static_cast<const bf16*>(nullptr));
       float m = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) m = act ? fmaxf(m, fabsf(f[i])) : m;
@@ -183,6 +187,7 @@ __global__ void __launch_bounds__(MXP_THREADS) permute_quant_mx_kernel(
         if (j >= k) break;
         if (slot[j] < 0) continue;
         *reinterpret_cast<uint2*>(xq + static_cast<int64_t>(slot[j]) * d + c) = make_uint2(w[0], w[1]);
+        if (xp) *reinterpret_cast<uint4*>(xp + static_cast<int64_t>(slot[j]) * d + c) = raw;
         if (writes_scale) {
           uint8_t* sf = xs + sfb[j] + (blk >> 2) * MX_CHUNK;
           sf[blk & 3] = static_cast<uint8_t>(e + 127);
@@ -221,13 +226,14 @@ int launch_mx_pack_weight_scales(const uint8_t* s, int E, int R, int K, int swig
 }
 
 int launch_permute_quant_mx(const void* x, const int32_t* sop, const int32_t* offsets,
-                            uint8_t* xq, uint8_t* xs, int T, int d, int k, int E, cudaStream_t st) {
+                            uint8_t* xq, uint8_t* xs, int T, int d, int k, int E, cudaStream_t st,
+                            void* xp) {
   const int wpb = MXP_THREADS / 32;
   int rb = (T + wpb - 1) / wpb;
   if (rb > num_sms() * 8) rb = num_sms() * 8;
   return launch("mxfp8_permute_quantize", permute_quant_mx_kernel, dim3(rb), dim3(MXP_THREADS), 0,
-                st, static_cast<const bf16*>(x), sop, offsets, xq, xs, T, d, k, E,
-                device_error_word());
+                st, static_cast<const bf16*>(x), sop, offsets, xq, xs, static_cast<bf16*>(xp), T, d,
+                k, E, device_error_word());
 }
 
 }  // namespace moe

@@ -30,6 +30,10 @@ CASES = {
     "bf16_single_expert": LayerConfig("bf16 e", 130, 128, 1, 1, 136),
     "bf16_256_experts": LayerConfig("bf16 f", 400, 128, 256, 8, 64, f_shared=64, shared_gate=1),
     "bf16_wide_rows": LayerConfig("bf16 g", 1100, 1024, 8, 2, 320, score_fn=SIGMOID, renorm=1),
+    # a handful of tokens: one partial row tile per live expert, most experts without rows
+    "bf16_one_token": LayerConfig("bf16 h", 1, 128, 8, 2, 64, f_shared=64, shared_gate=1),
+    "bf16_seven_tokens_128e": LayerConfig("bf16 i", 7, 256, 128, 8, 128, score_fn=SIGMOID,
+                                          renorm=1),
 }
 
 

@@ -25,8 +25,8 @@ import moe_inputs
 import oracle.moe_oracle as O
 import oracle.mxfp8_oracle as MX
 
-from .helpers import (assert_close, mx_act_pad_bytes, mx_unpack_act_scales, mx_weight_index, np64,
-                      oracle_layer, rel_err, run_layer)
+from .helpers import (assert_close, clean_inputs, mx_act_pad_bytes, mx_unpack_act_scales,
+                      mx_weight_index, np64, oracle_layer, rel_err, run_layer)
 
 pytestmark = pytest.mark.gpu
 
@@ -248,3 +248,56 @@ def test_mxfp8_layer_forward_is_the_composed_stages(name):
     e = rel_err(np64(y), ref["fwd"]["y"])
     assert e < 0.15, e
     print(f"{name}: y vs unquantised {e:.3f}")
+
+
+def test_mxfp8_forward_saves_the_bf16_state_for_the_bf16_backward():
+    """With saved.x_perm / act / h given, moe_layer_fwd_mxfp8 writes the permuted bf16 rows, the bf16
+    [a | u] and h of its MXFP8 products (bit-identical to the stage calls), y is unchanged, and
+    moe_layer_bwd on that state gives gradients within the forward's rounding of the oracle's."""
+    lc = LAYER_CASES["sigmoid-shared"]
+    host, _ = clean_inputs(lc)       # routing clear of near-ties: the oracle selects the same sets
+    inp = {k: (None if v is None else v.cuda()) for k, v in host.items()}
+    cfg = moe.cfg_from(lc)
+    m = moe.alloc_mxfp8_experts(cfg, inp["W1"], inp["W2"])
+    ws_f = moe.workspace(cfg, moe.WS_LAYER_FWD)
+    lean = moe.alloc_saved(cfg)
+    lean["x_perm"] = lean["act"] = lean["h"] = None
+    y0 = torch.empty_like(inp["x"])
+    moe.moe_layer_fwd_mxfp8(cfg, inp["x"], inp["W_r"], inp["b_r"], m, inp["Ws1"], inp["Ws2"],
+                            inp["w_sg"], y0, lean, ws_f)
+    saved = moe.alloc_saved(cfg)
+    y = torch.empty_like(inp["x"])
+    moe.moe_layer_fwd_mxfp8(cfg, inp["x"], inp["W_r"], inp["b_r"], m, inp["Ws1"], inp["Ws2"],
+                            inp["w_sg"], y, saved, ws_f)
+    sync()
+    assert torch.equal(y, y0)
+    xp = torch.empty_like(saved["x_perm"])
+    moe.moe_permute(cfg, inp["x"], saved["slot_of_pair"], xp)
+    h = torch.empty_like(saved["h"])
+    act = torch.empty_like(saved["act"])
+    moe.moe_grouped_swiglu_fwd_mxfp8(cfg, m["x_perm_q"], m["x_perm_s"], saved["offsets"], m["W1_q"],
+                                     m["W1_sp"], m["W2_q"], m["W2_sp"], h, act,
+                                     torch.empty_like(m["h_q"]), torch.empty_like(m["h_s"]),
+                                     torch.empty_like(saved["y_perm"]))
+    sync()
+    assert torch.equal(saved["x_perm"], xp)
+    assert torch.equal(saved["h"], h) and torch.equal(saved["act"], act)
+    f32 = torch.float32
+    E, d, f, fs = lc.E, lc.d, lc.f, lc.f_shared
+    g = dict(dx=torch.empty_like(inp["x"]), dW_r=torch.empty(E, d, dtype=f32, device="cuda"),
+             dW1=torch.empty(E, 2 * f, d, dtype=f32, device="cuda"),
+             dW2=torch.empty(E, d, f, dtype=f32, device="cuda"),
+             dWs1=torch.empty(2 * fs, d, dtype=f32, device="cuda"),
+             dWs2=torch.empty(d, fs, dtype=f32, device="cuda"))
+    moe.moe_layer_bwd(cfg, inp["dy"], inp["x"], inp["W_r"], inp["W1"], inp["W2"], inp["Ws1"],
+                      inp["Ws2"], None, saved, g["dx"], g["dW_r"], g["dW1"], g["dW2"], g["dWs1"],
+                      g["dWs2"], None, moe.workspace(cfg, moe.WS_LAYER_BWD))
+    sync()
+    ref = oracle_layer(lc, {k: (None if v is None else v.cpu()) for k, v in inp.items()})
+    errs = {}
+    for name in ("dx", "dW1", "dW2", "dW_r", "dWs1", "dWs2"):
+        gpu = np64(g[name])
+        assert np.isfinite(gpu).all(), name
+        errs[name] = rel_err(gpu, ref["bwd"][name])
+        assert errs[name] < 0.15, (name, errs[name])
+    print("mxfp8 forward + bf16 backward vs unquantised:", {k: f"{v:.3f}" for k, v in errs.items()})
