@@ -474,7 +474,8 @@ def run_gpu(args, lc):
     down_s.wait_stream(stream)
     with torch.cuda.stream(up_s):
         x_d[0].copy_(x_h[0], non_blocking=True)
-        dy_d[0].copy_(dy_h[0], non_blocking=True)
+        if lc.backward:                    # a forward-only step reads no dy
+            dy_d[0].copy_(dy_h[0], non_blocking=True)
         uploaded[0].record(up_s)
     for i in range(e2e_steps):
         b = i & 1
@@ -492,7 +493,8 @@ def run_gpu(args, lc):
                 if i >= 1:
                     up_s.wait_event(computed[nb])  # step i-1 no longer reads x_d[nb], dy_d[nb]
                 x_d[nb].copy_(x_h[nb], non_blocking=True)
-                dy_d[nb].copy_(dy_h[nb], non_blocking=True)
+                if lc.backward:
+                    dy_d[nb].copy_(dy_h[nb], non_blocking=True)
                 uploaded[nb].record(up_s)
         with torch.cuda.stream(down_s):
             down_s.wait_event(computed[b])
@@ -507,7 +509,7 @@ def run_gpu(args, lc):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     e2e_value = replica_throughput(lc.T, e2e_steps, world, e2e_ms)
     esz = inp["x"].element_size()
-    h2d = 2 * lc.T * lc.d * esz
+    h2d = (2 if lc.backward else 1) * lc.T * lc.d * esz
     d2h = 2 * lc.T * lc.d * esz if lc.backward else lc.T * lc.d * esz
     assert torch.equal(y_h[(e2e_steps - 1) & 1].to(dev), y), "e2e output differs from the device run"
 
