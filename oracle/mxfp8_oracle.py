@@ -101,3 +101,50 @@ def fc2_mx(hq, hs, W2q, W2s, offsets):
             y[lo:hi] = H[lo:hi] @ mx_decode(W2q[e], W2s[e]).T
     return y
 
+
+
+# ----------------------------------------------------------------------------- data gradients
+# Readings (the pages fix none of it): the data gradients run on MXFP8 operands with blocks along
+# each product's own reduction dimension -- dy_perm [N, d] in row blocks along d for fc2's data
+# gradient, [da | du] [N, 2f] in row blocks along 2f for fc1's; the weights in blocks along their
+# first (K) dimension: W2 [d, f] in 32-row blocks along d, W1 [2f, d] in 32-row blocks along 2f
+# (the "columnwise" copies; the forward's copies block the other dimension).  [da | du] is
+# quantised from its bf16 value.  The weight gradients stay out of this (they reduce over tokens).
+
+def mx_quantize_cols(x, block=BLOCK):
+    """MXFP8 codes of x in blocks of 32 consecutive rows (along axis -2), one scale per block and
+    column.  Returns (codes with x's shape, scale bytes [..., R / block, C])."""
+    x64 = np.asarray(x, dtype=np.float64)
+    q, s = mx_quantize(np.swapaxes(x64, -1, -2), block)
+    return np.ascontiguousarray(np.swapaxes(q, -1, -2)), np.ascontiguousarray(np.swapaxes(s, -1, -2))
+
+
+def mx_decode_cols(codes, scales, block=BLOCK):
+    """Decoded values of row-blocked codes: code value times 2^(its block's byte - 127)."""
+    v = mx_decode(np.swapaxes(np.asarray(codes), -1, -2), np.swapaxes(np.asarray(scales), -1, -2),
+                  block)
+    return np.swapaxes(v, -1, -2)
+
+
+def fc2_dgrad_mx(dyq, dys, W2cq, W2cs, offsets):
+    """dh[s] = dec(dyq[s], dys[s]) . decc(W2cq[e], W2cs[e]) for the rows s of expert e: [N, f]."""
+    E, d, f = W2cq.shape
+    DY = mx_decode(dyq, dys)
+    dh = np.zeros((DY.shape[0], f))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            dh[lo:hi] = DY[lo:hi] @ mx_decode_cols(W2cq[e], W2cs[e])
+    return dh
+
+
+def fc1_dgrad_mx(dHq, dHs, W1cq, W1cs, offsets):
+    """dx_perm[s] = dec(dHq[s], dHs[s]) . decc(W1cq[e], W1cs[e]) for the rows s of expert e: [N, d]."""
+    E, two_f, d = W1cq.shape
+    DH = mx_decode(dHq, dHs)
+    dx = np.zeros((DH.shape[0], d))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            dx[lo:hi] = DH[lo:hi] @ mx_decode_cols(W1cq[e], W1cs[e])
+    return dx

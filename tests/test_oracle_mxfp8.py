@@ -118,6 +118,58 @@ def test_block_scaled_swiglu_equals_library_on_representable_operands():
         assert np.allclose(y[lo:hi], (Hd @ torch.from_numpy(W2[e]).T).numpy(), rtol=1e-12, atol=0)
 
 
+def grid_cols(rng, R, C, shifts):
+    """An R x C matrix on the E4M3 grid with a power-of-two scale per 32-row block and column
+    (shifts [R/32, C]): its column blocks quantise exactly, with exponents `shifts`."""
+    return np.swapaxes(grid_blocks(rng, C, R, shifts.T), 0, 1)
+
+
+def test_column_blocks_round_trip_and_their_scales():
+    rng = np.random.default_rng(4)
+    R, C = 96, 40
+    shifts = rng.integers(-9, 9, size=(R // 32, C))
+    x = grid_cols(rng, R, C, shifts)
+    q, s = MX.mx_quantize_cols(x)
+    assert s.shape == (R // 32, C)
+    assert np.array_equal(s.astype(np.int64) - 127, shifts)
+    assert np.array_equal(MX.mx_decode_cols(q, s), x)
+    # one block by hand: rows 32..63 of column 5 scaled by 2^3 carry exponent 3
+    y = np.zeros((64, 8))
+    y[40, 5], y[33, 5] = 448.0 * 8, -3.0
+    qy, sy = MX.mx_quantize_cols(y)
+    # -3 / 2^3 = -0.375 = -1.5 * 2^-2: sign, exponent field 5, mantissa 4 -> 0xAC
+    assert sy[1, 5] == 130 and sy[0, 5] == 0 and qy[40, 5] == 0x7E and qy[33, 5] == 0xAC
+
+
+def test_block_scaled_data_gradients_equal_library_on_representable_operands():
+    """dy and [da | du] on the grid in row blocks, W2 and W1 on the grid in column blocks, each
+    block with its own power of two: quantisation is exact, so fc2's and fc1's data gradients
+    must equal torch's fp64 products of the unquantised operands."""
+    rng = np.random.default_rng(5)
+    E, f, d, N = 3, 64, 96, 20
+    offsets = np.array([0, 9, 9, 20])
+    dy = grid_blocks(rng, N, d, rng.integers(-8, 0, size=(N, d // 32)))
+    dH = grid_blocks(rng, N, 2 * f, rng.integers(-8, 0, size=(N, 2 * f // 32)))
+    W2 = np.stack([grid_cols(rng, d, f, rng.integers(-12, -4, size=(d // 32, f))) for _ in range(E)])
+    W1 = np.stack([grid_cols(rng, 2 * f, d, rng.integers(-12, -4, size=(2 * f // 32, d)))
+                   for _ in range(E)])
+    dyq, dys = MX.mx_quantize(dy)
+    dHq, dHs = MX.mx_quantize(dH)
+    W2q, W2s = MX.mx_quantize_cols(W2)
+    W1q, W1s = MX.mx_quantize_cols(W1)
+    dh = MX.fc2_dgrad_mx(dyq, dys, W2q, W2s, offsets)
+    dx = MX.fc1_dgrad_mx(dHq, dHs, W1q, W1s, offsets)
+    for e in range(E):
+        lo, hi = offsets[e], offsets[e + 1]
+        if hi == lo:
+            continue
+        ref_dh = (torch.from_numpy(dy[lo:hi]) @ torch.from_numpy(W2[e])).numpy()
+        ref_dx = (torch.from_numpy(dH[lo:hi]) @ torch.from_numpy(W1[e])).numpy()
+        assert np.allclose(dh[lo:hi], ref_dh, rtol=1e-12, atol=0)
+        assert np.allclose(dx[lo:hi], ref_dx, rtol=1e-12, atol=0)
+    assert not dh[9:9].any()
+
+
 def _pins_pass():
     try:
         test_shared_exponent_closed_forms()
@@ -125,6 +177,8 @@ def _pins_pass():
         test_codes_match_library_after_block_division()
         test_error_bound_and_saturation()
         test_block_scaled_swiglu_equals_library_on_representable_operands()
+        test_column_blocks_round_trip_and_their_scales()
+        test_block_scaled_data_gradients_equal_library_on_representable_operands()
     except AssertionError:
         return False
     return True
@@ -157,6 +211,9 @@ def _exponent_ceil(amax):
     return np.clip(np.where(a > 0, ce - 8, -127), -127, 127).astype(np.int64)
 
 
+_mx_quantize_cols = MX.mx_quantize_cols
+_mx_decode_cols = MX.mx_decode_cols
+
 MUTANTS = {
     "exponent_ceil": ("shared_exponent", lambda a: _exponent_ceil(a)),
     "emax_7": ("shared_exponent", lambda a: np.maximum(_shared_exponent(a) + 1, -127)),
@@ -164,6 +221,11 @@ MUTANTS = {
     "half_block_amax": ("mx_quantize", _quantize_first_half_amax),
     "scales_reversed": ("mx_decode", _decode_blocks_reversed),
     "scale_not_applied": ("mx_decode", lambda c, s, block=32: F8.e4m3_decode(np.asarray(c))),
+    # column blocks: each block decoded with its neighbour's scales; exponents one too large
+    "column_scales_rolled": ("mx_decode_cols", lambda c, s, block=32: _mx_decode_cols(
+        c, np.roll(np.asarray(s), 1, axis=-2), block)),
+    "column_exponent_plus_one": ("mx_quantize_cols", lambda x, block=32: (
+        _mx_quantize_cols(x, block)[0], (_mx_quantize_cols(x, block)[1] + 1).astype(np.uint8))),
 }
 
 
