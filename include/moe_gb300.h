@@ -271,7 +271,14 @@ int moe_grouped_swiglu_bwd_fp8(const moe_cfg* cfg, const uint8_t* x_perm_q, cons
  *     rows 96t..96t+95 then up rows f+96t..f+96t+95; fc2 tile t: rows 192t..192t+191) and per
  *     128-element K chunk kc, two such chunks (tile rows 0..127, 128..255) at
  *     ((e * tiles + t) * ceil(K/128) + kc) * 1024; rows and blocks past the weight are 127. */
-enum { MOE_MX_SCALES_X = 0, MOE_MX_SCALES_H = 1, MOE_MX_SCALES_W1 = 2, MOE_MX_SCALES_W2 = 3 };
+enum { MOE_MX_SCALES_X = 0, MOE_MX_SCALES_H = 1, MOE_MX_SCALES_W1 = 2, MOE_MX_SCALES_W2 = 3,
+       MOE_MX_SCALES_DH1 = 4, MOE_MX_SCALES_W1C = 5, MOE_MX_SCALES_W2C = 6 };
+/* The data gradients' layouts: MOE_MX_SCALES_DH1 is [da | du] [N,2f] in the activation layout
+ * (K = 2f).  MOE_MX_SCALES_W1C / _W2C are the weights blocked down their rows (W1 [2f,d] along 2f,
+ * W2 [d,f] along d, as moe_mxfp8_prepare_dgrad_weights makes them): per expert, per tile of 128
+ * columns (d for W1, f for W2) and per 128-row K chunk, one 512-byte chunk at
+ * ((e * tiles + t) * ceil(K/128) + kc) * 512, byte (c % 32) * 16 + (c / 32) * 4 + j for column c
+ * of the tile and block j of the chunk; columns and blocks past the weight are 127. */
 /* Bytes of one packed scale buffer for cfg (0 for an invalid cfg or `which`). */
 size_t moe_mxfp8_scale_bytes(const moe_cfg* cfg, int which);
 
@@ -325,6 +332,43 @@ typedef struct moe_mxfp8_experts {
   uint8_t* h_q;
   uint8_t* h_s;
 } moe_mxfp8_experts;
+
+/* The data gradients' copies of the expert weights, blocked along the dimension the data
+ * gradients reduce over: W1 [E,2f,d] in 32-row blocks along 2f, W2 [E,d,f] in 32-row blocks along d
+ * (codes W1c_q / W2c_q in the weights' layouts; plain scales W1c_s [E,2f/32,d], W2c_s [E,d/32,f];
+ * packed W1c_sp (MOE_MX_SCALES_W1C bytes), W2c_sp (MOE_MX_SCALES_W2C)).  Done once per weight
+ * update, beside moe_quantize_mxfp8 / moe_mxfp8_pack_expert_scales for the forward's copies. */
+int moe_mxfp8_prepare_dgrad_weights(const moe_cfg* cfg, const void* W1, const void* W2,
+                                    uint8_t* W1c_q, uint8_t* W1c_s, uint8_t* W1c_sp,
+                                    uint8_t* W2c_q, uint8_t* W2c_s, uint8_t* W2c_sp, void* stream);
+
+/* The routed experts' data gradients on MXFP8 operands: dy_perm [N,d] (bf16, rows in expert order)
+ * quantised along d into dy_q, dy_s (MOE_MX_SCALES_X layout); for rows s of expert e
+ *   dh[s] = dec(dy_q[s], dy_s) . decc(W2c_q[e], W2c_sp)       (fp32 accumulation)
+ *   [da | du] = SwiGLU backward of dh at act[s] ([a | u], bf16 [N,2f]), rounded to bf16: written to
+ *     dH1 [N,2f] unless NULL, and quantised along 2f into dH1_q, dH1_s (MOE_MX_SCALES_DH1);
+ *   dx_perm[s] = dec(dH1_q[s], dH1_s) . decc(W1c_q[e], W1c_sp)  (bf16 [N,d])
+ * with the weights' column-blocked copies (moe_mxfp8_prepare_dgrad_weights).  d and f multiples of
+ * 32; cfg->dtype MOE_DTYPE_BF16. */
+int moe_grouped_swiglu_dgrad_mxfp8(const moe_cfg* cfg, const void* dy_perm, const int32_t* offsets,
+                                   const void* act, const uint8_t* W1c_q, const uint8_t* W1c_sp,
+                                   const uint8_t* W2c_q, const uint8_t* W2c_sp, uint8_t* dy_q,
+                                   uint8_t* dy_s, void* dH1, uint8_t* dH1_q, uint8_t* dH1_s,
+                                   void* dx_perm, void* stream);
+
+/* MXFP8 data-gradient state for moe_layer_bwd_mxfp8: the weights' column-blocked copies (read
+ * only) and the buffers the backward writes (dy_q [N,d], dy_s MOE_MX_SCALES_X bytes, dH1_q
+ * [N,2f], dH1_s MOE_MX_SCALES_DH1 bytes). */
+typedef struct moe_mxfp8_dgrad {
+  const uint8_t* W1c_q;
+  const uint8_t* W1c_sp;
+  const uint8_t* W2c_q;
+  const uint8_t* W2c_sp;
+  uint8_t* dy_q;
+  uint8_t* dy_s;
+  uint8_t* dH1_q;
+  uint8_t* dH1_s;
+} moe_mxfp8_dgrad;
 
 /* Unpermute + weighted combine: "Megatron-Bridge 深度剖析", §Expert Parallel 基础 (Step 3,
  * results sent back to token order) and §Shared Expert Overlap (shared output added).
@@ -453,6 +497,17 @@ typedef struct moe_fp8_experts {
 int moe_layer_fwd_mxfp8(const moe_cfg* cfg, const void* x, const void* W_r, const float* b_r,
                         const moe_mxfp8_experts* mx, const void* Ws1, const void* Ws2,
                         const void* w_sg, void* y, const moe_saved* saved, void* ws,
+                        size_t ws_bytes, void* stream);
+
+/* The layer backward after moe_layer_fwd_mxfp8 (given saved.x_perm, act and h): moe_layer_bwd,
+ * except that the routed experts' data gradients run on MXFP8 operands
+ * (moe_grouped_swiglu_dgrad_mxfp8 on mxd's weights and buffers); their weight gradients stay bf16
+ * products of the saved bf16 x_perm and h with the bf16 dy_perm and [da | du] (fp32 out), as do
+ * the router's and the shared expert's backward.  Workspace MOE_WS_LAYER_BWD. */
+int moe_layer_bwd_mxfp8(const moe_cfg* cfg, const void* dy, const void* x, const void* W_r,
+                        const moe_mxfp8_dgrad* mxd, const void* Ws1, const void* Ws2,
+                        const void* w_sg, const moe_saved* saved, void* dx, float* dW_r,
+                        float* dW1, float* dW2, float* dWs1, float* dWs2, float* dw_sg, void* ws,
                         size_t ws_bytes, void* stream);
 
 /* moe_layer_fwd with the routed experts on E4M3 operands: x is permuted and quantised in one

@@ -23,7 +23,8 @@ SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 DTYPE_BF16, DTYPE_F32 = 0, 1
 BIAS_LOGIT, BIAS_SELECT = 0, 1
 WS_ROUTE, WS_FFN_FWD, WS_FFN_BWD, WS_LAYER_FWD, WS_LAYER_BWD, WS_FFN_BWD_FP8, WS_LAYER_BWD_FP8 = range(7)
-MX_SCALES_X, MX_SCALES_H, MX_SCALES_W1, MX_SCALES_W2 = range(4)
+MX_SCALES_X, MX_SCALES_H, MX_SCALES_W1, MX_SCALES_W2, MX_SCALES_DH1, MX_SCALES_W1C, MX_SCALES_W2C = \
+    range(7)
 
 
 class MoeCfg(ctypes.Structure):
@@ -49,6 +50,11 @@ class MoeMxfp8Experts(ctypes.Structure):
                 ("W1_q", "W1_sp", "W2_q", "W2_sp", "x_perm_q", "x_perm_s", "h_q", "h_s")]
 
 
+class MoeMxfp8Dgrad(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("W1c_q", "W1c_sp", "W2c_q", "W2c_sp", "dy_q", "dy_s", "dH1_q", "dH1_s")]
+
+
 _VP = ctypes.c_void_p
 _SZ = ctypes.c_size_t
 _CFG = ctypes.POINTER(MoeCfg)
@@ -72,6 +78,10 @@ _SIGS = {
     "moe_grouped_swiglu_fwd_mxfp8": (ctypes.c_int, [_CFG] + [_VP] * 13),
     "moe_layer_fwd_mxfp8": (ctypes.c_int, [_CFG] + [_VP] * 3 + [ctypes.POINTER(MoeMxfp8Experts)]
                             + [_VP] * 4 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP]),
+    "moe_mxfp8_prepare_dgrad_weights": (ctypes.c_int, [_CFG] + [_VP] * 9),
+    "moe_grouped_swiglu_dgrad_mxfp8": (ctypes.c_int, [_CFG] + [_VP] * 14),
+    "moe_layer_bwd_mxfp8": (ctypes.c_int, [_CFG] + [_VP] * 3 + [ctypes.POINTER(MoeMxfp8Dgrad)]
+                            + [_VP] * 3 + [ctypes.POINTER(MoeSaved)] + [_VP] * 8 + [_SZ, _VP]),
     "moe_unpermute_combine": (ctypes.c_int, [_CFG] + [_VP] * 7),
     "moe_unpermute_combine_bwd": (ctypes.c_int, [_CFG] + [_VP] * 11),
     "moe_layer_fwd": (ctypes.c_int, [_CFG] + [_VP] * 9 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP]),
@@ -311,6 +321,51 @@ def moe_layer_fwd_mxfp8(cfg, x, W_r, b_r, mx, Ws1, Ws2, w_sg, y, saved, ws, stre
     _check(lib().moe_layer_fwd_mxfp8(ctypes.byref(cfg), _p(x), _p(W_r), _p(b_r), ctypes.byref(ms),
                                      _p(Ws1), _p(Ws2), _p(w_sg), _p(y), ctypes.byref(st), _p(ws),
                                      ws.numel(), _stream(stream)), "moe_layer_fwd_mxfp8")
+
+
+def alloc_mxfp8_dgrad(cfg, W1, W2, device="cuda", stream=None):
+    """The data gradients' MXFP8 state (torch tensors): W1 and W2 quantised once in blocks down
+    their rows (codes, plain and packed scales), and the buffers the MXFP8 backward writes."""
+    import torch
+    E, d, f = cfg.E, cfg.d, cfg.f
+    N = max(cfg.T, 1) * cfg.k
+    u8 = torch.uint8
+    m = dict(W1c_q=torch.empty(E, 2 * f, d, dtype=u8, device=device),
+             W1c_s=torch.empty(E, 2 * f // 32, d, dtype=u8, device=device),
+             W1c_sp=torch.empty(mxfp8_scale_bytes(cfg, MX_SCALES_W1C), dtype=u8, device=device),
+             W2c_q=torch.empty(E, d, f, dtype=u8, device=device),
+             W2c_s=torch.empty(E, d // 32, f, dtype=u8, device=device),
+             W2c_sp=torch.empty(mxfp8_scale_bytes(cfg, MX_SCALES_W2C), dtype=u8, device=device),
+             dy_q=torch.empty(N, d, dtype=u8, device=device),
+             dy_s=torch.empty(mxfp8_scale_bytes(cfg, MX_SCALES_X), dtype=u8, device=device),
+             dH1_q=torch.empty(N, 2 * f, dtype=u8, device=device),
+             dH1_s=torch.empty(mxfp8_scale_bytes(cfg, MX_SCALES_DH1), dtype=u8, device=device))
+    _check(lib().moe_mxfp8_prepare_dgrad_weights(
+        ctypes.byref(cfg), _p(W1), _p(W2), _p(m["W1c_q"]), _p(m["W1c_s"]), _p(m["W1c_sp"]),
+        _p(m["W2c_q"]), _p(m["W2c_s"]), _p(m["W2c_sp"]), _stream(stream)),
+        "moe_mxfp8_prepare_dgrad_weights")
+    return m
+
+
+def moe_grouped_swiglu_dgrad_mxfp8(cfg, dy_perm, offsets, act, mxd, dH1, dx_perm, stream=None):
+    _check(lib().moe_grouped_swiglu_dgrad_mxfp8(
+        ctypes.byref(cfg), _p(dy_perm), _p(offsets), _p(act), _p(mxd["W1c_q"]), _p(mxd["W1c_sp"]),
+        _p(mxd["W2c_q"]), _p(mxd["W2c_sp"]), _p(mxd["dy_q"]), _p(mxd["dy_s"]), _p(dH1),
+        _p(mxd["dH1_q"]), _p(mxd["dH1_s"]), _p(dx_perm), _stream(stream)),
+        "moe_grouped_swiglu_dgrad_mxfp8")
+
+
+def mxd_struct(m):
+    return MoeMxfp8Dgrad(*[m[n].data_ptr() for n, _ in MoeMxfp8Dgrad._fields_])
+
+
+def moe_layer_bwd_mxfp8(cfg, dy, x, W_r, mxd, Ws1, Ws2, w_sg, saved, dx, dW_r, dW1, dW2, dWs1, dWs2,
+                        dw_sg, ws, stream=None):
+    st, ms = saved_struct(saved), mxd_struct(mxd)
+    _check(lib().moe_layer_bwd_mxfp8(ctypes.byref(cfg), _p(dy), _p(x), _p(W_r), ctypes.byref(ms),
+                                     _p(Ws1), _p(Ws2), _p(w_sg), ctypes.byref(st), _p(dx), _p(dW_r),
+                                     _p(dW1), _p(dW2), _p(dWs1), _p(dWs2), _p(dw_sg), _p(ws),
+                                     ws.numel(), _stream(stream)), "moe_layer_bwd_mxfp8")
 
 
 def moe_unpermute_combine(cfg, y_perm, gate, slot_of_pair, shared_out, shared_coef, y, stream=None):

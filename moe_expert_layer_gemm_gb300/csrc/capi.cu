@@ -1041,6 +1041,13 @@ size_t moe_mxfp8_scale_bytes(const moe_cfg* c, int which) {
       return static_cast<size_t>(c->E) * mx_fc1_tiles(c->f) * mx_kch(c->d) * MX_SFB_BYTES;
     case MOE_MX_SCALES_W2:
       return static_cast<size_t>(c->E) * mx_fc2_tiles(c->d) * mx_kch(c->f) * MX_SFB_BYTES;
+    case MOE_MX_SCALES_DH1: return static_cast<size_t>(mx_act_scale_bytes(N, c->E, 2 * c->f));
+    case MOE_MX_SCALES_W1C:   // W1 read as [2f (K), d (N)]: tiles of 128 columns of d
+      return static_cast<size_t>(c->E) * ((c->d + MX_BN_DGRAD - 1) / MX_BN_DGRAD) *
+             mx_kch(2 * c->f) * MX_CHUNK;
+    case MOE_MX_SCALES_W2C:   // W2 read as [d (K), f (N)]: tiles of 128 columns of f
+      return static_cast<size_t>(c->E) * ((c->f + MX_BN_DGRAD - 1) / MX_BN_DGRAD) * mx_kch(c->d) *
+             MX_CHUNK;
     default: return 0;
   }
 }
@@ -1099,6 +1106,188 @@ int moe_grouped_swiglu_fwd_mxfp8(const moe_cfg* c, const uint8_t* x_perm_q,
   if (N == 0) return MOE_OK;
   return ffn_fwd_mx_impl(c, offsets, N, x_perm_q, x_perm_s, W1_q, W1_sp, W2_q, W2_sp, h, act, h_q,
                          h_s, y_perm, S(stream));
+}
+
+// MXFP8 data gradients of the routed experts: dy_perm quantised along d (rows in expert order),
+// fc2's data gradient with the SwiGLU backward ([da | du] in bf16 when dH1 is given, and as
+// MXFP8 codes along 2f), fc1's data gradient.  The weights are the column-blocked copies, read in
+// their stored layouts (MN-major).
+static int dgrad_mx_impl(const moe_cfg* c, const int32_t* offsets, int64_t N, const void* dy_perm,
+                         const void* act, const uint8_t* W1c_q, const uint8_t* W1c_sp,
+                         const uint8_t* W2c_q, const uint8_t* W2c_sp, uint8_t* dy_q,
+                         uint8_t* dy_s, void* dH1, uint8_t* dH1_q, uint8_t* dH1_s, void* dx_perm,
+                         cudaStream_t st) {
+  const int d = c->d, f = c->f, E = c->E;
+  MOE_TRY(launch_permute_quant_mx(dy_perm, nullptr, offsets, dy_q, dy_s, static_cast<int>(N), d, 1,
+                                  E, st));
+  GemmDesc a = desc0();
+  a.name = "gemm_fc2_dgrad_mxfp8";
+  a.sched = RAGGED_M;
+  a.epi = EPI_SWIGLU_BWD;
+  a.G = E;
+  a.offsets = offsets;
+  a.M = static_cast<int>(N);
+  a.N = f;
+  a.K = d;
+  a.A = opnd(dy_q, N, d, false);
+  a.B = opnd(W2c_q, static_cast<int64_t>(E) * d, f, true);
+  a.b_group_rows = d;
+  a.f = f;
+  a.out = dH1;
+  a.ldo = 2 * f;
+  a.aux = act;
+  a.ld_aux = 2 * f;
+  a.fp8 = true;
+  a.mx = true;
+  a.sfa = dy_s;
+  a.sfb = W2c_sp;
+  a.q_out = dH1_q;
+  a.q_sf = dH1_s;
+  MOE_TRY(gemm_tc(a, st));
+  GemmDesc b = desc0();
+  b.name = "gemm_fc1_dgrad_mxfp8";
+  b.sched = RAGGED_M;
+  b.epi = EPI_STORE;
+  b.G = E;
+  b.offsets = offsets;
+  b.M = static_cast<int>(N);
+  b.N = d;
+  b.K = 2 * f;
+  b.A = opnd(dH1_q, N, 2 * f, false);
+  b.B = opnd(W1c_q, static_cast<int64_t>(E) * 2 * f, d, true);
+  b.b_group_rows = 2 * f;
+  b.out = dx_perm;
+  b.ldo = d;
+  b.fp8 = true;
+  b.mx = true;
+  b.sfa = dH1_s;
+  b.sfb = W1c_sp;
+  return gemm_tc(b, st);
+}
+
+// The routed experts' backward with MXFP8 data gradients and bf16 weight gradients: dy quantised;
+// fc2's data gradient + SwiGLU backward (dH1 in bf16 and MXFP8); fc2's weight gradient from the
+// bf16 dy_perm and h; fc1's data gradient on the MXFP8 dH1 (dx_perm may alias dy_perm: it is
+// written after fc2's weight gradient has read it); fc1's weight gradient from the bf16 dH1 and
+// x_perm.
+static int ffn_bwd_mx_impl(const moe_cfg* c, const int32_t* offsets, int64_t N, const void* x_perm,
+                           const void* act, const void* h, const void* dy_perm, void* dH1,
+                           void* dx_perm, float* dW1, float* dW2, int* sched, cudaStream_t st,
+                           const moe_mxfp8_dgrad* m) {
+  const int d = c->d, f = c->f, E = c->E;
+  MOE_TRY(launch_permute_quant_mx(dy_perm, nullptr, offsets, m->dy_q, m->dy_s, static_cast<int>(N),
+                                  d, 1, E, st));
+  GemmDesc a = desc0();
+  a.name = "gemm_fc2_dgrad_mxfp8";
+  a.sched = RAGGED_M;
+  a.epi = EPI_SWIGLU_BWD;
+  a.G = E;
+  a.offsets = offsets;
+  a.M = static_cast<int>(N);
+  a.N = f;
+  a.K = d;
+  a.A = opnd(m->dy_q, N, d, false);
+  a.B = opnd(m->W2c_q, static_cast<int64_t>(E) * d, f, true);
+  a.b_group_rows = d;
+  a.f = f;
+  a.out = dH1;
+  a.ldo = 2 * f;
+  a.aux = act;
+  a.ld_aux = 2 * f;
+  a.fp8 = true;
+  a.mx = true;
+  a.sfa = m->dy_s;
+  a.sfb = m->W2c_sp;
+  a.q_out = m->dH1_q;
+  a.q_sf = m->dH1_s;
+  MOE_TRY(gemm_tc(a, st));
+  GemmDesc b = desc0();
+  b.name = "gemm_fc2_wgrad";
+  b.sched = RAGGED_K;
+  b.epi = EPI_F32;
+  b.G = E;
+  b.offsets = offsets;
+  b.M = d;
+  b.N = f;
+  b.K = static_cast<int>(N);
+  b.A = opnd(dy_perm, N, d, true);
+  b.B = opnd(h, N, f, true);
+  b.out = dW2;
+  b.ldo = f;
+  b.out_group_stride = static_cast<int64_t>(d) * f;
+  b.tile_ctr = sched;
+  MOE_TRY(gemm_tc(b, st));
+  GemmDesc e = desc0();
+  e.name = "gemm_fc1_dgrad_mxfp8";
+  e.sched = RAGGED_M;
+  e.epi = EPI_STORE;
+  e.G = E;
+  e.offsets = offsets;
+  e.M = static_cast<int>(N);
+  e.N = d;
+  e.K = 2 * f;
+  e.A = opnd(m->dH1_q, N, 2 * f, false);
+  e.B = opnd(m->W1c_q, static_cast<int64_t>(E) * 2 * f, d, true);
+  e.b_group_rows = 2 * f;
+  e.out = dx_perm;
+  e.ldo = d;
+  e.fp8 = true;
+  e.mx = true;
+  e.sfa = m->dH1_s;
+  e.sfb = m->W1c_sp;
+  MOE_TRY(gemm_tc(e, st));
+  GemmDesc w = desc0();
+  w.name = "gemm_fc1_wgrad";
+  w.sched = RAGGED_K;
+  w.epi = EPI_F32;
+  w.G = E;
+  w.offsets = offsets;
+  w.M = 2 * f;
+  w.N = d;
+  w.K = static_cast<int>(N);
+  w.A = opnd(dH1, N, 2 * f, true);
+  w.B = opnd(x_perm, N, d, true);
+  w.out = dW1;
+  w.ldo = d;
+  w.out_group_stride = static_cast<int64_t>(2) * f * d;
+  w.tile_ctr = sched + 4;
+  return gemm_tc(w, st);
+}
+
+int moe_mxfp8_prepare_dgrad_weights(const moe_cfg* c, const void* W1, const void* W2,
+                                    uint8_t* W1c_q, uint8_t* W1c_s, uint8_t* W1c_sp,
+                                    uint8_t* W2c_q, uint8_t* W2c_s, uint8_t* W2c_sp, void* stream) {
+  MOE_TRY(check_mx_cfg(c));
+  const struct { const void* p; const char* n; } req[] = {
+      {W1, "W1"},       {W2, "W2"},         {W1c_q, "W1c_q"}, {W1c_s, "W1c_s"},
+      {W1c_sp, "W1c_sp"}, {W2c_q, "W2c_q"}, {W2c_s, "W2c_s"}, {W2c_sp, "W2c_sp"}};
+  for (const auto& r : req) MOE_TRY(check_ptr(r.p, r.n, true));
+  cudaStream_t st = S(stream);
+  const int E = c->E, d = c->d, f = c->f;
+  // W1 [E, 2f, d] in 32-row blocks along 2f; its columns (d) are the B-rows of fc1's data gradient
+  MOE_TRY(launch_mx_quantize_cols(W1, E, 2 * f, d, W1c_q, W1c_s, st));
+  MOE_TRY(launch_mx_pack_weight_scales(W1c_s, E, d, 2 * f, 0, W1c_sp, st, MX_BN_DGRAD, 1));
+  // W2 [E, d, f] in 32-row blocks along d; its columns (f) are the B-rows of fc2's data gradient
+  MOE_TRY(launch_mx_quantize_cols(W2, E, d, f, W2c_q, W2c_s, st));
+  return launch_mx_pack_weight_scales(W2c_s, E, f, d, 0, W2c_sp, st, MX_BN_DGRAD, 1);
+}
+
+int moe_grouped_swiglu_dgrad_mxfp8(const moe_cfg* c, const void* dy_perm, const int32_t* offsets,
+                                   const void* act, const uint8_t* W1c_q, const uint8_t* W1c_sp,
+                                   const uint8_t* W2c_q, const uint8_t* W2c_sp, uint8_t* dy_q,
+                                   uint8_t* dy_s, void* dH1, uint8_t* dH1_q, uint8_t* dH1_s,
+                                   void* dx_perm, void* stream) {
+  MOE_TRY(check_mx_cfg(c));
+  const struct { const void* p; const char* n; } req[] = {
+      {dy_perm, "dy_perm"}, {offsets, "offsets"}, {act, "act"},     {W1c_q, "W1c_q"},
+      {W1c_sp, "W1c_sp"},   {W2c_q, "W2c_q"},     {W2c_sp, "W2c_sp"}, {dy_q, "dy_q"},
+      {dy_s, "dy_s"},       {dH1_q, "dH1_q"},     {dH1_s, "dH1_s"},  {dx_perm, "dx_perm"}};
+  for (const auto& r : req) MOE_TRY(check_ptr(r.p, r.n, true));
+  MOE_TRY(check_ptr(dH1, "dH1", false));
+  const int64_t N = Nrows(c);
+  if (N == 0) return MOE_OK;
+  return dgrad_mx_impl(c, offsets, N, dy_perm, act, W1c_q, W1c_sp, W2c_q, W2c_sp, dy_q, dy_s, dH1,
+                       dH1_q, dH1_s, dx_perm, S(stream));
 }
 
 int moe_grouped_swiglu_bwd_fp8(const moe_cfg* c, const uint8_t* x_perm_q, const float* x_scale,
@@ -1367,15 +1556,26 @@ static int layer_bwd_impl(const moe_cfg* c, const void* dy, const void* x, const
                           const void* W1, const void* W2, const moe_fp8_experts* q,
                           const void* Ws1, const void* Ws2, const void* w_sg, const moe_saved* s,
                           void* dx, float* dW_r, float* dW1, float* dW2, float* dWs1,
-                          float* dWs2, float* dw_sg, void* ws, size_t ws_bytes, void* stream) {
+                          float* dWs2, float* dw_sg, void* ws, size_t ws_bytes, void* stream,
+                          const moe_mxfp8_dgrad* mxd = nullptr) {
   MOE_TRY(check_cfg(c));
   const bool sh = c->f_shared > 0, gt = c->shared_gate != 0;
   MOE_TRY(check_ptr(dy, "dy", true));
   MOE_TRY(check_ptr(x, "x", true));
   MOE_TRY(check_ptr(W_r, "W_r", true));
-  MOE_TRY(check_ptr(W1, "W1", !q));
-  MOE_TRY(check_ptr(W2, "W2", !q));
+  MOE_TRY(check_ptr(W1, "W1", !q && !mxd));
+  MOE_TRY(check_ptr(W2, "W2", !q && !mxd));
   if (q) MOE_TRY(check_fp8_experts(c, q));
+  if (mxd) {
+    MOE_TRY(check_mx_cfg(c));
+    if (permute_fused(c))
+      return fail(MOE_ERR_UNSUPPORTED, "the MXFP8 backward reads saved.x_perm (no fused permute)");
+    const struct { const void* p; const char* n; } req[] = {
+        {mxd->W1c_q, "mxd.W1c_q"}, {mxd->W1c_sp, "mxd.W1c_sp"}, {mxd->W2c_q, "mxd.W2c_q"},
+        {mxd->W2c_sp, "mxd.W2c_sp"}, {mxd->dy_q, "mxd.dy_q"},  {mxd->dy_s, "mxd.dy_s"},
+        {mxd->dH1_q, "mxd.dH1_q"}, {mxd->dH1_s, "mxd.dH1_s"}};
+    for (const auto& r : req) MOE_TRY(check_ptr(r.p, r.n, true));
+  }
   const bool sq = shared_fp8(c, q);
   MOE_TRY(check_ptr(Ws1, "Ws1", sh && !sq));
   MOE_TRY(check_ptr(Ws2, "Ws2", sh && !sq));
@@ -1487,7 +1687,10 @@ static int layer_bwd_impl(const moe_cfg* c, const void* dy, const void* x, const
       return fail(MOE_ERR_CUDA, "recording the side stream's completion failed");
   }
   // routed experts (dx_perm overwrites dy_perm once it is no longer read)
-  if (q)
+  if (mxd)
+    MOE_TRY(ffn_bwd_mx_impl(c, s->offsets, Nrows(c), s->x_perm, s->act, s->h, w.dy_perm, w.dH1,
+                            w.dy_perm, dW1, dW2, w.sched, st, mxd));
+  else if (q)
     MOE_TRY(ffn_bwd_fp8_impl(c, c->E, s->offsets, Nrows(c), c->f, q->x_perm_q, q->scales + 0, q->W1_q, q->W1_scale,
                              q->W2_q, q->W2_scale, s->act, q->h_q, q->scales + 2, w.dy_perm, dy_q,
                              q->scales + 4, q->scales + 5, w.dH1, dH1_q, q->scales + 6,
@@ -1543,6 +1746,16 @@ int moe_layer_bwd(const moe_cfg* c, const void* dy, const void* x, const void* W
                   void* stream) {
   return layer_bwd_impl(c, dy, x, W_r, W1, W2, nullptr, Ws1, Ws2, w_sg, s, dx, dW_r, dW1, dW2,
                         dWs1, dWs2, dw_sg, ws, ws_bytes, stream);
+}
+
+int moe_layer_bwd_mxfp8(const moe_cfg* c, const void* dy, const void* x, const void* W_r,
+                        const moe_mxfp8_dgrad* mxd, const void* Ws1, const void* Ws2,
+                        const void* w_sg, const moe_saved* s, void* dx, float* dW_r, float* dW1,
+                        float* dW2, float* dWs1, float* dWs2, float* dw_sg, void* ws,
+                        size_t ws_bytes, void* stream) {
+  if (!mxd) return fail(MOE_ERR_INVALID_ARG, "mxd is NULL");
+  return layer_bwd_impl(c, dy, x, W_r, nullptr, nullptr, nullptr, Ws1, Ws2, w_sg, s, dx, dW_r, dW1,
+                        dW2, dWs1, dWs2, dw_sg, ws, ws_bytes, stream, mxd);
 }
 
 int moe_layer_bwd_fp8(const moe_cfg* c, const void* dy, const void* x, const void* W_r,

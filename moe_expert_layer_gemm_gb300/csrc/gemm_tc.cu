@@ -144,8 +144,9 @@ template <int BN, int SCHED, int EPI, bool F8 = false> struct EpiWidth {
   static constexpr int slabs = SlabsPerWarp<SCHED, EPI, warps>::n;
 };
 
-// SFS: bytes of MXFP8 block scales per stage (0 without); MAXST: most stages the ring may have.
-template <int BN, bool TMA_OUT, int EPI_WARPS, int SLABS, int SFS = 0, int MAXST = 6>
+// SFS: bytes of MXFP8 block scales per stage (0 without); MAXST: most stages the ring may have;
+// TCOLS: TMEM columns to allocate (0: the two accumulators' power of two).
+template <int BN, bool TMA_OUT, int EPI_WARPS, int SLABS, int SFS = 0, int MAXST = 6, int TCOLS = 0>
 struct TileCfg {
   static constexpr int B_STAGE = BN * BK * 2;
   static constexpr int STAGING = TMA_OUT ? EPI_WARPS * SLABS * SLAB : 0;
@@ -157,18 +158,21 @@ struct TileCfg {
   static constexpr int SF_RING = STAGES * SFS;   // after the staging slabs
   static constexpr int SMEM = RING + STAGING + SF_RING + AUX;
   // two accumulators of BN columns; allocations are powers of two of at least 32 columns
-  static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
-                                 : 2 * BN <= 256 ? 256 : 512;
-  static constexpr int ACC_STRIDE = TMEM_COLS / 2;   // column of accumulator 1 (aligned)
+  static constexpr int ACC_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
+                                : 2 * BN <= 256 ? 256 : 512;
+  static constexpr int TMEM_COLS = TCOLS ? TCOLS : ACC_COLS;
+  static constexpr int ACC_STRIDE = ACC_COLS / 2;   // column of accumulator 1 (aligned)
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
 };
 
 // MXFP8 tiles: two accumulators of BN columns, then a 16-column TMEM slot per ring stage for the
-// stage's block scales (A: 4 columns, B: 4 per 128 rows of the tile, at +8).  With BN = 192 the
-// 512 columns hold both accumulators (0..191, 256..447) and four stages' scales (448..511).
+// stage's block scales (A: 4 columns, B: 4 per 128 rows of the tile, at +8), in a 512-column
+// allocation.  BN = 192: accumulators 0..191 and 256..447, four stages' scales in 448..511;
+// BN = 128: accumulators 0..127 and 128..255, scale slots from 256.
 constexpr int MX_SF_COLS = 16;
 template <int BN> struct MxCfg {
-  static constexpr int SF_STAGE = MX_CHUNK + MX_SFB_BYTES;   // A chunk, then B chunks
+  static constexpr int SFB_CH = (BN + 127) / 128;             // 512-byte B chunks per stage
+  static constexpr int SF_STAGE = MX_CHUNK * (1 + SFB_CH);    // A chunk, then B chunks
   static constexpr int ACC_STRIDE = 2 * BN <= 256 ? 128 : 256;
   static constexpr int SF_COL0 = ACC_STRIDE + BN;
   static constexpr int MAX_STAGES = (512 - SF_COL0) / MX_SF_COLS;
@@ -176,7 +180,8 @@ template <int BN> struct MxCfg {
 template <int BN, int SCHED, int EPI, bool F8, bool MX> struct CfgOf {
   using type = TileCfg<BN, OutPath<SCHED, EPI>::tma, EpiWidth<BN, SCHED, EPI, F8>::warps,
                        EpiWidth<BN, SCHED, EPI, F8>::slabs, MX ? MxCfg<BN>::SF_STAGE : 0,
-                       MX ? MxCfg<BN>::MAX_STAGES : 6>;
+                       MX ? (MxCfg<BN>::MAX_STAGES < 6 ? MxCfg<BN>::MAX_STAGES : 6) : 6,
+                       MX ? 512 : 0>;
 };
 
 struct KArgs {
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
   constexpr int MN_CHUNK = BKE * 128;   // bytes of one such chunk in a stage
   static_assert(!F8 || (!GATHER && !MC), "FP8 operands: no gathered or cluster-shared loads");
   // MXFP8: K-major E4M3 operands of a row-ragged product; one stage is one 128-element K chunk
-  static_assert(!MX || (F8 && SCHED == RAGGED_M && !A_MN && !B_MN && BN <= 256 &&
+  static_assert(!MX || (F8 && SCHED == RAGGED_M && !A_MN && (!B_MN || BN % 128 == 0) && BN <= 256 &&
                         C::ACC_STRIDE == MxCfg<BN>::ACC_STRIDE &&
                         MxCfg<BN>::SF_COL0 + C::STAGES * MX_SF_COLS <= C::TMEM_COLS),
                 "MXFP8 tile configuration");
@@ -641,8 +646,8 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
           ptx::bulk_load(sf_dst, p.sfa + (static_cast<int64_t>(ti.mt) * p.kch + kb) * MX_CHUNK,
                          MX_CHUNK, &full[stg]);
           const int64_t wt = static_cast<int64_t>(ti.g) * S::n_tiles(p) + ti.nt;
-          ptx::bulk_load(sf_dst + MX_CHUNK, p.sfb + (wt * p.kch + kb) * MX_SFB_BYTES, MX_SFB_BYTES,
-                         &full[stg]);
+          constexpr int SFB = MX_CHUNK * MxCfg<BN>::SFB_CH;
+          ptx::bulk_load(sf_dst + MX_CHUNK, p.sfb + (wt * p.kch + kb) * SFB, SFB, &full[stg]);
         }
       };
       // Run-time tiles: the next tile is claimed before the current one's loads are issued,
@@ -754,7 +759,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
             const uint32_t sf_s = ptx::smem_u32(sSF + stage * MxCfg<BN>::SF_STAGE);
             ptx::tmem_cp_32x128_x4(sf_t, ptx::smem_desc_plain(sf_s, 128));
 #pragma unroll
-            for (int ch = 0; ch < MX_SFB_CHUNKS; ++ch)
+            for (int ch = 0; ch < MxCfg<BN>::SFB_CH; ++ch)
               ptx::tmem_cp_32x128_x4(sf_t + 8 + 4 * ch,
                                      ptx::smem_desc_plain(sf_s + MX_CHUNK * (1 + ch), 128));
           }
@@ -1083,6 +1088,68 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
                 }
               }
               slab_store_2d(part == 0 ? &tmO1 : &tmO2, s2, lane, col, row0);
+            }
+          }
+        }
+      } else if (MX && EPI == EPI_SWIGLU_BWD) {
+        // [da | du] from dh and the saved [a | u] of the row, written in bf16 (the weight
+        // gradients' operand) when out is given and as MXFP8 codes and block scales along 2f
+        // (fc1's data-gradient operand): a thread's 32 columns are one block of da and one of du
+        const bf16* arow = static_cast<const bf16*>(p.aux) + row * p.ld_aux;
+        bf16* drow = p.out ? static_cast<bf16*>(p.out) + row * p.ldo : nullptr;
+        uint8_t* qrow = p.q_out + static_cast<int64_t>(row) * 2 * p.f;
+        uint8_t* sfrow = p.q_sf + static_cast<int64_t>(ti.mt) * p.kch_out * MX_CHUNK + (r & 31) * 16 +
+                         (r >> 5) * 4;
+        const int nb2 = 2 * p.f / 32;   // blocks of a [da | du] row
+#pragma unroll 1
+        for (int c = c_lo; c < c_hi; c += 32) {
+          const int col = ti.n0 + c;
+          if (col >= p.f) break;
+          uint32_t dh[32];
+          ptx::tmem_ld32(t_row + c, dh);
+          ptx::tmem_ld_wait();
+          if (!valid) continue;
+          float da[32], du[32];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            float av[8], uv[8];
+            unpack16(ld16(arow + col + v * 8), av, static_cast<const bf16*>(nullptr));
+            unpack16(ld16(arow + p.f + col + v * 8), uv, static_cast<const bf16*>(nullptr));
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float g = __uint_as_float(dh[v * 8 + i]);
+              const float s = sigmoid_f<MOE_FAST_SIGMOID_F8 != 0>(av[i]);
+              da[v * 8 + i] = __bfloat162float(__float2bfloat16_rn(g * uv[i] * (s + av[i] * s * (1.0f - s))));
+              du[v * 8 + i] = __bfloat162float(__float2bfloat16_rn(g * av[i] * s));
+            }
+            if (drow) {
+              st16(drow + col + v * 8, pack16(da + 8 * v, static_cast<const bf16*>(nullptr)));
+              st16(drow + p.f + col + v * 8, pack16(du + 8 * v, static_cast<const bf16*>(nullptr)));
+            }
+          }
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const float* vals = half ? du : da;
+            float am = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(vals[i]));
+            const int ex = mx_exponent(am);
+            const float inv = mx_inv_scale(ex);
+            uint32_t w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t lo = cvt_e4m3x2(vals[4 * j] * inv, vals[4 * j + 1] * inv);
+              const uint32_t hi = cvt_e4m3x2(vals[4 * j + 2] * inv, vals[4 * j + 3] * inv);
+              w[j] = lo | (hi << 16);
+            }
+            const int qc = half * p.f + col;   // column of this block in [da | du]
+            *reinterpret_cast<uint4*>(qrow + qc) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(qrow + qc + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+            const int blk = qc >> 5;
+            uint8_t* sf = sfrow + (blk >> 2) * MX_CHUNK;
+            sf[blk & 3] = static_cast<uint8_t>(ex + 127);
+            if (blk == nb2 - 1) {
+              for (int j = (blk & 3) + 1; j < 4; ++j) sf[j] = 127;   // blocks past 2f: 2^0
             }
           }
         }
@@ -1834,7 +1901,7 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
       MOE_TRY(map_bf16(&mo[1], g.out2, rows, g.f, g.ldo2, 32));
       MOE_TRY(map_bf16(&mo[2], static_cast<const bf16*>(g.out2) + g.f, rows, g.f, g.ldo2, 32));
     }
-  } else if (EPI == EPI_SWIGLU_BWD) {
+  } else if (EPI == EPI_SWIGLU_BWD && !MX) {   // (MXFP8: direct loads and stores, no maps)
     MOE_TRY(map_bf16(&mo[0], g.out, rows, g.f, g.ldo, 32));
     MOE_TRY(map_bf16(&mo[1], static_cast<const bf16*>(g.out) + g.f, rows, g.f, g.ldo, 32));
     MOE_TRY(map_bf16(&mo[2], g.aux, rows, 2 * static_cast<int64_t>(g.f), g.ld_aux, 32));
@@ -1868,7 +1935,7 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   a.q_out = g.q_out;
   a.q_sf = g.q_sf;
   a.kch = static_cast<int>(mx_kch(g.K));
-  a.kch_out = static_cast<int>(mx_kch(g.f));
+  a.kch_out = static_cast<int>(mx_kch(EPI == EPI_SWIGLU_BWD ? 2 * static_cast<int64_t>(g.f) : g.f));
   if (F8 && !MX && (!g.a_scale || !g.b_scale)) {
     set_error("%s: FP8 operands need their scales", name);
     return MOE_ERR_INVALID_ARG;
@@ -1876,9 +1943,11 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   if (MX) {
     const bool aligned = (reinterpret_cast<uintptr_t>(g.sfa) & 15u) == 0 &&
                          (reinterpret_cast<uintptr_t>(g.sfb) & 15u) == 0;
+    const bool swiglu = EPI == EPI_SWIGLU_FWD || EPI == EPI_SWIGLU_BWD;
     if (!g.sfa || !g.sfb || !aligned || g.K % 32 != 0 ||
-        (EPI == EPI_SWIGLU_FWD && (!g.q_out || !g.q_sf || g.f % 32 != 0 ||
-                                   (reinterpret_cast<uintptr_t>(g.q_out) & 15u) != 0))) {
+        (swiglu && (!g.q_out || !g.q_sf || g.f % 32 != 0 ||
+                    (reinterpret_cast<uintptr_t>(g.q_out) & 15u) != 0)) ||
+        (EPI == EPI_SWIGLU_BWD && !g.aux)) {
       set_error("%s: MXFP8 operands need 16-byte aligned block scales, K (and f) multiples of 32 "
                 "and, for SwiGLU, h's code and scale buffers", name);
       return MOE_ERR_INVALID_ARG;
@@ -1964,6 +2033,15 @@ int gemm_tc(const GemmDesc& g, cudaStream_t st) {
       if (g.epi == EPI_STORE)
         return run<MX_BN, false, false, RAGGED_M, EPI_STORE, false, true, true>(g, "gemm_fc2_mxfp8",
                                                                                st);
+    }
+    // the data gradients: weights read MN-major (their stored layout), 128-column tiles
+    if (!g.gather && g.sched == RAGGED_M && !g.A.mn_major && g.B.mn_major) {
+      if (g.epi == EPI_SWIGLU_BWD)
+        return run<MX_BN_DGRAD, false, true, RAGGED_M, EPI_SWIGLU_BWD, false, true, true>(
+            g, "gemm_fc2_dgrad_mxfp8", st);
+      if (g.epi == EPI_STORE)
+        return run<MX_BN_DGRAD, false, true, RAGGED_M, EPI_STORE, false, true, true>(
+            g, "gemm_fc1_dgrad_mxfp8", st);
     }
     set_error("gemm_tc: unsupported MXFP8 combination sched=%d epi=%d a_mn=%d b_mn=%d", g.sched,
               g.epi, (int)g.A.mn_major, (int)g.B.mn_major);

@@ -197,7 +197,9 @@ struct GemmDesc {
 // Scales of rows or blocks past the operand's end are 127 (2^0) in weight chunks; activation
 // chunks leave rows past an expert's end unwritten (their products are never stored) and set
 // blocks past K to 127.
-constexpr int MX_BN = 192;                 // output columns of an MXFP8 tile
+constexpr int MX_BN = 192;                 // output columns of an MXFP8 forward tile
+constexpr int MX_BN_DGRAD = 128;           // of an MXFP8 data-gradient tile (MN-major weights
+                                           // come in 128-column chunks)
 constexpr int MX_CHUNK = 512;
 constexpr int MX_SFB_CHUNKS = (MX_BN + 127) / 128;
 constexpr int MX_SFB_BYTES = MX_SFB_CHUNKS * MX_CHUNK;
@@ -233,12 +235,20 @@ int launch_permute_quant_e4m3(const void* x, const int32_t* sop, uint8_t* xq, ui
 // row-major E8M0 scales [rows, cols / 32].
 int launch_mx_quantize(const void* x, int64_t rows, int cols, uint8_t* q, uint8_t* s,
                        cudaStream_t st);
-// Row-major weight scales [E, R, K / 32] -> the packed weight layout; swiglu_f > 0: fc1 tiles
-// over R = 2 * swiglu_f rows, 0: fc2 tiles over R rows.
+// Weight scales -> the packed weight layout with tiles of tile_rows B-rows; swiglu_f > 0: fc1
+// tiles over R = 2 * swiglu_f rows, 0: plain tiles over R B-rows.  Row-major scales [E, R, K/32]
+// (blocks along each B-row's K), or with cols scales [E, K/32, R] of a weight whose columns are
+// the B-rows (blocks along its rows, as the data gradients read W1 and W2).
 int launch_mx_pack_weight_scales(const uint8_t* s, int E, int R, int K, int swiglu_f,
-                                 uint8_t* packed, cudaStream_t st);
+                                 uint8_t* packed, cudaStream_t st, int tile_rows = MX_BN,
+                                 int cols = 0);
+// G groups of R x C bf16 rows quantised in 32-row blocks down each column: codes in x's layout,
+// scales [G, R/32, C].
+int launch_mx_quantize_cols(const void* x, int G, int R, int C, uint8_t* q, uint8_t* s,
+                            cudaStream_t st);
 // Permute + quantise: x_perm_q[slot(t, j)] = MXFP8 codes of x[t], scales in the packed
 // activation layout (row tiles from the routing offsets); xp (optional): the bf16 rows too.
+// sop = NULL (with k = 1): row t is slot t (quantising rows already in expert order).
 int launch_permute_quant_mx(const void* x, const int32_t* sop, const int32_t* offsets,
                             uint8_t* xq, uint8_t* xs, int T, int d, int k, int E, cudaStream_t st,
                             void* xp = nullptr);

@@ -57,20 +57,24 @@ __global__ void __launch_bounds__(256) mx_quant_kernel(const bf16* __restrict__ 
   }
 }
 
-// One thread per byte of the packed weight-scale layout (internal.h): E experts x NT tiles x kch
-// chunks x MX_SFB_BYTES.  Byte pos of a 512-byte chunk ch holds row (ch * 128 + (pos / 4) % 4 *
-// 32 + pos / 16) of the tile, block kc * 4 + pos % 4.
+// One thread per byte of a packed weight-scale layout (internal.h): E experts x NT tiles of TR
+// B-rows x kch chunks x ceil(TR / 128) chunks of 512 bytes.  Byte pos of chunk ch holds tile row
+// ch * 128 + (pos / 4) % 4 * 32 + pos / 16, block kc * 4 + pos % 4.  B-row r of expert e is
+// weight row r (scales s[e][r][block], blocks along the weight's rows' K) or, with cols, weight
+// column r (scales s[e][block][r], blocks along its columns).
 __global__ void __launch_bounds__(256) mx_pack_wscales_kernel(const uint8_t* __restrict__ s, int E,
                                                               int R, int nb, int swiglu_f, int NT,
-                                                              int kch, uint8_t* __restrict__ out) {
-  const int64_t total = static_cast<int64_t>(E) * NT * kch * MX_SFB_BYTES;
+                                                              int kch, int TR, int cols,
+                                                              uint8_t* __restrict__ out) {
+  const int CH = (TR + 127) / 128;
+  const int64_t total = static_cast<int64_t>(E) * NT * kch * CH * MX_CHUNK;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += stride) {
     const int pos = static_cast<int>(i % MX_CHUNK);
     int64_t rest = i / MX_CHUNK;
-    const int ch = static_cast<int>(rest % MX_SFB_CHUNKS);
-    rest /= MX_SFB_CHUNKS;
+    const int ch = static_cast<int>(rest % CH);
+    rest /= CH;
     const int kc = static_cast<int>(rest % kch);
     rest /= kch;
     const int nt = static_cast<int>(rest % NT);
@@ -78,18 +82,44 @@ __global__ void __launch_bounds__(256) mx_pack_wscales_kernel(const uint8_t* __r
     const int rt = ch * 128 + ((pos >> 2) & 3) * 32 + (pos >> 4);   // row inside the tile
     const int blk = kc * 4 + (pos & 3);
     int row = -1;
-    if (rt < MX_BN) {
+    if (rt < TR) {
       if (swiglu_f > 0) {
-        const int half = MX_BN / 2;
+        const int half = TR / 2;
         const int hc = nt * half + (rt < half ? rt : rt - half);   // h column of this B row
         if (hc < swiglu_f) row = rt < half ? hc : swiglu_f + hc;
       } else {
-        const int r = nt * MX_BN + rt;
+        const int r = nt * TR + rt;
         if (r < R) row = r;
       }
     }
-    out[i] = (row >= 0 && blk < nb) ? s[(static_cast<int64_t>(e) * R + row) * nb + blk]
-                                    : static_cast<uint8_t>(127);
+    const int64_t src = cols ? (static_cast<int64_t>(e) * nb + blk) * R + row
+                             : (static_cast<int64_t>(e) * R + row) * nb + blk;
+    out[i] = (row >= 0 && blk < nb) ? s[src] : static_cast<uint8_t>(127);
+  }
+}
+
+// One thread per (group g, 32-row block b, column c) of G groups of R x C bf16 rows (R % 32 ==
+// 0): the block's 32 values down column c, codes in x's layout, scales s[g][b][c].  Consecutive
+// threads take consecutive columns, so every row access is coalesced.
+__global__ void __launch_bounds__(256) mx_quant_cols_kernel(const bf16* __restrict__ x, int G, int R,
+                                                            int C, uint8_t* __restrict__ q,
+                                                            uint8_t* __restrict__ s) {
+  const int64_t nbr = R / 32;
+  const int64_t total = static_cast<int64_t>(G) * nbr * C;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const int c = static_cast<int>(i % C);
+    const int64_t gb = i / C;                      // g * nbr + b
+    const int64_t r0 = gb * 32;                    // first row of the block in the G*R rows
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(x[(r0 + j) * C + c]);
+    uint32_t w[8];
+    const int e = quant_block32(v, w);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) q[(r0 + j) * C + c] = static_cast<uint8_t>(w[j >> 2] >> (8 * (j & 3)));
+    s[gb * C + c] = static_cast<uint8_t>(e + 127);
   }
 }
 
@@ -135,7 +165,7 @@ __global__ void __launch_bounds__(MXP_THREADS) permute_quant_mx_kernel(
     int my_slot = -1;
     int64_t my_sf = 0;
     if (lane < k) {
-      my_slot = sop[static_cast<int64_t>(t) * k + lane];
+      my_slot = sop ? sop[static_cast<int64_t>(t) * k + lane] : t;   // no map: row t is slot t
       if (my_slot < 0 || my_slot >= N || my_slot >= s_off[E]) {
         record_error(err, DEVERR_BAD_SLOT);
         my_slot = -1;
@@ -217,12 +247,21 @@ int launch_mx_quantize(const void* x, int64_t rows, int cols, uint8_t* q, uint8_
 }
 
 int launch_mx_pack_weight_scales(const uint8_t* s, int E, int R, int K, int swiglu_f,
-                                 uint8_t* packed, cudaStream_t st) {
-  const int NT = static_cast<int>(swiglu_f > 0 ? mx_fc1_tiles(swiglu_f) : mx_fc2_tiles(R));
+                                 uint8_t* packed, cudaStream_t st, int tile_rows, int cols) {
+  const int NT = static_cast<int>(swiglu_f > 0 ? (swiglu_f + tile_rows / 2 - 1) / (tile_rows / 2)
+                                               : (R + tile_rows - 1) / tile_rows);
   const int kch = static_cast<int>(mx_kch(K));
-  const int64_t total = static_cast<int64_t>(E) * NT * kch * MX_SFB_BYTES;
+  const int64_t total = static_cast<int64_t>(E) * NT * kch * ((tile_rows + 127) / 128) * MX_CHUNK;
   return launch("mxfp8_pack_scales", mx_pack_wscales_kernel, dim3(grid_for(total, 256)), dim3(256),
-                0, st, s, E, R, K / 32, swiglu_f, NT, kch, packed);
+                0, st, s, E, R, K / 32, swiglu_f, NT, kch, tile_rows, cols, packed);
+}
+
+int launch_mx_quantize_cols(const void* x, int G, int R, int C, uint8_t* q, uint8_t* s,
+                            cudaStream_t st) {
+  const int64_t n = static_cast<int64_t>(G) * (R / 32) * C;
+  if (n == 0) return MOE_OK;
+  return launch("mxfp8_quantize_cols", mx_quant_cols_kernel, dim3(grid_for(n, 256)), dim3(256), 0,
+                st, static_cast<const bf16*>(x), G, R, C, q, s);
 }
 
 int launch_permute_quant_mx(const void* x, const int32_t* sop, const int32_t* offsets,

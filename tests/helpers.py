@@ -223,3 +223,16 @@ def mx_weight_index(E, R, K, swiglu_f):
     t, rt = t[None, :, None], rt[None, :, None]
     return ((e * NT + t) * kch + b // 4) * 1024 + (rt // 128) * 512 + (rt % 32) * 16 + \
         ((rt % 128) // 32) * 4 + b % 4
+
+
+def mx_weight_index_cols(E, N, K, tile=128):
+    """Index [E, K/32, N] into a packed weight layout whose B-rows are the weight's N columns in
+    tiles of `tile` (MOE_MX_SCALES_W1C / _W2C: scales of 32-row blocks down each column)."""
+    kch, nb = (K + 127) // 128, K // 32
+    NT = (N + tile - 1) // tile
+    n = np.arange(N)[None, None, :]
+    t, rt = n // tile, n % tile
+    e = np.arange(E)[:, None, None]
+    b = np.arange(nb)[None, :, None]
+    return ((e * NT + t) * kch + b // 4) * ((tile + 127) // 128 * 512) + (rt // 128) * 512 + \
+        (rt % 32) * 16 + ((rt % 128) // 32) * 4 + b % 4

@@ -12,7 +12,13 @@
     quantisation of the GPU's bf16 h; y_perm within tolerance of the oracle's fc2 on those codes;
     and against the unquantised bf16 experts within the format's rounding bound;
   * moe_layer_fwd_mxfp8: routing and shared expert identical to the bf16 layer's, y bit-identical
-    to the composed stage calls, and within the format's rounding of the unquantised layer.
+    to the composed stage calls, and within the format's rounding of the unquantised layer;
+  * the data gradients: the weights' column-blocked codes and scales bit-identical to the
+    oracle's (packed scales at their places), dy's codes bit-identical, [da | du] within the bf16
+    tolerance of the oracle's SwiGLU backward of its fc2 data gradient on the same codes, its codes
+    bit-identical to the oracle's quantisation of the GPU's bf16 [da | du], dx_perm within the bf16
+    tolerance of the oracle's fc1 data gradient of those codes; moe_layer_bwd_mxfp8 against the
+    bf16 backward on the same saved state and the unquantised oracle.
 Shapes cover several tiles with ragged tails, experts without rows, K not a multiple of 128 (a
 partial last scale chunk) and f not a multiple of the 96-column SwiGLU tile.
 """
@@ -25,8 +31,10 @@ import moe_inputs
 import oracle.moe_oracle as O
 import oracle.mxfp8_oracle as MX
 
+import oracle.fp8_oracle as F8
+
 from .helpers import (assert_close, clean_inputs, mx_act_pad_bytes, mx_unpack_act_scales,
-                      mx_weight_index, np64, oracle_layer, rel_err, run_layer)
+                      mx_weight_index, mx_weight_index_cols, np64, oracle_layer, rel_err, run_layer)
 
 pytestmark = pytest.mark.gpu
 
@@ -301,3 +309,105 @@ def test_mxfp8_forward_saves_the_bf16_state_for_the_bf16_backward():
         errs[name] = rel_err(gpu, ref["bwd"][name])
         assert errs[name] < 0.15, (name, errs[name])
     print("mxfp8 forward + bf16 backward vs unquantised:", {k: f"{v:.3f}" for k, v in errs.items()})
+
+
+@pytest.mark.parametrize("E,d,f", [(3, 256, 160), (2, 2688, 1856), (4, 224, 96)])
+def test_dgrad_weight_copies(E, d, f):
+    cfg = moe.make_cfg(64, d, E, 2, f)
+    W1 = (varied((E, 2 * f, d), d, 2.0).float() * 0.05).bfloat16().cuda()
+    W2 = (varied((E, d, f), d + 1, 2.0).float() * 0.05).bfloat16().cuda()
+    m = moe.alloc_mxfp8_dgrad(cfg, W1, W2)
+    sync()
+    for W, pre, K, N in ((W1, "W1c", 2 * f, d), (W2, "W2c", d, f)):
+        rq, rs = MX.mx_quantize_cols(W.double().cpu().numpy())
+        assert np.array_equal(m[pre + "_q"].cpu().numpy(), rq)
+        assert np.array_equal(m[pre + "_s"].cpu().numpy(), rs)
+        p = m[pre + "_sp"].cpu().numpy()
+        idx = mx_weight_index_cols(E, N, K)
+        assert np.array_equal(p[idx], rs)
+        rest = np.ones(p.size, bool)
+        rest[idx.ravel()] = False
+        assert (p[rest] == 127).all()
+
+
+@pytest.mark.parametrize("T,d,E,k,f,empty", [(600, 256, 8, 2, 160, 2), (1024, 2048, 128, 8, 768, 0),
+                                             (257, 2688, 8, 6, 1856, 0), (700, 224, 256, 8, 128, 40)])
+def test_mxfp8_data_gradients(T, d, E, k, f, empty):
+    r = routed(T, E, k, d + f + 1, empty)
+    N = T * k
+    o = r["offsets"]
+    cfg = moe.make_cfg(T, d, E, k, f)
+    W1 = (varied((E, 2 * f, d), d, 2.0).float() * 0.05).bfloat16().cuda()
+    W2 = (varied((E, d, f), d + 1, 2.0).float() * 0.05).bfloat16().cuda()
+    m = moe.alloc_mxfp8_dgrad(cfg, W1, W2)
+    dyp = varied((N, d), N).cuda()
+    g = torch.Generator().manual_seed(N)
+    act = (torch.randn(N, 2 * f, generator=g) * 2).bfloat16().cuda()
+    off = torch.from_numpy(o).cuda()
+    dH1 = torch.empty(N, 2 * f, dtype=torch.bfloat16, device="cuda")
+    dxp = torch.empty(N, d, dtype=torch.bfloat16, device="cuda")
+    moe.moe_grouped_swiglu_dgrad_mxfp8(cfg, dyp, off, act, m, dH1, dxp)
+    sync()
+    # dy's codes and scales
+    rq, rs = MX.mx_quantize(np64(dyp))
+    assert np.array_equal(m["dy_q"].cpu().numpy(), rq)
+    assert np.array_equal(mx_unpack_act_scales(m["dy_s"].cpu().numpy(), o, N, d), rs)
+    # fc2's data gradient and the SwiGLU backward on those codes
+    W2cq, W2cs = m["W2c_q"].cpu().numpy(), m["W2c_s"].cpu().numpy()
+    dh = MX.fc2_dgrad_mx(rq, rs, W2cq, W2cs, o)
+    ref_dH1 = F8.swiglu_backward(dh, np64(act))
+    e_dh1 = assert_close("dH1", np64(dH1), ref_dH1, TOL_OUT)
+    # [da | du]'s codes and scales: the oracle's quantisation of the GPU's bf16 [da | du]
+    hq, hs = MX.mx_quantize(np64(dH1))
+    assert np.array_equal(m["dH1_q"].cpu().numpy(), hq)
+    dhs = m["dH1_s"].cpu().numpy()
+    assert np.array_equal(mx_unpack_act_scales(dhs, o, N, 2 * f), hs)
+    assert (mx_act_pad_bytes(dhs, o, N, 2 * f) == 127).all()
+    ref_dx = MX.fc1_dgrad_mx(hq, hs, m["W1c_q"].cpu().numpy(), m["W1c_s"].cpu().numpy(), o)
+    e_dx = assert_close("dx_perm", np64(dxp), ref_dx, TOL_OUT)
+    print(f"dH1 {e_dh1:.2e} dx_perm {e_dx:.2e}")
+
+
+def test_mxfp8_layer_backward():
+    """moe_layer_bwd_mxfp8 after moe_layer_fwd_mxfp8: the weight gradients and dx against the bf16
+    backward on the same saved state (they differ by the data gradients' MXFP8 rounding) and
+    against the unquantised oracle."""
+    lc = LAYER_CASES["sigmoid-shared"]
+    host, _ = clean_inputs(lc)
+    inp = {k: (None if v is None else v.cuda()) for k, v in host.items()}
+    cfg = moe.cfg_from(lc)
+    m = moe.alloc_mxfp8_experts(cfg, inp["W1"], inp["W2"])
+    mxd = moe.alloc_mxfp8_dgrad(cfg, inp["W1"], inp["W2"])
+    saved = moe.alloc_saved(cfg)
+    y = torch.empty_like(inp["x"])
+    moe.moe_layer_fwd_mxfp8(cfg, inp["x"], inp["W_r"], inp["b_r"], m, inp["Ws1"], inp["Ws2"],
+                            inp["w_sg"], y, saved, moe.workspace(cfg, moe.WS_LAYER_FWD))
+    f32 = torch.float32
+    E, d, f, fs = lc.E, lc.d, lc.f, lc.f_shared
+
+    def grads():
+        return dict(dx=torch.empty_like(inp["x"]), dW_r=torch.empty(E, d, dtype=f32, device="cuda"),
+                    dW1=torch.empty(E, 2 * f, d, dtype=f32, device="cuda"),
+                    dW2=torch.empty(E, d, f, dtype=f32, device="cuda"),
+                    dWs1=torch.empty(2 * fs, d, dtype=f32, device="cuda"),
+                    dWs2=torch.empty(d, fs, dtype=f32, device="cuda"))
+    ws = moe.workspace(cfg, moe.WS_LAYER_BWD)
+    g16, gmx = grads(), grads()
+    moe.moe_layer_bwd(cfg, inp["dy"], inp["x"], inp["W_r"], inp["W1"], inp["W2"], inp["Ws1"],
+                      inp["Ws2"], None, saved, g16["dx"], g16["dW_r"], g16["dW1"], g16["dW2"],
+                      g16["dWs1"], g16["dWs2"], None, ws)
+    moe.moe_layer_bwd_mxfp8(cfg, inp["dy"], inp["x"], inp["W_r"], mxd, inp["Ws1"], inp["Ws2"], None,
+                            saved, gmx["dx"], gmx["dW_r"], gmx["dW1"], gmx["dW2"], gmx["dWs1"],
+                            gmx["dWs2"], None, ws)
+    sync()
+    # the router's and shared expert's gradients do not depend on the routed data gradients
+    for name in ("dW_r", "dWs1", "dWs2", "dW2"):
+        assert torch.equal(gmx[name], g16[name]), name
+    ref = oracle_layer(lc, {k: (None if v is None else v.cpu()) for k, v in inp.items()})
+    errs = {}
+    for name in ("dx", "dW1"):
+        errs[name + " vs bf16"] = rel_err(np64(gmx[name]), np64(g16[name]))
+        assert errs[name + " vs bf16"] < 0.1, errs
+        errs[name + " vs oracle"] = rel_err(np64(gmx[name]), ref["bwd"][name])
+        assert errs[name + " vs oracle"] < 0.15, errs
+    print("mxfp8 layer backward:", {k: f"{v:.3f}" for k, v in errs.items()})
