@@ -101,7 +101,12 @@ def kernel_work(lc, trace=None, steps=1):
     # pair's codes and its block scales (one byte per 32)
     w["gemm_fc1_swiglu_mxfp8"] = w["gemm_fc1_swiglu"]
     w["gemm_fc2_mxfp8"] = w["gemm_fc2"]
-    w["mxfp8_permute_quantize"] = ("hbm", T * d * 2 + N * d * 33 / 32 + N * 4)
+    w["gemm_fc2_dgrad_mxfp8"] = w["gemm_fc2_dgrad"]
+    w["gemm_fc1_dgrad_mxfp8"] = w["gemm_fc1_dgrad"]
+    # (with a backward, the MXFP8 forward also writes the bf16 x_perm the weight gradient reads)
+    w["mxfp8_permute_quantize"] = ("hbm", T * d * 2 + N * d * 33 / 32 + N * 4 +
+                                   (N * d * 2 if lc.backward else 0))
+    w["mxfp8_quantize_rows"] = ("hbm", N * d * 2 + N * d * 33 / 32)   # dy_perm in expert order
     return w
 
 
@@ -127,6 +132,10 @@ def gemm_bytes(lc):
     q = 33 / 32
     out["gemm_fc1_swiglu_mxfp8"] = T * k * d * q + E * 2 * f * d * q + T * k * f * q
     out["gemm_fc2_mxfp8"] = T * k * f * q + E * d * f * q + T * k * d * 2
+    # data gradients: dy's and the weights' codes in; [da | du] in bf16 and as codes, dx out
+    out["gemm_fc2_dgrad_mxfp8"] = T * k * d * q + E * d * f * q + T * k * 2 * f * 2 + \
+        T * k * 2 * f * (2 + q)
+    out["gemm_fc1_dgrad_mxfp8"] = T * k * 2 * f * q + E * 2 * f * d * q + T * k * d * 2
     return out
 
 
@@ -311,10 +320,12 @@ def run_gpu(args, lc):
     stream = torch.cuda.current_stream()
     mxq = None
     if args.mxfp8:
-        # MXFP8 routed experts (quantised once, outside the timed steps).  Forward-only
-        # configurations keep routing and y_perm alone; with a backward, the forward also saves
-        # the bf16 x_perm, [a | u] and h that the bf16 backward reads
+        # MXFP8 routed experts (weights quantised once, outside the timed steps, both copies).
+        # Forward-only configurations keep routing and y_perm alone; with a backward, the forward
+        # also saves the bf16 x_perm, [a | u] and h, and the backward runs the routed data
+        # gradients on MXFP8 operands and the weight gradients in bf16
         mxq = moe.alloc_mxfp8_experts(cfg, inp["W1"], inp["W2"], dev)
+        mxd = moe.alloc_mxfp8_dgrad(cfg, inp["W1"], inp["W2"], dev) if lc.backward else None
         if not lc.backward:
             saved["x_perm"] = saved["act"] = saved["h"] = None
     fp8q = None
@@ -328,10 +339,10 @@ def run_gpu(args, lc):
             moe.moe_layer_fwd_mxfp8(cfg, x, inp["W_r"], inp["b_r"], mxq, inp["Ws1"], inp["Ws2"],
                                     inp["w_sg"], yout, saved, ws_f)
             if lc.backward:
-                moe.moe_layer_bwd(cfg, dy, x, inp["W_r"], inp["W1"], inp["W2"], inp["Ws1"],
-                                  inp["Ws2"], inp["w_sg"], saved, dxout, grads["dW_r"],
-                                  grads["dW1"], grads["dW2"], grads["dWs1"], grads["dWs2"],
-                                  grads["dw_sg"], ws_b)
+                moe.moe_layer_bwd_mxfp8(cfg, dy, x, inp["W_r"], mxd, inp["Ws1"], inp["Ws2"],
+                                        inp["w_sg"], saved, dxout, grads["dW_r"], grads["dW1"],
+                                        grads["dW2"], grads["dWs1"], grads["dWs2"],
+                                        grads["dw_sg"], ws_b)
             return
         if fp8q is not None:
             moe.moe_layer_fwd_fp8(cfg, x, inp["W_r"], inp["b_r"], fp8q, inp["Ws1"], inp["Ws2"],
@@ -591,8 +602,8 @@ def run_gpu(args, lc):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": ("e4m3 experts, bf16 router/combine" if args.fp8 else
-                  ("mxfp8 experts in the forward (e4m3, e8m0 scale per 32), bf16 backward, "
-                   "bf16 router/shared/combine" if lc.backward else
+                  ("mxfp8 expert products (e4m3, e8m0 scale per 32) in the forward and the data "
+                   "gradients, bf16 weight gradients, bf16 router/shared/combine" if lc.backward else
                    "mxfp8 experts (e4m3, e8m0 scale per 32), bf16 router/shared/combine")
                   if args.mxfp8 else lc.dtype),
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights, random init)",
@@ -911,9 +922,9 @@ def main():
                     help="time the layer with its experts in FP8 E4M3 (moe_layer_fwd_fp8 / "
                          "moe_layer_bwd_fp8) instead of bf16")
     ap.add_argument("--mxfp8", action="store_true",
-                    help="time the layer with MXFP8 routed experts in the forward "
-                         "(moe_layer_fwd_mxfp8) and the bf16 backward (moe_layer_bwd) on its saved "
-                         "state; --mxfp8-forward-only times the forward alone")
+                    help="time the layer with MXFP8 routed experts: moe_layer_fwd_mxfp8, and "
+                         "moe_layer_bwd_mxfp8 (MXFP8 data gradients, bf16 weight gradients) where "
+                         "the configuration has a backward; --mxfp8-forward-only: the forward alone")
     ap.add_argument("--mxfp8-forward-only", action="store_true",
                     help="with --mxfp8: the step is the forward, also on workloads with a backward")
     ap.add_argument("--e2e-steps", type=int, default=20)

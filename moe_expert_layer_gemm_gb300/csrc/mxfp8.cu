@@ -270,7 +270,8 @@ int launch_permute_quant_mx(const void* x, const int32_t* sop, const int32_t* of
   const int wpb = MXP_THREADS / 32;
   int rb = (T + wpb - 1) / wpb;
   if (rb > num_sms() * 8) rb = num_sms() * 8;
-  return launch("mxfp8_permute_quantize", permute_quant_mx_kernel, dim3(rb), dim3(MXP_THREADS), 0,
+  return launch(sop ? "mxfp8_permute_quantize" : "mxfp8_quantize_rows", permute_quant_mx_kernel,
+                dim3(rb), dim3(MXP_THREADS), 0,
                 st, static_cast<const bf16*>(x), sop, offsets, xq, xs, static_cast<bf16*>(xp), T, d,
                 k, E, device_error_word());
 }
