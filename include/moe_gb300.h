@@ -275,10 +275,11 @@ enum { MOE_MX_SCALES_X = 0, MOE_MX_SCALES_H = 1, MOE_MX_SCALES_W1 = 2, MOE_MX_SC
        MOE_MX_SCALES_DH1 = 4, MOE_MX_SCALES_W1C = 5, MOE_MX_SCALES_W2C = 6 };
 /* The data gradients' layouts: MOE_MX_SCALES_DH1 is [da | du] [N,2f] in the activation layout
  * (K = 2f).  MOE_MX_SCALES_W1C / _W2C are the weights blocked down their rows (W1 [2f,d] along 2f,
- * W2 [d,f] along d, as moe_mxfp8_prepare_dgrad_weights makes them): per expert, per tile of 128
- * columns (d for W1, f for W2) and per 128-row K chunk, one 512-byte chunk at
- * ((e * tiles + t) * ceil(K/128) + kc) * 512, byte (c % 32) * 16 + (c / 32) * 4 + j for column c
- * of the tile and block j of the chunk; columns and blocks past the weight are 127. */
+ * W2 [d,f] along d, as moe_mxfp8_prepare_dgrad_weights makes them): per expert, per tile of
+ * columns (256 of d for W1, 128 of f for W2) and per 128-row K chunk, one 512-byte chunk per 128
+ * columns of the tile, at ((e * tiles + t) * ceil(K/128) + kc) * (512 per 128 tile columns), byte
+ * (c % 32) * 16 + (c % 128 / 32) * 4 + j for column c and block j of the K chunk; columns and
+ * blocks past the weight are 127. */
 /* Bytes of one packed scale buffer for cfg (0 for an invalid cfg or `which`). */
 size_t moe_mxfp8_scale_bytes(const moe_cfg* cfg, int which);
 

@@ -1042,12 +1042,12 @@ size_t moe_mxfp8_scale_bytes(const moe_cfg* c, int which) {
     case MOE_MX_SCALES_W2:
       return static_cast<size_t>(c->E) * mx_fc2_tiles(c->d) * mx_kch(c->f) * MX_SFB_BYTES;
     case MOE_MX_SCALES_DH1: return static_cast<size_t>(mx_act_scale_bytes(N, c->E, 2 * c->f));
-    case MOE_MX_SCALES_W1C:   // W1 read as [2f (K), d (N)]: tiles of 128 columns of d
-      return static_cast<size_t>(c->E) * ((c->d + MX_BN_DGRAD - 1) / MX_BN_DGRAD) *
-             mx_kch(2 * c->f) * MX_CHUNK;
-    case MOE_MX_SCALES_W2C:   // W2 read as [d (K), f (N)]: tiles of 128 columns of f
-      return static_cast<size_t>(c->E) * ((c->f + MX_BN_DGRAD - 1) / MX_BN_DGRAD) * mx_kch(c->d) *
-             MX_CHUNK;
+    case MOE_MX_SCALES_W1C:   // W1 read as [2f (K), d (N)]: tiles of MX_BN_DGRAD1 columns of d
+      return static_cast<size_t>(c->E) * ((c->d + MX_BN_DGRAD1 - 1) / MX_BN_DGRAD1) *
+             mx_kch(2 * c->f) * ((MX_BN_DGRAD1 + 127) / 128) * MX_CHUNK;
+    case MOE_MX_SCALES_W2C:   // W2 read as [d (K), f (N)]: tiles of MX_BN_DGRAD2 columns of f
+      return static_cast<size_t>(c->E) * ((c->f + MX_BN_DGRAD2 - 1) / MX_BN_DGRAD2) *
+             mx_kch(c->d) * ((MX_BN_DGRAD2 + 127) / 128) * MX_CHUNK;
     default: return 0;
   }
 }
@@ -1266,10 +1266,10 @@ int moe_mxfp8_prepare_dgrad_weights(const moe_cfg* c, const void* W1, const void
   const int E = c->E, d = c->d, f = c->f;
   // W1 [E, 2f, d] in 32-row blocks along 2f; its columns (d) are the B-rows of fc1's data gradient
   MOE_TRY(launch_mx_quantize_cols(W1, E, 2 * f, d, W1c_q, W1c_s, st));
-  MOE_TRY(launch_mx_pack_weight_scales(W1c_s, E, d, 2 * f, 0, W1c_sp, st, MX_BN_DGRAD, 1));
+  MOE_TRY(launch_mx_pack_weight_scales(W1c_s, E, d, 2 * f, 0, W1c_sp, st, MX_BN_DGRAD1, 1));
   // W2 [E, d, f] in 32-row blocks along d; its columns (f) are the B-rows of fc2's data gradient
   MOE_TRY(launch_mx_quantize_cols(W2, E, d, f, W2c_q, W2c_s, st));
-  return launch_mx_pack_weight_scales(W2c_s, E, f, d, 0, W2c_sp, st, MX_BN_DGRAD, 1);
+  return launch_mx_pack_weight_scales(W2c_s, E, f, d, 0, W2c_sp, st, MX_BN_DGRAD2, 1);
 }
 
 int moe_grouped_swiglu_dgrad_mxfp8(const moe_cfg* c, const void* dy_perm, const int32_t* offsets,

@@ -165,21 +165,30 @@ struct TileCfg {
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
 };
 
-// MXFP8 tiles: two accumulators of BN columns, then a 16-column TMEM slot per ring stage for the
-// stage's block scales (A: 4 columns, B: 4 per 128 rows of the tile, at +8), in a 512-column
-// allocation.  BN = 192: accumulators 0..191 and 256..447, four stages' scales in 448..511;
-// BN = 128: accumulators 0..127 and 128..255, scale slots from 256.
+// MXFP8 tiles: the accumulators, then a 16-column TMEM slot per ring stage for the stage's block
+// scales (A: 4 columns, B: 4 per 128 rows of the tile, at +8), in a 512-column allocation.
+// BN = 192: two accumulators 0..191 and 256..447, four stages' scales in 448..511.  BN = 256: one
+// accumulator 0..255 (two would fill the 512 columns), scale slots from 256; the next tile's MMAs
+// then wait for the epilogue to drain it.
 constexpr int MX_SF_COLS = 16;
 template <int BN> struct MxCfg {
+  static constexpr int NACC = BN > 192 ? 1 : 2;               // accumulators
   static constexpr int SFB_CH = (BN + 127) / 128;             // 512-byte B chunks per stage
   static constexpr int SF_STAGE = MX_CHUNK * (1 + SFB_CH);    // A chunk, then B chunks
   static constexpr int ACC_STRIDE = 2 * BN <= 256 ? 128 : 256;
-  static constexpr int SF_COL0 = ACC_STRIDE + BN;
+  static constexpr int SF_COL0 = NACC == 1 ? BN : ACC_STRIDE + BN;
   static constexpr int MAX_STAGES = (512 - SF_COL0) / MX_SF_COLS;
 };
+// Epilogue staging: the MXFP8 SwiGLU backward stores directly (no slabs), and the 256-column
+// MXFP8 products keep one slab per warp, which leaves room for a fourth ring stage beside their
+// block scales.
+template <int BN, int SCHED, int EPI, bool F8, bool MX> struct EpiOf {
+  static constexpr bool staged = OutPath<SCHED, EPI>::tma && !(MX && EPI == EPI_SWIGLU_BWD);
+  static constexpr int slabs = (MX && BN == 256) ? 1 : EpiWidth<BN, SCHED, EPI, F8>::slabs;
+};
 template <int BN, int SCHED, int EPI, bool F8, bool MX> struct CfgOf {
-  using type = TileCfg<BN, OutPath<SCHED, EPI>::tma, EpiWidth<BN, SCHED, EPI, F8>::warps,
-                       EpiWidth<BN, SCHED, EPI, F8>::slabs, MX ? MxCfg<BN>::SF_STAGE : 0,
+  using type = TileCfg<BN, EpiOf<BN, SCHED, EPI, F8, MX>::staged, EpiWidth<BN, SCHED, EPI, F8>::warps,
+                       EpiOf<BN, SCHED, EPI, F8, MX>::slabs, MX ? MxCfg<BN>::SF_STAGE : 0,
                        MX ? (MxCfg<BN>::MAX_STAGES < 6 ? MxCfg<BN>::MAX_STAGES : 6) : 6,
                        MX ? 512 : 0>;
 };
@@ -320,7 +329,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
                    const __grid_constant__ CUtensorMap tmO2, const KArgs p) {
   constexpr bool TMA_OUT = OutPath<SCHED, EPI>::tma;
   constexpr int EPI_WARPS = EpiWidth<BN, SCHED, EPI, F8>::warps;
-  constexpr int SLABS = EpiWidth<BN, SCHED, EPI, F8>::slabs;
+  constexpr int SLABS = EpiOf<BN, SCHED, EPI, F8, MX>::slabs;
   using C = typename CfgOf<BN, SCHED, EPI, F8, MX>::type;
   constexpr bool MC = McMode<SCHED, EPI>::on;
   constexpr bool DYN = DynMode<SCHED, EPI>::on;
@@ -343,6 +352,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
                 "MXFP8 tile configuration");
   constexpr int STAGES = C::STAGES;
   constexpr uint32_t STAGE_TX = A_STAGE + C::B_STAGE + (MX ? MxCfg<BN>::SF_STAGE : 0);
+  constexpr int NACC = MX ? MxCfg<BN>::NACC : 2;   // TMEM accumulators (tile i uses i % NACC)
 
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sA = smem;
@@ -789,7 +799,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
       if (!ok) break;
       if (lane == 0) ptx::umma_commit(&tfull[acc]);   // accumulator ready for the epilogue
       __syncwarp();
-      acc ^= 1;
+      if (NACC == 2) acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
   } else {
@@ -1321,7 +1331,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
       if (aborted) break;
-      acc ^= 1;
+      if (NACC == 2) acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
     if (lane == 0) ptx::bulk_wait_all();   // every store of this warp has landed
@@ -2037,10 +2047,10 @@ int gemm_tc(const GemmDesc& g, cudaStream_t st) {
     // the data gradients: weights read MN-major (their stored layout), 128-column tiles
     if (!g.gather && g.sched == RAGGED_M && !g.A.mn_major && g.B.mn_major) {
       if (g.epi == EPI_SWIGLU_BWD)
-        return run<MX_BN_DGRAD, false, true, RAGGED_M, EPI_SWIGLU_BWD, false, true, true>(
+        return run<MX_BN_DGRAD2, false, true, RAGGED_M, EPI_SWIGLU_BWD, false, true, true>(
             g, "gemm_fc2_dgrad_mxfp8", st);
       if (g.epi == EPI_STORE)
-        return run<MX_BN_DGRAD, false, true, RAGGED_M, EPI_STORE, false, true, true>(
+        return run<MX_BN_DGRAD1, false, true, RAGGED_M, EPI_STORE, false, true, true>(
             g, "gemm_fc1_dgrad_mxfp8", st);
     }
     set_error("gemm_tc: unsupported MXFP8 combination sched=%d epi=%d a_mn=%d b_mn=%d", g.sched,

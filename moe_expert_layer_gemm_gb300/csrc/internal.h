@@ -198,8 +198,11 @@ struct GemmDesc {
 // chunks leave rows past an expert's end unwritten (their products are never stored) and set
 // blocks past K to 127.
 constexpr int MX_BN = 192;                 // output columns of an MXFP8 forward tile
-constexpr int MX_BN_DGRAD = 128;           // of an MXFP8 data-gradient tile (MN-major weights
-                                           // come in 128-column chunks)
+// MXFP8 data-gradient tiles (MN-major weights come in 128-column chunks): fc1's 256 columns wide
+// with one accumulator (fewer operand bytes per FLOP); fc2's, whose SwiGLU-backward epilogue is
+// long, 128 wide with two, so that the epilogue overlaps the next tile's MMAs.
+constexpr int MX_BN_DGRAD1 = 256;
+constexpr int MX_BN_DGRAD2 = 128;
 constexpr int MX_CHUNK = 512;
 constexpr int MX_SFB_CHUNKS = (MX_BN + 127) / 128;
 constexpr int MX_SFB_BYTES = MX_SFB_CHUNKS * MX_CHUNK;

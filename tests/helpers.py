@@ -225,7 +225,7 @@ def mx_weight_index(E, R, K, swiglu_f):
         ((rt % 128) // 32) * 4 + b % 4
 
 
-def mx_weight_index_cols(E, N, K, tile=128):
+def mx_weight_index_cols(E, N, K, tile=256):
     """Index [E, K/32, N] into a packed weight layout whose B-rows are the weight's N columns in
     tiles of `tile` (MOE_MX_SCALES_W1C / _W2C: scales of 32-row blocks down each column)."""
     kch, nb = (K + 127) // 128, K // 32

@@ -318,12 +318,12 @@ def test_dgrad_weight_copies(E, d, f):
     W2 = (varied((E, d, f), d + 1, 2.0).float() * 0.05).bfloat16().cuda()
     m = moe.alloc_mxfp8_dgrad(cfg, W1, W2)
     sync()
-    for W, pre, K, N in ((W1, "W1c", 2 * f, d), (W2, "W2c", d, f)):
+    for W, pre, K, N, tile in ((W1, "W1c", 2 * f, d, 256), (W2, "W2c", d, f, 128)):
         rq, rs = MX.mx_quantize_cols(W.double().cpu().numpy())
         assert np.array_equal(m[pre + "_q"].cpu().numpy(), rq)
         assert np.array_equal(m[pre + "_s"].cpu().numpy(), rs)
         p = m[pre + "_sp"].cpu().numpy()
-        idx = mx_weight_index_cols(E, N, K)
+        idx = mx_weight_index_cols(E, N, K, tile)
         assert np.array_equal(p[idx], rs)
         rest = np.ones(p.size, bool)
         rest[idx.ravel()] = False
