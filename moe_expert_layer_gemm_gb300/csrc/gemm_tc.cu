@@ -179,11 +179,10 @@ template <int BN> struct MxCfg {
   static constexpr int SF_COL0 = NACC == 1 ? BN : ACC_STRIDE + BN;
   static constexpr int MAX_STAGES = (512 - SF_COL0) / MX_SF_COLS;
 };
-// Epilogue staging: the MXFP8 SwiGLU backward stores directly (no slabs), and the 256-column
-// MXFP8 products keep one slab per warp, which leaves room for a fourth ring stage beside their
-// block scales.
+// Epilogue staging: the 256-column MXFP8 products keep one slab per warp, which leaves room for a
+// fourth ring stage beside their block scales.
 template <int BN, int SCHED, int EPI, bool F8, bool MX> struct EpiOf {
-  static constexpr bool staged = OutPath<SCHED, EPI>::tma && !(MX && EPI == EPI_SWIGLU_BWD);
+  static constexpr bool staged = OutPath<SCHED, EPI>::tma;
   static constexpr int slabs = (MX && BN == 256) ? 1 : EpiWidth<BN, SCHED, EPI, F8>::slabs;
 };
 template <int BN, int SCHED, int EPI, bool F8, bool MX> struct CfgOf {
@@ -905,7 +904,9 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
       // Full slabs go out through TMA (the maps clip at the tensors' edges).  For ragged rows a
       // slab that crosses the end of its expert's rows would overwrite the next expert's: it is
       // written with masked stores instead.
-      const bool tma_slab = TMA_OUT && (SCHED == RAGGED_K ? rows_here > 0 : rows_here == 32);
+      // (the MXFP8 SwiGLU backward stages through slabs only when [da | du] is also stored in bf16)
+      const bool tma_slab = TMA_OUT && (SCHED == RAGGED_K ? rows_here > 0 : rows_here == 32) &&
+                            (!(MX && EPI == EPI_SWIGLU_BWD) || p.out != nullptr);
       // FP8: the accumulator holds products of decoded E4M3 values; both scales apply here
       // (MXFP8: the block scales were applied by the MMAs)
       const float sc = F8 && !MX ? __ldg(p.a_scale) * __ldg(p.b_scale + (p.b_scale_per_group ? ti.g : 0)) : 1.0f;
@@ -1101,7 +1102,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
             }
           }
         }
-      } else if (MX && EPI == EPI_SWIGLU_BWD) {
+      } else if (MX && EPI == EPI_SWIGLU_BWD && !tma_slab) {
         // [da | du] from dh and the saved [a | u] of the row, written in bf16 (the weight
         // gradients' operand) when out is given and as MXFP8 codes and block scales along 2f
         // (fc1's data-gradient operand): a thread's 32 columns are one block of da and one of du
@@ -1186,6 +1187,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
             uint32_t dh[32];
             ptx::tmem_ld32(t_row + c + 32 * hf, dh);
             ptx::tmem_ld_wait();
+            float dav[MX ? 32 : 1], duv[MX ? 32 : 1];   // MXFP8: the block's bf16 values
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               float av[8], uv[8], da[8], du[8];
@@ -1203,9 +1205,49 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
                   track(da[i]);
                   track(du[i]);
                 }
+                if (MX) {
+                  da[i] = __bfloat162float(__float2bfloat16_rn(da[i]));
+                  du[i] = __bfloat162float(__float2bfloat16_rn(du[i]));
+                  dav[MX ? 8 * j + i : 0] = da[i];
+                  duv[MX ? 8 * j + i : 0] = du[i];
+                }
               }
               slab_put(sa, lane, 4 * hf + j, pack16(da, static_cast<const bf16*>(nullptr)));
               slab_put(su, lane, 4 * hf + j, pack16(du, static_cast<const bf16*>(nullptr)));
+            }
+            const int qc0 = col + 32 * hf;   // MXFP8: this block's column in the da half
+            if (MX && qc0 < p.f) {
+              // the 32 values are one block of da and one of du along [da | du]: codes and scale
+              uint8_t* qrow = p.q_out + static_cast<int64_t>(row) * 2 * p.f;
+              uint8_t* sfrow = p.q_sf + static_cast<int64_t>(ti.mt) * p.kch_out * MX_CHUNK +
+                               (r & 31) * 16 + (r >> 5) * 4;
+              const int nb2 = 2 * p.f / 32;
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                const float* vals = half ? duv : dav;
+                float am = 0.f;
+#pragma unroll
+                for (int i = 0; i < (MX ? 32 : 1); ++i) am = fmaxf(am, fabsf(vals[i]));
+                const int ex = mx_exponent(am);
+                const float inv = mx_inv_scale(ex);
+                uint32_t w[8];
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                  const int b0 = MX ? 4 * jj : 0;
+                  const uint32_t lo = cvt_e4m3x2(vals[b0] * inv, vals[MX ? b0 + 1 : 0] * inv);
+                  const uint32_t hi = cvt_e4m3x2(vals[MX ? b0 + 2 : 0] * inv, vals[MX ? b0 + 3 : 0] * inv);
+                  w[jj] = lo | (hi << 16);
+                }
+                const int qc = half * p.f + qc0;
+                *reinterpret_cast<uint4*>(qrow + qc) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4*>(qrow + qc + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+                const int blk = qc >> 5;
+                uint8_t* sfp = sfrow + (blk >> 2) * MX_CHUNK;
+                sfp[blk & 3] = static_cast<uint8_t>(ex + 127);
+                if (blk == nb2 - 1) {
+                  for (int jj = (blk & 3) + 1; jj < 4; ++jj) sfp[jj] = 127;   // blocks past 2f
+                }
+              }
             }
           }
           slab_store_2d(&tmO0, sa, lane, col, row0);
@@ -1911,7 +1953,7 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
       MOE_TRY(map_bf16(&mo[1], g.out2, rows, g.f, g.ldo2, 32));
       MOE_TRY(map_bf16(&mo[2], static_cast<const bf16*>(g.out2) + g.f, rows, g.f, g.ldo2, 32));
     }
-  } else if (EPI == EPI_SWIGLU_BWD && !MX) {   // (MXFP8: direct loads and stores, no maps)
+  } else if (EPI == EPI_SWIGLU_BWD && (!MX || g.out)) {   // (MXFP8 without bf16 out: direct stores)
     MOE_TRY(map_bf16(&mo[0], g.out, rows, g.f, g.ldo, 32));
     MOE_TRY(map_bf16(&mo[1], static_cast<const bf16*>(g.out) + g.f, rows, g.f, g.ldo, 32));
     MOE_TRY(map_bf16(&mo[2], g.aux, rows, 2 * static_cast<int64_t>(g.f), g.ld_aux, 32));
