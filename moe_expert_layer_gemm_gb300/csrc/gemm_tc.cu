@@ -1,5 +1,6 @@
-// Grouped GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), bf16 in, fp32
-// accumulate.  One kernel template serves every matrix product of the layer:
+// Grouped GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), bf16 in (or E4M3 with
+// a tensorwise scale, or MXFP8: E4M3 with an E8M0 scale per 32 K-elements), fp32 accumulate.
+// One kernel template serves every matrix product of the layer:
 //   fc1 + SwiGLU, fc2 (ragged rows per expert), their data gradients (ragged rows, weights read
 //   MN-major), their weight gradients (ragged reduction per expert), the router and the
 //   shared expert (one group).
@@ -10,7 +11,9 @@
 // CTA organisation (persistent, one CTA per SM):
 //   warp 0     TMA producer: loads A/B k-blocks into a STAGES-deep shared-memory ring
 //   warp 1     MMA issuer: owns TMEM (2 accumulators of BN fp32 columns), issues
-//              tcgen05.mma (M=128, N=BN, K=16) per k-step, commits to the ring's empty barriers
+//              tcgen05.mma (M=128, N=BN, K=16 bf16 / 32 E4M3) per k-step, commits to the ring's
+//              empty barriers; MXFP8: first copies the stage's block scales into a TMEM slot
+//              (tcgen05.cp) for the block-scaled MMAs
 //   warps 2..  epilogue (4 or 8 warps): TMEM -> registers (tcgen05.ld) -> fused epilogue ->
 //              a swizzled shared-memory slab per warp (32 rows x 128 bytes) -> TMA bulk-tensor
 //              store, overlapped with the next tile's MMAs through the second accumulator
