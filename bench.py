@@ -107,6 +107,8 @@ def kernel_work(lc, trace=None, steps=1):
     w["mxfp8_permute_quantize"] = ("hbm", T * d * 2 + N * d * 33 / 32 + N * 4 +
                                    (N * d * 2 if lc.backward else 0))
     w["mxfp8_quantize_rows"] = ("hbm", N * d * 2 + N * d * 33 / 32)   # dy_perm in expert order
+    # the combine backward that also writes dy_perm's codes and scales
+    w["combine_bwd_mxfp8"] = ("hbm", w["combine_bwd"][1] + N * d * 33 / 32)
     return w
 
 

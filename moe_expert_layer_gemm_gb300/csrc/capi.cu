@@ -1173,10 +1173,11 @@ static int dgrad_mx_impl(const moe_cfg* c, const int32_t* offsets, int64_t N, co
 static int ffn_bwd_mx_impl(const moe_cfg* c, const int32_t* offsets, int64_t N, const void* x_perm,
                            const void* act, const void* h, const void* dy_perm, void* dH1,
                            void* dx_perm, float* dW1, float* dW2, int* sched, cudaStream_t st,
-                           const moe_mxfp8_dgrad* m) {
+                           const moe_mxfp8_dgrad* m, bool dy_quantised = false) {
   const int d = c->d, f = c->f, E = c->E;
-  MOE_TRY(launch_permute_quant_mx(dy_perm, nullptr, offsets, m->dy_q, m->dy_s, static_cast<int>(N),
-                                  d, 1, E, st));
+  if (!dy_quantised)   // else the layer's combine backward wrote dy_perm's codes and scales
+    MOE_TRY(launch_permute_quant_mx(dy_perm, nullptr, offsets, m->dy_q, m->dy_s,
+                                    static_cast<int>(N), d, 1, E, st));
   GemmDesc a = desc0();
   a.name = "gemm_fc2_dgrad_mxfp8";
   a.sched = RAGGED_M;
@@ -1614,10 +1615,15 @@ static int layer_bwd_impl(const moe_cfg* c, const void* dy, const void* x, const
   if (q && (cudaMemsetAsync(q->scales + 5, 0, sizeof(float), st) != cudaSuccess ||
             (sq && cudaMemsetAsync(q->scales + 11, 0, sizeof(float), st) != cudaSuccess)))
     return fail(MOE_ERR_CUDA, "clearing the gradient amaxes failed");
-  MOE_TRY(launch_combine_bwd(c->dtype, dy, s->y_perm, s->gate, s->slot_of_pair,
-                             sh ? s->s_out : nullptr, gt ? s->s_coef : nullptr, w.dy_perm, w.dgate,
-                             w.dshared, w.dcoef, T, d, k, st, q ? q->scales + 5 : nullptr,
-                             sq ? q->scales + 11 : nullptr));
+  if (mxd)   // MXFP8 data gradients: dy_perm's codes come out of the same pass
+    MOE_TRY(launch_combine_bwd_mx(dy, s->y_perm, s->gate, s->slot_of_pair, sh ? s->s_out : nullptr,
+                                  gt ? s->s_coef : nullptr, w.dy_perm, w.dgate, w.dshared, w.dcoef,
+                                  T, d, k, s->offsets, E, mxd->dy_q, mxd->dy_s, st));
+  else
+    MOE_TRY(launch_combine_bwd(c->dtype, dy, s->y_perm, s->gate, s->slot_of_pair,
+                               sh ? s->s_out : nullptr, gt ? s->s_coef : nullptr, w.dy_perm,
+                               w.dgate, w.dshared, w.dcoef, T, d, k, st,
+                               q ? q->scales + 5 : nullptr, sq ? q->scales + 11 : nullptr));
   // 2.-6. The routed experts run on `st`; the shared expert and the router's backward (which
   // need only combine-backward outputs) run on the side stream concurrently; dx waits for both.
   SideStream* side = (MOE_SHARED_OVERLAP_BWD && g_overlap.load()) ? side_stream() : nullptr;
@@ -1689,7 +1695,7 @@ static int layer_bwd_impl(const moe_cfg* c, const void* dy, const void* x, const
   // routed experts (dx_perm overwrites dy_perm once it is no longer read)
   if (mxd)
     MOE_TRY(ffn_bwd_mx_impl(c, s->offsets, Nrows(c), s->x_perm, s->act, s->h, w.dy_perm, w.dH1,
-                            w.dy_perm, dW1, dW2, w.sched, st, mxd));
+                            w.dy_perm, dW1, dW2, w.sched, st, mxd, true));
   else if (q)
     MOE_TRY(ffn_bwd_fp8_impl(c, c->E, s->offsets, Nrows(c), c->f, q->x_perm_q, q->scales + 0, q->W1_q, q->W1_scale,
                              q->W2_q, q->W2_scale, s->act, q->h_q, q->scales + 2, w.dy_perm, dy_q,

@@ -128,4 +128,45 @@ __device__ __forceinline__ float mx_inv_scale(int e) {
   return __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
 }
 
+// MXFP8 activation scales are packed per 128-row tile of the expert-sorted rows (the GEMMs' row
+// tiles).  s_off <- offsets[0..E]; s_pre[e] <- sum over e' < e of ceil(rows_e' / 128).  Called by
+// every thread of the block (it synchronises); warp 0 scans.
+__device__ __forceinline__ void mx_tile_prefix(const int32_t* offsets, int E, int* s_off,
+                                               int* s_pre) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = offsets[i];
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int lo = min(E, lane * per), hi = min(E, lo + per);
+    int local = 0;
+    for (int e = lo; e < hi; ++e) local += (s_off[e + 1] - s_off[e] + 127) / 128;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int e = lo; e < hi; ++e) {
+      s_pre[e] = run;
+      run += (s_off[e + 1] - s_off[e] + 127) / 128;
+    }
+  }
+  __syncthreads();
+}
+// Byte offset of row `slot`'s scales (its row of its tile's first 512-byte chunk) in the packed
+// activation layout with kch 128-element chunks per row (slot < s_off[E]).
+__device__ __forceinline__ int64_t mx_row_scale_base(int slot, const int* s_off, const int* s_pre,
+                                                     int E, int kch) {
+  int lo = 0, hi = E;   // the largest e with s_off[e] <= slot: the expert that holds it
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_off[mid] <= slot) lo = mid; else hi = mid;
+  }
+  const int rr = slot - s_off[lo];
+  return (static_cast<int64_t>(s_pre[lo]) + rr / 128) * kch * 512 + ((rr & 127) & 31) * 16 +
+         ((rr & 127) >> 5) * 4;
+}
+
 }  // namespace moe

@@ -103,6 +103,12 @@ int launch_combine_bwd(int dtype, const void* dy, const void* y_perm, const floa
                        const float* shared_coef, void* dy_perm, float* dgate, void* dshared,
                        float* dcoef, int T, int d, int k, cudaStream_t st, float* amax_dy = nullptr,
                        float* amax_ds = nullptr);
+// As launch_combine_bwd (bf16 only), and dy_perm's MXFP8 codes and packed scales as it stores it.
+int launch_combine_bwd_mx(const void* dy, const void* y_perm, const float* gate,
+                          const int32_t* sop, const void* shared_out, const float* shared_coef,
+                          void* dy_perm, float* dgate, void* dshared, float* dcoef, int T, int d,
+                          int k, const int32_t* offsets, int E, uint8_t* dy_q, uint8_t* dy_s,
+                          cudaStream_t st);
 int launch_gather_sum(int dtype, const void* dx_perm, const int32_t* slot_of_pair,
                       const void* dx_shared, const void* dx_router, const float* dz,
                       const void* w_sg, void* dx, int T, int d, int k, cudaStream_t st);

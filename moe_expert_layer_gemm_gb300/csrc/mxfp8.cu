@@ -134,28 +134,8 @@ __global__ void __launch_bounds__(MXP_THREADS) permute_quant_mx_kernel(
     int E, int* err) {
   __shared__ int s_off[MOE_MAX_EXPERTS + 1];
   __shared__ int s_pre[MOE_MAX_EXPERTS + 1];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = offsets[i];
-  __syncthreads();
-  if (warp == 0) {
-    // s_pre[e] = sum_{e' < e} ceil(rows_e' / 128), lane L over experts [L*per, (L+1)*per)
-    const int per = (E + 31) / 32;
-    const int lo = min(E, lane * per), hi = min(E, lo + per);
-    int local = 0;
-    for (int e = lo; e < hi; ++e) local += (s_off[e + 1] - s_off[e] + 127) / 128;
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    int run = incl - local;
-    for (int e = lo; e < hi; ++e) {
-      s_pre[e] = run;
-      run += (s_off[e + 1] - s_off[e] + 127) / 128;
-    }
-  }
-  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  mx_tile_prefix(offsets, E, s_off, s_pre);
   const int64_t N = static_cast<int64_t>(Tn) * k;
   const int kch = (d + 127) / 128;
   const int nb = d / 32;
@@ -170,14 +150,7 @@ __global__ void __launch_bounds__(MXP_THREADS) permute_quant_mx_kernel(
         record_error(err, DEVERR_BAD_SLOT);
         my_slot = -1;
       } else {
-        int lo = 0, hi = E;   // largest e with s_off[e] <= slot (an expert that holds it)
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (s_off[mid] <= my_slot) lo = mid; else hi = mid;
-        }
-        const int rr = my_slot - s_off[lo];
-        my_sf = (static_cast<int64_t>(s_pre[lo]) + rr / 128) * kch * MX_CHUNK +
-                ((rr & 127) & 31) * 16 + ((rr & 127) >> 5) * 4;
+        my_sf = mx_row_scale_base(my_slot, s_off, s_pre, E, kch);
       }
     }
     int slot[MOE_MAX_TOPK];

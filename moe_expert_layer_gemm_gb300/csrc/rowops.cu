@@ -252,6 +252,143 @@ __global__ void __launch_bounds__(ROW_THREADS) combine_bwd_kernel(
   }
 }
 
+// The combine backward of an MXFP8 data-gradient backward (bf16 only): as combine_bwd_kernel,
+// and each dy_perm row it stores is also quantised to MXFP8 (blocks of 32 along d, from the bf16
+// value stored) into dy_q [N, d], with its scales in dy_s in the packed activation layout of the
+// routing's 128-row tiles: the fc2 data gradient's A operand, without a second pass over dy_perm.
+// A 4-lane group holds one 32-block (8 values a lane), so a block's amax takes two shuffles.
+__global__ void __launch_bounds__(ROW_THREADS, 2) combine_bwd_mx_kernel(
+    const bf16* __restrict__ dy, const bf16* __restrict__ y_perm, const float* __restrict__ gate,
+    const int32_t* __restrict__ sop, const bf16* __restrict__ shared_out,
+    const float* __restrict__ shared_coef, bf16* __restrict__ dy_perm, float* __restrict__ dgate,
+    bf16* __restrict__ dshared, float* __restrict__ dcoef, int Tn, int d, int k,
+    const int32_t* __restrict__ offsets, int E, uint8_t* __restrict__ dy_q,
+    uint8_t* __restrict__ dy_s, int* err) {
+  __shared__ int s_off[MOE_MAX_EXPERTS + 1];
+  __shared__ int s_pre[MOE_MAX_EXPERTS + 1];
+  mx_tile_prefix(offsets, E, s_off, s_pre);
+  constexpr int VE = 8;
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int vpr = d / VE;
+  const int kch = (d + 127) / 128;
+  const int nb = d / 32;
+  const bf16* tag = nullptr;
+  for (int t = gw; t < Tn; t += nw) {
+    const int64_t pk = static_cast<int64_t>(t) * k;
+    int my_slot = lane < k ? checked_slot(sop[pk + lane], Tn, k, err) : -1;
+    int64_t my_sf = 0;
+    if (my_slot >= s_off[E]) {   // beyond the routed rows: the map and the offsets disagree
+      record_error(err, DEVERR_BAD_SLOT);
+      my_slot = -1;
+    }
+    if (my_slot >= 0) my_sf = mx_row_scale_base(my_slot, s_off, s_pre, E, kch);
+    const float my_g = lane < k ? gate[pk + lane] : 0.f;
+    const float c = shared_coef ? shared_coef[t] : 1.0f;
+    int slot[MAXK];
+    float gj[MAXK];
+#pragma unroll
+    for (int j = 0; j < MAXK; ++j) {
+      slot[j] = __shfl_sync(0xffffffffu, my_slot, j);
+      gj[j] = __shfl_sync(0xffffffffu, my_g, j);
+    }
+    float dot[MAXK];
+#pragma unroll
+    for (int j = 0; j < MAXK; ++j) dot[j] = 0.f;
+    float dotc = 0.f;
+    const char* dyrow = reinterpret_cast<const char*>(dy + static_cast<int64_t>(t) * d);
+    for (int v0 = 0; v0 < vpr; v0 += 32) {   // every lane stays for the group shuffles
+      const int v = v0 + lane;
+      const bool act = v < vpr;   // d % 32 == 0: a 4-lane group is all in or all out
+      float g_in[VE];
+      unpack16(act ? ld_nc16(dyrow + static_cast<int64_t>(v) * 16) : make_uint4(0, 0, 0, 0), g_in,
+               tag);
+      uint4 raw[MAXK];
+#pragma unroll
+      for (int j = 0; j < MAXK; ++j) {
+        if (j < k && act) {
+          const int s = slot[j] < 0 ? 0 : slot[j];
+          raw[j] = ld_nc16(reinterpret_cast<const char*>(y_perm + static_cast<int64_t>(s) * d) +
+                           static_cast<int64_t>(v) * 16);
+        }
+      }
+      const int blk = (v * VE) >> 5;
+      const bool writes_scale = act && (lane & 3) == 0;
+      const bool pads = writes_scale && blk == nb - 1 && (nb & 3) != 0;
+#pragma unroll
+      for (int j = 0; j < MAXK; ++j) {
+        if (j >= k) break;
+        const int s = slot[j];
+        float o[VE];
+        float m = 0.f;
+        if (act) {
+          float yv[VE];
+          unpack16(raw[j], yv, tag);
+#pragma unroll
+          for (int i = 0; i < VE; ++i) {
+            dot[j] = fmaf(g_in[i], yv[i], dot[j]);
+            o[i] = as_stored(gj[j] * g_in[i], tag);   // the bf16 value dy_perm holds
+            m = fmaxf(m, fabsf(o[i]));
+          }
+        }
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        const int64_t sfb = __shfl_sync(0xffffffffu, my_sf, j);   // (re-read: fewer live registers)
+        if (!act || s < 0) continue;
+        const int64_t row = static_cast<int64_t>(s) * d;
+        st16(reinterpret_cast<char*>(dy_perm + row) + static_cast<int64_t>(v) * 16, pack16(o, tag));
+        const int e = mx_exponent(m);
+        const float inv = mx_inv_scale(e);
+        uint32_t w[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint32_t lo = cvt_e4m3x2(o[4 * q] * inv, o[4 * q + 1] * inv);
+          const uint32_t hi = cvt_e4m3x2(o[4 * q + 2] * inv, o[4 * q + 3] * inv);
+          w[q] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint2*>(dy_q + row + static_cast<int64_t>(v) * VE) =
+            make_uint2(w[0], w[1]);
+        if (writes_scale) {
+          uint8_t* sf = dy_s + sfb + (blk >> 2) * MX_CHUNK;
+          sf[blk & 3] = static_cast<uint8_t>(e + 127);
+          if (pads)
+            for (int q = (blk & 3) + 1; q < 4; ++q) sf[q] = 127;   // blocks past d: 2^0
+        }
+      }
+      if (shared_out && act) {
+        if (dcoef) {
+          float sv[VE];
+          unpack16(ld_nc16(reinterpret_cast<const char*>(shared_out + static_cast<int64_t>(t) * d) +
+                           static_cast<int64_t>(v) * 16),
+                   sv, tag);
+#pragma unroll
+          for (int i = 0; i < VE; ++i) dotc = fmaf(g_in[i], sv[i], dotc);
+        }
+        if (dshared) {
+          float o[VE];
+#pragma unroll
+          for (int i = 0; i < VE; ++i) o[i] = c * g_in[i];
+          st16(reinterpret_cast<char*>(dshared + static_cast<int64_t>(t) * d) +
+                   static_cast<int64_t>(v) * 16,
+               pack16(o, tag));
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < MAXK; ++j) {
+      if (j < k) {
+        const float s = warp_sum(dot[j]);
+        if (lane == 0) dgate[pk + j] = s;
+      }
+    }
+    if (shared_out && dcoef) {
+      const float s = warp_sum(dotc);
+      if (lane == 0) dcoef[t] = s;
+    }
+  }
+}
+
 // ----------------------------------------------------------------------------- permute bwd
 // dx[t] = sum_j dx_perm[slot(t,j)] + dx_shared[t] + dx_router[t] + dz[t] * w_sg  (fp32, that
 // order, one rounding).  Optional terms are skipped when their pointer is null.
@@ -535,6 +672,17 @@ int launch_combine_bwd(int dtype, const void* dy, const void* y_perm, const floa
                 (const float*)dy, (const float*)y_perm, gate, sop, (const float*)shared_out,
                 shared_coef, (float*)dy_perm, dgate, (float*)dshared, dcoef, T, d, k,
                 device_error_word(), ady, ads);
+}
+
+int launch_combine_bwd_mx(const void* dy, const void* y_perm, const float* gate,
+                          const int32_t* sop, const void* shared_out, const float* shared_coef,
+                          void* dy_perm, float* dgate, void* dshared, float* dcoef, int T, int d,
+                          int k, const int32_t* offsets, int E, uint8_t* dy_q, uint8_t* dy_s,
+                          cudaStream_t st) {
+  return launch("combine_bwd_mxfp8", combine_bwd_mx_kernel, row_grid(T), dim3(ROW_THREADS), 0, st,
+                (const bf16*)dy, (const bf16*)y_perm, gate, sop, (const bf16*)shared_out,
+                shared_coef, (bf16*)dy_perm, dgate, (bf16*)dshared, dcoef, T, d, k, offsets, E,
+                dy_q, dy_s, device_error_word());
 }
 
 int launch_gather_sum(int dtype, const void* dx_perm, const int32_t* sop, const void* dx_shared,

@@ -400,6 +400,17 @@ def test_mxfp8_layer_backward():
                             saved, gmx["dx"], gmx["dW_r"], gmx["dW1"], gmx["dW2"], gmx["dWs1"],
                             gmx["dWs2"], None, ws)
     sync()
+    # dy_perm's codes and scales, written by the combine backward: the oracle's quantisation of
+    # dy_perm[slot(t, j)] = bf16(gate[t, j] * dy[t]) (an fp32 product rounded once, as stored)
+    N = lc.T * lc.k
+    sop = np64(saved["slot_of_pair"]).astype(np.int64).reshape(-1)
+    prod = (saved["gate"].cpu().float()[..., None] * inp["dy"].cpu().float()[:, None, :])
+    dy_perm = np.zeros((N, d))
+    dy_perm[sop] = np64(prod.to(torch.bfloat16).reshape(N, d))
+    rq, rs = MX.mx_quantize(dy_perm)
+    o = np64(saved["offsets"]).astype(np.int64)
+    assert np.array_equal(mxd["dy_q"].cpu().numpy(), rq)
+    assert np.array_equal(mx_unpack_act_scales(mxd["dy_s"].cpu().numpy(), o, N, d), rs)
     # the router's and shared expert's gradients do not depend on the routed data gradients
     for name in ("dW_r", "dWs1", "dWs2", "dW2"):
         assert torch.equal(gmx[name], g16[name]), name
