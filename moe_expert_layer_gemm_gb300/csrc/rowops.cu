@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(ROW_THREADS) permute_kernel(const T* __restric
 // y[t] = sum_{j<k} gate[t,j] * y_perm[slot(t,j)]  (+ c_t * shared_out[t]); fp32, j ascending,
 // the shared term last, one rounding.
 template <typename T>
-__global__ void __launch_bounds__(ROW_THREADS) combine_kernel(
+__global__ void __launch_bounds__(ROW_THREADS, 3) combine_kernel(
     const T* __restrict__ y_perm, const float* __restrict__ gate, const int32_t* __restrict__ sop,
     const T* __restrict__ shared_out, const float* __restrict__ shared_coef, T* __restrict__ y,
     int Tn, int d, int k, int* err) {
@@ -109,6 +109,10 @@ __global__ void __launch_bounds__(ROW_THREADS) combine_kernel(
                            static_cast<int64_t>(v) * 16);
         }
       }
+      uint4 raw_s = make_uint4(0, 0, 0, 0);   // requested with the routed rows, used last
+      if (shared_out)
+        raw_s = ld_nc16(reinterpret_cast<const char*>(shared_out + static_cast<int64_t>(t) * d) +
+                        static_cast<int64_t>(v) * 16);
       float acc[VE];
 #pragma unroll
       for (int i = 0; i < VE; ++i) acc[i] = 0.f;
@@ -124,9 +128,7 @@ __global__ void __launch_bounds__(ROW_THREADS) combine_kernel(
       }
       if (shared_out) {
         float val[VE];
-        unpack16(ld_nc16(reinterpret_cast<const char*>(shared_out + static_cast<int64_t>(t) * d) +
-                         static_cast<int64_t>(v) * 16),
-                 val, static_cast<const T*>(nullptr));
+        unpack16(raw_s, val, static_cast<const T*>(nullptr));
 #pragma unroll
         for (int i = 0; i < VE; ++i) acc[i] = fmaf(c, val[i], acc[i]);
       }
@@ -393,7 +395,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 2) combine_bwd_mx_kernel(
 // dx[t] = sum_j dx_perm[slot(t,j)] + dx_shared[t] + dx_router[t] + dz[t] * w_sg  (fp32, that
 // order, one rounding).  Optional terms are skipped when their pointer is null.
 template <typename T>
-__global__ void __launch_bounds__(ROW_THREADS) gather_sum_kernel(
+__global__ void __launch_bounds__(ROW_THREADS, 3) gather_sum_kernel(
     const T* __restrict__ dx_perm, const int32_t* __restrict__ sop, const T* __restrict__ dx_shared,
     const T* __restrict__ dx_router, const float* __restrict__ dz, const T* __restrict__ w_sg,
     T* __restrict__ dx, int Tn, int d, int k, int* err) {
@@ -419,6 +421,11 @@ __global__ void __launch_bounds__(ROW_THREADS) gather_sum_kernel(
                            static_cast<int64_t>(v) * 16);
         }
       }
+      // the per-token terms are requested with the routed rows and added after them
+      const int64_t ro = static_cast<int64_t>(t) * d * sizeof(T) + static_cast<int64_t>(v) * 16;
+      uint4 raw_s = make_uint4(0, 0, 0, 0), raw_r = make_uint4(0, 0, 0, 0);
+      if (dx_shared) raw_s = ld_nc16(reinterpret_cast<const char*>(dx_shared) + ro);
+      if (dx_router) raw_r = ld_nc16(reinterpret_cast<const char*>(dx_router) + ro);
       float acc[VE];
 #pragma unroll
       for (int i = 0; i < VE; ++i) acc[i] = 0.f;
@@ -431,18 +438,15 @@ __global__ void __launch_bounds__(ROW_THREADS) gather_sum_kernel(
           for (int i = 0; i < VE; ++i) acc[i] += val[i];
         }
       }
-      const int64_t ro = static_cast<int64_t>(t) * d * sizeof(T) + static_cast<int64_t>(v) * 16;
       if (dx_shared) {
         float val[VE];
-        unpack16(ld_nc16(reinterpret_cast<const char*>(dx_shared) + ro), val,
-                 static_cast<const T*>(nullptr));
+        unpack16(raw_s, val, static_cast<const T*>(nullptr));
 #pragma unroll
         for (int i = 0; i < VE; ++i) acc[i] += val[i];
       }
       if (dx_router) {
         float val[VE];
-        unpack16(ld_nc16(reinterpret_cast<const char*>(dx_router) + ro), val,
-                 static_cast<const T*>(nullptr));
+        unpack16(raw_r, val, static_cast<const T*>(nullptr));
 #pragma unroll
         for (int i = 0; i < VE; ++i) acc[i] += val[i];
       }
