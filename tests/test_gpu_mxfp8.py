@@ -210,6 +210,9 @@ LAYER_CASES = {
                                             score_fn=O.SOFTMAX, renorm=1, shared_gate=1,
                                             router_init="uniform"),
     "no-shared": moe_inputs.LayerConfig("mx plain", 500, 2688, 8, 2, 1856),
+    # d = 224 and 2f = 192: the last 128-wide scale chunk of a row is partly padding
+    "ragged-d": moe_inputs.LayerConfig("mx ragged d", 131, 224, 8, 3, 96, f_shared=64,
+                                       score_fn=O.SOFTMAX, renorm=1, shared_gate=1),
 }
 
 
@@ -368,11 +371,12 @@ def test_mxfp8_data_gradients(T, d, E, k, f, empty):
     print(f"dH1 {e_dh1:.2e} dx_perm {e_dx:.2e}")
 
 
-def test_mxfp8_layer_backward():
+@pytest.mark.parametrize("name", ["sigmoid-shared", "ragged-d"])
+def test_mxfp8_layer_backward(name):
     """moe_layer_bwd_mxfp8 after moe_layer_fwd_mxfp8: the weight gradients and dx against the bf16
     backward on the same saved state (they differ by the data gradients' MXFP8 rounding) and
     against the unquantised oracle."""
-    lc = LAYER_CASES["sigmoid-shared"]
+    lc = LAYER_CASES[name]
     host, _ = clean_inputs(lc)
     inp = {k: (None if v is None else v.cuda()) for k, v in host.items()}
     cfg = moe.cfg_from(lc)
@@ -390,15 +394,16 @@ def test_mxfp8_layer_backward():
                     dW1=torch.empty(E, 2 * f, d, dtype=f32, device="cuda"),
                     dW2=torch.empty(E, d, f, dtype=f32, device="cuda"),
                     dWs1=torch.empty(2 * fs, d, dtype=f32, device="cuda"),
-                    dWs2=torch.empty(d, fs, dtype=f32, device="cuda"))
+                    dWs2=torch.empty(d, fs, dtype=f32, device="cuda"),
+                    dw_sg=torch.empty(d, dtype=f32, device="cuda") if lc.shared_gate else None)
     ws = moe.workspace(cfg, moe.WS_LAYER_BWD)
     g16, gmx = grads(), grads()
     moe.moe_layer_bwd(cfg, inp["dy"], inp["x"], inp["W_r"], inp["W1"], inp["W2"], inp["Ws1"],
-                      inp["Ws2"], None, saved, g16["dx"], g16["dW_r"], g16["dW1"], g16["dW2"],
-                      g16["dWs1"], g16["dWs2"], None, ws)
-    moe.moe_layer_bwd_mxfp8(cfg, inp["dy"], inp["x"], inp["W_r"], mxd, inp["Ws1"], inp["Ws2"], None,
-                            saved, gmx["dx"], gmx["dW_r"], gmx["dW1"], gmx["dW2"], gmx["dWs1"],
-                            gmx["dWs2"], None, ws)
+                      inp["Ws2"], inp["w_sg"], saved, g16["dx"], g16["dW_r"], g16["dW1"],
+                      g16["dW2"], g16["dWs1"], g16["dWs2"], g16["dw_sg"], ws)
+    moe.moe_layer_bwd_mxfp8(cfg, inp["dy"], inp["x"], inp["W_r"], mxd, inp["Ws1"], inp["Ws2"],
+                            inp["w_sg"], saved, gmx["dx"], gmx["dW_r"], gmx["dW1"], gmx["dW2"],
+                            gmx["dWs1"], gmx["dWs2"], gmx["dw_sg"], ws)
     sync()
     # dy_perm's codes and scales, written by the combine backward: the oracle's quantisation of
     # dy_perm[slot(t, j)] = bf16(gate[t, j] * dy[t]) (an fp32 product rounded once, as stored)
@@ -411,14 +416,15 @@ def test_mxfp8_layer_backward():
     o = np64(saved["offsets"]).astype(np.int64)
     assert np.array_equal(mxd["dy_q"].cpu().numpy(), rq)
     assert np.array_equal(mx_unpack_act_scales(mxd["dy_s"].cpu().numpy(), o, N, d), rs)
+    assert (mx_act_pad_bytes(mxd["dy_s"].cpu().numpy(), o, N, d) == 127).all()
     # the router's and shared expert's gradients do not depend on the routed data gradients
-    for name in ("dW_r", "dWs1", "dWs2", "dW2"):
-        assert torch.equal(gmx[name], g16[name]), name
+    for g in ("dW_r", "dWs1", "dWs2", "dW2") + (("dw_sg",) if lc.shared_gate else ()):
+        assert torch.equal(gmx[g], g16[g]), g
     ref = oracle_layer(lc, {k: (None if v is None else v.cpu()) for k, v in inp.items()})
     errs = {}
-    for name in ("dx", "dW1"):
-        errs[name + " vs bf16"] = rel_err(np64(gmx[name]), np64(g16[name]))
-        assert errs[name + " vs bf16"] < 0.1, errs
-        errs[name + " vs oracle"] = rel_err(np64(gmx[name]), ref["bwd"][name])
-        assert errs[name + " vs oracle"] < 0.15, errs
+    for g in ("dx", "dW1"):
+        errs[g + " vs bf16"] = rel_err(np64(gmx[g]), np64(g16[g]))
+        assert errs[g + " vs bf16"] < 0.1, errs
+        errs[g + " vs oracle"] = rel_err(np64(gmx[g]), ref["bwd"][g])
+        assert errs[g + " vs oracle"] < 0.15, errs
     print("mxfp8 layer backward:", {k: f"{v:.3f}" for k, v in errs.items()})
