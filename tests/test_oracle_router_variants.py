@@ -10,8 +10,10 @@ against a restatement of the oracle's own formulas; planted mistakes must fail a
   * layer gradients with the loss and with a selection-only bias -- finite differences of
     sum(y * dy) + L_aux through the whole oracle layer
   * expert bias -- a bias larger than any score range forces its experts into every token's
-    choice; the gates never change with the bias; zero bias selects as the logits do; the
-    update moves each bias by -rate, 0 or +rate by the sign of (mean load - load)
+    choice; the gates never change with the bias; zero bias selects as the logits do; two
+    hand-worked softmax rows where score + bias, logit + bias and sigmoid + bias choose
+    different experts; the update moves each bias by -rate, 0 or +rate by the sign of
+    (mean load - load)
 """
 import types
 
@@ -187,6 +189,37 @@ def test_selection_bias_forces_its_experts_and_never_moves_the_gates():
     assert np.allclose(f1["logits"], inp["x"] @ inp["W_r"].T, rtol=0, atol=1e-13)
 
 
+def test_softmax_selection_keys_by_hand():
+    """Softmax routing with a selection-only bias ("Megatron-Bridge 深度剖析", §Nemotron-3-Nano
+    配置, expert-bias correction; the reading that the bias is added to the softmax over all E
+    experts).  Two hand-worked rows, chosen so that the three plausible keys disagree:
+
+    row A, logits [2, 0, 0], bias [0, 0.75, 0]:
+      softmax over E: e^2 / (e^2 + 2) = 7.389056 / 9.389056 = 0.786986, 1 / 9.389056 = 0.106507
+      keys = [0.786986, 0.856507, 0.106507] -> top-1 is expert 1, top-2 is (1, 0);
+      logit + bias = [2, 0.75, 0] would pick expert 0.
+    row B, logits [1, 0], bias [0, 0.3]:
+      softmax: e / (e + 1) = 0.731059, 1 / (e + 1) = 0.268941
+      keys = [0.731059, 0.568941] -> top-1 is expert 0;
+      sigmoid + bias = [0.731059, 0.5 + 0.3 = 0.8] would pick expert 1.
+    """
+    kA = O.selection_keys(np.array([[2.0, 0.0, 0.0]], np.float32), O.SOFTMAX,
+                          np.array([0.0, 0.75, 0.0], np.float32))
+    assert kA.dtype == np.float32
+    assert np.allclose(kA[0], [0.786986, 0.856507, 0.106507], rtol=0, atol=2e-6)
+    assert O.select_topk(kA, 1).tolist() == [[1]]
+    assert O.select_topk(kA, 2).tolist() == [[1, 0]]
+    kB = O.selection_keys(np.array([[1.0, 0.0]], np.float32), O.SOFTMAX,
+                          np.array([0.0, 0.3], np.float32))
+    assert np.allclose(kB[0], [0.731059, 0.568941], rtol=0, atol=2e-6)
+    assert O.select_topk(kB, 1).tolist() == [[0]]
+    # the same row B under sigmoid routing does pick expert 1 (the two branches differ here)
+    kS = O.selection_keys(np.array([[1.0, 0.0]], np.float32), O.SIGMOID,
+                          np.array([0.0, 0.3], np.float32))
+    assert np.allclose(kS[0], [0.731059, 0.8], rtol=0, atol=2e-6)
+    assert O.select_topk(kS, 1).tolist() == [[1]]
+
+
 @pytest.mark.parametrize("score_fn", SCORES)
 def test_zero_selection_bias_selects_as_the_logits(score_fn):
     rng = np.random.default_rng(7)
@@ -230,6 +263,7 @@ def _variant_pins_pass():
             test_aux_loss_gradient_finite_differences(s)
         test_aux_loss_softmax_gradient_rows_sum_to_zero()
         test_selection_bias_forces_its_experts_and_never_moves_the_gates()
+        test_softmax_selection_keys_by_hand()
         test_expert_bias_update_by_hand()
     except AssertionError:
         return False
@@ -253,6 +287,14 @@ MUTANTS = {
         "score_probs", lambda l, s, _f=O.score_probs: O.sigmoid(l) if s == O.SIGMOID else _f(l, s)),
     "selection_ignores_bias": (
         "selection_keys", lambda l, s, b, _f=O.selection_keys: _f(l, s, np.zeros_like(b))),
+    # softmax routing that adds the bias to the raw logits, or to the sigmoid, instead of to the
+    # softmax over all experts
+    "softmax_keys_are_logit_plus_bias": (
+        "selection_keys", lambda l, s, b, _f=O.selection_keys: (
+            np.asarray(l, np.float32) + np.asarray(b, np.float32)[None, :]).astype(np.float32)
+        if s == O.SOFTMAX else _f(l, s, b)),
+    "softmax_keys_are_sigmoid_plus_bias": (
+        "selection_keys", lambda l, s, b, _f=O.selection_keys: _f(l, O.SIGMOID, b)),
     "bias_update_reversed": (
         "expert_bias_update", lambda b, c, T, k, r, _f=O.expert_bias_update: _f(b, c, T, k, -r)),
 }
