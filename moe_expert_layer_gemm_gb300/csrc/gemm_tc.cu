@@ -17,8 +17,8 @@
 //   warps 2..  epilogue (4 or 8 warps): TMEM -> registers (tcgen05.ld) -> fused epilogue ->
 //              a swizzled shared-memory slab per warp (32 rows x 128 bytes) -> TMA bulk-tensor
 //              store, overlapped with the next tile's MMAs through the second accumulator
-// Tiles are BM=128 rows x BN columns x BK=64; a CTA (or a 2-CTA cluster, for the weight
-// gradients) walks tiles unit, unit + units, ...
+// Tiles are BM=128 rows x BN columns x BK=64; a CTA walks tiles blockIdx.x, blockIdx.x +
+// gridDim.x, ... or, for the weight gradients, claims them at run time.
 #include <cuda.h>
 #include <string.h>
 
@@ -51,9 +51,6 @@ template <int SCHED, int EPI> struct OutPath {
 #define MOE_EPI8_OTHER 0
 #endif
 
-#ifndef MOE_MC_WGRAD
-#define MOE_MC_WGRAD 1
-#endif
 #ifndef MOE_DYN_WGRAD
 #define MOE_DYN_WGRAD 1
 #endif
@@ -66,24 +63,6 @@ template <int SCHED, int EPI> struct OutPath {
 // tiles start first and the short ones fill in behind them (longest-processing-time-first).
 template <int SCHED, int EPI> struct DynMode {
   static constexpr bool on = SCHED == RAGGED_K && EPI == EPI_F32 && MOE_DYN_WGRAD != 0;
-};
-
-// Clusters of two CTAs on vertically adjacent 128-row tiles of the same output block: both
-// need the same B k-block, so each loads half of it and multicasts it into both CTAs' shared
-// memory (this GPU's own memory), cutting each CTA's operand reads from L2 by a third.  Each
-// CTA keeps its own MMAs, TMEM and epilogue.  Row-ragged products walk 256-row tiles inside one
-// expert; the lower CTA of an expert's last tile may have no rows: it still delivers its half
-// of B but skips its A loads and MMAs.  Weight gradients use it only with the static walk.
-// Row-ragged products keep it as a build option: measured slower on GB300 (fc1 + SwiGLU
-// 1.49 -> 1.57 ms, fc2 dgrad 0.98 -> 1.07 ms on the 128-expert layer): the pairs run in
-// lockstep and the extra 256-row tails cost more than the L2 reads saved.
-#ifndef MOE_MC_ROWS
-#define MOE_MC_ROWS 0
-#endif
-template <int SCHED, int EPI> struct McMode {
-  static constexpr bool on =
-      (SCHED == RAGGED_K && EPI == EPI_F32 && MOE_MC_WGRAD != 0 && !DynMode<SCHED, EPI>::on) ||
-      (SCHED == RAGGED_M && EPI != EPI_F32 && MOE_MC_ROWS != 0);
 };
 
 // L2 priorities of the weight gradients: their fp32 blocks are written once and never read
@@ -333,20 +312,18 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
   constexpr int EPI_WARPS = EpiWidth<BN, SCHED, EPI, F8>::warps;
   constexpr int SLABS = EpiOf<BN, SCHED, EPI, F8, MX>::slabs;
   using C = typename CfgOf<BN, SCHED, EPI, F8, MX>::type;
-  constexpr bool MC = McMode<SCHED, EPI>::on;
   constexpr bool DYN = DynMode<SCHED, EPI>::on;
-  static_assert(!MC || BN % 128 == 0, "cluster pairs split B in 128-row halves");
   // gathered operands: A of a row-ragged product (K-major) or B of a weight gradient (MN-major)
-  static_assert(!GATHER || (!MC && ((SCHED == RAGGED_M && !A_MN) || (SCHED == RAGGED_K && B_MN))),
+  static_assert(!GATHER || (SCHED == RAGGED_M && !A_MN) || (SCHED == RAGGED_K && B_MN),
                 "unsupported gathered operand");
-  constexpr int TM = MC ? 2 * BM : BM;   // rows of one walker tile (a CTA, or a cluster pair)
+  constexpr int TM = BM;   // rows of one walker tile
   // K elements per stage: 128-byte rows hold 64 bf16 or 128 E4M3 values
   constexpr int BKE = F8 ? 2 * BK : BK;
   using S = Sched<BN, SCHED, EPI, TM, BKE>;
   // MN-major operand tiles are chunks of 128-byte rows along K: 64 bf16 or 128 E4M3 of M/N each
   constexpr int MNW = F8 ? 128 : 64;
   constexpr int MN_CHUNK = BKE * 128;   // bytes of one such chunk in a stage
-  static_assert(!F8 || (!GATHER && !MC), "FP8 operands: no gathered or cluster-shared loads");
+  static_assert(!F8 || !GATHER, "FP8 operands: no gathered loads");
   // MXFP8: K-major E4M3 operands of a row-ragged product; one stage is one 128-element K chunk
   static_assert(!MX || (F8 && SCHED == RAGGED_M && !A_MN && (!B_MN || BN % 128 == 0) && BN <= 256 &&
                         C::ACC_STRIDE == MxCfg<BN>::ACC_STRIDE &&
@@ -377,11 +354,9 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
   const int* s_ord = DYN ? s_pre : nullptr;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Tile walker: one per CTA, or one per CTA pair of a cluster (rank 0 takes the upper 128 rows
-  // of the pair's 256-row tile, rank 1 the lower).
-  const uint32_t rank = MC ? ptx::cluster_ctarank() : 0u;
-  const int unit = MC ? static_cast<int>(ptx::cluster_id_x()) : static_cast<int>(blockIdx.x);
-  const int units = MC ? static_cast<int>(ptx::cluster_count_x()) : static_cast<int>(gridDim.x);
+  // Tile walker: one per CTA (static walk), or tiles claimed at run time (DYN).
+  const int unit = static_cast<int>(blockIdx.x);
+  const int units = static_cast<int>(gridDim.x);
 
   // 128-byte swizzled tiles need 1024-byte aligned shared memory.
   if ((ptx::smem_u32(smem) & 1023u) != 0) {
@@ -391,7 +366,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       ptx::mbar_init(&full[i], 1);
-      ptx::mbar_init(&empty[i], MC ? 2 : 1);   // clusters: both CTAs' MMAs release a stage
+      ptx::mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&tfull[i], 1);
@@ -463,10 +438,8 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
   __syncthreads();
 
   const int total = S::total(p, s_pre);
-  // nothing for this CTA (the same decision in both CTAs of a pair)
+  // nothing for this CTA
   if (DYN ? total == 0 : unit >= total) return;
-  // Clusters: every barrier of both CTAs is initialised before either writes into the other.
-  if (MC) ptx::cluster_sync();
 
   if (warp == 1) {
     ptx::tmem_alloc(tmem_holder, C::TMEM_COLS);
@@ -601,13 +574,12 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
       int armed[STAGES];
       for (int i = 0; i < STAGES; ++i) armed[i] = -1;
       bool ok = true;
-      // Loads of k-block kb of tile ti into `stage` (B halves multicast within a cluster).
+      // Loads of k-block kb of tile ti into `stage`.
       auto issue = [&](const TileInfo& ti, int kb, int stg) {
         uint8_t* a_dst = sA + stg * A_STAGE;
         uint8_t* b_dst = sB + stg * C::B_STAGE;
         const int kk = ti.k0 + kb * BKE;
-        const int m_cta = ti.m0 + static_cast<int>(rank) * BM;
-        const bool live = !(MC && SCHED == RAGGED_M) || m_cta < ti.m_end;
+        const int m_cta = ti.m0;
         auto box = [&](void* dst, const CUtensorMap* m, int c0, int c1) {
           if (SCHED == RAGGED_K && MOE_WGRAD_LOAD_HINT)
             ptx::tma_load_2d_hint(dst, m, &full[stg], c0, c1, ptx::policy_evict_last());
@@ -615,22 +587,14 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
             ptx::tma_load_2d(dst, m, &full[stg], c0, c1);
         };
         if (!A_MN) {
-          if (live) box(a_dst, &tmA, kk, m_cta);
+          box(a_dst, &tmA, kk, m_cta);
         } else {
 #pragma unroll
           for (int c = 0; c < BM / MNW; ++c) box(a_dst + c * MN_CHUNK, &tmA, m_cta + MNW * c, kk);
         }
         if (!B_MN) {
           const int brow = static_cast<int>(ti.g * p.b_group_rows) + ti.n0;
-          if (MC) {
-            // this CTA's 128 B rows (SwiGLU: rank 0 the gate block, rank 1 the up block),
-            // delivered to both CTAs of the pair
-            const int row = EPI == EPI_SWIGLU_FWD
-                                ? brow + (rank ? static_cast<int>(p.b_up_rows) : 0)
-                                : brow + static_cast<int>(rank) * (BN / 2);
-            ptx::tma_load_2d_multicast(b_dst + rank * (BN / 2) * 128, &tmB, &full[stg], kk, row,
-                                       0x3);
-          } else if (EPI == EPI_SWIGLU_FWD) {
+          if (EPI == EPI_SWIGLU_FWD) {
             box(b_dst, &tmB, kk, brow);
             box(b_dst + (BN / 2) * 128, &tmB, kk, brow + static_cast<int>(p.b_up_rows));
           } else {
@@ -638,19 +602,8 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
           }
         } else {
           const int krow = (SCHED == RAGGED_M) ? static_cast<int>(ti.g * p.b_group_rows) + kk : kk;
-          if (MC) {
-            // this CTA's half of the B boxes, delivered to both CTAs of the pair
-            constexpr int HALF = BN / 128;
 #pragma unroll
-            for (int i = 0; i < HALF; ++i) {
-              const int c = static_cast<int>(rank) * HALF + i;
-              ptx::tma_load_2d_multicast(b_dst + c * (BK * 128), &tmB, &full[stg], ti.n0 + 64 * c,
-                                         krow, 0x3);
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < BN / MNW; ++c) box(b_dst + c * MN_CHUNK, &tmB, ti.n0 + MNW * c, krow);
-          }
+          for (int c = 0; c < BN / MNW; ++c) box(b_dst + c * MN_CHUNK, &tmB, ti.n0 + MNW * c, krow);
         }
         if (MX) {
           // this K chunk's block scales: the A row tile's chunk, then the B tile's chunks
@@ -686,13 +639,9 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
           if (tile >= total) break;
         }
         const TileInfo ti = S::decode(p, s_off, s_pre, s_ord, tile);
-        // bytes landing in this CTA per stage: its A block (unless it has no rows) and all of B
-        const bool a_live = !(MC && SCHED == RAGGED_M) ||
-                            ti.m0 + static_cast<int>(rank) * BM < ti.m_end;
-        const uint32_t tx = a_live ? STAGE_TX : STAGE_TX - A_STAGE;
         for (int kb = 0; kb < ti.kblocks; ++kb) {
           if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(&full[stage], tx);
+          ptx::mbar_arrive_expect_tx(&full[stage], STAGE_TX);
           armed[stage] = static_cast<int>(phase);
           issue(ti, kb, stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -738,9 +687,6 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
       if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::ACC_STRIDE);
-      // a cluster CTA without rows in this tile consumes the stages but issues no MMAs
-      const bool a_live = !(MC && SCHED == RAGGED_M) ||
-                          ti.m0 + static_cast<int>(rank) * BM < ti.m_end;
       for (int kb = 0; kb < ti.kblocks; ++kb) {
         if (!ptx::mbar_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
         uint8_t* a_src = sA + stage * A_STAGE;
@@ -777,7 +723,6 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
           }
 #pragma unroll
           for (int k16 = 0; k16 < BK / 16; ++k16) {
-            if (!a_live) break;
             // one instruction takes 32 bytes of K: 16 bf16 or 32 E4M3 -- along a K-major row, or
             // that many 128-byte rows of an MN-major chunk
             constexpr uint32_t MN_KSTEP = (F8 ? 32 : 16) * 128;
@@ -791,9 +736,8 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
             else if (F8) ptx::umma_f8(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
             else ptx::umma_bf16(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
           }
-          // frees the smem stage (in both CTAs of a cluster) when these MMAs finish
-          if (MC) ptx::umma_commit_multicast(&empty[stage], 0x3);
-          else ptx::umma_commit(&empty[stage]);
+          // frees the smem stage when these MMAs finish
+          ptx::umma_commit(&empty[stage]);
         }
         __syncwarp();
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -870,7 +814,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
         if (tile >= total) break;
       }
       const TileInfo ti = S::decode(p, s_off, s_pre, s_ord, tile);
-      const int m_cta = ti.m0 + static_cast<int>(rank) * BM;   // this CTA's rows of the tile
+      const int m_cta = ti.m0;                      // this CTA's rows of the tile
       const int row0 = m_cta + q * 32;              // first row of this warp's slab
       const int rows_here = min(32, ti.m_end - row0);
       const int row = m_cta + r;
@@ -1385,9 +1329,6 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
 
   ptx::tc_fence_before();
   __syncthreads();
-  // Clusters: neither CTA leaves while the other may still write into its shared memory or
-  // arrive on its barriers.
-  if (MC) ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
@@ -1717,13 +1658,18 @@ __global__ void __launch_bounds__(pairk::THREADS, 1)
               const uint64_t bd = ptx::smem_desc_sw128(b_addr + k16 * 2048, BK * 128, 1024);
               ptx::umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
             }
-            ptx::umma_commit_pair(&empty[stage], 0x3);   // frees the stage in both CTAs
+            // frees the stage in both CTAs
+            ptx::umma_commit_pair(ptx::mapa(ptx::smem_u32(&empty[stage]), 0));
+            ptx::umma_commit_pair(ptx::mapa(ptx::smem_u32(&empty[stage]), 1));
           }
           __syncwarp();
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        if (lane == 0) ptx::umma_commit_pair(&tfull[acc], 0x3);   // both CTAs' epilogues
+        if (lane == 0) {   // both CTAs' epilogues
+          ptx::umma_commit_pair(ptx::mapa(ptx::smem_u32(&tfull[acc]), 0));
+          ptx::umma_commit_pair(ptx::mapa(ptx::smem_u32(&tfull[acc]), 1));
+        }
         __syncwarp();
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
@@ -1943,7 +1889,7 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   MOE_TRY(map_operand(&mb, g.B,
                       (GATHER && SCHED == RAGGED_K) ? 1
                       : B_MN ? KROWS
-                             : ((EPI == EPI_SWIGLU_FWD || McMode<SCHED, EPI>::on) ? BN / 2 : BN),
+                             : (EPI == EPI_SWIGLU_FWD ? BN / 2 : BN),
                       F8));
   const int64_t rows = g.M;   // RAGGED_M: rows of the output (capacity)
   if (EPI == EPI_STORE) {
@@ -2023,9 +1969,6 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
       return MOE_ERR_CUDA;
     }
   }
-  if (McMode<SCHED, EPI>::on)
-    return launch_clusters(name, kern, dim3(num_sms() & ~1), dim3(C::THREADS), C::SMEM, 2, st, ma,
-                           mb, mo[0], mo[1], mo[2], a);
   return launch(name, kern, dim3(num_sms()), dim3(C::THREADS), C::SMEM, st, ma, mb, mo[0], mo[1],
                 mo[2], a);
 }

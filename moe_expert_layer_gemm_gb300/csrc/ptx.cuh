@@ -251,17 +251,6 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// The same box written to the same shared-memory offset of every CTA in cta_mask (this
-// GPU's own memory only); each destination CTA's barrier at `bar`'s offset gets the bytes.
-__device__ __forceinline__ void tma_load_2d_multicast(void* smem_dst, const void* desc, uint64_t* bar,
-                                                      int32_t c0, int32_t c1, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%4, %5}], [%2], %3;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(desc)), "r"(smem_u32(bar)), "h"(cta_mask), "r"(c0), "r"(c1)
-      : "memory");
-}
-
 // ------------------------------------------------------------------ tcgen05
 // Shared-memory matrix descriptor (128-byte swizzle, sm_100 family layout version 1).
 //   start address, leading-dimension byte offset (LBO), stride-dimension byte offset (SBO),
@@ -413,13 +402,13 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, 
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// Arrive on the barrier at `bar`'s offset in every CTA of cta_mask once the pair's MMAs issued
-// so far by this thread are done.
-__device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+// Arrive on the barrier at cluster address `bar_cluster_addr` (this CTA's or the other CTA's
+// of the pair, from mapa) once the pair's MMAs issued so far by this thread are done.  A pair
+// signals both of its CTAs with two of these, one per barrier.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar_cluster_addr) {
   asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          bar_cluster_addr)
       : "memory");
 }
 
@@ -428,14 +417,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-// As umma_commit, arriving on the barrier at the same offset in every CTA of cta_mask.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
       : "memory");
 }
 // 32 lanes x 32 consecutive fp32 columns: thread i of the warp gets its lane's 32 values.
