@@ -197,8 +197,75 @@ def replica_throughput(tokens_per_rank_step, steps, world, ms_max):
 
 # ----------------------------------------------------------------------------- clocks
 
+class NvmlClockSampler:
+    """SM clock, its maximum, power and the clock-event (throttle) reasons of one GPU, read through
+    NVML (read-only queries) every `period` seconds on a host thread during the timed region, so
+    that even a short region gets several samples.  The GPU is found by its PCI bus id."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, device, period=0.01):
+        import ctypes
+        import threading
+        import torch
+        self.ok = False
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return
+        nv = self.nv
+        if nv.nvmlInit_v2() != 0:
+            return
+        pr = torch.cuda.get_device_properties(device)
+        bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0".encode()
+        self.h = ctypes.c_void_p()
+        if nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(self.h)) != 0:
+            return
+        self.reason_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        self.samples = []
+        self.period = period
+        self.stop_ev = threading.Event()
+        self.ok = True
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        import ctypes
+        sm, mx, pw = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(sm)) != 0:   # NVML_CLOCK_SM
+            return None
+        self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+        self.nv.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(pw))
+        self.reason_fn(self.h, ctypes.byref(rs))
+        return sm.value, mx.value, pw.value / 1000.0, rs.value
+
+    def _run(self):
+        while not self.stop_ev.is_set():
+            r = self._read()
+            if r is not None:
+                self.samples.append(r)
+            self.stop_ev.wait(self.period)
+
+    def stop(self):
+        if not self.ok:
+            return None
+        self.stop_ev.set()
+        self.thread.join(timeout=5)
+        self.nv.nvmlShutdown()
+        if not self.samples:
+            return None
+        reasons = sorted({n for *_, rs in self.samples for b, n in self.REASONS.items() if rs & b})
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                "sm_max_mhz": max(s[1] for s in self.samples), "reasons": reasons,
+                "samples": len(self.samples), "power_w_max": round(max(s[2] for s in self.samples), 1),
+                "source": f"NVML every {int(self.period * 1e3)} ms"}
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region (used
+    when NVML cannot be loaded)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -240,7 +307,12 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi every 200 ms"}
+
+
+def start_clock_sampler(device, gpu_index):
+    s = NvmlClockSampler(device)
+    return s if s.ok else ClockSampler(gpu_index)
 
 
 # ----------------------------------------------------------------------------- CPU oracle leg
@@ -320,6 +392,9 @@ def run_gpu(args, lc):
     ws_f = moe.workspace(cfg, moe.WS_LAYER_FWD, dev)
     ws_b = moe.workspace(cfg, moe.WS_LAYER_BWD_FP8 if args.fp8 else moe.WS_LAYER_BWD, dev)
     stream = torch.cuda.current_stream()
+    # the caller-owned second stream of the layer calls (shared expert and router backward beside
+    # the routed experts)
+    side = moe.SideStream(dev)
     mxq = None
     if args.mxfp8:
         # MXFP8 routed experts (weights quantised once, outside the timed steps, both copies).
@@ -336,30 +411,31 @@ def run_gpu(args, lc):
         fp8q = moe.alloc_fp8_experts(cfg, inp["W1"], inp["W2"], dev, Ws1=inp["Ws1"], Ws2=inp["Ws2"])
         saved["x_perm"] = None
 
-    def step(x, dy, yout, dxout):
+    def step(x, dy, yout, dxout, side=side):
         if mxq is not None:
             moe.moe_layer_fwd_mxfp8(cfg, x, inp["W_r"], inp["b_r"], mxq, inp["Ws1"], inp["Ws2"],
-                                    inp["w_sg"], yout, saved, ws_f)
+                                    inp["w_sg"], yout, saved, ws_f, side=side)
             if lc.backward:
                 moe.moe_layer_bwd_mxfp8(cfg, dy, x, inp["W_r"], mxd, inp["Ws1"], inp["Ws2"],
                                         inp["w_sg"], saved, dxout, grads["dW_r"], grads["dW1"],
                                         grads["dW2"], grads["dWs1"], grads["dWs2"],
-                                        grads["dw_sg"], ws_b)
+                                        grads["dw_sg"], ws_b, side=side)
             return
         if fp8q is not None:
             moe.moe_layer_fwd_fp8(cfg, x, inp["W_r"], inp["b_r"], fp8q, inp["Ws1"], inp["Ws2"],
-                                  inp["w_sg"], yout, saved, ws_f)
+                                  inp["w_sg"], yout, saved, ws_f, side=side)
             if lc.backward:
                 moe.moe_layer_bwd_fp8(cfg, dy, x, inp["W_r"], fp8q, inp["Ws1"], inp["Ws2"],
                                       inp["w_sg"], saved, dxout, grads["dW_r"], grads["dW1"],
-                                      grads["dW2"], grads["dWs1"], grads["dWs2"], grads["dw_sg"], ws_b)
+                                      grads["dW2"], grads["dWs1"], grads["dWs2"], grads["dw_sg"], ws_b,
+                                      side=side)
             return
         moe.moe_layer_fwd(cfg, x, inp["W_r"], inp["b_r"], inp["W1"], inp["W2"], inp["Ws1"],
-                          inp["Ws2"], inp["w_sg"], yout, saved, ws_f)
+                          inp["Ws2"], inp["w_sg"], yout, saved, ws_f, side=side)
         if lc.backward:
             moe.moe_layer_bwd(cfg, dy, x, inp["W_r"], inp["W1"], inp["W2"], inp["Ws1"], inp["Ws2"],
                               inp["w_sg"], saved, dxout, grads["dW_r"], grads["dW1"], grads["dW2"],
-                              grads["dWs1"], grads["dWs2"], grads["dw_sg"], ws_b)
+                              grads["dWs1"], grads["dWs2"], grads["dw_sg"], ws_b, side=side)
 
     def barrier():
         if world > 1:
@@ -404,7 +480,7 @@ def run_gpu(args, lc):
             gpu_index = int(vis.split(",")[local])
         except (ValueError, IndexError):
             pass
-    clocks = ClockSampler(gpu_index)
+    clocks = start_clock_sampler(dev, gpu_index)
     launches0 = moe.launch_count()
     barrier()
     torch.cuda.synchronize()
@@ -423,10 +499,9 @@ def run_gpu(args, lc):
     moe.check_device_error()
 
     # ---- per-kernel attribution: a second timed region with every launch bracketed by CUDA
-    # events on its stream, the shared expert's side stream off (concurrent kernels would share
-    # the SMs and their event times would overlap); identical results, serial order.
+    # events on its stream, without the side stream (concurrent kernels would share the SMs and
+    # their event times would overlap); identical results, serial order.
     n_trace = max(3, min(args.steps, 20))
-    prev_overlap = moe.set_stream_overlap(False)
     moe.trace_read()   # drop anything recorded before
     moe.trace_enable(True)
     torch.cuda.synchronize()
@@ -434,12 +509,11 @@ def run_gpu(args, lc):
     tr1 = torch.cuda.Event(enable_timing=True)
     tr0.record(stream)
     for _ in range(n_trace):
-        step(inp["x"], inp["dy"], y, grads["dx"])
+        step(inp["x"], inp["dy"], y, grads["dx"], side=None)
     tr1.record(stream)
     torch.cuda.synchronize()
     moe.trace_enable(False)
     trace = moe.trace_read()
-    moe.set_stream_overlap(prev_overlap)
     trace_ms_step = tr0.elapsed_time(tr1) / n_trace
     moe.check_device_error()
     ms_max = max_over_ranks(ms_total, dev)
@@ -541,12 +615,16 @@ def run_gpu(args, lc):
     peaks, peak_src = load_peaks()
     work = kernel_work(lc, trace, n_trace)
     flops_of = dict(work)      # FLOPs of the GEMMs, whatever bound their roofline takes
-    bf16_peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    # Peaks: the burst figure (a short timed region: the kernels are timed inside a
+    # sub-second region, as a kernel timed alone) and the sustained one beside it.
+    bf16_burst = peaks.get("bf16_tflops", peaks.get("bf16_tflops_sustained"))
+    bf16_sus = peaks.get("bf16_tflops_sustained", bf16_burst)
 
-    def tensor_peak(name):
+    def tensor_peak(name, sustained=False):
         # E4M3 products (tensorwise or block-scaled): twice the measured bf16 rate (the nominal
         # dense fp8 : bf16 ratio)
-        return 2.0 * bf16_peak if name.endswith(("_fp8", "_mxfp8")) else bf16_peak
+        p = bf16_sus if sustained else bf16_burst
+        return 2.0 * p if name.endswith(("_fp8", "_mxfp8")) else p
 
     gbytes = gemm_bytes(lc) if lc.dtype == "bf16" else {}
     kern = {}
@@ -559,13 +637,15 @@ def run_gpu(args, lc):
         avg_ms = ms / max(1, n_launch)
         if kind == "tensor":
             ach = amount / (avg_ms / 1e3) / 1e12
-            unit, peak = "TFLOP/s", tensor_peak(name)
+            unit, peak, peak_s = "TFLOP/s", tensor_peak(name), tensor_peak(name, True)
         else:
             ach = amount / (avg_ms / 1e3) / 1e9
             unit, peak = "GB/s", peaks["hbm_gbs"]
+            peak_s = peak
         kern[name] = {"launches": n_launch, "ms_per_launch": round(avg_ms, 4),
                       "share": None, "achieved": round(ach, 1), "unit": unit,
-                      "frac": round(ach / peak, 4) if amount else None}
+                      "frac": round(ach / peak, 4) if amount else None,
+                      "frac_sustained": round(ach / peak_s, 4) if amount else None}
     tot = sum(ms for _, ms in trace.values()) or 1.0
     for name, (n_launch, ms) in trace.items():
         kern[name]["share"] = round(ms / tot, 4)
@@ -579,9 +659,11 @@ def run_gpu(args, lc):
         roof = {"bound": kind, "kernel": dom, "achieved": kd["achieved"],
                 "peak": tensor_peak(dom) if kind == "tensor" else peaks["hbm_gbs"],
                 "unit": kd["unit"], "frac": kd["frac"], "traffic": traffic,
-                "peak_source": f"{peak_src} (" + ("2 x bf16_tflops_sustained, nominal fp8:bf16 ratio"
-                                                  if fp8_dom else "bf16_tflops_sustained"
-                                                  if kind == "tensor" else "hbm_gbs") + ")"}
+                "peak_source": f"{peak_src} (" + ("2 x bf16_tflops (burst), nominal fp8:bf16 ratio"
+                                                  if fp8_dom else "bf16_tflops (burst)"
+                                                  if kind == "tensor" else "hbm_gbs") + ")",
+                "peak_sustained": tensor_peak(dom, True) if kind == "tensor" else peaks["hbm_gbs"],
+                "frac_sustained": kd["frac_sustained"]}
     gemm_ms = sum(ms for n, (_, ms) in trace.items() if n.startswith("gemm_"))
     gemm_flops = sum(flops_of[n][1] * trace[n][0] for n in trace
                      if n.startswith("gemm_") and n in flops_of)
@@ -617,7 +699,8 @@ def run_gpu(args, lc):
                    "global_batch": lc.T * world, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (expert weights alone exceed 129 MB), no flush"},
         "tflops": round(flops_step / (ms_step / 1e3) / 1e12, 1),
-        "pct_bf16_peak": round(flops_step / (ms_step / 1e3) / 1e12 / peaks["bf16_tflops_sustained"], 4),
+        "pct_bf16_peak": round(flops_step / (ms_step / 1e3) / 1e12 / bf16_burst, 4),
+        "pct_bf16_peak_sustained": round(flops_step / (ms_step / 1e3) / 1e12 / bf16_sus, 4),
         "grouped_gemm_tflops": round(gemm_tflops, 1) if gemm_tflops else None,
         "roofline": roof,
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -815,14 +898,15 @@ def mxfp8_layer_fwd(args, lc, cfg, inp, dev):
     mx = moe.alloc_mxfp8_experts(cfg, inp["W1"], inp["W2"], dev)
     y = torch.empty_like(inp["x"])
     ws_f = moe.workspace(cfg, moe.WS_LAYER_FWD, dev)
+    side = moe.SideStream(dev)
 
     def f16():
         moe.moe_layer_fwd(cfg, inp["x"], inp["W_r"], inp["b_r"], inp["W1"], inp["W2"], inp["Ws1"],
-                          inp["Ws2"], inp["w_sg"], y, s16, ws_f)
+                          inp["Ws2"], inp["w_sg"], y, s16, ws_f, side=side)
 
     def fmx():
         moe.moe_layer_fwd_mxfp8(cfg, inp["x"], inp["W_r"], inp["b_r"], mx, inp["Ws1"], inp["Ws2"],
-                                inp["w_sg"], y, smx, ws_f)
+                                inp["w_sg"], y, smx, ws_f, side=side)
 
     n = max(5, min(args.steps, 50))
     ms16, graphed = graph_timed(args, f16, dev, n)
@@ -854,14 +938,15 @@ def fp8_layer(args, lc, cfg, inp, dev, ms_bf16):
              dw_sg=torch.empty(lc.d, dtype=f32, device=dev) if lc.shared_gate else None)
     ws_f = moe.workspace(cfg, moe.WS_LAYER_FWD, dev)
     ws_b = moe.workspace(cfg, moe.WS_LAYER_BWD_FP8, dev)
+    side = moe.SideStream(dev)
 
     def step():
         moe.moe_layer_fwd_fp8(cfg, inp["x"], inp["W_r"], inp["b_r"], q, inp["Ws1"], inp["Ws2"],
-                              inp["w_sg"], y, saved, ws_f)
+                              inp["w_sg"], y, saved, ws_f, side=side)
         if lc.backward:
             moe.moe_layer_bwd_fp8(cfg, inp["dy"], inp["x"], inp["W_r"], q, inp["Ws1"], inp["Ws2"],
                                   inp["w_sg"], saved, g["dx"], g["dW_r"], g["dW1"], g["dW2"],
-                                  g["dWs1"], g["dWs2"], g["dw_sg"], ws_b)
+                                  g["dWs1"], g["dWs2"], g["dw_sg"], ws_b, side=side)
 
     n = max(5, min(args.steps, 50))
     ms, graphed = graph_timed(args, step, dev, n)
@@ -910,13 +995,14 @@ def run_reference(args, lc):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=250)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="deepseek", choices=list(moe_inputs.CONFIGS))
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-tokens", type=int, default=512)
-    ap.add_argument("--ref-tokens", type=int, default=64)
+    # the oracle's token sample: the same seeded tokens in cpu_baseline and in --impl reference
+    ap.add_argument("--cpu-tokens", type=int, default=256)
+    ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 expert comparison")
     ap.add_argument("--no-graph", action="store_true", help="time eager calls, not a CUDA graph")

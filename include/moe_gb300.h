@@ -24,9 +24,11 @@
  *     caller's workspace, sized by moe_workspace_bytes().
  *   - Every pointer must be 16-byte aligned (MOE_ERR_ALIGNMENT otherwise).
  *   - All work is enqueued on `stream` (a cudaStream_t passed as void*, NULL = legacy default
- *     stream) and is asynchronous with respect to the host.  Calls keep no state between
- *     them; two calls may run concurrently on different streams if their buffers and
- *     workspaces are distinct.
+ *     stream), and for the layer calls also on the caller's optional side stream
+ *     (moe_side_stream), and is asynchronous with respect to the host.  The library owns no
+ *     stream, event or global switch, and calls keep no state between them; two calls may run
+ *     concurrently on different streams if their buffers, workspaces and side streams are
+ *     distinct.  (moe_route_topk_noalloc is the one exception: its scratch is shared; see it.)
  *   - Row-major dense layouts; T tokens, d = d_model, E experts, k experts per token,
  *     f = expert ffn width, f_s = shared expert ffn width, N = T*k routed rows.
  *   - Activations and weights are in cfg->dtype (bf16 or fp32).  Router logits, gates and
@@ -137,8 +139,9 @@ int moe_route_topk(const moe_cfg* cfg, const void* x, const void* W_r, const flo
  *   Scratch: a fixed 512 KB array inside the library, held on every GPU that loads it until the
  *   process exits.  E * ceil(T/256) must not exceed 65536 (e.g. T = 65536 tokens with E = 256,
  *   or T = 131072 with E = 128); larger calls return MOE_ERR_UNSUPPORTED.
- *   The first call on a device looks up the array's device address (cudaGetSymbolAddress):
- *   make that first call before any stream capture.
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress),
+ *   and so does the first call after the device's context was replaced (cudaDeviceReset): make
+ *   those calls before any stream capture.
  *   All calls share the one array and every call overwrites what it reads, so nothing needs
  *   clearing; but calls whose GPU work overlaps (different streams or host threads without
  *   ordering between them) race on it and give wrong results: order them.
@@ -433,16 +436,39 @@ int moe_router_aux_loss(const moe_cfg* cfg, const float* logits, const int32_t* 
 int moe_expert_bias_update(const moe_cfg* cfg, const int32_t* counts, float* e_bias, float rate,
                            void* stream);
 
+/* The layer calls' second stream, owned by the caller ("Megatron-Bridge 深度剖析", §Shared
+ * Expert Overlap: the shared expert's work runs beside the routed experts' instead of after
+ * them).  Given one, moe_layer_fwd* run the shared expert (and its gate) on `stream` while
+ * routing, permute and the routed experts run on the call's stream, and moe_layer_bwd* run the
+ * shared expert's backward and the router's backward on it while the routed experts' backward
+ * runs; the call's stream then waits for it before the combine (forward) or the dx gather
+ * (backward).
+ *   stream: a cudaStream_t (as void*) other than the call's stream;
+ *   fork, join: two distinct cudaEvent_t (as void*; cudaEventDisableTiming suffices), which the
+ *     call records and waits on.
+ * All three are created and destroyed by the caller; the library keeps no reference once the
+ * call returns, and the side stream's work is ordered before the call's stream continues.  One
+ * moe_side_stream must not serve two calls whose work can overlap (their event records would
+ * interleave): give each concurrent caller its own.  NULL (the pointer): everything runs on the
+ * call's stream in order.  Results are bit-identical either way.  MOE_ERR_INVALID_ARG if a
+ * field is NULL, fork == join, or stream is the call's stream. */
+typedef struct moe_side_stream {
+  void* stream;
+  void* fork;
+  void* join;
+} moe_side_stream;
+
 /* Whole layer forward: route, permute, grouped SwiGLU, shared expert, combine.
  *   x [T,d]; W_r [E,d]; b_r [E] fp32 or NULL (cfg->bias_mode says how it acts);
  *   W1 [E,2f,d]; W2 [E,d,f];
  *   Ws1 [2f_s,d], Ws2 [d,f_s] (NULL without shared expert); w_sg [d] (NULL without gate).
  *   y [T,d].  `saved` receives everything the backward needs, and with cfg->aux_coeff > 0
- *   the load-balancing loss in saved->aux_loss (moe_router_aux_loss). */
+ *   the load-balancing loss in saved->aux_loss (moe_router_aux_loss).  side: see
+ *   moe_side_stream (NULL: one stream). */
 int moe_layer_fwd(const moe_cfg* cfg, const void* x, const void* W_r, const float* b_r,
                   const void* W1, const void* W2, const void* Ws1, const void* Ws2,
                   const void* w_sg, void* y, const moe_saved* saved, void* ws, size_t ws_bytes,
-                  void* stream);
+                  void* stream, const moe_side_stream* side);
 
 /* Whole layer backward, for the upstream gradient dy [T,d].  No gradient flows through the
  * expert selection (it is piecewise constant in the logits); b_r gets none (an input).
@@ -451,12 +477,13 @@ int moe_layer_fwd(const moe_cfg* cfg, const void* x, const void* W_r, const floa
  *   w_e = aux_coeff*E*counts[e]/(k*T^2),  G_t = sum_e p[t,e] w_e,
  *   softmax: dl[t,e] += p[t,e] (w_e - G_t);  sigmoid: dl[t,e] += s(1-s)(w_e - G_t)/sum_e s.
  *   Outputs: dx [T,d] (dtype); dW_r [E,d], dW1 [E,2f,d], dW2 [E,d,f], dWs1 [2f_s,d],
- *   dWs2 [d,f_s], dw_sg [d] -- all fp32 (the shared ones NULL when absent). */
+ *   dWs2 [d,f_s], dw_sg [d] -- all fp32 (the shared ones NULL when absent).
+ *   side: see moe_side_stream (NULL: one stream). */
 int moe_layer_bwd(const moe_cfg* cfg, const void* dy, const void* x, const void* W_r,
                   const void* W1, const void* W2, const void* Ws1, const void* Ws2,
                   const void* w_sg, const moe_saved* saved, void* dx, float* dW_r, float* dW1,
                   float* dW2, float* dWs1, float* dWs2, float* dw_sg, void* ws, size_t ws_bytes,
-                  void* stream);
+                  void* stream, const moe_side_stream* side);
 
 /* The experts of a layer in FP8 ("Megatron-Bridge 深度剖析", §FP8 训练: E4M3, tensorwise
  * scaling, FP8 parameters, weight gradients in FP8).  Caller-owned device buffers:
@@ -498,7 +525,7 @@ typedef struct moe_fp8_experts {
 int moe_layer_fwd_mxfp8(const moe_cfg* cfg, const void* x, const void* W_r, const float* b_r,
                         const moe_mxfp8_experts* mx, const void* Ws1, const void* Ws2,
                         const void* w_sg, void* y, const moe_saved* saved, void* ws,
-                        size_t ws_bytes, void* stream);
+                        size_t ws_bytes, void* stream, const moe_side_stream* side);
 
 /* The layer backward after moe_layer_fwd_mxfp8 (given saved.x_perm, act and h): moe_layer_bwd,
  * except that the routed experts' data gradients run on MXFP8 operands
@@ -509,7 +536,7 @@ int moe_layer_bwd_mxfp8(const moe_cfg* cfg, const void* dy, const void* x, const
                         const moe_mxfp8_dgrad* mxd, const void* Ws1, const void* Ws2,
                         const void* w_sg, const moe_saved* saved, void* dx, float* dW_r,
                         float* dW1, float* dW2, float* dWs1, float* dWs2, float* dw_sg, void* ws,
-                        size_t ws_bytes, void* stream);
+                        size_t ws_bytes, void* stream, const moe_side_stream* side);
 
 /* moe_layer_fwd with the routed experts on E4M3 operands: x is permuted and quantised in one
  * pass (moe_permute_quantize_e4m3) and the experts run as moe_grouped_swiglu_fwd_fp8 does, with
@@ -520,7 +547,7 @@ int moe_layer_bwd_mxfp8(const moe_cfg* cfg, const void* dy, const void* x, const
 int moe_layer_fwd_fp8(const moe_cfg* cfg, const void* x, const void* W_r, const float* b_r,
                       const moe_fp8_experts* fp8, const void* Ws1, const void* Ws2,
                       const void* w_sg, void* y, const moe_saved* saved, void* ws, size_t ws_bytes,
-                      void* stream);
+                      void* stream, const moe_side_stream* side);
 
 /* moe_layer_bwd after moe_layer_fwd_fp8: the routed experts' backward runs as
  * moe_grouped_swiglu_bwd_fp8 does (dy_perm and [da | du] quantised, both data gradients and
@@ -531,7 +558,7 @@ int moe_layer_bwd_fp8(const moe_cfg* cfg, const void* dy, const void* x, const v
                       const moe_fp8_experts* fp8, const void* Ws1, const void* Ws2,
                       const void* w_sg, const moe_saved* saved, void* dx, float* dW_r, float* dW1,
                       float* dW2, float* dWs1, float* dWs2, float* dw_sg, void* ws,
-                      size_t ws_bytes, void* stream);
+                      size_t ws_bytes, void* stream, const moe_side_stream* side);
 
 /* Message of the last error on this host thread ("" if none). */
 const char* moe_last_error(void);
@@ -551,13 +578,6 @@ uint64_t moe_launch_count(void);
 int moe_trace_enable(int on);
 /* Fills up to `cap` entries; returns the number of kernel kinds seen (or < 0 on error). */
 int moe_trace_read(char* names, int name_stride, int* launches, double* total_ms, int cap);
-
-/* Side-stream overlap switch for moe_layer_fwd / moe_layer_bwd ("Megatron-Bridge 深度剖析",
- * §Shared Expert Overlap): 1 (default) runs the shared expert (and, in the backward, the router's
- * backward) on a library-owned side stream concurrently with the routed experts; 0 runs
- * everything on the caller's stream in order (useful for per-kernel timing).  Results are
- * identical either way.  Process-wide; returns the previous setting. */
-int moe_set_stream_overlap(int on);
 
 /* Self-test of the failure path of the pipelined kernels: launches one block that waits, through
  * the same bounded mbarrier wait as every GEMM pipeline (here with a 50 ms limit), on a barrier

@@ -55,9 +55,37 @@ class MoeMxfp8Dgrad(ctypes.Structure):
                 ("W1c_q", "W1c_sp", "W2c_q", "W2c_sp", "dy_q", "dy_s", "dH1_q", "dH1_s")]
 
 
+class MoeSideStream(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("stream", "fork", "join")]
+
+
+class SideStream:
+    """A caller-owned second stream for the layer calls (moe_side_stream): a torch CUDA stream and
+    two events, on `device`.  Pass it as `side=` to moe_layer_fwd* / moe_layer_bwd* so that the
+    shared expert (and, in the backward, the router's backward) runs beside the routed experts.
+    One SideStream serves one sequence of calls; concurrent callers each need their own."""
+
+    def __init__(self, device="cuda"):
+        import torch
+        self.stream = torch.cuda.Stream(device=device)
+        self.fork = torch.cuda.Event()
+        self.join = torch.cuda.Event()
+        # torch creates an event's CUDA handle on its first record
+        with torch.cuda.device(self.stream.device):
+            self.fork.record(self.stream)
+            self.join.record(self.stream)
+        self.struct = MoeSideStream(self.stream.cuda_stream, self.fork.cuda_event,
+                                    self.join.cuda_event)
+
+
+def _side(side):
+    return None if side is None else ctypes.byref(side.struct)
+
+
 _VP = ctypes.c_void_p
 _SZ = ctypes.c_size_t
 _CFG = ctypes.POINTER(MoeCfg)
+_SIDE = ctypes.POINTER(MoeSideStream)
 _SIGS = {
     "moe_workspace_bytes": (_SZ, [_CFG, ctypes.c_int]),
     "moe_route_topk": (ctypes.c_int, [_CFG] + [_VP] * 12 + [_SZ, _VP]),
@@ -77,21 +105,22 @@ _SIGS = {
     "moe_permute_quantize_mxfp8": (ctypes.c_int, [_CFG] + [_VP] * 6),
     "moe_grouped_swiglu_fwd_mxfp8": (ctypes.c_int, [_CFG] + [_VP] * 13),
     "moe_layer_fwd_mxfp8": (ctypes.c_int, [_CFG] + [_VP] * 3 + [ctypes.POINTER(MoeMxfp8Experts)]
-                            + [_VP] * 4 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP]),
+                            + [_VP] * 4 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP, _SIDE]),
     "moe_mxfp8_prepare_dgrad_weights": (ctypes.c_int, [_CFG] + [_VP] * 9),
     "moe_grouped_swiglu_dgrad_mxfp8": (ctypes.c_int, [_CFG] + [_VP] * 14),
     "moe_layer_bwd_mxfp8": (ctypes.c_int, [_CFG] + [_VP] * 3 + [ctypes.POINTER(MoeMxfp8Dgrad)]
-                            + [_VP] * 3 + [ctypes.POINTER(MoeSaved)] + [_VP] * 8 + [_SZ, _VP]),
+                            + [_VP] * 3 + [ctypes.POINTER(MoeSaved)] + [_VP] * 8 + [_SZ, _VP, _SIDE]),
     "moe_unpermute_combine": (ctypes.c_int, [_CFG] + [_VP] * 7),
     "moe_unpermute_combine_bwd": (ctypes.c_int, [_CFG] + [_VP] * 11),
-    "moe_layer_fwd": (ctypes.c_int, [_CFG] + [_VP] * 9 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP]),
+    "moe_layer_fwd": (ctypes.c_int, [_CFG] + [_VP] * 9 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP,
+                                                       _SIDE]),
     "moe_selftest_wait_timeout": (ctypes.c_int, [_VP, _VP]),
     "moe_layer_fwd_fp8": (ctypes.c_int, [_CFG] + [_VP] * 3 + [ctypes.POINTER(MoeFp8Experts)]
-                          + [_VP] * 4 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP]),
+                          + [_VP] * 4 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP, _SIDE]),
     "moe_layer_bwd_fp8": (ctypes.c_int, [_CFG] + [_VP] * 3 + [ctypes.POINTER(MoeFp8Experts)]
-                          + [_VP] * 3 + [ctypes.POINTER(MoeSaved)] + [_VP] * 8 + [_SZ, _VP]),
+                          + [_VP] * 3 + [ctypes.POINTER(MoeSaved)] + [_VP] * 8 + [_SZ, _VP, _SIDE]),
     "moe_layer_bwd": (ctypes.c_int, [_CFG] + [_VP] * 8 + [ctypes.POINTER(MoeSaved)] + [_VP] * 8
-                      + [_SZ, _VP]),
+                      + [_SZ, _VP, _SIDE]),
     "moe_router_aux_loss": (ctypes.c_int, [_CFG, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "moe_expert_bias_update": (ctypes.c_int, [_CFG, _VP, _VP, ctypes.c_float, _VP]),
     "moe_last_error": (ctypes.c_char_p, []),
@@ -101,7 +130,6 @@ _SIGS = {
     "moe_trace_read": (ctypes.c_int, [ctypes.c_char_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                       ctypes.POINTER(ctypes.c_double), ctypes.c_int]),
     "moe_version": (ctypes.c_int, []),
-    "moe_set_stream_overlap": (ctypes.c_int, [ctypes.c_int]),
 }
 
 _lib = None
@@ -316,11 +344,11 @@ def mx_struct(m):
     return MoeMxfp8Experts(*[m[n].data_ptr() for n, _ in MoeMxfp8Experts._fields_])
 
 
-def moe_layer_fwd_mxfp8(cfg, x, W_r, b_r, mx, Ws1, Ws2, w_sg, y, saved, ws, stream=None):
+def moe_layer_fwd_mxfp8(cfg, x, W_r, b_r, mx, Ws1, Ws2, w_sg, y, saved, ws, stream=None, side=None):
     st, ms = saved_struct(saved), mx_struct(mx)
     _check(lib().moe_layer_fwd_mxfp8(ctypes.byref(cfg), _p(x), _p(W_r), _p(b_r), ctypes.byref(ms),
                                      _p(Ws1), _p(Ws2), _p(w_sg), _p(y), ctypes.byref(st), _p(ws),
-                                     ws.numel(), _stream(stream)), "moe_layer_fwd_mxfp8")
+                                     ws.numel(), _stream(stream), _side(side)), "moe_layer_fwd_mxfp8")
 
 
 def alloc_mxfp8_dgrad(cfg, W1, W2, device="cuda", stream=None):
@@ -360,12 +388,12 @@ def mxd_struct(m):
 
 
 def moe_layer_bwd_mxfp8(cfg, dy, x, W_r, mxd, Ws1, Ws2, w_sg, saved, dx, dW_r, dW1, dW2, dWs1, dWs2,
-                        dw_sg, ws, stream=None):
+                        dw_sg, ws, stream=None, side=None):
     st, ms = saved_struct(saved), mxd_struct(mxd)
     _check(lib().moe_layer_bwd_mxfp8(ctypes.byref(cfg), _p(dy), _p(x), _p(W_r), ctypes.byref(ms),
                                      _p(Ws1), _p(Ws2), _p(w_sg), ctypes.byref(st), _p(dx), _p(dW_r),
                                      _p(dW1), _p(dW2), _p(dWs1), _p(dWs2), _p(dw_sg), _p(ws),
-                                     ws.numel(), _stream(stream)), "moe_layer_bwd_mxfp8")
+                                     ws.numel(), _stream(stream), _side(side)), "moe_layer_bwd_mxfp8")
 
 
 def moe_unpermute_combine(cfg, y_perm, gate, slot_of_pair, shared_out, shared_coef, y, stream=None):
@@ -430,20 +458,20 @@ def saved_struct(saved):
     return MoeSaved(*[None if saved[n] is None else saved[n].data_ptr() for n in SAVED_FIELDS])
 
 
-def moe_layer_fwd(cfg, x, W_r, b_r, W1, W2, Ws1, Ws2, w_sg, y, saved, ws, stream=None):
+def moe_layer_fwd(cfg, x, W_r, b_r, W1, W2, Ws1, Ws2, w_sg, y, saved, ws, stream=None, side=None):
     st = saved_struct(saved)
     _check(lib().moe_layer_fwd(ctypes.byref(cfg), _p(x), _p(W_r), _p(b_r), _p(W1), _p(W2), _p(Ws1),
                                _p(Ws2), _p(w_sg), _p(y), ctypes.byref(st), _p(ws), ws.numel(),
-                               _stream(stream)), "moe_layer_fwd")
+                               _stream(stream), _side(side)), "moe_layer_fwd")
 
 
 def moe_layer_bwd(cfg, dy, x, W_r, W1, W2, Ws1, Ws2, w_sg, saved, dx, dW_r, dW1, dW2, dWs1, dWs2,
-                  dw_sg, ws, stream=None):
+                  dw_sg, ws, stream=None, side=None):
     st = saved_struct(saved)
     _check(lib().moe_layer_bwd(ctypes.byref(cfg), _p(dy), _p(x), _p(W_r), _p(W1), _p(W2), _p(Ws1),
                                _p(Ws2), _p(w_sg), ctypes.byref(st), _p(dx), _p(dW_r), _p(dW1),
                                _p(dW2), _p(dWs1), _p(dWs2), _p(dw_sg), _p(ws), ws.numel(),
-                               _stream(stream)), "moe_layer_bwd")
+                               _stream(stream), _side(side)), "moe_layer_bwd")
 
 
 def alloc_fp8_experts(cfg, W1, W2, device="cuda", stream=None, Ws1=None, Ws2=None):
@@ -482,30 +510,25 @@ def fp8_struct(q):
                            for n, _ in MoeFp8Experts._fields_])
 
 
-def moe_layer_fwd_fp8(cfg, x, W_r, b_r, fp8, Ws1, Ws2, w_sg, y, saved, ws, stream=None):
+def moe_layer_fwd_fp8(cfg, x, W_r, b_r, fp8, Ws1, Ws2, w_sg, y, saved, ws, stream=None, side=None):
     st, qs = saved_struct(saved), fp8_struct(fp8)
     _check(lib().moe_layer_fwd_fp8(ctypes.byref(cfg), _p(x), _p(W_r), _p(b_r), ctypes.byref(qs),
                                    _p(Ws1), _p(Ws2), _p(w_sg), _p(y), ctypes.byref(st), _p(ws),
-                                   ws.numel(), _stream(stream)), "moe_layer_fwd_fp8")
+                                   ws.numel(), _stream(stream), _side(side)), "moe_layer_fwd_fp8")
 
 
 def moe_layer_bwd_fp8(cfg, dy, x, W_r, fp8, Ws1, Ws2, w_sg, saved, dx, dW_r, dW1, dW2, dWs1, dWs2,
-                      dw_sg, ws, stream=None):
+                      dw_sg, ws, stream=None, side=None):
     st, qs = saved_struct(saved), fp8_struct(fp8)
     _check(lib().moe_layer_bwd_fp8(ctypes.byref(cfg), _p(dy), _p(x), _p(W_r), ctypes.byref(qs),
                                    _p(Ws1), _p(Ws2), _p(w_sg), ctypes.byref(st), _p(dx), _p(dW_r),
                                    _p(dW1), _p(dW2), _p(dWs1), _p(dWs2), _p(dw_sg), _p(ws),
-                                   ws.numel(), _stream(stream)), "moe_layer_bwd_fp8")
+                                   ws.numel(), _stream(stream), _side(side)), "moe_layer_bwd_fp8")
 
 
 def moe_selftest_wait_timeout(observed, stream=None):
     """Run the bounded-wait self-test (see include/moe_gb300.h); observed: int32 device tensor."""
     _check(lib().moe_selftest_wait_timeout(_p(observed), _stream(stream)), "moe_selftest_wait_timeout")
-
-
-def set_stream_overlap(on):
-    """Side-stream overlap of the layer calls on (default) or off; returns the previous setting."""
-    return int(lib().moe_set_stream_overlap(1 if on else 0))
 
 
 def check_device_error(stream=None):

@@ -38,7 +38,6 @@ static int fail(int code, const char* fmt, ...) {
 __device__ int g_device_error;
 
 static std::mutex g_dev_mu;
-static int* g_err_ptr[64];
 static int g_sms[64];
 
 static int current_device() {
@@ -47,16 +46,62 @@ static int current_device() {
   return dev;
 }
 
-int* device_error_word() {
-  const int dev = current_device();
-  if (dev < 0) return nullptr;
-  std::lock_guard<std::mutex> lk(g_dev_mu);
-  if (!g_err_ptr[dev]) {
+// Unique id of the calling thread's current context, 0 if there is none (or it was destroyed).
+// The driver's cuCtxGetCurrent / cuCtxGetId are reached through the runtime's entry-point query,
+// as the tensor-map encoder is: the library does not link libcuda.
+static unsigned long long current_ctx_id() {
+  typedef int (*GetCurrentFn)(void**);
+  typedef int (*GetIdFn)(void*, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-    g_err_ptr[dev] = static_cast<int*>(p);
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  void* ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != 0 || !ctx || get_id(ctx, &id) != 0) return 0;
+  return id;
+}
+
+int symbol_address(const void* symbol, SymbolCache* cache, void** out, const char* what) {
+  const int dev = current_device();
+  if (dev < 0) {
+    set_error("%s: no usable current device", what);
+    return MOE_ERR_CUDA;
   }
-  return g_err_ptr[dev];
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  const unsigned long long id = current_ctx_id();
+  if (!cache->ptr[dev] || id == 0 || cache->ctx[dev] != id) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, symbol);
+    if (e != cudaSuccess || !p) {
+      set_error("%s: cudaGetSymbolAddress failed on device %d: %s", what, dev,
+                cudaGetErrorString(e));
+      return MOE_ERR_CUDA;
+    }
+    cache->ptr[dev] = p;
+    cache->ctx[dev] = current_ctx_id();   // the lookup made the primary context current
+  }
+  *out = cache->ptr[dev];
+  return MOE_OK;
+}
+
+static SymbolCache g_err_sym;
+
+int* device_error_word() {
+  void* p = nullptr;
+  if (symbol_address(&g_device_error, &g_err_sym, &p, "device error word") != MOE_OK) return nullptr;
+  return static_cast<int*>(p);
 }
 
 int num_sms() {
@@ -73,45 +118,30 @@ int num_sms() {
 
 // ------------------------------------------------------------------ side stream
 // "Megatron-Bridge 深度剖析", §Shared Expert Overlap: the shared expert's computation overlaps
-// the routed path instead of following it.  One library-owned non-blocking stream and a
-// fork/join event pair per device, created on the first layer call (make that call before any
-// stream capture).  A call's forked section is enqueued under g_side_mu so that calls from
-// several host threads do not interleave their records of the shared events.
-#ifndef MOE_SHARED_OVERLAP
-#define MOE_SHARED_OVERLAP 1
-#endif
-#ifndef MOE_SHARED_OVERLAP_FWD
-#define MOE_SHARED_OVERLAP_FWD MOE_SHARED_OVERLAP
-#endif
-#ifndef MOE_SHARED_OVERLAP_BWD
-#define MOE_SHARED_OVERLAP_BWD MOE_SHARED_OVERLAP
-#endif
-
-// Runtime switch (moe_set_stream_overlap): 1 = use the side stream (default), 0 = run the
-// forked work on the caller's stream.
-static std::atomic<int> g_overlap{1};
-
+// the routed path instead of following it.  The second stream and its fork/join events are the
+// caller's (moe_side_stream); the library holds no stream, event or switch of its own.
 struct SideStream {
-  cudaStream_t s = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-  bool ok = false;
+  cudaStream_t s;
+  cudaEvent_t fork, join;
 };
-static SideStream g_side[64];
-static std::mutex g_side_mu;
 
-// The device's side stream, or nullptr (then the caller runs everything on its own stream).
-static SideStream* side_stream() {
-  const int dev = current_device();
-  if (dev < 0) return nullptr;
-  std::lock_guard<std::mutex> lk(g_dev_mu);
-  SideStream& ss = g_side[dev];
-  if (!ss.ok && !ss.s) {
-    ss.ok = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) == cudaSuccess &&
-            cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) == cudaSuccess &&
-            cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) == cudaSuccess;
-    if (!ss.s) ss.s = reinterpret_cast<cudaStream_t>(-1);   // creation failed: do not retry
-  }
-  return ss.ok ? &ss : nullptr;
+static int check_side(const moe_side_stream* side, void* stream) {
+  if (!side) return MOE_OK;
+  if (!side->stream || !side->fork || !side->join)
+    return fail(MOE_ERR_INVALID_ARG, "side: stream, fork and join must all be given");
+  if (side->stream == stream)
+    return fail(MOE_ERR_INVALID_ARG, "side.stream must differ from the call's stream");
+  if (side->fork == side->join)
+    return fail(MOE_ERR_INVALID_ARG, "side.fork and side.join must be different events");
+  return MOE_OK;
+}
+
+static SideStream side_of(const moe_side_stream* side) {
+  SideStream ss;
+  ss.s = static_cast<cudaStream_t>(side->stream);
+  ss.fork = static_cast<cudaEvent_t>(side->fork);
+  ss.join = static_cast<cudaEvent_t>(side->join);
+  return ss;
 }
 
 // ------------------------------------------------------------------ launch accounting, tracing
@@ -661,13 +691,7 @@ using namespace moe;
 // ====================================================================== C ABI
 extern "C" {
 
-int moe_version(void) { return 103; }
-
-int moe_set_stream_overlap(int on) {
-  const int prev = g_overlap.load();
-  g_overlap.store(on ? 1 : 0);
-  return prev;
-}
+int moe_version(void) { return 200; }
 
 const char* moe_last_error(void) { return g_errbuf; }
 
@@ -1457,8 +1481,9 @@ static int layer_fwd_impl(const moe_cfg* c, const void* x, const void* W_r, cons
                           const void* W1, const void* W2, const moe_fp8_experts* q,
                           const void* Ws1, const void* Ws2, const void* w_sg, void* y,
                           const moe_saved* s, void* ws, size_t ws_bytes, void* stream,
-                          const moe_mxfp8_experts* mx = nullptr) {
+                          const moe_side_stream* side_in, const moe_mxfp8_experts* mx = nullptr) {
   MOE_TRY(check_cfg(c));
+  MOE_TRY(check_side(side_in, stream));
   MOE_TRY(check_ptr(x, "x", true));
   MOE_TRY(check_ptr(W_r, "W_r", true));
   MOE_TRY(check_ptr(b_r, "b_r", false));
@@ -1484,10 +1509,14 @@ static int layer_fwd_impl(const moe_cfg* c, const void* x, const void* W_r, cons
   }
   Carve cv(ws);
   RouteWs w = carve_route(cv, c);
-  // The shared expert (and its gate) needs only x: it runs on the side stream while the routed
-  // path (routing, permute, grouped SwiGLU) runs on `st`; the combine waits for both.
-  SideStream* side = (sh && MOE_SHARED_OVERLAP_FWD && g_overlap.load()) ? side_stream() : nullptr;
-  std::unique_lock<std::mutex> side_lk(g_side_mu, std::defer_lock);
+  // The shared expert (and its gate) needs only x: with a side stream it runs there while the
+  // routed path (routing, permute, grouped SwiGLU) runs on `st`; the combine waits for both.
+  SideStream side_ss;
+  SideStream* side = nullptr;
+  if (sh && side_in) {
+    side_ss = side_of(side_in);
+    side = &side_ss;
+  }
   auto shared_fwd = [&](cudaStream_t ss) -> int {
     if (gt) MOE_TRY(launch_shared_gate(c->dtype, x, w_sg, s->s_coef, c->T, c->d, ss));
     if (sq)
@@ -1510,7 +1539,6 @@ static int layer_fwd_impl(const moe_cfg* c, const void* x, const void* W_r, cons
     MOE_TRY(launch_permute_quant_mx(x, s->slot_of_pair, s->offsets, mx->x_perm_q, mx->x_perm_s,
                                     c->T, c->d, c->k, c->E, st, s->x_perm));
   if (side) {
-    side_lk.lock();
     if (cudaEventRecord(side->fork, st) != cudaSuccess ||
         cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess)
       return fail(MOE_ERR_CUDA, "forking the shared expert onto the side stream failed");
@@ -1544,7 +1572,6 @@ static int layer_fwd_impl(const moe_cfg* c, const void* x, const void* W_r, cons
   if (side) {
     if (cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess)
       return fail(MOE_ERR_CUDA, "joining the side stream failed");
-    side_lk.unlock();
   } else if (sh) {
     MOE_TRY(shared_fwd(st));
   }
@@ -1558,8 +1585,9 @@ static int layer_bwd_impl(const moe_cfg* c, const void* dy, const void* x, const
                           const void* Ws1, const void* Ws2, const void* w_sg, const moe_saved* s,
                           void* dx, float* dW_r, float* dW1, float* dW2, float* dWs1,
                           float* dWs2, float* dw_sg, void* ws, size_t ws_bytes, void* stream,
-                          const moe_mxfp8_dgrad* mxd = nullptr) {
+                          const moe_side_stream* side_in, const moe_mxfp8_dgrad* mxd = nullptr) {
   MOE_TRY(check_cfg(c));
+  MOE_TRY(check_side(side_in, stream));
   const bool sh = c->f_shared > 0, gt = c->shared_gate != 0;
   MOE_TRY(check_ptr(dy, "dy", true));
   MOE_TRY(check_ptr(x, "x", true));
@@ -1625,9 +1653,14 @@ static int layer_bwd_impl(const moe_cfg* c, const void* dy, const void* x, const
                                w.dgate, w.dshared, w.dcoef, T, d, k, st,
                                q ? q->scales + 5 : nullptr, sq ? q->scales + 11 : nullptr));
   // 2.-6. The routed experts run on `st`; the shared expert and the router's backward (which
-  // need only combine-backward outputs) run on the side stream concurrently; dx waits for both.
-  SideStream* side = (MOE_SHARED_OVERLAP_BWD && g_overlap.load()) ? side_stream() : nullptr;
-  std::unique_lock<std::mutex> side_lk(g_side_mu, std::defer_lock);
+  // need only combine-backward outputs) run on the side stream, when given, concurrently; dx
+  // waits for both.
+  SideStream side_ss;
+  SideStream* side = nullptr;
+  if (side_in) {
+    side_ss = side_of(side_in);
+    side = &side_ss;
+  }
   auto side_work = [&](cudaStream_t ss) -> int {
     // shared expert (one group of all T tokens)
     if (sq)
@@ -1684,7 +1717,6 @@ static int layer_bwd_impl(const moe_cfg* c, const void* dy, const void* x, const
     return launch_split_reduce(w.part, S_, mr, d, dW_r, E, gt ? dw_sg : nullptr, ss);
   };
   if (side) {
-    side_lk.lock();
     if (cudaEventRecord(side->fork, st) != cudaSuccess ||
         cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess)
       return fail(MOE_ERR_CUDA, "forking onto the side stream failed");
@@ -1710,7 +1742,6 @@ static int layer_bwd_impl(const moe_cfg* c, const void* dy, const void* x, const
   if (side) {
     if (cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess)
       return fail(MOE_ERR_CUDA, "joining the side stream failed");
-    side_lk.unlock();
   } else {
     MOE_TRY(side_work(st));
   }
@@ -1722,56 +1753,56 @@ static int layer_bwd_impl(const moe_cfg* c, const void* dy, const void* x, const
 int moe_layer_fwd(const moe_cfg* c, const void* x, const void* W_r, const float* b_r,
                   const void* W1, const void* W2, const void* Ws1, const void* Ws2,
                   const void* w_sg, void* y, const moe_saved* s, void* ws, size_t ws_bytes,
-                  void* stream) {
+                  void* stream, const moe_side_stream* side) {
   return layer_fwd_impl(c, x, W_r, b_r, W1, W2, nullptr, Ws1, Ws2, w_sg, y, s, ws, ws_bytes,
-                        stream);
+                        stream, side);
 }
 
 int moe_layer_fwd_mxfp8(const moe_cfg* c, const void* x, const void* W_r, const float* b_r,
                         const moe_mxfp8_experts* mx, const void* Ws1, const void* Ws2,
                         const void* w_sg, void* y, const moe_saved* saved, void* ws,
-                        size_t ws_bytes, void* stream) {
+                        size_t ws_bytes, void* stream, const moe_side_stream* side) {
   if (!mx) return fail(MOE_ERR_INVALID_ARG, "mx is NULL");
   return layer_fwd_impl(c, x, W_r, b_r, nullptr, nullptr, nullptr, Ws1, Ws2, w_sg, y, saved, ws,
-                        ws_bytes, stream, mx);
+                        ws_bytes, stream, side, mx);
 }
 
 int moe_layer_fwd_fp8(const moe_cfg* c, const void* x, const void* W_r, const float* b_r,
                       const moe_fp8_experts* q, const void* Ws1, const void* Ws2,
                       const void* w_sg, void* y, const moe_saved* s, void* ws, size_t ws_bytes,
-                      void* stream) {
+                      void* stream, const moe_side_stream* side) {
   if (!q) return fail(MOE_ERR_INVALID_ARG, "fp8 is NULL");
   return layer_fwd_impl(c, x, W_r, b_r, nullptr, nullptr, q, Ws1, Ws2, w_sg, y, s, ws, ws_bytes,
-                        stream);
+                        stream, side);
 }
 
 int moe_layer_bwd(const moe_cfg* c, const void* dy, const void* x, const void* W_r,
                   const void* W1, const void* W2, const void* Ws1, const void* Ws2,
                   const void* w_sg, const moe_saved* s, void* dx, float* dW_r, float* dW1,
                   float* dW2, float* dWs1, float* dWs2, float* dw_sg, void* ws, size_t ws_bytes,
-                  void* stream) {
+                  void* stream, const moe_side_stream* side) {
   return layer_bwd_impl(c, dy, x, W_r, W1, W2, nullptr, Ws1, Ws2, w_sg, s, dx, dW_r, dW1, dW2,
-                        dWs1, dWs2, dw_sg, ws, ws_bytes, stream);
+                        dWs1, dWs2, dw_sg, ws, ws_bytes, stream, side);
 }
 
 int moe_layer_bwd_mxfp8(const moe_cfg* c, const void* dy, const void* x, const void* W_r,
                         const moe_mxfp8_dgrad* mxd, const void* Ws1, const void* Ws2,
                         const void* w_sg, const moe_saved* s, void* dx, float* dW_r, float* dW1,
                         float* dW2, float* dWs1, float* dWs2, float* dw_sg, void* ws,
-                        size_t ws_bytes, void* stream) {
+                        size_t ws_bytes, void* stream, const moe_side_stream* side) {
   if (!mxd) return fail(MOE_ERR_INVALID_ARG, "mxd is NULL");
   return layer_bwd_impl(c, dy, x, W_r, nullptr, nullptr, nullptr, Ws1, Ws2, w_sg, s, dx, dW_r, dW1,
-                        dW2, dWs1, dWs2, dw_sg, ws, ws_bytes, stream, mxd);
+                        dW2, dWs1, dWs2, dw_sg, ws, ws_bytes, stream, side, mxd);
 }
 
 int moe_layer_bwd_fp8(const moe_cfg* c, const void* dy, const void* x, const void* W_r,
                       const moe_fp8_experts* q, const void* Ws1, const void* Ws2,
                       const void* w_sg, const moe_saved* s, void* dx, float* dW_r, float* dW1,
                       float* dW2, float* dWs1, float* dWs2, float* dw_sg, void* ws,
-                      size_t ws_bytes, void* stream) {
+                      size_t ws_bytes, void* stream, const moe_side_stream* side) {
   if (!q) return fail(MOE_ERR_INVALID_ARG, "fp8 is NULL");
   return layer_bwd_impl(c, dy, x, W_r, nullptr, nullptr, q, Ws1, Ws2, w_sg, s, dx, dW_r, dW1, dW2,
-                        dWs1, dWs2, dw_sg, ws, ws_bytes, stream);
+                        dWs1, dWs2, dw_sg, ws, ws_bytes, stream, side);
 }
 
 }  // extern "C"

@@ -19,6 +19,17 @@ void count_launch();
 void set_error(const char* fmt, ...);
 int* device_error_word();   // per-device error word (nullptr if CUDA is unusable)
 int num_sms();
+// Device address of a __device__ variable of this library in the current context.  Addresses
+// are cached per device together with the unique id of the context they were looked up in, and
+// looked up again when the current context differs (after cudaDeviceReset the module is loaded
+// into a new context and its variables may sit elsewhere).  The lookup initialises the device's
+// primary context if needed, so make the first call on a device before any stream capture.
+// MOE_OK or MOE_ERR_CUDA (message set).
+struct SymbolCache {
+  void* ptr[64];
+  unsigned long long ctx[64];
+};
+int symbol_address(const void* symbol, SymbolCache* cache, void** out, const char* what);
 
 template <typename... KArgs, typename... Args>
 int launch(const char* name, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,

@@ -21,29 +21,15 @@ namespace moe {
 constexpr int NOALLOC_ROUTE_MAX_ENTRIES = 65536;
 static __device__ __align__(256) int32_t g_route_scratch[2 * NOALLOC_ROUTE_MAX_ENTRIES];
 
-static std::mutex g_scratch_mu;
-static int32_t* g_scratch_ptr[64];
+static SymbolCache g_scratch_sym;
 
-// Device address of the array on the current device, looked up once per device.
+// Device address of the array in the current device's context: looked up (cudaGetSymbolAddress)
+// on the first call on a device, and again whenever the device's context has changed since (a
+// cudaDeviceReset in between), so the kernels never receive a stale address.
 static int route_scratch(int32_t** out) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= 64) {
-    set_error("moe_route_topk_noalloc: no usable current device (%s)", cudaGetErrorString(e));
-    return MOE_ERR_CUDA;
-  }
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_route_scratch);
-    if (e != cudaSuccess || !p) {
-      set_error("moe_route_topk_noalloc: cudaGetSymbolAddress failed on device %d: %s", dev,
-                cudaGetErrorString(e));
-      return MOE_ERR_CUDA;
-    }
-    g_scratch_ptr[dev] = static_cast<int32_t*>(p);
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  MOE_TRY(symbol_address(g_route_scratch, &g_scratch_sym, &p, "moe_route_topk_noalloc"));
+  *out = static_cast<int32_t*>(p);
   return MOE_OK;
 }
 

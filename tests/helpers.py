@@ -80,16 +80,24 @@ def clean_inputs(lc, seed=0, tries=80):
     raise AssertionError("no seed with a clear routing margin")
 
 
-def run_layer(lc, inp, backward=True, T=None):
-    """Forward (and backward) through the C ABI; returns dict of torch tensors on the device."""
+def run_layer(lc, inp, backward=True, T=None, side=True, stream=None, sync=True):
+    """Forward (and backward) through the C ABI; returns dict of torch tensors on the device.
+    side=True: the shared expert and the router backward run on a caller-owned side stream
+    (moe_side_stream), as bench.py runs them; False: one stream; or a moe.SideStream.
+    stream: the calls' stream (default: the current one); sync=False returns without waiting
+    for the GPU (the caller synchronises and checks the device error word)."""
     cfg = moe.cfg_from(lc, T=T)
     dev = inp["x"].device
+    if side is True:
+        side = moe.SideStream(dev)
+    elif side is False:
+        side = None
     saved = moe.alloc_saved(cfg, dev)
     y = torch.empty_like(inp["x"])
     ws_f = moe.workspace(cfg, moe.WS_LAYER_FWD, dev)
     moe.moe_layer_fwd(cfg, inp["x"], inp["W_r"], inp["b_r"], inp["W1"], inp["W2"], inp["Ws1"],
-                      inp["Ws2"], inp["w_sg"], y, saved, ws_f)
-    out = dict(y=y, saved=saved, cfg=cfg)
+                      inp["Ws2"], inp["w_sg"], y, saved, ws_f, stream=stream, side=side)
+    out = dict(y=y, saved=saved, cfg=cfg, _keep=[ws_f, side])   # alive until the GPU is done
     if backward:
         E, d, f, fs = cfg.E, cfg.d, cfg.f, cfg.f_shared
         f32 = torch.float32
@@ -105,10 +113,12 @@ def run_layer(lc, inp, backward=True, T=None):
         ws_b = moe.workspace(cfg, moe.WS_LAYER_BWD, dev)
         moe.moe_layer_bwd(cfg, inp["dy"], inp["x"], inp["W_r"], inp["W1"], inp["W2"], inp["Ws1"],
                           inp["Ws2"], inp["w_sg"], saved, g["dx"], g["dW_r"], g["dW1"], g["dW2"],
-                          g["dWs1"], g["dWs2"], g["dw_sg"], ws_b)
+                          g["dWs1"], g["dWs2"], g["dw_sg"], ws_b, stream=stream, side=side)
         out.update(g)
-    torch.cuda.synchronize()
-    moe.check_device_error()
+        out["_keep"].append(ws_b)
+    if sync:
+        torch.cuda.synchronize()
+        moe.check_device_error()
     return out
 
 

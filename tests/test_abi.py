@@ -83,6 +83,31 @@ def test_workspace_sizes_grow_with_the_layer():
         assert L.moe_workspace_bytes(ctypes.byref(big), w) > L.moe_workspace_bytes(ctypes.byref(small), w)
 
 
+def test_side_stream_arguments_are_checked_on_the_host():
+    """moe_side_stream (the caller's second stream for the layer calls): every field required,
+    fork and join distinct, the side stream not the call's own stream.  Rejected before any
+    launch; NULL (no side stream) passes this check and fails later on the missing buffers."""
+    c = cfg(f_shared=128)
+    ws = 1 << 30
+    a, b, e1, e2 = (ctypes.c_void_p((1 << 20) * i) for i in (3, 4, 5, 6))
+    bad = [moe.MoeSideStream(None, e1, e2), moe.MoeSideStream(b, None, e2),
+           moe.MoeSideStream(b, e1, None), moe.MoeSideStream(b, e1, e1),
+           moe.MoeSideStream(a, e1, e2)]                 # a is also the call's stream below
+    args_f = [P] * 9
+    for sd in bad:
+        assert L.moe_layer_fwd(ctypes.byref(c), *args_f, None, P, ws, a, ctypes.byref(sd)) == -1
+        assert b"side" in L.moe_last_error()
+        assert L.moe_layer_bwd(ctypes.byref(c), *([P] * 8), None, *([P] * 7), P, ws, a,
+                               ctypes.byref(sd)) == -1
+        assert b"side" in L.moe_last_error()
+    good = moe.MoeSideStream(b, e1, e2)
+    # a good side stream gets past its check: the NULL saved struct is what fails
+    assert L.moe_layer_fwd(ctypes.byref(c), *args_f, None, P, ws, a, ctypes.byref(good)) == -1
+    assert b"saved" in L.moe_last_error()
+    assert L.moe_layer_fwd(ctypes.byref(c), *args_f, None, P, ws, a, None) == -1
+    assert b"saved" in L.moe_last_error()
+
+
 def test_router_variant_entry_points_check_arguments():
     c = cfg(aux_coeff=1e-4)
     ws_n = L.moe_workspace_bytes(ctypes.byref(c), 0)
@@ -127,7 +152,7 @@ def test_mxfp8_entry_points_check_arguments():
     assert L.moe_grouped_swiglu_fwd_mxfp8(ctypes.byref(c), *args) == -1
     assert b"W1_q" in L.moe_last_error()
     assert L.moe_layer_fwd_mxfp8(ctypes.byref(c), P, P, None, None, None, None, None, P, None, P,
-                                 1 << 30, None) == -1
+                                 1 << 30, None, None) == -1
 
 
 def test_binding_argument_counts_match_the_header():

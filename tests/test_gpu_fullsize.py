@@ -10,6 +10,10 @@ compute one piece at a time:
   * y and dx on sampled tokens (whole forward and backward of those tokens, their experts,
     the shared expert and the router);
   * dW1, dW2 of sampled experts (all of an expert's rows, when none of them is a near tie);
+  * dW_r, dWs1, dWs2 and dw_sg as whole tensors: the router's weight gradient (split over
+    tokens, then a fixed-order sum) and the shared expert's (one group of all T rows, a
+    reduction of K = T = 16384 or 32768 rows), against the oracle's whole forward + backward
+    routed on the GPU's fp32 logits (so that near-tie rows take the same experts);
   * a second run of the same step gives bit-identical outputs (no float atomics, fixed-order
     sums, tiles claimed at run time but each reduced by one CTA).
 """
@@ -118,6 +122,25 @@ def test_fullsize_sampled_expert_weight_gradients(full_run):
         _, dW1e, dW2e = O.swiglu_ffn_backward(host["W1"][e], host["W2"][e], X, a, u, h, do)
         assert_close(f"dW1[{e}] ({len(t_list)} rows)", np64(gpu["dW1"][e]), dW1e, TOL[lc.dtype])
         assert_close(f"dW2[{e}] ({len(t_list)} rows)", np64(gpu["dW2"][e]), dW2e, TOL[lc.dtype])
+
+
+def test_fullsize_router_and_shared_weight_gradients(full_run):
+    lc, inp, gpu, host = full_run
+    if not lc.backward:
+        pytest.skip("forward-only workload")
+    s = gpu["saved"]
+    lg32 = np64(s["logits"]).astype(np.float32)
+    fwd = O.layer_forward(lc, host, selection_logits32=lg32)
+    assert (fwd["idx"] == np64(s["idx"])).all()
+    bwd = O.layer_backward(lc, host, fwd, host["dy"])
+    checked = []
+    for n in ("dW_r", "dWs1", "dWs2", "dw_sg"):
+        if gpu.get(n) is None:
+            assert bwd.get(n) is None, n
+            continue
+        checked.append((n, assert_close(n, np64(gpu[n]), bwd[n], TOL[lc.dtype])))
+    assert [n for n, _ in checked][:3] == ["dW_r", "dWs1", "dWs2"]
+    print(lc.name, {n: f"{e:.2e}" for n, e in checked})
 
 
 def test_fullsize_rerun_is_bit_identical(full_run):

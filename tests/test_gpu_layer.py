@@ -87,27 +87,32 @@ def test_zero_tokens():
 
 
 def test_layer_step_replays_from_a_cuda_graph():
-    """The layer calls are capturable (no allocation, stream-ordered memsets, side-stream
-    fork/join by events): a captured forward + backward replayed from a CUDA graph gives
-    bit-identical results to the eager calls."""
+    """The layer calls are capturable (no allocation, stream-ordered memsets, the caller's side
+    stream forked and joined by its events): a captured forward + backward replayed from a CUDA
+    graph gives bit-identical results to the eager calls, and those equal the calls without a
+    side stream."""
     import moe_expert_layer_gemm_gb300 as moe
     lc = CASES["bf16_sigmoid_zipf_shared"]
     inp, _ = clean_inputs(lc)
     d = inputs_to(inp, "cuda")
     eager = run_layer(lc, d)                      # also performs the one-time setup uncaptured
+    serial = run_layer(lc, d, side=False)
+    for n in ["y", "dx", "dW_r", "dW1", "dW2", "dWs1", "dWs2"]:
+        assert torch.equal(eager[n], serial[n]), n
     cfg = moe.cfg_from(lc)
     saved = moe.alloc_saved(cfg, "cuda")
     y = torch.empty_like(d["x"])
     g = {n: torch.empty_like(eager[n]) for n in ["dx", "dW_r", "dW1", "dW2", "dWs1", "dWs2"]}
     ws_f = moe.workspace(cfg, moe.WS_LAYER_FWD)
     ws_b = moe.workspace(cfg, moe.WS_LAYER_BWD)
+    side = moe.SideStream("cuda")
 
     def step():
         moe.moe_layer_fwd(cfg, d["x"], d["W_r"], d["b_r"], d["W1"], d["W2"], d["Ws1"], d["Ws2"],
-                          d["w_sg"], y, saved, ws_f)
+                          d["w_sg"], y, saved, ws_f, side=side)
         moe.moe_layer_bwd(cfg, d["dy"], d["x"], d["W_r"], d["W1"], d["W2"], d["Ws1"], d["Ws2"],
                           d["w_sg"], saved, g["dx"], g["dW_r"], g["dW1"], g["dW2"], g["dWs1"],
-                          g["dWs2"], None, ws_b)
+                          g["dWs2"], None, ws_b, side=side)
 
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -126,3 +131,26 @@ def test_layer_step_replays_from_a_cuda_graph():
     assert torch.equal(y, eager["y"])
     for n, t in g.items():
         assert torch.equal(t, eager[n]), n
+
+
+def test_two_layer_steps_run_concurrently_on_their_own_streams():
+    """The library owns no stream or switch: two forward + backward steps issued back to back on
+    two streams, each with its own buffers, workspaces and side stream, may run at the same
+    time, and each gives the results of the same step run alone."""
+    import moe_expert_layer_gemm_gb300 as moe
+    lc = CASES["bf16_sigmoid_zipf_shared"]
+    runs = []
+    for seed in (0, 1):
+        inp, _ = clean_inputs(lc, seed=seed)
+        runs.append(inputs_to(inp, "cuda"))
+    alone = [run_layer(lc, d) for d in runs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    # the second step is enqueued while the first may still run
+    together = [run_layer(lc, runs[i], stream=streams[i], sync=False) for i in (0, 1)]
+    torch.cuda.synchronize()
+    moe.check_device_error()
+    for i in (0, 1):
+        for n in ["y", "dx", "dW_r", "dW1", "dW2", "dWs1", "dWs2"]:
+            assert torch.equal(together[i][n], alone[i][n]), (i, n)
