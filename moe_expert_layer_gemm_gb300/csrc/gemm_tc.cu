@@ -1336,33 +1336,30 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
 }
 
 // ---------------------------------------------------------------- weight gradients on CTA pairs
-// The same weight-gradient product (dW_g = A_g^T . B_g over each group's reduction rows, fp32
-// blocks) on 2-SM tensor-core instructions (tcgen05 cta_group::2).  A cluster of two CTAs owns
-// a 256 x 256 output tile: each CTA loads its 128 rows of A and its 128 columns of B per
-// k-block (32 KB instead of 48 KB), and the even CTA issues M = 256, N = 256 MMAs that read
-// both CTAs' shared memory and leave rows 0..127 in its TMEM and rows 128..255 in the other's.
-// Per FLOP, each SM takes in a third fewer operand bytes, and the smaller stages make room for
-// six of them instead of four.
+// A weight gradient of ONE group (dW = A^T . B over all K rows, fp32 block; the shared expert's)
+// on 2-SM tensor-core instructions (tcgen05 cta_group::2).  A cluster of two CTAs owns a
+// 256 x 256 output tile: each CTA loads its 128 rows of A and its 128 columns of B per k-block
+// (32 KB), and the even CTA issues M = 256, N = 256 MMAs that read both CTAs' shared memory and
+// leave output rows 0..127 in its TMEM and rows 128..255 in the other CTA's.  Per FLOP each SM
+// takes in a third fewer operand bytes than with one-CTA 128 x 256 tiles (48 KB per k-block).
+// The group's rows are all of A's and B's rows, so the last k-block reads zeros past their end
+// (TMA fills rows outside the tensor with zeros): nothing to mask.
 //
-// Protocol (stage s of the ring, tile t):
-//   * the even CTA's producer claims tiles (heaviest experts first, as the one-CTA kernel) and
+// Protocol (stage s of the operand ring, tile t):
+//   * the even CTA's producer claims tiles (heaviest groups first, as the one-CTA kernel) and
 //     hands each to both CTAs' consumers through a feed ring written into both CTAs;
-//   * both producers wait for their own empty[s] (released by the even CTA's MMA commit, which
-//     arrives on both CTAs), then load; the odd CTA's copies count their bytes on the even
-//     CTA's full[s] and it arrives there too (full[s] expects two arrivals);
-//   * a group's last k-block, when it runs past the group's end, is loaded by the odd CTA onto
-//     its own barrier, its rows past the end zeroed, and only then does it arrive on the even
-//     CTA's full[s] (the even CTA zeroes its own rows before issuing);
+//   * both producers wait for their own empty[s] (the even CTA's MMA commit arrives on both),
+//     then load; the even one arms full[s] with both CTAs' bytes, the odd one's copies count
+//     their bytes on the even CTA's full[s] (cta_group::2 copies), and it does not arrive;
 //   * the MMAs' commit arrives on tfull in both CTAs; each CTA's epilogue stores its own 128
 //     rows and arrives on the even CTA's tempty, which the MMA warp waits on before reusing an
 //     accumulator.
 // Every wait is bounded (abort flag and error word as in the one-CTA kernel).
-// Build option, off by default: parity-green, but slower on GB300 than the one-CTA kernel
-// (fc1 weight gradient of the 128-expert layer 1.90 -> 2.15 ms).  These products are bound by
-// DRAM (about 7 GB per fc1 launch, 5.1 GB of it the fp32 gradient blocks, at ~4 TB/s of mixed
-// read/write traffic), not by the operand bytes each SM takes in, which is what pairs reduce.
+// Build option (on): 0 runs one-group weight gradients on the one-CTA kernel too.  Several
+// groups always take the one-CTA kernel: with skewed routing most of their tiles only store,
+// and its two accumulators overlap one tile's stores with the next tile's MMAs.
 #ifndef MOE_PAIR_WGRAD
-#define MOE_PAIR_WGRAD 0
+#define MOE_PAIR_WGRAD 1
 #endif
 
 namespace pairk {
@@ -1372,14 +1369,17 @@ constexpr int A_ST = BM * BK * 2;              // 16 KB
 constexpr int B_ST = HB * BK * 2;              // 16 KB
 constexpr int EW = 4;                          // epilogue warps
 #ifndef MOE_PAIR_SLABS
-#define MOE_PAIR_SLABS 4
+#define MOE_PAIR_SLABS 2
 #endif
 constexpr int SLABS_P = MOE_PAIR_SLABS;        // fp32 stores in flight per epilogue warp
-constexpr int STAGING = EW * SLABS_P * SLAB;   // 32 KB
+constexpr int STAGING = EW * SLABS_P * SLAB;
 constexpr int AUX = 3072;
 constexpr int MAX_SMEM = 232448;
 constexpr int FIT = (MAX_SMEM - STAGING - AUX) / (A_ST + B_ST);
-constexpr int STAGES = FIT < 6 ? FIT : 6;
+#ifndef MOE_PAIR_MAX_STAGES
+#define MOE_PAIR_MAX_STAGES 8
+#endif
+constexpr int STAGES = FIT < MOE_PAIR_MAX_STAGES ? FIT : MOE_PAIR_MAX_STAGES;
 constexpr int RING = STAGES * (A_ST + B_ST);
 constexpr int SMEM = RING + STAGING + AUX;
 constexpr int THREADS = 64 + 32 * EW;
@@ -1398,13 +1398,12 @@ __global__ void __launch_bounds__(pairk::THREADS, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_ST;
   uint8_t* staging = smem + RING;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING + STAGING);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING + STAGING);   // even CTA's are used
   uint64_t* empty = full + STAGES;
-  uint64_t* pfull = empty + STAGES;       // odd CTA: its own copies of a group's last k-block
-  uint64_t* tfull = pfull + STAGES;
-  uint64_t* tempty = tfull + 2;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;           // even CTA's are used
   uint64_t* feed_full = tempty + 2;
-  uint64_t* feed_empty = feed_full + FEED;
+  uint64_t* feed_empty = feed_full + FEED;   // even CTA's are used
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(feed_empty + FEED);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* s_bad = reinterpret_cast<int*>(tmem_holder + 2);
@@ -1422,9 +1421,8 @@ __global__ void __launch_bounds__(pairk::THREADS, 1)
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      ptx::mbar_init(&full[i], 2);     // even producer (with the bytes) + odd producer
+      ptx::mbar_init(&full[i], 1);     // the even producer's arrival (with both CTAs' bytes)
       ptx::mbar_init(&empty[i], 1);    // the pair's MMA commit
-      ptx::mbar_init(&pfull[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&tfull[i], 1);
@@ -1478,140 +1476,82 @@ __global__ void __launch_bounds__(pairk::THREADS, 1)
   const uint32_t tmem_base = *tmem_holder;
   // the even CTA's barriers as seen from the odd CTA
   auto even_addr = [&](const void* local) { return ptx::mapa(ptx::smem_u32(local), 0); };
-  // rows of this k-block (counted from its start) that belong to the group, if fewer than BK
-  auto tail_rows = [&](const TileInfo& ti, int kb) {
-    return kb == ti.kblocks - 1 ? ti.k_end - (ti.k0 + kb * BK) : BK;
-  };
-  // zero rows [valid, BK) of this CTA's A block (MN-major: row r of chunk c is 128 bytes)
-  auto zero_tail = [&](uint8_t* a_src, int valid) {
-    const int nbytes = (BK - valid) * 128;
-    for (int c = 0; c < BM / 64; ++c) {
-      uint8_t* base = a_src + c * (BK * 128) + valid * 128;
-      for (int o = lane * 16; o < nbytes; o += 32 * 16)
-        *reinterpret_cast<uint4*>(base + o) = make_uint4(0, 0, 0, 0);
-    }
-    ptx::fence_proxy_async_smem();
-  };
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producers
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t pph = 0;                    // odd CTA: parity of each stage's pfull barrier
-    int fslot = 0;
-    uint32_t fphase = 0;
-    bool ok = true;
-    int armed[STAGES];
-    for (int i = 0; i < STAGES; ++i) armed[i] = -1;
-    int tail_pending = -1;               // odd CTA: a pfull stage whose copies may be in flight
-    const int m_off = static_cast<int>(rank) * BM;    // this CTA's rows of the pair tile
-    const int n_off = static_cast<int>(rank) * HB;    // this CTA's columns of B
-    int next = (even && lane == 0) ? atomicAdd(p.tile_ctr, 1) : 0;
-    for (;;) {
-      // -------- the tile: claimed and published by the even CTA, received by the odd one
-      int tile = 0;
-      bool w = true;
-      if (lane == 0) {
+    // ------------------------------------------------------------ producers (lane 0)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int fslot = 0;
+      uint32_t fphase = 0;
+      bool ok = true;
+      int armed[STAGES];
+      for (int i = 0; i < STAGES; ++i) armed[i] = -1;
+      const int m_off = static_cast<int>(rank) * BM;    // this CTA's rows of the pair tile
+      const int n_off = static_cast<int>(rank) * HB;    // this CTA's columns of B
+      int next = even ? atomicAdd(p.tile_ctr, 1) : 0;
+      for (;;) {
+        // -------- the tile: claimed and published by the even CTA, received by the odd one
+        int tile;
         if (even) {
           tile = next < total ? next : -1;
-          w = ptx::mbar_wait_cluster(&feed_empty[fslot], fphase ^ 1u, abort_flag, p.err);
-          if (w) {
-            s_feed[fslot] = tile;
-            ptx::st_cluster_u32(ptx::mapa(ptx::smem_u32(const_cast<int*>(&s_feed[fslot])), 1),
-                                static_cast<uint32_t>(tile));
-            ptx::mbar_arrive(&feed_full[fslot]);
-            ptx::mbar_arrive_remote(ptx::mapa(ptx::smem_u32(&feed_full[fslot]), 1));
-            if (tile >= 0) next = atomicAdd(p.tile_ctr, 1);
+          if (!ptx::mbar_wait_cluster(&feed_empty[fslot], fphase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
           }
+          s_feed[fslot] = tile;
+          ptx::st_cluster_u32(ptx::mapa(ptx::smem_u32(const_cast<int*>(&s_feed[fslot])), 1),
+                              static_cast<uint32_t>(tile));
+          ptx::mbar_arrive(&feed_full[fslot]);
+          ptx::mbar_arrive_remote(ptx::mapa(ptx::smem_u32(&feed_full[fslot]), 1));
+          if (tile >= 0) next = atomicAdd(p.tile_ctr, 1);
         } else {
-          w = ptx::mbar_wait_cluster(&feed_full[fslot], fphase, abort_flag, p.err);
-          if (w) {
-            tile = s_feed[fslot];
-            ptx::mbar_arrive_remote(even_addr(&feed_empty[fslot]));
+          if (!ptx::mbar_wait_cluster(&feed_full[fslot], fphase, abort_flag, p.err)) {
+            ok = false;
+            break;
           }
+          tile = s_feed[fslot];
+          ptx::mbar_arrive_remote(even_addr(&feed_empty[fslot]));
         }
-      }
-      w = __shfl_sync(0xffffffffu, w, 0);
-      tile = __shfl_sync(0xffffffffu, tile, 0);
-      if (!w) { ok = false; break; }
-      if (++fslot == FEED) { fslot = 0; fphase ^= 1u; }
-      if (tile < 0) break;
-      const TileInfo ti = S::decode(p, s_off, nullptr, s_ord, tile);
-      for (int kb = 0; kb < ti.kblocks; ++kb) {
-        const int kk = ti.k0 + kb * BK;
-        const int valid = tail_rows(ti, kb);
-        const bool tail = valid < BK;
-        uint8_t* a_dst = sA + stage * A_ST;
-        uint8_t* b_dst = sB + stage * B_ST;
-        // (stage release by the MMA commit: CTA-scope waits, as for any tensor-core arrival)
-        if (lane == 0) w = ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err);
-        w = __shfl_sync(0xffffffffu, w, 0);
-        if (!w) { ok = false; break; }
-        if (even) {
-          if (lane == 0) {
-            // own bytes, and the odd CTA's unless this is a short last k-block
-            ptx::mbar_arrive_expect_tx(&full[stage], tail ? A_ST + B_ST : 2 * (A_ST + B_ST));
+        if (++fslot == FEED) { fslot = 0; fphase ^= 1u; }
+        if (tile < 0) break;
+        const TileInfo ti = S::decode(p, s_off, nullptr, s_ord, tile);
+        const CUtensorMap* ma = &tmA;
+        for (int kb = 0; kb < ti.kblocks; ++kb) {
+          const int kk = ti.k0 + kb * BK;
+          uint8_t* a_dst = sA + stage * A_ST;
+          uint8_t* b_dst = sB + stage * B_ST;
+          if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+          if (even) {
+            ptx::mbar_arrive_expect_tx(&full[stage], 2 * (A_ST + B_ST));
             armed[stage] = static_cast<int>(phase);
 #pragma unroll
             for (int c = 0; c < BM / 64; ++c)
-              ptx::tma_load_2d(a_dst + c * (BK * 128), &tmA, &full[stage], ti.m0 + m_off + 64 * c, kk);
+              ptx::tma_load_2d(a_dst + c * (BK * 128), ma, &full[stage], ti.m0 + m_off + 64 * c, kk);
 #pragma unroll
             for (int c = 0; c < HB / 64; ++c)
               ptx::tma_load_2d(b_dst + c * (BK * 128), &tmB, &full[stage], ti.n0 + n_off + 64 * c, kk);
-          }
-        } else if (!tail) {
-          if (lane == 0) {
+          } else {
             const uint32_t fb = even_addr(&full[stage]);
 #pragma unroll
             for (int c = 0; c < BM / 64; ++c)
-              ptx::tma_load_2d_pair(a_dst + c * (BK * 128), &tmA, fb, ti.m0 + m_off + 64 * c, kk);
+              ptx::tma_load_2d_pair(a_dst + c * (BK * 128), ma, fb, ti.m0 + m_off + 64 * c, kk);
 #pragma unroll
             for (int c = 0; c < HB / 64; ++c)
               ptx::tma_load_2d_pair(b_dst + c * (BK * 128), &tmB, fb, ti.n0 + n_off + 64 * c, kk);
-            // the bytes are ordered by the copies' own completion on full[stage]: this arrival
-            // only counts (a release here would wait for the copies just issued)
-            ptx::mbar_arrive_remote_relaxed(fb);
           }
-        } else {
-          // short last k-block: land on our own barrier, zero the rows past the group, then
-          // release it to the even CTA
-          if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(&pfull[stage], A_ST + B_ST);
-            tail_pending = stage;
-#pragma unroll
-            for (int c = 0; c < BM / 64; ++c)
-              ptx::tma_load_2d(a_dst + c * (BK * 128), &tmA, &pfull[stage], ti.m0 + m_off + 64 * c, kk);
-#pragma unroll
-            for (int c = 0; c < HB / 64; ++c)
-              ptx::tma_load_2d(b_dst + c * (BK * 128), &tmB, &pfull[stage], ti.n0 + n_off + 64 * c, kk);
-            w = ptx::mbar_wait(&pfull[stage], (pph >> stage) & 1u, abort_flag, p.err);
-          }
-          w = __shfl_sync(0xffffffffu, w, 0);
-          if (!w) { ok = false; break; }
-          pph ^= 1u << stage;
-          tail_pending = -1;
-          zero_tail(a_dst, valid);
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive_remote(even_addr(&full[stage]));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        __syncwarp();
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        if (!ok) break;
       }
-      if (!ok) break;
-    }
-    if (!ok && lane == 0) {
-      // Unwinding: let this CTA's copies land before the CTA exits (bounded).
-      const uint64_t t0 = ptx::globaltimer();
-      if (even) {
+      if (!ok && even) {
+        // Unwinding: let every copy into an armed stage land before the CTA exits (bounded).
+        const uint64_t t0 = ptx::globaltimer();
         for (int i = 0; i < STAGES; ++i) {
           if (armed[i] < 0) continue;
           while (!ptx::mbar_try_wait_acq_cluster(&full[i], static_cast<uint32_t>(armed[i])) &&
                  ptx::globaltimer() - t0 < 100000000ull) {
           }
-        }
-      } else if (tail_pending >= 0) {
-        while (!ptx::mbar_try_wait(&pfull[tail_pending], (pph >> tail_pending) & 1u) &&
-               ptx::globaltimer() - t0 < 100000000ull) {
         }
       }
     }
@@ -1638,20 +1578,11 @@ __global__ void __launch_bounds__(pairk::THREADS, 1)
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN2);
         for (int kb = 0; kb < ti.kblocks; ++kb) {
-          const int valid = tail_rows(ti, kb);
-          // a short last k-block carries the odd CTA's ordinary stores (its zeroed rows):
-          // cluster-scope acquire; the other stages complete on TMA bytes alone
-          const bool got = valid < BK
-                               ? ptx::mbar_wait_cluster(&full[stage], phase, abort_flag, p.err)
-                               : ptx::mbar_wait(&full[stage], phase, abort_flag, p.err);
-          if (!got) { ok = false; break; }
-          uint8_t* a_src = sA + stage * A_ST;
-          uint8_t* b_src = sB + stage * B_ST;
-          if (valid < BK) zero_tail(a_src, valid);
-          __syncwarp();
+          if (!ptx::mbar_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
           ptx::tc_fence_after();
           if (lane == 0) {
-            const uint32_t a_addr = ptx::smem_u32(a_src), b_addr = ptx::smem_u32(b_src);
+            const uint32_t a_addr = ptx::smem_u32(sA + stage * A_ST);
+            const uint32_t b_addr = ptx::smem_u32(sB + stage * B_ST);
 #pragma unroll
             for (int k16 = 0; k16 < BK / 16; ++k16) {
               const uint64_t ad = ptx::smem_desc_sw128(a_addr + k16 * 2048, BK * 128, 1024);
@@ -1973,7 +1904,37 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
                 mo[2], a);
 }
 
-// Weight gradient on CTA pairs (tc_wgrad_pair_kernel).
+// CTA pairs of tc_wgrad_pair_kernel that can be resident at once on the current device (one per
+// two SMs at most: a pair must sit in one GPC), so that the persistent grid is a single wave.
+int pair_clusters() {
+  static int cached[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms() / 2;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!cached[dev]) {
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms() & ~1);
+    cfg.blockDim = dim3(pairk::THREADS);
+    cfg.dynamicSmemBytes = pairk::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_wgrad_pair_kernel, &cfg) != cudaSuccess || n < 1) {
+      cudaGetLastError();   // clear it: the launch reports any real problem
+      n = num_sms() / 2;
+    }
+    cached[dev] = n < num_sms() / 2 ? n : num_sms() / 2;
+  }
+  return cached[dev];
+}
+
+// A one-group weight gradient on CTA pairs (tc_wgrad_pair_kernel).
 int run_wgrad_pair(const GemmDesc& g, cudaStream_t st) {
   using namespace pairk;
   const char* name = g.name ? g.name : "gemm_wgrad";
@@ -2011,8 +1972,8 @@ int run_wgrad_pair(const GemmDesc& g, cudaStream_t st) {
     set_error("%s: clearing the tile counter failed", name);
     return MOE_ERR_CUDA;
   }
-  return launch_clusters(name, tc_wgrad_pair_kernel, dim3(num_sms() & ~1), dim3(THREADS), SMEM, 2,
-                         st, ma, mb, mo, a);
+  return launch_clusters(name, tc_wgrad_pair_kernel, dim3(2 * pair_clusters()), dim3(THREADS),
+                         SMEM, 2, st, ma, mb, mo, a);
 }
 
 }  // namespace
@@ -2091,7 +2052,9 @@ int gemm_tc(const GemmDesc& g, cudaStream_t st) {
   }
   if (g.sched == RAGGED_K && g.A.mn_major && g.B.mn_major && g.epi == EPI_F32) {
     if (g.gather) return run<256, true, true, RAGGED_K, EPI_F32, true>(g, "gemm_wgrad", st);
-    if (MOE_PAIR_WGRAD) return run_wgrad_pair(g, st);
+    // one group whose rows are all of both operands' rows (the shared expert): CTA pairs
+    if (MOE_PAIR_WGRAD && g.G == 1 && !g.offsets && g.M > 256 && g.A.rows == g.K && g.B.rows == g.K)
+      return run_wgrad_pair(g, st);
     return run<256, true, true, RAGGED_K, EPI_F32>(g, "gemm_wgrad", st);
   }
   set_error("gemm_tc: unsupported combination sched=%d epi=%d a_mn=%d b_mn=%d", g.sched, g.epi,
