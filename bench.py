@@ -66,7 +66,6 @@ def kernel_work(lc, trace=None, steps=1):
         "gemm_router_wgrad": ("tensor", 2.0 * T * d * (E + g)),
         "route_topk": ("hbm", T * E * 4 + N * 8),
         "route_scan": ("hbm", 0.0),
-        "route_hist": ("hbm", N * 4),
         "route_slots": ("hbm", N * 4 + N * 8),
         "permute": ("hbm", T * d * b * (1 + k) + N * 4),
         "combine": ("hbm", T * d * b * (k + 1) + N * 8 + (T * d * b if fs else 0)),
@@ -664,6 +663,23 @@ def run_gpu(args, lc):
                                                   if kind == "tensor" else "hbm_gbs") + ")",
                 "peak_sustained": tensor_peak(dom, True) if kind == "tensor" else peaks["hbm_gbs"],
                 "frac_sustained": kd["frac_sustained"]}
+    # The routing chain of the forward: router GEMM (whose epilogue also selects, with bf16
+    # operands), top-k (given or fp32 logits), the scan (large histograms only) and the slot maps.
+    # Its algorithmic bytes: x and W_r read, fp32 logits written, idx, gate and both slot maps
+    # written (4 x N x 4 bytes).
+    chain = [n for n in ("gemm_router", "route_topk", "route_scan", "route_slots") if n in trace]
+    routing = None
+    if chain:
+        r_ms = sum(trace[n][1] for n in chain) / n_trace
+        r_bytes = (lc.T * lc.d * (2 if lc.dtype == "bf16" else 4) * 1.0 +
+                   lc.E * lc.d * (2 if lc.dtype == "bf16" else 4) + lc.T * lc.E * 4 +
+                   16.0 * lc.T * lc.k)
+        r_ach = r_bytes / (r_ms / 1e3) / 1e9
+        rest = [n for n in chain if n != "gemm_router"]
+        routing = {"launches": chain, "ms_per_step": round(r_ms, 4),
+                   "bytes": int(r_bytes), "achieved": round(r_ach, 1), "unit": "GB/s",
+                   "frac": round(r_ach / peaks["hbm_gbs"], 4),
+                   "after_gemm_ms": round(sum(trace[n][1] for n in rest) / n_trace, 4)}
     gemm_ms = sum(ms for n, (_, ms) in trace.items() if n.startswith("gemm_"))
     gemm_flops = sum(flops_of[n][1] * trace[n][0] for n in trace
                      if n.startswith("gemm_") and n in flops_of)
@@ -703,6 +719,7 @@ def run_gpu(args, lc):
         "pct_bf16_peak_sustained": round(flops_step / (ms_step / 1e3) / 1e12 / bf16_sus, 4),
         "grouped_gemm_tflops": round(gemm_tflops, 1) if gemm_tflops else None,
         "roofline": roof,
+        "routing_chain": routing,
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),

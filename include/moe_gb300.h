@@ -136,9 +136,10 @@ int moe_route_topk(const moe_cfg* cfg, const void* x, const void* W_r, const flo
  * only input and output tensors).  Arguments, outputs and errors are those of moe_route_topk,
  * without ws / ws_bytes, and with one more requirement: logits_in or logits_out must be set
  * (the router logits need a caller buffer; MOE_ERR_INVALID_ARG otherwise).
- *   Scratch: a fixed 512 KB array inside the library, held on every GPU that loads it until the
- *   process exits.  E * ceil(T/256) must not exceed 65536 (e.g. T = 65536 tokens with E = 256,
- *   or T = 131072 with E = 128); larger calls return MOE_ERR_UNSUPPORTED.
+ *   Scratch: a fixed 128 KB array inside the library (the expert histogram: one row of E16 bytes
+ *   per 128 tokens, E16 = E rounded up to a power of two of at least 16), held on every GPU that
+ *   loads it until the process exits.  ceil(T/128) * E16 must not exceed 131072 (e.g. T = 65536
+ *   tokens with E = 256, or T = 131072 with E = 128); larger calls return MOE_ERR_UNSUPPORTED.
  *   The first call on a device looks up the array's device address (cudaGetSymbolAddress),
  *   and so does the first call after the device's context was replaced (cudaDeviceReset): make
  *   those calls before any stream capture.

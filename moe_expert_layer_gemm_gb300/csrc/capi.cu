@@ -217,18 +217,19 @@ static int router_splits(const moe_cfg* c) {
 }
 
 struct RouteWs {
-  int32_t* hist;
-  int32_t* base;
+  uint8_t* hist;     // expert histogram [route_rows(T)][route_ldh(E)] bytes
+  int32_t* rowpre;   // its per-row prefixes [E][route_rows(T)]: large histograms only, else null
   float* logits;
-  float* aux;   // balancing-loss partial sums [route_blocks(T)][E]
+  float* aux;        // balancing-loss partial sums [route_blocks(T)][E]
 };
 static RouteWs carve_route(Carve& cv, const moe_cfg* c) {
   RouteWs w;
-  const size_t nb = static_cast<size_t>(route_blocks(c->T)) * c->E;
-  w.hist = static_cast<int32_t*>(cv.take(nb * 4));
-  w.base = static_cast<int32_t*>(cv.take(nb * 4));
+  w.hist = static_cast<uint8_t*>(cv.take(static_cast<size_t>(route_hist_bytes(c->T, c->E))));
+  w.rowpre = nullptr;
+  if (!route_hist_direct(c->T, c->E))
+    w.rowpre = static_cast<int32_t*>(cv.take(static_cast<size_t>(route_rows(c->T)) * c->E * 4));
   w.logits = static_cast<float*>(cv.take(static_cast<size_t>(c->T) * c->E * 4));
-  w.aux = static_cast<float*>(cv.take(nb * 4));
+  w.aux = static_cast<float*>(cv.take(static_cast<size_t>(route_blocks(c->T)) * c->E * 4));
   return w;
 }
 
@@ -361,6 +362,7 @@ static int route_impl(const moe_cfg* c, const void* x, const void* W_r, const fl
   // selection-only expert bias of the top-k.
   const bool select_bias = c->bias_mode == MOE_BIAS_SELECT;
   const float* logits = logits_in;
+  bool selected = false;   // idx, gate and the histogram rows already written
   if (!logits) {
     float* dst = logits_out ? logits_out : w.logits;
     GemmDesc g = desc0();
@@ -376,14 +378,26 @@ static int route_impl(const moe_cfg* c, const void* x, const void* W_r, const fl
     g.out = dst;
     g.ldo = c->E;
     g.bias = select_bias ? nullptr : b_r;
+    if (c->dtype == MOE_DTYPE_BF16) {
+      // tensor-core router: each epilogue thread holds one token's E logits in tensor memory
+      // and routes the token there (selection, gates, its tile's histogram row)
+      g.rt.idx = idx;
+      g.rt.gate = gate;
+      g.rt.hist = w.hist;
+      g.rt.sel_bias = select_bias ? b_r : nullptr;
+      g.rt.k = c->k;
+      g.rt.score_fn = c->score_fn;
+      g.rt.renorm = c->renorm;
+      g.rt.ldh = route_ldh(c->E);
+      selected = true;
+    }
     MOE_TRY(gemm(c, g, st));
     logits = dst;
   }
-  MOE_TRY(launch_topk(logits, c->T, c->E, c->k, c->score_fn, c->renorm,
-                      select_bias ? b_r : nullptr, idx, gate, w.hist, st));
-  MOE_TRY(launch_scan(w.hist, c->E, route_blocks(c->T), w.base, counts, st));
-  MOE_TRY(launch_slots(idx, c->T, c->k, c->E, w.base, counts, offsets, sop, tos, st));
-  return MOE_OK;
+  if (!selected)
+    MOE_TRY(launch_topk(logits, c->T, c->E, c->k, c->score_fn, c->renorm,
+                        select_bias ? b_r : nullptr, idx, gate, w.hist, st));
+  return launch_slots(idx, c->T, c->k, c->E, w.hist, w.rowpre, counts, offsets, sop, tos, st);
 }
 
 // fc1 + SwiGLU and fc2 for G groups whose rows are given by offsets (null: one group of `rows`).
@@ -1819,10 +1833,10 @@ int validate_ptr(const void* p, const char* name, bool required) {
 int route_stages(const moe_cfg* c, const void* x, const void* W_r, const float* b_r,
                  const float* logits_in, float* logits_out, int32_t* idx, float* gate,
                  int32_t* counts, int32_t* offsets, int32_t* slot_of_pair, int32_t* token_of_slot,
-                 int32_t* hist, int32_t* base, cudaStream_t st) {
+                 uint8_t* hist, int32_t* rowpre, cudaStream_t st) {
   RouteWs w;
   w.hist = hist;
-  w.base = base;
+  w.rowpre = rowpre;
   w.logits = nullptr;
   w.aux = nullptr;
   return route_impl(c, x, W_r, b_r, logits_in, logits_out, idx, gate, counts, offsets,

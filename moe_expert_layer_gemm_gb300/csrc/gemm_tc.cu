@@ -27,6 +27,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
+#include "route_row.cuh"
 
 namespace moe {
 
@@ -128,17 +129,19 @@ template <int BN, int SCHED, int EPI, bool F8 = false> struct EpiWidth {
 
 // SFS: bytes of MXFP8 block scales per stage (0 without); MAXST: most stages the ring may have;
 // TCOLS: TMEM columns to allocate (0: the two accumulators' power of two).
-template <int BN, bool TMA_OUT, int EPI_WARPS, int SLABS, int SFS = 0, int MAXST = 6, int TCOLS = 0>
+// XTRA: bytes after the AUX block (the router epilogue's histogram buffers).
+template <int BN, bool TMA_OUT, int EPI_WARPS, int SLABS, int SFS = 0, int MAXST = 6, int TCOLS = 0,
+          int XTRA = 0>
 struct TileCfg {
   static constexpr int B_STAGE = BN * BK * 2;
   static constexpr int STAGING = TMA_OUT ? EPI_WARPS * SLABS * SLAB : 0;
   static constexpr int AUX = 3072;   // barriers, TMEM address, flags, group tables
   static constexpr int MAX_SMEM = 232448;   // opt-in dynamic shared memory per block
-  static constexpr int FIT = (MAX_SMEM - STAGING - AUX) / (A_STAGE + B_STAGE + SFS);
+  static constexpr int FIT = (MAX_SMEM - STAGING - AUX - XTRA) / (A_STAGE + B_STAGE + SFS);
   static constexpr int STAGES = FIT < MAXST ? FIT : MAXST;
   static constexpr int RING = STAGES * (A_STAGE + B_STAGE);
   static constexpr int SF_RING = STAGES * SFS;   // after the staging slabs
-  static constexpr int SMEM = RING + STAGING + SF_RING + AUX;
+  static constexpr int SMEM = RING + STAGING + SF_RING + AUX + XTRA;
   // two accumulators of BN columns; allocations are powers of two of at least 32 columns
   static constexpr int ACC_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
                                 : 2 * BN <= 256 ? 256 : 512;
@@ -167,11 +170,44 @@ template <int BN, int SCHED, int EPI, bool F8, bool MX> struct EpiOf {
   static constexpr bool staged = OutPath<SCHED, EPI>::tma;
   static constexpr int slabs = (MX && BN == 256) ? 1 : EpiWidth<BN, SCHED, EPI, F8>::slabs;
 };
+// The router product (fp32 logits, bf16 operands) routes its tokens in the epilogue.
+template <int SCHED, int EPI, bool F8> struct RouterOf {
+  static constexpr bool on = SCHED == RAGGED_M && EPI == EPI_F32 && !F8;
+  // an mbarrier (64 bytes reserved), two tile histograms of MOE_MAX_EXPERTS ints, the logit bias
+  // and the selection bias (MOE_MAX_EXPERTS floats each), and every epilogue thread's 32 staged
+  // keys (rows of 33 words: a warp's stores of one key index fall in 32 distinct banks)
+  static constexpr int HIST_OFF = 64;
+  static constexpr int LBIAS_OFF = HIST_OFF + 2 * MOE_MAX_EXPERTS * 4;
+  static constexpr int SBIAS_OFF = LBIAS_OFF + MOE_MAX_EXPERTS * 4;
+  static constexpr int STG_OFF = SBIAS_OFF + MOE_MAX_EXPERTS * 4;
+  static constexpr int STG_LD = 33;
+  static constexpr int XTRA = on ? STG_OFF + BM * STG_LD * 4 : 0;
+};
 template <int BN, int SCHED, int EPI, bool F8, bool MX> struct CfgOf {
   using type = TileCfg<BN, EpiOf<BN, SCHED, EPI, F8, MX>::staged, EpiWidth<BN, SCHED, EPI, F8>::warps,
                        EpiOf<BN, SCHED, EPI, F8, MX>::slabs, MX ? MxCfg<BN>::SF_STAGE : 0,
                        MX ? (MxCfg<BN>::MAX_STAGES < 6 ? MxCfg<BN>::MAX_STAGES : 6) : 6,
-                       MX ? 512 : 0>;
+                       MX ? 512 : 0, RouterOf<SCHED, EPI, F8>::XTRA>;
+};
+
+// The router epilogue's logits of one token (this thread's TMEM lane), 32 experts at a time, as
+// the epilogue stores them (accumulator + logit bias); at(e) re-reads the stored value.
+struct TmemLogits {
+  uint32_t t_row;
+  const float* bias;   // the logit bias in shared memory (zero past E), or null
+  const float* row;    // this token's stored logits (null for a row past the tensor's end)
+  __device__ __forceinline__ void chunk(int q, float (&v)[32]) const {
+    uint32_t u[32];
+    ptx::tmem_ld32(t_row + static_cast<uint32_t>(q * 32), u);
+    ptx::tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(u[i]);
+    if (bias) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] += bias[q * 32 + i];
+    }
+  }
+  __device__ __forceinline__ float at(int e) const { return row ? row[e] : 0.f; }
 };
 
 struct KArgs {
@@ -200,6 +236,7 @@ struct KArgs {
   uint8_t* q_sf;           // MXFP8 SwiGLU forward: h block scales (activation layout)
   int kch;                 // MXFP8: 128-element K chunks of the operands
   int kch_out;             // MXFP8 SwiGLU forward: 128-element chunks of h's rows
+  RouterEpi rt;            // router top-k in the epilogue (rt.idx null: off)
   int* err;
 };
 
@@ -352,6 +389,15 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
   int* s_pre = s_off + (MAXG + 1);   // RAGGED_M: tile prefix; DYN: groups by row count
   volatile int* s_feed = s_pre + (MAXG + 1);
   const int* s_ord = DYN ? s_pre : nullptr;
+  // router epilogue: the histogram barrier (one arrival per epilogue warp) and two histograms
+  // (tiles alternate between them)
+  constexpr bool ROUTER = RouterOf<SCHED, EPI, F8>::on && !MX;
+  uint8_t* xtra = smem + C::RING + C::STAGING + C::SF_RING + C::AUX;
+  uint64_t* hbar = reinterpret_cast<uint64_t*>(xtra);
+  int* s_rhist = reinterpret_cast<int*>(xtra + RouterOf<SCHED, EPI, F8>::HIST_OFF);
+  float* s_lbias = reinterpret_cast<float*>(xtra + RouterOf<SCHED, EPI, F8>::LBIAS_OFF);
+  float* s_sbias = reinterpret_cast<float*>(xtra + RouterOf<SCHED, EPI, F8>::SBIAS_OFF);
+  unsigned* s_stg = reinterpret_cast<unsigned*>(xtra + RouterOf<SCHED, EPI, F8>::STG_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Tile walker: one per CTA (static walk), or tiles claimed at run time (DYN).
@@ -373,6 +419,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
       ptx::mbar_init(&tempty[i], EPI_WARPS);
     }
     for (int i = 0; i < EPI_WARPS; ++i) ptx::mbar_init(&epi_bar[i], 1);
+    if (ROUTER) ptx::mbar_init(hbar, EPI_WARPS);
     if (DYN) {
       for (int i = 0; i < FEED; ++i) {
         ptx::mbar_init(&feed_full[i], 1);
@@ -383,6 +430,13 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
     ptx::fence_barrier_init();
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmB);
+  }
+  if (ROUTER && p.rt.idx) {
+    for (int i = threadIdx.x; i < 2 * MOE_MAX_EXPERTS; i += blockDim.x) s_rhist[i] = 0;
+    for (int i = threadIdx.x; i < MOE_MAX_EXPERTS; i += blockDim.x) {
+      s_lbias[i] = (p.bias && i < p.N) ? p.bias[i] : 0.f;
+      s_sbias[i] = (p.rt.sel_bias && i < p.N) ? p.rt.sel_bias[i] : 0.f;
+    }
   }
   // Group table: row (RAGGED_M) or reduction (RAGGED_K) offsets, and for RAGGED_M the prefix
   // of per-group row-tile counts.
@@ -800,6 +854,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
     };
     int fslot = 0;
     uint32_t fphase = 0;
+    uint32_t hphase = 0;   // router: phase of the histogram barrier (tiles alternate buffers)
     for (int it = 0;; ++it) {
       int tile;
       if (DYN) {
@@ -1289,9 +1344,16 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
             } else {
               float* o = static_cast<float*>(p.out) + ti.g * p.out_group_stride + row * p.ldo + col;
               if ((p.ldo & 3) != 0 || (ncol & 3) != 0) {
-                // unaligned rows (e.g. router logits with E % 4 != 0): scalar stores
-                for (int i = 0; i < ncol; ++i)
-                  o[i] = __uint_as_float(v32[i]) + (p.bias ? p.bias[col + i] : 0.f);
+                // unaligned rows (e.g. router logits with E % 4 != 0): scalar stores (unrolled,
+                // so that v32 stays in registers)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  if (i < ncol) {
+                    float fv = __uint_as_float(v32[i]);
+                    if (p.bias) fv += p.bias[col + i];
+                    o[i] = fv;
+                  }
+                }
                 continue;
               }
 #pragma unroll
@@ -1316,10 +1378,58 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
         const float m = warp_max(hmax);   // non-negative floats order like their bit patterns
         if (lane == 0 && m > 0.f) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), __float_as_uint(m));
       }
+      // Router: this thread's token -- selection, gates and its experts' counts for the tile's
+      // histogram row.  The whole warp reads tensor memory (tcgen05.ld is warp-collective); only
+      // rows inside the tensor are written.
+      int rsel[MOE_MAX_TOPK];
+      if (ROUTER && p.rt.idx && rows_here > 0) {
+        TmemLogits src;
+        src.t_row = t_row;
+        src.bias = p.bias ? s_lbias : nullptr;
+        src.row = valid ? static_cast<const float*>(p.out) + row * p.ldo : nullptr;
+        rrow::Rule rule;
+        rule.E = p.N;
+        rule.k = p.rt.k;
+        rule.score_fn = p.rt.score_fn;
+        rule.renorm = p.rt.renorm;
+        rule.sel_bias = p.rt.sel_bias ? s_sbias : nullptr;
+        float rg[MOE_MAX_TOPK];
+        rrow::route_row<MOE_MAX_TOPK>(src, rule, s_stg + r * RouterOf<SCHED, EPI, F8>::STG_LD,
+                                      rsel, rg);
+        if (valid) {
+#pragma unroll
+          for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+            if (j < p.rt.k) {
+              p.rt.idx[static_cast<int64_t>(row) * p.rt.k + j] = rsel[j];
+              p.rt.gate[static_cast<int64_t>(row) * p.rt.k + j] = rg[j];
+            }
+          }
+        }
+      }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
       if (aborted) break;
+      if (ROUTER && p.rt.idx) {
+        // the tile's histogram row: every epilogue warp adds its tokens' experts, arrives, and
+        // after all four have arrived writes a quarter of the row and clears it for the tile
+        // after next (which uses this buffer again only after the next tile's arrivals)
+        int* h = s_rhist + (it & 1) * MOE_MAX_EXPERTS;
+        if (rows_here > 0 && valid) {
+#pragma unroll
+          for (int j = 0; j < MOE_MAX_TOPK; ++j)
+            if (j < p.rt.k) atomicAdd(&h[rsel[j]], 1);
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(hbar);
+        if (!ptx::mbar_wait(hbar, hphase, abort_flag, p.err)) break;
+        hphase ^= 1u;
+        uint8_t* hrow = p.rt.hist + static_cast<int64_t>(ti.mt) * p.rt.ldh;
+        for (int x = e * 32 + lane; x < p.rt.ldh; x += EPI_WARPS * 32) {
+          hrow[x] = static_cast<uint8_t>(x < p.N ? h[x] : 0);
+          if (x < MOE_MAX_EXPERTS) h[x] = 0;
+        }
+      }
       if (NACC == 2) acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -1868,6 +1978,19 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   a.q_sf = g.q_sf;
   a.kch = static_cast<int>(mx_kch(g.K));
   a.kch_out = static_cast<int>(mx_kch(EPI == EPI_SWIGLU_BWD ? 2 * static_cast<int64_t>(g.f) : g.f));
+  a.rt = g.rt;
+  if (g.rt.idx) {
+    const bool ok = RouterOf<SCHED, EPI, F8>::on && !MX && g.G == 1 && !g.offsets && g.N <= BN &&
+                    g.N <= MOE_MAX_EXPERTS && g.rt.gate && g.rt.hist && g.rt.k >= 1 &&
+                    g.rt.k <= MOE_MAX_TOPK && g.rt.k <= g.N && g.rt.ldh >= g.N &&
+                    g.ldo == g.N;
+    if (!ok) {
+      set_error("%s: the router epilogue needs one group of fp32 logits whose E columns fit one "
+                "tile, k in [1, min(E, %d)] and its idx, gate and histogram buffers", name,
+                MOE_MAX_TOPK);
+      return MOE_ERR_INVALID_ARG;
+    }
+  }
   if (F8 && !MX && (!g.a_scale || !g.b_scale)) {
     set_error("%s: FP8 operands need their scales", name);
     return MOE_ERR_INVALID_ARG;

@@ -83,25 +83,44 @@ int launch_clusters(const char* name, void (*kern)(KArgs...), dim3 grid, dim3 bl
   } while (0)
 
 // ------------------------------------------------------------------ routing (route.cu)
+// Balancing-loss partial sums: one block per 256 tokens.
 constexpr int ROUTE_TOK_PER_BLOCK = 256;
 inline int route_blocks(int T) { return (T + ROUTE_TOK_PER_BLOCK - 1) / ROUTE_TOK_PER_BLOCK; }
 
-// sel_bias: selection-only expert bias [E] (keys = score + bias) or null (keys = logits).
+// Expert histogram: one row per 128 tokens (a router GEMM row tile), one byte per expert (a row
+// counts at most 128 tokens), rows of route_ldh(E) bytes (E rounded up to a power of two of at
+// least 16, so that a row is whole 16-byte chunks and a warp covers whole rows).
+constexpr int ROUTE_HIST_TOK = 128;
+constexpr int ROUTE_SLOT_TOK = 256;          // tokens per block of the slots kernel
+// Largest histogram every slots block reads whole; past it a scan kernel forms the per-row
+// prefixes first (into rowpre: E * route_rows(T) int32).
+constexpr int64_t ROUTE_DIRECT_BYTES = 131072;
+inline int route_rows(int T) { return (T + ROUTE_HIST_TOK - 1) / ROUTE_HIST_TOK; }
+inline int route_ldh(int E) {
+  int l = 16;
+  while (l < E) l <<= 1;
+  return l;
+}
+inline int64_t route_hist_bytes(int T, int E) {
+  return static_cast<int64_t>(route_rows(T)) * route_ldh(E);
+}
+inline bool route_hist_direct(int T, int E) { return route_hist_bytes(T, E) <= ROUTE_DIRECT_BYTES; }
+
+// Per-token selection and gates (sel_bias: selection-only expert bias [E], keys = score + bias;
+// null: keys = logits), and the histogram rows.
 int launch_topk(const float* logits, int T, int E, int k, int score_fn, int renorm,
-                const float* sel_bias, int32_t* idx, float* gate, int32_t* hist, cudaStream_t st);
+                const float* sel_bias, int32_t* idx, float* gate, uint8_t* hist, cudaStream_t st);
 // Load-balancing loss; partial: route_blocks(T) * E floats of scratch.
 int launch_aux_loss(const float* logits, const int32_t* counts, int T, int E, int k, int score_fn,
                     float coeff, float* partial, float* out, cudaStream_t st);
 int launch_bias_update(const int32_t* counts, float* bias, int T, int k, int E, float rate,
                        cudaStream_t st);
-// Per expert: exclusive prefix of its row of hist (base[e][b], from the expert's first slot) and
-// counts[e].
-int launch_scan(const int32_t* hist, int E, int nblk, int32_t* base, int32_t* counts,
-                cudaStream_t st);
-// offsets (the exclusive scan of counts, E+1 entries) and both slot maps.
-int launch_slots(const int32_t* idx, int T, int k, int E, const int32_t* base,
-                 const int32_t* counts, int32_t* offsets, int32_t* slot_of_pair,
-                 int32_t* token_of_slot, cudaStream_t st);
+// counts, offsets (the exclusive scan of counts, E+1 entries) and both slot maps from the
+// histogram and idx.  rowpre (E * route_rows(T) int32) is used only when the histogram is larger
+// than ROUTE_DIRECT_BYTES (may be null otherwise).
+int launch_slots(const int32_t* idx, int T, int k, int E, const uint8_t* hist, int32_t* rowpre,
+                 int32_t* counts, int32_t* offsets, int32_t* slot_of_pair, int32_t* token_of_slot,
+                 cudaStream_t st);
 
 // ------------------------------------------------------------------ row kernels (rowops.cu)
 int launch_permute(int dtype, const void* x, const int32_t* slot_of_pair, void* x_perm, int T,
@@ -158,6 +177,16 @@ struct Operand {
   bool mn_major;
 };
 
+// The router GEMM's epilogue routes its tokens: idx and gate [T, k] and the expert histogram
+// rows of its row tiles (hist: [route_rows(T)][ldh] bytes), as launch_topk would from the logits.
+struct RouterEpi {
+  int32_t* idx;
+  float* gate;
+  uint8_t* hist;
+  const float* sel_bias;   // selection-only expert bias [E] or null
+  int k, score_fn, renorm, ldh;
+};
+
 struct GemmDesc {
   const char* name;        // trace name (kernel kind) of this product
   int sched;
@@ -198,6 +227,9 @@ struct GemmDesc {
   // layout, row tiles as this product's); `out` (bf16 h) and `out2` ([a | u]) may be null.
   uint8_t* q_out;
   uint8_t* q_sf;
+  // Router top-k in the epilogue (RAGGED_M fp32 logits, bf16 operands, E <= the tile's width so
+  // that one column tile holds a token's every logit): rt.idx null = off.
+  RouterEpi rt;
 };
 
 // ------------------------------------------------------------------ MXFP8 packed scales
@@ -238,7 +270,7 @@ int validate_ptr(const void* p, const char* name, bool required);
 int route_stages(const moe_cfg* c, const void* x, const void* W_r, const float* b_r,
                  const float* logits_in, float* logits_out, int32_t* idx, float* gate,
                  int32_t* counts, int32_t* offsets, int32_t* slot_of_pair, int32_t* token_of_slot,
-                 int32_t* hist, int32_t* base, cudaStream_t st);
+                 uint8_t* hist, int32_t* rowpre, cudaStream_t st);
 
 // E4M3 tensorwise quantisation of `groups` blocks of per_group bf16 values (fp8.cu).
 int launch_quantize_e4m3(const void* x, int64_t per_group, int groups, uint8_t* q, float* scale,

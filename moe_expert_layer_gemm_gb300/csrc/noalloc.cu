@@ -16,20 +16,22 @@
 
 namespace moe {
 
-// Two int32 tables of E * ceil(T / 256) entries each (512 KB in all).  Every GPU that loads the
-// library holds this array until the process exits.
-constexpr int NOALLOC_ROUTE_MAX_ENTRIES = 65536;
-static __device__ __align__(256) int32_t g_route_scratch[2 * NOALLOC_ROUTE_MAX_ENTRIES];
+// The expert histogram: ceil(T / 128) rows of route_ldh(E) bytes (E rounded up to a power of two
+// of at least 16), 128 KB at most -- the size the slots kernel reads whole, so these calls never
+// need the larger histograms' row-prefix table.  Every GPU that loads the library holds this
+// array until the process exits.
+constexpr int NOALLOC_ROUTE_MAX_BYTES = static_cast<int>(ROUTE_DIRECT_BYTES);
+static __device__ __align__(256) uint8_t g_route_scratch[NOALLOC_ROUTE_MAX_BYTES];
 
 static SymbolCache g_scratch_sym;
 
 // Device address of the array in the current device's context: looked up (cudaGetSymbolAddress)
 // on the first call on a device, and again whenever the device's context has changed since (a
 // cudaDeviceReset in between), so the kernels never receive a stale address.
-static int route_scratch(int32_t** out) {
+static int route_scratch(uint8_t** out) {
   void* p = nullptr;
   MOE_TRY(symbol_address(g_route_scratch, &g_scratch_sym, &p, "moe_route_topk_noalloc"));
-  *out = static_cast<int32_t*>(p);
+  *out = static_cast<uint8_t*>(p);
   return MOE_OK;
 }
 
@@ -48,11 +50,12 @@ extern "C" int moe_route_topk_noalloc(const moe_cfg* c, const void* x, const voi
               "logits need a caller buffer)");
     return MOE_ERR_INVALID_ARG;
   }
-  const int64_t entries = static_cast<int64_t>(c->E) * route_blocks(c->T);
-  if (entries > NOALLOC_ROUTE_MAX_ENTRIES) {
-    set_error("moe_route_topk_noalloc: E * ceil(T/256) = %lld exceeds the built-in scratch of "
-              "%d entries (e.g. T=65536 with E=256); use moe_route_topk with a workspace",
-              static_cast<long long>(entries), NOALLOC_ROUTE_MAX_ENTRIES);
+  const int64_t bytes = route_hist_bytes(c->T, c->E);
+  if (bytes > NOALLOC_ROUTE_MAX_BYTES) {
+    set_error("moe_route_topk_noalloc: ceil(T/128) * E16 = %lld (E16: E rounded up to a power "
+              "of two, at least 16) exceeds the built-in scratch of %d bytes (e.g. T=65536 with "
+              "E=256); use moe_route_topk with a workspace",
+              static_cast<long long>(bytes), NOALLOC_ROUTE_MAX_BYTES);
     return MOE_ERR_UNSUPPORTED;
   }
   MOE_TRY(validate_ptr(x, "x", !logits_in));
@@ -75,12 +78,10 @@ extern "C" int moe_route_topk_noalloc(const moe_cfg* c, const void* x, const voi
     }
     return MOE_OK;
   }
-  int32_t* scratch = nullptr;
-  MOE_TRY(route_scratch(&scratch));
-  // hist and base are written in full by the histogram and scan kernels before they are read,
-  // so the array needs no clearing between calls.
-  int32_t* hist = scratch;
-  int32_t* base = scratch + NOALLOC_ROUTE_MAX_ENTRIES;
+  uint8_t* hist = nullptr;
+  MOE_TRY(route_scratch(&hist));
+  // every histogram row is written in full (by the top-k kernel or the router GEMM) before the
+  // slots kernel reads it, so the array needs no clearing between calls
   return route_stages(c, x, W_r, b_r, logits_in, logits_out, idx, gate, counts, offsets,
-                      slot_of_pair, token_of_slot, hist, base, st);
+                      slot_of_pair, token_of_slot, hist, nullptr, st);
 }

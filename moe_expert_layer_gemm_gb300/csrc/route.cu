@@ -1,4 +1,4 @@
-// Routing: top-k selection + gates, per-expert histogram, prefix sum, token<->slot maps.
+// Routing: top-k selection + gates, per-expert histogram, prefix sums, token<->slot maps.
 //
 // "Megatron-Bridge 深度剖析", §Expert Parallel 基础 (workflow figure, Step 1: the router
 // picks the top-k experts of every token; Step 2: tokens are regrouped by expert).  On one GPU
@@ -6,244 +6,141 @@
 //   counts[e], offsets[e] = sum_{e'<e} counts[e'],
 //   slot(t, j) = offsets[e] + #{t' < t : t' picked e},  e = idx[t, j].
 //
-// Four launches:
-//   topk  -- one warp per token (grid-stride over all tokens): k rounds of a warp-wide max
-//            (fp32 key, ties to the lower expert index), gates in fp32, lane j computing pair
-//            j's.  The key is the logit,
-//            or, with a selection-only expert bias ("Megatron-Bridge 深度剖析",
-//            §Nemotron-3-Nano 配置: sigmoid routing with expert-bias correction as in DeepSeek
-//            V3), the fp32 score (softmax over E, or sigmoid) plus the expert's bias.
-//   hist  -- one block per 256 tokens: per-expert counts of the block, hist[e][block].
-//   scan  -- one block per expert: the exclusive prefix of its row of hist (the first slot of
-//            each block's tokens of that expert, counted from the expert's first slot) and
-//            its count.
-//   slots -- per block: offsets = the exclusive scan of counts (formed by every block, written
-//            out by block 0); per-expert bitmasks of the block's tokens; the rank of token t
-//            among the block's tokens of expert e is the popcount of the mask bits below t.
-// All integer, so the result is exact and independent of scheduling.
+// Two launches (or, with bf16 operands, one plus the router GEMM, whose epilogue does the
+// first one's work on the accumulator):
+//   topk  -- one thread per token (route_row.cuh): selection keys, the k best in (key desc,
+//            expert asc) order, gates in fp32; one block per 128 tokens also writes the block's
+//            row of the expert histogram hist[row][e] (bytes: a row counts at most 128 tokens).
+//   slots -- one block per 256 tokens, in clusters of 8.  A cluster reads the whole histogram
+//            (it is small: T/128 rows of E bytes), each block an eighth, and shares the sums
+//            through distributed shared memory: every block gets each expert's total and the
+//            count of its tokens in earlier blocks; block 0 writes counts and offsets.  Per-expert
+//            bitmasks of the block's tokens then give each token's rank among the block's tokens
+//            of its expert, and the block writes its pairs' slots and its slots' tokens as
+//            contiguous runs.
+// Where the histogram is larger than ROUTE_DIRECT_BYTES, a scan kernel forms those per-block
+// prefixes and the totals first (three launches).  All integer, so the result is exact and
+// independent of scheduling.
 #include <limits.h>
 
 #include "common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
+#include "route_row.cuh"
 
 namespace moe {
 
-constexpr int TPB = ROUTE_TOK_PER_BLOCK;   // tokens per histogram / slot block
-constexpr int MASK_WORDS = TPB / 32;        // 8 words of 32 token bits per expert
+constexpr int HT = ROUTE_HIST_TOK;            // tokens per histogram row (128)
+constexpr int ST = ROUTE_SLOT_TOK;            // tokens per slots block (256)
+constexpr int SWORDS = ST / 32;               // 32-token mask words per expert in a slots block
+constexpr int SWARPS = ST / 32;               // warps of a slots block
+static_assert(SWORDS <= 32 && (SWORDS & (SWORDS - 1)) == 0, "mask words per expert: a power of two");
 constexpr int MAXK = MOE_MAX_TOPK;
-#define NEG_INF __int_as_float(0xff800000u)
+constexpr int SCL = 8;                        // slots blocks per cluster
+constexpr int SOWN = SCL * (ST / HT);         // histogram rows of a cluster's own tokens
+constexpr int TPB = ROUTE_TOK_PER_BLOCK;   // tokens per block of the balancing-loss sums
 
-template <int EPL>
-__device__ __forceinline__ void load_logit_row(const float* __restrict__ logits, int t, int T,
-                                               int E, int lane, float (&v)[EPL]) {
+// logits of one token from global memory (fp32 rows of E; 16-byte loads when rows are aligned)
+struct GlobalRow {
+  const float* row;
+  int E;
+  bool vec;
+  __device__ __forceinline__ void chunk(int q, float (&v)[32]) const {
+    const int e0 = q * 32;
+    if (vec) {
 #pragma unroll
-  for (int q = 0; q < EPL; ++q) {
-    const int e = q * 32 + lane;
-    v[q] = (t < T && e < E) ? __ldg(logits + static_cast<int64_t>(t) * E + e) : NEG_INF;
-  }
-}
-
-// A float as an unsigned integer with the same order (for single-instruction warp reductions);
-// -0 becomes +0 first, so that the two zeros tie as they compare equal.
-__device__ __forceinline__ unsigned ordered_key(float f) {
-  unsigned b = __float_as_uint(f);
-  if (b == 0x80000000u) b = 0u;
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-// Sum over lanes 0..7 (k <= 8 pairs live there, the other lanes hold zeros), result in lane 0
-// and every lane of its group of eight.  The same value as a full-warp butterfly over those
-// lanes: the skipped steps would only add zeros.
-__device__ __forceinline__ float sum8(float v) {
-#pragma unroll
-  for (int o = 4; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-template <int EPL>
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E,
-                                                   int k, int score_fn, int renorm,
-                                                   const float* __restrict__ sel_bias,
-                                                   int32_t* __restrict__ idx,
-                                                   float* __restrict__ gate, int* err) {
-  const int lane = threadIdx.x & 31;
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nw = (gridDim.x * blockDim.x) >> 5;
-  float cur[EPL], nxt[EPL], bias[EPL];
-  load_logit_row<EPL>(logits, gw, T, E, lane, cur);
-#pragma unroll
-  for (int q = 0; q < EPL; ++q) {
-    const int e = q * 32 + lane;
-    bias[q] = (sel_bias && e < E) ? __ldg(sel_bias + e) : 0.f;
-  }
-
-  for (int t = gw; t < T; t += nw) {
-    load_logit_row<EPL>(logits, t + nw, T, E, lane, nxt);   // next token's row in flight
-
-    // ---- selection keys: the logits, or score + expert bias (row max kept for the gates)
-    float key[EPL];
-    float rmax = NEG_INF;
-    if (sel_bias) {
-      if (score_fn == MOE_SCORE_SOFTMAX) {
-#pragma unroll
-        for (int q = 0; q < EPL; ++q) rmax = fmaxf(rmax, cur[q]);
-        rmax = warp_max(rmax);
-        float ex[EPL], part = 0.f;
-#pragma unroll
-        for (int q = 0; q < EPL; ++q) {
-          ex[q] = (q * 32 + lane < E) ? expf(cur[q] - rmax) : 0.f;
-          part += ex[q];
+      for (int i = 0; i < 8; ++i) {
+        if (e0 + 4 * i < E) {
+          const float4 f = __ldg(reinterpret_cast<const float4*>(row + e0) + i);
+          v[4 * i] = f.x;
+          v[4 * i + 1] = f.y;
+          v[4 * i + 2] = f.z;
+          v[4 * i + 3] = f.w;
         }
-        const float z = warp_sum(part);
-#pragma unroll
-        for (int q = 0; q < EPL; ++q)
-          key[q] = (q * 32 + lane < E) ? ex[q] / z + bias[q] : NEG_INF;
-      } else {
-#pragma unroll
-        for (int q = 0; q < EPL; ++q)
-          key[q] = (q * 32 + lane < E) ? sigmoid_f(cur[q]) + bias[q] : NEG_INF;
       }
     } else {
 #pragma unroll
-      for (int q = 0; q < EPL; ++q) key[q] = cur[q];
+      for (int i = 0; i < 32; ++i)
+        if (e0 + i < E) v[i] = __ldg(row + e0 + i);
     }
-
-    // ---- selection: k rounds of a warp-wide max, order (key desc, expert asc).  Each lane first
-    // sorts its EPL (key, expert) pairs, so a round compares only the lanes' heads: the largest
-    // key, then the lowest expert among the lanes holding it -- two single-instruction warp
-    // reductions (redux.sync) on the keys as order-preserving integers.  The winning lane moves
-    // on to its next pair.
-    unsigned hk[EPL];
-    int he[EPL];
-#pragma unroll
-    for (int q = 0; q < EPL; ++q) {
-      const int e = q * 32 + lane;
-      // a NaN key (outside the inputs' contract) ranks as -inf, so every round still has a
-      // maximum that some lane holds and the selection stays within [0, E)
-      hk[q] = ordered_key((e < E && key[q] == key[q]) ? key[q] : NEG_INF);
-      he[q] = e < E ? e : INT_MAX;
-    }
-#pragma unroll
-    for (int i = 1; i < EPL; ++i)          // insertion sort, (key desc, expert asc)
-#pragma unroll
-      for (int q = i; q > 0; --q)
-        if (hk[q] > hk[q - 1] || (hk[q] == hk[q - 1] && he[q] < he[q - 1])) {
-          const unsigned tk = hk[q];
-          hk[q] = hk[q - 1];
-          hk[q - 1] = tk;
-          const int te = he[q];
-          he[q] = he[q - 1];
-          he[q - 1] = te;
-        }
-    int my_e = 0;                          // lane j: the j-th selected expert
-#pragma unroll
-    for (int j = 0; j < MAXK; ++j) {
-      if (j < k) {
-        const unsigned m = __reduce_max_sync(0xffffffffu, hk[0]);
-        const int e = __reduce_min_sync(0xffffffffu, hk[0] == m ? he[0] : INT_MAX);
-        if (lane == j) my_e = e;
-        if ((e & 31) == lane) {            // the winner drops its head
-#pragma unroll
-          for (int q = 0; q + 1 < EPL; ++q) {
-            hk[q] = hk[q + 1];
-            he[q] = he[q + 1];
-          }
-          hk[EPL - 1] = 0u;   // below every key (-inf is 0x007FFFFF)
-          he[EPL - 1] = INT_MAX;
-        }
-      }
-    }
-
-    // ---- gates (fp32), lane j for pair j: the selected expert's logit (in L1 from the row load)
-    if (lane < k && (my_e < 0 || my_e >= E)) {   // cannot happen; never index with it
-      record_error(err, DEVERR_BAD_EXPERT);
-      my_e = 0;
-    }
-    const float lv = lane < k ? __ldg(logits + static_cast<int64_t>(t) * E + my_e) : NEG_INF;
-    float g;
-    if (score_fn == MOE_SCORE_SOFTMAX) {
-      // shift: the row maximum (over all E without renorm, over the selected with it); without
-      // a selection bias the top-1 logit is both
-      float m;
-      if (!sel_bias) m = __shfl_sync(0xffffffffu, lv, 0);
-      else if (renorm) m = __shfl_sync(0xffffffffu, warp_max(lv), 0);
-      else m = rmax;
-      const float ex = lane < k ? expf(lv - m) : 0.f;
-      float denom;
-      if (renorm) {
-        denom = sum8(ex);   // pairs live in lanes 0..k-1
-      } else {
-        float part = 0.f;
-#pragma unroll
-        for (int q = 0; q < EPL; ++q)
-          if (q * 32 + lane < E) part += expf(cur[q] - m);
-        denom = warp_sum(part);
-      }
-      denom = __shfl_sync(0xffffffffu, denom, 0);   // one value for every lane
-      g = ex * (1.0f / denom);
-    } else {
-      g = lane < k ? sigmoid_f(lv) : 0.f;
-      if (renorm) {
-        const float sum = __shfl_sync(0xffffffffu, sum8(g), 0);
-        g *= 1.0f / sum;
-      }
-    }
-
-    // ---- outputs: lane j writes pair j
-    if (lane < k) {
-      idx[static_cast<int64_t>(t) * k + lane] = my_e;
-      gate[static_cast<int64_t>(t) * k + lane] = g;
-    }
-#pragma unroll
-    for (int q = 0; q < EPL; ++q) cur[q] = nxt[q];
   }
-}
+  __device__ __forceinline__ float at(int e) const { return __ldg(row + e); }
+};
 
-// Per-block expert counts: hist[e][b] = number of tokens of block b (256 tokens) that picked e.
-__global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ idx, int T, int k,
-                                                   int E, int32_t* __restrict__ hist, int nblk,
-                                                   int* err) {
+// One thread per token, one block per histogram row.  KL: the selection list's length (>= k).
+template <int KL>
+__global__ void __launch_bounds__(HT) topk_kernel(const float* __restrict__ logits, int T, int E,
+                                                  int k, int score_fn, int renorm,
+                                                  const float* __restrict__ sel_bias,
+                                                  int32_t* __restrict__ idx,
+                                                  float* __restrict__ gate,
+                                                  uint8_t* __restrict__ hist, int ldh, int* err) {
   __shared__ int cnt[MOE_MAX_EXPERTS];
+  __shared__ unsigned stg[HT * 33];   // each thread's staged keys (rows of 33: no bank conflicts)
+  __shared__ float sbias[MOE_MAX_EXPERTS];
   const int tid = threadIdx.x;
-  for (int i = tid; i < E; i += blockDim.x) cnt[i] = 0;
+  for (int e = tid; e < E; e += HT) {
+    cnt[e] = 0;
+    sbias[e] = sel_bias ? sel_bias[e] : 0.f;
+  }
   __syncthreads();
-  const int t = blockIdx.x * TPB + tid;
+  const int t = blockIdx.x * HT + tid;
   if (t < T) {
-    for (int j = 0; j < k; ++j) {
-      const int e = idx[static_cast<int64_t>(t) * k + j];
-      if (e < 0 || e >= E) record_error(err, DEVERR_BAD_EXPERT);
-      else atomicAdd(&cnt[e], 1);
+    GlobalRow src;
+    src.row = logits + static_cast<int64_t>(t) * E;
+    src.E = E;
+    src.vec = (E & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
+    rrow::Rule r;
+    r.E = E;
+    r.k = k;
+    r.score_fn = score_fn;
+    r.renorm = renorm;
+    r.sel_bias = sel_bias ? sbias : nullptr;
+    int sel[KL];
+    float g[KL];
+    rrow::route_row<KL>(src, r, stg + tid * 33, sel, g);
+#pragma unroll
+    for (int j = 0; j < KL; ++j) {
+      if (j < k) {
+        int e = sel[j];
+        if (e < 0 || e >= E) {   // cannot happen; never index with it
+          record_error(err, DEVERR_BAD_EXPERT);
+          e = 0;
+        }
+        idx[static_cast<int64_t>(t) * k + j] = e;
+        gate[static_cast<int64_t>(t) * k + j] = g[j];
+        atomicAdd(&cnt[e], 1);
+      }
     }
   }
   __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) hist[static_cast<int64_t>(e) * nblk + blockIdx.x] = cnt[e];
+  for (int e = tid; e < ldh; e += HT)
+    hist[static_cast<int64_t>(blockIdx.x) * ldh + e] = static_cast<uint8_t>(e < E ? cnt[e] : 0);
 }
 
-// Per expert e (one block each): the exclusive prefix of hist[e][0..nblk) -- the first slot of
-// block b's tokens of expert e, counted from the expert's first slot -- and the row total
-// counts[e].  Each thread takes 8 consecutive entries; a block-wide scan of the threads' sums
-// gives their starts.  The experts' own offsets are the scan of counts, which every slots block
-// forms itself (it needs all of them).
+// Large histograms only: per expert e (one block each), rowpre[e][r] = the exclusive prefix of
+// hist[.][e] over rows (the expert's tokens in rows before r) and counts[e] = the column total.
+// Each thread takes 8 consecutive rows; a block-wide scan of the threads' sums gives their starts.
 constexpr int RSCAN_THREADS = 256;
 constexpr int RSCAN_PER = 8;
 
-__global__ void __launch_bounds__(RSCAN_THREADS) row_scan_kernel(const int32_t* __restrict__ hist,
-                                                                 int nblk,
+__global__ void __launch_bounds__(RSCAN_THREADS) col_scan_kernel(const uint8_t* __restrict__ hist,
+                                                                 int ldh, int nrows,
                                                                  int32_t* __restrict__ rowpre,
                                                                  int32_t* __restrict__ counts) {
   __shared__ int warp_tot[RSCAN_THREADS / 32];
   __shared__ int chunk_tot;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int32_t* row = hist + static_cast<int64_t>(blockIdx.x) * nblk;
-  int32_t* out = rowpre + static_cast<int64_t>(blockIdx.x) * nblk;
+  const int e = blockIdx.x;
+  int32_t* out = rowpre + static_cast<int64_t>(e) * nrows;
   int carry = 0;
-  for (int c0 = 0; c0 < nblk; c0 += RSCAN_THREADS * RSCAN_PER) {
+  for (int c0 = 0; c0 < nrows; c0 += RSCAN_THREADS * RSCAN_PER) {
     const int i0 = c0 + tid * RSCAN_PER;
     int v[RSCAN_PER];
     int local = 0;
 #pragma unroll
     for (int i = 0; i < RSCAN_PER; ++i) {
-      v[i] = i0 + i < nblk ? row[i0 + i] : 0;
+      v[i] = i0 + i < nrows ? hist[static_cast<int64_t>(i0 + i) * ldh + e] : 0;
       local += v[i];
     }
     int incl = local;
@@ -267,91 +164,340 @@ __global__ void __launch_bounds__(RSCAN_THREADS) row_scan_kernel(const int32_t* 
     int run = carry + warp_tot[warp] + incl - local;
 #pragma unroll
     for (int i = 0; i < RSCAN_PER; ++i) {
-      if (i0 + i < nblk) out[i0 + i] = run;
+      if (i0 + i < nrows) out[i0 + i] = run;
       run += v[i];
     }
     carry += chunk_tot;
     __syncthreads();   // warp_tot and chunk_tot are rewritten by the next chunk
   }
-  if (tid == 0) counts[blockIdx.x] = carry;
+  if (tid == 0) counts[e] = carry;
 }
 
-__global__ void __launch_bounds__(256) slots_kernel(const int32_t* __restrict__ idx, int T, int k,
-                                                    int E, const int32_t* __restrict__ rowpre,
-                                                    const int32_t* __restrict__ counts,
-                                                    int32_t* __restrict__ offsets, int nblk,
-                                                    int32_t* __restrict__ slot_of_pair,
-                                                    int32_t* __restrict__ token_of_slot,
-                                                    int* err) {
-  __shared__ uint32_t mask[MOE_MAX_EXPERTS * MASK_WORDS];
-  __shared__ int s_off[MOE_MAX_EXPERTS + 1];
-  const int tid = threadIdx.x;
-  for (int i = tid; i < E * MASK_WORDS; i += blockDim.x) mask[i] = 0u;
-  if (tid < 32) {
-    // offsets = exclusive scan of counts (E <= 256: 8 experts per lane, in expert order)
-    constexpr int PER = MOE_MAX_EXPERTS / 32;
-    int v[PER];
-    int local = 0;
+// 32 x 32 bit matrix, row i in lane i (bit b = column b), transposed: lane i receives column i.
+// Five rounds swap the off-diagonal blocks of size 16, 8, 4, 2, 1 between lane pairs.
+__device__ __forceinline__ uint32_t transpose32(uint32_t x, int lane) {
+  const uint32_t lo_mask[5] = {0x0000ffffu, 0x00ff00ffu, 0x0f0f0f0fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+  for (int s = 0; s < 5; ++s) {
+    const int j = 16 >> s;
+    const uint32_t m = lo_mask[s];
+    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, j);
+    x = (lane & j) ? ((x & ~m) | ((y & ~m) >> j)) : ((x & m) | ((y & m) << j));
+  }
+  return x;
+}
+
+// Shared memory of a slots block: phase 1 (the histogram's column sums) and phase 2 (the token
+// bitmasks and their per-word prefix counts) use the same bytes.
+struct SlotsSmem {
+  int cpart[2][MOE_MAX_EXPERTS];   // this CTA's share of the sums before / after the cluster's rows
+  int pre[MOE_MAX_EXPERTS];        // the expert's tokens in earlier blocks
+  int off[MOE_MAX_EXPERTS + 1];    // offsets (exclusive scan of the totals)
+  int boff[MOE_MAX_EXPERTS];       // the expert's first pair in the block's expert order
+  int gbase[MOE_MAX_EXPERTS];      // global slot of block-order position p: gbase[e] + p
+  union {
+    int part[SWARPS][2][MOE_MAX_EXPERTS];   // per warp: sums over rows before / from the block's
+    struct {
+      // bit i of word w: token 32w + i picked e (rows padded by one word: a warp's stores of
+      // 32 experts' words fall in distinct banks)
+      uint32_t mask[MOE_MAX_EXPERTS][SWORDS + 1];
+      int wpre[MOE_MAX_EXPERTS][SWORDS];        // tokens of e in words before w
+    } m;
+  } u;
+  int sop[ST * MAXK];              // the block's slot_of_pair, as it lies in memory
+  int tok[ST * MAXK];              // the block's pairs in expert order: token ...
+  uint8_t ex[ST * MAXK];           // ... and expert
+};
+
+// rowpre/counts_in: null (the block sums the histogram itself) or the scan kernel's results.
+__global__ void __launch_bounds__(ST) slots_kernel(const int32_t* __restrict__ idx, int T, int k,
+                                                   int E, const uint8_t* __restrict__ hist,
+                                                   int ldh, int nrows,
+                                                   const int32_t* __restrict__ rowpre,
+                                                   const int32_t* __restrict__ counts_in,
+                                                   int32_t* __restrict__ counts,
+                                                   int32_t* __restrict__ offsets,
+                                                   int32_t* __restrict__ slot_of_pair,
+                                                   int32_t* __restrict__ token_of_slot, int* err) {
+  __shared__ SlotsSmem sm;
+  __shared__ int wsum[SWARPS];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r0 = blockIdx.x * (ST / HT);   // this block's first histogram row
+  // this thread's token's experts, loaded first so that their latency overlaps the sums below
+  const int t = blockIdx.x * ST + tid;
+  int ev[MAXK];
+#pragma unroll
+  for (int j = 0; j < MAXK; ++j)
+    ev[j] = (j < k && t < T) ? __ldg(idx + static_cast<int64_t>(t) * k + j) : -1;
+  if (!rowpre) {
+    // ---- column sums of the histogram, split over the cluster: the rows before the cluster's
+    // own (P) and after them (Q) are read by the cluster's SCL blocks in turn, each block sums its
+    // rows, and every block then adds all SCL shares (distributed shared memory, fixed order);
+    // the SOWN rows of the cluster's own tokens each block reads itself.
+    // Lane -> 16-byte chunk c of a row (cpr chunks per row, a power of two) and one of the 32/cpr
+    // rows a warp instruction covers.
+    const int crank = static_cast<int>(ptx::cluster_ctarank());
+    const int R0 = (blockIdx.x - crank) * (ST / HT);   // the cluster's first row
+    const int cpr = ldh >> 4, rpi = 32 / cpr;
+    const int c = lane & (cpr - 1), rsub = lane / cpr;
+    // bytes summed in 16-bit lanes (a lane's rows count at most 32 x 128 tokens in a histogram
+    // of ROUTE_DIRECT_BYTES): word x of a chunk holds experts 4x..4x+3; its even bytes go to
+    // *_ev[x], its odd ones to *_od[x]
+    uint32_t lo_ev[4], lo_od[4], hi_ev[4], hi_od[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) lo_ev[x] = lo_od[x] = hi_ev[x] = hi_od[x] = 0u;
+    const int step = SCL * SWARPS * rpi;
+    const uint4* h4 = reinterpret_cast<const uint4*>(hist) + c;
+    const int ld4 = ldh >> 4;
+    int r = (crank * SWARPS + warp) * rpi + rsub;
+#pragma unroll 4
+    for (; r < nrows && r < R0; r += step) {
+      const uint4 w = __ldg(h4 + static_cast<int64_t>(r) * ld4);
+      const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        lo_ev[x] += wv[x] & 0x00ff00ffu;
+        lo_od[x] += (wv[x] >> 8) & 0x00ff00ffu;
+      }
+    }
+    while (r < R0 + SOWN) r += step;   // (the cluster's own rows: below)
+#pragma unroll 4
+    for (; r < nrows; r += step) {
+      const uint4 w = __ldg(h4 + static_cast<int64_t>(r) * ld4);
+      const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        hi_ev[x] += wv[x] & 0x00ff00ffu;
+        hi_od[x] += (wv[x] >> 8) & 0x00ff00ffu;
+      }
+    }
+    // lanes sharing a chunk add their packed sums (a warp's rows count at most 128 x 128 tokens
+    // per 16-bit lane in such a histogram), then unpack
+    for (int o = cpr; o < 32; o <<= 1) {
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        lo_ev[x] += __shfl_xor_sync(0xffffffffu, lo_ev[x], o);
+        lo_od[x] += __shfl_xor_sync(0xffffffffu, lo_od[x], o);
+        hi_ev[x] += __shfl_xor_sync(0xffffffffu, hi_ev[x], o);
+        hi_od[x] += __shfl_xor_sync(0xffffffffu, hi_od[x], o);
+      }
+    }
+    int lo[16], hi[16];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      lo[4 * x] = lo_ev[x] & 0xffffu;
+      lo[4 * x + 1] = lo_od[x] & 0xffffu;
+      lo[4 * x + 2] = lo_ev[x] >> 16;
+      lo[4 * x + 3] = lo_od[x] >> 16;
+      hi[4 * x] = hi_ev[x] & 0xffffu;
+      hi[4 * x + 1] = hi_od[x] & 0xffffu;
+      hi[4 * x + 2] = hi_ev[x] >> 16;
+      hi[4 * x + 3] = hi_od[x] >> 16;
+    }
+    if (rsub == 0) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        sm.u.part[warp][0][c * 16 + i] = lo[i];
+        sm.u.part[warp][1][c * 16 + i] = hi[i];
+      }
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += ST) {
+      int a = 0, b = 0;
+#pragma unroll
+      for (int w = 0; w < SWARPS; ++w) {
+        a += sm.u.part[w][0][e];
+        b += sm.u.part[w][1][e];
+      }
+      sm.cpart[0][e] = a;
+      sm.cpart[1][e] = b;
+    }
+    ptx::cluster_sync();   // every block's share is in its shared memory
+    for (int e = tid; e < E; e += ST) {
+      int P = 0, Q = 0;
+      const uint32_t a0 = ptx::smem_u32(&sm.cpart[0][e]), a1 = ptx::smem_u32(&sm.cpart[1][e]);
+#pragma unroll
+      for (int q = 0; q < SCL; ++q) {
+        P += static_cast<int>(ptx::ld_cluster_u32(ptx::mapa(a0, q)));
+        Q += static_cast<int>(ptx::ld_cluster_u32(ptx::mapa(a1, q)));
+      }
+      // the cluster's own rows: those before this block's, and all of them
+      int own_before = 0, own_all = 0;
+#pragma unroll 4
+      for (int rr = R0; rr < R0 + SOWN && rr < nrows; ++rr) {
+        const int v = hist[static_cast<int64_t>(rr) * ldh + e];
+        own_all += v;
+        if (rr < r0) own_before += v;
+      }
+      sm.pre[e] = P + own_before;
+      sm.off[e] = P + own_all + Q;   // the total, until the scan below replaces it
+    }
+    ptx::cluster_sync();   // no block leaves or reuses its shares while another may read them
+  } else {
+    for (int e = tid; e < E; e += ST) {
+      sm.pre[e] = r0 < nrows ? rowpre[static_cast<int64_t>(e) * nrows + r0] : 0;
+      sm.off[e] = counts_in[e];
+    }
+  }
+  __syncthreads();   // (phase 1's shared memory is reused below)
+  // ---- offsets: the exclusive scan of the totals; each thread takes E/ST (at most one when
+  // E <= ST, else a run of consecutive experts)
+  {
+    constexpr int PER = (MOE_MAX_EXPERTS + ST - 1) / ST;
+    int v[PER], local = 0;
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int e = tid * PER + i;
-      v[i] = e < E ? counts[e] : 0;
+      v[i] = e < E ? sm.off[e] : 0;
       local += v[i];
     }
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int u = __shfl_up_sync(0xffffffffu, incl, o);
-      if (tid >= o) incl += u;
+      if (lane >= o) incl += u;
     }
-    int run = incl - local;
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += wsum[w];
+    int run = before + incl - local;
+    if (blockIdx.x == 0 && !rowpre) {
+#pragma unroll
+      for (int i = 0; i < PER; ++i)
+        if (tid * PER + i < E) counts[tid * PER + i] = v[i];
+    }
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int e = tid * PER + i;
-      if (e < E) s_off[e] = run;
+      if (e < E) sm.off[e] = run;
       run += v[i];
     }
-    if (tid == 31) s_off[E] = incl;
+    if (tid == ST - 1) sm.off[E] = run;   // the last thread's run ends at the grand total
+    __syncthreads();
   }
-  __syncthreads();
   if (blockIdx.x == 0)
-    for (int e = tid; e <= E; e += blockDim.x) offsets[e] = s_off[e];
-  const int t = blockIdx.x * TPB + tid;
-  const int w = tid >> 5, bit = tid & 31;
-  int ev[MAXK];
+    for (int e = tid; e <= E; e += ST) offsets[e] = sm.off[e];
+  // ---- this block's tokens: per expert, a bitmask of the warp's tokens that picked it.  Each
+  // lane holds its token's experts as a bitset (word w: experts 32w .. 32w+31); transposing a
+  // word across the warp gives lane i the mask of the tokens that picked expert 32w + i.
+  uint32_t bs[MOE_MAX_EXPERTS / 32];
+#pragma unroll
+  for (int w = 0; w < MOE_MAX_EXPERTS / 32; ++w) bs[w] = 0u;
 #pragma unroll
   for (int j = 0; j < MAXK; ++j) {
-    ev[j] = -1;
-    if (j < k && t < T) {
-      int e = idx[static_cast<int64_t>(t) * k + j];
-      if (e < 0 || e >= E) {
+    if (j < k) {
+      int e = ev[j];
+      if (e >= E || e < -1) {
         record_error(err, DEVERR_BAD_EXPERT);
-        e = -1;
-      } else {
-        atomicOr(&mask[e * MASK_WORDS + w], 1u << bit);
+        e = ev[j] = -1;
       }
-      ev[j] = e;
+#pragma unroll
+      for (int w = 0; w < MOE_MAX_EXPERTS / 32; ++w)
+        bs[w] |= (e >= 0 && (e >> 5) == w) ? 1u << (e & 31) : 0u;
+      sm.sop[tid * k + j] = -1;   // (stays -1 only for a pair whose expert was out of range)
+    }
+  }
+  const int nwords = (E + 31) >> 5;
+#pragma unroll
+  for (int w = 0; w < MOE_MAX_EXPERTS / 32; ++w) {
+    if (w < nwords) {
+      const uint32_t m = transpose32(bs[w], lane);
+      if (w * 32 + lane < E) sm.u.m.mask[w * 32 + lane][warp] = m;
     }
   }
   __syncthreads();
+  // per expert, the exclusive prefix of its words' popcounts (SWORDS lanes per expert; the loop
+  // bound is the same for every thread, so each shuffle has the whole warp); the last word's
+  // inclusive sum is the expert's pair count in this block
+  for (int e0 = 0; e0 < E; e0 += ST / SWORDS) {
+    const int e = e0 + tid / SWORDS, w = tid & (SWORDS - 1);
+    const int c = e < E ? __popc(sm.u.m.mask[e][w]) : 0;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < SWORDS; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o, SWORDS);
+      if (w >= o) incl += u;
+    }
+    if (e < E) {
+      sm.u.m.wpre[e][w] = incl - c;
+      if (w == SWORDS - 1) sm.boff[e] = incl;
+    }
+  }
+  __syncthreads();
+  // the block's expert order: boff = the exclusive scan of the experts' pair counts (one expert
+  // per thread, E <= ST)
+  int npairs;
+  {
+    const int ne = tid < E ? sm.boff[tid] : 0;
+    int incl = ne;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < SWARPS; ++w) {
+      if (w < warp) before += wsum[w];
+      all += wsum[w];
+    }
+    npairs = all;
+    if (tid < E) {
+      const int bo = before + incl - ne;
+      sm.boff[tid] = bo;
+      sm.gbase[tid] = sm.off[tid] + sm.pre[tid] - bo;
+    }
+    __syncthreads();
+  }
   const int64_t N = static_cast<int64_t>(T) * k;
+  const uint32_t below = (1u << lane) - 1u;
 #pragma unroll
   for (int j = 0; j < MAXK; ++j) {
     const int e = ev[j];
     if (e < 0) continue;
-    int rank = __popc(mask[e * MASK_WORDS + w] & ((1u << bit) - 1u));
-    for (int ww = 0; ww < w; ++ww) rank += __popc(mask[e * MASK_WORDS + ww]);
-    const int s = s_off[e] + rowpre[static_cast<int64_t>(e) * nblk + blockIdx.x] + rank;
-    if (s < 0 || s >= N) {
+    const int p = sm.boff[e] + sm.u.m.wpre[e][warp] + __popc(sm.u.m.mask[e][warp] & below);
+    sm.sop[tid * k + j] = sm.gbase[e] + p;
+    sm.tok[p] = t;
+    sm.ex[p] = static_cast<uint8_t>(e);
+  }
+  __syncthreads();
+  // ---- out: slot_of_pair of the block's tokens is one contiguous run; token_of_slot takes the
+  // block's pairs in expert order, each expert's a contiguous run of slots
+  const int t0 = blockIdx.x * ST;
+  const int nt = min(ST, T - t0);
+  int32_t* sop_out = slot_of_pair + static_cast<int64_t>(t0) * k;
+  for (int i = tid; i < nt * k; i += ST) {
+    const int sv = sm.sop[i];
+    if (sv >= N) record_error(err, DEVERR_BAD_SLOT);
+    sop_out[i] = sv < N ? sv : -1;
+  }
+  for (int i = tid; i < npairs; i += ST) {
+    const int64_t sv = static_cast<int64_t>(sm.gbase[sm.ex[i]]) + i;
+    if (sv < 0 || sv >= N) {
       record_error(err, DEVERR_BAD_SLOT);
       continue;
     }
-    slot_of_pair[static_cast<int64_t>(t) * k + j] = s;
-    token_of_slot[s] = t;
+    token_of_slot[sv] = sm.tok[i];
   }
 }
 
 // ----------------------------------------------------------------------------- balancing loss
+#define NEG_INF __int_as_float(0xff800000u)
+
+// Lane `lane` of a warp loads experts lane, lane + 32, ... of token t's logits (-inf past E or T).
+template <int EPL>
+__device__ __forceinline__ void load_logit_row(const float* __restrict__ logits, int t, int T,
+                                               int E, int lane, float (&v)[EPL]) {
+#pragma unroll
+  for (int q = 0; q < EPL; ++q) {
+    const int e = q * 32 + lane;
+    v[q] = (t < T && e < E) ? __ldg(logits + static_cast<int64_t>(t) * E + e) : NEG_INF;
+  }
+}
+
 // "Megatron-Bridge 深度剖析", §Nemotron-3-Nano 配置 (moe_aux_loss_coeff): the load-balancing loss
 //   L = coeff * E / (k * T^2) * sum_e counts[e] * sum_t p[t, e],
 // p[t,:] = softmax(l_t) (softmax routing) or s / sum(s), s = sigmoid(l_t) (sigmoid routing).
@@ -464,41 +610,41 @@ int launch_bias_update(const int32_t* counts, float* bias, int T, int k, int E, 
 }
 
 int launch_topk(const float* logits, int T, int E, int k, int score_fn, int renorm,
-                const float* sel_bias, int32_t* idx, float* gate, int32_t* hist, cudaStream_t st) {
-  const int nblk = route_blocks(T);
-  int blocks = (T + 7) / 8;   // 8 warps per block, one token per warp at a time
-  if (blocks > num_sms() * 8) blocks = num_sms() * 8;
-  const dim3 grid(blocks), block(256);
-  int rc;
-  if (E <= 32)
-    rc = launch("route_topk", topk_kernel<1>, grid, block, 0, st, logits, T, E, k, score_fn, renorm,
-                sel_bias, idx, gate, device_error_word());
-  else if (E <= 64)
-    rc = launch("route_topk", topk_kernel<2>, grid, block, 0, st, logits, T, E, k, score_fn, renorm,
-                sel_bias, idx, gate, device_error_word());
-  else if (E <= 128)
-    rc = launch("route_topk", topk_kernel<4>, grid, block, 0, st, logits, T, E, k, score_fn, renorm,
-                sel_bias, idx, gate, device_error_word());
-  else
-    rc = launch("route_topk", topk_kernel<8>, grid, block, 0, st, logits, T, E, k, score_fn, renorm,
-                sel_bias, idx, gate, device_error_word());
-  MOE_TRY(rc);
-  return launch("route_hist", hist_kernel, dim3(nblk), dim3(TPB), 0, st, idx, T, k, E, hist, nblk,
-                device_error_word());
+                const float* sel_bias, int32_t* idx, float* gate, uint8_t* hist, cudaStream_t st) {
+  const dim3 grid(route_rows(T)), block(HT);
+  const int ldh = route_ldh(E);
+  int* err = device_error_word();
+  if (k <= 2)
+    return launch("route_topk", topk_kernel<2>, grid, block, 0, st, logits, T, E, k, score_fn,
+                  renorm, sel_bias, idx, gate, hist, ldh, err);
+  if (k <= 4)
+    return launch("route_topk", topk_kernel<4>, grid, block, 0, st, logits, T, E, k, score_fn,
+                  renorm, sel_bias, idx, gate, hist, ldh, err);
+  return launch("route_topk", topk_kernel<MAXK>, grid, block, 0, st, logits, T, E, k, score_fn,
+                renorm, sel_bias, idx, gate, hist, ldh, err);
 }
 
-int launch_scan(const int32_t* hist, int E, int nblk, int32_t* base, int32_t* counts,
-                cudaStream_t st) {
-  return launch("route_scan", row_scan_kernel, dim3(E), dim3(RSCAN_THREADS), 0, st, hist, nblk,
-                base, counts);
-}
-
-int launch_slots(const int32_t* idx, int T, int k, int E, const int32_t* base,
-                 const int32_t* counts, int32_t* offsets, int32_t* slot_of_pair,
-                 int32_t* token_of_slot, cudaStream_t st) {
-  const int nblk = route_blocks(T);
-  return launch("route_slots", slots_kernel, dim3(nblk), dim3(256), 0, st, idx, T, k, E, base,
-                counts, offsets, nblk, slot_of_pair, token_of_slot, device_error_word());
+int launch_slots(const int32_t* idx, int T, int k, int E, const uint8_t* hist, int32_t* rowpre,
+                 int32_t* counts, int32_t* offsets, int32_t* slot_of_pair, int32_t* token_of_slot,
+                 cudaStream_t st) {
+  const int nrows = route_rows(T), ldh = route_ldh(E);
+  const bool direct = route_hist_direct(T, E);
+  if (!direct) {
+    if (!rowpre) {
+      set_error("route_slots: a histogram of %lld bytes needs the row-prefix scratch",
+                static_cast<long long>(nrows) * ldh);
+      return MOE_ERR_INVALID_ARG;
+    }
+    MOE_TRY(launch("route_scan", col_scan_kernel, dim3(E), dim3(RSCAN_THREADS), 0, st, hist, ldh,
+                   nrows, rowpre, counts));
+  }
+  // whole clusters: blocks past the tokens only take their share of the histogram sums
+  const int nblk = (T + ST - 1) / ST;
+  const int grid = (nblk + SCL - 1) / SCL * SCL;
+  return launch_clusters("route_slots", slots_kernel, dim3(grid), dim3(ST), 0, SCL, st, idx, T, k,
+                         E, hist, ldh, nrows, direct ? nullptr : rowpre,
+                         direct ? nullptr : counts, counts, offsets, slot_of_pair, token_of_slot,
+                         device_error_word());
 }
 
 }  // namespace moe

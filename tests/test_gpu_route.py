@@ -3,7 +3,9 @@ counts, offsets and both permutation maps bit-for-bit; gates within fp32 roundin
 
 Includes the routing/permute stress workload at full size (T=65536, E=128, top-8 sigmoid) with
 its degenerate cases: every token on the same 8 experts, 32 experts that receive nothing, and
-integer logits with massive exact ties.
+integer logits with massive exact ties; a histogram past the size every slots block reads whole
+(the scan path); and the bf16 router GEMM, whose epilogue routes the tokens from its
+accumulator, against the top-k kernel on the logits that GEMM wrote -- bit for bit.
 """
 import numpy as np
 import pytest
@@ -18,8 +20,10 @@ from .helpers import np64
 pytestmark = pytest.mark.gpu
 
 
-def route_gpu(T, E, k, score_fn, renorm, logits):
-    cfg = moe.make_cfg(T, 8, E, k, 8, score_fn=score_fn, renorm=renorm)
+def route_gpu(T, E, k, score_fn, renorm, logits, x=None, W_r=None, b_r=None,
+              bias_mode=moe.BIAS_LOGIT, logits_out=None):
+    d = 8 if x is None else x.shape[1]
+    cfg = moe.make_cfg(T, d, E, k, 8, score_fn=score_fn, renorm=renorm, bias_mode=bias_mode)
     dev = "cuda"
     i32 = torch.int32
     out = dict(idx=torch.full((T, k), -7, dtype=i32, device=dev),
@@ -29,8 +33,8 @@ def route_gpu(T, E, k, score_fn, renorm, logits):
                slot_of_pair=torch.full((T, k), -7, dtype=i32, device=dev),
                token_of_slot=torch.full((max(T * k, 1),), -7, dtype=i32, device=dev))
     ws = moe.workspace(cfg, moe.WS_ROUTE, dev)
-    moe.moe_route_topk(cfg, None, None, None, logits, None, out["idx"], out["gate"], out["counts"],
-                       out["offsets"], out["slot_of_pair"], out["token_of_slot"], ws)
+    moe.moe_route_topk(cfg, x, W_r, b_r, logits, logits_out, out["idx"], out["gate"],
+                       out["counts"], out["offsets"], out["slot_of_pair"], out["token_of_slot"], ws)
     torch.cuda.synchronize()
     moe.check_device_error()
     return {n: t.cpu().numpy() for n, t in out.items()}
@@ -95,3 +99,64 @@ def test_route_nan_logits_stay_in_range(E, k):
     assert (idx[20:] == r["idx"]).all()
     # whole-NaN rows: every key ranks as -inf, ties go to the lowest experts
     assert (idx[:10] == np.arange(k)).all()
+
+
+def test_route_large_histogram_takes_the_scan_path():
+    """T=140000, E=128: 1094 histogram rows of 128 bytes, past the 128 KB every slots block reads
+    whole, so a scan kernel forms the per-row prefixes first."""
+    T, E, k = 140000, 128, 8
+    lg = torch.randint(-20, 20, (T, E), generator=torch.Generator().manual_seed(3)).float()
+    lg[: T // 2, :8] += 100.0                 # half the tokens on the same 8 experts
+    check_route(T, E, k, 1, 0, lg)
+
+
+def _router_inputs(T, d, E, seed, integer=False):
+    g = torch.Generator().manual_seed(seed)
+    if integer:
+        # logits are exact integer sums of +-1 products: many exact ties between experts
+        x = torch.randint(-1, 2, (T, d), generator=g).float()
+        W = torch.randint(-1, 2, (E, d), generator=g).float()
+        b = torch.randint(-2, 3, (E,), generator=g).float()
+    else:
+        x = torch.randn(T, d, generator=g)
+        W = torch.randn(E, d, generator=g) * 0.05
+        b = torch.randn(E, generator=g) * 0.3
+    return x.bfloat16().cuda(), W.bfloat16().cuda(), b.cuda()
+
+
+def _gemm_vs_kernel(T, d, E, k, score_fn, renorm, bias_mode, seed, integer=False):
+    x, W, b = _router_inputs(T, d, E, seed, integer)
+    lg = torch.empty(T, E, device="cuda")
+    fused = route_gpu(T, E, k, score_fn, renorm, None, x=x, W_r=W, b_r=b, bias_mode=bias_mode,
+                      logits_out=lg)
+    # the same logits through the standalone top-k kernel (the selection bias, if any, again)
+    alone = route_gpu(T, E, k, score_fn, renorm, lg.clone(), b_r=b, bias_mode=bias_mode)
+    for n in ("idx", "counts", "offsets", "slot_of_pair", "token_of_slot"):
+        assert np.array_equal(fused[n], alone[n]), n
+    assert np.array_equal(fused["gate"].view(np.uint32), alone["gate"].view(np.uint32)), "gate bits"
+    # and both against the oracle on those logits (selection exact: the keys are fp32 logits)
+    if bias_mode == moe.BIAS_LOGIT:
+        r = O.route(lg.cpu().numpy(), k, E, score_fn, renorm)
+        assert np.array_equal(fused["idx"], r["idx"])
+        assert np.array_equal(fused["slot_of_pair"], r["slot_of_pair"])
+        err = np.abs(fused["gate"] - r["gate"]).max() / np.abs(r["gate"]).max()
+        assert err < 2e-6, f"gate error {err}"
+    return fused
+
+
+@pytest.mark.parametrize("E,k", [(8, 2), (5, 3), (64, 6), (128, 8), (160, 4), (256, 8), (256, 1)])
+@pytest.mark.parametrize("score_fn,renorm", [(0, 1), (0, 0), (1, 1), (1, 0)])
+def test_router_gemm_epilogue_routes_as_the_topk_kernel(E, k, score_fn, renorm):
+    _gemm_vs_kernel(1000, 256, E, k, score_fn, renorm, moe.BIAS_LOGIT, seed=E * 7 + k)
+
+
+@pytest.mark.parametrize("E,k", [(64, 6), (256, 8)])
+@pytest.mark.parametrize("score_fn,renorm", [(0, 1), (0, 0), (1, 1), (1, 0)])
+def test_router_gemm_epilogue_with_selection_bias(E, k, score_fn, renorm):
+    _gemm_vs_kernel(777, 192, E, k, score_fn, renorm, moe.BIAS_SELECT, seed=E + k)
+
+
+@pytest.mark.parametrize("T,E,k", [(4097, 128, 8), (300, 16, 4), (129, 256, 8)])
+def test_router_gemm_epilogue_integer_ties(T, E, k):
+    f = _gemm_vs_kernel(T, 128, E, k, 1, 1, moe.BIAS_LOGIT, seed=T, integer=True)
+    assert len(set(map(tuple, f["idx"].tolist()))) > 1

@@ -70,10 +70,10 @@ def test_noalloc_route_matches_workspace_route_on_two_calls():
 def test_noalloc_route_rejects_calls_beyond_its_scratch():
     L = moe.lib()
     P = ctypes.c_void_p(1 << 20)
-    big = moe.make_cfg(131072 + 256, 8, 128, 8, 8)   # E * ceil(T/256) = 128 * 513 > 65536
+    big = moe.make_cfg(131072 + 256, 8, 128, 8, 8)   # ceil(T/128) * 128 = 131328 > 131072
     rc = L.moe_route_topk_noalloc(ctypes.byref(big), None, None, None, P, None, P, P, P, P, P, P,
                                   None)
-    assert rc == -2 and b"65536" in L.moe_last_error()
+    assert rc == -2 and b"131072" in L.moe_last_error()
     ok = moe.make_cfg(1024, 8, 16, 2, 8)
     rc = L.moe_route_topk_noalloc(ctypes.byref(ok), P, P, None, None, None, P, P, P, P, P, P, None)
     assert rc == -1 and b"logits" in L.moe_last_error()
