@@ -976,6 +976,94 @@ def fp8_layer(args, lc, cfg, inp, dev, ms_bf16):
 
 # ----------------------------------------------------------------------------- reference arm
 
+def run_route_only(args, lc):
+    """Routing alone on the workload's tokens: moe_route_topk from x (router GEMM whose epilogue
+    selects, then the slot maps) and from given fp32 logits (top-k kernel, then the slot maps),
+    each timed as a CUDA graph of `steps` calls after `warmup` eager ones, with a per-kernel
+    CUDA-event trace beside it.  The chain's algorithmic bytes: x and W_r read, fp32 logits
+    written (the GEMM path) or read (the given-logits path), idx, gate and both slot maps written."""
+    import torch
+
+    import moe_expert_layer_gemm_gb300 as moe
+    from moe_expert_layer_gemm_gb300 import build as _build
+
+    if not os.path.exists(moe._lib.LIB_PATH):
+        _build.build()
+    moe.lib()
+    dev = torch.device("cuda", 0)
+    inp = moe_inputs.make_layer_inputs(lc, seed=args.seed, device=dev)
+    x, W_r, b_r = inp["x"], inp["W_r"], inp["b_r"]
+    del inp
+    torch.cuda.empty_cache()
+    cfg = moe.cfg_from(lc)
+    T, E, k = lc.T, lc.E, lc.k
+    i32 = torch.int32
+    o = dict(idx=torch.empty(T, k, dtype=i32, device=dev), gate=torch.empty(T, k, device=dev),
+             counts=torch.empty(E, dtype=i32, device=dev),
+             offsets=torch.empty(E + 1, dtype=i32, device=dev),
+             sop=torch.empty(T, k, dtype=i32, device=dev),
+             tos=torch.empty(max(T * k, 1), dtype=i32, device=dev))
+    lg = torch.empty(T, E, device=dev)
+    lg_in = torch.empty(T, E, device=dev)
+    ws = moe.workspace(cfg, moe.WS_ROUTE, dev)
+    stream = torch.cuda.Stream(dev)
+    peaks, _ = load_peaks()
+    b = 2 if lc.dtype == "bf16" else 4
+    maps = 16.0 * T * k
+    paths = {
+        "from_x": (lambda: moe.moe_route_topk(cfg, x, W_r, b_r, None, lg, o["idx"], o["gate"],
+                                              o["counts"], o["offsets"], o["sop"], o["tos"], ws,
+                                              stream=stream),
+                   T * lc.d * b + E * lc.d * b + T * E * 4.0 + maps),
+        "from_logits": (lambda: moe.moe_route_topk(cfg, None, None, b_r, lg_in, None, o["idx"],
+                                                   o["gate"], o["counts"], o["offsets"], o["sop"],
+                                                   o["tos"], ws, stream=stream),
+                        T * E * 4.0 + maps),
+    }
+    out = {}
+    with torch.cuda.stream(stream):
+        paths["from_x"][0]()
+        lg_in.copy_(lg)   # the logits the router GEMM wrote
+        for name, (fn, nbytes) in paths.items():
+            for _ in range(args.warmup):
+                fn()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(args.steps):
+                    fn()
+            g.replay()
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            stream.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / args.steps
+            moe.trace_read()
+            moe.trace_enable(True)
+            n_tr = max(3, min(args.steps, 20))
+            for _ in range(n_tr):
+                fn()
+            stream.synchronize()
+            moe.trace_enable(False)
+            tr = moe.trace_read()
+            moe.check_device_error()
+            out[name] = {"us_per_call": round(us, 2),
+                         "achieved": round(nbytes / (us * 1e-6) / 1e9, 1), "unit": "GB/s",
+                         "frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                         "bytes": int(nbytes),
+                         "kernels_us": {n: round(ms * 1e3 / max(1, c), 2) for n, (c, ms) in tr.items()},
+                         "launches_per_call": int(sum(c for c, _ in tr.values()) / n_tr)}
+    return {"metric": "routing time per call (moe_route_topk)", "value": out["from_x"]["us_per_call"],
+            "unit": "us", "higher_is_better": False, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "data": "synthetic (the workload's seeded x, W_r, b_r)",
+            "config": {"workload": lc.name, "T": T, "d_model": lc.d, "experts": E, "top_k": k,
+                       "score_fn": "sigmoid" if lc.score_fn else "softmax",
+                       "renorm": bool(lc.renorm), "timing": "CUDA graph of `steps` calls"},
+            "paths": out}
+
+
 def run_reference(args, lc):
     """The fp64 CPU oracle as the reference arm: each step is the oracle's forward + backward on
     a bounded, seeded sample of the same workload's tokens (all experts)."""
@@ -1033,6 +1121,9 @@ def main():
     ap.add_argument("--mxfp8-forward-only", action="store_true",
                     help="with --mxfp8: the step is the forward, also on workloads with a backward")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--route-only", action="store_true",
+                    help="time moe_route_topk alone on the workload's tokens (from x through the "
+                         "router GEMM, and from given logits); prints its own JSON line")
     args = ap.parse_args()
     if args.fp8 and args.mxfp8:
         ap.error("--fp8 and --mxfp8 are exclusive")
@@ -1040,7 +1131,10 @@ def main():
     lc = moe_inputs.CONFIGS[args.workload]
     if args.mxfp8 and args.mxfp8_forward_only:
         lc = lc.replace(backward=False)
-    out = run_reference(args, lc) if args.impl == "reference" else run_gpu(args, lc)
+    if args.route_only:
+        out = run_route_only(args, lc)
+    else:
+        out = run_reference(args, lc) if args.impl == "reference" else run_gpu(args, lc)
     if out is not None:
         print(json.dumps(out), flush=True)
 
