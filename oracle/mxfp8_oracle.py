@@ -148,3 +148,64 @@ def fc1_dgrad_mx(dHq, dHs, W1cq, W1cs, offsets):
         if hi > lo:
             dx[lo:hi] = DH[lo:hi] @ mx_decode_cols(W1cq[e], W1cs[e])
     return dx
+
+
+# ----------------------------------------------------------------------------- weight gradients
+# The weight gradients reduce over each expert's tokens (dW1[e] = dH1_e^T . x_e, [2f, d];
+# dW2[e] = dy_e^T . h_e, [d, f]), so the reduction dimension of their MXFP8 operands is the token
+# one.  Readings (the pages fix none of it, §FP8 训练 names fp8_wgrad and §新硬件适配 MXFP8):
+#   * inside expert e's rows [offsets[e], offsets[e+1]) every column is cut into blocks of 32
+#     consecutive rows counted from the segment's first row; a block never holds rows of two
+#     experts, and a segment's last block may be short;
+#   * a short block's missing rows count as zeros (they leave its amax unchanged and no code is
+#     stored for them);
+#   * each block's exponent and codes follow the rules above (the same as the forward's blocks);
+#     all four operands are quantised from their bf16 values.
+
+def mx_quantize_segments(x, offsets, block=BLOCK):
+    """Token-direction MXFP8 of x [N, C] inside each expert segment.  Returns (codes [N, C]
+    uint8, [scales of expert e: uint8 [ceil(n_e / 32), C] for each e])."""
+    x64 = np.asarray(x, dtype=np.float64)
+    N, C = x64.shape
+    codes = np.zeros((N, C), dtype=np.uint8)
+    scales = []
+    for e in range(len(offsets) - 1):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        n = hi - lo
+        nb = -(-n // block)
+        padded = np.zeros((nb * block, C))
+        padded[:n] = x64[lo:hi]
+        q, s = mx_quantize_cols(padded, block)
+        codes[lo:hi] = q[:n]
+        scales.append(s)
+    return codes, scales
+
+
+def mx_decode_segments(codes, scales, offsets, block=BLOCK):
+    """Decoded values [N, C] of segment-blocked codes (fp64)."""
+    c = np.asarray(codes)
+    out = np.zeros(c.shape)
+    for e in range(len(offsets) - 1):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        n = hi - lo
+        if n == 0:
+            continue
+        nb = -(-n // block)
+        padded = np.zeros((nb * block, c.shape[1]), dtype=np.uint8)
+        padded[:n] = c[lo:hi]
+        out[lo:hi] = mx_decode_cols(padded, scales[e], block)[:n]
+    return out
+
+
+def wgrad_mx(aq, a_s, bq, b_s, offsets):
+    """dW[e] = dec(A_e)^T . dec(B_e) for every expert e (fp64), A_e and B_e the expert's rows of
+    the segment-blocked operands A [N, M] and B [N, C]: [E, M, C]."""
+    A = mx_decode_segments(aq, a_s, offsets)
+    B = mx_decode_segments(bq, b_s, offsets)
+    E = len(offsets) - 1
+    dW = np.zeros((E, A.shape[1], B.shape[1]))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            dW[e] = A[lo:hi].T @ B[lo:hi]
+    return dW
