@@ -106,6 +106,12 @@ def kernel_work(lc, trace=None, steps=1):
     w["mxfp8_permute_quantize"] = ("hbm", T * d * 2 + N * d * 33 / 32 + N * 4 +
                                    (N * d * 2 if lc.backward else 0))
     w["mxfp8_quantize_rows"] = ("hbm", N * d * 2 + N * d * 33 / 32)   # dy_perm in expert order
+    # the weight gradients' token-direction quantisation: x_perm, dy_perm, h and [da | du] read in
+    # bf16, written as codes plus one scale byte per 32 (four launches a step)
+    w["mxfp8_quantize_tokens"] = ("hbm", per("mxfp8_quantize_tokens",
+                                             N * (2 * d + 3 * f) * (2 + 33 / 32)))
+    w["gemm_fc2_wgrad_mxfp8"] = w["gemm_fc2_wgrad"]
+    w["gemm_fc1_wgrad_mxfp8"] = w["gemm_fc1_wgrad"]
     # the combine backward that also writes dy_perm's codes and scales
     w["combine_bwd_mxfp8"] = ("hbm", w["combine_bwd"][1] + N * d * 33 / 32)
     return w
@@ -137,6 +143,9 @@ def gemm_bytes(lc):
     out["gemm_fc2_dgrad_mxfp8"] = T * k * d * q + E * d * f * q + T * k * 2 * f * 2 + \
         T * k * 2 * f * (2 + q)
     out["gemm_fc1_dgrad_mxfp8"] = T * k * 2 * f * q + E * 2 * f * d * q + T * k * d * 2
+    # weight gradients: both token-blocked operands' codes and scales in, fp32 blocks out
+    out["gemm_fc2_wgrad_mxfp8"] = T * k * (d + f) * q + E * d * f * 4
+    out["gemm_fc1_wgrad_mxfp8"] = T * k * (2 * f + d) * q + E * 2 * f * d * 4
     return out
 
 
@@ -399,9 +408,12 @@ def run_gpu(args, lc):
         # MXFP8 routed experts (weights quantised once, outside the timed steps, both copies).
         # Forward-only configurations keep routing and y_perm alone; with a backward, the forward
         # also saves the bf16 x_perm, [a | u] and h, and the backward runs the routed data
-        # gradients on MXFP8 operands and the weight gradients in bf16
+        # gradients on MXFP8 operands and the weight gradients on token-blocked MXFP8 operands
+        # (bf16 with --mxfp8-bf16-wgrad)
         mxq = moe.alloc_mxfp8_experts(cfg, inp["W1"], inp["W2"], dev)
         mxd = moe.alloc_mxfp8_dgrad(cfg, inp["W1"], inp["W2"], dev) if lc.backward else None
+        if mxd is not None and not args.mxfp8_bf16_wgrad:
+            mxd["wgrad_ws"] = moe.workspace(cfg, moe.WS_WGRAD_MXFP8, dev)
         if not lc.backward:
             saved["x_perm"] = saved["act"] = saved["h"] = None
     fp8q = None
@@ -702,8 +714,12 @@ def run_gpu(args, lc):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": ("e4m3 experts, bf16 router/combine" if args.fp8 else
-                  ("mxfp8 expert products (e4m3, e8m0 scale per 32) in the forward and the data "
-                   "gradients, bf16 weight gradients, bf16 router/shared/combine" if lc.backward else
+                  (("mxfp8 expert products (e4m3, e8m0 scale per 32) in the forward and the data "
+                    "gradients, bf16 weight gradients, bf16 router/shared/combine"
+                    if args.mxfp8_bf16_wgrad else
+                    "mxfp8 expert products (e4m3, e8m0 scale per 32) in the forward, the data "
+                    "gradients and the weight gradients (token blocks), bf16 router/shared/combine")
+                   if lc.backward else
                    "mxfp8 experts (e4m3, e8m0 scale per 32), bf16 router/shared/combine")
                   if args.mxfp8 else lc.dtype),
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights, random init)",
@@ -1118,6 +1134,8 @@ def main():
                     help="time the layer with MXFP8 routed experts: moe_layer_fwd_mxfp8, and "
                          "moe_layer_bwd_mxfp8 (MXFP8 data gradients, bf16 weight gradients) where "
                          "the configuration has a backward; --mxfp8-forward-only: the forward alone")
+    ap.add_argument("--mxfp8-bf16-wgrad", action="store_true",
+                    help="with --mxfp8: the routed weight gradients in bf16 instead of MXFP8")
     ap.add_argument("--mxfp8-forward-only", action="store_true",
                     help="with --mxfp8: the step is the forward, also on workloads with a backward")
     ap.add_argument("--e2e-steps", type=int, default=20)

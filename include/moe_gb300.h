@@ -101,7 +101,8 @@ enum {
   MOE_WS_LAYER_FWD = 3,   /* moe_layer_fwd                            */
   MOE_WS_LAYER_BWD = 4,   /* moe_layer_bwd                            */
   MOE_WS_FFN_BWD_FP8 = 5, /* moe_grouped_swiglu_bwd_fp8               */
-  MOE_WS_LAYER_BWD_FP8 = 6 /* moe_layer_bwd_fp8                       */
+  MOE_WS_LAYER_BWD_FP8 = 6, /* moe_layer_bwd_fp8                      */
+  MOE_WS_WGRAD_MXFP8 = 7  /* moe_grouped_swiglu_wgrad_mxfp8; moe_mxfp8_dgrad.wgrad_ws */
 };
 
 /* Bytes of caller workspace the call `which` needs for cfg (0 if cfg is invalid). */
@@ -276,7 +277,8 @@ int moe_grouped_swiglu_bwd_fp8(const moe_cfg* cfg, const uint8_t* x_perm_q, cons
  *     128-element K chunk kc, two such chunks (tile rows 0..127, 128..255) at
  *     ((e * tiles + t) * ceil(K/128) + kc) * 1024; rows and blocks past the weight are 127. */
 enum { MOE_MX_SCALES_X = 0, MOE_MX_SCALES_H = 1, MOE_MX_SCALES_W1 = 2, MOE_MX_SCALES_W2 = 3,
-       MOE_MX_SCALES_DH1 = 4, MOE_MX_SCALES_W1C = 5, MOE_MX_SCALES_W2C = 6 };
+       MOE_MX_SCALES_DH1 = 4, MOE_MX_SCALES_W1C = 5, MOE_MX_SCALES_W2C = 6,
+       MOE_MX_SCALES_TOK_D = 7, MOE_MX_SCALES_TOK_F = 8, MOE_MX_SCALES_TOK_2F = 9 };
 /* The data gradients' layouts: MOE_MX_SCALES_DH1 is [da | du] [N,2f] in the activation layout
  * (K = 2f).  MOE_MX_SCALES_W1C / _W2C are the weights blocked down their rows (W1 [2f,d] along 2f,
  * W2 [d,f] along d, as moe_mxfp8_prepare_dgrad_weights makes them): per expert, per tile of
@@ -284,6 +286,14 @@ enum { MOE_MX_SCALES_X = 0, MOE_MX_SCALES_H = 1, MOE_MX_SCALES_W1 = 2, MOE_MX_SC
  * columns of the tile, at ((e * tiles + t) * ceil(K/128) + kc) * (512 per 128 tile columns), byte
  * (c % 32) * 16 + (c % 128 / 32) * 4 + j for column c and block j of the K chunk; columns and
  * blocks past the weight are 127. */
+/* The weight gradients' layouts (their reduction dimension is the tokens):
+ * MOE_MX_SCALES_TOK_D / _F / _2F hold an [N, C] operand (C = d: x_perm or dy_perm; f: h; 2f:
+ * [da | du]) blocked down its columns in 32-row blocks counted from each expert segment's first
+ * row (a segment's last block may be short).  Per 128-column tile ct and 128-token chunk kc of
+ * the expert segments -- chunk kc of rows s of expert e is cbase[e] + (s - off_e) / 128, cbase[e]
+ * = sum_{e'<e} ceil(n_e' / 128) -- one 512-byte chunk at (ct * (N / 128 + E) + kc) * 512, byte
+ * (c % 32) * 16 + (c % 128 / 32) * 4 + j for column c and block j of the chunk; the blocks of a
+ * segment's last chunk past its rows are 127. */
 /* Bytes of one packed scale buffer for cfg (0 for an invalid cfg or `which`). */
 size_t moe_mxfp8_scale_bytes(const moe_cfg* cfg, int which);
 
@@ -373,7 +383,34 @@ typedef struct moe_mxfp8_dgrad {
   uint8_t* dy_s;
   uint8_t* dH1_q;
   uint8_t* dH1_s;
+  /* Scratch for MXFP8 weight gradients (moe_workspace_bytes(cfg, MOE_WS_WGRAD_MXFP8) bytes):
+   * when set, the routed experts' dW1 and dW2 run as moe_grouped_swiglu_wgrad_mxfp8 does; NULL:
+   * they run on the bf16 operands. */
+  void* wgrad_ws;
+  size_t wgrad_ws_bytes;
 } moe_mxfp8_dgrad;
+
+/* MXFP8 weight gradients: "Megatron-Bridge 深度剖析", §FP8 训练 (the weight gradient in FP8,
+ * fp8_wgrad) and §新硬件适配 (MXFP8).  Their reduction dimension is each expert's tokens, so the
+ * operands are blocked along the tokens inside every expert segment.
+ * moe_mxfp8_quantize_tokens: x [N, cols] bf16 (cols a multiple of 32) -> codes q [N, cols] and
+ *   scales s in the token-chunk layout (MOE_MX_SCALES_TOK_*, for cols = d, f or 2f; in general
+ *   ceil(cols/128) * (N/128 + E) * 512 bytes), cbase [E+1] int32 the segments' first chunks.
+ *   offsets [E+1] as from routing (non-decreasing, from 0 to at most N; MOE_ERR_DEVICE_CHECK from
+ *   moe_check_device_error otherwise, nothing written).
+ * moe_grouped_swiglu_wgrad_mxfp8: for the rows s of expert e (offsets),
+ *     dW1[e] = dec(dH1 blocks)^T . dec(x_perm blocks)   [2f, d]
+ *     dW2[e] = dec(dy_perm blocks)^T . dec(h blocks)    [d, f]
+ *   fp32 accumulation; every operand [N, .] bf16 is quantised by moe_mxfp8_quantize_tokens into
+ *   the workspace (MOE_WS_WGRAD_MXFP8).  An expert without rows gets zero blocks.  cfg->dtype
+ *   MOE_DTYPE_BF16, d and f multiples of 32. */
+int moe_mxfp8_quantize_tokens(const moe_cfg* cfg, const void* x, int32_t cols,
+                              const int32_t* offsets, uint8_t* q, uint8_t* s, int32_t* cbase,
+                              void* stream);
+int moe_grouped_swiglu_wgrad_mxfp8(const moe_cfg* cfg, const int32_t* offsets, const void* x_perm,
+                                   const void* h, const void* dy_perm, const void* dH1,
+                                   float* dW1, float* dW2, void* ws, size_t ws_bytes,
+                                   void* stream);
 
 /* Unpermute + weighted combine: "Megatron-Bridge 深度剖析", §Expert Parallel 基础 (Step 3,
  * results sent back to token order) and §Shared Expert Overlap (shared output added).
@@ -530,9 +567,10 @@ int moe_layer_fwd_mxfp8(const moe_cfg* cfg, const void* x, const void* W_r, cons
 
 /* The layer backward after moe_layer_fwd_mxfp8 (given saved.x_perm, act and h): moe_layer_bwd,
  * except that the routed experts' data gradients run on MXFP8 operands
- * (moe_grouped_swiglu_dgrad_mxfp8 on mxd's weights and buffers); their weight gradients stay bf16
- * products of the saved bf16 x_perm and h with the bf16 dy_perm and [da | du] (fp32 out), as do
- * the router's and the shared expert's backward.  Workspace MOE_WS_LAYER_BWD. */
+ * (moe_grouped_swiglu_dgrad_mxfp8 on mxd's weights and buffers).  Their weight gradients run in
+ * MXFP8 too when mxd->wgrad_ws is set (moe_grouped_swiglu_wgrad_mxfp8 on the saved bf16 x_perm and
+ * h and the bf16 dy_perm and [da | du]); otherwise they are bf16 products of those operands (fp32
+ * out).  The router's and the shared expert's backward stay bf16.  Workspace MOE_WS_LAYER_BWD. */
 int moe_layer_bwd_mxfp8(const moe_cfg* cfg, const void* dy, const void* x, const void* W_r,
                         const moe_mxfp8_dgrad* mxd, const void* Ws1, const void* Ws2,
                         const void* w_sg, const moe_saved* saved, void* dx, float* dW_r,

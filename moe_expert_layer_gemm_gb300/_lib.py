@@ -22,9 +22,10 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3:
 SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 DTYPE_BF16, DTYPE_F32 = 0, 1
 BIAS_LOGIT, BIAS_SELECT = 0, 1
-WS_ROUTE, WS_FFN_FWD, WS_FFN_BWD, WS_LAYER_FWD, WS_LAYER_BWD, WS_FFN_BWD_FP8, WS_LAYER_BWD_FP8 = range(7)
-MX_SCALES_X, MX_SCALES_H, MX_SCALES_W1, MX_SCALES_W2, MX_SCALES_DH1, MX_SCALES_W1C, MX_SCALES_W2C = \
-    range(7)
+WS_ROUTE, WS_FFN_FWD, WS_FFN_BWD, WS_LAYER_FWD, WS_LAYER_BWD, WS_FFN_BWD_FP8, WS_LAYER_BWD_FP8, \
+    WS_WGRAD_MXFP8 = range(8)
+MX_SCALES_X, MX_SCALES_H, MX_SCALES_W1, MX_SCALES_W2, MX_SCALES_DH1, MX_SCALES_W1C, MX_SCALES_W2C, \
+    MX_SCALES_TOK_D, MX_SCALES_TOK_F, MX_SCALES_TOK_2F = range(10)
 
 
 class MoeCfg(ctypes.Structure):
@@ -52,7 +53,8 @@ class MoeMxfp8Experts(ctypes.Structure):
 
 class MoeMxfp8Dgrad(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("W1c_q", "W1c_sp", "W2c_q", "W2c_sp", "dy_q", "dy_s", "dH1_q", "dH1_s")]
+                ("W1c_q", "W1c_sp", "W2c_q", "W2c_sp", "dy_q", "dy_s", "dH1_q", "dH1_s",
+                 "wgrad_ws")] + [("wgrad_ws_bytes", ctypes.c_size_t)]
 
 
 class MoeSideStream(ctypes.Structure):
@@ -108,6 +110,8 @@ _SIGS = {
                             + [_VP] * 4 + [ctypes.POINTER(MoeSaved), _VP, _SZ, _VP, _SIDE]),
     "moe_mxfp8_prepare_dgrad_weights": (ctypes.c_int, [_CFG] + [_VP] * 9),
     "moe_grouped_swiglu_dgrad_mxfp8": (ctypes.c_int, [_CFG] + [_VP] * 14),
+    "moe_mxfp8_quantize_tokens": (ctypes.c_int, [_CFG, _VP, ctypes.c_int32] + [_VP] * 5),
+    "moe_grouped_swiglu_wgrad_mxfp8": (ctypes.c_int, [_CFG] + [_VP] * 8 + [_SZ, _VP]),
     "moe_layer_bwd_mxfp8": (ctypes.c_int, [_CFG] + [_VP] * 3 + [ctypes.POINTER(MoeMxfp8Dgrad)]
                             + [_VP] * 3 + [ctypes.POINTER(MoeSaved)] + [_VP] * 8 + [_SZ, _VP, _SIDE]),
     "moe_unpermute_combine": (ctypes.c_int, [_CFG] + [_VP] * 7),
@@ -383,8 +387,27 @@ def moe_grouped_swiglu_dgrad_mxfp8(cfg, dy_perm, offsets, act, mxd, dH1, dx_perm
         "moe_grouped_swiglu_dgrad_mxfp8")
 
 
+def moe_mxfp8_quantize_tokens(cfg, x, offsets, q, s, cbase, stream=None):
+    """Token-direction MXFP8 of x [N, C] inside the expert segments (see the header)."""
+    _check(lib().moe_mxfp8_quantize_tokens(ctypes.byref(cfg), _p(x), int(x.shape[1]), _p(offsets),
+                                           _p(q), _p(s), _p(cbase), _stream(stream)),
+           "moe_mxfp8_quantize_tokens")
+
+
+def moe_grouped_swiglu_wgrad_mxfp8(cfg, offsets, x_perm, h, dy_perm, dH1, dW1, dW2, ws,
+                                   stream=None):
+    _check(lib().moe_grouped_swiglu_wgrad_mxfp8(
+        ctypes.byref(cfg), _p(offsets), _p(x_perm), _p(h), _p(dy_perm), _p(dH1), _p(dW1), _p(dW2),
+        _p(ws), 0 if ws is None else ws.numel(), _stream(stream)), "moe_grouped_swiglu_wgrad_mxfp8")
+
+
 def mxd_struct(m):
-    return MoeMxfp8Dgrad(*[m[n].data_ptr() for n, _ in MoeMxfp8Dgrad._fields_])
+    """The struct of an mxfp8_dgrad_state dict; with m["wgrad_ws"] (a uint8 tensor of
+    workspace_bytes(cfg, WS_WGRAD_MXFP8)) the weight gradients run in MXFP8 too."""
+    ws = m.get("wgrad_ws")
+    ptrs = [m[n].data_ptr() for n, _ in MoeMxfp8Dgrad._fields_[:8]]
+    return MoeMxfp8Dgrad(*ptrs, None if ws is None else ws.data_ptr(),
+                         0 if ws is None else ws.numel())
 
 
 def moe_layer_bwd_mxfp8(cfg, dy, x, W_r, mxd, Ws1, Ws2, w_sg, saved, dx, dW_r, dW1, dW2, dWs1, dWs2,

@@ -233,6 +233,31 @@ static RouteWs carve_route(Carve& cv, const moe_cfg* c) {
   return w;
 }
 
+// Scratch of the MXFP8 weight gradients: the four operands quantised along the tokens (codes in
+// their [N, C] layouts, scales in the token-chunk layout) and the chunk bases of the experts.
+struct WgMxWs {
+  int32_t* cbase;
+  uint8_t *x_q, *dy_q, *h_q, *dH1_q;
+  uint8_t *x_s, *dy_s, *h_s, *dH1_s;
+  int* sched;   // two 16-byte tile counters
+};
+static WgMxWs carve_wgmx(Carve& cv, const moe_cfg* c) {
+  WgMxWs w;
+  const int64_t N = static_cast<int64_t>(c->T) * c->k;
+  const int E = c->E, d = c->d, f = c->f;
+  w.cbase = static_cast<int32_t*>(cv.take((E + 1) * sizeof(int32_t)));
+  w.x_q = static_cast<uint8_t*>(cv.take(static_cast<size_t>(N) * d));
+  w.dy_q = static_cast<uint8_t*>(cv.take(static_cast<size_t>(N) * d));
+  w.h_q = static_cast<uint8_t*>(cv.take(static_cast<size_t>(N) * f));
+  w.dH1_q = static_cast<uint8_t*>(cv.take(static_cast<size_t>(N) * 2 * f));
+  w.x_s = static_cast<uint8_t*>(cv.take(static_cast<size_t>(mx_tok_scale_bytes(N, E, d))));
+  w.dy_s = static_cast<uint8_t*>(cv.take(static_cast<size_t>(mx_tok_scale_bytes(N, E, d))));
+  w.h_s = static_cast<uint8_t*>(cv.take(static_cast<size_t>(mx_tok_scale_bytes(N, E, f))));
+  w.dH1_s = static_cast<uint8_t*>(cv.take(static_cast<size_t>(mx_tok_scale_bytes(N, E, 2 * f))));
+  w.sched = static_cast<int*>(cv.take(2 * 16));
+  return w;
+}
+
 // Counters of the weight-gradient GEMMs' run-time tile scheduling, one 16-byte slot per launch
 // (routed fc2, routed fc1, shared fc2, shared fc1, router).
 constexpr int SCHED_SLOTS = 5;
@@ -705,7 +730,7 @@ using namespace moe;
 // ====================================================================== C ABI
 extern "C" {
 
-int moe_version(void) { return 200; }
+int moe_version(void) { return 201; }
 
 const char* moe_last_error(void) { return g_errbuf; }
 
@@ -787,6 +812,9 @@ size_t moe_workspace_bytes(const moe_cfg* c, int which) {
       break;
     case MOE_WS_FFN_BWD_FP8:
       cv.take(2 * 4 * sizeof(int));
+      break;
+    case MOE_WS_WGRAD_MXFP8:
+      carve_wgmx(cv, c);
       break;
     case MOE_WS_LAYER_BWD_FP8:
       carve_bwd(cv, c);
@@ -1086,6 +1114,9 @@ size_t moe_mxfp8_scale_bytes(const moe_cfg* c, int which) {
     case MOE_MX_SCALES_W2C:   // W2 read as [d (K), f (N)]: tiles of MX_BN_DGRAD2 columns of f
       return static_cast<size_t>(c->E) * ((c->f + MX_BN_DGRAD2 - 1) / MX_BN_DGRAD2) *
              mx_kch(c->d) * ((MX_BN_DGRAD2 + 127) / 128) * MX_CHUNK;
+    case MOE_MX_SCALES_TOK_D: return static_cast<size_t>(mx_tok_scale_bytes(N, c->E, c->d));
+    case MOE_MX_SCALES_TOK_F: return static_cast<size_t>(mx_tok_scale_bytes(N, c->E, c->f));
+    case MOE_MX_SCALES_TOK_2F: return static_cast<size_t>(mx_tok_scale_bytes(N, c->E, 2 * c->f));
     default: return 0;
   }
 }
@@ -1208,6 +1239,54 @@ static int dgrad_mx_impl(const moe_cfg* c, const int32_t* offsets, int64_t N, co
 // bf16 dy_perm and h; fc1's data gradient on the MXFP8 dH1 (dx_perm may alias dy_perm: it is
 // written after fc2's weight gradient has read it); fc1's weight gradient from the bf16 dH1 and
 // x_perm.
+// One expert weight gradient on token-blocked MXFP8 operands: out[e] = dec(A_e)^T . dec(B_e),
+// A [N, M] and B [N, C] codes (MN-major: the tokens are the reduction dimension).
+static int wgrad_mx_gemm(const moe_cfg* c, const int32_t* offsets, int64_t N, const uint8_t* aq,
+                         const uint8_t* as, int M, const uint8_t* bq, const uint8_t* bs, int C,
+                         const int32_t* cbase, float* out, int* ctr, const char* name,
+                         cudaStream_t st) {
+  GemmDesc w = desc0();
+  w.name = name;
+  w.sched = RAGGED_K;
+  w.epi = EPI_F32;
+  w.G = c->E;
+  w.offsets = offsets;
+  w.M = M;
+  w.N = C;
+  w.K = static_cast<int>(N);
+  w.A = opnd(aq, N, M, true);
+  w.B = opnd(bq, N, C, true);
+  w.out = out;
+  w.ldo = C;
+  w.out_group_stride = static_cast<int64_t>(M) * C;
+  w.tile_ctr = ctr;
+  w.fp8 = true;
+  w.mx = true;
+  w.sfa = as;
+  w.sfb = bs;
+  w.mx_cbase = cbase;
+  return gemm_tc(w, st);
+}
+
+// fc2's (dW2 = dy^T h) or fc1's (dW1 = [da | du]^T x_perm) weight gradient in MXFP8: both operands
+// quantised along the tokens inside the expert segments, then the block-scaled product.
+static int wgrad2_mx(const moe_cfg* c, const int32_t* offsets, int64_t N, const void* dy_perm,
+                     const void* h, float* dW2, const WgMxWs& w, int* ctr, cudaStream_t st) {
+  const int E = c->E, d = c->d, f = c->f;
+  MOE_TRY(launch_mx_quantize_tokens(dy_perm, N, d, offsets, E, w.dy_q, w.dy_s, w.cbase, st));
+  MOE_TRY(launch_mx_quantize_tokens(h, N, f, offsets, E, w.h_q, w.h_s, w.cbase, st));
+  return wgrad_mx_gemm(c, offsets, N, w.dy_q, w.dy_s, d, w.h_q, w.h_s, f, w.cbase, dW2, ctr,
+                       "gemm_fc2_wgrad_mxfp8", st);
+}
+static int wgrad1_mx(const moe_cfg* c, const int32_t* offsets, int64_t N, const void* dH1,
+                     const void* x_perm, float* dW1, const WgMxWs& w, int* ctr, cudaStream_t st) {
+  const int E = c->E, d = c->d, f = c->f;
+  MOE_TRY(launch_mx_quantize_tokens(dH1, N, 2 * f, offsets, E, w.dH1_q, w.dH1_s, w.cbase, st));
+  MOE_TRY(launch_mx_quantize_tokens(x_perm, N, d, offsets, E, w.x_q, w.x_s, w.cbase, st));
+  return wgrad_mx_gemm(c, offsets, N, w.dH1_q, w.dH1_s, 2 * f, w.x_q, w.x_s, d, w.cbase, dW1, ctr,
+                       "gemm_fc1_wgrad_mxfp8", st);
+}
+
 static int ffn_bwd_mx_impl(const moe_cfg* c, const int32_t* offsets, int64_t N, const void* x_perm,
                            const void* act, const void* h, const void* dy_perm, void* dH1,
                            void* dx_perm, float* dW1, float* dW2, int* sched, cudaStream_t st,
@@ -1240,22 +1319,30 @@ static int ffn_bwd_mx_impl(const moe_cfg* c, const int32_t* offsets, int64_t N, 
   a.q_out = m->dH1_q;
   a.q_sf = m->dH1_s;
   MOE_TRY(gemm_tc(a, st));
-  GemmDesc b = desc0();
-  b.name = "gemm_fc2_wgrad";
-  b.sched = RAGGED_K;
-  b.epi = EPI_F32;
-  b.G = E;
-  b.offsets = offsets;
-  b.M = d;
-  b.N = f;
-  b.K = static_cast<int>(N);
-  b.A = opnd(dy_perm, N, d, true);
-  b.B = opnd(h, N, f, true);
-  b.out = dW2;
-  b.ldo = f;
-  b.out_group_stride = static_cast<int64_t>(d) * f;
-  b.tile_ctr = sched;
-  MOE_TRY(gemm_tc(b, st));
+  // MXFP8 weight gradients when the caller lends their scratch, else bf16 ones
+  WgMxWs wm;
+  if (m->wgrad_ws) {
+    Carve cv(m->wgrad_ws);
+    wm = carve_wgmx(cv, c);
+    MOE_TRY(wgrad2_mx(c, offsets, N, dy_perm, h, dW2, wm, sched, st));
+  } else {
+    GemmDesc b = desc0();
+    b.name = "gemm_fc2_wgrad";
+    b.sched = RAGGED_K;
+    b.epi = EPI_F32;
+    b.G = E;
+    b.offsets = offsets;
+    b.M = d;
+    b.N = f;
+    b.K = static_cast<int>(N);
+    b.A = opnd(dy_perm, N, d, true);
+    b.B = opnd(h, N, f, true);
+    b.out = dW2;
+    b.ldo = f;
+    b.out_group_stride = static_cast<int64_t>(d) * f;
+    b.tile_ctr = sched;
+    MOE_TRY(gemm_tc(b, st));
+  }
   GemmDesc e = desc0();
   e.name = "gemm_fc1_dgrad_mxfp8";
   e.sched = RAGGED_M;
@@ -1275,6 +1362,7 @@ static int ffn_bwd_mx_impl(const moe_cfg* c, const int32_t* offsets, int64_t N, 
   e.sfa = m->dH1_s;
   e.sfb = m->W1c_sp;
   MOE_TRY(gemm_tc(e, st));
+  if (m->wgrad_ws) return wgrad1_mx(c, offsets, N, dH1, x_perm, dW1, wm, sched + 4, st);
   GemmDesc w = desc0();
   w.name = "gemm_fc1_wgrad";
   w.sched = RAGGED_K;
@@ -1309,6 +1397,36 @@ int moe_mxfp8_prepare_dgrad_weights(const moe_cfg* c, const void* W1, const void
   // W2 [E, d, f] in 32-row blocks along d; its columns (f) are the B-rows of fc2's data gradient
   MOE_TRY(launch_mx_quantize_cols(W2, E, d, f, W2c_q, W2c_s, st));
   return launch_mx_pack_weight_scales(W2c_s, E, f, d, 0, W2c_sp, st, MX_BN_DGRAD2, 1);
+}
+
+int moe_mxfp8_quantize_tokens(const moe_cfg* c, const void* x, int32_t cols,
+                              const int32_t* offsets, uint8_t* q, uint8_t* s, int32_t* cbase,
+                              void* stream) {
+  MOE_TRY(check_mx_cfg(c));
+  if (cols <= 0 || cols % 32)
+    return fail(MOE_ERR_UNSUPPORTED, "cols=%d: a positive multiple of 32 is needed", cols);
+  const struct { const void* p; const char* n; } req[] = {
+      {x, "x"}, {offsets, "offsets"}, {q, "q"}, {s, "s"}, {cbase, "cbase"}};
+  for (const auto& r : req) MOE_TRY(check_ptr(r.p, r.n, true));
+  return launch_mx_quantize_tokens(x, Nrows(c), cols, offsets, c->E, q, s, cbase, S(stream));
+}
+
+int moe_grouped_swiglu_wgrad_mxfp8(const moe_cfg* c, const int32_t* offsets, const void* x_perm,
+                                   const void* h, const void* dy_perm, const void* dH1,
+                                   float* dW1, float* dW2, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  MOE_TRY(check_mx_cfg(c));
+  const struct { const void* p; const char* n; } req[] = {
+      {offsets, "offsets"}, {x_perm, "x_perm"}, {h, "h"}, {dy_perm, "dy_perm"},
+      {dH1, "dH1"},         {dW1, "dW1"},       {dW2, "dW2"}};
+  for (const auto& r : req) MOE_TRY(check_ptr(r.p, r.n, true));
+  MOE_TRY(check_ws(c, MOE_WS_WGRAD_MXFP8, ws, ws_bytes));
+  Carve cv(ws);
+  const WgMxWs w = carve_wgmx(cv, c);
+  cudaStream_t st = S(stream);
+  const int64_t N = Nrows(c);
+  MOE_TRY(wgrad2_mx(c, offsets, N, dy_perm, h, dW2, w, w.sched, st));
+  return wgrad1_mx(c, offsets, N, dH1, x_perm, dW1, w, w.sched + 4, st);
 }
 
 int moe_grouped_swiglu_dgrad_mxfp8(const moe_cfg* c, const void* dy_perm, const int32_t* offsets,
@@ -1618,6 +1736,7 @@ static int layer_bwd_impl(const moe_cfg* c, const void* dy, const void* x, const
         {mxd->W2c_sp, "mxd.W2c_sp"}, {mxd->dy_q, "mxd.dy_q"},  {mxd->dy_s, "mxd.dy_s"},
         {mxd->dH1_q, "mxd.dH1_q"}, {mxd->dH1_s, "mxd.dH1_s"}};
     for (const auto& r : req) MOE_TRY(check_ptr(r.p, r.n, true));
+    if (mxd->wgrad_ws) MOE_TRY(check_ws(c, MOE_WS_WGRAD_MXFP8, mxd->wgrad_ws, mxd->wgrad_ws_bytes));
   }
   const bool sq = shared_fp8(c, q);
   MOE_TRY(check_ptr(Ws1, "Ws1", sh && !sq));

@@ -234,7 +234,9 @@ struct KArgs {
   const uint8_t* sfb;      // MXFP8: packed block scales of B (weight layout)
   uint8_t* q_out;          // MXFP8 SwiGLU forward: h codes [rows, f]
   uint8_t* q_sf;           // MXFP8 SwiGLU forward: h block scales (activation layout)
-  int kch;                 // MXFP8: 128-element K chunks of the operands
+  int kch;                 // MXFP8: 128-element K chunks of the operands (weight gradients:
+                           // the token-chunk capacity of the scale layouts)
+  const int32_t* cbase;    // MXFP8 weight gradients: each group's first token chunk
   int kch_out;             // MXFP8 SwiGLU forward: 128-element chunks of h's rows
   RouterEpi rt;            // router top-k in the epilogue (rt.idx null: off)
   int* err;
@@ -361,8 +363,12 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
   constexpr int MNW = F8 ? 128 : 64;
   constexpr int MN_CHUNK = BKE * 128;   // bytes of one such chunk in a stage
   static_assert(!F8 || !GATHER, "FP8 operands: no gathered loads");
-  // MXFP8: K-major E4M3 operands of a row-ragged product; one stage is one 128-element K chunk
-  static_assert(!MX || (F8 && SCHED == RAGGED_M && !A_MN && (!B_MN || BN % 128 == 0) && BN <= 256 &&
+  // MXFP8: K-major E4M3 operands of a row-ragged product, or the MN-major token-blocked operands
+  // of a weight gradient (128-wide tiles); one stage is one 128-element K chunk
+  static_assert(!MX || (F8 &&
+                        ((SCHED == RAGGED_M && !A_MN && (!B_MN || BN % 128 == 0)) ||
+                         (SCHED == RAGGED_K && A_MN && B_MN && EPI == EPI_F32 && BN == 128)) &&
+                        BN <= 256 &&
                         C::ACC_STRIDE == MxCfg<BN>::ACC_STRIDE &&
                         MxCfg<BN>::SF_COL0 + C::STAGES * MX_SF_COLS <= C::TMEM_COLS),
                 "MXFP8 tile configuration");
@@ -662,11 +668,21 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
         if (MX) {
           // this K chunk's block scales: the A row tile's chunk, then the B tile's chunks
           uint8_t* sf_dst = sSF + stg * MxCfg<BN>::SF_STAGE;
-          ptx::bulk_load(sf_dst, p.sfa + (static_cast<int64_t>(ti.mt) * p.kch + kb) * MX_CHUNK,
-                         MX_CHUNK, &full[stg]);
-          const int64_t wt = static_cast<int64_t>(ti.g) * S::n_tiles(p) + ti.nt;
           constexpr int SFB = MX_CHUNK * MxCfg<BN>::SFB_CH;
-          ptx::bulk_load(sf_dst + MX_CHUNK, p.sfb + (wt * p.kch + kb) * SFB, SFB, &full[stg]);
+          if (SCHED == RAGGED_K) {
+            // token chunk kb of group g's rows; A's and B's 128-row tiles
+            const int64_t kc = __ldg(p.cbase + ti.g) + kb;
+            ptx::bulk_load(sf_dst, p.sfa + (static_cast<int64_t>(ti.mt) * p.kch + kc) * MX_CHUNK,
+                           MX_CHUNK, &full[stg]);
+            ptx::bulk_load(sf_dst + MX_CHUNK,
+                           p.sfb + (static_cast<int64_t>(ti.nt) * p.kch + kc) * MX_CHUNK, SFB,
+                           &full[stg]);
+          } else {
+            ptx::bulk_load(sf_dst, p.sfa + (static_cast<int64_t>(ti.mt) * p.kch + kb) * MX_CHUNK,
+                           MX_CHUNK, &full[stg]);
+            const int64_t wt = static_cast<int64_t>(ti.g) * S::n_tiles(p) + ti.nt;
+            ptx::bulk_load(sf_dst + MX_CHUNK, p.sfb + (wt * p.kch + kb) * SFB, SFB, &full[stg]);
+          }
         }
       };
       // Run-time tiles: the next tile is claimed before the current one's loads are issued,
@@ -1976,7 +1992,8 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
   a.sfb = g.sfb;
   a.q_out = g.q_out;
   a.q_sf = g.q_sf;
-  a.kch = static_cast<int>(mx_kch(g.K));
+  a.kch = static_cast<int>(SCHED == RAGGED_K ? mx_tok_chunks(g.K, g.G) : mx_kch(g.K));
+  a.cbase = g.mx_cbase;
   a.kch_out = static_cast<int>(mx_kch(EPI == EPI_SWIGLU_BWD ? 2 * static_cast<int64_t>(g.f) : g.f));
   a.rt = g.rt;
   if (g.rt.idx) {
@@ -1999,12 +2016,14 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
     const bool aligned = (reinterpret_cast<uintptr_t>(g.sfa) & 15u) == 0 &&
                          (reinterpret_cast<uintptr_t>(g.sfb) & 15u) == 0;
     const bool swiglu = EPI == EPI_SWIGLU_FWD || EPI == EPI_SWIGLU_BWD;
-    if (!g.sfa || !g.sfb || !aligned || g.K % 32 != 0 ||
+    if (!g.sfa || !g.sfb || !aligned || (SCHED == RAGGED_M && g.K % 32 != 0) ||
+        (SCHED == RAGGED_K && (!g.mx_cbase || !g.offsets)) ||
         (swiglu && (!g.q_out || !g.q_sf || g.f % 32 != 0 ||
                     (reinterpret_cast<uintptr_t>(g.q_out) & 15u) != 0)) ||
         (EPI == EPI_SWIGLU_BWD && !g.aux)) {
       set_error("%s: MXFP8 operands need 16-byte aligned block scales, K (and f) multiples of 32 "
-                "and, for SwiGLU, h's code and scale buffers", name);
+                "(weight gradients: the groups' offsets and token-chunk bases) and, for SwiGLU, "
+                "h's code and scale buffers", name);
       return MOE_ERR_INVALID_ARG;
     }
   }
@@ -2125,6 +2144,9 @@ int gemm_tc(const GemmDesc& g, cudaStream_t st) {
         return run<MX_BN_DGRAD1, false, true, RAGGED_M, EPI_STORE, false, true, true>(
             g, "gemm_fc1_dgrad_mxfp8", st);
     }
+    // the weight gradients: token-blocked MN-major operands, 128 x 128 tiles (two accumulators)
+    if (!g.gather && g.sched == RAGGED_K && g.A.mn_major && g.B.mn_major && g.epi == EPI_F32)
+      return run<128, true, true, RAGGED_K, EPI_F32, false, true, true>(g, "gemm_wgrad_mxfp8", st);
     set_error("gemm_tc: unsupported MXFP8 combination sched=%d epi=%d a_mn=%d b_mn=%d", g.sched,
               g.epi, (int)g.A.mn_major, (int)g.B.mn_major);
     return MOE_ERR_UNSUPPORTED;

@@ -223,6 +223,10 @@ struct GemmDesc {
   bool mx;
   const uint8_t* sfa;
   const uint8_t* sfb;
+  // MXFP8 weight gradients (RAGGED_K): the first 128-token chunk of each group's rows in the
+  // token-chunk scale layouts of sfa / sfb; those layouts hold mx_tok_chunks(K, G) chunks per
+  // 128-row tile.
+  const int32_t* mx_cbase;
   // MXFP8 SwiGLU forward: h as MXFP8 codes [rows, f] and its packed block scales (the A-operand
   // layout, row tiles as this product's); `out` (bf16 h) and `out2` ([a | u]) may be null.
   uint8_t* q_out;
@@ -256,6 +260,12 @@ constexpr int MX_CHUNK = 512;
 constexpr int MX_SFB_CHUNKS = (MX_BN + 127) / 128;
 constexpr int MX_SFB_BYTES = MX_SFB_CHUNKS * MX_CHUNK;
 inline int64_t mx_kch(int64_t K) { return (K + 127) / 128; }
+// Token-direction operands of the MXFP8 weight gradients: 128-token chunks of the expert segments
+// (at most N / 128 + E of them), per 128-column tile one 512-byte chunk each.
+inline int64_t mx_tok_chunks(int64_t N, int E) { return N / 128 + E; }
+inline int64_t mx_tok_scale_bytes(int64_t N, int E, int64_t C) {
+  return ((C + 127) / 128) * mx_tok_chunks(N, E) * MX_CHUNK;
+}
 // an upper bound of sum_e ceil(rows_e / 128) for N rows over E experts
 inline int64_t mx_row_tiles(int64_t N, int E) { return (N + 127 * static_cast<int64_t>(E)) / 128 + 1; }
 inline int64_t mx_act_scale_bytes(int64_t N, int E, int64_t K) {
@@ -296,6 +306,11 @@ int launch_mx_pack_weight_scales(const uint8_t* s, int E, int R, int K, int swig
                                  int cols = 0);
 // G groups of R x C bf16 rows quantised in 32-row blocks down each column: codes in x's layout,
 // scales [G, R/32, C].
+// Token-direction blocks of x [N, C] bf16 inside the expert segments given by offsets [E+1]:
+// codes q [N, C], scales in the packed token-chunk layout (mx_tok_scale_bytes), chunk bases
+// cbase [E+1] (sum of ceil(n_e / 128) over the experts before e).
+int launch_mx_quantize_tokens(const void* x, int64_t N, int C, const int32_t* offsets, int E,
+                              uint8_t* q, uint8_t* s, int32_t* cbase, cudaStream_t st);
 int launch_mx_quantize_cols(const void* x, int G, int R, int C, uint8_t* q, uint8_t* s,
                             cudaStream_t st);
 // Permute + quantise: x_perm_q[slot(t, j)] = MXFP8 codes of x[t], scales in the packed

@@ -14,6 +14,9 @@
 //   permute_quant_mx_kernel  x [T, d] -> the permuted codes x_perm_q[slot] and its scales in the
 //                          packed activation layout (row tiles from the routing offsets), and
 //                          optionally the permuted bf16 rows themselves (for a bf16 backward)
+//   mx_quant_tokens_kernel the weight gradients' operands [N, C]: blocks of 32 rows down each
+//                          column inside every expert segment (the tokens are their reduction
+//                          dimension), codes in place, scales in the packed token-chunk layout
 #include "common.cuh"
 #include "internal.h"
 
@@ -202,6 +205,101 @@ __global__ void __launch_bounds__(MXP_THREADS) permute_quant_mx_kernel(
   }
 }
 
+// Token-direction blocks of the weight gradients' operands: one thread per (32-row block of an
+// expert segment, 2 adjacent columns) of x [N, C] bf16 (C % 32 == 0).  The blocks of expert e are
+// counted from its first row; its last block may be short (the missing rows are zeros for the
+// amax and store nothing).  Codes go to q in x's layout.  A block's scale byte goes to the packed
+// layout: 128-token chunk kc = cbase[e] + b / 4 of the expert segments (cbase[e] = sum_{e'<e}
+// ceil(n_e' / 128)), column tile c / 128, chunk at ((c / 128) * kct + kc) * 512, byte (c % 32) *
+// 16 + (c % 128 / 32) * 4 + b % 4; the later blocks of a segment's last chunk (no rows) get 127.
+// Block 0 writes cbase.  A warp covers 64 adjacent columns: 128-byte row reads, 64-byte code
+// rows.  The block's 32 rows are held as packed bf16 pairs between the amax and the rounding.
+constexpr int MXT_COLS = 2;   // columns per thread
+__global__ void __launch_bounds__(256) mx_quant_tokens_kernel(const bf16* __restrict__ x,
+                                                              const int32_t* __restrict__ offsets,
+                                                              int E, int C, int64_t N, int64_t kct,
+                                                              uint8_t* __restrict__ q,
+                                                              uint8_t* __restrict__ s,
+                                                              int32_t* __restrict__ cbase,
+                                                              int* err) {
+  __shared__ int s_off[MOE_MAX_EXPERTS + 1], s_bp[MOE_MAX_EXPERTS + 1], s_cp[MOE_MAX_EXPERTS + 1];
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) {
+    int bp = 0, cp = 0, bad = offsets[0] != 0;
+    for (int e = 0; e <= E; ++e) {
+      const int o = offsets[e];
+      s_off[e] = o;
+      s_bp[e] = bp;
+      s_cp[e] = cp;
+      if (e < E) {
+        const int n = offsets[e + 1] - o;
+        if (n < 0) bad = 1;
+        bp += (n + 31) / 32;
+        cp += (n + 127) / 128;
+      }
+    }
+    if (s_off[E] > N || cp > kct) bad = 1;
+    if (bad) record_error(err, DEVERR_BAD_OFFSETS);
+    s_bad = bad;
+  }
+  __syncthreads();
+  if (s_bad) return;
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) cbase[e] = s_cp[e];
+  const int CG = C / MXT_COLS;   // column groups
+  const int64_t total = static_cast<int64_t>(s_bp[E]) * CG;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const int c0 = static_cast<int>(i % CG) * MXT_COLS;
+    const int gb = static_cast<int>(i / CG);
+    int lo = 0, hi = E;   // the expert of block gb: the largest e with s_bp[e] <= gb
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_bp[mid] <= gb) lo = mid;
+      else hi = mid;
+    }
+    const int e = lo;
+    const int b = gb - s_bp[e];
+    const int n = s_off[e + 1] - s_off[e];
+    const int64_t r0 = s_off[e] + 32 * static_cast<int64_t>(b);
+    const int nr = min(32, n - 32 * b);
+    uint32_t raw[32];   // row j: columns c0, c0+1 as a bf16 pair
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      raw[j] = j < nr ? __ldg(reinterpret_cast<const uint32_t*>(x + (r0 + j) * C + c0)) : 0u;
+    float am[MXT_COLS] = {0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      am[0] = fmaxf(am[0], fabsf(__uint_as_float(raw[j] << 16)));
+      am[1] = fmaxf(am[1], fabsf(__uint_as_float(raw[j] & 0xffff0000u)));
+    }
+    int ex[MXT_COLS];
+    float inv[MXT_COLS];
+#pragma unroll
+    for (int u = 0; u < MXT_COLS; ++u) {
+      ex[u] = mx_exponent(am[u]);
+      inv[u] = mx_inv_scale(ex[u]);
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < nr)
+        *reinterpret_cast<uint16_t*>(q + (r0 + j) * C + c0) =
+            cvt_e4m3x2(__uint_as_float(raw[j] << 16) * inv[0],
+                       __uint_as_float(raw[j] & 0xffff0000u) * inv[1]);
+    const int64_t kc = s_cp[e] + b / 4;
+    const bool last = 32 * (b + 1) >= n;   // the segment's last block
+#pragma unroll
+    for (int u = 0; u < MXT_COLS; ++u) {
+      const int c = c0 + u, rr = c & 127;
+      uint8_t* row = s + ((c >> 7) * kct + kc) * MX_CHUNK + (rr & 31) * 16 + (rr >> 5) * 4;
+      row[b & 3] = static_cast<uint8_t>(ex[u] + 127);
+      if (last)   // the chunk's later blocks hold no rows
+        for (int j4 = (b & 3) + 1; j4 < 4; ++j4) row[j4] = 127;
+    }
+  }
+}
+
 int grid_for(int64_t items, int per_block) {
   int64_t b = (items + per_block - 1) / per_block;
   const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
@@ -235,6 +333,14 @@ int launch_mx_quantize_cols(const void* x, int G, int R, int C, uint8_t* q, uint
   if (n == 0) return MOE_OK;
   return launch("mxfp8_quantize_cols", mx_quant_cols_kernel, dim3(grid_for(n, 256)), dim3(256), 0,
                 st, static_cast<const bf16*>(x), G, R, C, q, s);
+}
+
+int launch_mx_quantize_tokens(const void* x, int64_t N, int C, const int32_t* offsets, int E,
+                              uint8_t* q, uint8_t* s, int32_t* cbase, cudaStream_t st) {
+  const int64_t items = (N / 32 + E) * static_cast<int64_t>(C / MXT_COLS);   // blocks <= N/32 + E
+  return launch("mxfp8_quantize_tokens", mx_quant_tokens_kernel, dim3(grid_for(items, 256)),
+                dim3(256), 0, st, static_cast<const bf16*>(x), offsets, E, C, N,
+                mx_tok_chunks(N, E), q, s, cbase, device_error_word());
 }
 
 int launch_permute_quant_mx(const void* x, const int32_t* sop, const int32_t* offsets,

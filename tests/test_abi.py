@@ -131,7 +131,7 @@ def test_mxfp8_entry_points_check_arguments():
     c = cfg(d=256, f=160)
     for which in range(4):
         assert L.moe_mxfp8_scale_bytes(ctypes.byref(c), which) > 0
-    assert L.moe_mxfp8_scale_bytes(ctypes.byref(c), 7) == 0
+    assert L.moe_mxfp8_scale_bytes(ctypes.byref(c), 10) == 0
     assert L.moe_mxfp8_scale_bytes(ctypes.byref(cfg(k=9)), moe.MX_SCALES_X) == 0
     # packed sizes: activations per 128-row tile and 128-element chunk, weights per 192-row tile
     N, E = 256 * 2, 8
@@ -153,6 +153,20 @@ def test_mxfp8_entry_points_check_arguments():
     assert b"W1_q" in L.moe_last_error()
     assert L.moe_layer_fwd_mxfp8(ctypes.byref(c), P, P, None, None, None, None, None, P, None, P,
                                  1 << 30, None, None) == -1
+    # the weight gradients' token-chunk layouts: ceil(C/128) column tiles x (N/128 + E) chunks
+    for which, C in ((moe.MX_SCALES_TOK_D, 256), (moe.MX_SCALES_TOK_F, 160),
+                     (moe.MX_SCALES_TOK_2F, 320)):
+        assert L.moe_mxfp8_scale_bytes(ctypes.byref(c), which) == -(-C // 128) * (N // 128 + E) * 512
+    assert L.moe_mxfp8_quantize_tokens(ctypes.byref(c), P, 48, P, P, P, P, None) == -2
+    assert L.moe_mxfp8_quantize_tokens(ctypes.byref(c), P, 64, None, P, P, P, None) == -1
+    assert L.moe_mxfp8_quantize_tokens(ctypes.byref(bad_f), P, 64, P, P, P, P, None) == -2
+    ws_need = L.moe_workspace_bytes(ctypes.byref(c), moe.WS_WGRAD_MXFP8)
+    assert ws_need >= N * (2 * 256 + 3 * 160)
+    assert L.moe_grouped_swiglu_wgrad_mxfp8(ctypes.byref(c), P, P, P, P, P, P, P, P, ws_need - 1,
+                                            None) == -3
+    assert L.moe_grouped_swiglu_wgrad_mxfp8(ctypes.byref(c), P, P, None, P, P, P, P, P, ws_need,
+                                            None) == -1
+    assert b"h" in L.moe_last_error()
 
 
 def test_binding_argument_counts_match_the_header():
