@@ -42,8 +42,15 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+FLAGS_STAMP = os.path.join(BUILD, "extra_flags.txt")
+
+
 def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
+    # objects built with other extra flags than now are stale too
+    prev = open(FLAGS_STAMP).read() if os.path.exists(FLAGS_STAMP) else None
+    if prev != " ".join(EXTRA):
+        force = True
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(INCLUDE, "moe_gb300.h"))
     cc = nvcc()
@@ -75,6 +82,8 @@ def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False) 
         if p.returncode != 0:
             sys.stderr.write(" ".join(cmd) + "\n" + p.stdout + p.stderr)
             raise RuntimeError("linking libmoe_gb300.so failed")
+    with open(FLAGS_STAMP, "w") as f:
+        f.write(" ".join(EXTRA))
     return LIB
 
 

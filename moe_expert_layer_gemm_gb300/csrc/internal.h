@@ -205,7 +205,8 @@ struct GemmDesc {
   const void* aux;
   int64_t ld_aux;
   const float* bias;
-  int* tile_ctr;           // RAGGED_K (bf16): device counter for run-time tile scheduling
+  int* tile_ctr;           // RAGGED_K: two device counters (8 bytes, 8-byte aligned) for
+                           // run-time tile scheduling
   // Gathered operand (bf16 only): row s of the operand is row gather[s] of the tensor the
   // Operand describes (A for RAGGED_M, with M rows; B for RAGGED_K, with K rows).  Null: plain.
   const int32_t* gather;
