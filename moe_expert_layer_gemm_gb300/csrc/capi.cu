@@ -1425,6 +1425,12 @@ int moe_grouped_swiglu_wgrad_mxfp8(const moe_cfg* c, const int32_t* offsets, con
   const WgMxWs w = carve_wgmx(cv, c);
   cudaStream_t st = S(stream);
   const int64_t N = Nrows(c);
+  if (N == 0) {   // no rows: every expert's weight gradients are zero blocks
+    if (cudaMemsetAsync(dW1, 0, sizeof(float) * c->E * 2 * c->f * c->d, st) != cudaSuccess ||
+        cudaMemsetAsync(dW2, 0, sizeof(float) * c->E * c->d * c->f, st) != cudaSuccess)
+      return fail(MOE_ERR_CUDA, "cudaMemsetAsync failed");
+    return MOE_OK;
+  }
   MOE_TRY(wgrad2_mx(c, offsets, N, dy_perm, h, dW2, w, w.sched, st));
   return wgrad1_mx(c, offsets, N, dH1, x_perm, dW1, w, w.sched + 4, st);
 }

@@ -187,3 +187,26 @@ def test_layer_backward_with_mxfp8_weight_gradients(name):
         errs[g + " vs oracle"] = rel_err(np64(gmx[g]), ref["bwd"][g])
         assert errs[g + " vs oracle"] < 0.2, errs
     print("mxfp8 weight gradients:", {k: f"{v:.3e}" for k, v in errs.items()})
+
+
+def test_zero_tokens():
+    """T = 0: the grouped weight gradients are zero blocks; the quantiser writes only the chunk
+    bases (all zero)."""
+    cfg = moe.make_cfg(0, 64, 4, 1, 64)
+    dev = "cuda"
+    # operand buffers (not read when there are no rows; one row each so that they are not null)
+    empty = torch.zeros(1, 64, dtype=torch.bfloat16, device=dev)
+    off = torch.zeros(5, dtype=torch.int32, device=dev)
+    dW1 = torch.full((4, 128, 64), float("nan"), device=dev)
+    dW2 = torch.full((4, 64, 64), float("nan"), device=dev)
+    ws = moe.workspace(cfg, moe.WS_WGRAD_MXFP8)
+    moe.moe_grouped_swiglu_wgrad_mxfp8(cfg, off, empty, empty, empty,
+                                       torch.zeros(1, 128, dtype=torch.bfloat16, device=dev),
+                                       dW1, dW2, ws)
+    cbase = torch.full((5,), -1, dtype=torch.int32, device=dev)
+    q = torch.empty(1, 64, dtype=torch.uint8, device=dev)
+    s = torch.empty(4 * 512, dtype=torch.uint8, device=dev)
+    moe.moe_mxfp8_quantize_tokens(cfg, empty, off, q, s, cbase)
+    sync()
+    assert not dW1.any() and not dW2.any()
+    assert not cbase.any()
