@@ -104,3 +104,44 @@ def test_sampled_rows_against_the_oracle(run):
     q2, s2 = MX.mx_quantize(h_gpu)
     assert np.array_equal(hq_gpu, q2) and np.array_equal(hs_all[slots], s2)
     assert_close("y_perm", y_gpu, ref_y, TOL_OUT)
+
+
+def test_weight_gradients_on_sampled_experts(run):
+    """moe_grouped_swiglu_wgrad_mxfp8 at full size on the layer's routing and bf16 h, x_perm from
+    the permute, seeded dy_perm and [da | du]: for the heaviest, median and lightest non-empty
+    experts, 64 sampled rows of dW1[e] and dW2[e] within fp32 accumulation of the oracle's fp64
+    token-block products.  A row i of dW1[e] needs only column i of [da | du] (column blocks are
+    independent) and all of x_perm's rows of e."""
+    lc, inp, m, saved, st = run
+    cfg = moe.cfg_from(lc)
+    N, d, f, E = lc.N, lc.d, lc.f, lc.E
+    bf = torch.bfloat16
+    off = saved["offsets"]
+    o = np64(off).astype(np.int64)
+    x_perm = torch.empty(N, d, dtype=bf, device="cuda")
+    moe.moe_permute(cfg, inp["x"], saved["slot_of_pair"], x_perm)
+    g = torch.Generator(device="cuda").manual_seed(7)
+    dy = (torch.randn(N, d, generator=g, device="cuda") * 0.1).to(bf)
+    dH = (torch.randn(N, 2 * f, generator=g, device="cuda") * 0.1).to(bf)
+    dW1 = torch.empty(E, 2 * f, d, device="cuda")
+    dW2 = torch.empty(E, d, f, device="cuda")
+    moe.moe_grouped_swiglu_wgrad_mxfp8(cfg, off, x_perm, st["h"], dy, dH, dW1, dW2,
+                                       moe.workspace(cfg, moe.WS_WGRAD_MXFP8))
+    torch.cuda.synchronize()
+    moe.check_device_error()
+    counts = np.diff(o)
+    order = [e for e in np.argsort(-counts, kind="stable") if counts[e] > 0]
+    rng = np.random.default_rng(3)
+    for e in (order[0], order[len(order) // 2], order[-1]):
+        lo, hi = int(o[e]), int(o[e + 1])
+        seg = [0, hi - lo]
+        r1 = np.sort(rng.choice(2 * f, 64, replace=False))
+        r2 = np.sort(rng.choice(d, 64, replace=False))
+        B1 = MX.mx_decode_segments(*MX.mx_quantize_segments(np64(x_perm[lo:hi]), seg), seg)
+        B2 = MX.mx_decode_segments(*MX.mx_quantize_segments(np64(st["h"][lo:hi]), seg), seg)
+        A1 = MX.mx_decode_segments(*MX.mx_quantize_segments(np64(dH[lo:hi, r1]), seg), seg)
+        A2 = MX.mx_decode_segments(*MX.mx_quantize_segments(np64(dy[lo:hi, r2]), seg), seg)
+        assert_close(f"dW1[{e}] ({hi - lo} rows)", np64(dW1[e][r1]), A1.T @ B1, 2e-5)
+        assert_close(f"dW2[{e}] ({hi - lo} rows)", np64(dW2[e][r2]), A2.T @ B2, 2e-5)
+    for e in np.nonzero(counts == 0)[0][:4]:
+        assert not dW1[e].any() and not dW2[e].any()
