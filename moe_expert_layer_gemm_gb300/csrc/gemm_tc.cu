@@ -1871,6 +1871,309 @@ __global__ void __launch_bounds__(pairk::THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------- row-ragged products on CTA pairs
+// A row-ragged product with bf16 output (fc2; the data gradient with MN-major weights) on CTA
+// pairs (tcgen05 cta_group::2): tiles of 256 rows (each CTA's 128, counted per group as in the
+// one-CTA kernel, so a group's last tile may run past its rows) by 256 columns.  Per k-block each
+// CTA loads its 128 A rows and 128 of the 256 B rows (K-major) or columns (MN-major): 32 KB per
+// SM instead of 48 for the same outputs, a third fewer operand bytes per FLOP.  Both CTAs walk
+// the same static tile sequence; the odd CTA's copies complete on the even CTA's barrier, the
+// even CTA's MMA warp issues the pair's MMAs and commits each stage and accumulator to both CTAs;
+// each CTA's epilogue stores its own 128 rows and releases the accumulator on the even CTA.
+namespace rpairk {
+constexpr int BN2 = 256;                  // output columns per pair tile
+constexpr int HB = BN2 / 2;               // B rows (K-major) or columns (MN-major) per CTA
+constexpr int A_ST = BM * BK * 2;         // 16 KB
+constexpr int B_ST = HB * BK * 2;         // 16 KB
+constexpr int EW = 4;                     // epilogue warps
+constexpr int SLABS_R = 2;
+constexpr int STAGING = EW * SLABS_R * SLAB;
+constexpr int AUX = 3072;
+constexpr int MAX_SMEM = 232448;
+constexpr int FIT = (MAX_SMEM - STAGING - AUX) / (A_ST + B_ST);
+constexpr int STAGES = FIT < 8 ? FIT : 8;
+constexpr int RING = STAGES * (A_ST + B_ST);
+constexpr int SMEM = RING + STAGING + AUX;
+constexpr int THREADS = 64 + 32 * EW;
+constexpr int TMEM_COLS = 512;            // two accumulators of 256 fp32 columns
+}  // namespace rpairk
+
+template <bool B_MN>
+__global__ void __launch_bounds__(rpairk::THREADS, 1)
+    tc_rows_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmO0, const KArgs p) {
+  using namespace rpairk;
+  using S = Sched<BN2, RAGGED_M, EPI_STORE, 2 * BM>;
+  constexpr int TM = 2 * BM;   // rows of a pair tile
+  constexpr uint32_t IDESC = ptx::idesc_bf16_f32(2 * BM, BN2, false, B_MN);
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_ST;
+  uint8_t* staging = smem + RING;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING + STAGING);   // even CTA's are used
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;           // even CTA's are used
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* s_bad = reinterpret_cast<int*>(tmem_holder + 2);
+  int* s_off = reinterpret_cast<int*>(tmem_holder + 4);
+  int* s_pre = s_off + (MAXG + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool even = rank == 0;
+  const int cid = static_cast<int>(blockIdx.x >> 1), ncl = static_cast<int>(gridDim.x >> 1);
+
+  if ((ptx::smem_u32(smem) & 1023u) != 0) {   // the same in both CTAs: both return
+    if (threadIdx.x == 0) record_error(p.err, DEVERR_SMEM_ALIGN);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      ptx::mbar_init(&full[i], 1);     // the even producer's arrival (with both CTAs' bytes)
+      ptx::mbar_init(&empty[i], 1);    // the pair's MMA commit
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&tfull[i], 1);
+      ptx::mbar_init(&tempty[i], 2 * EW);   // both CTAs' epilogue warps
+    }
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  for (int i = threadIdx.x; i <= p.G; i += blockDim.x)
+    s_off[i] = p.offsets ? p.offsets[i] : static_cast<int>((static_cast<int64_t>(p.M) * i) / p.G);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int bad = (s_off[0] < 0 || s_off[p.G] > p.M) ? 1 : 0;
+    for (int i = 0; i < p.G && !bad; ++i) bad = s_off[i + 1] < s_off[i];
+    *s_bad = bad;
+    if (bad && even) record_error(p.err, DEVERR_BAD_OFFSETS);
+  }
+  __syncthreads();
+  if (*s_bad) return;                    // the same decision in both CTAs
+  if (warp == 0) {
+    // s_pre[g] = sum_{g' < g} ceil(rows_g' / 256): lane L scans groups [L*per, (L+1)*per)
+    const int per = (p.G + 31) / 32;
+    const int lo = min(p.G, lane * per), hi = min(p.G, lo + per);
+    int local = 0;
+    for (int g = lo; g < hi; ++g) local += (s_off[g + 1] - s_off[g] + TM - 1) / TM;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int g = lo; g < hi; ++g) {
+      s_pre[g] = run;
+      run += (s_off[g + 1] - s_off[g] + TM - 1) / TM;
+    }
+    if (lane == 31) s_pre[p.G] = incl;
+  }
+  __syncthreads();
+  const int total = S::total(p, s_pre);
+  if (cid >= total) return;              // the same decision in both CTAs of the cluster
+  ptx::cluster_sync();                   // both CTAs' barriers exist before either touches them
+
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(tmem_holder, TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  auto even_addr = [&](const void* local) { return ptx::mapa(ptx::smem_u32(local), 0); };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producers (lane 0)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int armed[STAGES];
+      for (int i = 0; i < STAGES; ++i) armed[i] = -1;
+      const int m_off = static_cast<int>(rank) * BM;    // this CTA's rows of the pair tile
+      const int n_off = static_cast<int>(rank) * HB;    // this CTA's half of B
+      for (int tile = cid; tile < total && ok; tile += ncl) {
+        const TileInfo ti = S::decode(p, s_off, s_pre, nullptr, tile);
+        for (int kb = 0; kb < ti.kblocks; ++kb) {
+          const int kk = kb * BK;
+          uint8_t* a_dst = sA + stage * A_ST;
+          uint8_t* b_dst = sB + stage * B_ST;
+          if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+          const uint32_t fb = even_addr(&full[stage]);
+          if (even) {
+            ptx::mbar_arrive_expect_tx(&full[stage], 2 * (A_ST + B_ST));
+            armed[stage] = static_cast<int>(phase);
+          }
+          auto load = [&](void* dst, const CUtensorMap* m, int c0, int c1) {
+            if (even) ptx::tma_load_2d(dst, m, &full[stage], c0, c1);
+            else ptx::tma_load_2d_pair(dst, m, fb, c0, c1);
+          };
+          load(a_dst, &tmA, kk, ti.m0 + m_off);
+          if (!B_MN) {
+            load(b_dst, &tmB, kk, static_cast<int>(ti.g * p.b_group_rows) + ti.n0 + n_off);
+          } else {
+            const int krow = static_cast<int>(ti.g * p.b_group_rows) + kk;
+#pragma unroll
+            for (int c = 0; c < HB / 64; ++c) load(b_dst + c * (BK * 128), &tmB, ti.n0 + n_off + 64 * c, krow);
+          }
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok && even) {
+        // Unwinding: let every copy into an armed stage land before the CTA exits (bounded).
+        const uint64_t t0 = ptx::globaltimer();
+        for (int i = 0; i < STAGES; ++i) {
+          if (armed[i] < 0) continue;
+          while (!ptx::mbar_try_wait_acq_cluster(&full[i], static_cast<uint32_t>(armed[i])) &&
+                 ptx::globaltimer() - t0 < 100000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (even) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = cid; tile < total && ok; tile += ncl) {
+        const TileInfo ti = S::decode(p, s_off, s_pre, nullptr, tile);
+        if (!ptx::mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err)) break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN2);
+        for (int kb = 0; kb < ti.kblocks; ++kb) {
+          if (!ptx::mbar_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
+          ptx::tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a_addr = ptx::smem_u32(sA + stage * A_ST);
+            const uint32_t b_addr = ptx::smem_u32(sB + stage * B_ST);
+#pragma unroll
+            for (int k16 = 0; k16 < BK / 16; ++k16) {
+              const uint64_t ad = ptx::smem_desc_sw128(a_addr + k16 * 32, 16, 1024);
+              const uint64_t bd = B_MN ? ptx::smem_desc_sw128(b_addr + k16 * 2048, BK * 128, 1024)
+                                       : ptx::smem_desc_sw128(b_addr + k16 * 32, 16, 1024);
+              ptx::umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k16) != 0 ? 1u : 0u);
+            }
+            // frees the stage in both CTAs
+            ptx::umma_commit_pair(ptx::mapa(ptx::smem_u32(&empty[stage]), 0));
+            ptx::umma_commit_pair(ptx::mapa(ptx::smem_u32(&empty[stage]), 1));
+          }
+          __syncwarp();
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        if (lane == 0) {   // both CTAs' epilogues
+          ptx::umma_commit_pair(ptx::mapa(ptx::smem_u32(&tfull[acc]), 0));
+          ptx::umma_commit_pair(ptx::mapa(ptx::smem_u32(&tfull[acc]), 1));
+        }
+        __syncwarp();
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int e = warp - 2;
+    const int q = warp & 3;
+    uint8_t* slabs = staging + e * (SLABS_R * SLAB);
+    int slab_sel = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    auto next_slab = [&]() -> uint8_t* {
+      if (lane == 0) ptx::bulk_wait_read<SLABS_R - 1>();
+      __syncwarp();
+      uint8_t* sl = slabs + slab_sel * SLAB;
+      if (++slab_sel == SLABS_R) slab_sel = 0;
+      return sl;
+    };
+    for (int tile = cid; tile < total; tile += ncl) {
+      const TileInfo ti = S::decode(p, s_off, s_pre, nullptr, tile);
+      const int row0 = ti.m0 + static_cast<int>(rank) * BM + q * 32;   // this warp's first row
+      const int rows_here = min(32, ti.m_end - row0);
+      const int row = row0 + lane;
+      if (!ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err)) break;
+      ptx::tc_fence_after();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * BN2);
+      if (rows_here == 32) {
+        // whole slabs out through TMA (the map clips at the tensor's columns)
+#pragma unroll 1
+        for (int c = 0; c < BN2; c += 64) {
+          const int col = ti.n0 + c;
+          if (col >= p.N) break;
+          uint32_t v0[32], v1[32];
+          ptx::tmem_ld32(t_row + c, v0);
+          ptx::tmem_ld32(t_row + c + 32, v1);
+          ptx::tmem_ld_wait();
+          uint8_t* slab = next_slab();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float a[8], b[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              a[i] = __uint_as_float(v0[8 * j + i]);
+              b[i] = __uint_as_float(v1[8 * j + i]);
+            }
+            slab_put(slab, lane, j, pack16(a, static_cast<const bf16*>(nullptr)));
+            slab_put(slab, lane, 4 + j, pack16(b, static_cast<const bf16*>(nullptr)));
+          }
+          slab_store_2d(&tmO0, slab, lane, col, row0);
+        }
+      } else if (rows_here > 0) {
+        // the group's last rows: masked stores (a whole slab would overwrite the next group's)
+#pragma unroll 1
+        for (int c = 0; c < BN2; c += 32) {
+          const int col = ti.n0 + c;
+          if (col >= p.N) break;
+          uint32_t v32[32];
+          ptx::tmem_ld32(t_row + c, v32);
+          ptx::tmem_ld_wait();
+          if (lane < rows_here) {
+            const int ncol = min(32, p.N - col);
+            bf16* o = static_cast<bf16*>(p.out) + row * p.ldo + col;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              if (v * 8 >= ncol) break;
+              float fv[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) fv[i] = __uint_as_float(v32[v * 8 + i]);
+              st16(o + v * 8, pack16(fv, static_cast<const bf16*>(nullptr)));
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (even) ptx::mbar_arrive(&tempty[acc]);
+        else ptx::mbar_arrive_remote(even_addr(&tempty[acc]));
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) ptx::bulk_wait_all();
+    __syncwarp();
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();   // neither CTA leaves while the other may still use its barriers or TMEM
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -2142,6 +2445,65 @@ int run_wgrad_pair(const GemmDesc& g, cudaStream_t st) {
                          SMEM, 2, st, ma, mb, mo, a);
 }
 
+// Row-ragged bf16 products (fc2, the data gradients) on CTA pairs (tc_rows_pair_kernel).
+#ifndef MOE_PAIR_ROWS
+#define MOE_PAIR_ROWS 0
+#endif
+template <bool B_MN>
+int run_rows_pair(const GemmDesc& g, cudaStream_t st) {
+  using namespace rpairk;
+  const char* name = g.name ? g.name : (B_MN ? "gemm_dgrad" : "gemm_fc2");
+  auto kern = tc_rows_pair_kernel<B_MN>;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  static int clusters[64];
+  std::call_once(attr_once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  });
+  if (attr_err != cudaSuccess) {
+    set_error("cudaFuncSetAttribute(%s, %d bytes): %s", name, SMEM, cudaGetErrorString(attr_err));
+    return MOE_ERR_CUDA;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (!clusters[dev]) {   // pairs resident at once: one persistent wave
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms() & ~1);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = num_sms() / 2;
+    }
+    clusters[dev] = n < num_sms() / 2 ? n : num_sms() / 2;
+  }
+  CUtensorMap ma, mb, mo;
+  MOE_TRY(map_operand(&ma, g.A, BM));
+  MOE_TRY(map_operand(&mb, g.B, B_MN ? BK : HB));
+  MOE_TRY(map_bf16(&mo, g.out, g.M, g.N, g.ldo, 32));
+  KArgs a;
+  memset(&a, 0, sizeof(a));
+  a.G = g.G;
+  a.offsets = g.offsets;
+  a.M = g.M;
+  a.N = g.N;
+  a.K = g.K;
+  a.b_group_rows = g.b_group_rows;
+  a.out = g.out;
+  a.ldo = g.ldo;
+  a.err = device_error_word();
+  return launch_clusters(name, kern, dim3(2 * clusters[dev]), dim3(THREADS), SMEM, 2, st, ma, mb,
+                         mo, a);
+}
+
 }  // namespace
 
 int gemm_tc(const GemmDesc& g, cudaStream_t st) {
@@ -2208,6 +2570,8 @@ int gemm_tc(const GemmDesc& g, cudaStream_t st) {
     if (g.epi == EPI_SWIGLU_BWD && g.B.mn_major)
       return n192 ? run<192, false, true, RAGGED_M, EPI_SWIGLU_BWD>(g, "gemm_fc2_dgrad_swiglu_bwd", st)
                   : run<256, false, true, RAGGED_M, EPI_SWIGLU_BWD>(g, "gemm_fc2_dgrad_swiglu_bwd", st);
+    if (MOE_PAIR_ROWS && g.epi == EPI_STORE && !n192)
+      return g.B.mn_major ? run_rows_pair<true>(g, st) : run_rows_pair<false>(g, st);
     if (g.epi == EPI_STORE && !g.B.mn_major)
       return n192 ? run<192, false, false, RAGGED_M, EPI_STORE>(g, "gemm_fc2", st)
                   : run<256, false, false, RAGGED_M, EPI_STORE>(g, "gemm_fc2", st);
