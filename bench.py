@@ -1080,6 +1080,95 @@ def run_route_only(args, lc):
             "paths": out}
 
 
+def run_wgrad_routings(args, lc):
+    """The routed experts' backward (moe_grouped_swiglu_bwd) on the workload's expert shapes under
+    several per-expert row distributions with the same total rows N = T*k where the distribution
+    allows: the workload's own routing (moe_route_topk on its seeded tokens), uniform, N/8 rows on
+    8 experts (the others empty), 64 rows on every expert and one row on every expert.  Operands
+    are seeded Gaussians; each distribution is timed per kernel with the CUDA-event trace over
+    `steps` calls after `warmup` eager ones.  For each weight gradient the line gives its
+    reduction FLOPs (2 per multiply-add, padded k-blocks not counted) and its fp32 block bytes."""
+    import numpy as np
+    import torch
+
+    import moe_expert_layer_gemm_gb300 as moe
+    from moe_expert_layer_gemm_gb300 import build as _build
+
+    if not os.path.exists(moe._lib.LIB_PATH):
+        _build.build()
+    moe.lib()
+    dev = torch.device("cuda", 0)
+    E, d, f, N = lc.E, lc.d, lc.f, lc.T * lc.k
+    # the workload's routing: counts from the library's own routing of the seeded tokens
+    inp = moe_inputs.make_layer_inputs(lc, seed=args.seed, device=dev)
+    cfg_r = moe.cfg_from(lc)
+    i32 = torch.int32
+    counts = torch.empty(E, dtype=i32, device=dev)
+    offsets = torch.empty(E + 1, dtype=i32, device=dev)
+    moe.moe_route_topk(cfg_r, inp["x"], inp["W_r"], inp["b_r"], None,
+                       torch.empty(lc.T, E, device=dev),
+                       torch.empty(lc.T, lc.k, dtype=i32, device=dev),
+                       torch.empty(lc.T, lc.k, device=dev), counts, offsets,
+                       torch.empty(lc.T, lc.k, dtype=i32, device=dev),
+                       torch.empty(N, dtype=i32, device=dev), moe.workspace(cfg_r, moe.WS_ROUTE, dev))
+    own = counts.cpu().numpy().astype(np.int64)
+    del inp
+    torch.cuda.empty_cache()
+    uni = np.full(E, N // E, np.int64)
+    uni[: N - uni.sum()] += 1
+    hot = np.zeros(E, np.int64)
+    hot[:8] = N // 8
+    hot[: N - hot.sum()] += 1
+    dists = {"workload": own, "uniform": uni, "8_experts": hot,
+             "64_rows_each": np.full(E, 64, np.int64), "1_row_each": np.ones(E, np.int64)}
+    g = torch.Generator(device=dev)
+    g.manual_seed(args.seed)
+    bf = torch.bfloat16
+    rows = max(int(c.sum()) for c in dists.values())
+    xp = torch.randn(rows, d, device=dev, generator=g).to(bf)
+    act = torch.randn(rows, 2 * f, device=dev, generator=g).to(bf)
+    h = torch.randn(rows, f, device=dev, generator=g).to(bf)
+    dyp = torch.randn(rows, d, device=dev, generator=g).to(bf)
+    dxp = torch.empty(rows, d, device=dev, dtype=bf)
+    W1 = (torch.randn(E, 2 * f, d, device=dev, generator=g) * 0.02).to(bf)
+    W2 = (torch.randn(E, d, f, device=dev, generator=g) * 0.02).to(bf)
+    dW1 = torch.empty(E, 2 * f, d, device=dev)
+    dW2 = torch.empty(E, d, f, device=dev)
+    out = {}
+    for name, c in dists.items():
+        n = int(c.sum())
+        cfg = moe.make_cfg(n, d, E, 1, f)
+        ws = moe.workspace(cfg, moe.WS_FFN_BWD, dev)
+        off = torch.tensor(np.concatenate([[0], np.cumsum(c)]), dtype=i32, device=dev)
+        call = lambda: moe.moe_grouped_swiglu_bwd(cfg, xp, off, W1, W2, act, h, dyp, dxp, dW1, dW2, ws)
+        for _ in range(args.warmup):
+            call()
+        torch.cuda.synchronize()
+        moe.trace_read()
+        moe.trace_enable(True)
+        for _ in range(args.steps):
+            call()
+        torch.cuda.synchronize()
+        moe.trace_enable(False)
+        tr = moe.trace_read()
+        moe.check_device_error()
+        ms = {k_: round(t / max(1, cnt), 4) for k_, (cnt, t) in tr.items()}
+        out[name] = {"rows": n, "max_rows": int(c.max()), "experts_with_rows": int((c > 0).sum()),
+                     "kernels_ms": ms,
+                     "fc1_wgrad": {"tflop": round(4.0 * n * d * f / 1e12, 4),
+                                   "fp32_gb": round(E * 2 * f * d * 4 / 1e9, 3)},
+                     "fc2_wgrad": {"tflop": round(2.0 * n * d * f / 1e12, 4),
+                                   "fp32_gb": round(E * d * f * 4 / 1e9, 3)}}
+        del ws
+    return {"metric": "routed-expert backward kernel times under per-expert row distributions",
+            "value": out["workload"]["kernels_ms"].get("gemm_fc1_wgrad"), "unit": "ms",
+            "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "data": "synthetic (seeded Gaussian operands; the workload's own routing counts)",
+            "config": {"workload": lc.name, "d_model": d, "experts": E, "ffn": f, "N": N,
+                       "timing": "per-kernel CUDA events, eager calls"},
+            "distributions": out}
+
+
 def run_reference(args, lc):
     """The fp64 CPU oracle as the reference arm: each step is the oracle's forward + backward on
     a bounded, seeded sample of the same workload's tokens (all experts)."""
@@ -1142,6 +1231,9 @@ def main():
     ap.add_argument("--route-only", action="store_true",
                     help="time moe_route_topk alone on the workload's tokens (from x through the "
                          "router GEMM, and from given logits); prints its own JSON line")
+    ap.add_argument("--wgrad-routings", action="store_true",
+                    help="time the routed experts' backward kernels under several per-expert row "
+                         "distributions of the workload's shapes; prints its own JSON line")
     args = ap.parse_args()
     if args.fp8 and args.mxfp8:
         ap.error("--fp8 and --mxfp8 are exclusive")
@@ -1151,6 +1243,8 @@ def main():
         lc = lc.replace(backward=False)
     if args.route_only:
         out = run_route_only(args, lc)
+    elif args.wgrad_routings:
+        out = run_wgrad_routings(args, lc)
     else:
         out = run_reference(args, lc) if args.impl == "reference" else run_gpu(args, lc)
     if out is not None:

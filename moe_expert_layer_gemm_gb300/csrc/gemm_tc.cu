@@ -112,20 +112,39 @@ __device__ __forceinline__ int claim_tile(int* ctr, int total, int& nclaims) {
 #define MOE_WGRAD_LSU_STORE 0
 #endif
 
+// Weight-gradient stores paced: for tiles whose reduction is 2..MOE_WGRAD_PACE_KB k-blocks, an
+// epilogue warp issues its next fp32 slab only once its previous stores have landed in memory
+// (one 4 KB store in flight per warp), rather than once the TMA engine has read them out of
+// shared memory.  Such tiles' MMAs take about as long as their 128 KB of stores, and unpaced a
+// burst of stores costs an SM about as long as its operand loads, with no overlap between the
+// two.  Pacing every tile, on the 128-expert layer: uniform routing (768 rows per expert) fc1's
+// weight gradient 1.74-1.75 -> 1.64 ms, fc2's 0.89 -> 0.85 ms; MTP-256e (about 1024 rows per
+// expert) 0.95 -> 0.90 and 0.51 -> 0.49 ms; 64 rows per expert, 8 experts of 12288 rows and the
+// DeepSeek-style routing unchanged or up to 2% slower -- hence the window (0: never paced).
+#ifndef MOE_WGRAD_PACE_KB
+#define MOE_WGRAD_PACE_KB 32
+#endif
+
 #ifndef MOE_TILE192
 #define MOE_TILE192 0
 #endif
 
 constexpr int FEED = 8;   // depth of the ring that passes run-time tile indices to the consumers
 
-// Staging slabs per epilogue warp: the SwiGLU backward needs two (saved a and u); weight
-// gradients take MOE_WGRAD_SLABS (stores in flight per warp); with 8 epilogue warps the others
-// make do with one so that the ring keeps four stages.
+// Staging slabs per epilogue warp: the SwiGLU backward takes one (32 columns of the saved a and
+// of u side by side, 64-byte swizzle), which leaves room for a fourth ring stage -- with two
+// slabs of 64 columns each the ring had three stages and fc2's data gradient on the 128-expert
+// layer took 0.98 ms instead of 0.87 (MOE_SWIGLU_BWD_ONESLAB=0 keeps that form; the MXFP8
+// backward keeps it too); weight gradients take MOE_WGRAD_SLABS (stores in flight per warp);
+// with 8 epilogue warps the others make do with one so that the ring keeps four stages.
 #ifndef MOE_WGRAD_SLABS
 #define MOE_WGRAD_SLABS 2
 #endif
+#ifndef MOE_SWIGLU_BWD_ONESLAB
+#define MOE_SWIGLU_BWD_ONESLAB 1
+#endif
 template <int SCHED, int EPI, int EPI_WARPS> struct SlabsPerWarp {
-  static constexpr int n = EPI == EPI_SWIGLU_BWD ? 2
+  static constexpr int n = EPI == EPI_SWIGLU_BWD ? (MOE_SWIGLU_BWD_ONESLAB ? 1 : 2)
                          : SCHED == RAGGED_K ? MOE_WGRAD_SLABS
                          : EPI_WARPS == 4 ? 2 : 1;
 };
@@ -192,7 +211,11 @@ template <int BN> struct MxCfg {
 // fourth ring stage beside their block scales.
 template <int BN, int SCHED, int EPI, bool F8, bool MX> struct EpiOf {
   static constexpr bool staged = OutPath<SCHED, EPI>::tma;
-  static constexpr int slabs = (MX && BN == 256) ? 1 : EpiWidth<BN, SCHED, EPI, F8>::slabs;
+  static constexpr int slabs = (MX && BN == 256) ? 1
+                              : (MX && EPI == EPI_SWIGLU_BWD) ? 2   // (the two-slab loop)
+                                                              : EpiWidth<BN, SCHED, EPI, F8>::slabs;
+  // the SwiGLU backward's one-slab loop (bf16 and tensorwise E4M3)
+  static constexpr bool half_slabs = EPI == EPI_SWIGLU_BWD && !MX && MOE_SWIGLU_BWD_ONESLAB;
 };
 // The router product (fp32 logits, bf16 operands) routes its tokens in the epilogue.
 template <int SCHED, int EPI, bool F8> struct RouterOf {
@@ -345,6 +368,14 @@ __device__ __forceinline__ void slab_put(uint8_t* slab, int lane, int j, const u
 __device__ __forceinline__ uint4 slab_get(const uint8_t* slab, int lane, int j) {
   return *reinterpret_cast<const uint4*>(slab + lane * 128 + ((j ^ (lane & 7)) << 4));
 }
+// A half slab is 32 rows x 64 bytes laid out as the 64-byte-swizzled box of a TMA map: the
+// 16-byte chunk j (0..3) of row r sits at r*64 + ((j ^ ((r >> 1) & 3)) * 16).
+__device__ __forceinline__ void half_put(uint8_t* h, int lane, int j, const uint4& v) {
+  *reinterpret_cast<uint4*>(h + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = v;
+}
+__device__ __forceinline__ uint4 half_get(const uint8_t* h, int lane, int j) {
+  return *reinterpret_cast<const uint4*>(h + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4));
+}
 // Make the warp's slab writes visible to the TMA engine, then store the slab (lane 0).
 __device__ __forceinline__ void slab_store_2d(const CUtensorMap* m, const uint8_t* slab, int lane,
                                               int c0, int c1) {
@@ -374,6 +405,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
   constexpr bool TMA_OUT = OutPath<SCHED, EPI>::tma;
   constexpr int EPI_WARPS = EpiWidth<BN, SCHED, EPI, F8>::warps;
   constexpr int SLABS = EpiOf<BN, SCHED, EPI, F8, MX>::slabs;
+  constexpr bool HALF_SLABS = EpiOf<BN, SCHED, EPI, F8, MX>::half_slabs;
   using C = typename CfgOf<BN, SCHED, EPI, F8, MX>::type;
   constexpr bool DYN = DynMode<SCHED, EPI>::on;
   // gathered operands: A of a row-ragged product (K-major) or B of a weight gradient (MN-major)
@@ -878,10 +910,13 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
         st16_cs(base + static_cast<int64_t>(row + r) * p.ldo + c4, v);
       }
     };
-    // Next free staging slab of this warp: at most SLABS-1 earlier stores may still read theirs.
+    // Next free staging slab of this warp: at most SLABS-1 earlier stores may still read theirs
+    // (a paced weight-gradient tile: every earlier store has landed).
+    bool pace = false;
     auto next_slab = [&]() -> uint8_t* {
       if (lane == 0) {
-        ptx::bulk_wait_read<SLABS - 1>();
+        if (SCHED == RAGGED_K && pace) ptx::bulk_wait<0>();
+        else ptx::bulk_wait_read<SLABS - 1>();
       }
       __syncwarp();
       uint8_t* s = slabs + slab_sel * SLAB;
@@ -905,6 +940,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
         if (tile >= total) break;
       }
       const TileInfo ti = S::decode(p, s_off, s_pre, s_ord, tile);
+      pace = SCHED == RAGGED_K && ti.kblocks >= 2 && ti.kblocks <= MOE_WGRAD_PACE_KB;
       const int m_cta = ti.m0;                      // this CTA's rows of the tile
       const int row0 = m_cta + q * 32;              // first row of this warp's slab
       const int rows_here = min(32, ti.m_end - row0);
@@ -1200,6 +1236,58 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
             if (blk == nb2 - 1) {
               for (int j = (blk & 3) + 1; j < 4; ++j) sf[j] = 127;   // blocks past 2f: 2^0
             }
+          }
+        }
+      } else if (tma_slab && HALF_SLABS) {
+        // acc = dh for f columns n0 .. n0+BN, 32 at a time.  The slab's two halves take the
+        // saved a and u of those columns (TMA, map tmO2 over act with 32 x 32 boxes), then the
+        // results da and du in their place, stored by TMA (maps tmO0, tmO1).
+        uint8_t* ha = slabs;
+        uint8_t* hu = slabs + SLAB / 2;
+#pragma unroll 1
+        for (int c = c_lo; c < c_hi; c += 32) {
+          const int col = ti.n0 + c;
+          if (col >= p.f) break;
+          if (lane == 0) {
+            ptx::bulk_wait_read<0>();   // the slab's previous stores have read it
+            ptx::mbar_arrive_expect_tx(my_bar, SLAB);
+            ptx::tma_load_2d(ha, &tmO2, my_bar, col, row0);
+            ptx::tma_load_2d(hu, &tmO2, my_bar, p.f + col, row0);
+          }
+          __syncwarp();
+          uint32_t dh[32];
+          ptx::tmem_ld32(t_row + c, dh);   // in flight while the loads land
+          const bool landed = ptx::mbar_wait(my_bar, ld_phase, abort_flag, p.err);
+          ptx::tmem_ld_wait(dh);
+          if (!landed) { aborted = true; break; }
+          ld_phase ^= 1u;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float av[8], uv[8], da[8], du[8];
+            unpack16(half_get(ha, lane, j), av, static_cast<const bf16*>(nullptr));
+            unpack16(half_get(hu, lane, j), uv, static_cast<const bf16*>(nullptr));
+            // columns past f (an edge tile) are never stored: keep them out of the amax
+            const bool live = col + 8 * j < p.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float g = __uint_as_float(dh[8 * j + i]) * sc;
+              const float s = sigmoid_f<F8 && MOE_FAST_SIGMOID_F8>(av[i]);
+              da[i] = g * uv[i] * (s + av[i] * s * (1.0f - s));
+              du[i] = g * av[i] * s;
+              if (live) {
+                track(da[i]);
+                track(du[i]);
+              }
+            }
+            half_put(ha, lane, j, pack16(da, static_cast<const bf16*>(nullptr)));
+            half_put(hu, lane, j, pack16(du, static_cast<const bf16*>(nullptr)));
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(&tmO0, ha, col, row0);
+            ptx::tma_store_2d(&tmO1, hu, col, row0);
+            ptx::bulk_commit();
           }
         }
       } else if (tma_slab && EPI == EPI_SWIGLU_BWD) {
@@ -2194,9 +2282,11 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// A tensor map with 128-byte swizzle; out-of-bounds elements read as zero and are not written.
+// A tensor map with 128-byte (or the given) swizzle; out-of-bounds elements read as zero and are
+// not written.
 int encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
-           const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+           const cuuint64_t* strides_bytes, const cuuint32_t* box,
+           CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     set_error("cuTensorMapEncodeTiled is not available from the driver");
@@ -2204,7 +2294,7 @@ int encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, c
   }
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = fn(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides_bytes,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     set_error("cuTensorMapEncodeTiled failed (%d): rank=%d dims=%llu,%llu box=%u,%u", (int)r, rank,
@@ -2220,6 +2310,16 @@ int map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
   cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box);
+}
+
+// bf16 rows x cols with row pitch ld (elements); box = 32 columns x 32 rows, 64-byte swizzle (a
+// half slab).
+int map_bf16_half(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {32u, 32u};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // fp32 [G][rows][cols] (group stride gs, row pitch ld, elements); box = 32 x 32 x 1.
@@ -2282,6 +2382,10 @@ int run(const GemmDesc& g, const char* kind, cudaStream_t st) {
       MOE_TRY(map_bf16(&mo[1], g.out2, rows, g.f, g.ldo2, 32));
       MOE_TRY(map_bf16(&mo[2], static_cast<const bf16*>(g.out2) + g.f, rows, g.f, g.ldo2, 32));
     }
+  } else if (EpiOf<BN, SCHED, EPI, F8, MX>::half_slabs) {   // the SwiGLU backward, one slab
+    MOE_TRY(map_bf16_half(&mo[0], g.out, rows, g.f, g.ldo));
+    MOE_TRY(map_bf16_half(&mo[1], static_cast<const bf16*>(g.out) + g.f, rows, g.f, g.ldo));
+    MOE_TRY(map_bf16_half(&mo[2], g.aux, rows, 2 * static_cast<int64_t>(g.f), g.ld_aux));
   } else if (EPI == EPI_SWIGLU_BWD && (!MX || g.out)) {   // (MXFP8 without bf16 out: direct stores)
     MOE_TRY(map_bf16(&mo[0], g.out, rows, g.f, g.ldo, 32));
     MOE_TRY(map_bf16(&mo[1], static_cast<const bf16*>(g.out) + g.f, rows, g.f, g.ldo, 32));
