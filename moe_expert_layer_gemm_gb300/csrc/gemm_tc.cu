@@ -19,6 +19,9 @@
 //              store, overlapped with the next tile's MMAs through the second accumulator
 // Tiles are BM=128 rows x BN columns x BK=64; a CTA walks tiles blockIdx.x, blockIdx.x +
 // gridDim.x, ... or, for the weight gradients, claims them at run time.
+// Beside it: tc_rows_tall_kernel (the bf16-store row-ragged products on 256 x 256 tiles, two
+// MMAs per K step sharing each B stage), tc_wgrad_pair_kernel (one-group weight gradients on
+// CTA pairs) and tc_rows_pair_kernel (a measured option, off).
 #include <cuda.h>
 #include <string.h>
 
@@ -1959,6 +1962,281 @@ __global__ void __launch_bounds__(pairk::THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------- row-ragged products, tall tiles
+// A row-ragged product with bf16 output (fc2; the data gradient with MN-major weights) on tiles
+// of 256 rows x 256 columns per CTA: per k-block the CTA loads two 128-row A boxes and one
+// 256-row B stage (64 KB) and issues two M = 128, N = 256 MMAs per K step that share the B stage,
+// one into each half of TMEM (rows 0..127 in columns 0..255, rows 128..255 in 256..511).  A
+// one-CTA 128 x 256 tile takes 48 KB per 128 x 256 x 64 k-block; this takes 32 KB for the same
+// work.  A group's rows are cut into 256-row tiles, and a last tile of at most 128 rows issues
+// only the first half's MMAs (and loads only that half of A), so groups are padded as with
+// 128-row tiles.  One accumulator set fills TMEM: each epilogue warp copies its 32 rows x 256
+// columns into registers (bf16) and releases the accumulator before it stores them, so the next
+// tile's MMAs wait only for those copies.  Ring: 3 stages of 64 KB; 8 epilogue warps (a TMEM
+// lane quadrant and a half each), one staging slab each.
+namespace tallk {
+constexpr int TM = 2 * BM;                // rows of a tile
+constexpr int BN2 = 256;                  // columns of a tile
+constexpr int A_ST = TM * BK * 2;         // 32 KB (two 128-row boxes)
+constexpr int B_ST = BN2 * BK * 2;        // 32 KB
+constexpr int EW = 8;                     // epilogue warps
+constexpr int STAGING = EW * SLAB;
+constexpr int AUX = 3072;
+constexpr int MAX_SMEM = 232448;
+constexpr int STAGES = (MAX_SMEM - STAGING - AUX) / (A_ST + B_ST);
+constexpr int RING = STAGES * (A_ST + B_ST);
+constexpr int SMEM = RING + STAGING + AUX;
+constexpr int THREADS = 64 + 32 * EW;
+constexpr int TMEM_COLS = 512;
+static_assert(STAGES >= 3, "tall tiles need three ring stages");
+}  // namespace tallk
+
+template <bool B_MN>
+__global__ void __launch_bounds__(tallk::THREADS, 1)
+    tc_rows_tall_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmO0, const KArgs p) {
+  using namespace tallk;
+  using S = Sched<BN2, RAGGED_M, EPI_STORE, TM>;
+  constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN2, false, B_MN);
+  constexpr int MN_CHUNK = BK * 128;      // one 64-column MN-major chunk of a stage
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_ST;
+  uint8_t* staging = smem + RING;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING + STAGING);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* s_bad = reinterpret_cast<int*>(tmem_holder + 2);
+  int* s_off = reinterpret_cast<int*>(tmem_holder + 4);
+  int* s_pre = s_off + (MAXG + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = static_cast<int>(blockIdx.x), units = static_cast<int>(gridDim.x);
+
+  if ((ptx::smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) record_error(p.err, DEVERR_SMEM_ALIGN);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&empty[i], 1);
+    }
+    ptx::mbar_init(tfull, 1);
+    ptx::mbar_init(tempty, EW);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  for (int i = threadIdx.x; i <= p.G; i += blockDim.x)
+    s_off[i] = p.offsets ? p.offsets[i] : static_cast<int>((static_cast<int64_t>(p.M) * i) / p.G);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int bad = (s_off[0] < 0 || s_off[p.G] > p.M) ? 1 : 0;
+    for (int i = 0; i < p.G && !bad; ++i) bad = s_off[i + 1] < s_off[i];
+    *s_bad = bad;
+    if (bad) record_error(p.err, DEVERR_BAD_OFFSETS);
+  }
+  __syncthreads();
+  if (*s_bad) return;
+  if (warp == 0) {
+    // s_pre[g] = sum_{g' < g} ceil(rows_g' / 256): lane L scans groups [L*per, (L+1)*per)
+    const int per = (p.G + 31) / 32;
+    const int lo = min(p.G, lane * per), hi = min(p.G, lo + per);
+    int local = 0;
+    for (int g = lo; g < hi; ++g) local += (s_off[g + 1] - s_off[g] + TM - 1) / TM;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int g = lo; g < hi; ++g) {
+      s_pre[g] = run;
+      run += (s_off[g + 1] - s_off[g] + TM - 1) / TM;
+    }
+    if (lane == 31) s_pre[p.G] = incl;
+  }
+  __syncthreads();
+  const int total = S::total(p, s_pre);
+  if (unit >= total) return;
+
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_holder, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (lane 0)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int armed[STAGES];
+      for (int i = 0; i < STAGES; ++i) armed[i] = -1;
+      bool ok = true;
+      for (int tile = unit; tile < total && ok; tile += units) {
+        const TileInfo ti = S::decode(p, s_off, s_pre, nullptr, tile);
+        const bool tall = ti.m_end - ti.m0 > BM;
+        const uint32_t tx = static_cast<uint32_t>((tall ? 2 : 1) * BM * BK * 2 + B_ST);
+        const int brow = static_cast<int>(ti.g * p.b_group_rows);
+        for (int kb = 0; kb < ti.kblocks; ++kb) {
+          const int kk = kb * BK;
+          if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(&full[stage], tx);
+          armed[stage] = static_cast<int>(phase);
+          uint8_t* a_dst = sA + stage * A_ST;
+          uint8_t* b_dst = sB + stage * B_ST;
+          ptx::tma_load_2d(a_dst, &tmA, &full[stage], kk, ti.m0);
+          if (tall) ptx::tma_load_2d(a_dst + BM * BK * 2, &tmA, &full[stage], kk, ti.m0 + BM);
+          if (!B_MN) {
+            ptx::tma_load_2d(b_dst, &tmB, &full[stage], kk, brow + ti.n0);
+          } else {
+#pragma unroll
+            for (int c = 0; c < BN2 / 64; ++c)
+              ptx::tma_load_2d(b_dst + c * MN_CHUNK, &tmB, &full[stage], ti.n0 + 64 * c, brow + kk);
+          }
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // Unwinding: let every copy this thread issued land before the CTA exits (bounded).
+        for (int i = 0; i < STAGES; ++i) {
+          if (armed[i] < 0) continue;
+          const uint64_t t0 = ptx::globaltimer();
+          while (!ptx::mbar_try_wait(&full[i], static_cast<uint32_t>(armed[i])) &&
+                 ptx::globaltimer() - t0 < 100000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = unit; tile < total && ok; tile += units) {
+      const TileInfo ti = S::decode(p, s_off, s_pre, nullptr, tile);
+      const bool tall = ti.m_end - ti.m0 > BM;
+      if (!ptx::mbar_wait(tempty, acc_phase ^ 1u, abort_flag, p.err)) break;
+      ptx::tc_fence_after();
+      for (int kb = 0; kb < ti.kblocks; ++kb) {
+        if (!ptx::mbar_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
+        ptx::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a_addr = ptx::smem_u32(sA + stage * A_ST);
+          const uint32_t b_addr = ptx::smem_u32(sB + stage * B_ST);
+#pragma unroll
+          for (int k16 = 0; k16 < BK / 16; ++k16) {
+            const uint64_t bd = B_MN ? ptx::smem_desc_sw128(b_addr + k16 * 2048, MN_CHUNK, 1024)
+                                     : ptx::smem_desc_sw128(b_addr + k16 * 32, 16, 1024);
+            const uint32_t accumulate = (kb | k16) != 0 ? 1u : 0u;
+            ptx::umma_bf16(tmem_base, ptx::smem_desc_sw128(a_addr + k16 * 32, 16, 1024), bd, IDESC,
+                           accumulate);
+            if (tall)
+              ptx::umma_bf16(tmem_base + BN2,
+                             ptx::smem_desc_sw128(a_addr + BM * BK * 2 + k16 * 32, 16, 1024), bd,
+                             IDESC, accumulate);
+          }
+          ptx::umma_commit(&empty[stage]);   // frees the stage when these MMAs finish
+        }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      if (lane == 0) ptx::umma_commit(tfull);   // accumulator ready for the epilogue
+      __syncwarp();
+      acc_phase ^= 1u;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (8 warps)
+    const int e = warp - 2;
+    const int q = warp & 3;               // TMEM lane quadrant this warp may access
+    const int h = e >> 2;                 // accumulator half: rows 128*h .. 128*h + 127
+    uint8_t* slab = staging + e * SLAB;
+    uint32_t acc_phase = 0;
+    for (int tile = unit; tile < total; tile += units) {
+      const TileInfo ti = S::decode(p, s_off, s_pre, nullptr, tile);
+      const int row0 = ti.m0 + h * BM + q * 32;   // this warp's first row
+      const int rows_here = min(32, ti.m_end - row0);
+      if (!ptx::mbar_wait(tfull, acc_phase, abort_flag, p.err)) break;
+      acc_phase ^= 1u;
+      ptx::tc_fence_after();
+      // the warp's 32 rows x 256 columns as bf16 pairs: pk[16 c + i] holds columns 32 c + 2 i, +1
+      uint32_t pk[BN2 / 2];
+      if (rows_here > 0) {
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                               static_cast<uint32_t>(h * BN2);
+#pragma unroll
+        for (int c = 0; c < BN2 / 32; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld32(t_row + 32 * c, v);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(v[8 * j + i]);
+            const uint4 u = pack16(f, static_cast<const bf16*>(nullptr));
+            pk[16 * c + 4 * j + 0] = u.x;
+            pk[16 * c + 4 * j + 1] = u.y;
+            pk[16 * c + 4 * j + 2] = u.z;
+            pk[16 * c + 4 * j + 3] = u.w;
+          }
+        }
+      }
+      // the accumulator may be overwritten once every warp holds its rows
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(tempty);
+      if (rows_here == 32) {
+        // 64 columns per slab, out through TMA (the map clips at the tensor's columns)
+#pragma unroll
+        for (int s = 0; s < BN2 / 64; ++s) {
+          const int col = ti.n0 + 64 * s;
+          if (col >= p.N) break;
+          if (lane == 0) ptx::bulk_wait_read<0>();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            slab_put(slab, lane, j,
+                     make_uint4(pk[32 * s + 4 * j], pk[32 * s + 4 * j + 1], pk[32 * s + 4 * j + 2],
+                                pk[32 * s + 4 * j + 3]));
+          slab_store_2d(&tmO0, slab, lane, col, row0);
+        }
+      } else if (rows_here > 0 && lane < rows_here) {
+        // the group's last rows: masked stores (a whole slab would overwrite the next group's)
+        bf16* o = static_cast<bf16*>(p.out) + static_cast<int64_t>(row0 + lane) * p.ldo + ti.n0;
+#pragma unroll
+        for (int v = 0; v < BN2 / 8; ++v) {
+          if (ti.n0 + 8 * v < p.N)
+            st16(o + 8 * v, make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]));
+        }
+      }
+    }
+    if (lane == 0) ptx::bulk_wait_all();
+    __syncwarp();
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
 // ---------------------------------------------------------------- row-ragged products on CTA pairs
 // A row-ragged product with bf16 output (fc2; the data gradient with MN-major weights) on CTA
 // pairs (tcgen05 cta_group::2): tiles of 256 rows (each CTA's 128, counted per group as in the
@@ -2549,6 +2827,45 @@ int run_wgrad_pair(const GemmDesc& g, cudaStream_t st) {
                          SMEM, 2, st, ma, mb, mo, a);
 }
 
+// Row-ragged bf16 products (fc2, the data gradients) on tall tiles (tc_rows_tall_kernel), on by
+// default: interleaved on the 128-expert layer fc2 0.762-0.766 -> 0.735-0.740 ms, fc1 dgrad
+// 1.432-1.446 -> 1.371-1.385 ms, shared fc1 dgrad 0.218-0.219 -> 0.205-0.208 ms.  0: the one-CTA
+// 128 x 256 kernel.
+#ifndef MOE_TALL_ROWS
+#define MOE_TALL_ROWS 1
+#endif
+template <bool B_MN>
+int run_rows_tall(const GemmDesc& g, cudaStream_t st) {
+  using namespace tallk;
+  const char* name = g.name ? g.name : (B_MN ? "gemm_dgrad" : "gemm_fc2");
+  auto kern = tc_rows_tall_kernel<B_MN>;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  });
+  if (attr_err != cudaSuccess) {
+    set_error("cudaFuncSetAttribute(%s, %d bytes): %s", name, SMEM, cudaGetErrorString(attr_err));
+    return MOE_ERR_CUDA;
+  }
+  CUtensorMap ma, mb, mo;
+  MOE_TRY(map_operand(&ma, g.A, BM));
+  MOE_TRY(map_operand(&mb, g.B, B_MN ? BK : BN2));
+  MOE_TRY(map_bf16(&mo, g.out, g.M, g.N, g.ldo, 32));
+  KArgs a;
+  memset(&a, 0, sizeof(a));
+  a.G = g.G;
+  a.offsets = g.offsets;
+  a.M = g.M;
+  a.N = g.N;
+  a.K = g.K;
+  a.b_group_rows = g.b_group_rows;
+  a.out = g.out;
+  a.ldo = g.ldo;
+  a.err = device_error_word();
+  return launch(name, kern, dim3(num_sms()), dim3(THREADS), SMEM, st, ma, mb, mo, a);
+}
+
 // Row-ragged bf16 products (fc2, the data gradients) on CTA pairs (tc_rows_pair_kernel).
 #ifndef MOE_PAIR_ROWS
 #define MOE_PAIR_ROWS 0
@@ -2674,6 +2991,8 @@ int gemm_tc(const GemmDesc& g, cudaStream_t st) {
     if (g.epi == EPI_SWIGLU_BWD && g.B.mn_major)
       return n192 ? run<192, false, true, RAGGED_M, EPI_SWIGLU_BWD>(g, "gemm_fc2_dgrad_swiglu_bwd", st)
                   : run<256, false, true, RAGGED_M, EPI_SWIGLU_BWD>(g, "gemm_fc2_dgrad_swiglu_bwd", st);
+    if (MOE_TALL_ROWS && g.epi == EPI_STORE && !n192 && g.G <= MAXG)
+      return g.B.mn_major ? run_rows_tall<true>(g, st) : run_rows_tall<false>(g, st);
     if (MOE_PAIR_ROWS && g.epi == EPI_STORE && !n192)
       return g.B.mn_major ? run_rows_pair<true>(g, st) : run_rows_pair<false>(g, st);
     if (g.epi == EPI_STORE && !g.B.mn_major)
