@@ -1169,6 +1169,96 @@ def run_wgrad_routings(args, lc):
             "distributions": out}
 
 
+def wait_kind_name(kind):
+    """The product a GEMM pipeline wait-statistics kind (moe_gemm_wait_stats) stands for here."""
+    if kind >= 48:
+        return "tall row tiles, B " + ("MN-major (data gradients)" if kind & 1 else "K-major (fc2)")
+    epi = ["bf16 store", "fp32", "SwiGLU forward", "SwiGLU backward"][(kind >> 3) & 3]
+    sched = "ragged reduction (weight gradients)" if kind & 4 else "ragged rows"
+    return f"one-CTA 128x256, {sched}, {epi}" + (", 8-bit" if kind & 32 else "")
+
+
+def run_wait_stats(args, lc):
+    """Where the tensor-core GEMMs' pipelines wait: the routed experts' forward
+    (moe_grouped_swiglu_fwd) and backward (moe_grouped_swiglu_bwd) on the workload's shapes and its
+    own routing counts, `steps` calls of each after `warmup`, with the library built with
+    MOE_WAIT_STATS=1.  Per kernel kind: the fraction of the CTAs' cycles the producer waited for a
+    free stage, the MMA warp for a loaded stage and for a free accumulator, the first epilogue
+    warp for a finished accumulator, and the CTA cycles per k-block."""
+    import numpy as np
+    import torch
+
+    import moe_expert_layer_gemm_gb300 as moe
+    from moe_expert_layer_gemm_gb300 import build as _build
+
+    if not os.path.exists(moe._lib.LIB_PATH):
+        _build.build()
+    moe.lib()
+    if moe.gemm_wait_stats() is None:
+        return {"metric": "GEMM pipeline wait fractions", "unavailable":
+                "the library was built without the counters: rebuild with "
+                "MOE_NVCC_EXTRA=-DMOE_WAIT_STATS=1"}
+    dev = torch.device("cuda", 0)
+    E, d, f, N = lc.E, lc.d, lc.f, lc.T * lc.k
+    inp = moe_inputs.make_layer_inputs(lc, seed=args.seed, device=dev)
+    cfg_r = moe.cfg_from(lc)
+    i32 = torch.int32
+    counts = torch.empty(E, dtype=i32, device=dev)
+    offsets = torch.empty(E + 1, dtype=i32, device=dev)
+    moe.moe_route_topk(cfg_r, inp["x"], inp["W_r"], inp["b_r"], None,
+                       torch.empty(lc.T, E, device=dev),
+                       torch.empty(lc.T, lc.k, dtype=i32, device=dev),
+                       torch.empty(lc.T, lc.k, device=dev), counts, offsets,
+                       torch.empty(lc.T, lc.k, dtype=i32, device=dev),
+                       torch.empty(N, dtype=i32, device=dev), moe.workspace(cfg_r, moe.WS_ROUTE, dev))
+    del inp
+    torch.cuda.empty_cache()
+    g = torch.Generator(device=dev)
+    g.manual_seed(args.seed)
+    bf = torch.bfloat16
+    xp = torch.randn(N, d, device=dev, generator=g).to(bf)
+    W1 = (torch.randn(E, 2 * f, d, device=dev, generator=g) * 0.02).to(bf)
+    W2 = (torch.randn(E, d, f, device=dev, generator=g) * 0.02).to(bf)
+    h = torch.empty(N, f, device=dev, dtype=bf)
+    act = torch.empty(N, 2 * f, device=dev, dtype=bf)
+    yp = torch.empty(N, d, device=dev, dtype=bf)
+    dyp = torch.randn(N, d, device=dev, generator=g).to(bf)
+    dxp = torch.empty(N, d, device=dev, dtype=bf)
+    dW1 = torch.empty(E, 2 * f, d, device=dev)
+    dW2 = torch.empty(E, d, f, device=dev)
+    cfg = moe.make_cfg(N, d, E, 1, f)
+    wsf = moe.workspace(cfg, moe.WS_FFN_FWD, dev)
+    wsb = moe.workspace(cfg, moe.WS_FFN_BWD, dev)
+    calls = {"forward": lambda: moe.moe_grouped_swiglu_fwd(cfg, xp, offsets, W1, W2, h, act, yp, wsf),
+             "backward": lambda: moe.moe_grouped_swiglu_bwd(cfg, xp, offsets, W1, W2, act, h, dyp, dxp,
+                                                            dW1, dW2, wsb)}
+    out = {}
+    for name, fn in calls.items():
+        for _ in range(args.warmup):
+            fn()
+        moe.gemm_wait_stats()
+        for _ in range(args.steps):
+            fn()
+        st = moe.gemm_wait_stats()
+        moe.check_device_error()
+        rows = {}
+        for kind, v in sorted(st.items()):
+            cyc = max(1, v["cta_cycles"])
+            rows[str(kind)] = {
+                "kernel": wait_kind_name(kind), "ctas": v["ctas"], "kblocks": v["kblocks"],
+                "mma_stage_wait": round(v["mma_stage_wait"] / cyc, 3),
+                "mma_accumulator_wait": round(v["mma_accumulator_wait"] / cyc, 3),
+                "producer_stage_wait": round(v["producer_stage_wait"] / cyc, 3),
+                "epilogue_accumulator_wait": round(v["epilogue_accumulator_wait"] / cyc, 3),
+                "cta_cycles_per_kblock": round(cyc / max(1, v["kblocks"]), 1)}
+        out[name] = rows
+    return {"metric": "GEMM pipeline wait fractions (of each kind's CTA cycles)", "unit": "fraction",
+            "steps": args.steps, "warmup": args.warmup,
+            "data": "synthetic (seeded Gaussian operands; the workload's own routing counts)",
+            "config": {"workload": lc.name, "d_model": d, "experts": E, "ffn": f, "N": N},
+            "calls": out}
+
+
 def run_reference(args, lc):
     """The fp64 CPU oracle as the reference arm: each step is the oracle's forward + backward on
     a bounded, seeded sample of the same workload's tokens (all experts)."""
@@ -1234,6 +1324,9 @@ def main():
     ap.add_argument("--wgrad-routings", action="store_true",
                     help="time the routed experts' backward kernels under several per-expert row "
                          "distributions of the workload's shapes; prints its own JSON line")
+    ap.add_argument("--wait-stats", action="store_true",
+                    help="where the GEMM pipelines wait (a library built with MOE_WAIT_STATS=1); "
+                         "prints its own JSON line")
     args = ap.parse_args()
     if args.fp8 and args.mxfp8:
         ap.error("--fp8 and --mxfp8 are exclusive")
@@ -1245,6 +1338,8 @@ def main():
         out = run_route_only(args, lc)
     elif args.wgrad_routings:
         out = run_wgrad_routings(args, lc)
+    elif args.wait_stats:
+        out = run_wait_stats(args, lc)
     else:
         out = run_reference(args, lc) if args.impl == "reference" else run_gpu(args, lc)
     if out is not None:

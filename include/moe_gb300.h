@@ -618,6 +618,20 @@ int moe_trace_enable(int on);
 /* Fills up to `cap` entries; returns the number of kernel kinds seen (or < 0 on error). */
 int moe_trace_read(char* names, int name_stride, int* launches, double* total_ms, int cap);
 
+/* GEMM pipeline wait statistics (tracing; a build option: the library built with
+ * -DMOE_WAIT_STATS=1, e.g. MOE_NVCC_EXTRA=-DMOE_WAIT_STATS=1 for build.py; otherwise this
+ * returns MOE_ERR_UNSUPPORTED and reads nothing).  Every tensor-core GEMM CTA adds, for its kernel
+ * kind, SM clock cycles summed over CTAs: [0] its TMA producer waiting for a free ring stage, [1]
+ * its MMA warp waiting for a loaded stage, [2] its MMA warp waiting for a free accumulator, [3]
+ * its first epilogue warp waiting for a finished accumulator, [4] the CTA's own cycles; then [5]
+ * the k-blocks its MMA warp consumed and [6] 1 (the CTA).  Kind k's seven values are
+ * out[7k .. 7k+6].  One-CTA kernel: k = (A MN-major) + 2 (B MN-major) + 4 (reduction ragged per
+ * group, the weight gradients) + 8 * epilogue (0 bf16 store, 1 fp32, 2 SwiGLU forward, 3 SwiGLU
+ * backward) + 32 (8-bit operands); tall row tiles (fc2 and the data gradients in bf16): k = 48 +
+ * (B MN-major).  The CTA-pair kernels are not counted.  Synchronises the device, copies the 64
+ * kinds (448 values; cap >= 448), clears them and returns 64. */
+int moe_gemm_wait_stats(uint64_t* out, int cap);
+
 /* Self-test of the failure path of the pipelined kernels: launches one block that waits, through
  * the same bounded mbarrier wait as every GEMM pipeline (here with a 50 ms limit), on a barrier
  * that nothing arrives on.  The wait gives up, the kernel raises its abort flag, records

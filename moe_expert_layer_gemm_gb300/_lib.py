@@ -130,6 +130,7 @@ _SIGS = {
     "moe_last_error": (ctypes.c_char_p, []),
     "moe_check_device_error": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_int32)]),
     "moe_launch_count": (ctypes.c_uint64, []),
+    "moe_gemm_wait_stats": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint64), ctypes.c_int]),
     "moe_trace_enable": (ctypes.c_int, [ctypes.c_int]),
     "moe_trace_read": (ctypes.c_int, [ctypes.c_char_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                       ctypes.POINTER(ctypes.c_double), ctypes.c_int]),
@@ -561,6 +562,28 @@ def check_device_error(stream=None):
 
 def launch_count():
     return int(lib().moe_launch_count())
+
+
+WAIT_FIELDS = ("producer_stage_wait", "mma_stage_wait", "mma_accumulator_wait",
+               "epilogue_accumulator_wait", "cta_cycles", "kblocks", "ctas")
+
+
+def gemm_wait_stats():
+    """{kernel kind: {field: value}} of the GEMM pipeline wait counters since the last read
+    (synchronises the device and clears them), or None when the library was built without
+    MOE_WAIT_STATS=1."""
+    buf = (ctypes.c_uint64 * (64 * 7))()
+    n = lib().moe_gemm_wait_stats(buf, 64 * 7)
+    if n == -2:   # MOE_ERR_UNSUPPORTED: built without the counters
+        return None
+    if n < 0:
+        _check(n, "moe_gemm_wait_stats")
+    out = {}
+    for kind in range(n):
+        v = [int(buf[7 * kind + i]) for i in range(7)]
+        if v[6]:
+            out[kind] = dict(zip(WAIT_FIELDS, v))
+    return out
 
 
 def trace_enable(on=True):

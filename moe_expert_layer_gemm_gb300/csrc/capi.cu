@@ -730,7 +730,7 @@ using namespace moe;
 // ====================================================================== C ABI
 extern "C" {
 
-int moe_version(void) { return 201; }
+int moe_version(void) { return 202; }
 
 const char* moe_last_error(void) { return g_errbuf; }
 

@@ -34,7 +34,52 @@
 
 namespace moe {
 
+// Pipeline wait statistics (build option MOE_WAIT_STATS=1, read by moe_gemm_wait_stats): per
+// kernel kind, SM clock cycles summed over CTAs -- 0 producer waiting for a free ring stage,
+// 1 MMA warp waiting for a loaded stage, 2 MMA warp waiting for a free accumulator, 3 the first
+// epilogue warp waiting for a finished accumulator, 4 the CTAs' own cycles -- and 5 the k-blocks
+// the MMA warps consumed, 6 the CTAs.
+#ifndef MOE_WAIT_STATS
+#define MOE_WAIT_STATS 0
+#endif
+constexpr int WAIT_KINDS = 64, WAIT_FIELDS = 7;
+__device__ unsigned long long g_wait_stats[WAIT_KINDS * WAIT_FIELDS];
+
 namespace {
+
+struct WaitStats {
+  unsigned long long t_start = 0, prod = 0, full = 0, acc = 0, epi = 0, kblocks = 0;
+  __device__ __forceinline__ void start() {
+    if (MOE_WAIT_STATS) t_start = clock64();
+  }
+  __device__ __forceinline__ unsigned long long now() const {
+    return MOE_WAIT_STATS ? static_cast<unsigned long long>(clock64()) : 0ull;
+  }
+  __device__ __forceinline__ void since(unsigned long long& field, unsigned long long t0) const {
+    if (MOE_WAIT_STATS) field += static_cast<unsigned long long>(clock64()) - t0;
+  }
+  // warp 0 lane 0 the producer, warp 1 lane 0 the MMA issuer, warp 2 lane 0 the first epilogue
+  __device__ __forceinline__ void flush(int kind, int warp, int lane) const {
+    if (!MOE_WAIT_STATS) return;
+    unsigned long long* g = g_wait_stats + kind * WAIT_FIELDS;
+    if (lane != 0) return;
+    if (warp == 0) atomicAdd(g + 0, prod);
+    if (warp == 1) {
+      atomicAdd(g + 1, full);
+      atomicAdd(g + 2, acc);
+      atomicAdd(g + 5, kblocks);
+    }
+    if (warp == 2) atomicAdd(g + 3, epi);
+  }
+  // after the CTA's last barrier, by one thread: its cycles and the CTA count
+  __device__ __forceinline__ void flush_cta(int kind) const {
+    if (!MOE_WAIT_STATS) return;
+    unsigned long long* g = g_wait_stats + kind * WAIT_FIELDS;
+    atomicAdd(g + 4, static_cast<unsigned long long>(clock64()) - t_start);
+    atomicAdd(g + 6, 1ull);
+  }
+};
+
 
 constexpr int BM = 128;
 constexpr int BK = 64;
@@ -464,6 +509,9 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
   float* s_sbias = reinterpret_cast<float*>(xtra + RouterOf<SCHED, EPI, F8>::SBIAS_OFF);
   unsigned* s_stg = reinterpret_cast<unsigned*>(xtra + RouterOf<SCHED, EPI, F8>::STG_OFF);
 
+  WaitStats wst;
+  wst.start();
+  constexpr int WAIT_KIND = (A_MN ? 1 : 0) | (B_MN ? 2 : 0) | (SCHED << 2) | (EPI << 3) | ((F8 || MX) ? 32 : 0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Tile walker: one per CTA (static walk), or tiles claimed at run time (DYN).
   const int unit = static_cast<int>(blockIdx.x);
@@ -765,7 +813,10 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
         }
         const TileInfo ti = S::decode(p, s_off, s_pre, s_ord, tile);
         for (int kb = 0; kb < ti.kblocks; ++kb) {
-          if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+          const unsigned long long w0 = wst.now();
+          const bool freed = ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err);
+          wst.since(wst.prod, w0);
+          if (!freed) { ok = false; break; }
           ptx::mbar_arrive_expect_tx(&full[stage], STAGE_TX);
           armed[stage] = static_cast<int>(phase);
           issue(ti, kb, stage);
@@ -809,11 +860,18 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
       }
       const TileInfo ti = S::decode(p, s_off, s_pre, s_ord, tile);
       if (ti.kblocks == 0) continue;
-      if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+      const unsigned long long wa = wst.now();
+      const bool drained = ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err);
+      wst.since(wst.acc, wa);
+      if (!drained) { ok = false; break; }
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::ACC_STRIDE);
       for (int kb = 0; kb < ti.kblocks; ++kb) {
-        if (!ptx::mbar_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
+        const unsigned long long wf = wst.now();
+        const bool landed = ptx::mbar_wait(&full[stage], phase, abort_flag, p.err);
+        wst.since(wst.full, wf);
+        ++wst.kblocks;
+        if (!landed) { ok = false; break; }
         uint8_t* a_src = sA + stage * A_STAGE;
         uint8_t* b_src = sB + stage * C::B_STAGE;
         if (SCHED == RAGGED_K && kb == ti.kblocks - 1) {
@@ -974,7 +1032,10 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
         }
         continue;
       }
-      if (!ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err)) break;
+      const unsigned long long we = wst.now();
+      const bool ready = ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err);
+      wst.since(wst.epi, we);
+      if (!ready) break;
       ptx::tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * C::ACC_STRIDE);
@@ -1564,8 +1625,10 @@ __global__ void __launch_bounds__(64 + 32 * EpiWidth<BN, SCHED, EPI, F8>::warps,
     __syncwarp();
   }
 
+  wst.flush(WAIT_KIND, warp, lane);
   ptx::tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) wst.flush_cta(WAIT_KIND);
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
@@ -2016,6 +2079,9 @@ __global__ void __launch_bounds__(tallk::THREADS, 1)
   int* s_pre = s_off + (MAXG + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  WaitStats wst;
+  wst.start();
+  constexpr int WAIT_KIND = 48 + (B_MN ? 1 : 0);
   const int unit = static_cast<int>(blockIdx.x), units = static_cast<int>(gridDim.x);
 
   if ((ptx::smem_u32(smem) & 1023u) != 0) {
@@ -2092,7 +2158,10 @@ __global__ void __launch_bounds__(tallk::THREADS, 1)
         const int brow = static_cast<int>(ti.g * p.b_group_rows);
         for (int kb = 0; kb < ti.kblocks; ++kb) {
           const int kk = kb * BK;
-          if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+          const unsigned long long w0 = wst.now();
+          const bool freed = ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err);
+          wst.since(wst.prod, w0);
+          if (!freed) { ok = false; break; }
           ptx::mbar_arrive_expect_tx(&full[stage], tx);
           armed[stage] = static_cast<int>(phase);
           uint8_t* a_dst = sA + stage * A_ST;
@@ -2129,10 +2198,17 @@ __global__ void __launch_bounds__(tallk::THREADS, 1)
     for (int tile = unit; tile < total && ok; tile += units) {
       const TileInfo ti = S::decode(p, s_off, s_pre, nullptr, tile);
       const bool tall = ti.m_end - ti.m0 > BM;
-      if (!ptx::mbar_wait(tempty, acc_phase ^ 1u, abort_flag, p.err)) break;
+      const unsigned long long wa = wst.now();
+      const bool drained = ptx::mbar_wait(tempty, acc_phase ^ 1u, abort_flag, p.err);
+      wst.since(wst.acc, wa);
+      if (!drained) break;
       ptx::tc_fence_after();
       for (int kb = 0; kb < ti.kblocks; ++kb) {
-        if (!ptx::mbar_wait(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
+        const unsigned long long wf = wst.now();
+        const bool landed = ptx::mbar_wait(&full[stage], phase, abort_flag, p.err);
+        wst.since(wst.full, wf);
+        ++wst.kblocks;
+        if (!landed) { ok = false; break; }
         ptx::tc_fence_after();
         if (lane == 0) {
           const uint32_t a_addr = ptx::smem_u32(sA + stage * A_ST);
@@ -2170,7 +2246,10 @@ __global__ void __launch_bounds__(tallk::THREADS, 1)
       const TileInfo ti = S::decode(p, s_off, s_pre, nullptr, tile);
       const int row0 = ti.m0 + h * BM + q * 32;   // this warp's first row
       const int rows_here = min(32, ti.m_end - row0);
-      if (!ptx::mbar_wait(tfull, acc_phase, abort_flag, p.err)) break;
+      const unsigned long long we = wst.now();
+      const bool ready = ptx::mbar_wait(tfull, acc_phase, abort_flag, p.err);
+      wst.since(wst.epi, we);
+      if (!ready) break;
       acc_phase ^= 1u;
       ptx::tc_fence_after();
       // the warp's 32 rows x 256 columns as bf16 pairs: pk[16 c + i] holds columns 32 c + 2 i, +1
@@ -2229,8 +2308,10 @@ __global__ void __launch_bounds__(tallk::THREADS, 1)
     __syncwarp();
   }
 
+  wst.flush(WAIT_KIND, warp, lane);
   ptx::tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) wst.flush_cta(WAIT_KIND);
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, TMEM_COLS);
@@ -2834,6 +2915,19 @@ int run_wgrad_pair(const GemmDesc& g, cudaStream_t st) {
 #ifndef MOE_TALL_ROWS
 #define MOE_TALL_ROWS 1
 #endif
+// Whole waves of tiles each form takes over the output's rows (the capacity, for grouped calls:
+// their per-group tails add tiles to both forms), a tall tile costing 1.92 one-CTA tiles (the
+// measured 4% gain per tile).  A one-group product of 4096 rows x 2688 columns is 176 tall tiles,
+// two waves on 152 SMs, against three waves of 352 one-CTA tiles: the one-CTA form is faster there
+// (shared fc2 on the 32-expert layer 35 us against 43 us tall).
+bool tall_pays(const GemmDesc& g) {
+  const int64_t sms = num_sms();
+  const int64_t nt = (g.N + 255) / 256;
+  const int64_t waves_tall = ((g.M + 255) / 256 * nt + sms - 1) / sms;
+  const int64_t waves_one = ((g.M + 127) / 128 * nt + sms - 1) / sms;
+  return waves_tall * 192 <= waves_one * 100;
+}
+
 template <bool B_MN>
 int run_rows_tall(const GemmDesc& g, cudaStream_t st) {
   using namespace tallk;
@@ -2991,7 +3085,7 @@ int gemm_tc(const GemmDesc& g, cudaStream_t st) {
     if (g.epi == EPI_SWIGLU_BWD && g.B.mn_major)
       return n192 ? run<192, false, true, RAGGED_M, EPI_SWIGLU_BWD>(g, "gemm_fc2_dgrad_swiglu_bwd", st)
                   : run<256, false, true, RAGGED_M, EPI_SWIGLU_BWD>(g, "gemm_fc2_dgrad_swiglu_bwd", st);
-    if (MOE_TALL_ROWS && g.epi == EPI_STORE && !n192 && g.G <= MAXG)
+    if (MOE_TALL_ROWS && g.epi == EPI_STORE && !n192 && g.G <= MAXG && tall_pays(g))
       return g.B.mn_major ? run_rows_tall<true>(g, st) : run_rows_tall<false>(g, st);
     if (MOE_PAIR_ROWS && g.epi == EPI_STORE && !n192)
       return g.B.mn_major ? run_rows_pair<true>(g, st) : run_rows_pair<false>(g, st);
@@ -3019,3 +3113,23 @@ int gemm_tc(const GemmDesc& g, cudaStream_t st) {
 }
 
 }  // namespace moe
+
+extern "C" int moe_gemm_wait_stats(uint64_t* out, int cap) {
+  using namespace moe;
+  if (!MOE_WAIT_STATS) {
+    set_error("moe_gemm_wait_stats: the library was built without MOE_WAIT_STATS=1");
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (!out || cap < WAIT_KINDS * WAIT_FIELDS) {
+    set_error("moe_gemm_wait_stats: out must hold %d values", WAIT_KINDS * WAIT_FIELDS);
+    return MOE_ERR_INVALID_ARG;
+  }
+  static unsigned long long zero[WAIT_KINDS * WAIT_FIELDS];
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpyFromSymbol(out, g_wait_stats, sizeof(zero)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_wait_stats, zero, sizeof(zero)) != cudaSuccess) {
+    set_error("moe_gemm_wait_stats: %s", cudaGetErrorString(cudaGetLastError()));
+    return MOE_ERR_CUDA;
+  }
+  return WAIT_KINDS;
+}

@@ -169,6 +169,16 @@ def test_mxfp8_entry_points_check_arguments():
     assert b"h" in L.moe_last_error()
 
 
+def test_wait_stats_need_their_build_option():
+    """The default library has no pipeline wait counters: the entry point says so on the host
+    (no device call) and the binding reads that as None."""
+    import ctypes
+    buf = (ctypes.c_uint64 * 448)()
+    assert moe.lib().moe_gemm_wait_stats(buf, 448) == -2
+    assert b"MOE_WAIT_STATS" in moe.lib().moe_last_error()
+    assert moe.gemm_wait_stats() is None
+
+
 def test_binding_argument_counts_match_the_header():
     """Every ctypes signature of the binding takes as many arguments as the header declares."""
     import re
