@@ -434,15 +434,6 @@ __device__ __forceinline__ void slab_store_2d(const CUtensorMap* m, const uint8_
     ptx::bulk_commit();
   }
 }
-__device__ __forceinline__ void slab_store_3d(const CUtensorMap* m, const uint8_t* slab, int lane,
-                                              int c0, int c1, int c2) {
-  ptx::fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) {
-    ptx::tma_store_3d(m, slab, c0, c1, c2);
-    ptx::bulk_commit();
-  }
-}
 
 template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, bool GATHER = false, bool F8 = false,
           bool MX = false>
