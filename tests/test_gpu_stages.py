@@ -73,6 +73,54 @@ def test_grouped_swiglu_fwd_bwd_stage():
     assert_close("dx_perm", np64(dxp), ref_dx, 2e-2)
 
 
+def test_tall_tiles_on_ragged_groups():
+    """fc2 and fc1's data gradient on 256-row tiles: with 8192 rows and d = 2048 the library takes
+    them (two waves of 256 x 256 tiles against four of 128 x 256 on a GPU of about 150 SMs).  The
+    groups' sizes cover the tall tile's cases: empty groups, a single row, tails of at most 128
+    rows (only the first half's MMAs), tails of 129 and 200 rows (a partial second half), whole
+    tiles of 256 and 512 rows, a 255-row group and one large group.  Every output row is written
+    (the buffers start as NaN) and matches the oracle's per-expert products."""
+    E, d, f = 16, 2048, 128
+    sizes = [0, 1, 100, 128, 129, 200, 256, 300, 385, 512, 640, 0, 1000, 1, 255]
+    sizes.append(8192 - sum(sizes))
+    N = sum(sizes)
+    off_np = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    cfg = moe.make_cfg(N, d, E, 1, f)
+    g = torch.Generator().manual_seed(21)
+    xp = torch.randn(N, d, generator=g).bfloat16()
+    W1 = (torch.randn(E, 2 * f, d, generator=g) * 0.03).bfloat16()
+    W2 = (torch.randn(E, d, f, generator=g) * 0.05).bfloat16()
+    dyp = torch.randn(N, d, generator=g).bfloat16()
+    c = {n: t.cuda() for n, t in dict(xp=xp, W1=W1, W2=W2, dyp=dyp,
+                                       off=torch.from_numpy(off_np)).items()}
+    nan = float("nan")
+    h = torch.full((N, f), nan, dtype=torch.bfloat16, device="cuda")
+    act = torch.full((N, 2 * f), nan, dtype=torch.bfloat16, device="cuda")
+    yp = torch.full((N, d), nan, dtype=torch.bfloat16, device="cuda")
+    moe.moe_grouped_swiglu_fwd(cfg, c["xp"], c["off"], c["W1"], c["W2"], h, act, yp)
+    dxp = torch.full((N, d), nan, dtype=torch.bfloat16, device="cuda")
+    dW1 = torch.empty(E, 2 * f, d, device="cuda")
+    dW2 = torch.empty(E, d, f, device="cuda")
+    ws = moe.workspace(cfg, moe.WS_FFN_BWD)
+    moe.moe_grouped_swiglu_bwd(cfg, c["xp"], c["off"], c["W1"], c["W2"], act, h, c["dyp"], dxp, dW1,
+                               dW2, ws)
+    torch.cuda.synchronize()
+    moe.check_device_error()
+    assert not torch.isnan(yp).any() and not torch.isnan(dxp).any()
+    X, dY = np64(xp), np64(dyp)
+    ref_y = np.zeros((N, d))
+    ref_dx = np.zeros((N, d))
+    for e in range(E):
+        sl = slice(off_np[e], off_np[e + 1])
+        if sizes[e] == 0:
+            continue
+        y_e, a, u, hh = O.swiglu_ffn(np64(W1[e]), np64(W2[e]), X[sl])
+        ref_y[sl] = y_e
+        ref_dx[sl] = O.swiglu_ffn_backward(np64(W1[e]), np64(W2[e]), X[sl], a, u, hh, dY[sl])[0]
+    assert_close("y_perm", np64(yp), ref_y, 2e-2)
+    assert_close("dx_perm", np64(dxp), ref_dx, 2e-2)
+
+
 @pytest.mark.parametrize("shared", [0, 1, 2])
 def test_combine_and_backward(shared):
     T, d, E, k = 500, 136, 12, 3
